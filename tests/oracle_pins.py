@@ -1,0 +1,308 @@
+"""Pins of the CPU oracle against values fixed outside it.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees with
+something it cannot have produced itself: a library cast (torch's bf16, fp16
+and e4m3 types), a published format table (OCP MX / OFP8, in
+``tests/golden``), a hand-worked case, exact integer or rational arithmetic,
+or an invariant of the definition.  ``test_oracle_pins.py`` runs them;
+``test_oracle_mutations.py`` plants plausible mistakes in the oracle and
+checks that some pin catches each one.
+"""
+from __future__ import annotations
+
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+from oracle import formats as F
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _load_table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append(line.split())
+    return rows
+
+
+def _same(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    both_nan = np.isnan(a) & np.isnan(b)
+    eq = (a == b) & (np.signbit(a) == np.signbit(b))
+    return bool(np.all(both_nan | eq))
+
+
+# ---------------------------------------------------------------------------
+# element formats
+# ---------------------------------------------------------------------------
+def pin_bf16_exhaustive():
+    u = np.arange(65536, dtype=np.uint16)
+    lib = torch.from_numpy(u.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert _same(F.bf16_to_f64(u), lib), "bf16 decode differs from torch.bfloat16"
+
+
+def pin_fp16_exhaustive():
+    u = np.arange(65536, dtype=np.uint16)
+    assert _same(F.fp16_to_f64(u), u.view(np.float16).astype(np.float64)), "fp16 decode differs from numpy"
+
+
+def pin_e4m3_exhaustive():
+    b = np.arange(256, dtype=np.uint8)
+    lib = torch.from_numpy(b).view(torch.float8_e4m3fn).double().numpy()
+    assert _same(F.e4m3_to_f64(b), lib), "e4m3 decode differs from torch.float8_e4m3fn"
+
+
+def pin_e4m3_spec_table():
+    for hexbyte, val in _load_table("e4m3_ocp_fp8.txt"):
+        got = F.e4m3_to_f64(np.array([int(hexbyte, 16)]))[0]
+        assert _same(got, float(val)), f"e4m3 0x{hexbyte}: {got} != {val}"
+
+
+def pin_e2m1_spec_table():
+    for code, val in _load_table("e2m1_ocp_mx_v1.txt"):
+        got = F.e2m1_to_f64(np.array([int(code)]))[0]
+        assert _same(got, float(val)), f"e2m1 code {code}: {got} != {val}"
+    # every e2m1 value lies on the e4m3 grid (torch cast round-trips exactly)
+    vals = F.e2m1_to_f64(np.arange(16))
+    back = torch.tensor(vals, dtype=torch.float32).to(torch.float8_e4m3fn).double().numpy()
+    assert _same(back, vals)
+
+
+def pin_ue8m0_spec_table():
+    for e, lg in _load_table("ue8m0_ocp_mx_v1.txt"):
+        got = F.ue8m0_to_f64(np.array([int(e)]))[0]
+        want = float("nan") if lg == "nan" else 2.0 ** int(lg)
+        assert _same(got, want), f"ue8m0 {e}: {got} != {want}"
+
+
+# ---------------------------------------------------------------------------
+# integer packing
+# ---------------------------------------------------------------------------
+def pin_int4_nibbles():
+    # bytes 0x21, 0xF8 hold codes 1, 2, 8, 15 (low nibble first)
+    u = F.unpack_nibbles(np.array([[0x21, 0xF8]], np.uint8), 4)
+    assert u.tolist() == [[1, 2, 8, 15]]
+    assert F.twos_complement(u, 4).tolist() == [[1, 2, -8, -1]]
+    # odd count: the last high nibble is padding
+    assert F.unpack_nibbles(np.array([[0x43, 0x05]], np.uint8), 3).tolist() == [[3, 4, 5]]
+
+
+def pin_int6_stream_exhaustive():
+    # every 6-bit code at each of the four phases of a 3-byte group, built as a
+    # Python big integer (code k << 6k) and serialised little-endian
+    for phase in range(4):
+        for code in range(64):
+            codes = [(7 * i + 3) % 64 for i in range(8)]
+            codes[phase] = code
+            codes[4 + phase] = 63 - code
+            big = sum(c << (6 * i) for i, c in enumerate(codes))
+            packed = np.frombuffer(big.to_bytes(6, "little"), dtype=np.uint8)[None, :]
+            got = F.unpack_int6(packed, 8)[0].tolist()
+            assert got == codes, (phase, code, got, codes)
+    assert F.twos_complement(np.array([31, 32, 63, 0]), 6).tolist() == [31, -32, -1, 0]
+
+
+# ---------------------------------------------------------------------------
+# hand-worked GEMM cases
+# ---------------------------------------------------------------------------
+def _hand_cases():
+    with open(os.path.join(GOLDEN, "hand_gemm_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+def _case_inputs(c):
+    m, n, k = c["m"], c["n"], c["k"]
+    if c["atype"] == "fp8":
+        xd = np.array(c["x_bytes"], np.uint8)
+        xs = np.array(c["x_scales"], np.float32)
+    else:
+        xb = np.zeros((m, k), np.uint16)
+        xb[:, :len(c["x_bits"][0])] = np.array(c["x_bits"], np.uint16)
+        xd, xs = xb, None
+    codes = np.array(c["codes"], np.uint8)[None]
+    if c["wtype"] == "fp8":
+        scales = np.array(c["scales"], np.float32)[None]
+    elif c["wtype"] == "mxfp4":
+        scales = np.array(c["scales"], np.uint8)[None]
+    else:
+        scales = np.array(c["scales_bits"], np.uint16)[None]
+    zeros = np.array(c["zeros"], np.uint8)[None] if "zeros" in c else None
+    return xd, xs, codes, scales, zeros
+
+
+def pin_hand_gemm_cases():
+    for c in _hand_cases():
+        xd, xs, codes, scales, zeros = _case_inputs(c)
+        w = oracle.dequantize(c["wtype"], c["n"], c["k"], codes, scales, zeros, c["group_k"],
+                              c["signed"], c["stype"], 1)
+        a = oracle.decode_activations(c["atype"], xd, xs)
+        nz = len(c["x_values"][0])
+        assert np.array_equal(a[:, :nz], np.array(c["x_values"], np.float64)), c["name"]
+        y = oracle.gemm_dense(a, w)
+        assert np.array_equal(y, np.array(c["y"], np.float64)), (c["name"], y.tolist(), c["y"])
+
+
+def pin_hand_moe_case():
+    with open(os.path.join(GOLDEN, "hand_moe_case.json")) as f:
+        c = json.load(f)
+    ids = np.array(c["topk_ids"], np.int32)
+    counts, offsets, perm = oracle.moe_route(ids, 3)
+    assert counts.tolist() == c["counts"] and offsets.tolist() == c["offsets"] and perm.tolist() == c["perm"]
+    # expert weights as int4 symmetric codes, scale 1, one group per row
+    wv = np.array(c["w_values"], np.int64)
+    codes = synth.pack_nibbles(wv & 0xF)
+    one = np.full((3, 2, 1), 0x3F80, np.uint16)
+    w = oracle.dequantize("int4", 2, 2, codes, one, None, 0, True, "bf16", 3)
+    assert np.array_equal(w, wv.astype(np.float64))
+    y = oracle.moe_gemm(np.array(c["x_values"], np.float64), ids, np.array(c["topk_w"], np.float32), w)
+    assert np.array_equal(y, np.array(c["y"], np.float64)), y.tolist()
+
+
+# ---------------------------------------------------------------------------
+# invariants and exact arithmetic
+# ---------------------------------------------------------------------------
+def pin_integer_invariant():
+    """All-ones scales with zero points at the code midpoint give the exact integer matmul."""
+    rng = np.random.default_rng(11)
+    for wtype, bits, mid in (("int4", 4, 8), ("int6", 6, 32)):
+        m, n, k, g = 3, 5, 256, 128
+        u = rng.integers(0, 2 ** bits, size=(1, n, k))
+        xi = rng.integers(-4, 5, size=(m, k))
+        pack = synth.pack_nibbles if bits == 4 else synth.pack_int6
+        zeros = pack(np.full((1, n, 4 if bits == 6 else k // g), mid))
+        ones = np.full((1, n, k // g), 0x3F80, np.uint16)
+        w = oracle.dequantize(wtype, n, k, pack(u), ones, zeros, g, False, "bf16", 1)
+        y = oracle.gemm_dense(F.bf16_to_f64(synth.to_bf16_bits(xi.astype(np.float64))), w)
+        exact = [[sum(int(xi[i, kk]) * (int(u[0, j, kk]) - mid) for kk in range(k)) for j in range(n)]
+                 for i in range(m)]
+        assert np.array_equal(y, np.array(exact, np.float64)), wtype
+
+
+def _scalar_code(wtype, row_bytes, kk):
+    """Independent per-element unpacking (bit arithmetic on one Python int)."""
+    if wtype in ("int4", "mxfp4"):
+        return (int(row_bytes[kk // 2]) >> (4 * (kk % 2))) & 0xF
+    stream = int.from_bytes(bytes(int(b) for b in row_bytes), "little")
+    return (stream >> (6 * kk)) & 0x3F
+
+
+def _frac_bf16(u):
+    t = torch.from_numpy(np.array([int(u)], np.uint16).view(np.int16)).view(torch.bfloat16)
+    return Fraction(float(t.double().item()))
+
+
+def pin_rational_bruteforce():
+    """Tiny random problems: oracle vs exact rational arithmetic in Python loops."""
+    e2m1_tab = {int(c): Fraction(v) for c, v in _load_table("e2m1_ocp_mx_v1.txt")}
+    for seed, wtype, zeros, group in ((1, "int4", False, 32), (2, "int4", True, 32), (3, "int6", True, 64),
+                                      (4, "int6", False, 0), (5, "mxfp4", False, 32)):
+        m, n, k = 2, 3, 64
+        qw = synth.random_codes_weight(seed, wtype, n, k, group_k=group, has_zeros=zeros)
+        x = synth.make_activations(np.random.default_rng(seed), m, k, "bf16")
+        y = oracle.gemm_dense(oracle.decode_activations("bf16", x.data),
+                              oracle.dequantize(qw.wtype, n, k, qw.codes, qw.scales, qw.zeros, qw.group_k,
+                                                qw.signed, qw.stype, 1))
+        bits = 6 if wtype == "int6" else 4
+        for i in range(m):
+            for j in range(n):
+                acc = Fraction(0)
+                for kk in range(k):
+                    c = _scalar_code(wtype, qw.codes[0, j], kk)
+                    if wtype == "mxfp4":
+                        wv = e2m1_tab[c] * Fraction(2) ** (int(qw.scales[0, j, kk // 32]) - 127)
+                    else:
+                        gi = 0 if group == 0 else kk // group
+                        s = _frac_bf16(qw.scales[0, j, gi])
+                        if zeros:
+                            z = _scalar_code(wtype, qw.zeros[0, j], gi)
+                            wv = (c - z) * s
+                        else:
+                            q = c - (1 << bits) if c >= (1 << (bits - 1)) else c
+                            wv = q * s
+                    acc += _frac_bf16(x.data[i, kk]) * wv
+                assert abs(float(acc) - y[i, j]) <= 1e-12 * (abs(float(acc)) + 1e-30), (wtype, i, j)
+
+
+def pin_fp8_block_definition():
+    """Block-scaled sum  sum_kb s_x s_w (e4m3 . e4m3)  with exact rationals, K spanning 3 blocks."""
+    qw = synth.random_codes_weight(7, "fp8", 130, 300)
+    acts = synth.make_activations(np.random.default_rng(7), 2, 300, "fp8")
+    y = oracle.gemm.reference(qw, acts)
+    e4 = lambda b: Fraction(float(torch.tensor([int(b)], dtype=torch.uint8)
+                                  .view(torch.float8_e4m3fn).double().item()))
+    for i in range(2):
+        for j in (0, 129):
+            tot = Fraction(0)
+            for kb in range(3):
+                part = sum(e4(acts.data[i, kk]) * e4(qw.codes[0, j, kk])
+                           for kk in range(kb * 128, min(300, kb * 128 + 128)))
+                tot += Fraction(float(acts.scales[i, kb])) * Fraction(float(qw.scales[0, j // 128, kb])) * part
+            assert abs(float(tot) - y[i, j]) <= 1e-12 * abs(float(tot)) + 1e-300, (i, j)
+
+
+def pin_quant_roundtrip():
+    """Quantise(dequantise(q)) == q for hand-picked codes whose group range fixes the scale."""
+    # int4 symmetric: each group's largest magnitude is 7, so absmax/7 recovers s
+    q = np.array([[[7, -3, 0, 1, -7, 2, 5, -1]]], np.int64)
+    s_bits = synth.to_bf16_bits(np.array([[[0.03125]]]))
+    w = oracle.dequantize("int4", 1, 8, synth.pack_nibbles(q & 0xF), s_bits, None, 0, True, "bf16", 1)
+    again = synth.quantize_int_groupwise(w, 4, 0, True, "bf16")
+    assert np.array_equal(again.codes, synth.pack_nibbles(q & 0xF)) and np.array_equal(again.scales, s_bits)
+    # int4 asymmetric: codes span 0..15, so (max-min)/15 recovers s and -min/s recovers z
+    u = np.array([[[0, 15, 3, 9, 4, 4, 12, 1]]], np.int64)
+    z = np.array([[[6]]], np.int64)
+    s_bits = synth.to_bf16_bits(np.array([[[0.0078125]]]))
+    w = oracle.dequantize("int4", 1, 8, synth.pack_nibbles(u), s_bits, synth.pack_nibbles(z), 0, False, "bf16", 1)
+    again = synth.quantize_int_groupwise(w, 4, 0, False, "bf16")
+    assert np.array_equal(again.codes, synth.pack_nibbles(u)) and np.array_equal(again.zeros, synth.pack_nibbles(z))
+    # mxfp4: a block whose largest magnitude is 6 recovers its exponent
+    codes = np.array([[list(range(16)) * 2]], np.int64)
+    e = np.array([[[121]]], np.uint8)
+    w = oracle.dequantize("mxfp4", 1, 32, synth.pack_nibbles(codes), e, None, 32, True, "ue8m0", 1)
+    again = synth.quantize_mxfp4(w)
+    assert np.array_equal(again.scales, e)
+    assert np.array_equal(oracle.dequantize("mxfp4", 1, 32, again.codes, again.scales, None, 32, True, "ue8m0", 1), w)
+
+
+def pin_moe_route_properties():
+    rng = np.random.default_rng(5)
+    for t, e in ((1, 4), (37, 16), (300, 128)):
+        ids = rng.integers(0, e, size=(t, 8)).astype(np.int32)
+        ids[: t // 3] = 0                              # a hot expert
+        counts, offsets, perm = oracle.moe_route(ids, e)
+        flat = ids.reshape(-1)
+        assert np.array_equal(counts, np.bincount(flat, minlength=e))
+        assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=e))]))
+        assert np.array_equal(perm, np.argsort(flat, kind="stable"))
+
+
+def pin_moe_reductions():
+    """topk = 1 with weight 1 reduces to a dense GEMM per expert; Y is linear in topk_w."""
+    rng = np.random.default_rng(9)
+    qw = synth.random_codes_weight(9, "mxfp4", 16, 64, num_experts=4)
+    wd = oracle.dequantize("mxfp4", 16, 64, qw.codes, qw.scales, None, 32, True, "ue8m0", 4)
+    a = rng.standard_normal((5, 64))
+    ids = np.array([[0], [3], [3], [1], [0]], np.int32)
+    y = oracle.moe_gemm(a, ids, np.ones((5, 1), np.float32), wd)
+    for t in range(5):
+        assert np.allclose(y[t], a[t] @ wd[ids[t, 0]].T, rtol=0, atol=1e-12)
+    ids2 = rng.integers(0, 4, size=(5, 3)).astype(np.int32)
+    w1 = (rng.integers(0, 64, size=(5, 3)) / 64.0).astype(np.float32)   # sums stay exact in fp32
+    w2 = (rng.integers(0, 64, size=(5, 3)) / 64.0).astype(np.float32)
+    ya = oracle.moe_gemm(a, ids2, w1, wd) + oracle.moe_gemm(a, ids2, w2, wd)
+    yb = oracle.moe_gemm(a, ids2, w1.astype(np.float64) + w2.astype(np.float64), wd)
+    assert np.allclose(ya, yb, rtol=1e-12, atol=1e-12)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
