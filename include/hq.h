@@ -1,0 +1,268 @@
+/*
+ * hq.h — C ABI of the GB300 (sm_103a) quantized GEMM library.
+ *
+ * The library computes the quantized GEMM of the Humming pages,
+ *
+ *     Y[M, N] = a(X)[M, K] . dequant(Wq, scales, zeros)[N, K]^T,
+ *
+ * for low-bit weights against 16-bit or FP8 activations, in a dense form and
+ * in an MoE grouped form over routed tokens.  Sources for each operation are
+ * cited at its declaration as "<page title>, <section>":
+ *   [README]   "Humming" (project README): Key Features, Support Matrix,
+ *              Usage Example.
+ *   [LAUNCH]   "Humming: Fast, Flexible Kernels for Quantized Inference"
+ *              (launch article): the paragraphs on the standard format,
+ *              preprocessing, pipelines and tuning controls.
+ *   [WIKI]     "Humming" (aiwiki article): sections "Quantization
+ *              representation", "Kernel configuration and compilation",
+ *              "Device and workload selection", "Precision and deployment
+ *              considerations".
+ *
+ * Conventions for every call:
+ *   - All device pointers are owned by the caller.  The library allocates no
+ *     device or host memory and keeps no mutable global state except a
+ *     read-mostly cache of per-device properties.
+ *   - Calls are stream-ordered and asynchronous unless stated otherwise.
+ *     Errors the host can detect are returned before anything is launched.
+ *   - Errors found on the device (a bounded wait that ran out, an expert id
+ *     out of range) are written into a status word at the start of the
+ *     caller's workspace; hq_status_read() synchronises and reads it.
+ *   - Pointers passed to the GEMM calls must be 16-byte aligned, and row
+ *     strides must be multiples of 16 bytes (the TMA rule); otherwise the
+ *     call returns HQ_ERR_ALIGNMENT.
+ *   - The compute calls need an sm_103 device (B300/GB300); on any other
+ *     device they return HQ_ERR_ARCH.  A transformed weight is tied to that
+ *     architecture ([WIKI] "Quantization representation": a transformed
+ *     layer must match its configured SM version).
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef HQ_H_
+#define HQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* CUDA stream handle (a cudaStream_t); NULL is the legacy default stream. */
+typedef void* hq_stream_t;
+
+typedef enum {
+  HQ_OK = 0,
+  HQ_ERR_INVALID_ARG = 1,         /* null pointer, bad enum, bad shape, bad group */
+  HQ_ERR_UNSUPPORTED = 2,         /* valid combination this build does not implement */
+  HQ_ERR_ALIGNMENT = 3,           /* pointer or stride breaks the 16-byte rule */
+  HQ_ERR_WORKSPACE_TOO_SMALL = 4, /* dst/workspace smaller than the *_size query */
+  HQ_ERR_CUDA = 5,                /* a CUDA runtime call failed */
+  HQ_ERR_DEVICE_TIMEOUT = 6,      /* a bounded device-side wait ran out */
+  HQ_ERR_ARCH = 7,                /* current device is not sm_103 */
+  HQ_ERR_INVALID_VALUE = 8        /* bad data found on the device (NaN scale, expert id out of range) */
+} hq_status;
+
+/* Weight element types ([README] Support Matrix; [WIKI] "Quantization representation"). */
+typedef enum {
+  HQ_W_INT4 = 0,      /* 4-bit integer codes, symmetric (two's complement) or with zero points */
+  HQ_W_INT6 = 1,      /* 6-bit integer codes, symmetric or with zero points */
+  HQ_W_MXFP4 = 2,     /* OCP MX e2m1 elements with one UE8M0 scale per 32 along K */
+  HQ_W_FP8_E4M3 = 3   /* OCP e4m3 elements with float32 128x128 block scales */
+} hq_wtype;
+
+/* Activation types ([README] Support Matrix rows FP16, BF16, FP8 e4m3). */
+typedef enum {
+  HQ_A_BF16 = 0,
+  HQ_A_FP16 = 1,
+  HQ_A_FP8_E4M3 = 2   /* with float32 per-token, per-128-K-group scales */
+} hq_atype;
+
+/* Scale types ([README] Key Features: BF16, FP16, UE8M0; float32 for FP8 block scales). */
+typedef enum {
+  HQ_S_BF16 = 0,
+  HQ_S_FP16 = 1,
+  HQ_S_FP32 = 2,
+  HQ_S_UE8M0 = 3
+} hq_stype;
+
+/*
+ * hq_weight_desc — one quantized weight in the standard storage format
+ * ([LAUNCH] standard format: weight format, scaling granularity, scale data
+ * type and zero points as separate parameters; [WIKI] "Quantization
+ * representation": channel, group and block scales, optional zero points, an
+ * expert dimension for MoE).
+ *
+ * Layout of the standard format, all row-major with a leading expert axis E
+ * (num_experts = 1 for dense weights), G = K / group_k groups per row
+ * (G = 1 when group_k = 0, "channelwise"):
+ *   INT4   codes  uint8 [E][N][ceil(K/2)]   element k in byte k/2, low nibble
+ *                                            for even k; two's complement when
+ *                                            signed_codes, else unsigned 0..15
+ *   INT6   codes  uint8 [E][N][3K/4]         little-endian bit stream per row,
+ *                                            code k in bits [6k, 6k+6)
+ *   MXFP4  codes  uint8 [E][N][K/2]          nibbles as INT4; e2m1 = S.EE.M
+ *   FP8    codes  uint8 [E][N][K]            e4m3 "fn" bytes
+ *   scales INT4/INT6: bf16 or fp16 [E][N][G]; MXFP4: UE8M0 bytes [E][N][K/32];
+ *          FP8: float32 [E][ceil(N/128)][ceil(K/128)]
+ *   zeros  INT4/INT6 with has_zeros only: unsigned codes packed exactly like
+ *          that format's codes, [E][N][packed(G)] (INT4: ceil(G/2) bytes,
+ *          INT6: 3*ceil(G/4) bytes)
+ * Dequantisation: symmetric int  w = q * s;  zero point  w = (q - z) * s;
+ * MXFP4  w = e2m1(q) * 2^(E - 127);  FP8  w = e4m3(q) * s_w[n/128][k/128].
+ *
+ * Constraints: INT4/INT6 group_k in {0, 32, 64, 128} or a multiple of 128,
+ * dividing K; INT6 needs K % 4 == 0; MXFP4 group_k = 32 (K % 32 == 0) and
+ * stype UE8M0; FP8 group_k = group_n = 128 and stype FP32; INT stype BF16 or
+ * FP16.  The codes/scales/zeros pointers are read by hq_transform only; the
+ * GEMM calls use the shape fields and ignore the pointers.
+ */
+typedef struct {
+  int32_t wtype;        /* hq_wtype */
+  int32_t stype;        /* hq_stype */
+  int32_t n;            /* output features N (rows of W) */
+  int32_t k;            /* reduction length K */
+  int32_t num_experts;  /* E >= 1 */
+  int32_t group_k;      /* scale group along K; 0 = one scale per row */
+  int32_t group_n;      /* 1, or 128 for FP8 block scales */
+  int32_t signed_codes; /* INT without zeros: 1 = two's complement codes */
+  int32_t has_zeros;    /* INT only: 1 = zero points present */
+  int32_t reserved;
+  const void* codes;    /* device pointer, standard format */
+  const void* scales;   /* device pointer, standard format */
+  const void* zeros;    /* device pointer or NULL */
+} hq_weight_desc;
+
+/* flags for hq_gemm / hq_moe_gemm */
+#define HQ_FLAG_BATCH_INVARIANT 0x1u /* no split-K: the reduction order does not depend on M
+                                        ([WIKI] "Precision and deployment considerations") */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t hq_version(void);
+
+/* Static string for a status code; never NULL. */
+const char* hq_status_string(int32_t status);
+
+/*
+ * hq_transform_size — bytes of the device buffer that hq_transform writes
+ * for this weight.  Host only; reads no pointer of the descriptor.
+ * Returns HQ_ERR_INVALID_ARG / HQ_ERR_UNSUPPORTED for an invalid descriptor.
+ */
+hq_status hq_transform_size(const hq_weight_desc* desc, size_t* bytes);
+
+/*
+ * hq_transform — repack a standard-format weight into the sm_103 tile layout
+ * ([LAUNCH] "Preprocessing then validates parameters, pads dimensions, and
+ * repacks these tensors into layouts suited to the target kernel"; [WIKI]
+ * "Quantization representation": transform() converts and transforms weights
+ * and associated parameters for execution).
+ *
+ * desc   standard-format device pointers (codes, scales, zeros)
+ * dst    device buffer of at least hq_transform_size() bytes, 256-byte
+ *        aligned; owned by the caller; opaque layout (tiles of 128 rows x
+ *        128 K, rows and K padded to 128 with zero-valued codes)
+ * Synchronous: it waits for the repack kernel on `stream` and returns
+ * HQ_ERR_INVALID_VALUE if the weight holds a NaN scale (UE8M0 0xFF) or a
+ * NaN e4m3 code; the buffer contents are then unspecified.
+ */
+hq_status hq_transform(const hq_weight_desc* desc, void* dst, size_t dst_bytes, hq_stream_t stream);
+
+/*
+ * hq_untransform — the exact inverse of hq_transform: writes the standard
+ * format back into caller buffers codes/scales/zeros (sizes as in the
+ * descriptor layout; zeros ignored without has_zeros).  Bit-exact for every
+ * input hq_transform accepts.  Asynchronous.
+ */
+hq_status hq_untransform(const hq_weight_desc* desc, const void* src, void* codes, void* scales,
+                         void* zeros, hq_stream_t stream);
+
+/*
+ * hq_gemm_workspace_size — bytes of workspace hq_gemm needs for this weight,
+ * M and activation type (status word, split-K counters and fp32 partials).
+ */
+hq_status hq_gemm_workspace_size(const hq_weight_desc* desc, int32_t m, int32_t atype, size_t* bytes);
+
+/*
+ * hq_workspace_init — zero a workspace (asynchronous memset on `stream`).
+ * A workspace must be initialised once before its first use; every call that
+ * completes leaves its counters at zero again, so re-initialising is only
+ * needed after HQ_ERR_DEVICE_TIMEOUT.
+ */
+hq_status hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);
+
+/*
+ * hq_gemm — dense quantized GEMM  Y = a(X) . dequant(W)^T  ([LAUNCH] WnA16
+ * and W8A8 paragraphs; [README] Usage Example layer(inputs)).
+ *
+ * wdesc     shape of the weight (pointers ignored); num_experts must be 1
+ * w_t       hq_transform output for wdesc
+ * m         rows of X and Y (0 is a no-op)
+ * atype     hq_atype; INT with group scales needs stype == atype; MXFP4 needs
+ *           BF16 or FP16; FP8 weights need FP8 activations
+ * x, ldx    X [m][k] row-major, row stride ldx elements (ldx >= k)
+ * x_scales  FP8 activations only: float32 [m][ceil(k/128)] row-major
+ * y, ldy    Y [m][n] row-major, bf16 for BF16/FP8 activations, fp16 for FP16
+ * workspace >= hq_gemm_workspace_size() bytes, initialised once
+ * flags     HQ_FLAG_* bits
+ * Accumulation is fp32 in tensor memory; the output is rounded once.
+ */
+hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32_t atype,
+                  const void* x, int64_t ldx, const float* x_scales, void* y, int64_t ldy,
+                  void* workspace, size_t ws_bytes, uint32_t flags, hq_stream_t stream);
+
+/*
+ * hq_moe_workspace_size — workspace for hq_moe_gemm (status word, routing
+ * counts and offsets, permutation, per-pair fp32 outputs).
+ */
+hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int32_t topk,
+                                int32_t atype, size_t* bytes);
+
+/*
+ * hq_moe_gemm — MoE grouped GEMM over routed tokens ([WIKI] "Device and
+ * workload selection": indexed input gathered through routing indices,
+ * grouped-contiguous execution per expert; [README] MoE GEMM).
+ *
+ * For flat pair f = t*topk + j with expert e = topk_ids[t][j]:
+ *   route   counts, offsets[E+1] (exclusive prefix sum), and the stable
+ *           permutation perm[offsets[e] + r] = r-th f (increasing) routed to e
+ *   GEMM    Z[f] = a(X[t]) . dequant(W_e)^T     (N outputs)
+ *   combine Y[t] = sum_j topk_w[t][j] * Z[t*topk + j], j in increasing order
+ *
+ * wdesc, w_t   expert weights [E][N][K] and their transform
+ * tokens, topk T and top-k; topk_ids int32 [T][topk], topk_w float32 [T][topk]
+ * x, ldx       activations [T][k]; y, ldy output [T][n] (bf16 for BF16 acts)
+ * expert_offsets_out  optional int32 [E+1]; perm_out optional int32 [T*topk]
+ * An expert id outside [0, E) makes its pair contribute nothing and sets
+ * HQ_ERR_INVALID_VALUE in the workspace status word.
+ */
+hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t tokens, int32_t topk,
+                      const int32_t* topk_ids, const float* topk_w, int32_t atype, const void* x,
+                      int64_t ldx, void* y, int64_t ldy, int32_t* expert_offsets_out,
+                      int32_t* perm_out, void* workspace, size_t ws_bytes, uint32_t flags,
+                      hq_stream_t stream);
+
+/*
+ * hq_status_read — synchronise `stream` and read the device status word of a
+ * workspace (HQ_OK when no device-side error was recorded).  With clear != 0
+ * the word is reset to HQ_OK afterwards.
+ */
+hq_status hq_status_read(void* workspace, int32_t clear, hq_stream_t stream, int32_t* device_status);
+
+/*
+ * hq_last_plan — the launch plan of the most recent hq_gemm / hq_moe_gemm
+ * call on this host thread: tile width along M (bn), split-K factor, grid
+ * size and kernel launches.  For tests and benchmarks.
+ */
+typedef struct {
+  int32_t bn;
+  int32_t splits;
+  int32_t grid;
+  int32_t launches;
+  int32_t stages;
+  int32_t reserved[3];
+} hq_plan_info;
+hq_status hq_last_plan(hq_plan_info* info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HQ_H_ */

@@ -1,0 +1,190 @@
+"""Python binding of the GB300 quantized GEMM library (``include/hq.h``).
+
+Argument marshalling only: every function here forwards to the C ABI of the
+in-tree ``libhq.so`` (built by ``_build.build()``), whose kernels do all the
+work.  Pointers may be given as integers or as objects with ``data_ptr()``
+(torch tensors); streams as integers, ``None`` (default stream) or objects
+with a ``cuda_stream`` attribute.  A non-OK status raises ``HQError``.
+
+There is no fallback: if the library is missing, importing the functions
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libhq.so")
+
+# enums of hq.h
+HQ_OK, HQ_ERR_INVALID_ARG, HQ_ERR_UNSUPPORTED, HQ_ERR_ALIGNMENT = 0, 1, 2, 3
+HQ_ERR_WORKSPACE_TOO_SMALL, HQ_ERR_CUDA, HQ_ERR_DEVICE_TIMEOUT, HQ_ERR_ARCH, HQ_ERR_INVALID_VALUE = 4, 5, 6, 7, 8
+HQ_W_INT4, HQ_W_INT6, HQ_W_MXFP4, HQ_W_FP8_E4M3 = 0, 1, 2, 3
+HQ_A_BF16, HQ_A_FP16, HQ_A_FP8_E4M3 = 0, 1, 2
+HQ_S_BF16, HQ_S_FP16, HQ_S_FP32, HQ_S_UE8M0 = 0, 1, 2, 3
+HQ_FLAG_BATCH_INVARIANT = 0x1
+
+WTYPES = {"int4": HQ_W_INT4, "int6": HQ_W_INT6, "mxfp4": HQ_W_MXFP4, "fp8": HQ_W_FP8_E4M3}
+ATYPES = {"bf16": HQ_A_BF16, "fp16": HQ_A_FP16, "fp8": HQ_A_FP8_E4M3}
+STYPES = {"bf16": HQ_S_BF16, "fp16": HQ_S_FP16, "fp32": HQ_S_FP32, "ue8m0": HQ_S_UE8M0}
+
+#: every symbol include/hq.h declares
+EXPORTS = [
+    "hq_version", "hq_status_string", "hq_transform_size", "hq_transform", "hq_untransform",
+    "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_moe_workspace_size", "hq_moe_gemm",
+    "hq_status_read", "hq_last_plan",
+]
+
+
+class HQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class WeightDesc(ctypes.Structure):
+    """hq_weight_desc."""
+    _fields_ = [
+        ("wtype", ctypes.c_int32), ("stype", ctypes.c_int32), ("n", ctypes.c_int32), ("k", ctypes.c_int32),
+        ("num_experts", ctypes.c_int32), ("group_k", ctypes.c_int32), ("group_n", ctypes.c_int32),
+        ("signed_codes", ctypes.c_int32), ("has_zeros", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zeros", ctypes.c_void_p),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    """hq_plan_info."""
+    _fields_ = [("bn", ctypes.c_int32), ("splits", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("launches", ctypes.c_int32), ("stages", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libhq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: run quantized_gemm_tma_gb300._build.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, u32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t
+        dp = ctypes.POINTER(WeightDesc)
+        sig = {
+            "hq_version": ([], i32),
+            "hq_status_string": ([i32], ctypes.c_char_p),
+            "hq_transform_size": ([dp, ctypes.POINTER(sz)], i32),
+            "hq_transform": ([dp, vp, sz, vp], i32),
+            "hq_untransform": ([dp, vp, vp, vp, vp, vp], i32),
+            "hq_gemm_workspace_size": ([dp, i32, i32, ctypes.POINTER(sz)], i32),
+            "hq_workspace_init": ([vp, sz, vp], i32),
+            "hq_gemm": ([dp, vp, i32, i32, vp, i64, vp, vp, i64, vp, sz, u32, vp], i32),
+            "hq_moe_workspace_size": ([dp, i32, i32, i32, ctypes.POINTER(sz)], i32),
+            "hq_moe_gemm": ([dp, vp, i32, i32, vp, vp, i32, vp, i64, vp, i64, vp, vp, vp, sz, u32, vp], i32),
+            "hq_status_read": ([vp, i32, vp, ctypes.POINTER(i32)], i32),
+            "hq_last_plan": ([ctypes.POINTER(PlanInfo)], i32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _check(st: int, where: str) -> None:
+    if st != HQ_OK:
+        raise HQError(st, where)
+
+
+def status_string(status: int) -> str:
+    return lib().hq_status_string(status).decode()
+
+
+def hq_version() -> int:
+    return int(lib().hq_version())
+
+
+def make_desc(wtype, stype, n, k, num_experts=1, group_k=128, group_n=1, signed_codes=True, has_zeros=False,
+              codes=None, scales=None, zeros=None) -> WeightDesc:
+    """Build an hq_weight_desc (enum names or values accepted)."""
+    return WeightDesc(WTYPES.get(wtype, wtype), STYPES.get(stype, stype), n, k, num_experts, group_k, group_n,
+                      1 if signed_codes else 0, 1 if has_zeros else 0, 0,
+                      _ptr(codes), _ptr(scales), _ptr(zeros))
+
+
+def hq_transform_size(desc: WeightDesc) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().hq_transform_size(ctypes.byref(desc), ctypes.byref(out)), "hq_transform_size")
+    return out.value
+
+
+def hq_transform(desc: WeightDesc, dst, dst_bytes: int, stream=None) -> None:
+    _check(lib().hq_transform(ctypes.byref(desc), _ptr(dst), dst_bytes, _stream(stream)), "hq_transform")
+
+
+def hq_untransform(desc: WeightDesc, src, codes, scales, zeros=None, stream=None) -> None:
+    _check(lib().hq_untransform(ctypes.byref(desc), _ptr(src), _ptr(codes), _ptr(scales), _ptr(zeros),
+                                _stream(stream)), "hq_untransform")
+
+
+def hq_gemm_workspace_size(desc: WeightDesc, m: int, atype) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().hq_gemm_workspace_size(ctypes.byref(desc), m, ATYPES.get(atype, atype), ctypes.byref(out)),
+           "hq_gemm_workspace_size")
+    return out.value
+
+
+def hq_workspace_init(workspace, nbytes: int, stream=None) -> None:
+    _check(lib().hq_workspace_init(_ptr(workspace), nbytes, _stream(stream)), "hq_workspace_init")
+
+
+def hq_gemm(desc: WeightDesc, w_t, m: int, atype, x, ldx: int, x_scales, y, ldy: int, workspace, ws_bytes: int,
+            flags: int = 0, stream=None) -> None:
+    _check(lib().hq_gemm(ctypes.byref(desc), _ptr(w_t), m, ATYPES.get(atype, atype), _ptr(x), ldx, _ptr(x_scales),
+                         _ptr(y), ldy, _ptr(workspace), ws_bytes, flags, _stream(stream)), "hq_gemm")
+
+
+def hq_moe_workspace_size(desc: WeightDesc, tokens: int, topk: int, atype) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().hq_moe_workspace_size(ctypes.byref(desc), tokens, topk, ATYPES.get(atype, atype),
+                                       ctypes.byref(out)), "hq_moe_workspace_size")
+    return out.value
+
+
+def hq_moe_gemm(desc: WeightDesc, w_t, tokens: int, topk: int, topk_ids, topk_w, atype, x, ldx: int, y, ldy: int,
+                expert_offsets_out, perm_out, workspace, ws_bytes: int, flags: int = 0, stream=None) -> None:
+    _check(lib().hq_moe_gemm(ctypes.byref(desc), _ptr(w_t), tokens, topk, _ptr(topk_ids), _ptr(topk_w),
+                             ATYPES.get(atype, atype), _ptr(x), ldx, _ptr(y), ldy, _ptr(expert_offsets_out),
+                             _ptr(perm_out), _ptr(workspace), ws_bytes, flags, _stream(stream)), "hq_moe_gemm")
+
+
+def hq_status_read(workspace, clear: bool = False, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _check(lib().hq_status_read(_ptr(workspace), 1 if clear else 0, _stream(stream), ctypes.byref(out)),
+           "hq_status_read")
+    return out.value
+
+
+def hq_last_plan() -> dict:
+    info = PlanInfo()
+    _check(lib().hq_last_plan(ctypes.byref(info)), "hq_last_plan")
+    return {"bn": info.bn, "splits": info.splits, "grid": info.grid, "launches": info.launches,
+            "stages": info.stages}

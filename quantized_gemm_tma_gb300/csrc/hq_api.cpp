@@ -1,0 +1,579 @@
+// hq_api.cpp — the C ABI declared in include/hq.h: argument validation, the
+// tile layout, launch planning ("device-specific heuristics" that pick tile
+// width and split-K from M, N, K and the SM count — Humming aiwiki article,
+// "Device and workload selection"; launch article, tuning-controls paragraph)
+// and kernel launches.  No memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "hq.h"
+#include "hq_internal.h"
+#include "hq_launch.h"
+
+namespace hq {
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+thread_local hq_plan_info g_last_plan{};
+
+// ------------------------------------------------------------------ devices
+struct DevInfo {
+  bool init = false;
+  int cc_major = 0, cc_minor = 0, sms = 0;
+  size_t smem_optin = 0;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+hq_status device_info(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return HQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return HQ_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return HQ_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HQ_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return HQ_ERR_CUDA;
+    d.smem_optin = static_cast<size_t>(v);
+    d.init = true;
+  }
+  *out = d;
+  if (d.cc_major != 10 || d.cc_minor != 3) return HQ_ERR_ARCH;
+  return HQ_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+hq_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return HQ_ERR_CUDA;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_elems * elem};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HQ_OK : HQ_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : dflt;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ layout
+hq_status make_layout(const hq_weight_desc& d, Layout* L) {
+  if (d.n <= 0 || d.k <= 0 || d.num_experts <= 0) return HQ_ERR_INVALID_ARG;
+  if (d.wtype < HQ_W_INT4 || d.wtype > HQ_W_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (d.stype < HQ_S_BF16 || d.stype > HQ_S_UE8M0) return HQ_ERR_INVALID_ARG;
+  std::memset(L, 0, sizeof(*L));
+  L->wtype = d.wtype; L->stype = d.stype; L->n = d.n; L->k = d.k; L->num_experts = d.num_experts;
+  L->group_k = d.group_k; L->signed_codes = d.signed_codes ? 1 : 0; L->has_zeros = d.has_zeros ? 1 : 0;
+  L->n_tiles = cdiv(d.n, kTileN); L->k_tiles = cdiv(d.k, kTileK);
+  L->n_pad = L->n_tiles * kTileN; L->k_pad = L->k_tiles * kTileK;
+  const bool is_int = d.wtype == HQ_W_INT4 || d.wtype == HQ_W_INT6;
+  if (is_int) {
+    if (d.stype != HQ_S_BF16 && d.stype != HQ_S_FP16) return HQ_ERR_INVALID_ARG;
+    if (d.group_n != 1 && d.group_n != 0) return HQ_ERR_INVALID_ARG;
+    const int g = d.group_k;
+    if (g < 0) return HQ_ERR_INVALID_ARG;
+    if (g != 0) {
+      if (!(g == 32 || g == 64 || g % 128 == 0)) return HQ_ERR_INVALID_ARG;
+      if (d.k % g != 0) return HQ_ERR_INVALID_ARG;
+    }
+    if (d.wtype == HQ_W_INT6 && d.k % 4 != 0) return HQ_ERR_INVALID_ARG;
+    L->channel = g == 0;
+    L->groups = g == 0 ? 1 : d.k / g;
+    L->g_kb = g == 0 ? 0 : (g < 128 ? 128 / g : 1);
+  } else if (d.wtype == HQ_W_MXFP4) {
+    if (d.stype != HQ_S_UE8M0 || d.group_k != 32 || d.k % 32 != 0 || d.has_zeros) return HQ_ERR_INVALID_ARG;
+    if (d.group_n != 1 && d.group_n != 0) return HQ_ERR_INVALID_ARG;
+  } else {
+    if (d.stype != HQ_S_FP32 || d.group_k != 128 || d.group_n != 128 || d.has_zeros) return HQ_ERR_INVALID_ARG;
+  }
+  uint32_t codes = 0, hi = 0, sc = 0, zr = 0;
+  switch (d.wtype) {
+    case HQ_W_INT4: codes = 8192; break;
+    case HQ_W_INT6: codes = 8192; hi = 4096; break;
+    case HQ_W_MXFP4: codes = 8192; sc = 512; break;
+    default: codes = 16384; break;
+  }
+  if (is_int && !L->channel) {
+    sc = 256u * L->g_kb;
+    if (L->has_zeros) zr = 128u * L->g_kb;
+  }
+  L->codes_bytes = codes;
+  L->hi_off = codes;
+  L->scale_off = codes + hi;
+  L->scale_bytes = sc;
+  L->zero_off = L->scale_off + sc;
+  L->zero_bytes = zr;
+  L->tile_bytes = L->zero_off + zr;
+  L->tiles_off = kHeaderBytes;
+  L->expert_stride = static_cast<uint64_t>(L->n_tiles) * L->k_tiles * L->tile_bytes;
+  uint64_t off = align_up(L->tiles_off + L->expert_stride * d.num_experts, kAlign);
+  if (is_int && L->channel) {
+    L->row_off = off;
+    off = align_up(off + 4ull * d.num_experts * L->n_pad, kAlign);
+    if (L->has_zeros) {
+      L->row_zero_off = off;
+      off = align_up(off + 1ull * d.num_experts * L->n_pad, kAlign);
+    }
+  }
+  if (d.wtype == HQ_W_FP8_E4M3) {
+    L->blk_off = off;
+    off = align_up(off + 4ull * d.num_experts * L->n_tiles * L->k_tiles, kAlign);
+  }
+  L->total = off;
+  return HQ_OK;
+}
+
+}  // namespace hq
+
+using namespace hq;
+
+// ====================================================================== C ABI
+extern "C" {
+
+int32_t hq_version(void) { return 100; }
+
+const char* hq_status_string(int32_t s) {
+  switch (s) {
+    case HQ_OK: return "ok";
+    case HQ_ERR_INVALID_ARG: return "invalid argument";
+    case HQ_ERR_UNSUPPORTED: return "unsupported combination";
+    case HQ_ERR_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+    case HQ_ERR_WORKSPACE_TOO_SMALL: return "buffer or workspace too small";
+    case HQ_ERR_CUDA: return "CUDA runtime error";
+    case HQ_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case HQ_ERR_ARCH: return "device is not sm_103";
+    case HQ_ERR_INVALID_VALUE: return "invalid value found on the device";
+    default: return "unknown status";
+  }
+}
+
+hq_status hq_transform_size(const hq_weight_desc* desc, size_t* bytes) {
+  if (!desc || !bytes) return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*desc, &L);
+  if (st != HQ_OK) return st;
+  *bytes = L.total;
+  return HQ_OK;
+}
+
+hq_status hq_transform(const hq_weight_desc* desc, void* dst, size_t dst_bytes, hq_stream_t stream) {
+  if (!desc || !dst) return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*desc, &L);
+  if (st != HQ_OK) return st;
+  if (!desc->codes || !desc->scales || (L.has_zeros && !desc->zeros)) return HQ_ERR_INVALID_ARG;
+  if (dst_bytes < L.total) return HQ_ERR_WORKSPACE_TOO_SMALL;
+  if ((reinterpret_cast<uintptr_t>(dst) & 255u) != 0) return HQ_ERR_ALIGNMENT;
+  if (desc->wtype == HQ_W_FP8_E4M3 && (reinterpret_cast<uintptr_t>(desc->scales) & 3u)) return HQ_ERR_ALIGNMENT;
+  if ((desc->wtype == HQ_W_INT4 || desc->wtype == HQ_W_INT6) && (reinterpret_cast<uintptr_t>(desc->scales) & 1u))
+    return HQ_ERR_ALIGNMENT;
+  DevInfo di;
+  st = device_info(&di);
+  if (st != HQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_repack(L, *desc, dst, s) != cudaSuccess) return HQ_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HQ_ERR_CUDA;
+  TileHeader h;
+  if (cudaMemcpy(&h, dst, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return HQ_ERR_CUDA;
+  if (h.magic != kMagic) return HQ_ERR_CUDA;
+  return h.invalid_count ? HQ_ERR_INVALID_VALUE : HQ_OK;
+}
+
+hq_status hq_untransform(const hq_weight_desc* desc, const void* src, void* codes, void* scales, void* zeros,
+                         hq_stream_t stream) {
+  if (!desc || !src || !codes || !scales) return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*desc, &L);
+  if (st != HQ_OK) return st;
+  if (L.has_zeros && !zeros) return HQ_ERR_INVALID_ARG;
+  DevInfo di;
+  st = device_info(&di);
+  if (st != HQ_OK) return st;
+  if (launch_unpack(L, src, codes, scales, zeros, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  return HQ_OK;
+}
+
+hq_status hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream) {
+  if (!workspace || bytes < kHeaderBytes) return HQ_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? HQ_OK
+                                                                                               : HQ_ERR_CUDA;
+}
+
+hq_status hq_status_read(void* workspace, int32_t clear, hq_stream_t stream, int32_t* device_status) {
+  if (!workspace || !device_status) return HQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HQ_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return HQ_ERR_CUDA;
+  *device_status = v;
+  if (clear && v != 0) {
+    if (cudaMemset(workspace, 0, sizeof(int32_t)) != cudaSuccess) return HQ_ERR_CUDA;
+  }
+  return HQ_OK;
+}
+
+hq_status hq_last_plan(hq_plan_info* info) {
+  if (!info) return HQ_ERR_INVALID_ARG;
+  *info = g_last_plan;
+  return HQ_OK;
+}
+
+}  // extern "C"
+
+// ====================================================================== GEMM planning
+namespace hq {
+namespace {
+
+constexpr int kMaxSplits = 64;
+constexpr int kPlanSmsBound = 192;  // >= the SM count of any sm_103 part (workspace sizing)
+
+struct DensePlan {
+  int bn, bn_max, m_tiles, splits, kb_per_split, stages, grid;
+  uint32_t smem;
+  int min_blocks;
+};
+
+// FP8: 128 tokens per tile (MMA M), 128 or 256 weight rows (MMA N), split-K
+// until the work items fill the SMs.
+struct Fp8Plan {
+  int bn, m_tiles, n_groups, splits, kb_per_split, stages, grid;
+  uint32_t smem;
+};
+
+Fp8Plan plan_fp8(const Layout& L, int m, int sms, size_t smem_optin, uint32_t flags) {
+  Fp8Plan p{};
+  p.m_tiles = cdiv(m, 128);
+  p.bn = (L.n_tiles >= 2 && p.m_tiles * cdiv(L.n_tiles, 2) >= sms / 2) ? 256 : 128;
+  const int forced_bn = env_int("HQ_FORCE_BN", 0);
+  if (forced_bn == 128 || forced_bn == 256) p.bn = forced_bn;
+  p.n_groups = cdiv(L.n_tiles, p.bn / 128);
+  const int tiles = p.m_tiles * p.n_groups;
+  int splits = 1;
+  if (!(flags & HQ_FLAG_BATCH_INVARIANT) && tiles < sms)
+    splits = std::min(std::max(1, sms / tiles), std::max(1, L.k_tiles / 4));
+  const int forced = env_int("HQ_FORCE_SPLITK", 0);
+  if (forced > 0 && !(flags & HQ_FLAG_BATCH_INVARIANT)) splits = std::min(forced, L.k_tiles);
+  splits = std::min(splits, kMaxSplits);
+  p.kb_per_split = cdiv(L.k_tiles, splits);
+  p.splits = cdiv(L.k_tiles, p.kb_per_split);
+  const size_t budget = std::min<size_t>(smem_optin, 232448) - 4096;
+  const uint32_t per_stage = 16384u * (p.bn / 128) + 16384u;
+  p.stages = std::max(2, static_cast<int>(std::min<size_t>(6, budget / per_stage)));
+  p.smem = fp8_smem_bytes(p.stages, p.bn);
+  p.grid = std::min(tiles * p.splits, sms);
+  return p;
+}
+
+// Split-K scratch of a plan: counters [m_tiles * n_tiles(or groups) * 8], fp32 partials.
+size_t splitk_bytes(int splits, int m_tiles, int n_tiles, int m, int n_pad) {
+  if (splits <= 1) return 0;
+  return align_up(sizeof(int) * static_cast<size_t>(m_tiles) * n_tiles * 8, kAlign) +
+         align_up(sizeof(float) * static_cast<size_t>(splits) * m * n_pad, kAlign);
+}
+
+// Heuristic for one GB300: tokens per tile from M, then split-K until the
+// (n-tile, m-tile, split) work items fill the SMs, with at least 4 K-tiles
+// per split so the fp32 partial traffic stays small next to the weights.
+DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_t flags) {
+  DensePlan p{};
+  if (m <= 64) {
+    p.bn_max = 64;
+    p.bn = std::max(16, cdiv(m, 16) * 16);
+  } else {
+    p.bn_max = 256;
+    p.bn = m <= 128 ? 128 : (m <= 192 ? 192 : 256);
+  }
+  const int forced_bn = env_int("HQ_FORCE_BN", 0);
+  if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) {
+    p.bn = forced_bn;
+    p.bn_max = forced_bn <= 64 ? 64 : 256;
+  }
+  p.m_tiles = cdiv(m, p.bn);
+  const int tiles = p.m_tiles * L.n_tiles;
+  p.min_blocks = wna16_min_blocks(p.bn_max);
+  const int slots = sms * p.min_blocks;
+  int splits = 1;
+  if (!(flags & HQ_FLAG_BATCH_INVARIANT) && tiles < slots) {
+    splits = std::min(std::max(1, slots / tiles), std::max(1, L.k_tiles / 4));
+  }
+  const int forced = env_int("HQ_FORCE_SPLITK", 0);
+  if (forced > 0 && !(flags & HQ_FLAG_BATCH_INVARIANT)) splits = std::min(forced, L.k_tiles);
+  splits = std::min(splits, kMaxSplits);
+  p.kb_per_split = cdiv(L.k_tiles, splits);
+  p.splits = cdiv(L.k_tiles, p.kb_per_split);  // every split gets >= 1 K-tile
+  const size_t budget = std::min<size_t>(smem_optin, 232448 / p.min_blocks) - 2048;
+  const uint32_t per_stage = ((L.tile_bytes + 127u) & ~127u) + static_cast<uint32_t>(p.bn) * 256u;
+  p.stages = static_cast<int>(std::min<size_t>(8, budget / per_stage));
+  p.stages = std::max(p.stages, 2);
+  p.smem = wna16_smem_bytes(p.stages, L.tile_bytes, p.bn, 0);
+  const int items = tiles * p.splits;
+  p.grid = std::min(items, slots);
+  return p;
+}
+
+}  // namespace
+}  // namespace hq
+
+extern "C" {
+
+hq_status hq_gemm_workspace_size(const hq_weight_desc* desc, int32_t m, int32_t atype, size_t* bytes) {
+  if (!desc || !bytes || m < 0) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*desc, &L);
+  if (st != HQ_OK) return st;
+  size_t ws = kAlign;  // status word
+  if (m > 0) {
+    // split-K scratch of the largest plan any sm_103 device would choose
+    size_t best = 0;
+    for (int sms = 1; sms <= kPlanSmsBound; sms = sms < 64 ? sms * 2 : sms + 8) {
+      if (desc->wtype == HQ_W_FP8_E4M3) {
+        const Fp8Plan p = plan_fp8(L, m, sms, 232448, 0);
+        best = std::max(best, splitk_bytes(p.splits, p.m_tiles, p.n_groups, m, L.n_pad));
+      } else {
+        const DensePlan p = plan_wna16(L, m, sms, 232448, 0);
+        best = std::max(best, splitk_bytes(p.splits, p.m_tiles, L.n_tiles, m, L.n_pad));
+      }
+    }
+    ws += best;
+  }
+  *bytes = ws;
+  return HQ_OK;
+}
+
+hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32_t atype, const void* x,
+                  int64_t ldx, const float* x_scales, void* y, int64_t ldy, void* workspace, size_t ws_bytes,
+                  uint32_t flags, hq_stream_t stream) {
+  if (!wdesc || m < 0) return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*wdesc, &L);
+  if (st != HQ_OK) return st;
+  if (L.num_experts != 1) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (m == 0) return HQ_OK;
+  if (!w_t || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;
+  if (ldx < L.k || ldy < L.n) return HQ_ERR_INVALID_ARG;
+  const bool fp8 = L.wtype == HQ_W_FP8_E4M3;
+  if (fp8 != (atype == HQ_A_FP8_E4M3)) return HQ_ERR_UNSUPPORTED;
+  if (fp8 && !x_scales) return HQ_ERR_INVALID_ARG;
+  if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel) {
+    if ((L.stype == HQ_S_BF16) != (atype == HQ_A_BF16)) return HQ_ERR_UNSUPPORTED;
+  }
+  if (L.wtype == HQ_W_MXFP4 && atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  const uint32_t xelem = fp8 ? 1 : 2;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(w_t) & 255u))
+    return HQ_ERR_ALIGNMENT;
+  if ((ldx * xelem) % 16 != 0 || (ldy * 2) % 4 != 0) return HQ_ERR_ALIGNMENT;
+  if (fp8 && !aligned16(x_scales)) return HQ_ERR_ALIGNMENT;
+  size_t need = 0;
+  hq_gemm_workspace_size(wdesc, m, atype, &need);
+  if (ws_bytes < need) return HQ_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  st = device_info(&di);
+  if (st != HQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* wt = static_cast<const uint8_t*>(w_t);
+
+  if (fp8) {
+    const Fp8Plan pl = plan_fp8(L, m, di.sms, di.smem_optin, flags);
+    Fp8Params p{};
+    p.tiles = wt + L.tiles_off;
+    p.expert_stride = L.expert_stride;
+    p.tile_bytes = L.tile_bytes;
+    p.blk_scale = reinterpret_cast<const float*>(wt + L.blk_off);
+    p.x_scale = x_scales;
+    p.n = L.n; p.n_pad = L.n_pad; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = m;
+    p.bn = pl.bn; p.m_tiles = pl.m_tiles; p.stages = pl.stages;
+    p.splits = pl.splits; p.kb_per_split = pl.kb_per_split;
+    p.idesc = idesc_e4m3(128, pl.bn);
+    p.y = y; p.ldy = ldy;
+    p.status = reinterpret_cast<int*>(ws);
+    p.counters = reinterpret_cast<int*>(ws + kAlign);
+    p.partials = reinterpret_cast<float*>(
+        ws + kAlign + align_up(sizeof(int) * static_cast<size_t>(pl.m_tiles) * pl.n_groups * 8, kAlign));
+    CUtensorMap tm;
+    st = encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, x, L.k, m, ldx, 128, 128);
+    if (st != HQ_OK) return st;
+    g_last_plan = hq_plan_info{pl.bn, pl.splits, pl.grid, 1, pl.stages, {0, 0, 0}};
+    if (env_int("HQ_TRACE", 0))
+      std::fprintf(stderr, "hq_gemm fp8: m=%d n=%d k=%d bn=%d splits=%d grid=%d stages=%d smem=%u\n", m, L.n, L.k,
+                   pl.bn, pl.splits, pl.grid, pl.stages, pl.smem);
+    return launch_fp8(p, tm, pl.bn, pl.grid, pl.smem, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+  }
+
+  const DensePlan pl = plan_wna16(L, m, di.sms, di.smem_optin, flags);
+  GemmParams p{};
+  p.tiles = wt + L.tiles_off;
+  p.expert_stride = L.expert_stride;
+  p.tile_bytes = L.tile_bytes; p.hi_off = L.hi_off; p.scale_off = L.scale_off; p.zero_off = L.zero_off;
+  p.g_kb = L.g_kb; p.group_k = L.group_k; p.has_zeros = L.has_zeros; p.channel = L.channel;
+  p.zero_sym = (L.has_zeros || !L.signed_codes) ? 0 : (L.wtype == HQ_W_INT4 ? 8 : 32);
+  p.row_scale = L.channel ? reinterpret_cast<const float*>(wt + L.row_off) : nullptr;
+  p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
+  p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = m;
+  p.bn = pl.bn; p.m_tiles = pl.m_tiles; p.splits = pl.splits; p.kb_per_split = pl.kb_per_split;
+  p.stages = pl.stages; p.a_stages = kWna16AStages;
+  p.idesc = idesc_f16(atype == HQ_A_BF16, 128, pl.bn);
+  p.y = y; p.ldy = ldy;
+  p.status = reinterpret_cast<int*>(ws);
+  size_t off = kAlign;
+  p.counters = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * static_cast<size_t>(pl.m_tiles) * L.n_tiles * kWna16DqWarps, kAlign);
+  p.partials = reinterpret_cast<float*>(ws + off);
+  p.num_experts = 1;
+  CUtensorMap tm;
+  st = encode_2d(&tm, atype == HQ_A_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x,
+                 L.k, m, ldx, 64, pl.bn);
+  if (st != HQ_OK) return st;
+  Wna16Launch l{};
+  l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
+  l.bf16 = atype == HQ_A_BF16;
+  l.bn_max = pl.bn_max;
+  l.moe = false;
+  l.grid = pl.grid;
+  l.smem = pl.smem;
+  g_last_plan = hq_plan_info{pl.bn, pl.splits, pl.grid, 1, pl.stages, {0, 0, 0}};
+  if (env_int("HQ_TRACE", 0))
+    std::fprintf(stderr, "hq_gemm: m=%d n=%d k=%d bn=%d splits=%d grid=%d stages=%d smem=%u\n", m, L.n, L.k, pl.bn,
+                 pl.splits, pl.grid, pl.stages, pl.smem);
+  return launch_wna16(l, p, tm, nullptr, 0, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ MoE
+hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int32_t topk, int32_t atype,
+                                size_t* bytes) {
+  if (!desc || !bytes || tokens < 0 || topk <= 0) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*desc, &L);
+  if (st != HQ_OK) return st;
+  const size_t pairs = static_cast<size_t>(tokens) * topk;
+  size_t ws = kAlign;
+  ws += 2 * align_up(sizeof(int) * (L.num_experts + 1), kAlign);
+  ws += align_up(sizeof(int) * std::max<size_t>(pairs, 1), kAlign);
+  ws += align_up(sizeof(float) * pairs * L.n_pad, kAlign);
+  *bytes = ws;
+  return HQ_OK;
+}
+
+hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t tokens, int32_t topk,
+                      const int32_t* topk_ids, const float* topk_w, int32_t atype, const void* x, int64_t ldx,
+                      void* y, int64_t ldy, int32_t* expert_offsets_out, int32_t* perm_out, void* workspace,
+                      size_t ws_bytes, uint32_t flags, hq_stream_t stream) {
+  (void)flags;
+  if (!wdesc || tokens < 0 || topk <= 0) return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*wdesc, &L);
+  if (st != HQ_OK) return st;
+  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (L.num_experts > 1024) return HQ_ERR_UNSUPPORTED;
+  if (tokens == 0) return HQ_OK;
+  if (!w_t || !topk_ids || !topk_w || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;
+  if (ldx < L.k || ldy < L.n) return HQ_ERR_INVALID_ARG;
+  if (atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  if (L.wtype == HQ_W_FP8_E4M3) return HQ_ERR_UNSUPPORTED;
+  if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.stype != HQ_S_BF16) return HQ_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(w_t) & 255u))
+    return HQ_ERR_ALIGNMENT;
+  if ((ldx * 2) % 16 != 0 || (ldy * 2) % 16 != 0 || L.k % 8 != 0) return HQ_ERR_ALIGNMENT;
+  const int64_t pairs = static_cast<int64_t>(tokens) * topk;
+  if (pairs > (1 << 24)) return HQ_ERR_UNSUPPORTED;
+  size_t need = 0;
+  hq_moe_workspace_size(wdesc, tokens, topk, atype, &need);
+  if (ws_bytes < need) return HQ_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  st = device_info(&di);
+  if (st != HQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* wt = static_cast<const uint8_t*>(w_t);
+  size_t off = kAlign;
+  int* exp_off = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * (L.num_experts + 1), kAlign);
+  int* tile_off = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * (L.num_experts + 1), kAlign);
+  int* perm = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * std::max<int64_t>(pairs, 1), kAlign);
+  float* zbuf = reinterpret_cast<float*>(ws + off);
+
+  // tokens per expert tile: from the mean rows per expert
+  const double mean_rows = static_cast<double>(pairs) / L.num_experts;
+  int bn = mean_rows <= 16 ? 16 : (mean_rows <= 32 ? 32 : (mean_rows <= 64 ? 64 : 128));
+  const int forced_bn = env_int("HQ_FORCE_BN", 0);
+  if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) bn = forced_bn;
+  const int bn_max = bn <= 64 ? 64 : 256;
+
+  if (launch_moe_route(topk_ids, static_cast<int>(pairs), L.num_experts, bn, exp_off, tile_off, perm,
+                       expert_offsets_out, perm_out, reinterpret_cast<int*>(ws), s) != cudaSuccess)
+    return HQ_ERR_CUDA;
+
+  GemmParams p{};
+  p.tiles = wt + L.tiles_off;
+  p.expert_stride = L.expert_stride;
+  p.tile_bytes = L.tile_bytes; p.hi_off = L.hi_off; p.scale_off = L.scale_off; p.zero_off = L.zero_off;
+  p.g_kb = L.g_kb; p.group_k = L.group_k; p.has_zeros = L.has_zeros; p.channel = L.channel;
+  p.zero_sym = (L.has_zeros || !L.signed_codes) ? 0 : (L.wtype == HQ_W_INT4 ? 8 : 32);
+  p.row_scale = L.channel ? reinterpret_cast<const float*>(wt + L.row_off) : nullptr;
+  p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
+  p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = tokens;
+  p.bn = bn; p.m_tiles = 0; p.splits = 1; p.kb_per_split = L.k_tiles;
+  p.a_stages = kWna16AStages;
+  p.idesc = idesc_f16(true, 128, bn);
+  p.status = reinterpret_cast<int*>(ws);
+  p.num_experts = L.num_experts; p.topk = topk;
+  p.tile_offsets = tile_off; p.expert_offsets = exp_off; p.perm = perm; p.topk_w = topk_w; p.zbuf = zbuf;
+  const int min_blocks = wna16_min_blocks(bn_max);
+  const size_t budget = std::min<size_t>(di.smem_optin, 232448 / min_blocks) - 2048 - 8 * (L.num_experts + 1);
+  const uint32_t per_stage = ((L.tile_bytes + 127u) & ~127u) + static_cast<uint32_t>(bn) * 256u;
+  p.stages = std::max(2, static_cast<int>(std::min<size_t>(8, budget / per_stage)));
+  Wna16Launch l{};
+  l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
+  l.bf16 = true;
+  l.bn_max = bn_max;
+  l.moe = true;
+  l.grid = di.sms * min_blocks;
+  l.smem = wna16_smem_bytes(p.stages, L.tile_bytes, bn, L.num_experts);
+  CUtensorMap tm;
+  std::memset(&tm, 0, sizeof(tm));
+  if (launch_wna16(l, p, tm, x, ldx, s) != cudaSuccess) return HQ_ERR_CUDA;
+  if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L.num_experts, L.n, L.n_pad, y, ldy, true, s) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  g_last_plan = hq_plan_info{bn, 1, l.grid, 3, p.stages, {0, 0, 0}};
+  return HQ_OK;
+}
+
+}  // extern "C"

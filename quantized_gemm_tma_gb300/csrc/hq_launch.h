@@ -1,0 +1,44 @@
+// hq_launch.h — kernel launchers implemented in the .cu files, called by the
+// host API (hq_api.cpp).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "hq_internal.h"
+
+namespace hq {
+
+// transform.cu
+cudaError_t launch_repack(const Layout& L, const hq_weight_desc& d, void* dst, cudaStream_t stream);
+cudaError_t launch_unpack(const Layout& L, const void* src, void* codes, void* scales, void* zeros,
+                          cudaStream_t stream);
+
+// wna16_*.cu: fmt = WFmt, bn_max in {64, 256}
+struct Wna16Launch {
+  int fmt;
+  bool bf16;
+  int bn_max;
+  bool moe;
+  int grid;
+  uint32_t smem;
+  int min_blocks;  // CTAs per SM the kernel was compiled for
+};
+cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows,
+                         int64_t ldx, cudaStream_t stream);
+uint32_t wna16_smem_bytes(int stages, uint32_t tile_bytes, int bn, int num_experts);
+int wna16_min_blocks(int bn_max);
+
+// gemm_fp8.cu
+cudaError_t launch_fp8(const Fp8Params& p, const CUtensorMap& tmap, int bn_max, int grid, uint32_t smem,
+                       cudaStream_t stream);
+uint32_t fp8_smem_bytes(int stages, int bn);
+
+// moe.cu
+cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, int bn, int* expert_offsets,
+                             int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* status,
+                             cudaStream_t stream);
+cudaError_t launch_moe_combine(const float* zbuf, const int* topk_ids, int tokens, int topk, int num_experts, int n,
+                               int n_pad, void* y, int64_t ldy, bool bf16, cudaStream_t stream);
+
+}  // namespace hq

@@ -1,0 +1,179 @@
+// moe.cu — MoE routing and combine around the grouped GEMM (Humming aiwiki
+// article, "Device and workload selection": indexed input gathered through
+// routing indices; grouped-contiguous execution places each expert's rows
+// together).
+//
+// route:   a stable counting sort of the T*topk (token, slot) pairs by expert
+//          in one CTA: per-warp histograms over contiguous segments, an
+//          exclusive prefix over experts and warps, then an in-order scatter
+//          (ranks inside a 32-pair step from __match_any_sync).  Also emits
+//          the prefix of m-tiles per expert for the grouped GEMM scheduler.
+// combine: Y[t, :] = sum_j Z[t*topk + j, :] in slot order (Z already carries
+//          the routing weight), rounded once to bf16.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "hq_internal.h"
+#include "hq_launch.h"
+
+namespace hq {
+namespace {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+// Block-wide exclusive scan of one value per thread (threads >= count hold 0).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += t;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+    int winc = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, winc, d);
+      if (lane >= d) winc += t;
+    }
+    warp_tot[lane] = winc - w;           // exclusive prefix of warp totals
+    if (lane == 31) warp_tot[32] = winc;  // grand total
+  }
+  __syncthreads();
+  total = warp_tot[32];
+  const int r = warp_tot[warp] + inc - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    moe_route_kernel(const int* __restrict__ ids, int pairs, int num_experts, int bn, int* __restrict__ exp_off,
+                     int* __restrict__ tile_off, int* __restrict__ perm, int* __restrict__ off_out,
+                     int* __restrict__ perm_out, int* __restrict__ status) {
+  extern __shared__ int sm[];
+  int* wcnt = sm;                                  // [warps][E]: per-warp counts, then write cursors
+  int* warp_tot = sm + kRouteWarps * num_experts;  // [33]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = num_experts;
+  const int seg = (pairs + kRouteWarps - 1) / kRouteWarps;
+  const int f0 = warp * seg, f1 = min(pairs, f0 + seg);
+
+  for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) wcnt[i] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int f = f0 + lane; f < f1; f += 32) {
+    const int e = ids[f];
+    if (e >= 0 && e < E) atomicAdd(&wcnt[warp * E + e], 1);
+    else bad = true;
+  }
+  if (bad) atomicCAS(status, 0, static_cast<int>(HQ_ERR_INVALID_VALUE));
+  __syncthreads();
+
+  // per-expert totals and exclusive prefix over experts (rows and m-tiles)
+  int cnt = 0;
+  if (tid < E)
+    for (int w = 0; w < kRouteWarps; ++w) cnt += wcnt[w * E + tid];
+  int rows_total = 0, tiles_total = 0;
+  const int row_base = block_exclusive_scan(tid < E ? cnt : 0, warp_tot, rows_total);
+  const int tile_base = block_exclusive_scan(tid < E ? (cnt + bn - 1) / bn : 0, warp_tot, tiles_total);
+  if (tid < E) {
+    exp_off[tid] = row_base;
+    tile_off[tid] = tile_base;
+    if (off_out) off_out[tid] = row_base;
+    // write cursor of each warp for this expert: row_base + counts of earlier warps
+    int run = row_base;
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int c = wcnt[w * E + tid];
+      wcnt[w * E + tid] = run;
+      run += c;
+    }
+  }
+  if (tid == 0) {
+    exp_off[E] = rows_total;
+    tile_off[E] = tiles_total;
+    if (off_out) off_out[E] = rows_total;
+  }
+  __syncthreads();
+
+  // stable scatter: each warp walks its segment in order, 32 pairs per step
+  int* cur = wcnt + warp * E;
+  for (int b = f0; b < f1; b += 32) {
+    const int f = b + lane;
+    int e = (f < f1) ? ids[f] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int pos = 0;
+    if (e >= 0) pos = cur[e] + rank;
+    __syncwarp();
+    if (e >= 0) {
+      perm[pos] = f;
+      if (perm_out) perm_out[pos] = f;
+      if (rank == 0) cur[e] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+// One thread per (token, 8 consecutive outputs).
+__global__ void moe_combine_kernel(const float* __restrict__ z, const int* __restrict__ ids, int tokens, int topk,
+                                   int num_experts, int n, int n_pad, __nv_bfloat16* __restrict__ y, int64_t ldy) {
+  const int groups = (n + 7) / 8;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(tokens) * groups) return;
+  const int t = static_cast<int>(idx / groups);
+  const int n0 = static_cast<int>(idx % groups) * 8;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int j = 0; j < topk; ++j) {
+    const int f = t * topk + j;
+    const int e = ids[f];
+    if (e < 0 || e >= num_experts) continue;
+    const float4* src = reinterpret_cast<const float4*>(z + static_cast<size_t>(f) * n_pad + n0);
+    const float4 a = __ldcs(src), b = __ldcs(src + 1);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  }
+  __nv_bfloat16* yr = y + static_cast<size_t>(t) * ldy + n0;
+  if (n0 + 8 <= n) {
+    uint4 o;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    *reinterpret_cast<uint4*>(yr) = o;
+  } else {
+    for (int i = 0; i < 8 && n0 + i < n; ++i) yr[i] = __float2bfloat16_rn(acc[i]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, int bn, int* expert_offsets,
+                             int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* status,
+                             cudaStream_t stream) {
+  const size_t smem = sizeof(int) * (static_cast<size_t>(kRouteWarps) * num_experts + 33);
+  cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  moe_route_kernel<<<1, kRouteThreads, smem, stream>>>(topk_ids, pairs, num_experts, bn, expert_offsets,
+                                                        tile_offsets, perm, offsets_out, perm_out, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_combine(const float* zbuf, const int* topk_ids, int tokens, int topk, int num_experts, int n,
+                               int n_pad, void* y, int64_t ldy, bool bf16, cudaStream_t stream) {
+  (void)bf16;
+  const int64_t threads = static_cast<int64_t>(tokens) * ((n + 7) / 8);
+  const int block = 256;
+  moe_combine_kernel<<<static_cast<unsigned>((threads + block - 1) / block), block, 0, stream>>>(
+      zbuf, topk_ids, tokens, topk, num_experts, n, n_pad, static_cast<__nv_bfloat16*>(y), ldy);
+  return cudaGetLastError();
+}
+
+}  // namespace hq

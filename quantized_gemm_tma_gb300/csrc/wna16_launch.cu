@@ -1,0 +1,30 @@
+// wna16_launch.cu — format dispatch of the WnA16 kernel launches.
+#include "gemm_wna16.cuh"
+#include "hq_launch.h"
+
+namespace hq {
+
+cudaError_t launch_wna16_int4(const Wna16Launch&, const GemmParams&, const CUtensorMap&, const void*, int64_t,
+                              cudaStream_t);
+cudaError_t launch_wna16_int6(const Wna16Launch&, const GemmParams&, const CUtensorMap&, const void*, int64_t,
+                              cudaStream_t);
+cudaError_t launch_wna16_mxfp4(const Wna16Launch&, const GemmParams&, const CUtensorMap&, const void*, int64_t,
+                               cudaStream_t);
+
+cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows,
+                         int64_t ldx, cudaStream_t stream) {
+  switch (l.fmt) {
+    case 0: return launch_wna16_int4(l, p, tmap, x_rows, ldx, stream);
+    case 1: return launch_wna16_int6(l, p, tmap, x_rows, ldx, stream);
+    case 2: return launch_wna16_mxfp4(l, p, tmap, x_rows, ldx, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+uint32_t wna16_smem_bytes(int stages, uint32_t tile_bytes, int bn, int num_experts) {
+  return wna16::smem_bytes(stages, tile_bytes, bn, num_experts);
+}
+
+int wna16_min_blocks(int bn_max) { return bn_max <= 64 ? 2 : 1; }
+
+}  // namespace hq

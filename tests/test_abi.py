@@ -1,0 +1,119 @@
+"""The C-ABI library loads, exports every symbol include/hq.h declares, and
+rejects bad arguments on the host before touching a GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "hq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hq_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def hq():
+    import quantized_gemm_tma_gb300 as m
+    from quantized_gemm_tma_gb300 import _build
+    _build.build()
+    return m
+
+
+def test_exports_every_declared_symbol(hq):
+    declared = _header_functions()
+    assert declared, "no functions parsed from hq.h"
+    assert sorted(hq.EXPORTS) == declared
+    lib = ctypes.CDLL(hq.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_strings(hq):
+    assert hq.hq_version() >= 100
+    for s in range(9):
+        assert hq.status_string(s) and hq.status_string(s) != "unknown status"
+
+
+def _desc(hq, **kw):
+    base = dict(wtype="int4", stype="bf16", n=256, k=512, group_k=128)
+    base.update(kw)
+    return hq.make_desc(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=0), 1), (dict(k=-5), 1), (dict(group_k=48), 1), (dict(group_k=96), 1), (dict(k=500), 1),
+    (dict(wtype="int6", k=130, group_k=0), 1), (dict(stype="fp32"), 1), (dict(wtype="mxfp4", stype="bf16"), 1),
+    (dict(wtype="mxfp4", stype="ue8m0", group_k=64), 1), (dict(wtype="fp8", stype="fp32", group_k=128, group_n=1), 1),
+    (dict(wtype=7), 1), (dict(num_experts=0), 1),
+])
+def test_transform_size_validation(hq, kw, status):
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_transform_size(_desc(hq, **kw))
+    assert ei.value.status == status
+
+
+def test_transform_size_layouts(hq):
+    # one 128x128 INT4 tile with bf16 g128 scales = 8192 + 256 bytes (+256 header)
+    assert hq.hq_transform_size(_desc(hq, n=128, k=128)) == 256 + 8192 + 256
+    s = hq.hq_transform_size(_desc(hq, n=8192, k=8192, has_zeros=True, signed_codes=False))
+    assert s == 256 + 64 * 64 * (8192 + 256 + 128)
+    # fp8: 16 KiB images + block scales
+    d = hq.make_desc("fp8", "fp32", 4096, 7168, group_k=128, group_n=128)
+    assert hq.hq_transform_size(d) >= 256 + 32 * 56 * 16384 + 4 * 32 * 56
+
+
+def test_gemm_host_validation(hq):
+    d = _desc(hq)
+    ws = 1 << 20
+    fake = 0x10000  # never dereferenced: every case below fails validation first
+    cases = [
+        (dict(m=-1), hq.HQ_ERR_INVALID_ARG),
+        (dict(atype=9), hq.HQ_ERR_INVALID_ARG),
+        (dict(x=None), hq.HQ_ERR_INVALID_ARG),
+        (dict(ldx=100), hq.HQ_ERR_INVALID_ARG),
+        (dict(atype="fp16"), hq.HQ_ERR_UNSUPPORTED),        # bf16 group scales need bf16 activations
+        (dict(atype="fp8"), hq.HQ_ERR_UNSUPPORTED),
+        (dict(x=fake + 8), hq.HQ_ERR_ALIGNMENT),
+        (dict(ldx=516), hq.HQ_ERR_ALIGNMENT),
+        (dict(ws_bytes=16), hq.HQ_ERR_WORKSPACE_TOO_SMALL),
+    ]
+    for over, want in cases:
+        args = dict(desc=d, w_t=fake, m=16, atype="bf16", x=fake, ldx=512, x_scales=None, y=fake, ldy=256,
+                    workspace=fake, ws_bytes=ws, flags=0, stream=None)
+        args.update(over)
+        with pytest.raises(hq.HQError) as ei:
+            hq.hq_gemm(args["desc"], args["w_t"], args["m"], args["atype"], args["x"], args["ldx"],
+                       args["x_scales"], args["y"], args["ldy"], args["workspace"], args["ws_bytes"],
+                       args["flags"], args["stream"])
+        assert ei.value.status == want, (over, ei.value.status)
+
+
+def test_gemm_m_zero_returns_ok_without_gpu(hq):
+    hq.hq_gemm(_desc(hq), 0, 0, "bf16", 0, 512, None, 0, 256, 0, 0, 0, None)
+
+
+def test_moe_host_validation(hq):
+    d = hq.make_desc("mxfp4", "ue8m0", 1536, 2048, num_experts=128, group_k=32)
+    fake = 0x10000
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_moe_gemm(d, fake, 16, 0, fake, fake, "bf16", fake, 2048, fake, 1536, None, None, fake, 1 << 30)
+    assert ei.value.status == hq.HQ_ERR_INVALID_ARG
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_moe_gemm(d, fake, 16, 8, fake, fake, "fp16", fake, 2048, fake, 1536, None, None, fake, 1 << 30)
+    assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
+    need = hq.hq_moe_workspace_size(d, 4096, 8, "bf16")
+    assert need >= 4096 * 8 * 1536 * 4
+
+
+def test_workspace_sizes_bounded(hq):
+    d = _desc(hq, n=8192, k=8192, has_zeros=True, signed_codes=False)
+    small = hq.hq_gemm_workspace_size(d, 16, "bf16")
+    big = hq.hq_gemm_workspace_size(d, 4096, "bf16")
+    assert small >= 256
+    # large M needs no split-K scratch; small M needs at most 64 splits of fp32 partials
+    assert big < 64 << 20
+    assert small <= 256 + 64 * 16 * 8192 * 4 + (1 << 20)

@@ -1,0 +1,140 @@
+"""Dense quantized GEMM: CUDA path vs the CPU oracle, element by element (GPU).
+
+Small cases span several 128x128 tiles with ragged M, N and K tails and run
+with and without split-K; the full-size cases are the benchmark shapes, in the
+launch configuration the benchmark times, checked on sampled rows.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tolerance import check
+
+pytestmark = pytest.mark.gpu
+
+
+def _ref(qw, acts, rows=None):
+    w = oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes, qw.scales, qw.zeros, qw.group_k, qw.signed, qw.stype,
+                          qw.num_experts)
+    a = oracle.decode_activations(acts.atype, acts.data, acts.scales)
+    if rows is not None:
+        a = a[rows]
+    return oracle.gemm_dense(a, w)
+
+
+def _gpu(qw, acts, **kw):
+    from gpu_helpers import DevWeight, run_gemm
+    return run_gemm(DevWeight(qw), acts, **kw)
+
+
+# ------------------------------------------------------------------ small, element-wise
+SMALL = [
+    # name, generator, m, n, k
+    ("w4a16_sym_g128", synth.dense_w4a16_sym, 16, 384, 1024),
+    ("w4a16_sym_g128_m1", synth.dense_w4a16_sym, 1, 256, 512),
+    ("w4a16_sym_g128_ragged", synth.dense_w4a16_sym, 37, 448, 640),
+    ("w4a16_asym_g128", synth.dense_w4a16_asym, 16, 512, 1024),
+    ("w4a16_asym_g128_m100", synth.dense_w4a16_asym, 100, 384, 768),
+    ("w4a16_asym_g128_m300", synth.dense_w4a16_asym, 300, 256, 512),
+    ("int6_channel_fp16", synth.dense_int6_channel, 128, 384, 1024),
+    ("int6_channel_fp16_ragged", synth.dense_int6_channel, 45, 200, 520),
+    ("fp8_block", synth.dense_fp8_block, 64, 512, 1024),
+    ("fp8_block_ragged", synth.dense_fp8_block, 130, 300, 700),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL)), ids=lambda i: SMALL[i][0])
+@pytest.mark.parametrize("flags", [0, 1], ids=["splitk", "batch_invariant"])
+def test_small_parity(idx, flags):
+    name, gen, m, n, k = SMALL[idx]
+    qw, acts = gen(idx, m, n, k)
+    check(_gpu(qw, acts, flags=flags), _ref(qw, acts), name)
+
+
+GROUPS = [
+    # wtype, group_k, zeros, stype/atype, m, n, k
+    ("int4", 32, True, "bf16", 20, 256, 384),
+    ("int4", 64, False, "fp16", 33, 256, 448),
+    ("int4", 256, True, "bf16", 17, 128, 1024),
+    ("int4", 0, True, "bf16", 9, 200, 300),
+    ("int4", 0, False, "fp16", 64, 256, 512),
+    ("int6", 128, True, "bf16", 50, 256, 512),
+    ("int6", 32, False, "fp16", 16, 128, 256),
+    ("int6", 0, True, "bf16", 24, 160, 256),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(GROUPS)), ids=lambda i: "-".join(map(str, GROUPS[i])))
+def test_group_variants(idx):
+    wtype, g, zeros, st, m, n, k = GROUPS[idx]
+    rng = np.random.default_rng(50 + idx)
+    w = rng.standard_normal((1, n, k)) * 0.02
+    qw = synth.quantize_int_groupwise(w, 4 if wtype == "int4" else 6, g, not zeros, st)
+    acts = synth.make_activations(rng, m, k, st)
+    check(_gpu(qw, acts), _ref(qw, acts), f"{wtype} g{g} zeros={zeros} {st}")
+
+
+def test_mxfp4_dense():
+    qw, acts, _ = synth.moe_mxfp4(1, 24, num_experts=1, n=384, k=512)
+    check(_gpu(qw, acts), _ref(qw, acts), "mxfp4 dense")
+
+
+def test_mxfp4_extreme_exponents():
+    """Scales at both ends of UE8M0 (subnormal bf16 results, E > 128 two-step path)."""
+    qw = synth.random_codes_weight(8, "mxfp4", 128, 256)
+    qw.scales[:] = np.where(np.arange(8)[None, None, :] % 2 == 0, 0, 140).astype(np.uint8)[:, :, :8]
+    acts = synth.make_activations(np.random.default_rng(8), 16, 256, "bf16")
+    y = _gpu(qw, acts)
+    r = _ref(qw, acts)
+    check(y, r, "mxfp4 extreme exponents")
+
+
+def test_strided_x_and_y():
+    qw, acts = synth.dense_w4a16_asym(7, 24, 256, 512)
+    check(_gpu(qw, acts, ldx=520, ldy=264), _ref(qw, acts), "strided")
+
+
+def test_m_zero_is_noop():
+    import torch
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import DevWeight, workspace
+    qw, acts = synth.dense_w4a16_sym(0, 1, 128, 128)
+    dw = DevWeight(qw)
+    ws = workspace(256)
+    hq.hq_gemm(dw.desc, dw.wt, 0, "bf16", 0, 128, None, 0, 128, ws, 256, 0, None)
+    torch.cuda.synchronize()
+
+
+def test_split_k_deterministic():
+    """Two runs with split-K give identical bits (fixed-order reduction)."""
+    qw, acts = synth.dense_w4a16_asym(3, 16, 512, 4096)
+    a = _gpu(qw, acts)
+    b = _gpu(qw, acts)
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ full size, sampled rows
+FULL = [
+    ("c1_w4a16_sym_16x1024x1024", synth.dense_w4a16_sym, 16, 1024, 1024),
+    ("c2_w4a16_asym_m1", synth.dense_w4a16_asym, 1, 8192, 8192),
+    ("c2_w4a16_asym_m16", synth.dense_w4a16_asym, 16, 8192, 8192),
+    ("c2_w4a16_asym_m128", synth.dense_w4a16_asym, 128, 8192, 8192),
+    ("c2_w4a16_asym_m1024", synth.dense_w4a16_asym, 1024, 8192, 8192),
+    ("c2_w4a16_asym_m4096", synth.dense_w4a16_asym, 4096, 8192, 8192),
+    ("c3_int6_channel_128x8192x8192", synth.dense_int6_channel, 128, 8192, 8192),
+    ("c4_fp8_block_m64", synth.dense_fp8_block, 64, 4096, 7168),
+    ("c4_fp8_block_m512", synth.dense_fp8_block, 512, 4096, 7168),
+    ("c4_fp8_block_m4096", synth.dense_fp8_block, 4096, 4096, 7168),
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("idx", range(len(FULL)), ids=lambda i: FULL[i][0])
+def test_full_size_sampled(idx):
+    name, gen, m, n, k = FULL[idx]
+    qw, acts = gen(0, m, n, k)
+    y = _gpu(qw, acts)
+    rng = np.random.default_rng(idx)
+    rows = np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, size=min(m, 24))]))
+    check(y[rows], _ref(qw, acts, rows), name)
