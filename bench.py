@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized GEMM hot path on one GB300 (or N replicas).
+
+One step = one pass over the dense W4A16 workload the metric is quoted on:
+asymmetric INT4 weights (uint4 zero points, group 128, bf16 scales), bf16
+activations, N = K = 8192, for every M of the sweep {1, 16, 128, 1024, 4096}
+(one hq_gemm call per M).  The MoE grouped GEMM (MXFP4 experts, E = 128,
+N = 1536, K = 2048, top-8 routing, T in {16, 256, 4096}) is timed the same
+way and reported under "moe".
+
+Timing: W untimed warm-up steps, then K timed steps.  Every GEMM call is
+bracketed by CUDA events on the stream it is launched on; L2 is flushed (a
+256 MiB write) before each call, outside the events.  `value` is the
+whole-job aggregate TFLOP/s: all FLOPs of the timed steps on all ranks over
+the slowest rank's summed GEMM time.  `e2e` is the same metric through the
+public C-ABI call with the step's activations copied in from pinned host
+memory and the outputs copied back, inside the timed region.
+
+`--impl reference` times the CPU oracle (the parity reference; this subject
+has no runnable reference implementation) on a bounded sample of the same
+workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Quantized GEMM TFLOP/s & HBM GB/s vs M (W4A16, MoE); % of roofline"
+N = K = 8192
+M_SWEEP = [1, 16, 128, 1024, 4096]
+MOE_T = [16, 256, 4096]
+MOE_E, MOE_N, MOE_K, MOE_TOPK = 128, 1536, 2048, 8
+WORKLOAD = ("dense W4A16: asymmetric INT4 g128 (uint4 zeros, bf16 scales), bf16 activations, "
+            "N=K=8192, M sweep {1,16,128,1024,4096}")
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def dense_bytes(m: int) -> int:
+    """Algorithmic bytes of one W4A16 call: packed weights + scales + zeros + activations."""
+    return N * K // 2 + N * (K // 128) * 2 + N * (K // 128) // 2 + m * K * 2
+
+
+def dense_flops(m: int) -> int:
+    return 2 * m * N * K
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(key)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if isinstance(v, (int, float)) and v > 0:
+                    out[key] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                out["source"] = "measured"
+                return out
+        except (OSError, ValueError):
+            pass
+    out = dict(FALLBACK)
+    out["source"] = "fallback"
+    return out
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- oracle (CPU)
+def cpu_oracle_sample(seed: int = 0, rows_cap: int = 256):
+    """Time the CPU oracle on a bounded sample of the same workload.
+
+    One dequantisation of the N=K=8192 weight plus float64 matmuls for every M
+    of the sweep, capped at `rows_cap` rows per M.  Returns (TFLOP/s, seconds,
+    description, cores).
+    """
+    import numpy as np
+    import oracle
+    import synth
+    qw, _ = synth.dense_w4a16_asym(seed, 1, N, K)
+    rng = np.random.default_rng(seed + 1)
+    t0 = time.perf_counter()
+    w = oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes, qw.scales, qw.zeros, qw.group_k, qw.signed, qw.stype, 1)
+    flops = 0
+    for m in M_SWEEP:
+        rows = min(m, rows_cap)
+        a = oracle.decode_activations("bf16", synth.to_bf16_bits(rng.standard_normal((rows, K))))
+        oracle.gemm_dense(a, w)
+        flops += dense_flops(rows)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    desc = (f"oracle (numpy, float64) on the N=K=8192 asym INT4 weight: one dequantisation plus matmuls for "
+            f"M in {M_SWEEP} capped at {rows_cap} rows each ({flops / 1e9:.1f} GFLOP)")
+    return flops / dt / 1e12, dt, desc, cores
+
+
+# ---------------------------------------------------------------------------- GPU arm
+def run_gpu(args, rank: int, world: int):
+    import numpy as np
+    import torch
+    import quantized_gemm_tma_gb300 as hq
+    import synth
+    from quantized_gemm_tma_gb300 import _build
+
+    if not os.path.exists(hq.LIB_PATH):
+        _build.build()
+    dev = torch.device("cuda", rank % torch.cuda.device_count())
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.to(dev)
+
+    # ---- dense workload (seeded), transformed once
+    qw, _ = synth.dense_w4a16_asym(0, 1, N, K)
+    codes, scales, zeros = to_dev(qw.codes), to_dev(qw.scales), to_dev(qw.zeros)
+    desc = hq.make_desc("int4", "bf16", N, K, 1, 128, 1, False, True, codes, scales, zeros)
+    wt_bytes = hq.hq_transform_size(desc)
+    wt = torch.empty(wt_bytes, dtype=torch.uint8, device=dev)
+    hq.hq_transform(desc, wt, wt_bytes, sh)
+    rng = np.random.default_rng(1)
+    xs, ys, wss, xh, yh = {}, {}, {}, {}, {}
+    for m in M_SWEEP:
+        xb = synth.to_bf16_bits(rng.standard_normal((m, K)))
+        xs[m] = to_dev(xb)
+        ys[m] = torch.empty((m, N), dtype=torch.bfloat16, device=dev)
+        need = hq.hq_gemm_workspace_size(desc, m, "bf16")
+        wss[m] = torch.zeros(need, dtype=torch.uint8, device=dev)
+        xh[m] = torch.from_numpy(xb.view(np.int16)).pin_memory()
+        yh[m] = torch.empty((m, N), dtype=torch.bfloat16).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches = {"n": 0}
+
+    def gemm(m):
+        hq.hq_gemm(desc, wt, m, "bf16", xs[m], K, None, ys[m], N, wss[m], wss[m].numel(), 0, sh)
+        launches["n"] += hq.hq_last_plan()["launches"]
+
+    # ---- MoE workload
+    moe = None
+    if not args.no_moe:
+        mq, _, _ = synth.moe_mxfp4(0, 1)
+        mdesc = hq.make_desc("mxfp4", "ue8m0", MOE_N, MOE_K, MOE_E, 32, 1, True, False,
+                             to_dev(mq.codes), to_dev(mq.scales), None)
+        mbytes = hq.hq_transform_size(mdesc)
+        mwt = torch.empty(mbytes, dtype=torch.uint8, device=dev)
+        hq.hq_transform(mdesc, mwt, mbytes, sh)
+        moe = {"desc": mdesc, "wt": mwt, "T": {}}
+        for t in MOE_T:
+            r = synth.make_routing(np.random.default_rng(10 + t), t, MOE_E, MOE_TOPK)
+            x = synth.to_bf16_bits(np.random.default_rng(20 + t).standard_normal((t, MOE_K)))
+            need = hq.hq_moe_workspace_size(mdesc, t, MOE_TOPK, "bf16")
+            touched = np.unique(r.topk_ids).size
+            moe["T"][t] = {"ids": to_dev(r.topk_ids.astype(np.int32)), "w": to_dev(r.topk_w.astype(np.float32)),
+                           "x": to_dev(x), "y": torch.empty((t, MOE_N), dtype=torch.bfloat16, device=dev),
+                           "ws": torch.zeros(need, dtype=torch.uint8, device=dev), "touched": int(touched)}
+        del mq
+
+    def moe_call(t):
+        d = moe["T"][t]
+        hq.hq_moe_gemm(moe["desc"], moe["wt"], t, MOE_TOPK, d["ids"], d["w"], "bf16", d["x"], MOE_K, d["y"], MOE_N,
+                       None, None, d["ws"], d["ws"].numel(), 0, sh)
+        launches["n"] += hq.hq_last_plan()["launches"]
+
+    def timed(fn, arg):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn(arg)
+        e1.record(stream)
+        return e0, e1
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        for m in M_SWEEP:
+            timed(gemm, m)
+        if moe:
+            for t in MOE_T:
+                timed(moe_call, t)
+    torch.cuda.synchronize()
+    st = hq.hq_status_read(wss[M_SWEEP[0]], 0, sh)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {hq.status_string(st)}")
+
+    # ---- timed steps
+    launches["n"] = 0
+    per_m = {m: [] for m in M_SWEEP}
+    per_t = {t: [] for t in MOE_T}
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        wall0 = time.perf_counter()
+        events = []
+        for _ in range(args.steps):
+            for m in M_SWEEP:
+                events.append(("d", m, *timed(gemm, m)))
+            if moe:
+                for t in MOE_T:
+                    events.append(("m", t, *timed(moe_call, t)))
+        barrier()
+        wall = time.perf_counter() - wall0
+    for kind, key, e0, e1 in events:
+        (per_m if kind == "d" else per_t)[key].append(e0.elapsed_time(e1) * 1e-3)
+    gpu_launches = launches["n"]
+
+    # ---- end to end through the C ABI with host buffers (pinned), same steps
+    e2e_times = []
+    for step in range(args.warmup + args.steps):
+        tot = 0.0
+        for m in M_SWEEP:
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            xs[m].copy_(xh[m].view(torch.int16), non_blocking=True)
+            gemm(m)
+            yh[m].copy_(ys[m], non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1) * 1e-3
+        if step >= args.warmup:
+            e2e_times.append(tot)
+    st = hq.hq_status_read(wss[M_SWEEP[0]], 0, sh)
+    if st != 0:
+        raise RuntimeError(f"device status: {hq.status_string(st)}")
+
+    res = {
+        "per_m": {m: statistics.mean(v) for m, v in per_m.items()},
+        "per_m_min": {m: min(v) for m, v in per_m.items()},
+        "step_s": sum(statistics.mean(v) for v in per_m.values()),
+        "e2e_step_s": statistics.mean(e2e_times),
+        "clocks": clk.summary(),
+        "wall_s": wall,
+        "gpu_launches": gpu_launches,
+        "plans": {},
+    }
+    for m in M_SWEEP:
+        gemm(m)
+        res["plans"][m] = hq.hq_last_plan()
+    if moe:
+        res["moe"] = {t: statistics.mean(v) for t, v in per_t.items()}
+        res["moe_touched"] = {t: moe["T"][t]["touched"] for t in MOE_T}
+    torch.cuda.synchronize()
+    return res
+
+
+def reduce_max(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-moe", action="store_true", help="skip the MoE sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # the CPU oracle, as it stands, on a bounded sample per step
+        times, flops_tot = [], 0.0
+        desc, cores = "", len(os.sched_getaffinity(0))
+        for i in range(args.warmup + args.steps):
+            v, dt, desc, cores = cpu_oracle_sample(seed=0, rows_cap=64)
+            if i >= args.warmup:
+                times.append(dt)
+                flops_tot += v * dt * 1e12
+        tot = sum(times)
+        val = flops_tot / tot / 1e12
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": WORKLOAD, "sample": desc},
+                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    res = run_gpu(args, local, world)
+    step_s = reduce_max(res["step_s"], world)
+    e2e_s = reduce_max(res["e2e_step_s"], world)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    pk = peaks()
+    flops_step = sum(dense_flops(m) for m in M_SWEEP)
+    value = world * flops_step / step_s / 1e12
+    sweep = []
+    for m in M_SWEEP:
+        t = res["per_m"][m]
+        by, fl = dense_bytes(m), dense_flops(m)
+        roof_t = max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
+        sweep.append({"m": m, "us": round(t * 1e6, 2), "us_min": round(res["per_m_min"][m] * 1e6, 2),
+                      "tflops": round(fl / t / 1e12, 2), "gbs": round(by / t / 1e9, 1),
+                      "roofline_frac": round(roof_t / t, 3),
+                      "bound": "hbm" if by / (pk["hbm_gbs"] * 1e9) >= fl / (pk["bf16_tflops"] * 1e12) else "tensor",
+                      "plan": res["plans"][m]})
+    big = M_SWEEP[-1]
+    t_big = res["per_m"][big]
+    ach = dense_flops(big) / t_big / 1e12
+    roofline = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / pk["bf16_tflops"], 4), "traffic": None,
+                "kernel": "wna16_kernel<INT4,bf16,256> (M=4096 launch)", "peak_source": pk["source"]}
+    dec = 16
+    t_dec = res["per_m"][dec]
+    gbs = dense_bytes(dec) / t_dec / 1e9
+    roofline_decode = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                       "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                       "kernel": "wna16_kernel<INT4,bf16,64> (M=16 launch)", "peak_source": pk["source"]}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "flushed (256 MiB write) before every timed call, outside the events",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "timing": "CUDA events around each hq_gemm call on its stream; value = FLOPs / summed mean times"},
+        "sweep": sweep,
+        "roofline": roofline,
+        "roofline_decode": roofline_decode,
+        "e2e": {"value": round(world * flops_step / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(m * K * 2 for m in M_SWEEP),
+                "d2h_bytes_per_step": sum(m * N * 2 for m in M_SWEEP)},
+        "gpu_launches": res["gpu_launches"],
+        "clocks": res["clocks"],
+    }
+    if "moe" in res:
+        msw = []
+        for t in MOE_T:
+            tt = res["moe"][t]
+            fl = 2 * t * MOE_TOPK * MOE_N * MOE_K
+            by = res["moe_touched"][t] * (MOE_N * MOE_K // 2 + MOE_N * MOE_K // 32) + t * MOE_K * 2
+            roof_t = max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
+            msw.append({"tokens": t, "us": round(tt * 1e6, 2), "tflops": round(fl / tt / 1e12, 2),
+                        "gbs": round(by / tt / 1e9, 1), "experts_touched": res["moe_touched"][t],
+                        "roofline_frac": round(roof_t / tt, 3)})
+        line["moe"] = {"workload": "MoE gate+up, MXFP4 (e2m1 + UE8M0/32) experts, E=128, N=1536, K=2048, top-8, "
+                                   "bf16 activations; route + grouped GEMM + combine per call",
+                       "sweep": msw}
+    if not args.no_cpu_baseline and world >= 1:
+        v, dt, desc, cores = cpu_oracle_sample(seed=0, rows_cap=256)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+                                "seconds": round(dt, 2)}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -236,17 +236,18 @@ _E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
 
 def _e2m1_encode(v: np.ndarray) -> np.ndarray:
-    """Round to the nearest e2m1 value (ties to the even code), saturating at 6."""
-    a = np.minimum(np.abs(v), 6.0)
-    d = np.abs(a[..., None] - _E2M1_GRID)
-    best = d.argmin(axis=-1)
-    # ties: argmin picks the lower code; move to the even one where needed
-    dmin = d.min(axis=-1)
-    nxt = np.minimum(best + 1, 7)
-    tie = (np.take_along_axis(d, nxt[..., None], -1)[..., 0] == dmin) & (best % 2 == 1) & (nxt != best)
-    best = np.where(tie, nxt, best)
-    sign = (np.signbit(v) & (best > 0)).astype(np.int64)
-    return (sign << 3) | best
+    """Round to the nearest e2m1 value (ties to the even code), saturating at 6.
+
+    The magnitude code is the number of decision thresholds (midpoints of the
+    grid 0, .5, 1, 1.5, 2, 3, 4, 6) that |v| passes; at a midpoint the
+    comparison is strict or not so that the tie lands on the even code.
+    """
+    a = np.abs(v)
+    code = (a > 0.25).view(np.uint8) + (a >= 0.75).view(np.uint8)
+    for thr, strict in ((1.25, True), (1.75, False), (2.5, True), (3.5, False), (5.0, True)):
+        code += (a > thr).view(np.uint8) if strict else (a >= thr).view(np.uint8)
+    sign = (np.signbit(v) & (code > 0)).view(np.uint8)
+    return (sign << 3) | code
 
 
 def quantize_mxfp4(w: np.ndarray) -> QuantWeight:
@@ -256,15 +257,16 @@ def quantize_mxfp4(w: np.ndarray) -> QuantWeight:
     e2m1 exponent), biased by 127 and clamped to [0, 254]; elements are
     rounded to e2m1 after division by 2^(E-127), saturating at 6.
     """
-    w = np.asarray(w, dtype=np.float64)
+    w = np.asarray(w)
+    if w.dtype not in (np.float32, np.float64):
+        w = w.astype(np.float64)
     e, n, k = w.shape
     assert k % 32 == 0
     wg = w.reshape(e, n, k // 32, 32)
     amax = np.abs(wg).max(axis=-1)
-    with np.errstate(divide="ignore"):
-        ex = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, 0)
-    big = np.clip(ex + 127, 0, 254).astype(np.int64)
-    scaled = wg / np.exp2(big - 127.0)[..., None]
+    _, ex = np.frexp(amax)                       # amax = f * 2^ex, f in [0.5, 1): floor(log2) = ex - 1
+    big = np.where(amax > 0, np.clip(ex - 1 - 2 + 127, 0, 254), 127).astype(np.int64)
+    scaled = np.ldexp(wg, (127 - big)[..., None].astype(np.int32))
     u = _e2m1_encode(scaled).reshape(e, n, k)
     return QuantWeight(wtype="mxfp4", n=n, k=k, num_experts=e, group_k=32, group_n=1,
                        stype="ue8m0", signed=True, codes=pack_nibbles(u),
@@ -356,8 +358,14 @@ def moe_mxfp4(seed: int, tokens: int, num_experts: int = 128, n: int = 1536, k: 
               topk: int = 8):
     """MoE gate+up weights in MXFP4 with bf16 activations and skewed top-k routing."""
     rng = np.random.default_rng(seed)
-    w = rng.standard_normal((num_experts, n, k)) * 0.02
-    qw = quantize_mxfp4(w)
+    codes, scales = [], []
+    for e0 in range(0, num_experts, 8):          # chunks of experts bound the memory
+        ne = min(8, num_experts - e0)
+        part = quantize_mxfp4(rng.standard_normal((ne, n, k), dtype=np.float32) * np.float32(0.02))
+        codes.append(part.codes)
+        scales.append(part.scales)
+    qw = QuantWeight("mxfp4", n, k, num_experts, 32, 1, "ue8m0", True, np.concatenate(codes),
+                     np.concatenate(scales))
     x = make_activations(rng, tokens, k, "bf16")
     r = make_routing(rng, tokens, num_experts, topk)
     return qw, x, r
