@@ -280,12 +280,12 @@ cudaError_t launch_fp8(const Fp8Params& p, const CUtensorMap& tmap, int bn, int 
                        cudaStream_t stream) {
   if (bn <= 128) {
     auto k = fp8::fp8_kernel<128>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k));
     if (e != cudaSuccess) return e;
     k<<<grid, fp8::kThreads, smem, stream>>>(p, tmap);
   } else {
     auto k = fp8::fp8_kernel<256>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k));
     if (e != cudaSuccess) return e;
     k<<<grid, fp8::kThreads, smem, stream>>>(p, tmap);
   }

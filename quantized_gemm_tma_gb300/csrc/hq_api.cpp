@@ -58,8 +58,13 @@ hq_status device_info(DevInfo* out) {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-hq_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, const void* base, uint64_t inner,
-                    uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer) {
+// 2-D map {inner, outer} (row stride in elements) with box {box_inner,
+// box_outer}; with slabs != 0 a 3-D map that views each row as slabs of
+// `inner` columns: low 32 bits of `slabs` = slab count, high 32 bits = slabs
+// per box (dims {inner, outer, slabs}, slab stride inner * elem bytes).
+hq_status encode_uncached(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, const void* base,
+                          uint64_t inner, uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner,
+                          uint32_t box_outer, uint64_t slabs) {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -69,21 +74,92 @@ hq_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, 
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
   if (!g_encode) return HQ_ERR_CUDA;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_stride_elems * elem};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (slabs == 0) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_elems * elem};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[3] = {inner, outer, slabs & 0xffffffffull};
+    cuuint64_t strides[2] = {row_stride_elems * elem, inner * elem};
+    cuuint32_t box[3] = {box_inner, box_outer, static_cast<cuuint32_t>(slabs >> 32)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? HQ_OK : HQ_ERR_CUDA;
+}
+
+// Tensor maps depend only on (address, shape, strides, box, type): keep the
+// last few per host thread so repeated calls on the same buffers skip the
+// driver encode.
+struct MapKey {
+  const void* base;
+  uint64_t inner, outer, stride, slabs;
+  uint32_t box_inner, box_outer, dtype;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && stride == o.stride && slabs == o.slabs &&
+           box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype;
+  }
+};
+struct MapCache {
+  static constexpr int kSlots = 16;
+  MapKey key[kSlots];
+  CUtensorMap map[kSlots];
+  int used = 0, next = 0;
+};
+thread_local MapCache g_maps;
+
+hq_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer,
+                    uint64_t slabs = 0) {
+  const MapKey k{base, inner, outer, row_stride_elems * elem, slabs, box_inner, box_outer, static_cast<uint32_t>(dtype)};
+  MapCache& c = g_maps;
+  for (int i = 0; i < c.used; ++i)
+    if (c.key[i] == k) {
+      *map = c.map[i];
+      return HQ_OK;
+    }
+  hq_status st = encode_uncached(map, dtype, elem, base, inner, outer, row_stride_elems, box_inner, box_outer, slabs);
+  if (st != HQ_OK) return st;
+  const int slot = c.used < MapCache::kSlots ? c.used++ : (c.next++ % MapCache::kSlots);
+  c.key[slot] = k;
+  c.map[slot] = *map;
+  return HQ_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tuning and trace switches from the environment, read once per process.
+struct EnvKnobs {
+  int force_bn = 0, force_splitk = 0, force_issuers = 0, trace = 0;
+};
+const EnvKnobs& env() {
+  static const EnvKnobs k = [] {
+    EnvKnobs e;
+    auto get = [](const char* name) {
+      const char* v = std::getenv(name);
+      return v ? std::atoi(v) : 0;
+    };
+    e.force_bn = get("HQ_FORCE_BN");
+    e.force_splitk = get("HQ_FORCE_SPLITK");
+    e.force_issuers = get("HQ_FORCE_ISSUERS");
+    e.trace = get("HQ_TRACE");
+    return e;
+  }();
+  return k;
+}
+
 int env_int(const char* name, int dflt) {
-  const char* v = std::getenv(name);
-  return v ? std::atoi(v) : dflt;
+  int v = 0;
+  if (!std::strcmp(name, "HQ_FORCE_BN")) v = env().force_bn;
+  else if (!std::strcmp(name, "HQ_FORCE_SPLITK")) v = env().force_splitk;
+  else if (!std::strcmp(name, "HQ_FORCE_ISSUERS")) v = env().force_issuers;
+  else if (!std::strcmp(name, "HQ_TRACE")) v = env().trace;
+  return v ? v : dflt;
 }
 
 }  // namespace

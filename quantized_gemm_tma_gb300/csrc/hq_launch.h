@@ -9,6 +9,10 @@
 
 namespace hq {
 
+// Raise a kernel's dynamic shared memory limit to the device maximum, once per
+// (kernel, device); later calls are a table lookup.
+cudaError_t ensure_smem_optin(const void* kernel);
+
 // transform.cu
 cudaError_t launch_repack(const Layout& L, const hq_weight_desc& d, void* dst, cudaStream_t stream);
 cudaError_t launch_unpack(const Layout& L, const void* src, void* codes, void* scales, void* zeros,

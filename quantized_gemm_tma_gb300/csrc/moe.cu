@@ -158,8 +158,7 @@ cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, in
                              int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* status,
                              cudaStream_t stream) {
   const size_t smem = sizeof(int) * (static_cast<size_t>(kRouteWarps) * num_experts + 33);
-  cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(moe_route_kernel));
   if (e != cudaSuccess) return e;
   moe_route_kernel<<<1, kRouteThreads, smem, stream>>>(topk_ids, pairs, num_experts, bn, expert_offsets,
                                                         tile_offsets, perm, offsets_out, perm_out, status);

@@ -11,7 +11,7 @@ template <bool BF16, int BN_MAX, bool MOE>
 cudaError_t run(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows, int64_t ldx,
                 cudaStream_t stream) {
   auto k = wna16::wna16_kernel<1, BF16, BN_MAX, MOE>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(l.smem));
+  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k));
   if (e != cudaSuccess) return e;
   k<<<l.grid, wna16::kThreads, l.smem, stream>>>(p, tmap, static_cast<const __nv_bfloat16*>(x_rows), ldx);
   return cudaGetLastError();

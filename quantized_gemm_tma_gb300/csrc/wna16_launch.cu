@@ -2,6 +2,8 @@
 #include "gemm_wna16.cuh"
 #include "hq_launch.h"
 
+#include <mutex>
+
 namespace hq {
 
 cudaError_t launch_wna16_int4(const Wna16Launch&, const GemmParams&, const CUtensorMap&, const void*, int64_t,
@@ -26,5 +28,31 @@ uint32_t wna16_smem_bytes(int stages, uint32_t tile_bytes, int bn, int num_exper
 }
 
 int wna16_min_blocks(int bn_max) { return bn_max <= 64 ? 2 : 1; }
+
+cudaError_t ensure_smem_optin(const void* kernel) {
+  constexpr int kSlots = 128;
+  static const void* funcs[kSlots];
+  static uint64_t done[kSlots];  // one bit per device
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  std::lock_guard<std::mutex> lk(mu);
+  int i = 0;
+  for (; i < kSlots && funcs[i]; ++i)
+    if (funcs[i] == kernel) break;
+  if (i < kSlots && funcs[i] == kernel && (done[i] & bit)) return cudaSuccess;
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e != cudaSuccess) return e;
+  if (i < kSlots) {
+    funcs[i] = kernel;
+    done[i] |= bit;
+  }
+  return cudaSuccess;
+}
 
 }  // namespace hq
