@@ -9,12 +9,16 @@ N = 1536, K = 2048, top-8 routing, T in {16, 256, 4096}) is timed the same
 way and reported under "moe".
 
 Timing: W untimed warm-up steps, then K timed steps.  Every GEMM call is
-bracketed by CUDA events on the stream it is launched on; L2 is flushed (a
-256 MiB write) before each call, outside the events.  `value` is the
-whole-job aggregate TFLOP/s: all FLOPs of the timed steps on all ranks over
-the slowest rank's summed GEMM time.  `e2e` is the same metric through the
-public C-ABI call with the step's activations copied in from pinned host
-memory and the outputs copied back, inside the timed region.
+bracketed by CUDA events on the stream it is launched on.  Consecutive calls
+rotate over 8 transformed copies of the weight (8 x 36 MiB, well above the
+129 MB L2) and 4 copies of each activation, so no call finds its operands in
+L2.  A device-side sleep is queued before the timed steps so that the host
+enqueues ahead of the GPU and host submission gaps stay outside the events.
+`value` is the whole-job aggregate TFLOP/s: all FLOPs of the timed steps on
+all ranks over the slowest rank's summed GEMM time.  `e2e` is the same metric
+through the public C-ABI call with host buffers: per step, the activations
+are copied in from pinned host memory, the GEMMs run and the outputs are
+copied back, timed by the host clock from enqueue to completion.
 
 `--impl reference` times the CPU oracle (the parity reference; this subject
 has no runnable reference implementation) on a bounded sample of the same
@@ -40,7 +44,10 @@ MOE_T = [16, 256, 4096]
 MOE_E, MOE_N, MOE_K, MOE_TOPK = 128, 1536, 2048, 8
 WORKLOAD = ("dense W4A16: asymmetric INT4 g128 (uint4 zeros, bf16 scales), bf16 activations, "
             "N=K=8192, M sweep {1,16,128,1024,4096}")
-L2_FLUSH_BYTES = 256 << 20
+W_COPIES = 8       # rotated transformed weight copies (> L2 in total)
+X_COPIES = 4       # rotated activation copies per M
+MOE_COPIES = 2     # rotated MoE expert sets (213 MB each)
+HEAD_START_CYCLES = 100_000_000
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -183,24 +190,39 @@ def run_gpu(args, rank: int, world: int):
     codes, scales, zeros = to_dev(qw.codes), to_dev(qw.scales), to_dev(qw.zeros)
     desc = hq.make_desc("int4", "bf16", N, K, 1, 128, 1, False, True, codes, scales, zeros)
     wt_bytes = hq.hq_transform_size(desc)
-    wt = torch.empty(wt_bytes, dtype=torch.uint8, device=dev)
-    hq.hq_transform(desc, wt, wt_bytes, sh)
+    wts = []
+    for _ in range(W_COPIES):
+        wt = torch.empty(wt_bytes, dtype=torch.uint8, device=dev)
+        hq.hq_transform(desc, wt, wt_bytes, sh)
+        wts.append(wt)
+    del codes, scales, zeros
     rng = np.random.default_rng(1)
     xs, ys, wss, xh, yh = {}, {}, {}, {}, {}
-    for m in M_SWEEP:
+    for m in args.m_sweep:
         xb = synth.to_bf16_bits(rng.standard_normal((m, K)))
-        xs[m] = to_dev(xb)
-        ys[m] = torch.empty((m, N), dtype=torch.bfloat16, device=dev)
+        xs[m] = [to_dev(xb) for _ in range(X_COPIES)]
+        ys[m] = [torch.empty((m, N), dtype=torch.bfloat16, device=dev) for _ in range(X_COPIES)]
         need = hq.hq_gemm_workspace_size(desc, m, "bf16")
         wss[m] = torch.zeros(need, dtype=torch.uint8, device=dev)
         xh[m] = torch.from_numpy(xb.view(np.int16)).pin_memory()
         yh[m] = torch.empty((m, N), dtype=torch.bfloat16).pin_memory()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     launches = {"n": 0}
+    rot = {"w": 0, "x": 0, "moe": 0}
 
     def gemm(m):
-        hq.hq_gemm(desc, wt, m, "bf16", xs[m], K, None, ys[m], N, wss[m], wss[m].numel(), 0, sh)
+        wt = wts[rot["w"] % W_COPIES]
+        i = rot["x"] % X_COPIES
+        rot["w"] += 1
+        rot["x"] += 1
+        hq.hq_gemm(desc, wt, m, "bf16", xs[m][i], K, None, ys[m][i], N, wss[m], wss[m].numel(), 0, sh)
         launches["n"] += hq.hq_last_plan()["launches"]
+
+    def gemm_host(m):
+        """One call as a user with host buffers makes it: H2D, GEMM, D2H."""
+        xs[m][0].copy_(xh[m].view(torch.int16), non_blocking=True)
+        rot["x"] = 0
+        gemm(m)
+        yh[m].copy_(ys[m][0], non_blocking=True)
 
     # ---- MoE workload
     moe = None
@@ -209,9 +231,12 @@ def run_gpu(args, rank: int, world: int):
         mdesc = hq.make_desc("mxfp4", "ue8m0", MOE_N, MOE_K, MOE_E, 32, 1, True, False,
                              to_dev(mq.codes), to_dev(mq.scales), None)
         mbytes = hq.hq_transform_size(mdesc)
-        mwt = torch.empty(mbytes, dtype=torch.uint8, device=dev)
-        hq.hq_transform(mdesc, mwt, mbytes, sh)
-        moe = {"desc": mdesc, "wt": mwt, "T": {}}
+        mwts = []
+        for _ in range(MOE_COPIES):
+            mwt = torch.empty(mbytes, dtype=torch.uint8, device=dev)
+            hq.hq_transform(mdesc, mwt, mbytes, sh)
+            mwts.append(mwt)
+        moe = {"desc": mdesc, "wt": mwts, "T": {}}
         for t in MOE_T:
             r = synth.make_routing(np.random.default_rng(10 + t), t, MOE_E, MOE_TOPK)
             x = synth.to_bf16_bits(np.random.default_rng(20 + t).standard_normal((t, MOE_K)))
@@ -224,12 +249,13 @@ def run_gpu(args, rank: int, world: int):
 
     def moe_call(t):
         d = moe["T"][t]
-        hq.hq_moe_gemm(moe["desc"], moe["wt"], t, MOE_TOPK, d["ids"], d["w"], "bf16", d["x"], MOE_K, d["y"], MOE_N,
+        mwt = moe["wt"][rot["moe"] % MOE_COPIES]
+        rot["moe"] += 1
+        hq.hq_moe_gemm(moe["desc"], mwt, t, MOE_TOPK, d["ids"], d["w"], "bf16", d["x"], MOE_K, d["y"], MOE_N,
                        None, None, d["ws"], d["ws"].numel(), 0, sh)
         launches["n"] += hq.hq_last_plan()["launches"]
 
     def timed(fn, arg):
-        flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -245,26 +271,27 @@ def run_gpu(args, rank: int, world: int):
 
     # ---- warm-up
     for _ in range(args.warmup):
-        for m in M_SWEEP:
+        for m in args.m_sweep:
             timed(gemm, m)
         if moe:
             for t in MOE_T:
                 timed(moe_call, t)
     torch.cuda.synchronize()
-    st = hq.hq_status_read(wss[M_SWEEP[0]], 0, sh)
+    st = hq.hq_status_read(wss[args.m_sweep[0]], 0, sh)
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {hq.status_string(st)}")
 
     # ---- timed steps
     launches["n"] = 0
-    per_m = {m: [] for m in M_SWEEP}
+    per_m = {m: [] for m in args.m_sweep}
     per_t = {t: [] for t in MOE_T}
     with ClockSampler(dev.index) as clk:
         barrier()
         wall0 = time.perf_counter()
+        torch.cuda._sleep(HEAD_START_CYCLES)
         events = []
         for _ in range(args.steps):
-            for m in M_SWEEP:
+            for m in args.m_sweep:
                 events.append(("d", m, *timed(gemm, m)))
             if moe:
                 for t in MOE_T:
@@ -275,24 +302,19 @@ def run_gpu(args, rank: int, world: int):
         (per_m if kind == "d" else per_t)[key].append(e0.elapsed_time(e1) * 1e-3)
     gpu_launches = launches["n"]
 
-    # ---- end to end through the C ABI with host buffers (pinned), same steps
+    # ---- end to end through the C ABI with host buffers (pinned): per step the
+    # host clock runs from the first H2D enqueue to the last D2H completion.
     e2e_times = []
-    for step in range(args.warmup + args.steps):
-        tot = 0.0
-        for m in M_SWEEP:
-            flush.zero_()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            xs[m].copy_(xh[m].view(torch.int16), non_blocking=True)
-            gemm(m)
-            yh[m].copy_(ys[m], non_blocking=True)
-            e1.record(stream)
-            e1.synchronize()
-            tot += e0.elapsed_time(e1) * 1e-3
-        if step >= args.warmup:
-            e2e_times.append(tot)
-    st = hq.hq_status_read(wss[M_SWEEP[0]], 0, sh)
+    if not args.no_e2e:
+        for step in range(args.warmup + args.steps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for m in args.m_sweep:
+                gemm_host(m)
+            stream.synchronize()
+            if step >= args.warmup:
+                e2e_times.append(time.perf_counter() - t0)
+    st = hq.hq_status_read(wss[args.m_sweep[0]], 0, sh)
     if st != 0:
         raise RuntimeError(f"device status: {hq.status_string(st)}")
 
@@ -300,13 +322,13 @@ def run_gpu(args, rank: int, world: int):
         "per_m": {m: statistics.mean(v) for m, v in per_m.items()},
         "per_m_min": {m: min(v) for m, v in per_m.items()},
         "step_s": sum(statistics.mean(v) for v in per_m.values()),
-        "e2e_step_s": statistics.mean(e2e_times),
+        "e2e_step_s": statistics.mean(e2e_times) if e2e_times else None,
         "clocks": clk.summary(),
         "wall_s": wall,
         "gpu_launches": gpu_launches,
         "plans": {},
     }
-    for m in M_SWEEP:
+    for m in args.m_sweep:
         gemm(m)
         res["plans"][m] = hq.hq_last_plan()
     if moe:
@@ -334,7 +356,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-moe", action="store_true", help="skip the MoE sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--m-sweep", type=str, default=",".join(map(str, M_SWEEP)),
+                    help="comma-separated M values of the dense sweep")
     args = ap.parse_args()
+    args.m_sweep = [int(v) for v in args.m_sweep.split(",") if v]
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -370,7 +396,7 @@ def main():
         dist.init_process_group("nccl")
     res = run_gpu(args, local, world)
     step_s = reduce_max(res["step_s"], world)
-    e2e_s = reduce_max(res["e2e_step_s"], world)
+    e2e_s = reduce_max(res["e2e_step_s"], world) if res["e2e_step_s"] is not None else None
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -378,10 +404,11 @@ def main():
         return
 
     pk = peaks()
-    flops_step = sum(dense_flops(m) for m in M_SWEEP)
+    sw = args.m_sweep
+    flops_step = sum(dense_flops(m) for m in sw)
     value = world * flops_step / step_s / 1e12
     sweep = []
-    for m in M_SWEEP:
+    for m in sw:
         t = res["per_m"][m]
         by, fl = dense_bytes(m), dense_flops(m)
         roof_t = max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
@@ -390,31 +417,34 @@ def main():
                       "roofline_frac": round(roof_t / t, 3),
                       "bound": "hbm" if by / (pk["hbm_gbs"] * 1e9) >= fl / (pk["bf16_tflops"] * 1e12) else "tensor",
                       "plan": res["plans"][m]})
-    big = M_SWEEP[-1]
+    big = max(sw)
     t_big = res["per_m"][big]
     ach = dense_flops(big) / t_big / 1e12
     roofline = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(ach / pk["bf16_tflops"], 4), "traffic": None,
-                "kernel": "wna16_kernel<INT4,bf16,256> (M=4096 launch)", "peak_source": pk["source"]}
-    dec = 16
+                "kernel": f"WnA16 INT4 kernel (M={big} launch)", "peak_source": pk["source"]}
+    dec = 16 if 16 in sw else min(sw)
     t_dec = res["per_m"][dec]
     gbs = dense_bytes(dec) / t_dec / 1e9
     roofline_decode = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                        "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
-                       "kernel": "wna16_kernel<INT4,bf16,64> (M=16 launch)", "peak_source": pk["source"]}
+                       "kernel": f"WnA16 INT4 kernel (M={dec} launch)", "peak_source": pk["source"]}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "l2": "flushed (256 MiB write) before every timed call, outside the events",
+        "config": {"workload": WORKLOAD, "m_sweep": sw,
+                   "l2": f"inputs larger than L2: calls rotate over {W_COPIES} weight copies "
+                         f"({W_COPIES * 36} MiB) and {X_COPIES} activation copies",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "timing": "CUDA events around each hq_gemm call on its stream; value = FLOPs / summed mean times"},
         "sweep": sweep,
         "roofline": roofline,
         "roofline_decode": roofline_decode,
-        "e2e": {"value": round(world * flops_step / e2e_s / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": sum(m * K * 2 for m in M_SWEEP),
-                "d2h_bytes_per_step": sum(m * N * 2 for m in M_SWEEP)},
+        "e2e": None if e2e_s is None else {
+            "value": round(world * flops_step / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": sum(m * K * 2 for m in sw), "d2h_bytes_per_step": sum(m * N * 2 for m in sw),
+            "ms_per_step": round(e2e_s * 1e3, 4)},
         "gpu_launches": res["gpu_launches"],
         "clocks": res["clocks"],
     }
