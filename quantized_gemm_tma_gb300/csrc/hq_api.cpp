@@ -474,9 +474,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
     return HQ_ERR_ALIGNMENT;
   if ((ldx * xelem) % 16 != 0 || (ldy * 2) % 4 != 0) return HQ_ERR_ALIGNMENT;
   if (fp8 && !aligned16(x_scales)) return HQ_ERR_ALIGNMENT;
-  size_t need = 0;
-  hq_gemm_workspace_size(wdesc, m, atype, &need);
-  if (ws_bytes < need) return HQ_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < kAlign) return HQ_ERR_WORKSPACE_TOO_SMALL;
   DevInfo di;
   st = device_info(&di);
   if (st != HQ_OK) return st;
@@ -486,6 +484,9 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
 
   if (fp8) {
     const Fp8Plan pl = plan_fp8(L, m, di.sms, di.smem_optin, flags);
+    // the plan this device runs needs at most what hq_gemm_workspace_size reports
+    if (ws_bytes < kAlign + splitk_bytes(pl.splits, pl.m_tiles, pl.n_groups, m, L.n_pad))
+      return HQ_ERR_WORKSPACE_TOO_SMALL;
     Fp8Params p{};
     p.tiles = wt + L.tiles_off;
     p.expert_stride = L.expert_stride;
@@ -512,6 +513,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   }
 
   const DensePlan pl = plan_wna16(L, m, di.sms, di.smem_optin, flags);
+  if (ws_bytes < kAlign + splitk_bytes(pl.splits, pl.m_tiles, L.n_tiles, m, L.n_pad)) return HQ_ERR_WORKSPACE_TOO_SMALL;
   GemmParams p{};
   p.tiles = wt + L.tiles_off;
   p.expert_stride = L.expert_stride;
