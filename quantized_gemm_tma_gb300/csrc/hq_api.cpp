@@ -335,6 +335,9 @@ namespace {
 
 constexpr int kMaxSplits = 64;
 constexpr int kPlanSmsBound = 192;  // >= the SM count of any sm_103 part (workspace sizing)
+// split-K runs only on problems of at most this many output tiles
+constexpr int kMaxSplitTiles = 512;
+constexpr size_t kCounterBytes = sizeof(int) * kMaxSplitTiles * 8;
 
 struct DensePlan {
   int bn, bn_max, m_tiles, splits, kb_per_split, stages, grid;
@@ -363,6 +366,7 @@ Fp8Plan plan_fp8(const Layout& L, int m, int sms, size_t smem_optin, uint32_t fl
   const int forced = env_int("HQ_FORCE_SPLITK", 0);
   if (forced > 0 && !(flags & HQ_FLAG_BATCH_INVARIANT)) splits = std::min(forced, L.k_tiles);
   splits = std::min(splits, kMaxSplits);
+  if (tiles > kMaxSplitTiles) splits = 1;
   p.kb_per_split = cdiv(L.k_tiles, splits);
   p.splits = cdiv(L.k_tiles, p.kb_per_split);
   const size_t budget = std::min<size_t>(smem_optin, 232448) - 4096;
@@ -373,11 +377,13 @@ Fp8Plan plan_fp8(const Layout& L, int m, int sms, size_t smem_optin, uint32_t fl
   return p;
 }
 
-// Split-K scratch of a plan: counters [m_tiles * n_tiles(or groups) * 8], fp32 partials.
-size_t splitk_bytes(int splits, int m_tiles, int n_tiles, int m, int n_pad) {
+// Split-K scratch: a counter region of fixed size right after the status word
+// (8 counters per split tile, at most kMaxSplitTiles tiles), then the fp32
+// partials.  The fixed offset keeps one problem's partials off another
+// problem's counters when a workspace is reused across shapes.
+size_t splitk_bytes(int splits, int m, int n_pad) {
   if (splits <= 1) return 0;
-  return align_up(sizeof(int) * static_cast<size_t>(m_tiles) * n_tiles * 8, kAlign) +
-         align_up(sizeof(float) * static_cast<size_t>(splits) * m * n_pad, kAlign);
+  return kCounterBytes + align_up(sizeof(float) * static_cast<size_t>(splits) * m * n_pad, kAlign);
 }
 
 // Heuristic for one GB300: tokens per tile from M, then split-K until the
@@ -408,6 +414,7 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   const int forced = env_int("HQ_FORCE_SPLITK", 0);
   if (forced > 0 && !(flags & HQ_FLAG_BATCH_INVARIANT)) splits = std::min(forced, L.k_tiles);
   splits = std::min(splits, kMaxSplits);
+  if (tiles > kMaxSplitTiles) splits = 1;
   p.kb_per_split = cdiv(L.k_tiles, splits);
   p.splits = cdiv(L.k_tiles, p.kb_per_split);  // every split gets >= 1 K-tile
   const size_t budget = std::min<size_t>(smem_optin, 232448 / p.min_blocks) - 2048;
@@ -438,10 +445,10 @@ hq_status hq_gemm_workspace_size(const hq_weight_desc* desc, int32_t m, int32_t 
     for (int sms = 1; sms <= kPlanSmsBound; sms = sms < 64 ? sms * 2 : sms + 8) {
       if (desc->wtype == HQ_W_FP8_E4M3) {
         const Fp8Plan p = plan_fp8(L, m, sms, 232448, 0);
-        best = std::max(best, splitk_bytes(p.splits, p.m_tiles, p.n_groups, m, L.n_pad));
+        best = std::max(best, splitk_bytes(p.splits, m, L.n_pad));
       } else {
         const DensePlan p = plan_wna16(L, m, sms, 232448, 0);
-        best = std::max(best, splitk_bytes(p.splits, p.m_tiles, L.n_tiles, m, L.n_pad));
+        best = std::max(best, splitk_bytes(p.splits, m, L.n_pad));
       }
     }
     ws += best;
@@ -485,7 +492,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   if (fp8) {
     const Fp8Plan pl = plan_fp8(L, m, di.sms, di.smem_optin, flags);
     // the plan this device runs needs at most what hq_gemm_workspace_size reports
-    if (ws_bytes < kAlign + splitk_bytes(pl.splits, pl.m_tiles, pl.n_groups, m, L.n_pad))
+    if (ws_bytes < kAlign + splitk_bytes(pl.splits, m, L.n_pad))
       return HQ_ERR_WORKSPACE_TOO_SMALL;
     Fp8Params p{};
     p.tiles = wt + L.tiles_off;
@@ -500,8 +507,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
     p.y = y; p.ldy = ldy;
     p.status = reinterpret_cast<int*>(ws);
     p.counters = reinterpret_cast<int*>(ws + kAlign);
-    p.partials = reinterpret_cast<float*>(
-        ws + kAlign + align_up(sizeof(int) * static_cast<size_t>(pl.m_tiles) * pl.n_groups * 8, kAlign));
+    p.partials = reinterpret_cast<float*>(ws + kAlign + kCounterBytes);
     CUtensorMap tm;
     st = encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, x, L.k, m, ldx, 128, 128);
     if (st != HQ_OK) return st;
@@ -513,7 +519,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   }
 
   const DensePlan pl = plan_wna16(L, m, di.sms, di.smem_optin, flags);
-  if (ws_bytes < kAlign + splitk_bytes(pl.splits, pl.m_tiles, L.n_tiles, m, L.n_pad)) return HQ_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < kAlign + splitk_bytes(pl.splits, m, L.n_pad)) return HQ_ERR_WORKSPACE_TOO_SMALL;
   GemmParams p{};
   p.tiles = wt + L.tiles_off;
   p.expert_stride = L.expert_stride;
@@ -528,10 +534,9 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   p.idesc = idesc_f16(atype == HQ_A_BF16, 128, pl.bn);
   p.y = y; p.ldy = ldy;
   p.status = reinterpret_cast<int*>(ws);
-  size_t off = kAlign;
-  p.counters = reinterpret_cast<int*>(ws + off);
-  off += align_up(sizeof(int) * static_cast<size_t>(pl.m_tiles) * L.n_tiles * kWna16DqWarps, kAlign);
-  p.partials = reinterpret_cast<float*>(ws + off);
+  static_assert(kWna16DqWarps <= 8, "counter region holds 8 counters per split tile");
+  p.counters = reinterpret_cast<int*>(ws + kAlign);
+  p.partials = reinterpret_cast<float*>(ws + kAlign + kCounterBytes);
   p.num_experts = 1;
   CUtensorMap tm;
   st = encode_2d(&tm, atype == HQ_A_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x,

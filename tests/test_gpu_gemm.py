@@ -114,6 +114,20 @@ def test_split_k_deterministic():
     assert np.array_equal(a, b)
 
 
+def test_workspace_reused_across_shapes():
+    """One workspace serves split-K problems of different shapes in turn: the
+    fp32 partials of one shape never land on the counters of the next."""
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import DevWeight, run_gemm, workspace
+    probs = [synth.dense_int6_channel(13, 8, 640, 2048), synth.dense_w4a16_asym(14, 300, 768, 1536),
+             synth.dense_w4a16_asym(11, 16, 1024, 4096), synth.dense_int6_channel(13, 8, 640, 2048)]
+    dws = [DevWeight(qw) for qw, _ in probs]
+    need = max(hq.hq_gemm_workspace_size(dw.desc, a.m, a.atype) for dw, (_, a) in zip(dws, probs))
+    ws = workspace(need)
+    for i, (dw, (qw, acts)) in enumerate(zip(dws, probs)):
+        check(run_gemm(dw, acts, ws=ws), _ref(qw, acts), f"shared workspace, problem {i}")
+
+
 # ------------------------------------------------------------------ full size, sampled rows
 FULL = [
     ("c1_w4a16_sym_16x1024x1024", synth.dense_w4a16_sym, 16, 1024, 1024),
