@@ -150,10 +150,10 @@ hq_status hq_transform_size(const hq_weight_desc* desc, size_t* bytes);
 
 /*
  * hq_transform — repack a standard-format weight into the sm_103 tile layout
- * ([LAUNCH] "Preprocessing then validates parameters, pads dimensions, and
- * repacks these tensors into layouts suited to the target kernel"; [WIKI]
- * "Quantization representation": transform() converts and transforms weights
- * and associated parameters for execution).
+ * ([LAUNCH] paragraph on preprocessing: parameters are checked, dimensions
+ * padded and the tensors rearranged for the kernel that will read them;
+ * [WIKI] "Quantization representation": the layer's transform step turns the
+ * weights and their side tensors into the execution layout).
  *
  * desc   standard-format device pointers (codes, scales, zeros)
  * dst    device buffer of at least hq_transform_size() bytes, 256-byte

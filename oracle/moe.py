@@ -3,7 +3,7 @@
 What is computed (aiwiki Humming article, section "Device and workload
 selection": the indexed path gathers input rows through routing indices,
 grouped-contiguous execution places each expert's rows together; README
-"Supports both Dense GEMM and MoE GEMM"):
+"Key Features": MoE GEMM is supported next to the dense GEMM):
 
 routing  For topk_ids [T, topk] over E experts, with flat pair index
          f = t*topk + j:
