@@ -21,7 +21,8 @@
  * Conventions for every call:
  *   - All device pointers are owned by the caller.  The library allocates no
  *     device or host memory and keeps no mutable global state except a
- *     read-mostly cache of per-device properties.
+ *     read-mostly cache of per-device properties and the fixed device scratch
+ *     that hq_gemm_noalloc uses (a module-load array, not an allocation).
  *   - Calls are stream-ordered and asynchronous unless stated otherwise.
  *     Errors the host can detect are returned before anything is launched.
  *   - Errors found on the device (a bounded wait that ran out, an expert id
@@ -207,6 +208,43 @@ hq_status hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);
 hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32_t atype,
                   const void* x, int64_t ldx, const float* x_scales, void* y, int64_t ldy,
                   void* workspace, size_t ws_bytes, uint32_t flags, hq_stream_t stream);
+
+/* Bytes of the fixed device scratch behind hq_gemm_noalloc (8 MiB). */
+#define HQ_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/*
+ * hq_gemm_noalloc — hq_gemm without a workspace argument.  The Humming pages
+ * have no counterpart: this is an interface convenience of this library.
+ *
+ * For callers that cannot hand the library a workspace: code that holds only
+ * its input and output pointers at the call site, with no device allocator
+ * it may call there (a plugin or custom-op interface that passes tensors but
+ * no scratch, or a runtime that forbids allocation once its memory plan is
+ * fixed).  The status word, split-K counters and fp32 partials live instead
+ * in one file-scope device array of HQ_NOALLOC_SCRATCH_BYTES per device,
+ * zero at module load; no call allocates host or device memory.
+ *
+ * Arguments are hq_gemm's, less workspace/ws_bytes, plus:
+ * device_status  optional 4-byte device word; if non-null, the scratch's
+ *                status word is copied there on `stream` after the GEMM.
+ *                That word is sticky: once a bounded device-side wait has run
+ *                out it stays set for the life of the process (the split-K
+ *                counters may then be stale), and every later copy shows it.
+ *
+ * Set-up: the first call with a given device current looks up the scratch's
+ * address (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture.
+ * Limit: a problem whose hq_gemm_workspace_size() exceeds
+ * HQ_NOALLOC_SCRATCH_BYTES is rejected with HQ_ERR_WORKSPACE_TOO_SMALL before
+ * anything is launched; use hq_gemm with a workspace for it.
+ * Concurrency: all calls on one device share the scratch.  Calls whose GPU
+ * work can overlap (different streams without an ordering event, or several
+ * host threads) race on it and give wrong results; serialise them on one
+ * stream or order them with events.
+ */
+hq_status hq_gemm_noalloc(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32_t atype,
+                          const void* x, int64_t ldx, const float* x_scales, void* y, int64_t ldy,
+                          uint32_t flags, int32_t* device_status, hq_stream_t stream);
 
 /*
  * hq_moe_workspace_size — workspace for hq_moe_gemm (status word, routing

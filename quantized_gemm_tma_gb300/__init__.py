@@ -32,9 +32,12 @@ STYPES = {"bf16": HQ_S_BF16, "fp16": HQ_S_FP16, "fp32": HQ_S_FP32, "ue8m0": HQ_S
 #: every symbol include/hq.h declares
 EXPORTS = [
     "hq_version", "hq_status_string", "hq_transform_size", "hq_transform", "hq_untransform",
-    "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_moe_workspace_size", "hq_moe_gemm",
-    "hq_status_read", "hq_last_plan",
+    "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_gemm_noalloc", "hq_moe_workspace_size",
+    "hq_moe_gemm", "hq_status_read", "hq_last_plan",
 ]
+
+#: size of the fixed device scratch behind hq_gemm_noalloc
+HQ_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class HQError(RuntimeError):
@@ -80,6 +83,7 @@ def lib() -> ctypes.CDLL:
             "hq_gemm_workspace_size": ([dp, i32, i32, ctypes.POINTER(sz)], i32),
             "hq_workspace_init": ([vp, sz, vp], i32),
             "hq_gemm": ([dp, vp, i32, i32, vp, i64, vp, vp, i64, vp, sz, u32, vp], i32),
+            "hq_gemm_noalloc": ([dp, vp, i32, i32, vp, i64, vp, vp, i64, u32, vp, vp], i32),
             "hq_moe_workspace_size": ([dp, i32, i32, i32, ctypes.POINTER(sz)], i32),
             "hq_moe_gemm": ([dp, vp, i32, i32, vp, vp, i32, vp, i64, vp, i64, vp, vp, vp, sz, u32, vp], i32),
             "hq_status_read": ([vp, i32, vp, ctypes.POINTER(i32)], i32),
@@ -160,6 +164,13 @@ def hq_gemm(desc: WeightDesc, w_t, m: int, atype, x, ldx: int, x_scales, y, ldy:
             flags: int = 0, stream=None) -> None:
     _check(lib().hq_gemm(ctypes.byref(desc), _ptr(w_t), m, ATYPES.get(atype, atype), _ptr(x), ldx, _ptr(x_scales),
                          _ptr(y), ldy, _ptr(workspace), ws_bytes, flags, _stream(stream)), "hq_gemm")
+
+
+def hq_gemm_noalloc(desc: WeightDesc, w_t, m: int, atype, x, ldx: int, x_scales, y, ldy: int, flags: int = 0,
+                    device_status=None, stream=None) -> None:
+    _check(lib().hq_gemm_noalloc(ctypes.byref(desc), _ptr(w_t), m, ATYPES.get(atype, atype), _ptr(x), ldx,
+                                 _ptr(x_scales), _ptr(y), ldy, flags, _ptr(device_status), _stream(stream)),
+           "hq_gemm_noalloc")
 
 
 def hq_moe_workspace_size(desc: WeightDesc, tokens: int, topk: int, atype) -> int:
