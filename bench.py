@@ -48,6 +48,11 @@ W_COPIES = 8       # rotated transformed weight copies (> L2 in total)
 X_COPIES = 4       # rotated activation copies per M
 MOE_COPIES = 2     # rotated MoE expert sets (213 MB each)
 HEAD_START_CYCLES = 100_000_000
+# DRAM bytes (read + write) per launch of the WnA16 INT4 kernel, from the ncu
+# capture summarised in profiles/wna16_int4_asym_g128_n8192_k8192.md, keyed by
+# M; valid only while the kernel sources hash to `sha` (else reported null).
+NCU_TRAFFIC = {"sha": "7f238ad03aeeea22", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
+               "bytes": {16: 35_536_640, 4096: 266_105_856 + 33_297_408}}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -58,6 +63,18 @@ def dense_bytes(m: int) -> int:
 
 def dense_flops(m: int) -> int:
     return 2 * m * N * K
+
+
+def ncu_traffic(m: int):
+    """Captured DRAM bytes per launch at this M, or None if the kernel changed since."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in NCU_TRAFFIC["files"]:
+        with open(os.path.join(ROOT, "quantized_gemm_tma_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != NCU_TRAFFIC["sha"]:
+        return None
+    return NCU_TRAFFIC["bytes"].get(m)
 
 
 def peaks():
@@ -421,13 +438,13 @@ def main():
     t_big = res["per_m"][big]
     ach = dense_flops(big) / t_big / 1e12
     roofline = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(ach / pk["bf16_tflops"], 4), "traffic": None,
+                "frac": round(ach / pk["bf16_tflops"], 4), "traffic": ncu_traffic(big),
                 "kernel": f"WnA16 INT4 kernel (M={big} launch)", "peak_source": pk["source"]}
     dec = 16 if 16 in sw else min(sw)
     t_dec = res["per_m"][dec]
     gbs = dense_bytes(dec) / t_dec / 1e9
     roofline_decode = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                       "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                       "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": ncu_traffic(dec),
                        "kernel": f"WnA16 INT4 kernel (M={dec} launch)", "peak_source": pk["source"]}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
