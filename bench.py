@@ -8,8 +8,11 @@ activations, N = K = 8192, for every M of the sweep {1, 16, 128, 1024, 4096}
 N = 1536, K = 2048, top-8 routing, T in {16, 256, 4096}) is timed the same
 way and reported under "moe".
 
-Timing: W untimed warm-up steps, then K timed steps.  Every GEMM call is
-bracketed by CUDA events on the stream it is launched on.  Consecutive calls
+Timing: W untimed warm-up steps, then K timed steps.  Each step makes one
+call per shape; the K calls of one shape are issued back to back (as
+consecutive layers of a model would be), timed with CUDA events on the
+launching stream in blocks of 25 calls, so a kernel's launch can overlap the
+previous kernel's tail (programmatic dependent launch).  Consecutive calls
 rotate over 8 transformed copies of the weight (8 x 36 MiB, well above the
 129 MB L2) and 4 copies of each activation, so no call finds its operands in
 L2.  A device-side sleep is queued before the timed steps so that the host
@@ -47,7 +50,8 @@ WORKLOAD = ("dense W4A16: asymmetric INT4 g128 (uint4 zeros, bf16 scales), bf16 
 W_COPIES = 8       # rotated transformed weight copies (> L2 in total)
 X_COPIES = 4       # rotated activation copies per M
 MOE_COPIES = 2     # rotated MoE expert sets (213 MB each)
-HEAD_START_CYCLES = 100_000_000
+HEAD_START_CYCLES = 200_000_000
+BLOCK = 25         # back-to-back calls of one shape between two events
 # DRAM bytes (read + write) per launch of the WnA16 INT4 kernel, from the ncu
 # capture summarised in profiles/wna16_int4_asym_g128_n8192_k8192.md, keyed by
 # M; valid only while the kernel sources hash to `sha` (else reported null).
@@ -298,25 +302,42 @@ def run_gpu(args, rank: int, world: int):
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {hq.status_string(st)}")
 
-    # ---- timed steps
+    # ---- timed steps: every step makes one call per shape; the calls of one
+    # shape run back to back (as consecutive layers would), BLOCK calls between
+    # two events, so one kernel's launch overlaps the previous one's tail.
     launches["n"] = 0
     per_m = {m: [] for m in args.m_sweep}
     per_t = {t: [] for t in MOE_T}
+
+    def blocks(fn, arg, n):
+        out = []
+        done = 0
+        while done < n:
+            k = min(BLOCK, n - done)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(k):
+                fn(arg)
+            e1.record(stream)
+            out.append((k, e0, e1))
+            done += k
+        return out
+
     with ClockSampler(dev.index) as clk:
         barrier()
         wall0 = time.perf_counter()
         torch.cuda._sleep(HEAD_START_CYCLES)
         events = []
-        for _ in range(args.steps):
-            for m in args.m_sweep:
-                events.append(("d", m, *timed(gemm, m)))
-            if moe:
-                for t in MOE_T:
-                    events.append(("m", t, *timed(moe_call, t)))
+        for m in args.m_sweep:
+            events += [("d", m, *b) for b in blocks(gemm, m, args.steps)]
+        if moe:
+            for t in MOE_T:
+                events += [("m", t, *b) for b in blocks(moe_call, t, args.steps)]
         barrier()
         wall = time.perf_counter() - wall0
-    for kind, key, e0, e1 in events:
-        (per_m if kind == "d" else per_t)[key].append(e0.elapsed_time(e1) * 1e-3)
+    for kind, key, k, e0, e1 in events:
+        (per_m if kind == "d" else per_t)[key].append(e0.elapsed_time(e1) * 1e-3 / k)
     gpu_launches = launches["n"]
 
     # ---- end to end through the C ABI with host buffers (pinned): per step the
@@ -454,7 +475,7 @@ def main():
                    "l2": f"inputs larger than L2: calls rotate over {W_COPIES} weight copies "
                          f"({W_COPIES * 36} MiB) and {X_COPIES} activation copies",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "timing": "CUDA events around each hq_gemm call on its stream; value = FLOPs / summed mean times"},
+                   "timing": "CUDA events on the launching stream around blocks of 25 back-to-back calls of one shape; value = FLOPs / summed mean per-call times"},
         "sweep": sweep,
         "roofline": roofline,
         "roofline_decode": roofline_decode,

@@ -286,16 +286,17 @@ hq_status hq_status_read(void* workspace, int32_t clear, hq_stream_t stream, int
 
 /*
  * hq_last_plan — the launch plan of the most recent hq_gemm / hq_moe_gemm
- * call on this host thread: tile width along M (bn), split-K factor, grid
- * size and kernel launches.  For tests and benchmarks.
+ * call on this host thread.  For tests and benchmarks.
  */
 typedef struct {
-  int32_t bn;
-  int32_t splits;
-  int32_t grid;
-  int32_t launches;
-  int32_t stages;
-  int32_t reserved[3];
+  int32_t bn;          /* tokens per output tile (MMA N for WnA16, M side for FP8) */
+  int32_t splits;      /* FP8: split-K factor; WnA16: 1 = whole tiles, 0 = stream-K */
+  int32_t grid;        /* CTAs of the GEMM kernel */
+  int32_t launches;    /* kernels launched by the call */
+  int32_t stages;      /* shared-memory pipeline stages */
+  int32_t tile_class;  /* WnA16 tile-width class (0: bn <= 16, 1: <= 64, 2: <= 128, 3: <= 256) */
+  int32_t groups;      /* WnA16 dequantiser groups of four warps */
+  int32_t reserved;
 } hq_plan_info;
 hq_status hq_last_plan(hq_plan_info* info);
 

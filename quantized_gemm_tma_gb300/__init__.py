@@ -59,7 +59,8 @@ class WeightDesc(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     """hq_plan_info."""
     _fields_ = [("bn", ctypes.c_int32), ("splits", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("launches", ctypes.c_int32), ("stages", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("launches", ctypes.c_int32), ("stages", ctypes.c_int32), ("tile_class", ctypes.c_int32),
+                ("groups", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -198,4 +199,4 @@ def hq_last_plan() -> dict:
     info = PlanInfo()
     _check(lib().hq_last_plan(ctypes.byref(info)), "hq_last_plan")
     return {"bn": info.bn, "splits": info.splits, "grid": info.grid, "launches": info.launches,
-            "stages": info.stages}
+            "stages": info.stages, "tile_class": info.tile_class, "groups": info.groups}

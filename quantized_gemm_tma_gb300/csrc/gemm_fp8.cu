@@ -46,7 +46,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kHalfCols = BN / 2;  // columns per epilogue warp
   constexpr int kNT = BN / 128;      // weight tiles per stage
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from smem_raw by an offset so that the
+  // compiler keeps shared-memory addressing for every access through it
+  uint8_t* smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = p.stages;
   constexpr uint32_t kWBytes = 16384u * kNT;
   constexpr uint32_t kXBytes = kTokTile * 128u;

@@ -2,31 +2,42 @@
 // low-bit weights (INT4 / INT6 / MXFP4) against BF16 or FP16 activations, in
 // a dense form and an MoE grouped form ("WnA16": low-bit weights with 16-bit
 // activations — Humming launch article, WnA16 paragraph; MoE GEMM — README
-// Key Features).
+// "Key Features").
 //
-// Computes D[n, m] = sum_k W[n, k] * X[m, k] per tile of 128 weight rows x BN
-// tokens ("swap AB": the weights are the MMA's M side, so decode-sized M only
-// pads the MMA N dimension, down to 16).
+// Computes D[n, m] = sum_k W[n, k] * X[m, k] per output tile of 128 weight
+// rows x BN tokens ("swap AB": the weights are the MMA's M side, so a
+// decode-sized M only pads the MMA N dimension, down to 16).
 //
-// Warp roles (320 threads, one CTA per SM):
-//   warp 0     TMA producer: one bulk copy per weight tile (codes, scales and
-//              zeros are contiguous in the transformed layout) and a 2-D
-//              tensor copy of the activation tile (128-byte swizzle) into a
-//              multi-stage shared-memory ring.  MoE: activation rows are
-//              gathered by routing index with cp.async into the same swizzled
-//              layout.
-//   warp 1     TMEM allocator and MMA issuer: one thread issues
-//              tcgen05.mma.kind::f16 with the A operand (dequantised weights)
-//              read from tensor memory and B (activations) from shared memory,
-//              fp32 accumulation in TMEM.
-//   warps 2-9  dequantisers: each thread owns one weight row (TMEM lane) and
-//              two 32-column chunks of every 128-column K block; it turns the
-//              packed codes into bf16x2/f16x2 pairs with magic-number integer
-//              to float conversion, applies zero point and scale, and writes
-//              them into the A ring in TMEM with tcgen05.st.  After the K loop
-//              the same warps run the epilogue (tcgen05.ld -> scale -> store,
-//              split-K partials with a deterministic last-arriver reduction,
-//              or the MoE per-pair weighted outputs).
+// Work: the CTA walks a list of units (tile, K-block range).  Dense problems
+// with few tiles are split "stream-K": the tiles' K-blocks are dealt out in
+// equal contiguous ranges, one per CTA, so every SM streams the same number
+// of weight bytes; a tile covered by several CTAs is finished by the last of
+// them, which sums the fp32 partials in CTA order (deterministic).  Problems
+// with many tiles, and MoE, take whole tiles round-robin.
+//
+// Pipeline per CTA (one CTA per SM), warp roles:
+//   warps 0-3    epilogue: one TMEM lane quarter each; wait for a unit's
+//                accumulators, sum the issuers' partial accumulators, scale
+//                and store Y (or a partial, or MoE per-pair rows).
+//   warps 4-19   dequantisers, in KPS groups; group g converts K-block g of
+//                each stage.  A thread owns one weight row (its TMEM lane)
+//                and 4/(16/KPS/4) of the block's four 32-column chunks, turns
+//                the packed codes into bf16x2/f16x2 pairs and writes them into
+//                the group's next A slot in TMEM with tcgen05.st.
+//   warp 20      producer: per stage, one bulk copy of up to KPS consecutive
+//                weight tiles (one contiguous run of the tile layout) and one
+//                tensor copy per 64-column activation slab (128-byte swizzle);
+//                MoE rows are gathered by routing index, four rows per
+//                tile::gather4 tensor copy.
+//   warps 21..   MMA issuers: issuer p takes K-block p of every stage and
+//                accumulates into its own TMEM accumulator, so up to four
+//                threads issue tcgen05.mma.kind::f16 concurrently (one thread
+//                issues an M128 K16 MMA only every ~50-100 cycles, which alone
+//                would leave a decode-sized tile short of the HBM rate).
+//
+// Every wait is bounded (2 s, or the CTA abort flag); on a timeout the CTA
+// records HQ_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and
+// exits.
 #pragma once
 
 #include <cuda.h>
@@ -40,16 +51,37 @@
 namespace hq {
 namespace wna16 {
 
-constexpr int kDqWarps = kWna16DqWarps;
-constexpr int kThreads = 64 + 32 * kDqWarps;
-constexpr int kAStages = kWna16AStages;
+// Tile-width classes: maximum tokens per tile, K-blocks per stage (= MMA
+// issuers = dequantiser groups), accumulator buffers.  The 16 dequantiser
+// warps form kKps groups; group g takes K-block g of every stage and owns
+// kDa = 4 / kKps A slots of 64 TMEM columns (a ring, so it can convert the
+// next K-block while the MMA still reads the last).  TMEM: A slots in
+// columns [0, 256), accumulators (kDacc x kIss x kBnMax columns) in
+// [256, 512).
+template <int CLS>
+struct Cls;
+template <>
+struct Cls<0> { static constexpr int kBnMax = 16, kKps = 2, kIss = 2, kDacc = 2; };
+template <>
+struct Cls<1> { static constexpr int kBnMax = 64, kKps = 2, kIss = 2, kDacc = 2; };
+template <>
+struct Cls<2> { static constexpr int kBnMax = 128, kKps = 1, kIss = 1, kDacc = 2; };
+template <>
+struct Cls<3> { static constexpr int kBnMax = 256, kKps = 1, kIss = 1, kDacc = 1; };
 
-template <int BN_MAX>
-struct Cfg {
-  static constexpr int kTmemCols = (BN_MAX + 64 * kAStages) <= 256 ? 256 : 512;
-  static constexpr int kAccCol = 0;
-  static constexpr int kACol = BN_MAX;
-};
+constexpr int kEpiWarps = 4;
+constexpr int kDqWarps = 16;
+constexpr int kASlots = 4;
+constexpr int kDqWarp0 = kEpiWarps;                        // first dequant warp
+constexpr int kProdWarp = kDqWarp0 + kDqWarps;             // producer warp
+constexpr int kIssWarp0 = kProdWarp + 1;                   // first MMA issuer warp
+constexpr int kKRing = 4;  // promotion: per-K-block accumulators per issuer (class 0)
+constexpr uint32_t kACol0 = 0;
+constexpr uint32_t kAccCol0 = 256;
+constexpr uint32_t kTmemCols = 512;
+
+template <int CLS>
+constexpr int threads() { return 32 * (kIssWarp0 + Cls<CLS>::kIss); }
 
 // ---------------------------------------------------------------- packed math
 template <bool BF16>
@@ -83,18 +115,74 @@ __device__ __forceinline__ constexpr uint32_t magic_half() {
   return BF16 ? 0x4300u : 0x6400u;  // 128.0 (bf16) / 1024.0 (fp16): unit spacing in the mantissa
 }
 
-// INT4 chunk of 32 codes (offset-binary u) -> 16 pairs of (u - z) [* s].
+template <bool BF16>
+__device__ __forceinline__ uint32_t h2fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  if constexpr (BF16) {
+    __nv_bfloat162 x = __hfma2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b),
+                               *reinterpret_cast<__nv_bfloat162*>(&c));
+    r = *reinterpret_cast<uint32_t*>(&x);
+  } else {
+    __half2 x = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
+                        *reinterpret_cast<__half2*>(&c));
+    r = *reinterpret_cast<uint32_t*>(&x);
+  }
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_of(float f) {
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  return b | (b << 16);
+}
+__device__ __forceinline__ uint32_t f16x2_of(float f) {
+  const uint32_t b = __half_as_ushort(__float2half_rn(f));
+  return b | (b << 16);
+}
+
+// INT4 chunk of 32 codes (offset-binary u, zero point z) -> 16 pairs of
+// (u - z) * s (SCALE) or of the unscaled difference (channelwise: bf16 gives
+// (u - z) * 2^-7, fp16 gives u - z; the row scale follows in the epilogue).
+// Word w of a chunk holds the pairs (w & 0x000F000F), (w & 0x00F000F0) and
+// the same masks of w >> 8.
+//   bf16: a byte b in the low half of a bf16 is the value b * 2^-133 (the
+//         subnormal range and the first normal binade line up), so a masked
+//         pair is u * 2^-133 or 16u * 2^-133; one FMA by 2^126 (2^122) minus
+//         z * 2^-7 gives (u - z) * 2^-7 exactly, and one multiply by s * 2^7
+//         rounds the product once, as (u - z) * s would be.
+//   fp16: OR with 1024.0 (0x6400) puts u (16u) in the mantissa; one FMA with
+//         1 (1/16) minus 1024 + z (64 + z) gives u - z exactly.
 template <bool BF16, bool SCALE>
-__device__ __forceinline__ void dq_int4(const uint4 q, uint32_t c2, uint32_t s2, uint32_t (&o)[16]) {
+__device__ __forceinline__ void dq_int4(const uint4 q, uint32_t z, uint32_t s16, uint32_t (&o)[16]) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  constexpr uint32_t M = magic_half<BF16>() * 0x00010001u;
+  uint32_t c_lo, c_hi, a_lo, a_hi, sc = 0;
+  if constexpr (BF16) {
+    c_lo = 0x7E807E80u;  // 2^126
+    c_hi = 0x7C807C80u;  // 2^122
+    // -z * 2^-7 and s * 2^7 are exact in bf16: take the top half of the fp32 bits
+    const float zf = __uint_as_float(0x4B000000u | z) - 8388608.f;
+    const uint32_t zb = __float_as_uint(zf * -0.0078125f) >> 16;
+    a_lo = a_hi = zb | (zb << 16);
+    if constexpr (SCALE) {
+      const uint32_t sb = __float_as_uint(__uint_as_float(s16 << 16) * 128.f) >> 16;
+      sc = sb | (sb << 16);
+    }
+  } else {
+    c_lo = 0x3C003C00u;  // 1
+    c_hi = 0x2C002C00u;  // 1/16
+    a_lo = f16x2_of(-(1024.f + static_cast<float>(z)));
+    a_hi = f16x2_of(-(64.f + static_cast<float>(z)));
+    if constexpr (SCALE) sc = s16 * 0x00010001u;
+  }
+  constexpr uint32_t M = BF16 ? 0u : 0x64006400u;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
+    const uint32_t w8 = w[j] >> 8;
+    const uint32_t p[4] = {(w[j] & 0x000F000Fu) | M, (w[j] & 0x00F000F0u) | M, (w8 & 0x000F000Fu) | M,
+                           (w8 & 0x00F000F0u) | M};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t v = ((w[j] >> (4 * i)) & 0x000F000Fu) | M;
-      const uint32_t t = h2sub<BF16>(v, c2);
-      o[4 * j + i] = SCALE ? h2mul<BF16>(t, s2) : t;
+      const uint32_t t = h2fma<BF16>(p[i], (i & 1) ? c_hi : c_lo, (i & 1) ? a_hi : a_lo);
+      o[4 * j + i] = SCALE ? h2mul<BF16>(t, sc) : t;
     }
   }
 }
@@ -149,413 +237,670 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, got) != 0;
 }
 
-// ---------------------------------------------------------------- work items
-struct Work {
-  int e, nt, row0, rows, kb0, kb1, split, mt;
+// Stage-ring position: slot and phase parity, advanced without division.
+struct Ring {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++s == n) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
 };
 
+// ---------------------------------------------------------------- work units
+struct Unit {
+  int e, nt, mt, tile, row0, rows, kb0, kb1;
+};
+
+// The CTA's list of units.  Every role walks the same list.
 template <bool MOE>
-__device__ __forceinline__ Work decode_work(const GemmParams& p, int w, const int* s_tile_off, const int* s_row_off) {
-  Work r;
-  if constexpr (!MOE) {
-    r.split = w % p.splits;
-    const int t = w / p.splits;
-    r.nt = t % p.n_tiles;
-    r.mt = t / p.n_tiles;
-    r.e = 0;
-    r.row0 = r.mt * p.bn;
-    r.rows = min(p.bn, p.m - r.row0);
-    r.kb0 = r.split * p.kb_per_split;
-    r.kb1 = min(p.k_tiles, r.kb0 + p.kb_per_split);
-  } else {
-    const int tile = w / p.n_tiles;
-    r.nt = w % p.n_tiles;
-    // expert e: last index with tile_off[e] <= tile
-    int lo = 0, hi = p.num_experts;  // invariant tile_off[lo] <= tile < tile_off[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_tile_off[mid] <= tile) lo = mid; else hi = mid;
+struct Sched {
+  long long it, it_end;  // stream-K: K-block iteration range of this CTA
+  int w;                 // whole-tile / MoE: next work index
+
+  __device__ __forceinline__ void init(const GemmParams& p) {
+    if (!MOE && p.stream_k) {
+      it = static_cast<long long>(blockIdx.x) * p.iters / gridDim.x;
+      it_end = static_cast<long long>(blockIdx.x + 1) * p.iters / gridDim.x;
     }
-    r.e = lo;
-    r.mt = tile - s_tile_off[lo];
-    r.row0 = s_row_off[lo] + r.mt * p.bn;
-    r.rows = min(p.bn, s_row_off[lo + 1] - r.row0);
-    r.kb0 = 0;
-    r.kb1 = p.k_tiles;
-    r.split = 0;
+    w = blockIdx.x;
   }
-  return r;
+
+  __device__ __forceinline__ bool next(const GemmParams& p, const int* s_tile_off, const int* s_row_off, Unit& u) {
+    if constexpr (!MOE) {
+      if (p.stream_k) {
+        if (it >= it_end) return false;
+        u.tile = static_cast<int>(it / p.k_tiles);
+        u.kb0 = static_cast<int>(it - static_cast<long long>(u.tile) * p.k_tiles);
+        const long long left = it_end - it;
+        u.kb1 = (left < p.k_tiles - u.kb0) ? u.kb0 + static_cast<int>(left) : p.k_tiles;
+        it += u.kb1 - u.kb0;
+      } else {
+        if (w >= p.num_tiles) return false;
+        u.tile = w;
+        u.kb0 = 0;
+        u.kb1 = p.k_tiles;
+        w += gridDim.x;
+      }
+      u.nt = u.tile % p.n_tiles;
+      u.mt = u.tile / p.n_tiles;
+      u.e = 0;
+      u.row0 = u.mt * p.bn;
+      u.rows = min(p.bn, p.m - u.row0);
+      return true;
+    } else {
+      const int total = s_tile_off[p.num_experts] * p.n_tiles;
+      if (w >= total) return false;
+      const int tile = w / p.n_tiles;
+      u.nt = w % p.n_tiles;
+      // expert e: last index with tile_off[e] <= tile
+      int lo = 0, hi = p.num_experts;  // invariant tile_off[lo] <= tile < tile_off[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tile_off[mid] <= tile) lo = mid; else hi = mid;
+      }
+      u.e = lo;
+      u.mt = tile - s_tile_off[lo];
+      u.tile = w;
+      u.row0 = s_row_off[lo] + u.mt * p.bn;
+      u.rows = min(p.bn, s_row_off[lo + 1] - u.row0);
+      u.kb0 = 0;
+      u.kb1 = p.k_tiles;
+      w += gridDim.x;
+      return true;
+    }
+  }
+};
+
+// Stream-K: the CTAs whose iteration ranges meet tile t are [c_first, c_last];
+// CTA c's range starts at floor(c * T / G).
+__device__ __forceinline__ int sk_cta_of(long long x, long long T, int G) {
+  // largest c with floor(c*T/G) <= x
+  return static_cast<int>(((x + 1) * G - 1) / T);
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int FMT, bool BF16, int BN_MAX, bool MOE>
-__global__ void __launch_bounds__(kThreads, (BN_MAX <= 64 ? 2 : 1))
+template <int FMT, bool BF16, int CLS, bool MOE>
+__global__ void __launch_bounds__(threads<CLS>(), 1)
     wna16_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x,
                  const __nv_bfloat16* __restrict__ x_rows /* MoE: activations [T][ldx] */, int64_t ldx) {
-  using C = Cfg<BN_MAX>;
+  using C = Cls<CLS>;
+  constexpr int KPS = C::kKps, ISS = C::kIss, DACC = C::kDacc, BNMAX = C::kBnMax;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from smem_raw by an offset so that the
+  // compiler keeps shared-memory addressing for every access through it
+  uint8_t* smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
 
+  constexpr int G = KPS;                 // dequantiser groups
+  constexpr int WG = kDqWarps / G;        // warps per group
+  constexpr int DA = kASlots / G;         // A slots per group
   const int S = p.stages;
   const int bn = p.bn;
   const uint32_t tile_bytes = p.tile_bytes;
-  const uint32_t w_stage_bytes = (tile_bytes + 127u) & ~127u;
-  const uint32_t x_stage_bytes = static_cast<uint32_t>(bn) * 256u;  // two 128-byte-wide K halves
+  const uint32_t w_stage = (KPS * tile_bytes + 1023u) & ~1023u;
+  const uint32_t slab = static_cast<uint32_t>(bn) * 128u;  // bn rows x 64 K (128 bytes, swizzled)
+  const uint32_t x_stage = 2u * KPS * slab;
   uint8_t* w_st = smem;
-  uint8_t* x_st = smem + ((S * w_stage_bytes + 1023u) & ~1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(x_st + S * x_stage_bytes);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + S;
-  uint64_t* a_full = bars + 2 * S;
-  uint64_t* a_empty = a_full + kAStages;
-  uint64_t* acc_full = a_empty + kAStages;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* tear = acc_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tear + 1);
+  uint8_t* x_st = smem + S * w_stage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(x_st + S * x_stage);
+  uint64_t* empty = full + S;
+  uint64_t* a_full = empty + S;
+  uint64_t* a_empty = a_full + kASlots;
+  uint64_t* acc_full = a_empty + kASlots;
+  uint64_t* acc_empty = acc_full + DACC;
+  uint64_t* tear = acc_empty + DACC;
+  uint64_t* k_full = tear + 1;              // promotion: [ISS][kKRing]
+  uint64_t* k_empty = k_full + 2 * kKRing;  // promotion: [ISS][kKRing]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(k_empty + 2 * kKRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_tile_off = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_tok = reinterpret_cast<int*>(tmem_slot + 4);  // MoE: token of each row of the unit
+  int* s_tile_off = s_tok + (MOE ? BNMAX : 0);
   int* s_row_off = s_tile_off + (MOE ? p.num_experts + 1 : 0);
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = dev::lane_id();
+  if (threadIdx.x == 0) HQ_TRACE_CTA(0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      dev::mbar_init(&full[s], MOE ? 33u : 1u);
-      dev::mbar_init(&empty[s], kDqWarps + 1);
+      dev::mbar_init(&full[s], 1u);
+      dev::mbar_init(&empty[s], kDqWarps + ISS + (p.promote ? kEpiWarps : 0));
     }
-    for (int j = 0; j < kAStages; ++j) {
-      dev::mbar_init(&a_full[j], kDqWarps);
-      dev::mbar_init(&a_empty[j], 1);
+    for (int a = 0; a < kASlots; ++a) {
+      dev::mbar_init(&a_full[a], WG);
+      dev::mbar_init(&a_empty[a], 1);
     }
-    dev::mbar_init(acc_full, 1);
-    dev::mbar_init(acc_empty, kDqWarps);
-    dev::mbar_init(tear, 1);
+    for (int b = 0; b < DACC; ++b) {
+      dev::mbar_init(&acc_full[b], ISS);
+      dev::mbar_init(&acc_empty[b], kEpiWarps);
+    }
+    dev::mbar_init(tear, ISS);
+    for (int k = 0; k < 2 * kKRing; ++k) {
+      dev::mbar_init(&k_full[k], 1);
+      dev::mbar_init(&k_empty[k], kEpiWarps);
+    }
     *abort_flag = 0;
     dev::fence_barrier_init();
   }
+  if (warp == 0) {
+    dev::tmem_alloc(tmem_slot, kTmemCols);
+    dev::tmem_relinquish();
+  }
+  if (warp == kProdWarp && lane == 0) dev::prefetch_tmap(&tmap_x);
+  // everything above overlaps the previous grid; global data only after this
+  dev::grid_dep_wait();
+  dev::grid_dep_launch();
   if constexpr (MOE) {
     for (int i = threadIdx.x; i <= p.num_experts; i += blockDim.x) {
       s_tile_off[i] = p.tile_offsets[i];
       s_row_off[i] = p.expert_offsets[i];
     }
   }
-  if (warp == 1) {
-    dev::tmem_alloc(tmem_slot, C::kTmemCols);
-    dev::tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0 && !MOE) dev::prefetch_tmap(&tmap_x);
   dev::tc_fence_before();
   __syncthreads();
   dev::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  [[maybe_unused]] int tr0 = 0;
+  if (threadIdx.x == 0) HQ_TRACE(15, tr0, 0);
 
-  const int total = MOE ? s_tile_off[p.num_experts] * p.n_tiles : p.n_tiles * p.m_tiles * p.splits;
-  const uint8_t* tiles_base = p.tiles;
-
-  if (warp == 0) {
+  if (warp == kProdWarp) {
     // ============================================================ producer
-    int it = 0;
+    Sched<MOE> sc;
+    sc.init(p);
+    Ring rg;
+    int issued = 0;
     bool ok = true;
-    if (MOE || lane == 0) {
-      const uint64_t pol = dev::policy_evict_first();
-      for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
-        const Work wk = decode_work<MOE>(p, w, s_tile_off, s_row_off);
-        const uint8_t* wt = tiles_base + static_cast<uint64_t>(wk.e) * p.expert_stride +
-                            static_cast<uint64_t>(wk.nt) * p.k_tiles * tile_bytes;
-        // MoE: this lane's gathered activation rows (token index per row)
-        int tok[BN_MAX / 32 > 0 ? BN_MAX / 32 : 1];
-        if constexpr (MOE) {
-#pragma unroll
-          for (int q = 0; q < (BN_MAX / 32 > 0 ? BN_MAX / 32 : 1); ++q) {
-            const int r = static_cast<int>(lane) + 32 * q;
-            tok[q] = (r < wk.rows) ? p.perm[wk.row0 + r] / p.topk : -1;
-          }
-        }
-        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
-          bool got;
-          if constexpr (MOE) got = warp_wait(&empty[s], ph ^ 1u, abort_flag);
-          else got = dev::mbar_wait(&empty[s], ph ^ 1u, abort_flag);
-          if (!got) {
-            ok = false;
-            break;
-          }
-          uint8_t* xs = x_st + s * x_stage_bytes;
-          if (!MOE || lane == 0) {
-            dev::mbar_arrive_expect_tx(&full[s], tile_bytes + (MOE ? 0u : x_stage_bytes));
-            dev::bulk_load_hint(w_st + s * w_stage_bytes, wt + static_cast<uint64_t>(kb) * tile_bytes, tile_bytes,
-                                &full[s], pol);
-          }
-          if constexpr (!MOE) {
-            dev::tma_load_2d(xs, &tmap_x, &full[s], kb * kTileK, wk.row0);
-            dev::tma_load_2d(xs + bn * 128, &tmap_x, &full[s], kb * kTileK + 64, wk.row0);
-          } else {
-            __syncwarp();
-            // rows r = lane + 32q; 16 chunks of 16 bytes per row (two 128-byte K halves)
-#pragma unroll
-            for (int q = 0; q < (BN_MAX / 32 > 0 ? BN_MAX / 32 : 1); ++q) {
-              const int r = static_cast<int>(lane) + 32 * q;
-              if (r < bn && tok[q] >= 0) {
-                const __nv_bfloat16* src = x_rows + static_cast<int64_t>(tok[q]) * ldx + kb * kTileK;
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                  const int half = c >> 3, j = c & 7;
-                  uint8_t* dst = xs + half * bn * 128 + r * 128 + ((j ^ (r & 7)) << 4);
-                  // columns at or beyond K are zero-filled (source size 0)
-                  const uint32_t src_bytes = (kb * kTileK + half * 64 + j * 8 < p.k) ? 16u : 0u;
-                  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dev::smem_u32(dst)),
-                               "l"(src + (src_bytes ? half * 64 + j * 8 : 0)), "r"(src_bytes)
-                               : "memory");
-                }
-              }
-            }
-            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dev::smem_u32(&full[s]))
-                         : "memory");
-          }
-        }
+    const uint64_t pol = dev::policy_evict_first();
+    [[maybe_unused]] int tr = 0;
+    Unit u;
+    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+      const uint8_t* wt = p.tiles + static_cast<uint64_t>(u.e) * p.expert_stride +
+                          static_cast<uint64_t>(u.nt) * p.k_tiles * tile_bytes;
+      if constexpr (MOE) {
+        for (int r = static_cast<int>(lane); r < BNMAX; r += 32)
+          s_tok[r] = (r < u.rows) ? p.perm[u.row0 + r] / p.topk : p.m;  // p.m = T: out of range
+        __syncwarp();
       }
-      if (!ok) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
-      // drain: wait until every copy this warp issued has landed
-      if constexpr (MOE) asm volatile("cp.async.wait_all;" ::: "memory");
-      if (!MOE || lane == 0) {
-        for (int s = 0; s < S && s < it; ++s) {
-          const int last = ((it - 1 - s) / S) * S + s;
-          const uint32_t ph = (last / S) & 1;
-          const uint64_t t0 = dev::globaltimer();
-          while (!dev::mbar_try_wait(&full[s], ph) && dev::globaltimer() - t0 < dev::kWaitTimeoutNs) {
+      for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
+        const int cnt = min(KPS, u.kb1 - kb);
+        if (!warp_wait(&empty[rg.s], rg.ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) HQ_TRACE(0, tr, (1ull << 24) | issued);
+        uint8_t* xs = x_st + rg.s * x_stage;
+        if (lane == 0) {
+          const uint32_t wbytes = static_cast<uint32_t>(cnt) * tile_bytes;
+          dev::mbar_arrive_expect_tx(&full[rg.s], wbytes + 2u * cnt * slab);
+          dev::bulk_load_hint(w_st + rg.s * w_stage, wt + static_cast<uint64_t>(kb) * tile_bytes, wbytes,
+                              &full[rg.s], pol);
+          if constexpr (!MOE) {
+            // one 64-column slab of bn rows per copy; columns past K and rows
+            // past M are zero-filled by the tensor copy
+            for (int z = 0; z < 2 * cnt; ++z)
+              dev::tma_load_2d(xs + z * slab, &tmap_x, &full[rg.s], (2 * kb + z) * 64, u.row0);
           }
+        }
+        if constexpr (MOE) {
+          // gathered rows, four per tensor copy (one-row boxes); rows past the
+          // unit and columns past K are out of range and zero-filled
+          if (lane == 0) {
+            for (int z = 0; z < 2 * cnt; ++z) {
+              const int x = (2 * kb + z) * 64;
+              for (int r = 0; r < bn; r += 4)
+                dev::tma_gather4(xs + z * slab + r * 128, &tmap_x, &full[rg.s], x, s_tok[r], s_tok[r + 1],
+                                 s_tok[r + 2], s_tok[r + 3]);
+            }
+          }
+        }
+        rg.next(S);
+        ++issued;
+      }
+    }
+    if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
+    // drain: every copy this warp issued has landed before the CTA can exit
+    if (lane == 0) {
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int last = ((issued - 1 - s) / S) * S + s;
+        const uint32_t ph = (last / S) & 1;
+        const uint64_t t0 = dev::globaltimer();
+        while (!dev::mbar_try_wait(&full[s], ph) && dev::globaltimer() - t0 < dev::kWaitTimeoutNs) {
         }
       }
     }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
+  } else if (warp >= kIssWarp0) {
+    // ============================================================ MMA issuers
+    const int pidx = warp - kIssWarp0;
     if (lane == 0) {
-      int it = 0, ia = 0, item = 0;
-      bool ok = true;
+      if (CLS == 0 && p.promote) {
+        // one accumulator per K-block in a ring of kKRing; the epilogue
+        // applies the K-block's scale in fp32 and sums in K order
+        Sched<MOE> sc;
+        sc.init(p);
+        Ring rg;
+        uint32_t cu = 0, ck = 0;
+        const uint32_t idesc = p.idesc;
+        bool ok = true;
+        Unit u;
+        while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+          for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
+            const int cnt = min(KPS, u.kb1 - kb);
+            if (!dev::mbar_wait(&full[rg.s], rg.ph, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (pidx < cnt) {
+              const int slot = pidx * DA + static_cast<int>(cu % DA);
+              const int ks = pidx * kKRing + static_cast<int>(ck % kKRing);
+              if (!dev::mbar_wait(&a_full[slot], (cu / DA) & 1u, abort_flag) ||
+                  !dev::mbar_wait(&k_empty[ks], ((ck / kKRing) & 1u) ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+              }
+              dev::tc_fence_after();
+              const uint32_t xs = dev::smem_u32(x_st + rg.s * x_stage) + 2u * pidx * slab;
+              const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(slot) * 64u;
+              const uint32_t d_tmem = tmem + kAccCol0 + static_cast<uint32_t>(ks * BNMAX);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t bdesc = dev::sw128_desc(xs + (kk >> 2) * slab + (kk & 3) * 32);
+                dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk == 0 ? 0u : 1u);
+              }
+              dev::tc_commit(&a_empty[slot]);
+              dev::tc_commit(&k_full[ks]);
+              ++cu;
+              ++ck;
+            }
+            dev::tc_commit(&empty[rg.s]);
+            rg.next(S);
+          }
+        }
+        if (!ok) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
+        dev::tc_commit(tear);
+      } else {
+      Sched<MOE> sc;
+      sc.init(p);
+      Ring rg;
+      uint32_t cu = 0;  // uses of this issuer's group's A ring
       const uint32_t idesc = p.idesc;
-      for (int w = blockIdx.x; ok && w < total; w += gridDim.x, ++item) {
-        const Work wk = decode_work<MOE>(p, w, s_tile_off, s_row_off);
-        if (!dev::mbar_wait(acc_empty, (item & 1) ^ 1u, abort_flag)) {
+      bool ok = true;
+      int ui = 0;
+      [[maybe_unused]] int tr = 0, ts = 0;
+      Unit u;
+      while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+        const int buf = DACC == 1 ? 0 : (ui & 1);
+        const uint32_t accph = static_cast<uint32_t>(DACC == 1 ? ui : (ui >> 1)) & 1u;
+        if (!dev::mbar_wait(&acc_empty[buf], accph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         dev::tc_fence_after();
-        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it, ++ia) {
-          const int s = it % S;
-          const int j = ia % kAStages;
-          if (!dev::mbar_wait(&full[s], (it / S) & 1, abort_flag) ||
-              !dev::mbar_wait(&a_full[j], (ia / kAStages) & 1, abort_flag)) {
+        const uint32_t d_tmem = tmem + kAccCol0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
+        bool first = true;
+        for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
+          const int cnt = min(KPS, u.kb1 - kb);
+          if (!dev::mbar_wait(&full[rg.s], rg.ph, abort_flag)) {
             ok = false;
             break;
           }
-          if constexpr (MOE) dev::fence_proxy_async_smem();  // cp.async rows -> tensor-core reads
-          dev::tc_fence_after();
-          const uint32_t xs = dev::smem_u32(x_st + s * x_stage_bytes);
+          HQ_TRACE(1 + pidx, tr, (2ull << 24) | ts);
+          if (pidx < cnt) {
+            const int slot = pidx * DA + static_cast<int>(cu % DA);
+            if (!dev::mbar_wait(&a_full[slot], (cu / DA) & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
+            dev::tc_fence_after();
+            const uint32_t xs = dev::smem_u32(x_st + rg.s * x_stage) + 2u * pidx * slab;
+            const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(slot) * 64u;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bdesc = dev::sw128_desc(xs + (kk >> 2) * bn * 128 + (kk & 3) * 32);
-            dev::mma_f16_ts(tmem + C::kAccCol, tmem + C::kACol + j * 64 + kk * 8, bdesc, idesc,
-                            (kb > wk.kb0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bdesc = dev::sw128_desc(xs + (kk >> 2) * slab + (kk & 3) * 32);
+              dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
+            }
+            dev::tc_commit(&a_empty[slot]);
+            ++cu;
           }
-          dev::tc_commit(&empty[s]);
-          dev::tc_commit(&a_empty[j]);
+          dev::tc_commit(&empty[rg.s]);
+          HQ_TRACE(1 + pidx, tr, (4ull << 24) | ts);
+          ++ts;
+          rg.next(S);
+          first = false;
         }
         if (!ok) break;
-        dev::tc_commit(acc_full);
+        dev::tc_commit(&acc_full[buf]);
+        ++ui;
       }
       if (!ok) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
-      // drain: all MMAs issued by this thread complete before TMEM is freed
-      dev::tc_commit(tear);
-      const uint64_t t0 = dev::globaltimer();
-      while (!dev::mbar_try_wait(tear, 0) && dev::globaltimer() - t0 < dev::kWaitTimeoutNs) {
+      dev::tc_commit(tear);  // arrives once every MMA this thread issued has completed
       }
     }
-  } else {
-    // ============================================================ dequant + epilogue
-    const int dq = warp - 2;            // 0..7
-    const int quarter = warp & 3;       // TMEM lane quarter this warp may access
-    const int half = dq >> 2;           // which two 32-column chunks of each K block
+  } else if (warp >= kDqWarp0) {
+    // ============================================================ dequantisers
+    const int dw = warp - kDqWarp0;
+    const int gi = dw / WG;                 // group = position within each stage
+    const int quarter = warp & 3;
+    const int sub = (dw % WG) >> 2;         // which G chunks of the 4 this warp converts
     const int r = quarter * 32 + static_cast<int>(lane);  // weight row within the tile (TMEM lane)
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    int it = 0, ia = 0, item = 0;
+    const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol0;
+    Sched<MOE> sc;
+    sc.init(p);
+    Ring rg;
+    uint32_t ca = 0;
+    int pend = -1;  // A slot whose stores were issued but not yet published
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < total; w += gridDim.x, ++item) {
-      const Work wk = decode_work<MOE>(p, w, s_tile_off, s_row_off);
-      const int n = wk.nt * kTileN + r;
+    [[maybe_unused]] int tr = 0, ts = 0;
+    const bool trace_me = (dw % WG) == 0 && lane == 0;
+    Unit u;
+    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+      const int n = u.nt * kTileN + r;
       uint32_t zrow = static_cast<uint32_t>(p.zero_sym);
-      if (p.channel && p.has_zeros) zrow = p.row_zero[static_cast<size_t>(wk.e) * p.n_pad + n];
-      for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it, ++ia) {
-        const int s = it % S;
-        if (!warp_wait(&full[s], (it / S) & 1, abort_flag)) {
+      if (p.channel && p.has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
+      for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
+        const int cnt = min(KPS, u.kb1 - kb);
+        if (!warp_wait(&full[rg.s], rg.ph, abort_flag)) {
           ok = false;
           break;
         }
-        const uint8_t* wsm = w_st + s * w_stage_bytes;
-        uint4 qc[2];
-        uint2 qh[2];
-        uint32_t c2[2], s2[2];
+        if (trace_me) HQ_TRACE(5 + gi, tr, (5ull << 24) | ts);
+        const bool real = gi < cnt;
+        uint4 qc[G];
+        uint2 qh[G];
+        uint32_t zz[G], ss[G];
+        if (real) {
+          const uint8_t* wsm = w_st + rg.s * w_stage + gi * tile_bytes;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * half + cc;
-          qc[cc] = *reinterpret_cast<const uint4*>(wsm + (c * kTileN + r) * 16);
-          if constexpr (FMT == static_cast<int>(WFmt::INT6))
-            qh[cc] = *reinterpret_cast<const uint2*>(wsm + p.hi_off + (c * kTileN + r) * 8);
-          if constexpr (FMT == static_cast<int>(WFmt::MXFP4)) {
-            s2[cc] = wsm[p.scale_off + r * 4 + c];
-            c2[cc] = 0;
-          } else {
-            uint32_t z = zrow;
-            uint32_t sc = 0;
-            if (!p.channel) {
-              const int g = (p.g_kb > 1) ? (32 * c) / p.group_k : 0;
-              sc = reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r * p.g_kb + g];
-              if (p.has_zeros) z = wsm[p.zero_off + r * p.g_kb + g];
+          for (int i = 0; i < G; ++i) {
+            const int c = sub * G + i;
+            qc[i] = *reinterpret_cast<const uint4*>(wsm + (c * kTileN + r) * 16);
+            if constexpr (FMT == static_cast<int>(WFmt::INT6))
+              qh[i] = *reinterpret_cast<const uint2*>(wsm + p.hi_off + (c * kTileN + r) * 8);
+            if constexpr (FMT == static_cast<int>(WFmt::MXFP4)) {
+              ss[i] = wsm[p.scale_off + r * 4 + c];
+              zz[i] = 0;
+            } else {
+              zz[i] = zrow;
+              ss[i] = 0;
+              if (!p.channel) {
+                const int g = (p.g_kb > 1) ? (32 * c) / p.group_k : 0;
+                ss[i] = reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r * p.g_kb + g];
+                if (p.has_zeros) zz[i] = wsm[p.zero_off + r * p.g_kb + g];
+              }
             }
-            c2[cc] = (magic_half<BF16>() + z) * 0x00010001u;
-            s2[cc] = sc * 0x00010001u;
           }
+        }
+        // publish the previous K-block's A slot while this stage's loads land
+        if (trace_me) HQ_TRACE(5 + gi, tr, (11ull << 24) | ts);
+        if (pend >= 0) {
+          dev::tmem_st_wait();
+          if (trace_me) HQ_TRACE(5 + gi, tr, (12ull << 24) | ts);
+          dev::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) dev::mbar_arrive(&a_full[pend]);
+          pend = -1;
         }
         __syncwarp();
-        if (lane == 0) dev::mbar_arrive(&empty[s]);
-        const int j = ia % kAStages;
-        if (!warp_wait(&a_empty[j], ((ia / kAStages) & 1) ^ 1u, abort_flag)) {
+        if (lane == 0) dev::mbar_arrive(&empty[rg.s]);
+        if (trace_me) HQ_TRACE(5 + gi, tr, (13ull << 24) | ts);
+        if (real) {
+          const int slot = gi * DA + static_cast<int>(ca % DA);
+          if (!warp_wait(&a_empty[slot], ((ca / DA) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (trace_me) HQ_TRACE(5 + gi, tr, (6ull << 24) | ts);
+          dev::tc_fence_after();
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            const int c = sub * G + i;
+            uint32_t o[16];
+            if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
+              if (p.channel || p.promote) dq_int4<BF16, false>(qc[i], zz[i], ss[i], o);
+              else dq_int4<BF16, true>(qc[i], zz[i], ss[i], o);
+            } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
+              const uint32_t c2 = (magic_half<BF16>() + zz[i]) * 0x00010001u;
+              if (p.channel || p.promote) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o);
+              else dq_int6<BF16, true>(qc[i], qh[i], c2, ss[i] * 0x00010001u, o);
+            } else {
+              dq_mxfp4(qc[i], ss[i], o);
+            }
+            dev::tmem_st16(a_lane + slot * 64 + c * 16, o);
+          }
+          pend = slot;
+          if (trace_me) HQ_TRACE(5 + gi, tr, (7ull << 24) | ts);
+          ++ca;
+        }
+        ++ts;
+        rg.next(S);
+      }
+    }
+    if (pend >= 0) {
+      dev::tmem_st_wait();
+      dev::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&a_full[pend]);
+    }
+    if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
+  } else {
+    // ============================================================ epilogue
+    const int quarter = warp;
+    const int r = quarter * 32 + static_cast<int>(lane);
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    Sched<MOE> sc;
+    sc.init(p);
+    bool ok = true;
+    int ui = 0;
+    [[maybe_unused]] Ring rg;       // promotion: stage ring position
+    [[maybe_unused]] uint32_t ck[2] = {0, 0};  // promotion: K-blocks taken from each issuer's ring
+    [[maybe_unused]] int tr = 0;
+    const bool trace_me = quarter == 0 && lane == 0;
+    // INT4 bf16 operands without a folded scale carry an extra 2^-7
+    constexpr float kOpFix = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
+    Unit u;
+    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+      const int n = u.nt * kTileN + r;
+      const bool n_ok = n < p.n;
+      const float rs = (p.channel && n_ok) ? p.row_scale[static_cast<size_t>(u.e) * p.n_pad + n] * kOpFix : 1.f;
+      const bool partial = !MOE && p.stream_k && (u.kb0 > 0 || u.kb1 < p.k_tiles);
+      float* pslot = partial ? p.partials + static_cast<size_t>(2 * blockIdx.x + (ui == 0 ? 0 : 1)) * bn * kTileN
+                             : nullptr;
+      // columns [16 ch, 16 ch + 16) of this row: partial, MoE row or Y
+      auto emit16 = [&](int ch, const float (&v)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int col = ch * 16 + i;
+          if (col >= u.rows) continue;
+          if (partial) {
+            pslot[static_cast<size_t>(col) * kTileN + r] = v[i];
+          } else if (n_ok) {
+            if constexpr (MOE) {
+              const int f = p.perm[u.row0 + col];
+              p.zbuf[static_cast<size_t>(f) * p.n_pad + n] = v[i] * rs * p.topk_w[f];
+            } else {
+              const size_t off = static_cast<size_t>(u.row0 + col) * p.ldy + n;
+              if constexpr (BF16) reinterpret_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(v[i] * rs);
+              else reinterpret_cast<__half*>(p.y)[off] = __float2half_rn(v[i] * rs);
+            }
+          }
+        }
+      };
+      bool promoted = false;
+      if constexpr (CLS == 0) {
+        if (p.promote) {
+          promoted = true;
+          // sum the unit's per-K-block accumulators in K order, each times its
+          // group scale (read from the stage before releasing it)
+          float tot[BNMAX];
+#pragma unroll
+          for (int i = 0; i < BNMAX; ++i) tot[i] = 0.f;
+          for (int kb = u.kb0; ok && kb < u.kb1; kb += KPS) {
+            const int cnt = min(KPS, u.kb1 - kb);
+            if (!warp_wait(&full[rg.s], rg.ph, abort_flag)) {
+              ok = false;
+              break;
+            }
+            float sk[KPS];
+#pragma unroll
+            for (int q = 0; q < KPS; ++q) {
+              sk[q] = 0.f;
+              if (q < cnt) {
+                const uint32_t s16 =
+                    *reinterpret_cast<const uint16_t*>(w_st + rg.s * w_stage + q * tile_bytes + p.scale_off + r * 2);
+                const float sf = BF16 ? __uint_as_float(s16 << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(s16)));
+                sk[q] = sf * kOpFix;
+              }
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(&empty[rg.s]);
+            rg.next(S);
+            for (int q = 0; q < cnt; ++q) {
+              const int ks = q * kKRing + static_cast<int>(ck[q] % kKRing);
+              if (!warp_wait(&k_full[ks], (ck[q] / kKRing) & 1u, abort_flag)) {
+                ok = false;
+                break;
+              }
+              dev::tc_fence_after();
+              const uint32_t acc = tmem + lane_base + kAccCol0 + static_cast<uint32_t>(ks * BNMAX);
+#pragma unroll
+              for (int ch = 0; ch < BNMAX / 16; ++ch) {
+                if (ch * 16 < bn) {
+                  uint32_t a[16];
+                  dev::tmem_ld16(acc + ch * 16, a);
+                  dev::tmem_ld_wait();
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) tot[ch * 16 + i] = fmaf(sk[q], __uint_as_float(a[i]), tot[ch * 16 + i]);
+                }
+              }
+              dev::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) dev::mbar_arrive(&k_empty[ks]);
+              ++ck[q];
+            }
+          }
+          if (!ok) break;
+#pragma unroll
+          for (int ch = 0; ch < BNMAX / 16; ++ch) {
+            if (ch * 16 < bn) {
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = tot[ch * 16 + i];
+              emit16(ch, v);
+            }
+          }
+        }
+      }
+      if (!promoted) {
+        const int buf = DACC == 1 ? 0 : (ui & 1);
+        const uint32_t accph = static_cast<uint32_t>(DACC == 1 ? ui : (ui >> 1)) & 1u;
+        if (!warp_wait(&acc_full[buf], accph, abort_flag)) {
           ok = false;
           break;
         }
+        if (trace_me) HQ_TRACE(9, tr, (8ull << 24) | ui);
         dev::tc_fence_after();
+        const int nval = min(ISS, u.kb1 - u.kb0);  // issuers that took at least one K-block
+        const uint32_t acc0 = tmem + lane_base + kAccCol0 + static_cast<uint32_t>(buf * ISS * BNMAX);
+        for (int ch = 0; ch < (bn >> 4); ++ch) {
+          float v[16];
+          {
+            uint32_t a[16];
+            dev::tmem_ld16(acc0 + ch * 16, a);
+            dev::tmem_ld_wait();
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * half + cc;
-          uint32_t o[16];
-          if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
-            if (p.channel) dq_int4<BF16, false>(qc[cc], c2[cc], 0, o);
-            else dq_int4<BF16, true>(qc[cc], c2[cc], s2[cc], o);
-          } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
-            if (p.channel) dq_int6<BF16, false>(qc[cc], qh[cc], c2[cc], 0, o);
-            else dq_int6<BF16, true>(qc[cc], qh[cc], c2[cc], s2[cc], o);
-          } else {
-            dq_mxfp4(qc[cc], s2[cc], o);
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(a[i]);
           }
-          dev::tmem_st16(tmem + lane_base + C::kACol + j * 64 + c * 16, o);
+          for (int is = 1; is < nval; ++is) {
+            uint32_t a[16];
+            dev::tmem_ld16(acc0 + is * BNMAX + ch * 16, a);
+            dev::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] += __uint_as_float(a[i]);
+          }
+          emit16(ch, v);
         }
-        dev::tmem_st_wait();
         dev::tc_fence_before();
         __syncwarp();
-        if (lane == 0) dev::mbar_arrive(&a_full[j]);
+        if (lane == 0) dev::mbar_arrive(&acc_empty[buf]);
+        if (trace_me) HQ_TRACE(9, tr, (9ull << 24) | ui);
       }
-      if (!ok) break;
-
-      // ---------------------------------------------------------- epilogue
-      if (!warp_wait(acc_full, item & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      dev::tc_fence_after();
-      const bool n_ok = n < p.n;
-      const float rs = (p.channel && n_ok) ? p.row_scale[static_cast<size_t>(wk.e) * p.n_pad + n] : 1.f;
-      const int nchunks = bn >> 4;
-      if constexpr (MOE) {
-        for (int ch = half; ch < nchunks; ch += 2) {
-          uint32_t v[16];
-          dev::tmem_ld16(tmem + lane_base + C::kAccCol + ch * 16, v);
-          dev::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = ch * 16 + i;
-            if (col < wk.rows && n_ok) {
-              const int f = p.perm[wk.row0 + col];
-              p.zbuf[static_cast<size_t>(f) * p.n_pad + n] = __uint_as_float(v[i]) * rs * p.topk_w[f];
-            }
-          }
-        }
-      } else if (p.splits == 1) {
-        for (int ch = half; ch < nchunks; ch += 2) {
-          uint32_t v[16];
-          dev::tmem_ld16(tmem + lane_base + C::kAccCol + ch * 16, v);
-          dev::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = ch * 16 + i;
-            if (col < wk.rows && n_ok) {
-              const float f = __uint_as_float(v[i]) * rs;
-              const size_t off = static_cast<size_t>(wk.row0 + col) * p.ldy + n;
-              if constexpr (BF16) reinterpret_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(f);
-              else reinterpret_cast<__half*>(p.y)[off] = __float2half_rn(f);
-            }
-          }
-        }
-      } else {
-        // split-K: store this split's fp32 partial, then the last of the
-        // `splits` warps covering the same (rows, columns) slice sums all
-        // partials in split order (deterministic) and writes Y.
-        for (int ch = half; ch < nchunks; ch += 2) {
-          uint32_t v[16];
-          dev::tmem_ld16(tmem + lane_base + C::kAccCol + ch * 16, v);
-          dev::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = ch * 16 + i;
-            if (col < wk.rows)
-              p.partials[(static_cast<size_t>(wk.split) * p.m + wk.row0 + col) * p.n_pad + n] = __uint_as_float(v[i]);
-          }
-        }
+      if (partial) {
+        // the last of the tile's CTAs sums every partial in CTA (= K) order
         __threadfence();
         __syncwarp();
-        int* ctr = p.counters + ((wk.mt * p.n_tiles + wk.nt) * kDqWarps + dq);
+        const long long T = p.iters;
+        const int Gc = static_cast<int>(gridDim.x);
+        const long long x0 = static_cast<long long>(u.tile) * p.k_tiles;
+        const int cf = sk_cta_of(x0, T, Gc);
+        const int cl = sk_cta_of(x0 + p.k_tiles - 1, T, Gc);
+        int* ctr = p.counters + u.tile * 4 + quarter;
         int last = 0;
-        if (lane == 0) last = (atomicAdd(ctr, 1) == p.splits - 1) ? 1 : 0;
+        if (lane == 0) last = (atomicAdd(ctr, 1) == cl - cf) ? 1 : 0;
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           __threadfence();
-          for (int ch = half; ch < nchunks; ch += 2) {
-            uint32_t v[16];
-            dev::tmem_ld16(tmem + lane_base + C::kAccCol + ch * 16, v);
-            dev::tmem_ld_wait();
+          // 8 columns at a time, contributors summed in CTA order
+          for (int ch = 0; ch * 8 < u.rows; ++ch) {
+            float v[8];
+            for (int c = cf; c <= cl; ++c) {
+              const long long begin = static_cast<long long>(c) * T / Gc;
+              const int slot = 2 * c + (begin >= x0 ? 0 : 1);
+              const float* src = p.partials + (static_cast<size_t>(slot) * bn + ch * 8) * kTileN + r;
+              float t[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int col = ch * 16 + i;
-              if (col < wk.rows && n_ok) {
-                float acc = 0.f;
-                for (int sp = 0; sp < p.splits; ++sp) {
-                  const float part = (sp == wk.split)
-                                         ? __uint_as_float(v[i])
-                                         : __ldcg(&p.partials[(static_cast<size_t>(sp) * p.m + wk.row0 + col) * p.n_pad + n]);
-                  acc = (sp == 0) ? part : acc + part;
+              for (int i = 0; i < 8; ++i) t[i] = __ldcg(src + i * kTileN);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] = (c == cf) ? t[i] : v[i] + t[i];
+            }
+            if (n_ok) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int col = ch * 8 + i;
+                if (col < u.rows) {
+                  const size_t off = static_cast<size_t>(u.row0 + col) * p.ldy + n;
+                  if constexpr (BF16) reinterpret_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(v[i] * rs);
+                  else reinterpret_cast<__half*>(p.y)[off] = __float2half_rn(v[i] * rs);
                 }
-                const float f = acc * rs;
-                const size_t off = static_cast<size_t>(wk.row0 + col) * p.ldy + n;
-                if constexpr (BF16) reinterpret_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(f);
-                else reinterpret_cast<__half*>(p.y)[off] = __float2half_rn(f);
               }
             }
           }
           if (lane == 0) *ctr = 0;  // ready for the next call
         }
+        if (trace_me) HQ_TRACE(9, tr, ((10ull + last) << 24) | ui);
       }
-      dev::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) dev::mbar_arrive(acc_empty);
+      ++ui;
     }
-    if (!ok) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
+    if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
   }
 
+  // ---------------------------------------------------------------- teardown
   dev::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (threadIdx.x == 0) HQ_TRACE(15, tr0, 1);
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t t0 = dev::globaltimer();
+      while (!dev::mbar_try_wait(tear, 0) && dev::globaltimer() - t0 < dev::kWaitTimeoutNs) {
+      }
+    }
     __syncwarp();
     dev::tc_fence_after();
-    dev::tmem_dealloc(tmem, C::kTmemCols);
+    dev::tmem_dealloc(tmem, kTmemCols);
+    if (lane == 0) HQ_TRACE_CTA(1);
   }
 }
 
-// Dynamic shared memory bytes for a launch.
+// Dynamic shared memory bytes for a launch of class CLS.
+template <int CLS>
 inline uint32_t smem_bytes(int stages, uint32_t tile_bytes, int bn, int num_experts) {
-  const uint32_t w = static_cast<uint32_t>(stages) * ((tile_bytes + 127u) & ~127u);
-  const uint32_t x = static_cast<uint32_t>(stages) * static_cast<uint32_t>(bn) * 256u;
-  const uint32_t bars = (2u * stages + 2u * kAStages + 3u) * 8u + 16u + 8u * (num_experts + 1);
-  return ((w + 1023u) & ~1023u) + x + bars + 1024u /* alignment slack */;
+  using C = Cls<CLS>;
+  const uint32_t w = static_cast<uint32_t>(stages) * ((C::kKps * tile_bytes + 1023u) & ~1023u);
+  const uint32_t x = static_cast<uint32_t>(stages) * 2u * C::kKps * static_cast<uint32_t>(bn) * 128u;
+  const uint32_t bars = (2u * stages + 2u * kASlots + 2u * C::kDacc + 1u + 4u * kKRing) * 8u + 16u;
+  const uint32_t moe = 4u * (C::kBnMax + 2u * (num_experts + 1));
+  return w + x + bars + moe + 1024u /* alignment slack */;
 }
 
 }  // namespace wna16

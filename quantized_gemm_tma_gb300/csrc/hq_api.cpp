@@ -340,9 +340,9 @@ constexpr int kMaxSplitTiles = 512;
 constexpr size_t kCounterBytes = sizeof(int) * kMaxSplitTiles * 8;
 
 struct DensePlan {
-  int bn, bn_max, m_tiles, splits, kb_per_split, stages, grid;
+  int cls, bn, m_tiles, tiles, stages, groups, grid, stream_k;
+  long long iters;
   uint32_t smem;
-  int min_blocks;
 };
 
 // FP8: 128 tokens per tile (MMA M), 128 or 256 weight rows (MMA N), split-K
@@ -381,49 +381,51 @@ Fp8Plan plan_fp8(const Layout& L, int m, int sms, size_t smem_optin, uint32_t fl
 // (8 counters per split tile, at most kMaxSplitTiles tiles), then the fp32
 // partials.  The fixed offset keeps one problem's partials off another
 // problem's counters when a workspace is reused across shapes.
+// Stream-K scratch: the counter region, then a head and a tail partial
+// [bn][128] fp32 per CTA.
+size_t streamk_bytes(int grid, int bn) {
+  return kCounterBytes + align_up(sizeof(float) * 2ull * grid * bn * kTileN, kAlign);
+}
+
 size_t splitk_bytes(int splits, int m, int n_pad) {
   if (splits <= 1) return 0;
   return kCounterBytes + align_up(sizeof(float) * static_cast<size_t>(splits) * m * n_pad, kAlign);
 }
 
-// Heuristic for one GB300: tokens per tile from M, then split-K until the
-// (n-tile, m-tile, split) work items fill the SMs, with at least 4 K-tiles
-// per split so the fp32 partial traffic stays small next to the weights.
+// Shared-memory stages for a tile-width class: as many as fit (2..8); the
+// dequantiser groups equal the class's K-blocks per stage.
+void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_optin, int* stages, int* groups) {
+  const size_t cap = std::min<size_t>(smem_optin, 232448);
+  int smax = 1;
+  for (int st = 2; st <= 8; ++st)
+    if (wna16_smem_bytes(cls, st, L.tile_bytes, bn, num_experts) <= cap) smax = st;
+  *stages = smax;
+  *groups = wna16_kps(cls);
+}
+
+int wna16_class(int bn) { return bn <= 16 ? 0 : (bn <= 64 ? 1 : (bn <= 128 ? 2 : 3)); }
+
+// Heuristic for one GB300: tokens per tile from M; problems with fewer than
+// four tiles per SM are split stream-K so every SM streams the same number
+// of weight K-blocks.
 DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_t flags) {
   DensePlan p{};
-  if (m <= 64) {
-    p.bn_max = 64;
-    p.bn = std::max(16, cdiv(m, 16) * 16);
-  } else {
-    p.bn_max = 256;
-    p.bn = m <= 128 ? 128 : (m <= 192 ? 192 : 256);
-  }
+  p.bn = m <= 64 ? std::max(16, cdiv(m, 16) * 16) : (m <= 128 ? 128 : (m <= 192 ? 192 : 256));
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
-  if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) {
-    p.bn = forced_bn;
-    p.bn_max = forced_bn <= 64 ? 64 : 256;
-  }
+  if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) p.bn = forced_bn;
+  p.cls = wna16_class(p.bn);
   p.m_tiles = cdiv(m, p.bn);
-  const int tiles = p.m_tiles * L.n_tiles;
-  p.min_blocks = wna16_min_blocks(p.bn_max);
-  const int slots = sms * p.min_blocks;
-  int splits = 1;
-  if (!(flags & HQ_FLAG_BATCH_INVARIANT) && tiles < slots) {
-    splits = std::min(std::max(1, slots / tiles), std::max(1, L.k_tiles / 4));
-  }
-  const int forced = env_int("HQ_FORCE_SPLITK", 0);
-  if (forced > 0 && !(flags & HQ_FLAG_BATCH_INVARIANT)) splits = std::min(forced, L.k_tiles);
-  splits = std::min(splits, kMaxSplits);
-  if (tiles > kMaxSplitTiles) splits = 1;
-  p.kb_per_split = cdiv(L.k_tiles, splits);
-  p.splits = cdiv(L.k_tiles, p.kb_per_split);  // every split gets >= 1 K-tile
-  const size_t budget = std::min<size_t>(smem_optin, 232448 / p.min_blocks) - 2048;
-  const uint32_t per_stage = ((L.tile_bytes + 127u) & ~127u) + static_cast<uint32_t>(p.bn) * 256u;
-  p.stages = static_cast<int>(std::min<size_t>(8, budget / per_stage));
-  p.stages = std::max(p.stages, 2);
-  p.smem = wna16_smem_bytes(p.stages, L.tile_bytes, p.bn, 0);
-  const int items = tiles * p.splits;
-  p.grid = std::min(items, slots);
+  p.tiles = p.m_tiles * L.n_tiles;
+  p.iters = static_cast<long long>(p.tiles) * L.k_tiles;
+  p.stream_k = !(flags & HQ_FLAG_BATCH_INVARIANT) && p.tiles < 4 * sms && p.tiles <= kMaxSplitTiles && L.k_tiles > 1;
+  const int forced_sk = env_int("HQ_FORCE_SPLITK", 0);  // 1: stream-K on, 2: off
+  if (forced_sk == 1 && !(flags & HQ_FLAG_BATCH_INVARIANT) && p.tiles <= kMaxSplitTiles) p.stream_k = 1;
+  if (forced_sk == 2) p.stream_k = 0;
+  plan_stages(p.cls, L, p.bn, 0, smem_optin, &p.stages, &p.groups);
+  p.smem = wna16_smem_bytes(p.cls, p.stages, L.tile_bytes, p.bn, 0);
+  // stream-K: at least 8 K-blocks per CTA, so that partial tiles stay few
+  p.grid = p.stream_k ? static_cast<int>(std::min<long long>(sms, std::max<long long>(1, (p.iters + 7) / 8)))
+                      : std::min(sms, p.tiles);
   return p;
 }
 
@@ -448,7 +450,7 @@ hq_status hq_gemm_workspace_size(const hq_weight_desc* desc, int32_t m, int32_t 
         best = std::max(best, splitk_bytes(p.splits, m, L.n_pad));
       } else {
         const DensePlan p = plan_wna16(L, m, sms, 232448, 0);
-        best = std::max(best, splitk_bytes(p.splits, m, L.n_pad));
+        if (p.stream_k) best = std::max(best, streamk_bytes(p.grid, p.bn));
       }
     }
     ws += best;
@@ -511,7 +513,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
     CUtensorMap tm;
     st = encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, x, L.k, m, ldx, 128, 128);
     if (st != HQ_OK) return st;
-    g_last_plan = hq_plan_info{pl.bn, pl.splits, pl.grid, 1, pl.stages, {0, 0, 0}};
+    g_last_plan = hq_plan_info{pl.bn, pl.splits, pl.grid, 1, pl.stages, 0, 0, 0};
     if (env_int("HQ_TRACE", 0))
       std::fprintf(stderr, "hq_gemm fp8: m=%d n=%d k=%d bn=%d splits=%d grid=%d stages=%d smem=%u\n", m, L.n, L.k,
                    pl.bn, pl.splits, pl.grid, pl.stages, pl.smem);
@@ -519,7 +521,8 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   }
 
   const DensePlan pl = plan_wna16(L, m, di.sms, di.smem_optin, flags);
-  if (ws_bytes < kAlign + splitk_bytes(pl.splits, m, L.n_pad)) return HQ_ERR_WORKSPACE_TOO_SMALL;
+  if (pl.stages < 2) return HQ_ERR_UNSUPPORTED;
+  if (ws_bytes < kAlign + (pl.stream_k ? streamk_bytes(pl.grid, pl.bn) : 0)) return HQ_ERR_WORKSPACE_TOO_SMALL;
   GemmParams p{};
   p.tiles = wt + L.tiles_off;
   p.expert_stride = L.expert_stride;
@@ -529,15 +532,17 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   p.row_scale = L.channel ? reinterpret_cast<const float*>(wt + L.row_off) : nullptr;
   p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
   p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = m;
-  p.bn = pl.bn; p.m_tiles = pl.m_tiles; p.splits = pl.splits; p.kb_per_split = pl.kb_per_split;
-  p.stages = pl.stages; p.a_stages = kWna16AStages;
+  p.bn = pl.bn; p.m_tiles = pl.m_tiles; p.num_tiles = pl.tiles;
+  p.stages = pl.stages; p.groups = pl.groups;
+  p.stream_k = pl.stream_k; p.iters = pl.iters;
+  p.promote = (pl.cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
   p.idesc = idesc_f16(atype == HQ_A_BF16, 128, pl.bn);
   p.y = y; p.ldy = ldy;
   p.status = reinterpret_cast<int*>(ws);
-  static_assert(kWna16DqWarps <= 8, "counter region holds 8 counters per split tile");
   p.counters = reinterpret_cast<int*>(ws + kAlign);
   p.partials = reinterpret_cast<float*>(ws + kAlign + kCounterBytes);
   p.num_experts = 1;
+  // X [M][K]: one box = 64 columns (128 bytes, swizzled) of bn rows
   CUtensorMap tm;
   st = encode_2d(&tm, atype == HQ_A_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x,
                  L.k, m, ldx, 64, pl.bn);
@@ -545,14 +550,14 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   Wna16Launch l{};
   l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
   l.bf16 = atype == HQ_A_BF16;
-  l.bn_max = pl.bn_max;
+  l.cls = pl.cls;
   l.moe = false;
   l.grid = pl.grid;
   l.smem = pl.smem;
-  g_last_plan = hq_plan_info{pl.bn, pl.splits, pl.grid, 1, pl.stages, {0, 0, 0}};
+  g_last_plan = hq_plan_info{pl.bn, pl.stream_k ? 0 : 1, pl.grid, 1, pl.stages, pl.cls, pl.groups, 0};
   if (env_int("HQ_TRACE", 0))
-    std::fprintf(stderr, "hq_gemm: m=%d n=%d k=%d bn=%d splits=%d grid=%d stages=%d smem=%u\n", m, L.n, L.k, pl.bn,
-                 pl.splits, pl.grid, pl.stages, pl.smem);
+    std::fprintf(stderr, "hq_gemm: m=%d n=%d k=%d bn=%d cls=%d stream_k=%d grid=%d stages=%d groups=%d smem=%u\n", m,
+                 L.n, L.k, pl.bn, pl.cls, pl.stream_k, pl.grid, pl.stages, pl.groups, pl.smem);
   return launch_wna16(l, p, tm, nullptr, 0, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
@@ -618,7 +623,7 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   int bn = mean_rows <= 16 ? 16 : (mean_rows <= 32 ? 32 : (mean_rows <= 64 ? 64 : 128));
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
   if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) bn = forced_bn;
-  const int bn_max = bn <= 64 ? 64 : 256;
+  const int cls = wna16_class(bn);
 
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L.num_experts, bn, exp_off, tile_off, perm,
                        expert_offsets_out, perm_out, reinterpret_cast<int*>(ws), s) != cudaSuccess)
@@ -633,29 +638,29 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   p.row_scale = L.channel ? reinterpret_cast<const float*>(wt + L.row_off) : nullptr;
   p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
   p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = tokens;
-  p.bn = bn; p.m_tiles = 0; p.splits = 1; p.kb_per_split = L.k_tiles;
-  p.a_stages = kWna16AStages;
+  p.bn = bn; p.m_tiles = 0; p.num_tiles = 0; p.stream_k = 0; p.iters = 0;
+  p.promote = (cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
   p.idesc = idesc_f16(true, 128, bn);
   p.status = reinterpret_cast<int*>(ws);
   p.num_experts = L.num_experts; p.topk = topk;
   p.tile_offsets = tile_off; p.expert_offsets = exp_off; p.perm = perm; p.topk_w = topk_w; p.zbuf = zbuf;
-  const int min_blocks = wna16_min_blocks(bn_max);
-  const size_t budget = std::min<size_t>(di.smem_optin, 232448 / min_blocks) - 2048 - 8 * (L.num_experts + 1);
-  const uint32_t per_stage = ((L.tile_bytes + 127u) & ~127u) + static_cast<uint32_t>(bn) * 256u;
-  p.stages = std::max(2, static_cast<int>(std::min<size_t>(8, budget / per_stage)));
+  plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.groups);
+  if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
   Wna16Launch l{};
   l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
   l.bf16 = true;
-  l.bn_max = bn_max;
+  l.cls = cls;
   l.moe = true;
-  l.grid = di.sms * min_blocks;
-  l.smem = wna16_smem_bytes(p.stages, L.tile_bytes, bn, L.num_experts);
+  l.grid = di.sms;
+  l.smem = wna16_smem_bytes(cls, p.stages, L.tile_bytes, bn, L.num_experts);
+  // X [T][K] gathered by token index: one-row boxes of 64 columns (four rows per copy)
   CUtensorMap tm;
-  std::memset(&tm, 0, sizeof(tm));
+  st = encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, tokens, ldx, 64, 1);
+  if (st != HQ_OK) return st;
   if (launch_wna16(l, p, tm, x, ldx, s) != cudaSuccess) return HQ_ERR_CUDA;
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L.num_experts, L.n, L.n_pad, y, ldy, true, s) != cudaSuccess)
     return HQ_ERR_CUDA;
-  g_last_plan = hq_plan_info{bn, 1, l.grid, 3, p.stages, {0, 0, 0}};
+  g_last_plan = hq_plan_info{bn, 1, l.grid, 3, p.stages, cls, p.groups, 0};
   return HQ_OK;
 }
 

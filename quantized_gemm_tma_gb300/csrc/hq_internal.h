@@ -87,9 +87,6 @@ HQ_HD constexpr uint32_t idesc_e4m3(int m, int n) {
 }
 
 // ------------------------------------------------------------------ GEMM
-constexpr int kWna16DqWarps = 8;   // dequant/epilogue warps of the WnA16 kernel
-constexpr int kWna16AStages = 2;   // TMEM A-operand ring depth
-
 enum class WFmt : int { INT4 = 0, INT6 = 1, MXFP4 = 2 };
 
 struct GemmParams {
@@ -102,14 +99,17 @@ struct GemmParams {
   int n, n_pad, k, k_tiles, n_tiles;
   int m;                    // dense: rows of X / Y
   int bn;                   // MMA N (tokens per tile), multiple of 16
-  int m_tiles, splits, kb_per_split;
-  int stages, a_stages;
+  int m_tiles, num_tiles;   // dense: token tiles, output tiles (m_tiles * n_tiles)
+  int stages, groups;       // shared-memory stages; dequantiser groups
+  int stream_k;             // dense: deal K-blocks out in equal ranges (1) or whole tiles (0)
+  int promote;              // one accumulator per K-block, group scale applied in fp32 by the epilogue
+  long long iters;          // stream-K: tiles * k_tiles
   uint32_t idesc;
   // output
   void* y;
   int64_t ldy;
-  float* partials;          // split-K: [splits][m][n_pad] fp32
-  int* counters;            // split-K: [m_tiles * n_tiles]
+  float* partials;          // stream-K: [2 * grid][bn][128] fp32 (head and tail unit of each CTA)
+  int* counters;            // stream-K: [tiles][4], zero between calls
   int* status;
   // MoE (grouped mode)
   int num_experts, topk;

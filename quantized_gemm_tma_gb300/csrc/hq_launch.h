@@ -13,25 +13,44 @@ namespace hq {
 // (kernel, device); later calls are a table lookup.
 cudaError_t ensure_smem_optin(const void* kernel);
 
+// Launch with programmatic stream serialization: the grid may begin its
+// prologue while the previous grid on the stream finishes; the kernel itself
+// waits (griddepcontrol.wait) before it touches global memory.
+template <typename... Args>
+cudaError_t launch_pdl(const void* kernel, int grid, int block, uint32_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* argv[] = {static_cast<void*>(&args)...};
+  return cudaLaunchKernelExC(&cfg, kernel, argv);
+}
+
 // transform.cu
 cudaError_t launch_repack(const Layout& L, const hq_weight_desc& d, void* dst, cudaStream_t stream);
 cudaError_t launch_unpack(const Layout& L, const void* src, void* codes, void* scales, void* zeros,
                           cudaStream_t stream);
 
-// wna16_*.cu: fmt = WFmt, bn_max in {64, 256}
+// wna16_*.cu: fmt = WFmt; cls = tile-width class (0: bn <= 16, 1: <= 64,
+// 2: <= 128, 3: <= 256)
 struct Wna16Launch {
   int fmt;
   bool bf16;
-  int bn_max;
+  int cls;
   bool moe;
   int grid;
   uint32_t smem;
-  int min_blocks;  // CTAs per SM the kernel was compiled for
 };
 cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows,
                          int64_t ldx, cudaStream_t stream);
-uint32_t wna16_smem_bytes(int stages, uint32_t tile_bytes, int bn, int num_experts);
-int wna16_min_blocks(int bn_max);
+uint32_t wna16_smem_bytes(int cls, int stages, uint32_t tile_bytes, int bn, int num_experts);
+int wna16_kps(int cls);  // K-blocks per shared-memory stage
 
 // gemm_fp8.cu
 cudaError_t launch_fp8(const Fp8Params& p, const CUtensorMap& tmap, int bn_max, int grid, uint32_t smem,

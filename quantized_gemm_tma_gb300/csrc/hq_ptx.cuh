@@ -66,15 +66,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns`
+// while the phase is incomplete; it resumes as soon as the phase completes,
+// so waiting warps stop taking issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false when
 // the wait gave up (timeout, or *abort became non-zero).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitTimeoutNs) return false;
   }
@@ -121,9 +134,38 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
       : "memory");
 }
 
+// 3-D tiled tensor copy global -> shared; coordinates innermost first.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y,
+                                            int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Gather four rows (y0..y3) of one 64-element-wide column slab starting at x
+// into four consecutive 128-byte rows of shared memory; the map's box is one
+// row high.  Out-of-range rows and columns are zero-filled.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y0,
+                                            int32_t y1, int32_t y2, int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
+
+// ---------------------------------------------------------------- grid dependencies
+// With programmatic dependent launch the grid may start while the previous
+// grid in the stream is still running: wait for it (and its memory) before
+// touching global data, and let the next grid start its own prologue early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
@@ -225,6 +267,37 @@ __device__ __forceinline__ void raise_error(int* status, volatile int* abort, in
   if (status) atomicCAS(status, 0, code);
   *abort = 1;
 }
+
+// Device-side event trace, compiled only into debug builds that define
+// HQ_ENABLE_TRACE: the first kTraceCtas CTAs record, per role slot, up to
+// kTraceEvents (globaltimer ns, tag) pairs into a per-translation-unit array.
+#if defined(HQ_ENABLE_TRACE)
+constexpr int kTraceCtas = 8, kTraceSlots = 16, kTraceEvents = 512;
+static __device__ unsigned long long g_trace[kTraceCtas * kTraceSlots * kTraceEvents * 2];
+static __device__ unsigned long long g_trace_cta[1024 * 2];
+#define HQ_TRACE_CTA(i)                                                            \
+  do {                                                                             \
+    if (blockIdx.x < 1024) ::hq::dev::g_trace_cta[blockIdx.x * 2 + (i)] = ::hq::dev::globaltimer(); \
+  } while (0)
+#define HQ_TRACE(slot, ctr, tag)                                                                          \
+  do {                                                                                                    \
+    if (blockIdx.x < ::hq::dev::kTraceCtas && (ctr) < ::hq::dev::kTraceEvents) {                          \
+      unsigned long long* e_ =                                                                            \
+          &::hq::dev::g_trace[((blockIdx.x * ::hq::dev::kTraceSlots + (slot)) * ::hq::dev::kTraceEvents + \
+                               (ctr)) * 2];                                                               \
+      e_[0] = ::hq::dev::globaltimer();                                                                   \
+      e_[1] = (tag);                                                                                      \
+    }                                                                                                     \
+    ++(ctr);                                                                                              \
+  } while (0)
+#else
+#define HQ_TRACE_CTA(i) \
+  do {                  \
+  } while (0)
+#define HQ_TRACE(slot, ctr, tag) \
+  do {                           \
+  } while (0)
+#endif
 
 }  // namespace dev
 }  // namespace hq

@@ -7,27 +7,55 @@
 namespace hq {
 namespace {
 
-template <bool BF16, int BN_MAX, bool MOE>
+template <bool BF16, int CLS, bool MOE>
 cudaError_t run(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows, int64_t ldx,
                 cudaStream_t stream) {
-  auto k = wna16::wna16_kernel<0, BF16, BN_MAX, MOE>;
+  auto k = wna16::wna16_kernel<0, BF16, CLS, MOE>;
   cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k));
   if (e != cudaSuccess) return e;
-  k<<<l.grid, wna16::kThreads, l.smem, stream>>>(p, tmap, static_cast<const __nv_bfloat16*>(x_rows), ldx);
-  return cudaGetLastError();
+  return launch_pdl(reinterpret_cast<const void*>(k), l.grid, wna16::threads<CLS>(), l.smem, stream, p, tmap,
+                    static_cast<const __nv_bfloat16*>(x_rows), ldx);
+}
+
+template <bool BF16, bool MOE>
+cudaError_t run_cls(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows,
+                    int64_t ldx, cudaStream_t stream) {
+  switch (l.cls) {
+    case 0: return run<BF16, 0, MOE>(l, p, tmap, x_rows, ldx, stream);
+    case 1: return run<BF16, 1, MOE>(l, p, tmap, x_rows, ldx, stream);
+    case 2: return run<BF16, 2, MOE>(l, p, tmap, x_rows, ldx, stream);
+    case 3: return run<BF16, 3, MOE>(l, p, tmap, x_rows, ldx, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_wna16_int4(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows,
-                             int64_t ldx, cudaStream_t stream) {
-  if (l.bf16 == true && l.bn_max == 64 && l.moe == false) return run<true, 64, false>(l, p, tmap, x_rows, ldx, stream);
-  if (l.bf16 == true && l.bn_max == 64 && l.moe == true) return run<true, 64, true>(l, p, tmap, x_rows, ldx, stream);
-  if (l.bf16 == true && l.bn_max == 256 && l.moe == false) return run<true, 256, false>(l, p, tmap, x_rows, ldx, stream);
-  if (l.bf16 == true && l.bn_max == 256 && l.moe == true) return run<true, 256, true>(l, p, tmap, x_rows, ldx, stream);
-  if (l.bf16 == false && l.bn_max == 64 && l.moe == false) return run<false, 64, false>(l, p, tmap, x_rows, ldx, stream);
-  if (l.bf16 == false && l.bn_max == 256 && l.moe == false) return run<false, 256, false>(l, p, tmap, x_rows, ldx, stream);
-  return cudaErrorInvalidValue;
+                              int64_t ldx, cudaStream_t stream) {
+  if (l.moe) return l.bf16 ? run_cls<true, true>(l, p, tmap, x_rows, ldx, stream) : cudaErrorInvalidValue;
+  return l.bf16 ? run_cls<true, false>(l, p, tmap, x_rows, ldx, stream)
+                : run_cls<false, false>(l, p, tmap, x_rows, ldx, stream);
 }
 
 }  // namespace hq
+
+#if defined(HQ_ENABLE_TRACE)
+// Debug builds only: copy (and optionally clear) the INT4 kernel's event trace.
+extern "C" int hq_trace_read(void* dst, size_t bytes, int clear) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+  if (bytes < sizeof(hq::dev::g_trace) + sizeof(hq::dev::g_trace_cta)) return 6;
+  if (cudaMemcpyFromSymbol(dst, hq::dev::g_trace, sizeof(hq::dev::g_trace)) != cudaSuccess) return 2;
+  if (cudaMemcpyFromSymbol(static_cast<char*>(dst) + sizeof(hq::dev::g_trace), hq::dev::g_trace_cta,
+                           sizeof(hq::dev::g_trace_cta)) != cudaSuccess)
+    return 5;
+  if (clear) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, hq::dev::g_trace) != cudaSuccess) return 3;
+    if (cudaMemset(p, 0, sizeof(hq::dev::g_trace)) != cudaSuccess) return 4;
+    if (cudaGetSymbolAddress(&p, hq::dev::g_trace_cta) != cudaSuccess) return 3;
+    if (cudaMemset(p, 0, sizeof(hq::dev::g_trace_cta)) != cudaSuccess) return 4;
+  }
+  return 0;
+}
+#endif

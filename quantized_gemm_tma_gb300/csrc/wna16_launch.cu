@@ -23,11 +23,23 @@ cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtens
   }
 }
 
-uint32_t wna16_smem_bytes(int stages, uint32_t tile_bytes, int bn, int num_experts) {
-  return wna16::smem_bytes(stages, tile_bytes, bn, num_experts);
+uint32_t wna16_smem_bytes(int cls, int stages, uint32_t tile_bytes, int bn, int num_experts) {
+  switch (cls) {
+    case 0: return wna16::smem_bytes<0>(stages, tile_bytes, bn, num_experts);
+    case 1: return wna16::smem_bytes<1>(stages, tile_bytes, bn, num_experts);
+    case 2: return wna16::smem_bytes<2>(stages, tile_bytes, bn, num_experts);
+    default: return wna16::smem_bytes<3>(stages, tile_bytes, bn, num_experts);
+  }
 }
 
-int wna16_min_blocks(int bn_max) { return bn_max <= 64 ? 2 : 1; }
+int wna16_kps(int cls) {
+  switch (cls) {
+    case 0: return wna16::Cls<0>::kKps;
+    case 1: return wna16::Cls<1>::kKps;
+    case 2: return wna16::Cls<2>::kKps;
+    default: return wna16::Cls<3>::kKps;
+  }
+}
 
 cudaError_t ensure_smem_optin(const void* kernel) {
   constexpr int kSlots = 128;
