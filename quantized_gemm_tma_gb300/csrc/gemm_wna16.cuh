@@ -24,12 +24,15 @@
 //                and 4/(16/KPS/4) of the block's four 32-column chunks, turns
 //                the packed codes into bf16x2/f16x2 pairs and writes them into
 //                the group's next A slot in TMEM with tcgen05.st.
-//   warp 20      producer: per stage, one bulk copy of up to KPS consecutive
-//                weight tiles (one contiguous run of the tile layout) and one
-//                tensor copy per 64-column activation slab (128-byte swizzle);
-//                MoE rows are gathered by routing index, four rows per
-//                tile::gather4 tensor copy.
-//   warps 21..   MMA issuers: issuer p takes K-block p of every stage and
+//   warp 20      weight producer: per stage one bulk copy of up to KPS
+//                consecutive weight tiles (one contiguous run of the tile
+//                layout) into the weight ring, released as soon as the
+//                dequantisers hold the codes in registers.
+//   warp 21      activation producer: per stage one tensor copy per 64-column
+//                slab (128-byte swizzle) into the activation ring, released
+//                by the MMA; MoE rows are gathered by routing index, four rows
+//                per tile::gather4 copy.
+//   warps 22..   MMA issuers: issuer p takes K-block p of every stage and
 //                accumulates into its own TMEM accumulator, so up to four
 //                threads issue tcgen05.mma.kind::f16 concurrently (one thread
 //                issues an M128 K16 MMA only every ~50-100 cycles, which alone
@@ -73,9 +76,11 @@ constexpr int kEpiWarps = 4;
 constexpr int kDqWarps = 16;
 constexpr int kASlots = 4;
 constexpr int kDqWarp0 = kEpiWarps;                        // first dequant warp
-constexpr int kProdWarp = kDqWarp0 + kDqWarps;             // producer warp
-constexpr int kIssWarp0 = kProdWarp + 1;                   // first MMA issuer warp
+constexpr int kProdWarp = kDqWarp0 + kDqWarps;             // weight producer warp
+constexpr int kXProdWarp = kProdWarp + 1;                  // activation producer warp
+constexpr int kIssWarp0 = kXProdWarp + 1;                  // first MMA issuer warp
 constexpr int kKRing = 4;  // promotion: per-K-block accumulators per issuer (class 0)
+constexpr int kSRing = 8;  // promotion: per-K-block row scales per group, in shared memory
 constexpr uint32_t kACol0 = 0;
 constexpr uint32_t kAccCol0 = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -324,38 +329,42 @@ __device__ __forceinline__ int sk_cta_of(long long x, long long T, int G) {
 // ---------------------------------------------------------------- the kernel
 template <int FMT, bool BF16, int CLS, bool MOE>
 __global__ void __launch_bounds__(threads<CLS>(), 1)
-    wna16_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x,
-                 const __nv_bfloat16* __restrict__ x_rows /* MoE: activations [T][ldx] */, int64_t ldx) {
+    wna16_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x) {
   using C = Cls<CLS>;
   constexpr int KPS = C::kKps, ISS = C::kIss, DACC = C::kDacc, BNMAX = C::kBnMax;
+  constexpr int G = KPS;                 // dequantiser groups
+  constexpr int WG = kDqWarps / G;        // warps per group
+  constexpr int DA = kASlots / G;         // A slots per group
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from smem_raw by an offset so that the
   // compiler keeps shared-memory addressing for every access through it
   uint8_t* smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
 
-  constexpr int G = KPS;                 // dequantiser groups
-  constexpr int WG = kDqWarps / G;        // warps per group
-  constexpr int DA = kASlots / G;         // A slots per group
-  const int S = p.stages;
+  const int SW = p.stages;    // weight ring (KPS tiles per stage)
+  const int SX = p.x_stages;  // activation ring (2 KPS slabs per stage)
   const int bn = p.bn;
   const uint32_t tile_bytes = p.tile_bytes;
   const uint32_t w_stage = (KPS * tile_bytes + 1023u) & ~1023u;
   const uint32_t slab = static_cast<uint32_t>(bn) * 128u;  // bn rows x 64 K (128 bytes, swizzled)
   const uint32_t x_stage = 2u * KPS * slab;
-  uint8_t* w_st = smem;
-  uint8_t* x_st = smem + S * w_stage;
-  uint64_t* full = reinterpret_cast<uint64_t*>(x_st + S * x_stage);
-  uint64_t* empty = full + S;
-  uint64_t* a_full = empty + S;
+  uint8_t* x_st = smem;                    // slabs first: 1024-byte aligned at any bn
+  uint8_t* w_st = smem + SX * x_stage;
+  uint64_t* w_full = reinterpret_cast<uint64_t*>(w_st + SW * w_stage);
+  uint64_t* w_empty = w_full + SW;
+  uint64_t* x_full = w_empty + SW;
+  uint64_t* x_empty = x_full + SX;
+  uint64_t* a_full = x_empty + SX;
   uint64_t* a_empty = a_full + kASlots;
   uint64_t* acc_full = a_empty + kASlots;
   uint64_t* acc_empty = acc_full + DACC;
   uint64_t* tear = acc_empty + DACC;
   uint64_t* k_full = tear + 1;              // promotion: [ISS][kKRing]
   uint64_t* k_empty = k_full + 2 * kKRing;  // promotion: [ISS][kKRing]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(k_empty + 2 * kKRing);
+  uint64_t* s_full = k_empty + 2 * kKRing;  // promotion: [G][kSRing]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 2 * kSRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_tok = reinterpret_cast<int*>(tmem_slot + 4);  // MoE: token of each row of the unit
+  float* s_scale = reinterpret_cast<float*>(tmem_slot + 4);  // promotion: [G][kSRing][128]
+  int* s_tok = reinterpret_cast<int*>(s_scale + (CLS == 0 ? 2 * kSRing * kTileN : 0));  // MoE: token per row
   int* s_tile_off = s_tok + (MOE ? BNMAX : 0);
   int* s_row_off = s_tile_off + (MOE ? p.num_experts + 1 : 0);
 
@@ -364,9 +373,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   if (threadIdx.x == 0) HQ_TRACE_CTA(0);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      dev::mbar_init(&full[s], 1u);
-      dev::mbar_init(&empty[s], kDqWarps + ISS + (p.promote ? kEpiWarps : 0));
+    for (int s = 0; s < SW; ++s) {
+      dev::mbar_init(&w_full[s], 1);
+      dev::mbar_init(&w_empty[s], kDqWarps);
+    }
+    for (int s = 0; s < SX; ++s) {
+      dev::mbar_init(&x_full[s], 1);
+      dev::mbar_init(&x_empty[s], ISS);
     }
     for (int a = 0; a < kASlots; ++a) {
       dev::mbar_init(&a_full[a], WG);
@@ -381,6 +394,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       dev::mbar_init(&k_full[k], 1);
       dev::mbar_init(&k_empty[k], kEpiWarps);
     }
+    for (int k = 0; k < 2 * kSRing; ++k) dev::mbar_init(&s_full[k], 4);
     *abort_flag = 0;
     dev::fence_barrier_init();
   }
@@ -388,16 +402,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     dev::tmem_alloc(tmem_slot, kTmemCols);
     dev::tmem_relinquish();
   }
-  if (warp == kProdWarp && lane == 0) dev::prefetch_tmap(&tmap_x);
-  // everything above overlaps the previous grid; global data only after this
-  dev::grid_dep_wait();
-  dev::grid_dep_launch();
-  if constexpr (MOE) {
-    for (int i = threadIdx.x; i <= p.num_experts; i += blockDim.x) {
-      s_tile_off[i] = p.tile_offsets[i];
-      s_row_off[i] = p.expert_offsets[i];
-    }
-  }
+  if (warp == kXProdWarp && lane == 0) dev::prefetch_tmap(&tmap_x);
   dev::tc_fence_before();
   __syncthreads();
   dev::tc_fence_after();
@@ -405,8 +410,43 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   [[maybe_unused]] int tr0 = 0;
   if (threadIdx.x == 0) HQ_TRACE(15, tr0, 0);
 
+  // Weights are constant while the GEMM runs (hq_transform is synchronous), so
+  // the first ring of weight copies is issued before waiting on the previous
+  // grid; activations and everything else only after the wait.
+  int n_pre = 0;
+  if constexpr (!MOE) {
+    if (warp == kProdWarp) {
+      if (lane == 0) {
+        Sched<MOE> sc;
+        sc.init(p);
+        const uint64_t pol = dev::policy_evict_first();
+        Unit u;
+        while (n_pre < SW && sc.next(p, s_tile_off, s_row_off, u)) {
+          const uint8_t* wt = p.tiles + static_cast<uint64_t>(u.nt) * p.k_tiles * tile_bytes;
+          for (int kb = u.kb0; kb < u.kb1 && n_pre < SW; kb += KPS, ++n_pre) {
+            const uint32_t wbytes = static_cast<uint32_t>(min(KPS, u.kb1 - kb)) * tile_bytes;
+            dev::mbar_arrive_expect_tx(&w_full[n_pre], wbytes);
+            dev::bulk_load_hint(w_st + n_pre * w_stage, wt + static_cast<uint64_t>(kb) * tile_bytes, wbytes,
+                                &w_full[n_pre], pol);
+          }
+        }
+      }
+      n_pre = __shfl_sync(0xffffffffu, n_pre, 0);
+    }
+  }
+  dev::grid_dep_wait();
+  dev::grid_dep_launch();
+  if (threadIdx.x == 0) HQ_TRACE_CTA(1);
+  if constexpr (MOE) {
+    for (int i = threadIdx.x; i <= p.num_experts; i += blockDim.x) {
+      s_tile_off[i] = p.tile_offsets[i];
+      s_row_off[i] = p.expert_offsets[i];
+    }
+    __syncthreads();
+  }
+
   if (warp == kProdWarp) {
-    // ============================================================ producer
+    // ============================================================ weight producer
     Sched<MOE> sc;
     sc.init(p);
     Ring rg;
@@ -418,6 +458,44 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
       const uint8_t* wt = p.tiles + static_cast<uint64_t>(u.e) * p.expert_stride +
                           static_cast<uint64_t>(u.nt) * p.k_tiles * tile_bytes;
+      for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
+        if (issued >= n_pre) {
+          if (!warp_wait(&w_empty[rg.s], rg.ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t wbytes = static_cast<uint32_t>(min(KPS, u.kb1 - kb)) * tile_bytes;
+            dev::mbar_arrive_expect_tx(&w_full[rg.s], wbytes);
+            dev::bulk_load_hint(w_st + rg.s * w_stage, wt + static_cast<uint64_t>(kb) * tile_bytes, wbytes,
+                                &w_full[rg.s], pol);
+          }
+        }
+        if (lane == 0) HQ_TRACE(0, tr, (1ull << 24) | issued);
+        rg.next(SW);
+        ++issued;
+      }
+    }
+    if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
+    // drain: every copy this warp issued has landed before the CTA can exit
+    if (lane == 0) {
+      for (int s = 0; s < SW && s < issued; ++s) {
+        const int last = ((issued - 1 - s) / SW) * SW + s;
+        const uint32_t ph = (last / SW) & 1;
+        const uint64_t t0 = dev::globaltimer();
+        while (!dev::mbar_try_wait(&w_full[s], ph) && dev::globaltimer() - t0 < dev::kWaitTimeoutNs) {
+        }
+      }
+    }
+  } else if (warp == kXProdWarp) {
+    // ============================================================ activation producer
+    Sched<MOE> sc;
+    sc.init(p);
+    Ring rg;
+    int issued = 0;
+    bool ok = true;
+    Unit u;
+    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
       if constexpr (MOE) {
         for (int r = static_cast<int>(lane); r < BNMAX; r += 32)
           s_tok[r] = (r < u.rows) ? p.perm[u.row0 + r] / p.topk : p.m;  // p.m = T: out of range
@@ -425,48 +503,40 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       }
       for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
         const int cnt = min(KPS, u.kb1 - kb);
-        if (!warp_wait(&empty[rg.s], rg.ph ^ 1u, abort_flag)) {
+        if (!warp_wait(&x_empty[rg.s], rg.ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        if (lane == 0) HQ_TRACE(0, tr, (1ull << 24) | issued);
         uint8_t* xs = x_st + rg.s * x_stage;
         if (lane == 0) {
-          const uint32_t wbytes = static_cast<uint32_t>(cnt) * tile_bytes;
-          dev::mbar_arrive_expect_tx(&full[rg.s], wbytes + 2u * cnt * slab);
-          dev::bulk_load_hint(w_st + rg.s * w_stage, wt + static_cast<uint64_t>(kb) * tile_bytes, wbytes,
-                              &full[rg.s], pol);
-          if constexpr (!MOE) {
-            // one 64-column slab of bn rows per copy; columns past K and rows
-            // past M are zero-filled by the tensor copy
-            for (int z = 0; z < 2 * cnt; ++z)
-              dev::tma_load_2d(xs + z * slab, &tmap_x, &full[rg.s], (2 * kb + z) * 64, u.row0);
-          }
-        }
-        if constexpr (MOE) {
-          // gathered rows, four per tensor copy (one-row boxes); rows past the
-          // unit and columns past K are out of range and zero-filled
-          if (lane == 0) {
-            for (int z = 0; z < 2 * cnt; ++z) {
-              const int x = (2 * kb + z) * 64;
+          dev::mbar_arrive_expect_tx(&x_full[rg.s], 2u * cnt * slab);
+          for (int z = 0; z < 2 * cnt; ++z) {
+            const int x = (2 * kb + z) * 64;
+            if constexpr (MOE) {
+              // gathered rows, four per tensor copy (one-row boxes); rows past
+              // the unit and columns past K are out of range and zero-filled
               for (int r = 0; r < bn; r += 4)
-                dev::tma_gather4(xs + z * slab + r * 128, &tmap_x, &full[rg.s], x, s_tok[r], s_tok[r + 1],
+                dev::tma_gather4(xs + z * slab + r * 128, &tmap_x, &x_full[rg.s], x, s_tok[r], s_tok[r + 1],
                                  s_tok[r + 2], s_tok[r + 3]);
+            } else {
+              // one 64-column slab of bn rows; columns past K and rows past M
+              // are zero-filled by the tensor copy
+              dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], x, u.row0);
             }
           }
         }
-        rg.next(S);
+        rg.next(SX);
         ++issued;
       }
+      if constexpr (MOE) __syncwarp();  // s_tok is rewritten for the next unit
     }
     if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
-    // drain: every copy this warp issued has landed before the CTA can exit
     if (lane == 0) {
-      for (int s = 0; s < S && s < issued; ++s) {
-        const int last = ((issued - 1 - s) / S) * S + s;
-        const uint32_t ph = (last / S) & 1;
+      for (int s = 0; s < SX && s < issued; ++s) {
+        const int last = ((issued - 1 - s) / SX) * SX + s;
+        const uint32_t ph = (last / SX) & 1;
         const uint64_t t0 = dev::globaltimer();
-        while (!dev::mbar_try_wait(&full[s], ph) && dev::globaltimer() - t0 < dev::kWaitTimeoutNs) {
+        while (!dev::mbar_try_wait(&x_full[s], ph) && dev::globaltimer() - t0 < dev::kWaitTimeoutNs) {
         }
       }
     }
@@ -474,109 +544,72 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     // ============================================================ MMA issuers
     const int pidx = warp - kIssWarp0;
     if (lane == 0) {
-      if (CLS == 0 && p.promote) {
-        // one accumulator per K-block in a ring of kKRing; the epilogue
-        // applies the K-block's scale in fp32 and sums in K order
-        Sched<MOE> sc;
-        sc.init(p);
-        Ring rg;
-        uint32_t cu = 0, ck = 0;
-        const uint32_t idesc = p.idesc;
-        bool ok = true;
-        Unit u;
-        while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
-          for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
-            const int cnt = min(KPS, u.kb1 - kb);
-            if (!dev::mbar_wait(&full[rg.s], rg.ph, abort_flag)) {
-              ok = false;
-              break;
-            }
-            if (pidx < cnt) {
-              const int slot = pidx * DA + static_cast<int>(cu % DA);
-              const int ks = pidx * kKRing + static_cast<int>(ck % kKRing);
-              if (!dev::mbar_wait(&a_full[slot], (cu / DA) & 1u, abort_flag) ||
-                  !dev::mbar_wait(&k_empty[ks], ((ck / kKRing) & 1u) ^ 1u, abort_flag)) {
-                ok = false;
-                break;
-              }
-              dev::tc_fence_after();
-              const uint32_t xs = dev::smem_u32(x_st + rg.s * x_stage) + 2u * pidx * slab;
-              const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(slot) * 64u;
-              const uint32_t d_tmem = tmem + kAccCol0 + static_cast<uint32_t>(ks * BNMAX);
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bdesc = dev::sw128_desc(xs + (kk >> 2) * slab + (kk & 3) * 32);
-                dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk == 0 ? 0u : 1u);
-              }
-              dev::tc_commit(&a_empty[slot]);
-              dev::tc_commit(&k_full[ks]);
-              ++cu;
-              ++ck;
-            }
-            dev::tc_commit(&empty[rg.s]);
-            rg.next(S);
-          }
-        }
-        if (!ok) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
-        dev::tc_commit(tear);
-      } else {
       Sched<MOE> sc;
       sc.init(p);
-      Ring rg;
-      uint32_t cu = 0;  // uses of this issuer's group's A ring
+      Ring rx;
+      uint32_t cu = 0, ck = 0;
       const uint32_t idesc = p.idesc;
+      const bool promote = CLS == 0 && p.promote;
       bool ok = true;
       int ui = 0;
       [[maybe_unused]] int tr = 0, ts = 0;
       Unit u;
       while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+        // whole-unit accumulator (double-buffered across units) unless promoting
         const int buf = DACC == 1 ? 0 : (ui & 1);
-        const uint32_t accph = static_cast<uint32_t>(DACC == 1 ? ui : (ui >> 1)) & 1u;
-        if (!dev::mbar_wait(&acc_empty[buf], accph ^ 1u, abort_flag)) {
-          ok = false;
-          break;
+        if (!promote) {
+          const uint32_t accph = static_cast<uint32_t>(DACC == 1 ? ui : (ui >> 1)) & 1u;
+          if (!dev::mbar_wait(&acc_empty[buf], accph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          dev::tc_fence_after();
         }
-        dev::tc_fence_after();
-        const uint32_t d_tmem = tmem + kAccCol0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
         bool first = true;
         for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
           const int cnt = min(KPS, u.kb1 - kb);
-          if (!dev::mbar_wait(&full[rg.s], rg.ph, abort_flag)) {
+          if (!dev::mbar_wait(&x_full[rx.s], rx.ph, abort_flag)) {
             ok = false;
             break;
           }
           HQ_TRACE(1 + pidx, tr, (2ull << 24) | ts);
           if (pidx < cnt) {
             const int slot = pidx * DA + static_cast<int>(cu % DA);
-            if (!dev::mbar_wait(&a_full[slot], (cu / DA) & 1u, abort_flag)) {
+            const int ks = pidx * kKRing + static_cast<int>(ck % kKRing);
+            if (!dev::mbar_wait(&a_full[slot], (cu / DA) & 1u, abort_flag) ||
+                (promote && !dev::mbar_wait(&k_empty[ks], ((ck / kKRing) & 1u) ^ 1u, abort_flag))) {
               ok = false;
               break;
             }
             HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
             dev::tc_fence_after();
-            const uint32_t xs = dev::smem_u32(x_st + rg.s * x_stage) + 2u * pidx * slab;
+            const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + 2u * pidx * slab;
             const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(slot) * 64u;
+            const uint32_t d_tmem = promote ? tmem + kAccCol0 + static_cast<uint32_t>(ks * BNMAX)
+                                            : tmem + kAccCol0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
+            const bool fresh = promote || first;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t bdesc = dev::sw128_desc(xs + (kk >> 2) * slab + (kk & 3) * 32);
-              dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
+              dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && kk == 0) ? 0u : 1u);
             }
             dev::tc_commit(&a_empty[slot]);
+            if (promote) dev::tc_commit(&k_full[ks]);
             ++cu;
+            ++ck;
           }
-          dev::tc_commit(&empty[rg.s]);
+          dev::tc_commit(&x_empty[rx.s]);
           HQ_TRACE(1 + pidx, tr, (4ull << 24) | ts);
           ++ts;
-          rg.next(S);
+          rx.next(SX);
           first = false;
         }
         if (!ok) break;
-        dev::tc_commit(&acc_full[buf]);
+        if (!promote) dev::tc_commit(&acc_full[buf]);
         ++ui;
       }
       if (!ok) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
       dev::tc_commit(tear);  // arrives once every MMA this thread issued has completed
-      }
     }
   } else if (warp >= kDqWarp0) {
     // ============================================================ dequantisers
@@ -586,6 +619,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     const int sub = (dw % WG) >> 2;         // which G chunks of the 4 this warp converts
     const int r = quarter * 32 + static_cast<int>(lane);  // weight row within the tile (TMEM lane)
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol0;
+    const bool promote = CLS == 0 && p.promote;
     Sched<MOE> sc;
     sc.init(p);
     Ring rg;
@@ -601,7 +635,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       if (p.channel && p.has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
       for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
         const int cnt = min(KPS, u.kb1 - kb);
-        if (!warp_wait(&full[rg.s], rg.ph, abort_flag)) {
+        if (!warp_wait(&w_full[rg.s], rg.ph, abort_flag)) {
           ok = false;
           break;
         }
@@ -632,19 +666,29 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             }
           }
         }
-        // publish the previous K-block's A slot while this stage's loads land
-        if (trace_me) HQ_TRACE(5 + gi, tr, (11ull << 24) | ts);
+        // promotion: the row's group scale goes to the epilogue through a ring
+        // (one phase per kSRing K-blocks; the epilogue trails by at most
+        // kASlots/G + kKRing K-blocks, fewer than kSRing)
+        if (promote && real && sub == 0) {
+          constexpr float kOpFixD = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
+          const uint32_t s16 = ss[0];
+          const float sf = BF16 ? __uint_as_float(s16 << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(s16)));
+          const int si = gi * kSRing + static_cast<int>(ca % kSRing);
+          s_scale[si * kTileN + r] = sf * kOpFixD;
+          __syncwarp();
+          if (lane == 0) dev::mbar_arrive(&s_full[si]);
+        }
+        // the weight stage is free once its codes are in registers
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
+        // publish the previous K-block's A slot while this one converts
         if (pend >= 0) {
           dev::tmem_st_wait();
-          if (trace_me) HQ_TRACE(5 + gi, tr, (12ull << 24) | ts);
           dev::tc_fence_before();
           __syncwarp();
           if (lane == 0) dev::mbar_arrive(&a_full[pend]);
           pend = -1;
         }
-        __syncwarp();
-        if (lane == 0) dev::mbar_arrive(&empty[rg.s]);
-        if (trace_me) HQ_TRACE(5 + gi, tr, (13ull << 24) | ts);
         if (real) {
           const int slot = gi * DA + static_cast<int>(ca % DA);
           if (!warp_wait(&a_empty[slot], ((ca / DA) & 1u) ^ 1u, abort_flag)) {
@@ -658,11 +702,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             const int c = sub * G + i;
             uint32_t o[16];
             if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
-              if (p.channel || p.promote) dq_int4<BF16, false>(qc[i], zz[i], ss[i], o);
+              if (p.channel || promote) dq_int4<BF16, false>(qc[i], zz[i], ss[i], o);
               else dq_int4<BF16, true>(qc[i], zz[i], ss[i], o);
             } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
               const uint32_t c2 = (magic_half<BF16>() + zz[i]) * 0x00010001u;
-              if (p.channel || p.promote) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o);
+              if (p.channel || promote) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o);
               else dq_int6<BF16, true>(qc[i], qh[i], c2, ss[i] * 0x00010001u, o);
             } else {
               dq_mxfp4(qc[i], ss[i], o);
@@ -674,7 +718,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           ++ca;
         }
         ++ts;
-        rg.next(S);
+        rg.next(SW);
       }
     }
     if (pend >= 0) {
@@ -693,7 +737,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     sc.init(p);
     bool ok = true;
     int ui = 0;
-    [[maybe_unused]] Ring rg;       // promotion: stage ring position
     [[maybe_unused]] uint32_t ck[2] = {0, 0};  // promotion: K-blocks taken from each issuer's ring
     [[maybe_unused]] int tr = 0;
     const bool trace_me = quarter == 0 && lane == 0;
@@ -709,12 +752,18 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
                              : nullptr;
       // columns [16 ch, 16 ch + 16) of this row: partial, MoE row or Y
       auto emit16 = [&](int ch, const float (&v)[16]) {
+        if (partial) {
+          float4* dst = reinterpret_cast<float4*>(pslot + static_cast<size_t>(r) * bn + ch * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          return;
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int col = ch * 16 + i;
           if (col >= u.rows) continue;
           if (partial) {
-            pslot[static_cast<size_t>(col) * kTileN + r] = v[i];
+            // stored below, 16 at a time
           } else if (n_ok) {
             if constexpr (MOE) {
               const int f = p.perm[u.row0 + col];
@@ -732,53 +781,37 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         if (p.promote) {
           promoted = true;
           // sum the unit's per-K-block accumulators in K order, each times its
-          // group scale (read from the stage before releasing it)
+          // group scale (read-only, loaded one K-block ahead)
           float tot[BNMAX];
 #pragma unroll
           for (int i = 0; i < BNMAX; ++i) tot[i] = 0.f;
-          for (int kb = u.kb0; ok && kb < u.kb1; kb += KPS) {
-            const int cnt = min(KPS, u.kb1 - kb);
-            if (!warp_wait(&full[rg.s], rg.ph, abort_flag)) {
+          for (int kb = u.kb0; kb < u.kb1; ++kb) {
+            const int q = (kb - u.kb0) & (KPS - 1);
+            const uint32_t cq = q ? ck[1] : ck[0];
+            const int ks = q * kKRing + static_cast<int>(cq % kKRing);
+            const int si = q * kSRing + static_cast<int>(cq % kSRing);
+            if (!warp_wait(&s_full[si], (cq / kSRing) & 1u, abort_flag) ||
+                !warp_wait(&k_full[ks], (cq / kKRing) & 1u, abort_flag)) {
               ok = false;
               break;
             }
-            float sk[KPS];
+            const float s_cur = s_scale[si * kTileN + r];
+            dev::tc_fence_after();
+            const uint32_t acc = tmem + lane_base + kAccCol0 + static_cast<uint32_t>(ks * BNMAX);
 #pragma unroll
-            for (int q = 0; q < KPS; ++q) {
-              sk[q] = 0.f;
-              if (q < cnt) {
-                const uint32_t s16 =
-                    *reinterpret_cast<const uint16_t*>(w_st + rg.s * w_stage + q * tile_bytes + p.scale_off + r * 2);
-                const float sf = BF16 ? __uint_as_float(s16 << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(s16)));
-                sk[q] = sf * kOpFix;
+            for (int ch = 0; ch < BNMAX / 16; ++ch) {
+              if (ch * 16 < bn) {
+                uint32_t a[16];
+                dev::tmem_ld16(acc + ch * 16, a);
+                dev::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) tot[ch * 16 + i] = fmaf(s_cur, __uint_as_float(a[i]), tot[ch * 16 + i]);
               }
             }
+            dev::tc_fence_before();
             __syncwarp();
-            if (lane == 0) dev::mbar_arrive(&empty[rg.s]);
-            rg.next(S);
-            for (int q = 0; q < cnt; ++q) {
-              const int ks = q * kKRing + static_cast<int>(ck[q] % kKRing);
-              if (!warp_wait(&k_full[ks], (ck[q] / kKRing) & 1u, abort_flag)) {
-                ok = false;
-                break;
-              }
-              dev::tc_fence_after();
-              const uint32_t acc = tmem + lane_base + kAccCol0 + static_cast<uint32_t>(ks * BNMAX);
-#pragma unroll
-              for (int ch = 0; ch < BNMAX / 16; ++ch) {
-                if (ch * 16 < bn) {
-                  uint32_t a[16];
-                  dev::tmem_ld16(acc + ch * 16, a);
-                  dev::tmem_ld_wait();
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) tot[ch * 16 + i] = fmaf(sk[q], __uint_as_float(a[i]), tot[ch * 16 + i]);
-                }
-              }
-              dev::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) dev::mbar_arrive(&k_empty[ks]);
-              ++ck[q];
-            }
+            if (lane == 0) dev::mbar_arrive(&k_empty[ks]);
+            if (q) ++ck[1]; else ++ck[0];
           }
           if (!ok) break;
 #pragma unroll
@@ -827,8 +860,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         if (trace_me) HQ_TRACE(9, tr, (9ull << 24) | ui);
       }
       if (partial) {
-        // the last of the tile's CTAs sums every partial in CTA (= K) order
-        __threadfence();
+        // The last of the tile's CTAs sums every partial in CTA (= K) order.
+        // Partials are [slot][row][bn] fp32, one contiguous run per row.
+        // __syncwarp orders the lanes' stores before lane 0's release.
         __syncwarp();
         const long long T = p.iters;
         const int Gc = static_cast<int>(gridDim.x);
@@ -837,27 +871,33 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         const int cl = sk_cta_of(x0 + p.k_tiles - 1, T, Gc);
         int* ctr = p.counters + u.tile * 4 + quarter;
         int last = 0;
-        if (lane == 0) last = (atomicAdd(ctr, 1) == cl - cf) ? 1 : 0;
+        if (lane == 0) last = (dev::atom_add_acq_rel_gpu(ctr, 1) == cl - cf) ? 1 : 0;
         last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();
         if (last) {
-          __threadfence();
-          // 8 columns at a time, contributors summed in CTA order
-          for (int ch = 0; ch * 8 < u.rows; ++ch) {
-            float v[8];
+          for (int ch = 0; ch * 16 < u.rows; ++ch) {
+            float v[16];
+#pragma unroll 1
             for (int c = cf; c <= cl; ++c) {
               const long long begin = static_cast<long long>(c) * T / Gc;
               const int slot = 2 * c + (begin >= x0 ? 0 : 1);
-              const float* src = p.partials + (static_cast<size_t>(slot) * bn + ch * 8) * kTileN + r;
-              float t[8];
+              const float4* src =
+                  reinterpret_cast<const float4*>(p.partials + (static_cast<size_t>(slot) * kTileN + r) * bn + ch * 16);
+              float4 t[4];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) t[i] = __ldcg(src + i * kTileN);
+              for (int i = 0; i < 4; ++i) t[i] = __ldcg(src + i);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] = (c == cf) ? t[i] : v[i] + t[i];
+              for (int i = 0; i < 4; ++i) {
+                v[4 * i + 0] = (c == cf) ? t[i].x : v[4 * i + 0] + t[i].x;
+                v[4 * i + 1] = (c == cf) ? t[i].y : v[4 * i + 1] + t[i].y;
+                v[4 * i + 2] = (c == cf) ? t[i].z : v[4 * i + 2] + t[i].z;
+                v[4 * i + 3] = (c == cf) ? t[i].w : v[4 * i + 3] + t[i].w;
+              }
             }
             if (n_ok) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const int col = ch * 8 + i;
+              for (int i = 0; i < 16; ++i) {
+                const int col = ch * 16 + i;
                 if (col < u.rows) {
                   const size_t off = static_cast<size_t>(u.row0 + col) * p.ldy + n;
                   if constexpr (BF16) reinterpret_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(v[i] * rs);
@@ -879,6 +919,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   dev::tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) HQ_TRACE(15, tr0, 1);
+  if (threadIdx.x == 0) HQ_TRACE_CTA(2);
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t t0 = dev::globaltimer();
@@ -888,19 +929,21 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     __syncwarp();
     dev::tc_fence_after();
     dev::tmem_dealloc(tmem, kTmemCols);
-    if (lane == 0) HQ_TRACE_CTA(1);
+    if (lane == 0) HQ_TRACE_CTA(3);
   }
 }
 
 // Dynamic shared memory bytes for a launch of class CLS.
 template <int CLS>
-inline uint32_t smem_bytes(int stages, uint32_t tile_bytes, int bn, int num_experts) {
+inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts) {
   using C = Cls<CLS>;
-  const uint32_t w = static_cast<uint32_t>(stages) * ((C::kKps * tile_bytes + 1023u) & ~1023u);
-  const uint32_t x = static_cast<uint32_t>(stages) * 2u * C::kKps * static_cast<uint32_t>(bn) * 128u;
-  const uint32_t bars = (2u * stages + 2u * kASlots + 2u * C::kDacc + 1u + 4u * kKRing) * 8u + 16u;
+  const uint32_t w = static_cast<uint32_t>(w_stages) * ((C::kKps * tile_bytes + 1023u) & ~1023u);
+  const uint32_t x = static_cast<uint32_t>(x_stages) * 2u * C::kKps * static_cast<uint32_t>(bn) * 128u;
+  const uint32_t bars =
+      (2u * w_stages + 2u * x_stages + 2u * kASlots + 2u * C::kDacc + 1u + 4u * kKRing + 2u * kSRing) * 8u + 16u;
+  const uint32_t scales = CLS == 0 ? 4u * 2u * kSRing * kTileN : 0u;
   const uint32_t moe = 4u * (C::kBnMax + 2u * (num_experts + 1));
-  return w + x + bars + moe + 1024u /* alignment slack */;
+  return w + x + bars + scales + moe + 1024u /* alignment slack */;
 }
 
 }  // namespace wna16

@@ -340,7 +340,7 @@ constexpr int kMaxSplitTiles = 512;
 constexpr size_t kCounterBytes = sizeof(int) * kMaxSplitTiles * 8;
 
 struct DensePlan {
-  int cls, bn, m_tiles, tiles, stages, groups, grid, stream_k;
+  int cls, bn, m_tiles, tiles, stages, x_stages, groups, grid, stream_k;
   long long iters;
   uint32_t smem;
 };
@@ -392,14 +392,20 @@ size_t splitk_bytes(int splits, int m, int n_pad) {
   return kCounterBytes + align_up(sizeof(float) * static_cast<size_t>(splits) * m * n_pad, kAlign);
 }
 
-// Shared-memory stages for a tile-width class: as many as fit (2..8); the
-// dequantiser groups equal the class's K-blocks per stage.
-void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_optin, int* stages, int* groups) {
+// Shared-memory rings for a tile-width class: a few activation stages (the
+// MMA holds them), then as many weight stages as fit, up to 8.
+void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_optin, int* w_stages,
+                 int* x_stages, int* groups) {
   const size_t cap = std::min<size_t>(smem_optin, 232448);
-  int smax = 1;
-  for (int st = 2; st <= 8; ++st)
-    if (wna16_smem_bytes(cls, st, L.tile_bytes, bn, num_experts) <= cap) smax = st;
-  *stages = smax;
+  static const int kXWant[4] = {6, 3, 3, 2};
+  int sx = kXWant[cls], sw = 0;
+  for (; sx >= 2; --sx) {
+    for (sw = 8; sw >= 2; --sw)
+      if (wna16_smem_bytes(cls, sw, sx, L.tile_bytes, bn, num_experts) <= cap) break;
+    if (sw >= 2) break;
+  }
+  *w_stages = sw >= 2 && sx >= 2 ? sw : 0;
+  *x_stages = sx;
   *groups = wna16_kps(cls);
 }
 
@@ -421,8 +427,8 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   const int forced_sk = env_int("HQ_FORCE_SPLITK", 0);  // 1: stream-K on, 2: off
   if (forced_sk == 1 && !(flags & HQ_FLAG_BATCH_INVARIANT) && p.tiles <= kMaxSplitTiles) p.stream_k = 1;
   if (forced_sk == 2) p.stream_k = 0;
-  plan_stages(p.cls, L, p.bn, 0, smem_optin, &p.stages, &p.groups);
-  p.smem = wna16_smem_bytes(p.cls, p.stages, L.tile_bytes, p.bn, 0);
+  plan_stages(p.cls, L, p.bn, 0, smem_optin, &p.stages, &p.x_stages, &p.groups);
+  p.smem = wna16_smem_bytes(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn, 0);
   // stream-K: at least 8 K-blocks per CTA, so that partial tiles stay few
   p.grid = p.stream_k ? static_cast<int>(std::min<long long>(sms, std::max<long long>(1, (p.iters + 7) / 8)))
                       : std::min(sms, p.tiles);
@@ -533,7 +539,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
   p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = m;
   p.bn = pl.bn; p.m_tiles = pl.m_tiles; p.num_tiles = pl.tiles;
-  p.stages = pl.stages; p.groups = pl.groups;
+  p.stages = pl.stages; p.x_stages = pl.x_stages; p.groups = pl.groups;
   p.stream_k = pl.stream_k; p.iters = pl.iters;
   p.promote = (pl.cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
   p.idesc = idesc_f16(atype == HQ_A_BF16, 128, pl.bn);
@@ -558,7 +564,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   if (env_int("HQ_TRACE", 0))
     std::fprintf(stderr, "hq_gemm: m=%d n=%d k=%d bn=%d cls=%d stream_k=%d grid=%d stages=%d groups=%d smem=%u\n", m,
                  L.n, L.k, pl.bn, pl.cls, pl.stream_k, pl.grid, pl.stages, pl.groups, pl.smem);
-  return launch_wna16(l, p, tm, nullptr, 0, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+  return launch_wna16(l, p, tm, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ MoE
@@ -644,7 +650,7 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   p.status = reinterpret_cast<int*>(ws);
   p.num_experts = L.num_experts; p.topk = topk;
   p.tile_offsets = tile_off; p.expert_offsets = exp_off; p.perm = perm; p.topk_w = topk_w; p.zbuf = zbuf;
-  plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.groups);
+  plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups);
   if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
   Wna16Launch l{};
   l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
@@ -652,12 +658,12 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   l.cls = cls;
   l.moe = true;
   l.grid = di.sms;
-  l.smem = wna16_smem_bytes(cls, p.stages, L.tile_bytes, bn, L.num_experts);
+  l.smem = wna16_smem_bytes(cls, p.stages, p.x_stages, L.tile_bytes, bn, L.num_experts);
   // X [T][K] gathered by token index: one-row boxes of 64 columns (four rows per copy)
   CUtensorMap tm;
   st = encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, tokens, ldx, 64, 1);
   if (st != HQ_OK) return st;
-  if (launch_wna16(l, p, tm, x, ldx, s) != cudaSuccess) return HQ_ERR_CUDA;
+  if (launch_wna16(l, p, tm, s) != cudaSuccess) return HQ_ERR_CUDA;
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L.num_experts, L.n, L.n_pad, y, ldy, true, s) != cudaSuccess)
     return HQ_ERR_CUDA;
   g_last_plan = hq_plan_info{bn, 1, l.grid, 3, p.stages, cls, p.groups, 0};

@@ -100,7 +100,8 @@ struct GemmParams {
   int m;                    // dense: rows of X / Y
   int bn;                   // MMA N (tokens per tile), multiple of 16
   int m_tiles, num_tiles;   // dense: token tiles, output tiles (m_tiles * n_tiles)
-  int stages, groups;       // shared-memory stages; dequantiser groups
+  int stages, x_stages;     // weight-ring and activation-ring stages
+  int groups;               // dequantiser groups (for reporting)
   int stream_k;             // dense: deal K-blocks out in equal ranges (1) or whole tiles (0)
   int promote;              // one accumulator per K-block, group scale applied in fp32 by the epilogue
   long long iters;          // stream-K: tiles * k_tiles

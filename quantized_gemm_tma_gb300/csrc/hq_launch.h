@@ -47,9 +47,8 @@ struct Wna16Launch {
   int grid;
   uint32_t smem;
 };
-cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows,
-                         int64_t ldx, cudaStream_t stream);
-uint32_t wna16_smem_bytes(int cls, int stages, uint32_t tile_bytes, int bn, int num_experts);
+cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, cudaStream_t stream);
+uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts);
 int wna16_kps(int cls);  // K-blocks per shared-memory stage
 
 // gemm_fp8.cu

@@ -54,6 +54,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Add `bytes` to the current phase's expected transaction count, no arrival.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Atomic add at GPU scope with acquire-release semantics; returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -271,14 +284,16 @@ __device__ __forceinline__ void raise_error(int* status, volatile int* abort, in
 // Device-side event trace, compiled only into debug builds that define
 // HQ_ENABLE_TRACE: the first kTraceCtas CTAs record, per role slot, up to
 // kTraceEvents (globaltimer ns, tag) pairs into a per-translation-unit array.
-#if defined(HQ_ENABLE_TRACE)
+#if defined(HQ_ENABLE_TRACE) || defined(HQ_ENABLE_TRACE_CTA)
 constexpr int kTraceCtas = 8, kTraceSlots = 16, kTraceEvents = 512;
 static __device__ unsigned long long g_trace[kTraceCtas * kTraceSlots * kTraceEvents * 2];
-static __device__ unsigned long long g_trace_cta[1024 * 2];
+static __device__ unsigned long long g_trace_cta[1024 * 4];
 #define HQ_TRACE_CTA(i)                                                            \
   do {                                                                             \
-    if (blockIdx.x < 1024) ::hq::dev::g_trace_cta[blockIdx.x * 2 + (i)] = ::hq::dev::globaltimer(); \
+    if (blockIdx.x < 1024) ::hq::dev::g_trace_cta[blockIdx.x * 4 + (i)] = ::hq::dev::globaltimer(); \
   } while (0)
+#endif
+#if defined(HQ_ENABLE_TRACE)
 #define HQ_TRACE(slot, ctr, tag)                                                                          \
   do {                                                                                                    \
     if (blockIdx.x < ::hq::dev::kTraceCtas && (ctr) < ::hq::dev::kTraceEvents) {                          \
@@ -291,9 +306,11 @@ static __device__ unsigned long long g_trace_cta[1024 * 2];
     ++(ctr);                                                                                              \
   } while (0)
 #else
+#if !defined(HQ_ENABLE_TRACE_CTA)
 #define HQ_TRACE_CTA(i) \
   do {                  \
   } while (0)
+#endif
 #define HQ_TRACE(slot, ctr, tag) \
   do {                           \
   } while (0)

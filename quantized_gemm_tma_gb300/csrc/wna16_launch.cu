@@ -6,29 +6,25 @@
 
 namespace hq {
 
-cudaError_t launch_wna16_int4(const Wna16Launch&, const GemmParams&, const CUtensorMap&, const void*, int64_t,
-                              cudaStream_t);
-cudaError_t launch_wna16_int6(const Wna16Launch&, const GemmParams&, const CUtensorMap&, const void*, int64_t,
-                              cudaStream_t);
-cudaError_t launch_wna16_mxfp4(const Wna16Launch&, const GemmParams&, const CUtensorMap&, const void*, int64_t,
-                               cudaStream_t);
+cudaError_t launch_wna16_int4(const Wna16Launch&, const GemmParams&, const CUtensorMap&, cudaStream_t);
+cudaError_t launch_wna16_int6(const Wna16Launch&, const GemmParams&, const CUtensorMap&, cudaStream_t);
+cudaError_t launch_wna16_mxfp4(const Wna16Launch&, const GemmParams&, const CUtensorMap&, cudaStream_t);
 
-cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows,
-                         int64_t ldx, cudaStream_t stream) {
+cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, cudaStream_t stream) {
   switch (l.fmt) {
-    case 0: return launch_wna16_int4(l, p, tmap, x_rows, ldx, stream);
-    case 1: return launch_wna16_int6(l, p, tmap, x_rows, ldx, stream);
-    case 2: return launch_wna16_mxfp4(l, p, tmap, x_rows, ldx, stream);
+    case 0: return launch_wna16_int4(l, p, tmap, stream);
+    case 1: return launch_wna16_int6(l, p, tmap, stream);
+    case 2: return launch_wna16_mxfp4(l, p, tmap, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-uint32_t wna16_smem_bytes(int cls, int stages, uint32_t tile_bytes, int bn, int num_experts) {
+uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts) {
   switch (cls) {
-    case 0: return wna16::smem_bytes<0>(stages, tile_bytes, bn, num_experts);
-    case 1: return wna16::smem_bytes<1>(stages, tile_bytes, bn, num_experts);
-    case 2: return wna16::smem_bytes<2>(stages, tile_bytes, bn, num_experts);
-    default: return wna16::smem_bytes<3>(stages, tile_bytes, bn, num_experts);
+    case 0: return wna16::smem_bytes<0>(w_stages, x_stages, tile_bytes, bn, num_experts);
+    case 1: return wna16::smem_bytes<1>(w_stages, x_stages, tile_bytes, bn, num_experts);
+    case 2: return wna16::smem_bytes<2>(w_stages, x_stages, tile_bytes, bn, num_experts);
+    default: return wna16::smem_bytes<3>(w_stages, x_stages, tile_bytes, bn, num_experts);
   }
 }
 

@@ -8,33 +8,30 @@ namespace hq {
 namespace {
 
 template <bool BF16, int CLS, bool MOE>
-cudaError_t run(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows, int64_t ldx,
-                cudaStream_t stream) {
+cudaError_t run(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, cudaStream_t stream) {
   auto k = wna16::wna16_kernel<2, BF16, CLS, MOE>;
   cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k));
   if (e != cudaSuccess) return e;
-  return launch_pdl(reinterpret_cast<const void*>(k), l.grid, wna16::threads<CLS>(), l.smem, stream, p, tmap,
-                    static_cast<const __nv_bfloat16*>(x_rows), ldx);
+  return launch_pdl(reinterpret_cast<const void*>(k), l.grid, wna16::threads<CLS>(), l.smem, stream, p, tmap);
 }
 
 template <bool BF16, bool MOE>
-cudaError_t run_cls(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows,
-                    int64_t ldx, cudaStream_t stream) {
+cudaError_t run_cls(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, cudaStream_t stream) {
   switch (l.cls) {
-    case 0: return run<BF16, 0, MOE>(l, p, tmap, x_rows, ldx, stream);
-    case 1: return run<BF16, 1, MOE>(l, p, tmap, x_rows, ldx, stream);
-    case 2: return run<BF16, 2, MOE>(l, p, tmap, x_rows, ldx, stream);
-    case 3: return run<BF16, 3, MOE>(l, p, tmap, x_rows, ldx, stream);
+    case 0: return run<BF16, 0, MOE>(l, p, tmap, stream);
+    case 1: return run<BF16, 1, MOE>(l, p, tmap, stream);
+    case 2: return run<BF16, 2, MOE>(l, p, tmap, stream);
+    case 3: return run<BF16, 3, MOE>(l, p, tmap, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_wna16_mxfp4(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, const void* x_rows,
-                              int64_t ldx, cudaStream_t stream) {
-  if (l.moe) return l.bf16 ? run_cls<true, true>(l, p, tmap, x_rows, ldx, stream) : cudaErrorInvalidValue;
-  return l.bf16 ? run_cls<true, false>(l, p, tmap, x_rows, ldx, stream) : cudaErrorInvalidValue;
+cudaError_t launch_wna16_mxfp4(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap,
+                              cudaStream_t stream) {
+  if (l.moe) return l.bf16 ? run_cls<true, true>(l, p, tmap, stream) : cudaErrorInvalidValue;
+  return l.bf16 ? run_cls<true, false>(l, p, tmap, stream) : cudaErrorInvalidValue;
 }
 
 }  // namespace hq
