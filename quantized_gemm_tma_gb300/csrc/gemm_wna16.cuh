@@ -861,8 +861,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       }
       if (partial) {
         // The last of the tile's CTAs sums every partial in CTA (= K) order.
-        // Partials are [slot][row][bn] fp32, one contiguous run per row.
-        // __syncwarp orders the lanes' stores before lane 0's release.
+        // Partials are [slot][row][bn] fp32, one contiguous run per row.  Every
+        // lane fences its own stores before lane 0 counts the warp in, and
+        // fences again before reading the other CTAs' partials.
+        dev::fence_acq_rel_gpu();
         __syncwarp();
         const long long T = p.iters;
         const int Gc = static_cast<int>(gridDim.x);
@@ -873,8 +875,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         int last = 0;
         if (lane == 0) last = (dev::atom_add_acq_rel_gpu(ctr, 1) == cl - cf) ? 1 : 0;
         last = __shfl_sync(0xffffffffu, last, 0);
-        __syncwarp();
         if (last) {
+          dev::fence_acq_rel_gpu();
+          // 16 columns at a time, contributors summed in CTA order
           for (int ch = 0; ch * 16 < u.rows; ++ch) {
             float v[16];
 #pragma unroll 1

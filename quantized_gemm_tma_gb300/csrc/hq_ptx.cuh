@@ -60,6 +60,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// GPU-scope acquire-release fence (orders this thread's prior and later
+// memory operations against other CTAs' synchronisation).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Atomic add at GPU scope with acquire-release semantics; returns the old value.
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
   int old;
