@@ -55,8 +55,8 @@ BLOCK = 25         # back-to-back calls of one shape between two events
 # DRAM bytes (read + write) per launch of the WnA16 INT4 kernel, from the ncu
 # capture summarised in profiles/wna16_int4_asym_g128_n8192_k8192.md, keyed by
 # M; valid only while the kernel sources hash to `sha` (else reported null).
-NCU_TRAFFIC = {"sha": "7f238ad03aeeea22", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
-               "bytes": {16: 35_536_640, 4096: 266_105_856 + 33_297_408}}
+NCU_TRAFFIC = {"sha": "dc2927b420d57674", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
+               "bytes": {16: 35_461_376}}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
