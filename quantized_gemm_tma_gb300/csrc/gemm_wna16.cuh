@@ -678,10 +678,30 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           __syncwarp();
           if (lane == 0) dev::mbar_arrive(&s_full[si]);
         }
-        // the weight stage is free once its codes are in registers
+        // convert first: the arithmetic covers the previous K-block's TMEM
+        // stores still in flight and the MMA that frees this K-block's slot
+        uint32_t o[G][16];
+        if (real) {
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
+              if (p.channel || promote) dq_int4<BF16, false>(qc[i], zz[i], ss[i], o[i]);
+              else dq_int4<BF16, true>(qc[i], zz[i], ss[i], o[i]);
+            } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
+              const uint32_t c2 = (magic_half<BF16>() + zz[i]) * 0x00010001u;
+              if (p.channel || promote) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o[i]);
+              else dq_int6<BF16, true>(qc[i], qh[i], c2, ss[i] * 0x00010001u, o[i]);
+            } else {
+              dq_mxfp4(qc[i], ss[i], o[i]);
+            }
+          }
+        }
+        // The weight stage is free once every lane has consumed its codes: the
+        // conversion above used them, so no lane's shared-memory load can still
+        // be in flight when lane 0 releases the stage to the next tensor copy.
         __syncwarp();
         if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
-        // publish the previous K-block's A slot while this one converts
+        // publish the previous K-block's A slot
         if (pend >= 0) {
           dev::tmem_st_wait();
           dev::tc_fence_before();
@@ -698,21 +718,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           if (trace_me) HQ_TRACE(5 + gi, tr, (6ull << 24) | ts);
           dev::tc_fence_after();
 #pragma unroll
-          for (int i = 0; i < G; ++i) {
-            const int c = sub * G + i;
-            uint32_t o[16];
-            if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
-              if (p.channel || promote) dq_int4<BF16, false>(qc[i], zz[i], ss[i], o);
-              else dq_int4<BF16, true>(qc[i], zz[i], ss[i], o);
-            } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
-              const uint32_t c2 = (magic_half<BF16>() + zz[i]) * 0x00010001u;
-              if (p.channel || promote) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o);
-              else dq_int6<BF16, true>(qc[i], qh[i], c2, ss[i] * 0x00010001u, o);
-            } else {
-              dq_mxfp4(qc[i], ss[i], o);
-            }
-            dev::tmem_st16(a_lane + slot * 64 + c * 16, o);
-          }
+          for (int i = 0; i < G; ++i) dev::tmem_st16(a_lane + slot * 64 + (sub * G + i) * 16, o[i]);
           pend = slot;
           if (trace_me) HQ_TRACE(5 + gi, tr, (7ull << 24) | ts);
           ++ca;
@@ -877,24 +883,42 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           dev::fence_acq_rel_gpu();
-          // 16 columns at a time, contributors summed in CTA order
+          // 16 columns at a time, contributors summed in CTA order; two
+          // contributors' loads are in flight together
           for (int ch = 0; ch * 16 < u.rows; ++ch) {
             float v[16];
-#pragma unroll 1
-            for (int c = cf; c <= cl; ++c) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            auto part = [&](int c) {
               const long long begin = static_cast<long long>(c) * T / Gc;
               const int slot = 2 * c + (begin >= x0 ? 0 : 1);
-              const float4* src =
-                  reinterpret_cast<const float4*>(p.partials + (static_cast<size_t>(slot) * kTileN + r) * bn + ch * 16);
-              float4 t[4];
+              return reinterpret_cast<const float4*>(p.partials + (static_cast<size_t>(slot) * kTileN + r) * bn + ch * 16);
+            };
+#pragma unroll 1
+            for (int c = cf; c <= cl; c += 2) {
+              const bool two = c + 1 <= cl;
+              const float4* sa = part(c);
+              const float4* sb = part(two ? c + 1 : c);
+              float4 ta[4], tb[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) t[i] = __ldcg(src + i);
+              for (int i = 0; i < 4; ++i) ta[i] = __ldcg(sa + i);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) tb[i] = __ldcg(sb + i);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                v[4 * i + 0] = (c == cf) ? t[i].x : v[4 * i + 0] + t[i].x;
-                v[4 * i + 1] = (c == cf) ? t[i].y : v[4 * i + 1] + t[i].y;
-                v[4 * i + 2] = (c == cf) ? t[i].z : v[4 * i + 2] + t[i].z;
-                v[4 * i + 3] = (c == cf) ? t[i].w : v[4 * i + 3] + t[i].w;
+                v[4 * i + 0] = (c == cf) ? ta[i].x : v[4 * i + 0] + ta[i].x;
+                v[4 * i + 1] = (c == cf) ? ta[i].y : v[4 * i + 1] + ta[i].y;
+                v[4 * i + 2] = (c == cf) ? ta[i].z : v[4 * i + 2] + ta[i].z;
+                v[4 * i + 3] = (c == cf) ? ta[i].w : v[4 * i + 3] + ta[i].w;
+              }
+              if (two) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  v[4 * i + 0] += tb[i].x;
+                  v[4 * i + 1] += tb[i].y;
+                  v[4 * i + 2] += tb[i].z;
+                  v[4 * i + 3] += tb[i].w;
+                }
               }
             }
             if (n_ok) {
