@@ -290,7 +290,7 @@ hq_status hq_status_read(void* workspace, int32_t clear, hq_stream_t stream, int
  */
 typedef struct {
   int32_t bn;          /* tokens per output tile (MMA N for WnA16, M side for FP8) */
-  int32_t splits;      /* FP8: split-K factor; WnA16: 1 = whole tiles, 0 = stream-K */
+  int32_t splits;      /* FP8: split-K factor; WnA16: 1 = whole tiles, 0 = stream-K, 2 = 2-CTA cluster split */
   int32_t grid;        /* CTAs of the GEMM kernel */
   int32_t launches;    /* kernels launched by the call */
   int32_t stages;      /* shared-memory pipeline stages */

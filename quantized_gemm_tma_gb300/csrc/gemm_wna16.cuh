@@ -275,7 +275,15 @@ struct Sched {
 
   __device__ __forceinline__ bool next(const GemmParams& p, const int* s_tile_off, const int* s_row_off, Unit& u) {
     if constexpr (!MOE) {
-      if (p.stream_k) {
+      if (p.cluster == 2) {
+        // one tile per 2-CTA cluster: rank 0 the lower half of K, rank 1 the rest
+        if (w != static_cast<int>(blockIdx.x)) return false;
+        u.tile = blockIdx.x >> 1;
+        const int kmid = p.k_tiles / 2;
+        u.kb0 = (blockIdx.x & 1) ? kmid : 0;
+        u.kb1 = (blockIdx.x & 1) ? p.k_tiles : kmid;
+        w = -1;
+      } else if (p.stream_k) {
         if (it >= it_end) return false;
         u.tile = static_cast<int>(it / p.k_tiles);
         u.kb0 = static_cast<int>(it - static_cast<long long>(u.tile) * p.k_tiles);
@@ -361,10 +369,14 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   uint64_t* k_full = tear + 1;              // promotion: [ISS][kKRing]
   uint64_t* k_empty = k_full + 2 * kKRing;  // promotion: [ISS][kKRing]
   uint64_t* s_full = k_empty + 2 * kKRing;  // promotion: [G][kSRing]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 2 * kSRing);
+  uint64_t* red_full = s_full + 2 * kSRing;  // cluster split: the peer's half arrived
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* s_scale = reinterpret_cast<float*>(tmem_slot + 4);  // promotion: [G][kSRing][128]
-  int* s_tok = reinterpret_cast<int*>(s_scale + (CLS == 0 ? 2 * kSRing * kTileN : 0));  // MoE: token per row
+  // promotion: [G][kSRing][128], 16-byte aligned
+  float* s_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16 +
+                                            ((16u - (dev::smem_u32(tmem_slot) & 15u)) & 15u));
+  float* s_red = s_scale + (CLS == 0 ? 2 * kSRing * kTileN : 0);  // cluster split: [128][16] fp32 (16-byte aligned)
+  int* s_tok = reinterpret_cast<int*>(s_red + (CLS == 0 ? kTileN * 16 : 0));  // MoE: token per row
   int* s_tile_off = s_tok + (MOE ? BNMAX : 0);
   int* s_row_off = s_tile_off + (MOE ? p.num_experts + 1 : 0);
 
@@ -395,6 +407,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       dev::mbar_init(&k_empty[k], kEpiWarps);
     }
     for (int k = 0; k < 2 * kSRing; ++k) dev::mbar_init(&s_full[k], 4);
+    dev::mbar_init(red_full, kEpiWarps);
     *abort_flag = 0;
     dev::fence_barrier_init();
   }
@@ -757,7 +770,35 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       float* pslot = partial ? p.partials + static_cast<size_t>(2 * blockIdx.x + (ui == 0 ? 0 : 1)) * bn * kTileN
                              : nullptr;
       // columns [16 ch, 16 ch + 16) of this row: partial, MoE row or Y
-      auto emit16 = [&](int ch, const float (&v)[16]) {
+      auto emit16 = [&](int ch, const float (&vin)[16]) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = vin[i];
+        if constexpr (CLS == 0 && !MOE) {
+          if (p.cluster == 2) {
+            // bn <= 16: one chunk.  Rank 1 hands its half-K sums to rank 0
+            // through distributed shared memory; rank 0 adds them after its
+            // own (K order) and writes Y.
+            const uint32_t red_row = dev::smem_u32(s_red + r * 16);
+            if (blockIdx.x & 1) {
+              const uint32_t dst = dev::map_shared(red_row, 0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dev::st_cluster_v4(dst + 16 * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              dev::fence_acq_rel_cluster();
+              __syncwarp();
+              if (lane == 0) dev::mbar_arrive_remote(dev::map_shared(dev::smem_u32(red_full), 0));
+              return;
+            }
+            bool got = dev::mbar_wait_cluster(red_full, 0, abort_flag);
+            got = __all_sync(0xffffffffu, got) != 0;
+            if (!got) {
+              if (lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
+              return;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] += s_red[r * 16 + i];
+          }
+        }
         if (partial) {
           float4* dst = reinterpret_cast<float4*>(pslot + static_cast<size_t>(r) * bn + ch * 16);
 #pragma unroll
@@ -967,8 +1008,8 @@ inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int 
   const uint32_t w = static_cast<uint32_t>(w_stages) * ((C::kKps * tile_bytes + 1023u) & ~1023u);
   const uint32_t x = static_cast<uint32_t>(x_stages) * 2u * C::kKps * static_cast<uint32_t>(bn) * 128u;
   const uint32_t bars =
-      (2u * w_stages + 2u * x_stages + 2u * kASlots + 2u * C::kDacc + 1u + 4u * kKRing + 2u * kSRing) * 8u + 16u;
-  const uint32_t scales = CLS == 0 ? 4u * 2u * kSRing * kTileN : 0u;
+      (2u * w_stages + 2u * x_stages + 2u * kASlots + 2u * C::kDacc + 1u + 4u * kKRing + 2u * kSRing + 1u) * 8u + 16u;
+  const uint32_t scales = CLS == 0 ? 4u * 2u * kSRing * kTileN + 4u * kTileN * 16u : 0u;
   const uint32_t moe = 4u * (C::kBnMax + 2u * (num_experts + 1));
   return w + x + bars + scales + moe + 1024u /* alignment slack */;
 }

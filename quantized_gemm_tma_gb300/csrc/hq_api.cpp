@@ -340,7 +340,7 @@ constexpr int kMaxSplitTiles = 512;
 constexpr size_t kCounterBytes = sizeof(int) * kMaxSplitTiles * 8;
 
 struct DensePlan {
-  int cls, bn, m_tiles, tiles, stages, x_stages, groups, grid, stream_k;
+  int cls, bn, m_tiles, tiles, stages, x_stages, groups, grid, stream_k, cluster;
   long long iters;
   uint32_t smem;
 };
@@ -427,11 +427,20 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   const int forced_sk = env_int("HQ_FORCE_SPLITK", 0);  // 1: stream-K on, 2: off
   if (forced_sk == 1 && !(flags & HQ_FLAG_BATCH_INVARIANT) && p.tiles <= kMaxSplitTiles) p.stream_k = 1;
   if (forced_sk == 2) p.stream_k = 0;
+  // A tile per 2-CTA cluster, K split in halves and combined through shared
+  // memory, when that fills most SMs: no cross-CTA global reduction at all.
+  p.cluster = 1;
+  if (p.cls == 0 && !(flags & HQ_FLAG_BATCH_INVARIANT) && L.k_tiles >= 2 && 2 * p.tiles <= sms &&
+      8 * p.tiles >= 3 * sms && env_int("HQ_FORCE_SPLITK", 0) == 0) {
+    p.cluster = 2;
+    p.stream_k = 0;
+  }
   plan_stages(p.cls, L, p.bn, 0, smem_optin, &p.stages, &p.x_stages, &p.groups);
   p.smem = wna16_smem_bytes(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn, 0);
   // stream-K: at least 8 K-blocks per CTA, so that partial tiles stay few
-  p.grid = p.stream_k ? static_cast<int>(std::min<long long>(sms, std::max<long long>(1, (p.iters + 7) / 8)))
-                      : std::min(sms, p.tiles);
+  p.grid = p.cluster == 2 ? 2 * p.tiles
+           : p.stream_k ? static_cast<int>(std::min<long long>(sms, std::max<long long>(1, (p.iters + 7) / 8)))
+                        : std::min(sms, p.tiles);
   return p;
 }
 
@@ -540,7 +549,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = m;
   p.bn = pl.bn; p.m_tiles = pl.m_tiles; p.num_tiles = pl.tiles;
   p.stages = pl.stages; p.x_stages = pl.x_stages; p.groups = pl.groups;
-  p.stream_k = pl.stream_k; p.iters = pl.iters;
+  p.stream_k = pl.stream_k; p.iters = pl.iters; p.cluster = pl.cluster;
   p.promote = (pl.cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
   p.idesc = idesc_f16(atype == HQ_A_BF16, 128, pl.bn);
   p.y = y; p.ldy = ldy;
@@ -560,7 +569,8 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   l.moe = false;
   l.grid = pl.grid;
   l.smem = pl.smem;
-  g_last_plan = hq_plan_info{pl.bn, pl.stream_k ? 0 : 1, pl.grid, 1, pl.stages, pl.cls, pl.groups, 0};
+  g_last_plan = hq_plan_info{pl.bn, pl.cluster == 2 ? 2 : (pl.stream_k ? 0 : 1), pl.grid, 1, pl.stages, pl.cls,
+                             pl.groups, 0};
   if (env_int("HQ_TRACE", 0))
     std::fprintf(stderr, "hq_gemm: m=%d n=%d k=%d bn=%d cls=%d stream_k=%d grid=%d stages=%d groups=%d smem=%u\n", m,
                  L.n, L.k, pl.bn, pl.cls, pl.stream_k, pl.grid, pl.stages, pl.groups, pl.smem);
@@ -644,7 +654,7 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   p.row_scale = L.channel ? reinterpret_cast<const float*>(wt + L.row_off) : nullptr;
   p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
   p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = tokens;
-  p.bn = bn; p.m_tiles = 0; p.num_tiles = 0; p.stream_k = 0; p.iters = 0;
+  p.bn = bn; p.m_tiles = 0; p.num_tiles = 0; p.stream_k = 0; p.iters = 0; p.cluster = 1;
   p.promote = (cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
   p.idesc = idesc_f16(true, 128, bn);
   p.status = reinterpret_cast<int*>(ws);

@@ -16,18 +16,24 @@ cudaError_t ensure_smem_optin(const void* kernel);
 // Launch with programmatic stream serialization: the grid may begin its
 // prologue while the previous grid on the stream finishes; the kernel itself
 // waits (griddepcontrol.wait) before it touches global memory.
+// `cluster` > 1 launches clusters of that many consecutive CTAs.
 template <typename... Args>
-cudaError_t launch_pdl(const void* kernel, int grid, int block, uint32_t smem, cudaStream_t stream, Args... args) {
-  cudaLaunchAttribute attr[1];
+cudaError_t launch_pdl(const void* kernel, int grid, int block, uint32_t smem, cudaStream_t stream, int cluster,
+                       Args... args) {
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster > 1 ? cluster : 1);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(static_cast<unsigned>(block));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   void* argv[] = {static_cast<void*>(&args)...};
   return cudaLaunchKernelExC(&cfg, kernel, argv);
 }

@@ -12,7 +12,8 @@ cudaError_t run(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tm
   auto k = wna16::wna16_kernel<2, BF16, CLS, MOE>;
   cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k));
   if (e != cudaSuccess) return e;
-  return launch_pdl(reinterpret_cast<const void*>(k), l.grid, wna16::threads<CLS>(), l.smem, stream, p, tmap);
+  return launch_pdl(reinterpret_cast<const void*>(k), l.grid, wna16::threads<CLS>(), l.smem, stream, p.cluster, p,
+                    tmap);
 }
 
 template <bool BF16, bool MOE>
