@@ -343,6 +343,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   constexpr int G = KPS;                 // dequantiser groups
   constexpr int WG = kDqWarps / G;        // warps per group
   constexpr int DA = kASlots / G;         // A slots per group
+  // MoE with wide tiles gathers activation rows with per-lane cp.async (one
+  // tile::gather4 copy moves only 512 bytes, too few for bn >= 64)
+  constexpr bool kLaneGather = MOE && CLS >= 1;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from smem_raw by an offset so that the
   // compiler keeps shared-memory addressing for every access through it
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       dev::mbar_init(&w_empty[s], kDqWarps);
     }
     for (int s = 0; s < SX; ++s) {
-      dev::mbar_init(&x_full[s], 1);
+      dev::mbar_init(&x_full[s], kLaneGather ? 32u : 1u);
       dev::mbar_init(&x_empty[s], ISS);
     }
     for (int a = 0; a < kASlots; ++a) {
@@ -521,7 +524,27 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           break;
         }
         uint8_t* xs = x_st + rg.s * x_stage;
-        if (lane == 0) {
+        if constexpr (kLaneGather) {
+          // rows r = lane + 32 j, sixteen 16-byte chunks per row and K-block
+          // (two 128-byte swizzled slabs); columns past K are zero-filled
+          for (int r = static_cast<int>(lane); r < u.rows; r += 32) {
+            const __nv_bfloat16* src_row = p.x_rows + static_cast<int64_t>(s_tok[r]) * p.ldx;
+            for (int z = 0; z < 2 * cnt; ++z) {
+              const int col0 = (2 * kb + z) * 64;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const int col = col0 + c * 8;
+                const bool valid = col < p.k;
+                uint8_t* dst = xs + z * slab + r * 128 + ((c ^ (r & 7)) << 4);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dev::smem_u32(dst)),
+                             "l"(valid ? src_row + col : src_row), "r"(valid ? 16u : 0u)
+                             : "memory");
+              }
+            }
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dev::smem_u32(&x_full[rg.s]))
+                       : "memory");
+        } else if (lane == 0) {
           dev::mbar_arrive_expect_tx(&x_full[rg.s], 2u * cnt * slab);
           for (int z = 0; z < 2 * cnt; ++z) {
             const int x = (2 * kb + z) * 64;
@@ -544,6 +567,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       if constexpr (MOE) __syncwarp();  // s_tok is rewritten for the next unit
     }
     if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
+    if constexpr (kLaneGather) asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0) {
       for (int s = 0; s < SX && s < issued; ++s) {
         const int last = ((issued - 1 - s) / SX) * SX + s;
@@ -595,6 +619,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               break;
             }
             HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
+            if constexpr (kLaneGather) dev::fence_proxy_async_smem();  // cp.async rows -> tensor-core reads
             dev::tc_fence_after();
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + 2u * pidx * slab;
             const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(slot) * 64u;
@@ -769,6 +794,23 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       const bool partial = !MOE && p.stream_k && (u.kb0 > 0 || u.kb1 < p.k_tiles);
       float* pslot = partial ? p.partials + static_cast<size_t>(2 * blockIdx.x + (ui == 0 ? 0 : 1)) * bn * kTileN
                              : nullptr;
+      // MoE: the unit's routed pairs and their weights, column 32k + lane in
+      // register k of each lane (loaded once per unit, broadcast per column)
+      constexpr int kMoeRegs = MOE ? BNMAX / 32 + (BNMAX % 32 ? 1 : 0) : 1;
+      [[maybe_unused]] int f_reg[kMoeRegs];
+      [[maybe_unused]] float w_reg[kMoeRegs];
+      if constexpr (MOE) {
+#pragma unroll
+        for (int k = 0; k < kMoeRegs; ++k) {
+          const int col = 32 * k + static_cast<int>(lane);
+          f_reg[k] = col < u.rows ? p.perm[u.row0 + col] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kMoeRegs; ++k) {
+          const int col = 32 * k + static_cast<int>(lane);
+          w_reg[k] = col < u.rows ? p.topk_w[f_reg[k]] : 0.f;
+        }
+      }
       // columns [16 ch, 16 ch + 16) of this row: partial, MoE row or Y
       auto emit16 = [&](int ch, const float (&vin)[16]) {
         float v[16];
@@ -805,16 +847,31 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           return;
         }
+        [[maybe_unused]] int fr = 0;
+        [[maybe_unused]] float wr = 0.f;
+        if constexpr (MOE) {
+          // columns 16 ch .. 16 ch + 15 live in register ch / 2, lanes 16 (ch & 1) + i
+#pragma unroll
+          for (int k = 0; k < kMoeRegs; ++k)
+            if ((ch >> 1) == k) {
+              fr = f_reg[k];
+              wr = w_reg[k];
+            }
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int col = ch * 16 + i;
+          if constexpr (MOE) {
+            const int f = __shfl_sync(0xffffffffu, fr, ((ch & 1) << 4) + i);
+            const float wf = __shfl_sync(0xffffffffu, wr, ((ch & 1) << 4) + i);
+            if (col < u.rows && n_ok) p.zbuf[static_cast<size_t>(f) * p.n_pad + n] = v[i] * rs * wf;
+            continue;
+          }
           if (col >= u.rows) continue;
           if (partial) {
             // stored below, 16 at a time
           } else if (n_ok) {
             if constexpr (MOE) {
-              const int f = p.perm[u.row0 + col];
-              p.zbuf[static_cast<size_t>(f) * p.n_pad + n] = v[i] * rs * p.topk_w[f];
             } else {
               const size_t off = static_cast<size_t>(u.row0 + col) * p.ldy + n;
               if constexpr (BF16) reinterpret_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(v[i] * rs);

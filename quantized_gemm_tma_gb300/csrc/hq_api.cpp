@@ -660,6 +660,7 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   p.status = reinterpret_cast<int*>(ws);
   p.num_experts = L.num_experts; p.topk = topk;
   p.tile_offsets = tile_off; p.expert_offsets = exp_off; p.perm = perm; p.topk_w = topk_w; p.zbuf = zbuf;
+  p.x_rows = static_cast<const __nv_bfloat16*>(x); p.ldx = ldx;
   plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups);
   if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
   Wna16Launch l{};

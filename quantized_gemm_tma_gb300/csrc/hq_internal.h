@@ -38,6 +38,8 @@
 
 #include "hq.h"
 
+struct __nv_bfloat16;
+
 namespace hq {
 
 constexpr int kTileN = 128;
@@ -119,6 +121,8 @@ struct GemmParams {
   const int* expert_offsets;// [E+1] row prefix
   const int* perm;          // [T*topk]
   const float* topk_w;      // [T*topk]
+  const __nv_bfloat16* x_rows;  // MoE: activations [T][ldx] (per-lane row gather)
+  int64_t ldx;
   float* zbuf;              // [T*topk][n_pad] weighted per-pair outputs
 };
 
