@@ -75,11 +75,12 @@ struct Cls<3> { static constexpr int kBnMax = 256, kKps = 1, kIss = 1, kDacc = 1
 constexpr int kEpiWarps = 4;
 constexpr int kDqWarps = 16;
 constexpr int kASlots = 4;
+constexpr int kABars = 8;  // A-slot barriers: kASlots slots, or 4 streams x 2 half slots
 constexpr int kDqWarp0 = kEpiWarps;                        // first dequant warp
 constexpr int kProdWarp = kDqWarp0 + kDqWarps;             // weight producer warp
 constexpr int kXProdWarp = kProdWarp + 1;                  // activation producer warp
 constexpr int kIssWarp0 = kXProdWarp + 1;                  // first MMA issuer warp
-constexpr int kKRing = 4;  // promotion: per-K-block accumulators per issuer (class 0)
+constexpr int kKRing = 8;  // promotion: per-K-block accumulators over all issuers (class 0)
 constexpr int kSRing = 8;  // promotion: per-K-block row scales per group, in shared memory
 constexpr uint32_t kACol0 = 0;
 constexpr uint32_t kAccCol0 = 256;
@@ -87,6 +88,14 @@ constexpr uint32_t kTmemCols = 512;
 
 template <int CLS>
 constexpr int threads() { return 32 * (kIssWarp0 + Cls<CLS>::kIss); }
+
+// Cluster split of a wide tile: rank 1's fp32 sums travel through rank 0's
+// ring area as [128 rows][kXchgLd] (4 floats of padding per row keep the
+// per-row 16-byte accesses of a warp on distinct banks).
+template <int CLS>
+constexpr int kXchgLd() { return Cls<CLS>::kBnMax + 4; }
+template <int CLS>
+constexpr uint32_t xchg_bytes() { return static_cast<uint32_t>(kTileN * kXchgLd<CLS>() * 4); }
 
 // ---------------------------------------------------------------- packed math
 template <bool BF16>
@@ -343,6 +352,15 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   constexpr int G = KPS;                 // dequantiser groups
   constexpr int WG = kDqWarps / G;        // warps per group
   constexpr int DA = kASlots / G;         // A slots per group
+  // Two K-blocks per stage: the dequantisers work as four streams.  Stream t
+  // takes K-block (t & 1) of every stage of parity (t >> 1), a whole K-block
+  // of its rows per warp, so the four warps sharing a scheduler are at
+  // different points of their pipelines instead of in lock step.
+  constexpr bool kStream = KPS == 2;
+  // Stream issuers: with four issuers, issuer t takes stream t's K-blocks;
+  // with two, issuer p takes position p of every stage (streams p and 2 + p).
+  constexpr bool kIssPerStream = kStream && ISS == 4;
+  constexpr int KR = kKRing / ISS;  // promotion: accumulator ring per issuer
   // MoE with wide tiles gathers activation rows with per-lane cp.async (one
   // tile::gather4 copy moves only 512 bytes, too few for bn >= 64)
   constexpr bool kLaneGather = MOE && CLS >= 1;
@@ -365,13 +383,14 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   uint64_t* x_full = w_empty + SW;
   uint64_t* x_empty = x_full + SX;
   uint64_t* a_full = x_empty + SX;
-  uint64_t* a_empty = a_full + kASlots;
-  uint64_t* acc_full = a_empty + kASlots;
+  constexpr int NAB = kStream ? kABars : kASlots;  // A-slot barriers of each kind
+  uint64_t* a_empty = a_full + NAB;
+  uint64_t* acc_full = a_empty + NAB;
   uint64_t* acc_empty = acc_full + DACC;
   uint64_t* tear = acc_empty + DACC;
-  uint64_t* k_full = tear + 1;              // promotion: [ISS][kKRing]
-  uint64_t* k_empty = k_full + 2 * kKRing;  // promotion: [ISS][kKRing]
-  uint64_t* s_full = k_empty + 2 * kKRing;  // promotion: [G][kSRing]
+  uint64_t* k_full = tear + 1;          // promotion: [ISS][KR]
+  uint64_t* k_empty = k_full + kKRing;  // promotion: [ISS][KR]
+  uint64_t* s_full = k_empty + kKRing;  // promotion: [G][kSRing]
   uint64_t* red_full = s_full + 2 * kSRing;  // cluster split: the peer's half arrived
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -390,14 +409,14 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < SW; ++s) {
       dev::mbar_init(&w_full[s], 1);
-      dev::mbar_init(&w_empty[s], kDqWarps);
+      dev::mbar_init(&w_empty[s], kStream ? 8 : kDqWarps);  // streams: the two of the stage's parity
     }
     for (int s = 0; s < SX; ++s) {
       dev::mbar_init(&x_full[s], kLaneGather ? 32u : 1u);
       dev::mbar_init(&x_empty[s], ISS);
     }
-    for (int a = 0; a < kASlots; ++a) {
-      dev::mbar_init(&a_full[a], WG);
+    for (int a = 0; a < NAB; ++a) {
+      dev::mbar_init(&a_full[a], kStream ? 4 : WG);
       dev::mbar_init(&a_empty[a], 1);
     }
     for (int b = 0; b < DACC; ++b) {
@@ -405,7 +424,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       dev::mbar_init(&acc_empty[b], kEpiWarps);
     }
     dev::mbar_init(tear, ISS);
-    for (int k = 0; k < 2 * kKRing; ++k) {
+    for (int k = 0; k < kKRing; ++k) {
       dev::mbar_init(&k_full[k], 1);
       dev::mbar_init(&k_empty[k], kEpiWarps);
     }
@@ -422,6 +441,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   dev::tc_fence_before();
   __syncthreads();
   dev::tc_fence_after();
+  // 2-CTA cluster: the peer's barriers must be initialised before the first
+  // remote arrive; the epilogue waits on this before touching the peer
+  if (!MOE && p.cluster == 2) dev::cluster_arrive();
   const uint32_t tmem = *tmem_slot;
   [[maybe_unused]] int tr0 = 0;
   if (threadIdx.x == 0) HQ_TRACE(15, tr0, 0);
@@ -579,6 +601,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     }
   } else if (warp >= kIssWarp0) {
     // ============================================================ MMA issuers
+    // One thread per issuer warp walks the schedule, waits and issues.
     const int pidx = warp - kIssWarp0;
     if (lane == 0) {
       Sched<MOE> sc;
@@ -590,6 +613,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       bool ok = true;
       int ui = 0;
       [[maybe_unused]] int tr = 0, ts = 0;
+      [[maybe_unused]] uint32_t cs0 = 0, cs1 = 0;  // streams: K-blocks taken from streams pidx, 2 + pidx
+      [[maybe_unused]] uint32_t S = 0;           // streams: stage counter
       Unit u;
       while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
         // whole-unit accumulator (double-buffered across units) unless promoting
@@ -610,11 +635,48 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             break;
           }
           HQ_TRACE(1 + pidx, tr, (2ull << 24) | ts);
-          if (pidx < cnt) {
+          // stream mode: the K-block at position q of this stage comes from
+          // stream 2 (S & 1) + q, in two halves (64 K each) published separately
+          const int q = kIssPerStream ? (pidx & 1) : pidx;
+          const bool mine = !kIssPerStream || (S & 1u) == static_cast<uint32_t>(pidx >> 1);
+          if (kStream && mine && q < cnt) {
+            const int t = 2 * static_cast<int>(S & 1u) + q;
+            const uint32_t aph = ((S & 1u) ? cs1 : cs0) & 1u;
+            const int ks = pidx * KR + static_cast<int>(ck % KR);
+            if (promote && !dev::mbar_wait(&k_empty[ks], ((ck / KR) & 1u) ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + 2u * q * slab;
+            const uint32_t d_tmem = promote ? tmem + kAccCol0 + static_cast<uint32_t>(ks * BNMAX)
+                                            : tmem + kAccCol0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
+            const bool fresh = promote || first;
+            for (int h = 0; h < 2 && ok; ++h) {
+              if (!dev::mbar_wait(&a_full[2 * t + h], aph, abort_flag)) {
+                ok = false;
+                break;
+              }
+              HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
+              if constexpr (kLaneGather) dev::fence_proxy_async_smem();  // cp.async rows -> tensor-core reads
+              dev::tc_fence_after();
+              const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(t * 64 + h * 32);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bdesc = dev::sw128_desc(xs + h * slab + kk * 32);
+                dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && h == 0 && kk == 0) ? 0u : 1u);
+              }
+              dev::tc_commit(&a_empty[2 * t + h]);
+            }
+            if (!ok) break;
+            if (promote) dev::tc_commit(&k_full[ks]);
+            ++ck;
+            if (S & 1u) ++cs1; else ++cs0;
+            first = false;
+          } else if (!kStream && pidx < cnt) {
             const int slot = pidx * DA + static_cast<int>(cu % DA);
-            const int ks = pidx * kKRing + static_cast<int>(ck % kKRing);
+            const int ks = pidx * KR + static_cast<int>(ck % KR);
             if (!dev::mbar_wait(&a_full[slot], (cu / DA) & 1u, abort_flag) ||
-                (promote && !dev::mbar_wait(&k_empty[ks], ((ck / kKRing) & 1u) ^ 1u, abort_flag))) {
+                (promote && !dev::mbar_wait(&k_empty[ks], ((ck / KR) & 1u) ^ 1u, abort_flag))) {
               ok = false;
               break;
             }
@@ -635,12 +697,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             if (promote) dev::tc_commit(&k_full[ks]);
             ++cu;
             ++ck;
+            first = false;
           }
           dev::tc_commit(&x_empty[rx.s]);
           HQ_TRACE(1 + pidx, tr, (4ull << 24) | ts);
           ++ts;
+          ++S;
           rx.next(SX);
-          first = false;
         }
         if (!ok) break;
         if (!promote) dev::tc_commit(&acc_full[buf]);
@@ -649,6 +712,132 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       if (!ok) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
       dev::tc_commit(tear);  // arrives once every MMA this thread issued has completed
     }
+  } else if (kStream && warp >= kDqWarp0) {
+    // ============================================================ dequantisers (streams)
+    const int dw = warp - kDqWarp0;
+    const int t = dw >> 2;                  // stream
+    const uint32_t sg = static_cast<uint32_t>(t >> 1);  // parity of the stages it takes
+    const int pos = t & 1;                  // K-block of those stages it converts
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + static_cast<int>(lane);  // weight row within the tile (TMEM lane)
+    const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol0 + static_cast<uint32_t>(t * 64);
+    const bool promote = CLS == 0 && p.promote;
+    Sched<MOE> sc;
+    sc.init(p);
+    Ring rg;
+    uint32_t ca = 0;    // this stream's K-blocks so far (one use of each half slot per K-block)
+    uint32_t cpos = 0;  // K-blocks at position pos so far, both parities (scale ring index)
+    uint32_t S = 0;     // stage counter
+    bool ok = true;
+    [[maybe_unused]] int tr = 0, ts = 0;
+    const bool trace_me = quarter == 0 && lane == 0;
+    uint32_t zrow = 0;
+    // chunks c0, c0 + 1 (64 K) of this row -> 2 x 16 pairs
+    auto convert2 = [&](const uint8_t* wsm, int c0, uint32_t (&o)[2][16]) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int c = c0 + i;
+        const uint4 q = *reinterpret_cast<const uint4*>(wsm + (c * kTileN + r) * 16);
+        uint32_t z = zrow, sc16 = 0;
+        if constexpr (FMT == static_cast<int>(WFmt::MXFP4)) {
+          sc16 = wsm[p.scale_off + r * 4 + c];
+        } else if (!p.channel) {
+          const int g = (p.g_kb > 1) ? (32 * c) / p.group_k : 0;
+          sc16 = reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r * p.g_kb + g];
+          if (p.has_zeros) z = wsm[p.zero_off + r * p.g_kb + g];
+        }
+        if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
+          if (p.channel || promote) dq_int4<BF16, false>(q, z, sc16, o[i]);
+          else dq_int4<BF16, true>(q, z, sc16, o[i]);
+        } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
+          const uint2 qh = *reinterpret_cast<const uint2*>(wsm + p.hi_off + (c * kTileN + r) * 8);
+          const uint32_t c2 = (magic_half<BF16>() + z) * 0x00010001u;
+          if (p.channel || promote) dq_int6<BF16, false>(q, qh, c2, 0, o[i]);
+          else dq_int6<BF16, true>(q, qh, c2, sc16 * 0x00010001u, o[i]);
+        } else {
+          dq_mxfp4(q, sc16, o[i]);
+        }
+      }
+    };
+    // issued stores -> visible to the MMA, then count in on the half slot
+    auto publish = [&](int hs) {
+      dev::tmem_st_wait();
+      dev::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&a_full[hs]);
+    };
+    Unit u;
+    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+      const int n = u.nt * kTileN + r;
+      zrow = static_cast<uint32_t>(p.zero_sym);
+      if (p.channel && p.has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
+      for (int kb = u.kb0; kb < u.kb1; kb += KPS, ++S) {
+        const int cnt = min(KPS, u.kb1 - kb);
+        if ((S & 1u) == sg) {
+          if (!warp_wait(&w_full[rg.s], rg.ph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (trace_me) HQ_TRACE(5 + t, tr, (5ull << 24) | ts);
+          if (pos < cnt) {
+            const uint8_t* wsm = w_st + rg.s * w_stage + pos * tile_bytes;
+            // promotion: the row's group scale goes to the epilogue through a
+            // ring.  Before this write the stream has seen the MMAs of its
+            // K-block before last complete; each of them waited until the
+            // epilogue released the accumulator KR uses back, and the epilogue
+            // reads a scale before releasing its accumulator, so every scale
+            // kSRing positions back has been read.
+            if (promote) {
+              constexpr float kOpFixD = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
+              const uint32_t s16 = reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r * p.g_kb];
+              const float sf = BF16 ? __uint_as_float(s16 << 16)
+                                    : __half2float(__ushort_as_half(static_cast<unsigned short>(s16)));
+              const int si = pos * kSRing + static_cast<int>(cpos % kSRing);
+              s_scale[si * kTileN + r] = sf * kOpFixD;
+              __syncwarp();
+              if (lane == 0) dev::mbar_arrive(&s_full[si]);
+            }
+            // The first half is published after the second is converted (the
+            // arithmetic covers its TMEM stores); the second right away.
+            const uint32_t aph = (ca & 1u) ^ 1u;
+            uint32_t o[2][16];
+            convert2(wsm, 0, o);
+            if (trace_me) HQ_TRACE(5 + t, tr, (12ull << 24) | ts);
+            if (!warp_wait(&a_empty[2 * t], aph, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (trace_me) HQ_TRACE(5 + t, tr, (6ull << 24) | ts);
+            dev::tc_fence_after();
+            dev::tmem_st16(a_lane + 0, o[0]);
+            dev::tmem_st16(a_lane + 16, o[1]);
+            convert2(wsm, 2, o);
+            // every lane's codes are consumed: the stage may be refilled
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
+            publish(2 * t);
+            if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
+            if (!warp_wait(&a_empty[2 * t + 1], aph, abort_flag)) {
+              ok = false;
+              break;
+            }
+            dev::tc_fence_after();
+            dev::tmem_st16(a_lane + 32, o[0]);
+            dev::tmem_st16(a_lane + 48, o[1]);
+            publish(2 * t + 1);
+            if (trace_me) HQ_TRACE(5 + t, tr, (7ull << 24) | ts);
+            ++ca;
+          } else {
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
+          }
+        }
+        if (pos < cnt) ++cpos;
+        ++ts;
+        rg.next(SW);
+      }
+    }
+    if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
   } else if (warp >= kDqWarp0) {
     // ============================================================ dequantisers
     const int dw = warp - kDqWarp0;
@@ -734,6 +923,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             }
           }
         }
+        if (trace_me) HQ_TRACE(5 + gi, tr, (12ull << 24) | ts);
         // The weight stage is free once every lane has consumed its codes: the
         // conversion above used them, so no lane's shared-memory load can still
         // be in flight when lane 0 releases the stage to the next tensor copy.
@@ -746,6 +936,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           __syncwarp();
           if (lane == 0) dev::mbar_arrive(&a_full[pend]);
           pend = -1;
+          if (trace_me) HQ_TRACE(5 + gi, tr, (13ull << 24) | ts);
         }
         if (real) {
           const int slot = gi * DA + static_cast<int>(ca % DA);
@@ -781,7 +972,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     sc.init(p);
     bool ok = true;
     int ui = 0;
-    [[maybe_unused]] uint32_t ck[2] = {0, 0};  // promotion: K-blocks taken from each issuer's ring
+    // promotion: K-blocks taken from each issuer's accumulator ring and from
+    // each position's scale ring; stream mode: stage counter (issuer choice)
+    [[maybe_unused]] uint32_t ck0 = 0, ck1 = 0, ck2 = 0, ck3 = 0, cp0 = 0, cp1 = 0;
+    [[maybe_unused]] uint32_t S = 0;
     [[maybe_unused]] int tr = 0;
     const bool trace_me = quarter == 0 && lane == 0;
     // INT4 bf16 operands without a folded scale carry an extra 2^-7
@@ -818,6 +1012,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         for (int i = 0; i < 16; ++i) v[i] = vin[i];
         if constexpr (CLS == 0 && !MOE) {
           if (p.cluster == 2) {
+            dev::cluster_wait();
             // bn <= 16: one chunk.  Rank 1 hands its half-K sums to rank 0
             // through distributed shared memory; rank 0 adds them after its
             // own (K order) and writes Y.
@@ -891,14 +1086,18 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           for (int i = 0; i < BNMAX; ++i) tot[i] = 0.f;
           for (int kb = u.kb0; kb < u.kb1; ++kb) {
             const int q = (kb - u.kb0) & (KPS - 1);
-            const uint32_t cq = q ? ck[1] : ck[0];
-            const int ks = q * kKRing + static_cast<int>(cq % kKRing);
-            const int si = q * kSRing + static_cast<int>(cq % kSRing);
-            if (!warp_wait(&s_full[si], (cq / kSRing) & 1u, abort_flag) ||
-                !warp_wait(&k_full[ks], (cq / kKRing) & 1u, abort_flag)) {
+            const uint32_t Si = S + static_cast<uint32_t>((kb - u.kb0) / KPS);
+            const int is = kIssPerStream ? 2 * static_cast<int>(Si & 1u) + q : q;  // issuer of this K-block
+            const uint32_t cq = is == 0 ? ck0 : is == 1 ? ck1 : is == 2 ? ck2 : ck3;
+            const uint32_t cs = q ? cp1 : cp0;
+            const int ks = is * KR + static_cast<int>(cq % KR);
+            const int si = q * kSRing + static_cast<int>(cs % kSRing);
+            if (!warp_wait(&s_full[si], (cs / kSRing) & 1u, abort_flag) ||
+                !warp_wait(&k_full[ks], (cq / KR) & 1u, abort_flag)) {
               ok = false;
               break;
             }
+            if (trace_me) HQ_TRACE(9, tr, (14ull << 24) | kb);
             const float s_cur = s_scale[si * kTileN + r];
             dev::tc_fence_after();
             const uint32_t acc = tmem + lane_base + kAccCol0 + static_cast<uint32_t>(ks * BNMAX);
@@ -915,7 +1114,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             dev::tc_fence_before();
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(&k_empty[ks]);
-            if (q) ++ck[1]; else ++ck[0];
+            if (is == 0) ++ck0; else if (is == 1) ++ck1; else if (is == 2) ++ck2; else ++ck3;
+            if (q) ++cp1; else ++cp0;
           }
           if (!ok) break;
 #pragma unroll
@@ -938,25 +1138,91 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         }
         if (trace_me) HQ_TRACE(9, tr, (8ull << 24) | ui);
         dev::tc_fence_after();
-        const int nval = min(ISS, u.kb1 - u.kb0);  // issuers that took at least one K-block
+        // issuers that took at least one K-block of the unit; their partial
+        // accumulators are summed in issuer order
+        const int nk = u.kb1 - u.kb0;
+        uint32_t parts;
+        if constexpr (kIssPerStream) {
+          const int par = static_cast<int>(S & 1u);
+          parts = (1u << (2 * par)) | (nk >= 2 ? 1u << (2 * par + 1) : 0u) | (nk >= 3 ? 1u << (2 * (par ^ 1)) : 0u) |
+                  (nk >= 4 ? 1u << (2 * (par ^ 1) + 1) : 0u);
+        } else {
+          parts = (1u << min(ISS, nk)) - 1u;
+        }
+        const int is0 = __ffs(parts) - 1;
         const uint32_t acc0 = tmem + lane_base + kAccCol0 + static_cast<uint32_t>(buf * ISS * BNMAX);
-        for (int ch = 0; ch < (bn >> 4); ++ch) {
-          float v[16];
-          {
-            uint32_t a[16];
-            dev::tmem_ld16(acc0 + ch * 16, a);
-            dev::tmem_ld_wait();
+        // the issuers' partial accumulators of 16 columns, summed in issuer order
+        auto acc16 = [&](int ch, float (&v)[16]) {
+          uint32_t a[16];
+          dev::tmem_ld16(acc0 + is0 * BNMAX + ch * 16, a);
+          dev::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(a[i]);
-          }
-          for (int is = 1; is < nval; ++is) {
-            uint32_t a[16];
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(a[i]);
+          for (int is = is0 + 1; is < ISS; ++is) {
+            if (!((parts >> is) & 1u)) continue;
             dev::tmem_ld16(acc0 + is * BNMAX + ch * 16, a);
             dev::tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] += __uint_as_float(a[i]);
           }
-          emit16(ch, v);
+        };
+        bool xchg = false;
+        if constexpr (CLS >= 1 && !MOE) xchg = p.cluster == 2;
+        if (!xchg) {
+          for (int ch = 0; ch < (bn >> 4); ++ch) {
+            float v[16];
+            acc16(ch, v);
+            emit16(ch, v);
+          }
+        } else if constexpr (CLS >= 1 && !MOE) {
+          // Cluster split, wide tiles: rank 1 writes its half-K sums into
+          // rank 0's shared memory (rank 0's rings are idle once its MMAs are
+          // done, which it signals first); rank 0 adds them after its own and
+          // stores Y.
+          dev::cluster_wait();
+          const uint32_t local = dev::smem_u32(smem);
+          if (blockIdx.x & 1) {
+            bool got = dev::mbar_wait_cluster(red_full, 0, abort_flag);  // rank 0 is ready
+            if (__all_sync(0xffffffffu, got) == 0) {
+              ok = false;
+              break;
+            }
+            const uint32_t xremote = dev::map_shared(local, 0);
+            for (int ch = 0; ch < (bn >> 4); ++ch) {
+              float v[16];
+              acc16(ch, v);
+              const uint32_t dst = xremote + static_cast<uint32_t>((r * kXchgLd<CLS>() + ch * 16) * 4);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dev::st_cluster_v4(dst + 16 * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+            dev::fence_acq_rel_cluster();
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive_remote(dev::map_shared(dev::smem_u32(red_full), 0));
+          } else {
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive_remote(dev::map_shared(dev::smem_u32(red_full), 1));
+            bool got = dev::mbar_wait_cluster(red_full, 0, abort_flag);  // rank 1's sums arrived
+            if (__all_sync(0xffffffffu, got) == 0) {
+              ok = false;
+              break;
+            }
+            const float* xbuf = reinterpret_cast<const float*>(smem);
+            for (int ch = 0; ch < (bn >> 4); ++ch) {
+              float v[16];
+              acc16(ch, v);
+              const float4* src = reinterpret_cast<const float4*>(xbuf + r * kXchgLd<CLS>() + ch * 16);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 t4 = src[i];
+                v[4 * i] += t4.x;
+                v[4 * i + 1] += t4.y;
+                v[4 * i + 2] += t4.z;
+                v[4 * i + 3] += t4.w;
+              }
+              emit16(ch, v);
+            }
+          }
         }
         dev::tc_fence_before();
         __syncwarp();
@@ -1036,6 +1302,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         if (trace_me) HQ_TRACE(9, tr, ((10ull + last) << 24) | ui);
       }
       ++ui;
+      S += static_cast<uint32_t>((u.kb1 - u.kb0 + KPS - 1) / KPS);
     }
     if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
   }
@@ -1065,7 +1332,8 @@ inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int 
   const uint32_t w = static_cast<uint32_t>(w_stages) * ((C::kKps * tile_bytes + 1023u) & ~1023u);
   const uint32_t x = static_cast<uint32_t>(x_stages) * 2u * C::kKps * static_cast<uint32_t>(bn) * 128u;
   const uint32_t bars =
-      (2u * w_stages + 2u * x_stages + 2u * kASlots + 2u * C::kDacc + 1u + 4u * kKRing + 2u * kSRing + 1u) * 8u + 16u;
+      (2u * w_stages + 2u * x_stages + 2u * (C::kKps == 2 ? kABars : kASlots) + 2u * C::kDacc + 1u + 2u * kKRing +
+       2u * kSRing + 1u) * 8u + 16u;
   const uint32_t scales = CLS == 0 ? 4u * 2u * kSRing * kTileN + 4u * kTileN * 16u : 0u;
   const uint32_t moe = 4u * (C::kBnMax + 2u * (num_experts + 1));
   return w + x + bars + scales + moe + 1024u /* alignment slack */;

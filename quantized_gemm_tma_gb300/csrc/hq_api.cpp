@@ -427,15 +427,16 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   const int forced_sk = env_int("HQ_FORCE_SPLITK", 0);  // 1: stream-K on, 2: off
   if (forced_sk == 1 && !(flags & HQ_FLAG_BATCH_INVARIANT) && p.tiles <= kMaxSplitTiles) p.stream_k = 1;
   if (forced_sk == 2) p.stream_k = 0;
-  // A tile per 2-CTA cluster, K split in halves and combined through shared
-  // memory, when that fills most SMs: no cross-CTA global reduction at all.
+  plan_stages(p.cls, L, p.bn, 0, smem_optin, &p.stages, &p.x_stages, &p.groups);
+  // A tile per 2-CTA cluster, K split in halves and combined through
+  // distributed shared memory, when that fills most SMs: no cross-CTA global
+  // reduction at all.
   p.cluster = 1;
-  if (p.cls == 0 && !(flags & HQ_FLAG_BATCH_INVARIANT) && L.k_tiles >= 2 && 2 * p.tiles <= sms &&
-      8 * p.tiles >= 3 * sms && env_int("HQ_FORCE_SPLITK", 0) == 0) {
+  if (!(flags & HQ_FLAG_BATCH_INVARIANT) && L.k_tiles >= 2 && 2 * p.tiles <= sms && 8 * p.tiles >= 3 * sms &&
+      env_int("HQ_FORCE_SPLITK", 0) == 0 && wna16_cluster_fits(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn)) {
     p.cluster = 2;
     p.stream_k = 0;
   }
-  plan_stages(p.cls, L, p.bn, 0, smem_optin, &p.stages, &p.x_stages, &p.groups);
   p.smem = wna16_smem_bytes(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn, 0);
   // stream-K: at least 8 K-blocks per CTA, so that partial tiles stay few
   p.grid = p.cluster == 2 ? 2 * p.tiles

@@ -198,6 +198,13 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
 
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
+// Split cluster barrier: every thread of the cluster arrives once (release),
+// and a thread that waits (acquire) sees what the others did before arriving,
+// e.g. their mbarrier initialisation.  Both CTAs of a cluster are resident
+// together, so the wait ends as soon as the peer has passed its arrive.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 // Arrive on an mbarrier in another CTA of the cluster (address from map_shared).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
@@ -342,13 +349,18 @@ static __device__ unsigned long long g_trace_cta[1024 * 4];
   } while (0)
 #endif
 #if defined(HQ_ENABLE_TRACE)
+#if defined(HQ_TRACE_CLOCK)
+#define HQ_TRACE_TIME() clock64()  // SM cycle counter: comparable across the warps of one CTA only
+#else
+#define HQ_TRACE_TIME() ::hq::dev::globaltimer()
+#endif
 #define HQ_TRACE(slot, ctr, tag)                                                                          \
   do {                                                                                                    \
     if (blockIdx.x < ::hq::dev::kTraceCtas && (ctr) < ::hq::dev::kTraceEvents) {                          \
       unsigned long long* e_ =                                                                            \
           &::hq::dev::g_trace[((blockIdx.x * ::hq::dev::kTraceSlots + (slot)) * ::hq::dev::kTraceEvents + \
                                (ctr)) * 2];                                                               \
-      e_[0] = ::hq::dev::globaltimer();                                                                   \
+      e_[0] = HQ_TRACE_TIME();                                                                            \
       e_[1] = (tag);                                                                                      \
     }                                                                                                     \
     ++(ctr);                                                                                              \

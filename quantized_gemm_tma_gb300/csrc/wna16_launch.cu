@@ -28,6 +28,15 @@ uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_byt
   }
 }
 
+bool wna16_cluster_fits(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn) {
+  if (cls == 0) return true;  // bn <= 16: rank 1's sums go to a dedicated buffer
+  const uint32_t kps = static_cast<uint32_t>(wna16_kps(cls));
+  const uint64_t rings = static_cast<uint64_t>(x_stages) * 2u * kps * static_cast<uint32_t>(bn) * 128u +
+                         static_cast<uint64_t>(w_stages) * ((kps * tile_bytes + 1023u) & ~1023u);
+  const uint32_t need = cls == 1 ? wna16::xchg_bytes<1>() : cls == 2 ? wna16::xchg_bytes<2>() : wna16::xchg_bytes<3>();
+  return need <= rings;
+}
+
 int wna16_kps(int cls) {
   switch (cls) {
     case 0: return wna16::Cls<0>::kKps;

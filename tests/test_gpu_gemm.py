@@ -114,6 +114,28 @@ def test_split_k_deterministic():
     assert np.array_equal(a, b)
 
 
+CLUSTER = [
+    # name, generator, m, n, k: 57..76 output tiles of 128 rows, so each tile
+    # runs on a 2-CTA cluster that splits K in halves (odd K-block counts give
+    # rank 1 the extra block)
+    ("w4a16_cls0_m16", synth.dense_w4a16_asym, 16, 8192, 640),
+    ("w4a16_cls1_m40", synth.dense_w4a16_asym, 40, 8192, 512),
+    ("w4a16_cls2_m100_ragged", synth.dense_w4a16_asym, 100, 8000, 384),
+    ("int6_cls2_fp16", synth.dense_int6_channel, 128, 7680, 256),
+    ("w4a16_cls3_m200", synth.dense_w4a16_sym, 200, 8192, 256),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(CLUSTER)), ids=lambda i: CLUSTER[i][0])
+def test_cluster_split(idx):
+    import quantized_gemm_tma_gb300 as hq
+    name, gen, m, n, k = CLUSTER[idx]
+    qw, acts = gen(40 + idx, m, n, k)
+    y = _gpu(qw, acts)
+    assert hq.hq_last_plan()["splits"] == 2, hq.hq_last_plan()
+    check(y, _ref(qw, acts), name)
+
+
 def test_workspace_reused_across_shapes():
     """One workspace serves split-K problems of different shapes in turn: the
     fp32 partials of one shape never land on the counters of the next."""
