@@ -263,6 +263,14 @@ struct Ring {
   }
 };
 
+// L2 policy of the weight copies: a dense problem with one row of tiles reads
+// every weight byte once (evict first, keep the cache for activations); with
+// several, each weight tile is read again by the next row of tiles.
+template <bool MOE>
+__device__ __forceinline__ uint64_t weight_policy(const GemmParams& p) {
+  return (!MOE && p.m_tiles > 1) ? dev::policy_evict_normal() : dev::policy_evict_first();
+}
+
 // ---------------------------------------------------------------- work units
 struct Unit {
   int e, nt, mt, tile, row0, rows, kb0, kb1;
@@ -457,7 +465,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       if (lane == 0) {
         Sched<MOE> sc;
         sc.init(p);
-        const uint64_t pol = dev::policy_evict_first();
+        const uint64_t pol = weight_policy<MOE>(p);
         Unit u;
         while (n_pre < SW && sc.next(p, s_tile_off, s_row_off, u)) {
           const uint8_t* wt = p.tiles + static_cast<uint64_t>(u.nt) * p.k_tiles * tile_bytes;
@@ -490,7 +498,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     Ring rg;
     int issued = 0;
     bool ok = true;
-    const uint64_t pol = dev::policy_evict_first();
+    const uint64_t pol = weight_policy<MOE>(p);
     [[maybe_unused]] int tr = 0;
     Unit u;
     while (ok && sc.next(p, s_tile_off, s_row_off, u)) {

@@ -635,9 +635,13 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   off += align_up(sizeof(int) * std::max<int64_t>(pairs, 1), kAlign);
   float* zbuf = reinterpret_cast<float*>(ws + off);
 
-  // tokens per expert tile: from the mean rows per expert
+  // Tokens per expert tile, from the mean rows per expert.  A tile's time is
+  // mostly its weight stream, so fewer, wider tiles win until the padding of
+  // the skewed experts' last tiles costs more MMA work than the weight re-reads
+  // it saves (measured on GB300 at E = 128, N = 1536, K = 2048, top-8: 32
+  // tokens per tile is best up to a mean of 16 rows per expert, 64 at 256).
   const double mean_rows = static_cast<double>(pairs) / L.num_experts;
-  int bn = mean_rows <= 16 ? 16 : (mean_rows <= 32 ? 32 : (mean_rows <= 64 ? 64 : 128));
+  int bn = mean_rows <= 32 ? 32 : (mean_rows <= 384 ? 64 : 128);
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
   if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) bn = forced_bn;
   const int cls = wna16_class(bn);

@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteChunk = 8;  // expert ids per lane loaded together
 
 // Block-wide exclusive scan of one value per thread (threads >= count hold 0).
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
@@ -65,11 +66,22 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 
   for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) wcnt[i] = 0;
   __syncthreads();
+  // ids are read kRouteChunk per lane at a time, so one load latency covers
+  // 32 x kRouteChunk pairs of the warp's segment
   bool bad = false;
-  for (int f = f0 + lane; f < f1; f += 32) {
-    const int e = ids[f];
-    if (e >= 0 && e < E) atomicAdd(&wcnt[warp * E + e], 1);
-    else bad = true;
+  for (int b = f0; b < f1; b += 32 * kRouteChunk) {
+    int ev[kRouteChunk];
+#pragma unroll
+    for (int j = 0; j < kRouteChunk; ++j) {
+      const int f = b + 32 * j + lane;
+      ev[j] = f < f1 ? ids[f] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kRouteChunk; ++j) {
+      if (b + 32 * j + lane >= f1) continue;
+      if (ev[j] >= 0 && ev[j] < E) atomicAdd(&wcnt[warp * E + ev[j]], 1);
+      else bad = true;
+    }
   }
   if (bad) atomicCAS(status, 0, static_cast<int>(HQ_ERR_INVALID_VALUE));
   __syncthreads();
@@ -102,21 +114,30 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 
   // stable scatter: each warp walks its segment in order, 32 pairs per step
   int* cur = wcnt + warp * E;
-  for (int b = f0; b < f1; b += 32) {
-    const int f = b + lane;
-    int e = (f < f1) ? ids[f] : -1;
-    if (e < 0 || e >= E) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    int pos = 0;
-    if (e >= 0) pos = cur[e] + rank;
-    __syncwarp();
-    if (e >= 0) {
-      perm[pos] = f;
-      if (perm_out) perm_out[pos] = f;
-      if (rank == 0) cur[e] += __popc(peers);
+  for (int b = f0; b < f1; b += 32 * kRouteChunk) {
+    int ev[kRouteChunk];
+#pragma unroll
+    for (int j = 0; j < kRouteChunk; ++j) {
+      const int f = b + 32 * j + lane;
+      ev[j] = f < f1 ? ids[f] : -1;
     }
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kRouteChunk; ++j) {
+      const int f = b + 32 * j + lane;
+      int e = ev[j];
+      if (e < 0 || e >= E) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      int pos = 0;
+      if (e >= 0) pos = cur[e] + rank;
+      __syncwarp();
+      if (e >= 0) {
+        perm[pos] = f;
+        if (perm_out) perm_out[pos] = f;
+        if (rank == 0) cur[e] += __popc(peers);
+      }
+      __syncwarp();
+    }
   }
 }
 
