@@ -55,8 +55,8 @@ BLOCK = 25         # back-to-back calls of one shape between two events
 # DRAM bytes (read + write) per launch of the WnA16 INT4 kernel, from the ncu
 # capture summarised in profiles/wna16_int4_asym_g128_n8192_k8192.md, keyed by
 # M; valid only while the kernel sources hash to `sha` (else reported null).
-NCU_TRAFFIC = {"sha": "dc2927b420d57674", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
-               "bytes": {16: 35_461_376}}
+NCU_TRAFFIC = {"sha": "0245844b5673c783", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
+               "bytes": {16: 35_467_008, 128: 37_304_576, 4096: 159_179_264}}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -454,7 +454,7 @@ def main():
                       "tflops": round(fl / t / 1e12, 2), "gbs": round(by / t / 1e9, 1),
                       "roofline_frac": round(roof_t / t, 3),
                       "bound": "hbm" if by / (pk["hbm_gbs"] * 1e9) >= fl / (pk["bf16_tflops"] * 1e12) else "tensor",
-                      "plan": res["plans"][m]})
+                      "algorithmic_bytes": by, "traffic": ncu_traffic(m), "plan": res["plans"][m]})
     big = max(sw)
     t_big = res["per_m"][big]
     ach = dense_flops(big) / t_big / 1e12
