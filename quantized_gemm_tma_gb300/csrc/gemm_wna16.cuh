@@ -354,7 +354,8 @@ __device__ __forceinline__ int sk_cta_of(long long x, long long T, int G) {
 // ---------------------------------------------------------------- the kernel
 template <int FMT, bool BF16, int CLS, bool MOE>
 __global__ void __launch_bounds__(threads<CLS>(), 1)
-    wna16_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x) {
+    wna16_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x,
+                 const __grid_constant__ CUtensorMap tmap_y) {
   using C = Cls<CLS>;
   constexpr int KPS = C::kKps, ISS = C::kIss, DACC = C::kDacc, BNMAX = C::kBnMax;
   constexpr int G = KPS;                 // dequantiser groups
@@ -409,6 +410,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   int* s_tok = reinterpret_cast<int*>(s_red + (CLS == 0 ? kTileN * 16 : 0));  // MoE: token per row
   int* s_tile_off = s_tok + (MOE ? BNMAX : 0);
   int* s_row_off = s_tile_off + (MOE ? p.num_experts + 1 : 0);
+  // dense Y stores: per epilogue warp two staging boxes of 16 tokens x 32 rows
+  // (16-bit), 128-byte aligned
+  uint16_t* y_stage = reinterpret_cast<uint16_t*>(
+      reinterpret_cast<uint8_t*>(s_row_off) + ((128u - (dev::smem_u32(s_row_off) & 127u)) & 127u));
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = dev::lane_id();
@@ -984,6 +989,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     // each position's scale ring; stream mode: stage counter (issuer choice)
     [[maybe_unused]] uint32_t ck0 = 0, ck1 = 0, ck2 = 0, ck3 = 0, cp0 = 0, cp1 = 0;
     [[maybe_unused]] uint32_t S = 0;
+    [[maybe_unused]] uint32_t ystg = 0;  // dense: tensor stores of Y issued by this warp
     [[maybe_unused]] int tr = 0;
     const bool trace_me = quarter == 0 && lane == 0;
     // INT4 bf16 operands without a folded scale carry an extra 2^-7
@@ -1049,6 +1055,28 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           return;
+        }
+        if constexpr (!MOE) {
+          if (p.y_tma) {
+            // tokens 16 ch .. 16 ch + 15 of rows quarter * 32 .. + 31: staged as
+            // [token][row] 16-bit, then one tensor store (clipped at M and N)
+            uint16_t* buf = y_stage + (quarter * 2 + (ystg & 1)) * (16 * 32);
+            if (ystg >= 2 && lane == 0) dev::bulk_wait_read<1>();  // the store two boxes back has read it
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if constexpr (BF16) buf[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i] * rs));
+              else buf[i * 32 + lane] = __half_as_ushort(__float2half_rn(v[i] * rs));
+            }
+            dev::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              dev::tma_store_2d(&tmap_y, buf, u.nt * kTileN + quarter * 32, u.row0 + ch * 16);
+              dev::bulk_commit();
+            }
+            ++ystg;
+            return;
+          }
         }
         [[maybe_unused]] int fr = 0;
         [[maybe_unused]] float wr = 0.f;
@@ -1312,6 +1340,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       ++ui;
       S += static_cast<uint32_t>((u.kb1 - u.kb0 + KPS - 1) / KPS);
     }
+    // every tensor store of Y has completed before the CTA exits
+    if constexpr (!MOE) {
+      if (p.y_tma && lane == 0) dev::bulk_wait<0>();
+    }
     if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
   }
 
@@ -1344,7 +1376,8 @@ inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int 
        2u * kSRing + 1u) * 8u + 16u;
   const uint32_t scales = CLS == 0 ? 4u * 2u * kSRing * kTileN + 4u * kTileN * 16u : 0u;
   const uint32_t moe = 4u * (C::kBnMax + 2u * (num_experts + 1));
-  return w + x + bars + scales + moe + 1024u /* alignment slack */;
+  const uint32_t ystage = num_experts == 0 ? kEpiWarps * 2u * 16u * 32u * 2u + 128u : 0u;  // dense Y boxes
+  return w + x + bars + scales + moe + ystage + 1024u /* alignment slack */;
 }
 
 }  // namespace wna16

@@ -64,7 +64,7 @@ std::once_flag g_encode_once;
 // per box (dims {inner, outer, slabs}, slab stride inner * elem bytes).
 hq_status encode_uncached(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, const void* base,
                           uint64_t inner, uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner,
-                          uint32_t box_outer, uint64_t slabs) {
+                          uint32_t box_outer, uint64_t slabs, bool swizzle) {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -81,7 +81,8 @@ hq_status encode_uncached(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t 
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                 swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     cuuint64_t dims[3] = {inner, outer, slabs & 0xffffffffull};
     cuuint64_t strides[2] = {row_stride_elems * elem, inner * elem};
@@ -99,10 +100,10 @@ hq_status encode_uncached(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t 
 struct MapKey {
   const void* base;
   uint64_t inner, outer, stride, slabs;
-  uint32_t box_inner, box_outer, dtype;
+  uint32_t box_inner, box_outer, dtype, swizzle;
   bool operator==(const MapKey& o) const {
     return base == o.base && inner == o.inner && outer == o.outer && stride == o.stride && slabs == o.slabs &&
-           box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype;
+           box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype && swizzle == o.swizzle;
   }
 };
 struct MapCache {
@@ -113,17 +114,21 @@ struct MapCache {
 };
 thread_local MapCache g_maps;
 
+// 128-byte swizzled boxes (operand loads) unless `swizzle` is false (plain
+// row-major boxes, e.g. output stores staged in shared memory).
 hq_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, const void* base, uint64_t inner,
                     uint64_t outer, uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer,
-                    uint64_t slabs = 0) {
-  const MapKey k{base, inner, outer, row_stride_elems * elem, slabs, box_inner, box_outer, static_cast<uint32_t>(dtype)};
+                    uint64_t slabs = 0, bool swizzle = true) {
+  const MapKey k{base, inner, outer, row_stride_elems * elem, slabs, box_inner, box_outer, static_cast<uint32_t>(dtype),
+                 swizzle ? 1u : 0u};
   MapCache& c = g_maps;
   for (int i = 0; i < c.used; ++i)
     if (c.key[i] == k) {
       *map = c.map[i];
       return HQ_OK;
     }
-  hq_status st = encode_uncached(map, dtype, elem, base, inner, outer, row_stride_elems, box_inner, box_outer, slabs);
+  hq_status st =
+      encode_uncached(map, dtype, elem, base, inner, outer, row_stride_elems, box_inner, box_outer, slabs, swizzle);
   if (st != HQ_OK) return st;
   const int slot = c.used < MapCache::kSlots ? c.used++ : (c.next++ % MapCache::kSlots);
   c.key[slot] = k;
@@ -559,10 +564,18 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   p.partials = reinterpret_cast<float*>(ws + kAlign + kCounterBytes);
   p.num_experts = 1;
   // X [M][K]: one box = 64 columns (128 bytes, swizzled) of bn rows
-  CUtensorMap tm;
-  st = encode_2d(&tm, atype == HQ_A_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x,
-                 L.k, m, ldx, 64, pl.bn);
+  const CUtensorMapDataType t16 = atype == HQ_A_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  Wna16Maps maps;
+  st = encode_2d(&maps.x, t16, 2, x, L.k, m, ldx, 64, pl.bn);
   if (st != HQ_OK) return st;
+  // Y [M][N]: tensor stores of 16 tokens x 32 output rows when its row pitch
+  // is a multiple of 16 bytes (the tensor-map stride rule); plain stores else
+  p.y_tma = (ldy * 2) % 16 == 0 ? 1 : 0;
+  maps.y = maps.x;
+  if (p.y_tma) {
+    st = encode_2d(&maps.y, t16, 2, y, L.n, m, ldy, 32, 16, 0, false);
+    if (st != HQ_OK) return st;
+  }
   Wna16Launch l{};
   l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
   l.bf16 = atype == HQ_A_BF16;
@@ -575,7 +588,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   if (env_int("HQ_TRACE", 0))
     std::fprintf(stderr, "hq_gemm: m=%d n=%d k=%d bn=%d cls=%d stream_k=%d grid=%d stages=%d groups=%d smem=%u\n", m,
                  L.n, L.k, pl.bn, pl.cls, pl.stream_k, pl.grid, pl.stages, pl.groups, pl.smem);
-  return launch_wna16(l, p, tm, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+  return launch_wna16(l, p, maps, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ MoE
@@ -676,10 +689,11 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   l.grid = di.sms;
   l.smem = wna16_smem_bytes(cls, p.stages, p.x_stages, L.tile_bytes, bn, L.num_experts);
   // X [T][K] gathered by token index: one-row boxes of 64 columns (four rows per copy)
-  CUtensorMap tm;
-  st = encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, tokens, ldx, 64, 1);
+  Wna16Maps maps;
+  st = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, tokens, ldx, 64, 1);
   if (st != HQ_OK) return st;
-  if (launch_wna16(l, p, tm, s) != cudaSuccess) return HQ_ERR_CUDA;
+  maps.y = maps.x;  // MoE writes per-pair fp32 rows with plain stores
+  if (launch_wna16(l, p, maps, s) != cudaSuccess) return HQ_ERR_CUDA;
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L.num_experts, L.n, L.n_pad, y, ldy, true, s) != cudaSuccess)
     return HQ_ERR_CUDA;
   g_last_plan = hq_plan_info{bn, 1, l.grid, 3, p.stages, cls, p.groups, 0};

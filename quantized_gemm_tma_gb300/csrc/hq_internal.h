@@ -112,6 +112,7 @@ struct GemmParams {
   // output
   void* y;
   int64_t ldy;
+  int y_tma;                // dense: Y written by tensor stores of 16 x 32 boxes through shared memory
   float* partials;          // stream-K: [2 * grid][bn][128] fp32 (head and tail unit of each CTA)
   int* counters;            // stream-K: [tiles][4], zero between calls
   int* status;

@@ -53,7 +53,12 @@ struct Wna16Launch {
   int grid;
   uint32_t smem;
 };
-cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, cudaStream_t stream);
+// Tensor maps of one WnA16 launch: activations (loads) and Y (dense stores;
+// unused when GemmParams::y_tma is 0).
+struct Wna16Maps {
+  CUtensorMap x, y;
+};
+cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const Wna16Maps& maps, cudaStream_t stream);
 uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts);
 int wna16_kps(int cls);  // K-blocks per shared-memory stage
 // whether a 2-CTA cluster split of this class can pass rank 1's sums through

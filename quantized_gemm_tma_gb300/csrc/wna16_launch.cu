@@ -6,15 +6,15 @@
 
 namespace hq {
 
-cudaError_t launch_wna16_int4(const Wna16Launch&, const GemmParams&, const CUtensorMap&, cudaStream_t);
-cudaError_t launch_wna16_int6(const Wna16Launch&, const GemmParams&, const CUtensorMap&, cudaStream_t);
-cudaError_t launch_wna16_mxfp4(const Wna16Launch&, const GemmParams&, const CUtensorMap&, cudaStream_t);
+cudaError_t launch_wna16_int4(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
+cudaError_t launch_wna16_int6(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
+cudaError_t launch_wna16_mxfp4(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
 
-cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const CUtensorMap& tmap, cudaStream_t stream) {
+cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const Wna16Maps& maps, cudaStream_t stream) {
   switch (l.fmt) {
-    case 0: return launch_wna16_int4(l, p, tmap, stream);
-    case 1: return launch_wna16_int6(l, p, tmap, stream);
-    case 2: return launch_wna16_mxfp4(l, p, tmap, stream);
+    case 0: return launch_wna16_int4(l, p, maps, stream);
+    case 1: return launch_wna16_int6(l, p, maps, stream);
+    case 2: return launch_wna16_mxfp4(l, p, maps, stream);
     default: return cudaErrorInvalidValue;
   }
 }

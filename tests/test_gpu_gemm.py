@@ -95,6 +95,14 @@ def test_strided_x_and_y():
     check(_gpu(qw, acts, ldx=520, ldy=264), _ref(qw, acts), "strided")
 
 
+def test_y_pitch_not_16_byte_multiple():
+    """A Y row pitch that tensor stores cannot take (516 bytes) falls back to plain stores."""
+    qw, acts = synth.dense_w4a16_asym(9, 24, 256, 512)
+    check(_gpu(qw, acts, ldy=258), _ref(qw, acts), "ldy 258")
+    qw, acts = synth.dense_w4a16_asym(10, 16, 8192, 640)  # cluster split with plain stores
+    check(_gpu(qw, acts, ldy=8194), _ref(qw, acts), "ldy 8194, cluster")
+
+
 def test_m_zero_is_noop():
     import torch
     import quantized_gemm_tma_gb300 as hq
