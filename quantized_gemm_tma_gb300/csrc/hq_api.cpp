@@ -429,6 +429,11 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   p.tiles = p.m_tiles * L.n_tiles;
   p.iters = static_cast<long long>(p.tiles) * L.k_tiles;
   p.stream_k = !(flags & HQ_FLAG_BATCH_INVARIANT) && p.tiles < 4 * sms && p.tiles <= kMaxSplitTiles && L.k_tiles > 1;
+  // Wide tiles (bn >= 128): once there are half as many tiles as SMs, whole
+  // tiles beat stream-K, whose fp32 partial reduction of 64-128 KB per tile
+  // costs more than the wave quantisation it removes (N = K = 8192 on GB300:
+  // M = 512 56 vs 102 us, M = 1024 119 vs 135 us, M = 2048 228 vs 231 us).
+  if (p.cls >= 2 && 2 * p.tiles >= sms) p.stream_k = 0;
   const int forced_sk = env_int("HQ_FORCE_SPLITK", 0);  // 1: stream-K on, 2: off
   if (forced_sk == 1 && !(flags & HQ_FLAG_BATCH_INVARIANT) && p.tiles <= kMaxSplitTiles) p.stream_k = 1;
   if (forced_sk == 2) p.stream_k = 0;
