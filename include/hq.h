@@ -278,6 +278,43 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
                       hq_stream_t stream);
 
 /*
+ * Grouped MoE input forms ([WIKI] "Device and workload selection": besides
+ * the indexed form above, the rows of each expert can be handed over already
+ * grouped, either back to back or in per-expert storage with a separate count
+ * of valid rows).
+ */
+#define HQ_MOE_GROUPED_CONTIGUOUS 0 /* rows of expert e: [offsets[e], offsets[e+1]) of X and Y */
+#define HQ_MOE_GROUPED_MASKED 1     /* rows of expert e: [e*rows, e*rows + counts[e]) of X and Y */
+
+/*
+ * hq_moe_grouped_workspace_size — workspace for hq_moe_grouped_gemm (status
+ * word, compacted offsets and tile prefix, row map of up to E*rows (masked)
+ * or rows (contiguous) entries).
+ */
+hq_status hq_moe_grouped_workspace_size(const hq_weight_desc* desc, int32_t form, int32_t rows, size_t* bytes);
+
+/*
+ * hq_moe_grouped_gemm — the per-expert GEMM on rows already grouped by
+ * expert, no routing weights and no combine:
+ *   Y[i] = a(X[i]) . dequant(W_e)^T   for every valid row i of expert e.
+ *
+ * form         HQ_MOE_GROUPED_CONTIGUOUS: expert_rows = int32 offsets[E+1]
+ *              (device), nondecreasing, offsets[E] <= rows; X, Y have `rows`
+ *              rows.  HQ_MOE_GROUPED_MASKED: expert_rows = int32 counts[E]
+ *              (device), 0 <= counts[e] <= rows; X, Y are [E][rows] blocks.
+ * expected_rows  rows per expert the caller expects (picks the tile width;
+ *              the counts stay on the device); <= 0: derived from `rows`
+ * x, ldx       activations (bf16); y, ldy output (bf16), 16-byte aligned rows
+ * Rows outside every expert's range are neither read nor written.  Invalid
+ * offsets or counts make that expert contribute nothing and set
+ * HQ_ERR_INVALID_VALUE in the workspace status word.  Asynchronous.
+ */
+hq_status hq_moe_grouped_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t form, int32_t rows,
+                              const int32_t* expert_rows, int32_t expected_rows, int32_t atype, const void* x,
+                              int64_t ldx, void* y, int64_t ldy, void* workspace, size_t ws_bytes, uint32_t flags,
+                              hq_stream_t stream);
+
+/*
  * hq_status_read — synchronise `stream` and read the device status word of a
  * workspace (HQ_OK when no device-side error was recorded).  With clear != 0
  * the word is reset to HQ_OK afterwards.
@@ -285,8 +322,8 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
 hq_status hq_status_read(void* workspace, int32_t clear, hq_stream_t stream, int32_t* device_status);
 
 /*
- * hq_last_plan — the launch plan of the most recent hq_gemm / hq_moe_gemm
- * call on this host thread.  For tests and benchmarks.
+ * hq_last_plan — the launch plan of the most recent hq_gemm / hq_moe_gemm /
+ * hq_moe_grouped_gemm call on this host thread.  For tests and benchmarks.
  */
 typedef struct {
   int32_t bn;          /* tokens per output tile (MMA N for WnA16, M side for FP8) */

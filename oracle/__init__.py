@@ -20,7 +20,8 @@ Modules:
              bf16, fp16), each from its bit-field definition
     gemm     dequantisation and the dense GEMM
     moe      routing (count, prefix sum, stable permutation) and the MoE
-             grouped GEMM with the routing-weighted combine
+             grouped GEMM with the routing-weighted combine; the grouped
+             (contiguous / masked) input forms
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against values fixed outside the oracle (library casts, published format
@@ -29,4 +30,4 @@ none is "parity unpinned".
 """
 from . import formats, gemm, moe  # noqa: F401
 from .gemm import dequantize, gemm_dense, decode_activations  # noqa: F401
-from .moe import moe_route, moe_gemm  # noqa: F401
+from .moe import moe_route, moe_gemm, moe_grouped_gemm  # noqa: F401

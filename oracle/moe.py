@@ -14,6 +14,12 @@ routing  For topk_ids [T, topk] over E experts, with flat pair index
 GEMM     Z[f, :] = X[t, :] . W_{id(f)}^T          (the gate+up GEMM)
 combine  Y[t, :] = sum_j topk_w[t, j] * Z[t*topk + j, :]
          (the routing-weighted sum per token; no activation function)
+
+Grouped forms (same section: rows arrive already grouped per expert, either
+back to back or in per-expert storage with a count of valid rows):
+         Y[i, :] = X[i, :] . W_e^T for every row i in expert e's range; the
+         ranges are [offsets[e], offsets[e+1]) (contiguous) or
+         [e*rows, e*rows + counts[e]) (masked); other rows are not defined.
 """
 from __future__ import annotations
 
@@ -68,3 +74,32 @@ def moe_reference(qw, acts, routing) -> np.ndarray:
                           qw.group_k, qw.signed, qw.stype, 1)[0]
     return moe_gemm(decode_activations(acts.atype, acts.data, acts.scales),
                     routing.topk_ids, routing.topk_w, expert)
+
+
+def moe_grouped_ranges(form: str, expert_rows, num_experts: int, rows: int):
+    """Row range [start, stop) of every expert for a grouped form."""
+    v = np.asarray(expert_rows, dtype=np.int64)
+    if form == "contiguous":
+        return [(int(v[e]), int(v[e + 1])) for e in range(num_experts)]
+    if form == "masked":
+        return [(e * rows, e * rows + int(v[e])) for e in range(num_experts)]
+    raise ValueError(form)
+
+
+def moe_grouped_gemm(a: np.ndarray, form: str, expert_rows, rows: int, w) -> dict:
+    """{row index: Y row (float64)} for every valid row of a grouped form.
+
+    ``a`` holds the activation rows of the whole X buffer (``rows`` rows for
+    contiguous, E*rows for masked); ``w`` as in ``moe_gemm``.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    get = w if callable(w) else (lambda e, _w=np.asarray(w, dtype=np.float64): _w[e])
+    n_exp = len(expert_rows) - 1 if form == "contiguous" else len(expert_rows)
+    out = {}
+    for e, (lo, hi) in enumerate(moe_grouped_ranges(form, expert_rows, n_exp, rows)):
+        if hi <= lo:
+            continue
+        z = a[lo:hi] @ np.asarray(get(e), dtype=np.float64).T
+        for i in range(lo, hi):
+            out[i] = z[i - lo]
+    return out

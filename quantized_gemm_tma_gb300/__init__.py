@@ -24,6 +24,7 @@ HQ_W_INT4, HQ_W_INT6, HQ_W_MXFP4, HQ_W_FP8_E4M3 = 0, 1, 2, 3
 HQ_A_BF16, HQ_A_FP16, HQ_A_FP8_E4M3 = 0, 1, 2
 HQ_S_BF16, HQ_S_FP16, HQ_S_FP32, HQ_S_UE8M0 = 0, 1, 2, 3
 HQ_FLAG_BATCH_INVARIANT = 0x1
+HQ_MOE_GROUPED_CONTIGUOUS, HQ_MOE_GROUPED_MASKED = 0, 1
 
 WTYPES = {"int4": HQ_W_INT4, "int6": HQ_W_INT6, "mxfp4": HQ_W_MXFP4, "fp8": HQ_W_FP8_E4M3}
 ATYPES = {"bf16": HQ_A_BF16, "fp16": HQ_A_FP16, "fp8": HQ_A_FP8_E4M3}
@@ -33,7 +34,7 @@ STYPES = {"bf16": HQ_S_BF16, "fp16": HQ_S_FP16, "fp32": HQ_S_FP32, "ue8m0": HQ_S
 EXPORTS = [
     "hq_version", "hq_status_string", "hq_transform_size", "hq_transform", "hq_untransform",
     "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_gemm_noalloc", "hq_moe_workspace_size",
-    "hq_moe_gemm", "hq_status_read", "hq_last_plan",
+    "hq_moe_gemm", "hq_moe_grouped_workspace_size", "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan",
 ]
 
 #: size of the fixed device scratch behind hq_gemm_noalloc
@@ -87,6 +88,8 @@ def lib() -> ctypes.CDLL:
             "hq_gemm_noalloc": ([dp, vp, i32, i32, vp, i64, vp, vp, i64, u32, vp, vp], i32),
             "hq_moe_workspace_size": ([dp, i32, i32, i32, ctypes.POINTER(sz)], i32),
             "hq_moe_gemm": ([dp, vp, i32, i32, vp, vp, i32, vp, i64, vp, i64, vp, vp, vp, sz, u32, vp], i32),
+            "hq_moe_grouped_workspace_size": ([dp, i32, i32, ctypes.POINTER(sz)], i32),
+            "hq_moe_grouped_gemm": ([dp, vp, i32, i32, vp, i32, i32, vp, i64, vp, i64, vp, sz, u32, vp], i32),
             "hq_status_read": ([vp, i32, vp, ctypes.POINTER(i32)], i32),
             "hq_last_plan": ([ctypes.POINTER(PlanInfo)], i32),
         }
@@ -186,6 +189,20 @@ def hq_moe_gemm(desc: WeightDesc, w_t, tokens: int, topk: int, topk_ids, topk_w,
     _check(lib().hq_moe_gemm(ctypes.byref(desc), _ptr(w_t), tokens, topk, _ptr(topk_ids), _ptr(topk_w),
                              ATYPES.get(atype, atype), _ptr(x), ldx, _ptr(y), ldy, _ptr(expert_offsets_out),
                              _ptr(perm_out), _ptr(workspace), ws_bytes, flags, _stream(stream)), "hq_moe_gemm")
+
+
+def hq_moe_grouped_workspace_size(desc: WeightDesc, form: int, rows: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().hq_moe_grouped_workspace_size(ctypes.byref(desc), form, rows, ctypes.byref(out)),
+           "hq_moe_grouped_workspace_size")
+    return out.value
+
+
+def hq_moe_grouped_gemm(desc: WeightDesc, w_t, form: int, rows: int, expert_rows, expected_rows: int, atype, x,
+                        ldx: int, y, ldy: int, workspace, ws_bytes: int, flags: int = 0, stream=None) -> None:
+    _check(lib().hq_moe_grouped_gemm(ctypes.byref(desc), _ptr(w_t), form, rows, _ptr(expert_rows), expected_rows,
+                                     ATYPES.get(atype, atype), _ptr(x), ldx, _ptr(y), ldy, _ptr(workspace),
+                                     ws_bytes, flags, _stream(stream)), "hq_moe_grouped_gemm")
 
 
 def hq_status_read(workspace, clear: bool = False, stream=None) -> int:

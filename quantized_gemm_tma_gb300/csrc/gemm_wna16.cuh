@@ -366,9 +366,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // of its rows per warp, so the four warps sharing a scheduler are at
   // different points of their pipelines instead of in lock step.
   constexpr bool kStream = KPS == 2;
-  // Stream issuers: with four issuers, issuer t takes stream t's K-blocks;
-  // with two, issuer p takes position p of every stage (streams p and 2 + p).
-  constexpr bool kIssPerStream = kStream && ISS == 4;
+  // With streams, issuer p takes K-block p of every stage, i.e. the K-blocks
+  // of streams p and 2 + p alternately.
   constexpr int KR = kKRing / ISS;  // promotion: accumulator ring per issuer
   // MoE with wide tiles gathers activation rows with per-lane cp.async (one
   // tile::gather4 copy moves only 512 bytes, too few for bn >= 64)
@@ -545,6 +544,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     Ring rg;
     int issued = 0;
     bool ok = true;
+    // per-lane gathers: the stage whose copies were issued last.  Each lane
+    // counts in on a stage only after its copies have completed and it has
+    // fenced them into the async proxy the tensor cores read through; that
+    // happens once the next stage is issued, so two stages are in flight.
+    [[maybe_unused]] int pend = -1;
     Unit u;
     while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
       if constexpr (MOE) {
@@ -577,8 +581,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               }
             }
           }
-          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dev::smem_u32(&x_full[rg.s]))
-                       : "memory");
+          asm volatile("cp.async.commit_group;" ::: "memory");
+          if (pend >= 0) {
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+            dev::fence_proxy_async_smem();
+            dev::mbar_arrive(&x_full[pend]);
+          }
+          pend = rg.s;
         } else if (lane == 0) {
           dev::mbar_arrive_expect_tx(&x_full[rg.s], 2u * cnt * slab);
           for (int z = 0; z < 2 * cnt; ++z) {
@@ -602,7 +611,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       if constexpr (MOE) __syncwarp();  // s_tok is rewritten for the next unit
     }
     if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
-    if constexpr (kLaneGather) asm volatile("cp.async.wait_all;" ::: "memory");
+    if constexpr (kLaneGather) {
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      if (pend >= 0) {
+        dev::fence_proxy_async_smem();
+        dev::mbar_arrive(&x_full[pend]);
+      }
+    }
     if (lane == 0) {
       for (int s = 0; s < SX && s < issued; ++s) {
         const int last = ((issued - 1 - s) / SX) * SX + s;
@@ -648,11 +663,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             break;
           }
           HQ_TRACE(1 + pidx, tr, (2ull << 24) | ts);
-          // stream mode: the K-block at position q of this stage comes from
-          // stream 2 (S & 1) + q, in two halves (64 K each) published separately
-          const int q = kIssPerStream ? (pidx & 1) : pidx;
-          const bool mine = !kIssPerStream || (S & 1u) == static_cast<uint32_t>(pidx >> 1);
-          if (kStream && mine && q < cnt) {
+          // stream mode: K-block pidx of this stage comes from stream
+          // 2 (S & 1) + pidx, in two halves (64 K each) published separately
+          const int q = pidx;
+          if (kStream && q < cnt) {
             const int t = 2 * static_cast<int>(S & 1u) + q;
             const uint32_t aph = ((S & 1u) ? cs1 : cs0) & 1u;
             const int ks = pidx * KR + static_cast<int>(ck % KR);
@@ -985,10 +999,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     sc.init(p);
     bool ok = true;
     int ui = 0;
-    // promotion: K-blocks taken from each issuer's accumulator ring and from
-    // each position's scale ring; stream mode: stage counter (issuer choice)
-    [[maybe_unused]] uint32_t ck0 = 0, ck1 = 0, ck2 = 0, ck3 = 0, cp0 = 0, cp1 = 0;
-    [[maybe_unused]] uint32_t S = 0;
+    // promotion: K-blocks taken from each issuer's accumulator ring (issuer q
+    // takes position q of every stage, so this also indexes its scale ring)
+    [[maybe_unused]] uint32_t ck0 = 0, ck1 = 0;
     [[maybe_unused]] uint32_t ystg = 0;  // dense: tensor stores of Y issued by this warp
     [[maybe_unused]] int tr = 0;
     const bool trace_me = quarter == 0 && lane == 0;
@@ -1016,7 +1029,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
 #pragma unroll
         for (int k = 0; k < kMoeRegs; ++k) {
           const int col = 32 * k + static_cast<int>(lane);
-          w_reg[k] = col < u.rows ? p.topk_w[f_reg[k]] : 0.f;
+          w_reg[k] = (col < u.rows && !p.moe_direct) ? p.topk_w[f_reg[k]] : 0.f;
         }
       }
       // columns [16 ch, 16 ch + 16) of this row: partial, MoE row or Y
@@ -1095,7 +1108,15 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           if constexpr (MOE) {
             const int f = __shfl_sync(0xffffffffu, fr, ((ch & 1) << 4) + i);
             const float wf = __shfl_sync(0xffffffffu, wr, ((ch & 1) << 4) + i);
-            if (col < u.rows && n_ok) p.zbuf[static_cast<size_t>(f) * p.n_pad + n] = v[i] * rs * wf;
+            if (col < u.rows && n_ok) {
+              if (p.moe_direct) {  // grouped forms: Y row f directly, 16-bit
+                const size_t off = static_cast<size_t>(f) * p.ldy + n;
+                if constexpr (BF16) reinterpret_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(v[i] * rs);
+                else reinterpret_cast<__half*>(p.y)[off] = __float2half_rn(v[i] * rs);
+              } else {
+                p.zbuf[static_cast<size_t>(f) * p.n_pad + n] = v[i] * rs * wf;
+              }
+            }
             continue;
           }
           if (col >= u.rows) continue;
@@ -1122,13 +1143,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           for (int i = 0; i < BNMAX; ++i) tot[i] = 0.f;
           for (int kb = u.kb0; kb < u.kb1; ++kb) {
             const int q = (kb - u.kb0) & (KPS - 1);
-            const uint32_t Si = S + static_cast<uint32_t>((kb - u.kb0) / KPS);
-            const int is = kIssPerStream ? 2 * static_cast<int>(Si & 1u) + q : q;  // issuer of this K-block
-            const uint32_t cq = is == 0 ? ck0 : is == 1 ? ck1 : is == 2 ? ck2 : ck3;
-            const uint32_t cs = q ? cp1 : cp0;
-            const int ks = is * KR + static_cast<int>(cq % KR);
-            const int si = q * kSRing + static_cast<int>(cs % kSRing);
-            if (!warp_wait(&s_full[si], (cs / kSRing) & 1u, abort_flag) ||
+            const uint32_t cq = q ? ck1 : ck0;
+            const int ks = q * KR + static_cast<int>(cq % KR);
+            const int si = q * kSRing + static_cast<int>(cq % kSRing);
+            if (!warp_wait(&s_full[si], (cq / kSRing) & 1u, abort_flag) ||
                 !warp_wait(&k_full[ks], (cq / KR) & 1u, abort_flag)) {
               ok = false;
               break;
@@ -1150,8 +1168,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             dev::tc_fence_before();
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(&k_empty[ks]);
-            if (is == 0) ++ck0; else if (is == 1) ++ck1; else if (is == 2) ++ck2; else ++ck3;
-            if (q) ++cp1; else ++cp0;
+            if (q) ++ck1; else ++ck0;
           }
           if (!ok) break;
 #pragma unroll
@@ -1176,15 +1193,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         dev::tc_fence_after();
         // issuers that took at least one K-block of the unit; their partial
         // accumulators are summed in issuer order
-        const int nk = u.kb1 - u.kb0;
-        uint32_t parts;
-        if constexpr (kIssPerStream) {
-          const int par = static_cast<int>(S & 1u);
-          parts = (1u << (2 * par)) | (nk >= 2 ? 1u << (2 * par + 1) : 0u) | (nk >= 3 ? 1u << (2 * (par ^ 1)) : 0u) |
-                  (nk >= 4 ? 1u << (2 * (par ^ 1) + 1) : 0u);
-        } else {
-          parts = (1u << min(ISS, nk)) - 1u;
-        }
+        const uint32_t parts = (1u << min(ISS, u.kb1 - u.kb0)) - 1u;
         const int is0 = __ffs(parts) - 1;
         const uint32_t acc0 = tmem + lane_base + kAccCol0 + static_cast<uint32_t>(buf * ISS * BNMAX);
         // the issuers' partial accumulators of 16 columns, summed in issuer order
@@ -1338,7 +1347,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         if (trace_me) HQ_TRACE(9, tr, ((10ull + last) << 24) | ui);
       }
       ++ui;
-      S += static_cast<uint32_t>((u.kb1 - u.kb0 + KPS - 1) / KPS);
     }
     // every tensor store of Y has completed before the CTA exits
     if constexpr (!MOE) {

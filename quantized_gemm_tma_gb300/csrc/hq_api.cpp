@@ -455,6 +455,64 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   return p;
 }
 
+// Tokens per expert tile, from the mean rows per expert.  A tile's time is
+// mostly its weight stream, so fewer, wider tiles win until the padding of
+// the skewed experts' last tiles costs more MMA work than the weight re-reads
+// it saves (measured on GB300 at E = 128, N = 1536, K = 2048, top-8: 32
+// tokens per tile is best up to a mean of 16 rows per expert, 64 at 256).
+int moe_tile_bn(double mean_rows) {
+  int bn = mean_rows <= 32 ? 32 : (mean_rows <= 384 ? 64 : 128);
+  const int forced_bn = env_int("HQ_FORCE_BN", 0);
+  if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) bn = forced_bn;
+  return bn;
+}
+
+// The grouped WnA16 GEMM over routed rows whose offsets, m-tile prefix and row
+// map are already in the workspace.  Row p of expert e's group reads X row
+// perm[p] / topk and writes either the weighted fp32 row zbuf[perm[p]]
+// (indexed form, combined afterwards) or Y row perm[p] directly (grouped forms).
+hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, int x_rows, int topk, const float* topk_w,
+                             const void* x, int64_t ldx, void* y, int64_t ldy, const int* exp_off,
+                             const int* tile_off, const int* perm, float* zbuf, int* status, bool direct,
+                             const DevInfo& di, cudaStream_t s, int* stages, int* groups) {
+  const int cls = wna16_class(bn);
+  GemmParams p{};
+  p.tiles = wt + L.tiles_off;
+  p.expert_stride = L.expert_stride;
+  p.tile_bytes = L.tile_bytes; p.hi_off = L.hi_off; p.scale_off = L.scale_off; p.zero_off = L.zero_off;
+  p.g_kb = L.g_kb; p.group_k = L.group_k; p.has_zeros = L.has_zeros; p.channel = L.channel;
+  p.zero_sym = (L.has_zeros || !L.signed_codes) ? 0 : (L.wtype == HQ_W_INT4 ? 8 : 32);
+  p.row_scale = L.channel ? reinterpret_cast<const float*>(wt + L.row_off) : nullptr;
+  p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
+  p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = x_rows;
+  p.bn = bn; p.m_tiles = 0; p.num_tiles = 0; p.stream_k = 0; p.iters = 0; p.cluster = 1;
+  p.promote = (cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
+  p.idesc = idesc_f16(true, 128, bn);
+  p.y = y; p.ldy = ldy; p.moe_direct = direct ? 1 : 0;
+  p.status = status;
+  p.num_experts = L.num_experts; p.topk = topk;
+  p.tile_offsets = tile_off; p.expert_offsets = exp_off; p.perm = perm; p.topk_w = topk_w; p.zbuf = zbuf;
+  p.x_rows = static_cast<const __nv_bfloat16*>(x); p.ldx = ldx;
+  plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups);
+  if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
+  Wna16Launch l{};
+  l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
+  l.bf16 = true;
+  l.cls = cls;
+  l.moe = true;
+  l.grid = di.sms;
+  l.smem = wna16_smem_bytes(cls, p.stages, p.x_stages, L.tile_bytes, bn, L.num_experts);
+  // X [rows][K] gathered by row index: one-row boxes of 64 columns (four rows per copy)
+  Wna16Maps maps;
+  hq_status st = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, x_rows, ldx, 64, 1);
+  if (st != HQ_OK) return st;
+  maps.y = maps.x;  // MoE output rows use plain stores
+  if (launch_wna16(l, p, maps, s) != cudaSuccess) return HQ_ERR_CUDA;
+  *stages = p.stages;
+  *groups = p.groups;
+  return HQ_OK;
+}
+
 }  // namespace
 }  // namespace hq
 
@@ -653,55 +711,87 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   off += align_up(sizeof(int) * std::max<int64_t>(pairs, 1), kAlign);
   float* zbuf = reinterpret_cast<float*>(ws + off);
 
-  // Tokens per expert tile, from the mean rows per expert.  A tile's time is
-  // mostly its weight stream, so fewer, wider tiles win until the padding of
-  // the skewed experts' last tiles costs more MMA work than the weight re-reads
-  // it saves (measured on GB300 at E = 128, N = 1536, K = 2048, top-8: 32
-  // tokens per tile is best up to a mean of 16 rows per expert, 64 at 256).
-  const double mean_rows = static_cast<double>(pairs) / L.num_experts;
-  int bn = mean_rows <= 32 ? 32 : (mean_rows <= 384 ? 64 : 128);
-  const int forced_bn = env_int("HQ_FORCE_BN", 0);
-  if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) bn = forced_bn;
-  const int cls = wna16_class(bn);
-
+  const int bn = moe_tile_bn(static_cast<double>(pairs) / L.num_experts);
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L.num_experts, bn, exp_off, tile_off, perm,
                        expert_offsets_out, perm_out, reinterpret_cast<int*>(ws), s) != cudaSuccess)
     return HQ_ERR_CUDA;
-
-  GemmParams p{};
-  p.tiles = wt + L.tiles_off;
-  p.expert_stride = L.expert_stride;
-  p.tile_bytes = L.tile_bytes; p.hi_off = L.hi_off; p.scale_off = L.scale_off; p.zero_off = L.zero_off;
-  p.g_kb = L.g_kb; p.group_k = L.group_k; p.has_zeros = L.has_zeros; p.channel = L.channel;
-  p.zero_sym = (L.has_zeros || !L.signed_codes) ? 0 : (L.wtype == HQ_W_INT4 ? 8 : 32);
-  p.row_scale = L.channel ? reinterpret_cast<const float*>(wt + L.row_off) : nullptr;
-  p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
-  p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = tokens;
-  p.bn = bn; p.m_tiles = 0; p.num_tiles = 0; p.stream_k = 0; p.iters = 0; p.cluster = 1;
-  p.promote = (cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
-  p.idesc = idesc_f16(true, 128, bn);
-  p.status = reinterpret_cast<int*>(ws);
-  p.num_experts = L.num_experts; p.topk = topk;
-  p.tile_offsets = tile_off; p.expert_offsets = exp_off; p.perm = perm; p.topk_w = topk_w; p.zbuf = zbuf;
-  p.x_rows = static_cast<const __nv_bfloat16*>(x); p.ldx = ldx;
-  plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups);
-  if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
-  Wna16Launch l{};
-  l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
-  l.bf16 = true;
-  l.cls = cls;
-  l.moe = true;
-  l.grid = di.sms;
-  l.smem = wna16_smem_bytes(cls, p.stages, p.x_stages, L.tile_bytes, bn, L.num_experts);
-  // X [T][K] gathered by token index: one-row boxes of 64 columns (four rows per copy)
-  Wna16Maps maps;
-  st = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, tokens, ldx, 64, 1);
+  int stages = 0, groups = 0;
+  st = launch_moe_grouped(L, wt, bn, tokens, topk, topk_w, x, ldx, y, ldy, exp_off, tile_off, perm, zbuf,
+                          reinterpret_cast<int*>(ws), false, di, s, &stages, &groups);
   if (st != HQ_OK) return st;
-  maps.y = maps.x;  // MoE writes per-pair fp32 rows with plain stores
-  if (launch_wna16(l, p, maps, s) != cudaSuccess) return HQ_ERR_CUDA;
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L.num_experts, L.n, L.n_pad, y, ldy, true, s) != cudaSuccess)
     return HQ_ERR_CUDA;
-  g_last_plan = hq_plan_info{bn, 1, l.grid, 3, p.stages, cls, p.groups, 0};
+  g_last_plan = hq_plan_info{bn, 1, di.sms, 3, stages, wna16_class(bn), groups, 0};
+  return HQ_OK;
+}
+
+hq_status hq_moe_grouped_workspace_size(const hq_weight_desc* desc, int32_t form, int32_t rows, size_t* bytes) {
+  if (!desc || !bytes || rows < 0 || (form != HQ_MOE_GROUPED_CONTIGUOUS && form != HQ_MOE_GROUPED_MASKED))
+    return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*desc, &L);
+  if (st != HQ_OK) return st;
+  const int64_t x_rows = form == HQ_MOE_GROUPED_MASKED ? static_cast<int64_t>(rows) * L.num_experts : rows;
+  size_t ws = kAlign;
+  ws += 2 * align_up(sizeof(int) * (L.num_experts + 1), kAlign);
+  ws += align_up(sizeof(int) * std::max<int64_t>(x_rows, 1), kAlign);
+  *bytes = ws;
+  return HQ_OK;
+}
+
+hq_status hq_moe_grouped_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t form, int32_t rows,
+                              const int32_t* expert_rows, int32_t expected_rows, int32_t atype, const void* x,
+                              int64_t ldx, void* y, int64_t ldy, void* workspace, size_t ws_bytes, uint32_t flags,
+                              hq_stream_t stream) {
+  (void)flags;
+  if (!wdesc || rows < 0 || (form != HQ_MOE_GROUPED_CONTIGUOUS && form != HQ_MOE_GROUPED_MASKED))
+    return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*wdesc, &L);
+  if (st != HQ_OK) return st;
+  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (L.num_experts > 1024) return HQ_ERR_UNSUPPORTED;
+  if (rows == 0) return HQ_OK;
+  if (!w_t || !expert_rows || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;
+  if (ldx < L.k || ldy < L.n) return HQ_ERR_INVALID_ARG;
+  if (atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  if (L.wtype == HQ_W_FP8_E4M3) return HQ_ERR_UNSUPPORTED;
+  if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.stype != HQ_S_BF16) return HQ_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(w_t) & 255u))
+    return HQ_ERR_ALIGNMENT;
+  if ((ldx * 2) % 16 != 0 || (ldy * 2) % 16 != 0 || L.k % 8 != 0) return HQ_ERR_ALIGNMENT;
+  const bool masked = form == HQ_MOE_GROUPED_MASKED;
+  const int64_t x_rows = masked ? static_cast<int64_t>(rows) * L.num_experts : rows;
+  if (x_rows > (1 << 24)) return HQ_ERR_UNSUPPORTED;
+  size_t need = 0;
+  hq_moe_grouped_workspace_size(wdesc, form, rows, &need);
+  if (ws_bytes < need) return HQ_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  st = device_info(&di);
+  if (st != HQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* wt = static_cast<const uint8_t*>(w_t);
+  size_t off = kAlign;
+  int* exp_off = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * (L.num_experts + 1), kAlign);
+  int* tile_off = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * (L.num_experts + 1), kAlign);
+  int* perm = reinterpret_cast<int*>(ws + off);
+  // tile width from the caller's expected rows per expert (the counts stay on
+  // the device), else from the mean that fills the given rows
+  const double mean_rows = expected_rows > 0 ? expected_rows
+                           : masked          ? static_cast<double>(rows)
+                                             : static_cast<double>(rows) / L.num_experts;
+  const int bn = moe_tile_bn(mean_rows);
+  if (launch_moe_grouped_route(expert_rows, masked, rows, L.num_experts, bn, exp_off, tile_off, perm,
+                               reinterpret_cast<int*>(ws), s) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  int stages = 0, groups = 0;
+  st = launch_moe_grouped(L, wt, bn, static_cast<int>(x_rows), 1, nullptr, x, ldx, y, ldy, exp_off, tile_off, perm,
+                          nullptr, reinterpret_cast<int*>(ws), true, di, s, &stages, &groups);
+  if (st != HQ_OK) return st;
+  g_last_plan = hq_plan_info{bn, 1, di.sms, 2, stages, wna16_class(bn), groups, 0};
   return HQ_OK;
 }
 

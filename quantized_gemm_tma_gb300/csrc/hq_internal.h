@@ -125,6 +125,7 @@ struct GemmParams {
   const __nv_bfloat16* x_rows;  // MoE: activations [T][ldx] (per-lane row gather)
   int64_t ldx;
   float* zbuf;              // [T*topk][n_pad] weighted per-pair outputs
+  int moe_direct;           // grouped forms: row f of Y (16-bit, ldy) instead of a weighted zbuf row
 };
 
 struct Fp8Params {

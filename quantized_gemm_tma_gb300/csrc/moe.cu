@@ -10,6 +10,8 @@
 //          the prefix of m-tiles per expert for the grouped GEMM scheduler.
 // combine: Y[t, :] = sum_j Z[t*topk + j, :] in slot order (Z already carries
 //          the routing weight), rounded once to bf16.
+// grouped: the grouped-contiguous and grouped-masked input forms (rows per
+//          expert given by the caller): offsets, tile prefix and row map.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -141,6 +143,61 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
 }
 
+// Grouped input forms: the rows of expert e are given, either contiguously
+// (rows [offs[e], offs[e+1]) of X and Y) or masked (rows [e*max_rows,
+// e*max_rows + counts[e]) of an [E][max_rows] block).  Writes the compacted
+// offsets, the m-tile prefix and, for compacted position p of expert e, the
+// X / Y row perm[p].  Invalid counts or offsets make the expert contribute
+// nothing and set HQ_ERR_INVALID_VALUE.
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    moe_grouped_route_kernel(const int* __restrict__ rows_in, int masked, int rows, int num_experts, int bn,
+                             int* __restrict__ exp_off, int* __restrict__ tile_off, int* __restrict__ perm,
+                             int* __restrict__ status) {
+  __shared__ int warp_tot[33];
+  __shared__ int s_off[kRouteThreads];
+  __shared__ int s_base[kRouteThreads];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = num_experts;
+  int cnt = 0, base = 0;
+  if (tid < E) {
+    if (masked) {
+      cnt = rows_in[tid];
+      base = tid * rows;
+      if (cnt < 0 || cnt > rows) {
+        atomicCAS(status, 0, static_cast<int>(HQ_ERR_INVALID_VALUE));
+        cnt = 0;
+      }
+    } else {
+      base = rows_in[tid];
+      const int end = rows_in[tid + 1];
+      cnt = end - base;
+      if (base < 0 || cnt < 0 || end > rows) {
+        atomicCAS(status, 0, static_cast<int>(HQ_ERR_INVALID_VALUE));
+        cnt = 0;
+        base = 0;
+      }
+    }
+  }
+  int rows_total = 0, tiles_total = 0;
+  const int row_base = block_exclusive_scan(cnt, warp_tot, rows_total);
+  const int tile_base = block_exclusive_scan((cnt + bn - 1) / bn, warp_tot, tiles_total);
+  if (tid < E) {
+    exp_off[tid] = row_base;
+    tile_off[tid] = tile_base;
+    s_off[tid] = row_base;
+    s_base[tid] = base;
+  }
+  if (tid == 0) {
+    exp_off[E] = rows_total;
+    tile_off[E] = tiles_total;
+  }
+  __syncthreads();
+  for (int e = warp; e < E; e += kRouteWarps) {
+    const int o = s_off[e], b = s_base[e], c = (e + 1 < E ? s_off[e + 1] : rows_total) - o;
+    for (int r = lane; r < c; r += 32) perm[o + r] = b + r;
+  }
+}
+
 // One thread per (token, 8 consecutive outputs).
 __global__ void moe_combine_kernel(const float* __restrict__ z, const int* __restrict__ ids, int tokens, int topk,
                                    int num_experts, int n, int n_pad, __nv_bfloat16* __restrict__ y, int64_t ldy) {
@@ -183,6 +240,15 @@ cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, in
   if (e != cudaSuccess) return e;
   moe_route_kernel<<<1, kRouteThreads, smem, stream>>>(topk_ids, pairs, num_experts, bn, expert_offsets,
                                                         tile_offsets, perm, offsets_out, perm_out, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_grouped_route(const int* rows_in, bool masked, int rows, int num_experts, int bn,
+                                     int* expert_offsets, int* tile_offsets, int* perm, int* status,
+                                     cudaStream_t stream) {
+  if (num_experts > kRouteThreads) return cudaErrorInvalidValue;
+  moe_grouped_route_kernel<<<1, kRouteThreads, 0, stream>>>(rows_in, masked ? 1 : 0, rows, num_experts, bn,
+                                                             expert_offsets, tile_offsets, perm, status);
   return cudaGetLastError();
 }
 

@@ -305,4 +305,31 @@ def pin_moe_reductions():
     assert np.allclose(ya, yb, rtol=1e-12, atol=1e-12)
 
 
+def pin_moe_grouped_forms():
+    """Grouped forms on tiny integer inputs against brute-force triple loops,
+    the masked form against the contiguous form on the same rows, and rows
+    outside every expert's range left out."""
+    rng = np.random.default_rng(13)
+    e_n, n, k, rows = 3, 4, 5, 4
+    w = rng.integers(-3, 4, size=(e_n, n, k)).astype(np.float64)
+    # contiguous: experts 0, 1, 2 own rows [0, 2), [2, 2), [2, 5) of 6 (row 5 unused)
+    offs = np.array([0, 2, 2, 5], np.int32)
+    xc = rng.integers(-4, 5, size=(6, k)).astype(np.float64)
+    yc = oracle.moe_grouped_gemm(xc, "contiguous", offs, 6, w)
+    assert sorted(yc) == [0, 1, 2, 3, 4]
+    owner = {0: 0, 1: 0, 2: 2, 3: 2, 4: 2}
+    for i, e in owner.items():
+        brute = [sum(xc[i, kk] * w[e, j, kk] for kk in range(k)) for j in range(n)]
+        assert np.array_equal(yc[i], np.array(brute)), (i, e)
+    # masked: counts 2, 0, 3 in blocks of 4 rows hold the same rows as above
+    counts = np.array([2, 0, 3], np.int32)
+    xm = np.zeros((e_n * rows, k))
+    xm[0:2] = xc[0:2]
+    xm[8:11] = xc[2:5]
+    ym = oracle.moe_grouped_gemm(xm, "masked", counts, rows, w)
+    assert sorted(ym) == [0, 1, 8, 9, 10]
+    for im, ic in ((0, 0), (1, 1), (8, 2), (9, 3), (10, 4)):
+        assert np.array_equal(ym[im], yc[ic]), (im, ic)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

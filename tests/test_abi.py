@@ -109,6 +109,31 @@ def test_moe_host_validation(hq):
     assert need >= 4096 * 8 * 1536 * 4
 
 
+def test_moe_grouped_host_validation(hq):
+    d = hq.make_desc("mxfp4", "ue8m0", 1536, 2048, num_experts=128, group_k=32)
+    fake = 0x10000
+    with pytest.raises(hq.HQError) as ei:  # unknown form
+        hq.hq_moe_grouped_gemm(d, fake, 7, 64, fake, 0, "bf16", fake, 2048, fake, 1536, fake, 1 << 30)
+    assert ei.value.status == hq.HQ_ERR_INVALID_ARG
+    with pytest.raises(hq.HQError) as ei:  # fp16 activations: the grouped kernels are bf16-only
+        hq.hq_moe_grouped_gemm(d, fake, hq.HQ_MOE_GROUPED_MASKED, 64, fake, 0, "fp16", fake, 2048, fake, 1536,
+                               fake, 1 << 30)
+    assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
+    with pytest.raises(hq.HQError) as ei:  # unaligned row pitch
+        hq.hq_moe_grouped_gemm(d, fake, hq.HQ_MOE_GROUPED_CONTIGUOUS, 64, fake, 0, "bf16", fake, 2052, fake, 1536,
+                               fake, 1 << 30)
+    assert ei.value.status == hq.HQ_ERR_ALIGNMENT
+    small = hq.hq_moe_grouped_workspace_size(d, hq.HQ_MOE_GROUPED_MASKED, 64)
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_moe_grouped_gemm(d, fake, hq.HQ_MOE_GROUPED_MASKED, 64, fake, 0, "bf16", fake, 2048, fake, 1536,
+                               fake, small - 1)
+    assert ei.value.status == hq.HQ_ERR_WORKSPACE_TOO_SMALL
+    # the row map covers E * rows (masked) or rows (contiguous) entries
+    assert small >= 128 * 64 * 4
+    assert hq.hq_moe_grouped_workspace_size(d, hq.HQ_MOE_GROUPED_CONTIGUOUS, 64) < small
+    hq.hq_moe_grouped_gemm(d, 0, hq.HQ_MOE_GROUPED_MASKED, 0, 0, 0, "bf16", 0, 2048, 0, 1536, 0, 0)  # no rows
+
+
 def test_workspace_sizes_bounded(hq):
     d = _desc(hq, n=8192, k=8192, has_zeros=True, signed_codes=False)
     small = hq.hq_gemm_workspace_size(d, 16, "bf16")

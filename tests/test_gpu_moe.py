@@ -92,3 +92,85 @@ def test_full_size_sampled(tokens):
     rng = np.random.default_rng(tokens)
     rows = np.unique(np.concatenate([[0, tokens - 1], rng.integers(0, tokens, size=min(tokens, 12))]))
     check(y[rows], _ref(qw, acts, r, rows), f"moe T={tokens}")
+
+
+# ------------------------------------------------------------------ grouped forms
+def _grouped(qw, form, rows, expert_rows, x_bits, expected=0, ldy=None):
+    """hq_moe_grouped_gemm on device copies; returns (Y as float64 with NaN where
+    nothing was written, device status)."""
+    import torch
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import DevWeight, stream, to_dev, workspace
+    dw = DevWeight(qw)
+    x_rows, k = x_bits.shape
+    ldx = -(-k // 8) * 8
+    xh = np.zeros((x_rows, ldx), np.uint16)
+    xh[:, :k] = x_bits
+    ldy = ldy or -(-qw.n // 8) * 8
+    y = torch.full((x_rows, ldy), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fcode = hq.HQ_MOE_GROUPED_MASKED if form == "masked" else hq.HQ_MOE_GROUPED_CONTIGUOUS
+    ws = workspace(hq.hq_moe_grouped_workspace_size(dw.desc, fcode, rows))
+    er = to_dev(np.asarray(expert_rows, np.int32))
+    hq.hq_moe_grouped_gemm(dw.desc, dw.wt, fcode, rows, er, expected, "bf16", to_dev(xh), ldx, y, ldy, ws,
+                           ws.numel(), 0, stream())
+    st = hq.hq_status_read(ws, clear=True, stream=stream())
+    return y[:, :qw.n].double().cpu().numpy(), st
+
+
+def _grouped_ref(qw, form, rows, expert_rows, x_bits):
+    def expert(e):
+        z = None if qw.zeros is None else qw.zeros[e:e + 1]
+        return oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes[e:e + 1], qw.scales[e:e + 1], z, qw.group_k,
+                                 qw.signed, qw.stype, 1)[0]
+    return oracle.moe_grouped_gemm(oracle.decode_activations("bf16", x_bits), form, expert_rows, rows, expert)
+
+
+GROUPED = [
+    # form, seed, weight, experts, n, k, rows (total, or per expert when masked)
+    ("masked", 20, "mxfp4", 8, 256, 512, 40),
+    ("masked", 21, "int4", 4, 384, 256, 300),       # several 64-token tiles per expert
+    ("contiguous", 22, "mxfp4", 8, 200, 384, 150),  # ragged N
+    ("contiguous", 23, "int4", 6, 256, 512, 700),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(GROUPED)), ids=lambda i: "-".join(map(str, GROUPED[i][:3])))
+def test_grouped_forms(idx):
+    form, seed, wt, e, n, k, rows = GROUPED[idx]
+    rng = np.random.default_rng(seed)
+    if wt == "mxfp4":
+        qw = synth.random_codes_weight(seed, "mxfp4", n, k, num_experts=e, group_k=32)
+    else:
+        qw = synth.quantize_int_groupwise(rng.standard_normal((e, n, k)) * 0.02, 4, 128, False, "bf16")
+    if form == "masked":
+        counts = rng.integers(0, rows + 1, size=e)
+        counts[0], counts[-1] = rows, 0               # a full block and an empty expert
+        expert_rows, x_rows = counts, e * rows
+    else:
+        cuts = np.sort(rng.integers(0, rows - 5, size=e - 1))
+        expert_rows = np.concatenate([[0], cuts, [rows - 5]])   # the last 5 rows belong to no expert
+        x_rows = rows
+    x_bits = synth.make_activations(rng, x_rows, k, "bf16").data
+    y, st = _grouped(qw, form, rows, expert_rows, x_bits)
+    assert st == 0
+    ref = _grouped_ref(qw, form, rows, expert_rows, x_bits)
+    valid = np.array(sorted(ref), dtype=np.int64)
+    check(y[valid], np.stack([ref[i] for i in valid]), f"grouped {GROUPED[idx]}")
+    untouched = np.setdiff1d(np.arange(x_rows), valid)
+    assert np.isnan(y[untouched]).all(), "rows outside every expert's range were written"
+
+
+def test_grouped_invalid_counts_set_status():
+    import quantized_gemm_tma_gb300 as hq
+    rng = np.random.default_rng(30)
+    qw = synth.random_codes_weight(30, "mxfp4", 128, 256, num_experts=4, group_k=32)
+    counts = np.array([16, 40, 3, 16])                 # expert 1 claims more rows than its block holds
+    x_bits = synth.make_activations(rng, 4 * 32, 256, "bf16").data
+    y, st = _grouped(qw, "masked", 32, counts, x_bits)
+    assert st == hq.HQ_ERR_INVALID_VALUE
+    ok = np.array(counts)
+    ok[1] = 0
+    ref = _grouped_ref(qw, "masked", 32, ok, x_bits)
+    valid = np.array(sorted(ref), dtype=np.int64)
+    check(y[valid], np.stack([ref[i] for i in valid]), "valid experts")
+    assert np.isnan(y[32:64]).all()

@@ -110,6 +110,14 @@ def _moe_unweighted(a, topk_ids, topk_w, w):
     return _orig_moe_gemm(a, topk_ids, np.ones_like(np.asarray(topk_w, dtype=np.float32)), w)
 
 
+_orig_ranges = MOE.moe_grouped_ranges
+
+
+def _ranges_masked_off_by_one(form, expert_rows, num_experts, rows):
+    r = _orig_ranges(form, expert_rows, num_experts, rows)
+    return [(lo, hi + 1) if form == "masked" and hi > lo else (lo, hi) for lo, hi in r]
+
+
 MUTATIONS = {
     "nibble_order_swapped": [(F, "unpack_nibbles", _swap_nibbles)],
     "int6_big_endian": [(F, "unpack_int6", _int6_big_endian)],
@@ -124,6 +132,7 @@ MUTATIONS = {
                                   (oracle, "decode_activations", _fp8_scale_transposed)],
     "moe_perm_unstable": [(MOE, "moe_route", _route_unstable), (oracle, "moe_route", _route_unstable)],
     "moe_combine_unweighted": [(MOE, "moe_gemm", _moe_unweighted), (oracle, "moe_gemm", _moe_unweighted)],
+    "moe_masked_count_off_by_one": [(MOE, "moe_grouped_ranges", _ranges_masked_off_by_one)],
 }
 
 
