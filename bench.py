@@ -55,7 +55,7 @@ BLOCK = 25         # back-to-back calls of one shape between two events
 # DRAM bytes (read + write) per launch of the WnA16 INT4 kernel, from the ncu
 # traffic capture listed in profiles/wna16_int4_asym_g128_n8192_k8192.md,
 # keyed by M; valid only while the kernel sources hash to `sha` (else null).
-NCU_TRAFFIC = {"sha": "3e014c3d2e3f8f15", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
+NCU_TRAFFIC = {"sha": "29395d556d0a38cd", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
                "bytes": {16: 35_468_544, 128: 37_302_784, 1024: 53_039_360, 4096: 165_367_296}}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 

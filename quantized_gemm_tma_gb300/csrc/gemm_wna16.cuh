@@ -8,35 +8,40 @@
 // rows x BN tokens ("swap AB": the weights are the MMA's M side, so a
 // decode-sized M only pads the MMA N dimension, down to 16).
 //
-// Work: the CTA walks a list of units (tile, K-block range).  Dense problems
-// with few tiles are split "stream-K": the tiles' K-blocks are dealt out in
-// equal contiguous ranges, one per CTA, so every SM streams the same number
-// of weight bytes; a tile covered by several CTAs is finished by the last of
-// them, which sums the fp32 partials in CTA order (deterministic).  Problems
-// with many tiles, and MoE, take whole tiles round-robin.
+// Work: the CTA walks a list of units (tile, K-block range).  A dense problem
+// whose tiles fill most SMs twice over runs each tile on a 2-CTA cluster that
+// splits K in halves (rank 1's fp32 sums reach rank 0 through distributed
+// shared memory).  Dense problems with few tiles are split "stream-K": the
+// tiles' K-blocks are dealt out in equal contiguous ranges, one per CTA, and
+// a tile covered by several CTAs is finished by the last of them, which sums
+// the fp32 partials in CTA order (deterministic).  Larger problems, and MoE,
+// take whole tiles round-robin.
 //
 // Pipeline per CTA (one CTA per SM), warp roles:
 //   warps 0-3    epilogue: one TMEM lane quarter each; wait for a unit's
-//                accumulators, sum the issuers' partial accumulators, scale
-//                and store Y (or a partial, or MoE per-pair rows).
-//   warps 4-19   dequantisers, in KPS groups; group g converts K-block g of
-//                each stage.  A thread owns one weight row (its TMEM lane)
-//                and 4/(16/KPS/4) of the block's four 32-column chunks, turns
-//                the packed codes into bf16x2/f16x2 pairs and writes them into
-//                the group's next A slot in TMEM with tcgen05.st.
+//                accumulators, sum the issuers' partial accumulators, scale,
+//                and store Y through shared-memory boxes and tensor stores
+//                (or a partial, a cluster exchange, or MoE per-pair rows).
+//   warps 4-19   dequantisers.  Two K-blocks per stage (bn <= 64): four
+//                streams, stream t converting K-block t & 1 of every stage of
+//                parity t >> 1 (a whole K-block of its 32 rows per warp).  One
+//                K-block per stage: all 16 warps on each K-block, one 32-column
+//                chunk each.  A thread owns one weight row (its TMEM lane),
+//                turns the packed codes into bf16x2/f16x2 pairs and writes
+//                them into an A slot in TMEM with tcgen05.st.
 //   warp 20      weight producer: per stage one bulk copy of up to KPS
 //                consecutive weight tiles (one contiguous run of the tile
-//                layout) into the weight ring, released as soon as the
-//                dequantisers hold the codes in registers.
+//                layout) into the weight ring, released once the dequantisers
+//                have converted the codes.
 //   warp 21      activation producer: per stage one tensor copy per 64-column
 //                slab (128-byte swizzle) into the activation ring, released
-//                by the MMA; MoE rows are gathered by routing index, four rows
-//                per tile::gather4 copy.
+//                by the MMA; MoE rows are gathered by routing index (per-lane
+//                16-byte copies, or four rows per tile::gather4 copy for
+//                16-token tiles).
 //   warps 22..   MMA issuers: issuer p takes K-block p of every stage and
-//                accumulates into its own TMEM accumulator, so up to four
-//                threads issue tcgen05.mma.kind::f16 concurrently (one thread
-//                issues an M128 K16 MMA only every ~50-100 cycles, which alone
-//                would leave a decode-sized tile short of the HBM rate).
+//                accumulates into its own TMEM accumulator, so two threads
+//                issue tcgen05.mma.kind::f16 concurrently for narrow tiles
+//                (one thread issues an M128 K16 MMA only every ~50 cycles).
 //
 // Every wait is bounded (2 s, or the CTA abort flag); on a timeout the CTA
 // records HQ_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and
@@ -55,12 +60,11 @@ namespace hq {
 namespace wna16 {
 
 // Tile-width classes: maximum tokens per tile, K-blocks per stage (= MMA
-// issuers = dequantiser groups), accumulator buffers.  The 16 dequantiser
-// warps form kKps groups; group g takes K-block g of every stage and owns
-// kDa = 4 / kKps A slots of 64 TMEM columns (a ring, so it can convert the
-// next K-block while the MMA still reads the last).  TMEM: A slots in
-// columns [0, 256), accumulators (kDacc x kIss x kBnMax columns) in
-// [256, 512).
+// issuers), accumulator buffers.  With one K-block per stage the 16
+// dequantiser warps share a ring of four A slots of 64 TMEM columns; with two
+// they form four streams of four warps, each owning one slot used as two half
+// slots of 32 columns.  TMEM: A slots in columns [0, 256), accumulators
+// (kDacc x kIss x kBnMax columns, or the promotion ring) in [256, 512).
 template <int CLS>
 struct Cls;
 template <>
