@@ -510,7 +510,7 @@ def main():
                                    "bf16 activations; route + grouped GEMM + combine per call",
                        "sweep": msw}
     if not args.no_cpu_baseline and world >= 1:
-        v, dt, desc, cores = cpu_oracle_sample(seed=0, rows_cap=2048)
+        v, dt, desc, cores = cpu_oracle_sample(seed=0, rows_cap=max(M_SWEEP))  # the whole sweep
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
                                 "seconds": round(dt, 2)}
     print(json.dumps(line), flush=True)
