@@ -387,11 +387,13 @@ def run_gpu(args, rank: int, world: int):
 
 
 def reduce_max(value: float, world: int) -> float:
+    """The maximum of `value` over all ranks (the slowest replica's time)."""
     if world <= 1:
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
