@@ -197,13 +197,18 @@ hq_status hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);
  * w_t       hq_transform output for wdesc
  * m         rows of X and Y (0 is a no-op)
  * atype     hq_atype; INT with group scales needs stype == atype; MXFP4 needs
- *           BF16 or FP16; FP8 weights need FP8 activations
- * x, ldx    X [m][k] row-major, row stride ldx elements (ldx >= k)
+ *           BF16; FP8 weights need FP8 activations
+ * x, ldx    X [m][k] row-major, row stride ldx elements (ldx >= k; the row
+ *           pitch a multiple of 16 bytes; x 16-byte aligned)
  * x_scales  FP8 activations only: float32 [m][ceil(k/128)] row-major
- * y, ldy    Y [m][n] row-major, bf16 for BF16/FP8 activations, fp16 for FP16
+ * y, ldy    Y [m][n] row-major, bf16 for BF16/FP8 activations, fp16 for FP16;
+ *           y 16-byte aligned, ldy even; with ldy a multiple of 8 the rows are
+ *           written by tensor stores, otherwise by plain stores
  * workspace >= hq_gemm_workspace_size() bytes, initialised once
  * flags     HQ_FLAG_* bits
- * Accumulation is fp32 in tensor memory; the output is rounded once.
+ * Accumulation is fp32 in tensor memory; the output is rounded once.  Errors
+ * found on the host (arguments, alignment HQ_ERR_ALIGNMENT, workspace size)
+ * return before any launch; device timeouts go to the workspace status word.
  */
 hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32_t atype,
                   const void* x, int64_t ldx, const float* x_scales, void* y, int64_t ldy,
