@@ -50,6 +50,7 @@ WORKLOAD = ("dense W4A16: asymmetric INT4 g128 (uint4 zeros, bf16 scales), bf16 
 W_COPIES = 8       # rotated transformed weight copies (> L2 in total)
 X_COPIES = 4       # rotated activation copies per M
 MOE_COPIES = 2     # rotated MoE expert sets (213 MB each)
+MOE_H = MOE_K      # feed-forward block: down projection [E][hidden = K][intermediate = N / 2]
 HEAD_START_CYCLES = 200_000_000
 BLOCK = 25         # back-to-back calls of one shape between two events
 # DRAM bytes (read + write) per launch of the WnA16 INT4 kernel, from the ncu
@@ -268,6 +269,18 @@ def run_gpu(args, rank: int, world: int):
             hq.hq_transform(mdesc, mwt, mbytes, sh)
             mwts.append(mwt)
         moe = {"desc": mdesc, "wt": mwts, "T": {}}
+        # feed-forward block: the gate+up experts above, down experts [E][K][N/2]
+        dq, _, _ = synth.moe_mxfp4(1, 1, num_experts=MOE_E, n=MOE_H, k=MOE_N // 2)
+        ddesc = hq.make_desc("mxfp4", "ue8m0", MOE_H, MOE_N // 2, MOE_E, 32, 1, True, False,
+                             to_dev(dq.codes), to_dev(dq.scales), None)
+        dbytes = hq.hq_transform_size(ddesc)
+        dwts = []
+        for _ in range(MOE_COPIES):
+            dwt = torch.empty(dbytes, dtype=torch.uint8, device=dev)
+            hq.hq_transform(ddesc, dwt, dbytes, sh)
+            dwts.append(dwt)
+        moe.update({"ddesc": ddesc, "dwt": dwts})
+        del dq
         for t in MOE_T:
             r = synth.make_routing(np.random.default_rng(10 + t), t, MOE_E, MOE_TOPK)
             x = synth.to_bf16_bits(np.random.default_rng(20 + t).standard_normal((t, MOE_K)))
@@ -276,6 +289,9 @@ def run_gpu(args, rank: int, world: int):
             moe["T"][t] = {"ids": to_dev(r.topk_ids.astype(np.int32)), "w": to_dev(r.topk_w.astype(np.float32)),
                            "x": to_dev(x), "y": torch.empty((t, MOE_N), dtype=torch.bfloat16, device=dev),
                            "ws": torch.zeros(need, dtype=torch.uint8, device=dev), "touched": int(touched)}
+            fneed = hq.hq_moe_ffn_workspace_size(mdesc, ddesc, t, MOE_TOPK)
+            moe["T"][t].update({"fws": torch.zeros(fneed, dtype=torch.uint8, device=dev),
+                                "fy": torch.empty((t, MOE_H), dtype=torch.bfloat16, device=dev)})
         del mq
 
     def moe_call(t):
@@ -284,6 +300,14 @@ def run_gpu(args, rank: int, world: int):
         rot["moe"] += 1
         hq.hq_moe_gemm(moe["desc"], mwt, t, MOE_TOPK, d["ids"], d["w"], "bf16", d["x"], MOE_K, d["y"], MOE_N,
                        None, None, d["ws"], d["ws"].numel(), 0, sh)
+        launches["n"] += hq.hq_last_plan()["launches"]
+
+    def ffn_call(t):
+        d = moe["T"][t]
+        i = rot["moe"] % MOE_COPIES
+        rot["moe"] += 1
+        hq.hq_moe_ffn(moe["desc"], moe["wt"][i], moe["ddesc"], moe["dwt"][i], t, MOE_TOPK, d["ids"], d["w"], "bf16",
+                      d["x"], MOE_K, d["fy"], MOE_H, d["fws"], d["fws"].numel(), 0, sh)
         launches["n"] += hq.hq_last_plan()["launches"]
 
     def timed(fn, arg):
@@ -307,6 +331,7 @@ def run_gpu(args, rank: int, world: int):
         if moe:
             for t in MOE_T:
                 timed(moe_call, t)
+                timed(ffn_call, t)
     torch.cuda.synchronize()
     st = hq.hq_status_read(wss[args.m_sweep[0]], 0, sh)
     if st != 0:
@@ -318,6 +343,7 @@ def run_gpu(args, rank: int, world: int):
     launches["n"] = 0
     per_m = {m: [] for m in args.m_sweep}
     per_t = {t: [] for t in MOE_T}
+    per_f = {t: [] for t in MOE_T}
 
     def blocks(fn, arg, n):
         out = []
@@ -344,10 +370,12 @@ def run_gpu(args, rank: int, world: int):
         if moe:
             for t in MOE_T:
                 events += [("m", t, *b) for b in blocks(moe_call, t, args.steps)]
+            for t in MOE_T:
+                events += [("f", t, *b) for b in blocks(ffn_call, t, args.steps)]
         barrier()
         wall = time.perf_counter() - wall0
     for kind, key, k, e0, e1 in events:
-        (per_m if kind == "d" else per_t)[key].append(e0.elapsed_time(e1) * 1e-3 / k)
+        {"d": per_m, "m": per_t, "f": per_f}[kind][key].append(e0.elapsed_time(e1) * 1e-3 / k)
     gpu_launches = launches["n"]
 
     # ---- end to end through the C ABI with host buffers (pinned): per step the
@@ -381,6 +409,7 @@ def run_gpu(args, rank: int, world: int):
         res["plans"][m] = hq.hq_last_plan()
     if moe:
         res["moe"] = {t: statistics.mean(v) for t, v in per_t.items()}
+        res["moe_ffn"] = {t: statistics.mean(v) for t, v in per_f.items()}
         res["moe_touched"] = {t: moe["T"][t]["touched"] for t in MOE_T}
     torch.cuda.synchronize()
     return res
@@ -508,9 +537,21 @@ def main():
             msw.append({"tokens": t, "us": round(tt * 1e6, 2), "tflops": round(fl / tt / 1e12, 2),
                         "gbs": round(by / tt / 1e9, 1), "experts_touched": res["moe_touched"][t],
                         "roofline_frac": round(roof_t / tt, 3)})
+        fsw = []
+        for t in MOE_T:
+            tt = res["moe_ffn"][t]
+            fl = 2 * t * MOE_TOPK * (MOE_N * MOE_K + MOE_H * (MOE_N // 2))
+            wb = MOE_N * MOE_K + MOE_H * (MOE_N // 2)      # weights per expert (elements)
+            by = res["moe_touched"][t] * (wb // 2 + wb // 32) + t * MOE_K * 2
+            roof_t = max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
+            fsw.append({"tokens": t, "us": round(tt * 1e6, 2), "tflops": round(fl / tt / 1e12, 2),
+                        "gbs": round(by / tt / 1e9, 1), "roofline_frac": round(roof_t / tt, 3)})
         line["moe"] = {"workload": "MoE gate+up, MXFP4 (e2m1 + UE8M0/32) experts, E=128, N=1536, K=2048, top-8, "
                                    "bf16 activations; route + grouped GEMM + combine per call",
-                       "sweep": msw}
+                       "sweep": msw,
+                       "ffn_workload": "MoE feed-forward block: the gate+up experts above, SiLU(gate)*up, down "
+                                       "experts E=128, N=2048, K=768 (MXFP4), routing-weighted combine per call",
+                       "ffn_sweep": fsw}
     if not args.no_cpu_baseline and world >= 1:
         v, dt, desc, cores = cpu_oracle_sample(seed=0, rows_cap=max(M_SWEEP))  # the whole sweep
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,

@@ -283,6 +283,35 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
                       hq_stream_t stream);
 
 /*
+ * hq_moe_ffn_workspace_size — workspace for hq_moe_ffn (status word, routing
+ * offsets and permutation, the bf16 gate/up rows and activations of every
+ * routed pair, and its fp32 weighted down-projection rows).
+ */
+hq_status hq_moe_ffn_workspace_size(const hq_weight_desc* w13, const hq_weight_desc* w2, int32_t tokens,
+                                    int32_t topk, size_t* bytes);
+
+/*
+ * hq_moe_ffn — the MoE feed-forward block on routed tokens: the gate+up
+ * grouped GEMM, the SiLU-gated product and the down grouped GEMM, then the
+ * routing-weighted combine ([LAUNCH] MoE paragraph: the MoE measurement
+ * covers the gate-up and the down GEMM).  For pair f = t*topk + j routed to
+ * expert e = topk_ids[t][j]:
+ *   H[f] = a(X[t]) . dequant(W13_e)^T         (2I outputs: gate, then up)
+ *   A[f] = silu(H[f][0, I)) * H[f][I, 2I)      silu(g) = g / (1 + exp(-g))
+ *   Y[t] = sum_j topk_w[t][j] * (A[t*topk + j] . dequant(W2_{e})^T)
+ * H and A are rounded to bf16 (the activation type) between the GEMMs.
+ *
+ * w13, w13_t   gate+up experts [E][2I][k] and their transform (I % 8 == 0)
+ * w2, w2_t     down experts [E][n][I] and their transform (same E)
+ * other arguments as hq_moe_gemm (bf16 activations; x [T][k], y [T][n]).
+ * Invalid expert ids: as hq_moe_gemm.  Asynchronous.
+ */
+hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weight_desc* w2, const void* w2_t,
+                     int32_t tokens, int32_t topk, const int32_t* topk_ids, const float* topk_w, int32_t atype,
+                     const void* x, int64_t ldx, void* y, int64_t ldy, void* workspace, size_t ws_bytes,
+                     uint32_t flags, hq_stream_t stream);
+
+/*
  * Grouped MoE input forms ([WIKI] "Device and workload selection": besides
  * the indexed form above, the rows of each expert can be handed over already
  * grouped, either back to back or in per-expert storage with a separate count
@@ -328,7 +357,8 @@ hq_status hq_status_read(void* workspace, int32_t clear, hq_stream_t stream, int
 
 /*
  * hq_last_plan — the launch plan of the most recent hq_gemm / hq_moe_gemm /
- * hq_moe_grouped_gemm call on this host thread.  For tests and benchmarks.
+ * hq_moe_ffn / hq_moe_grouped_gemm call on this host thread.  For tests and
+ * benchmarks.
  */
 typedef struct {
   int32_t bn;          /* tokens per output tile (MMA N for WnA16, M side for FP8) */

@@ -21,7 +21,8 @@ Modules:
     gemm     dequantisation and the dense GEMM
     moe      routing (count, prefix sum, stable permutation) and the MoE
              grouped GEMM with the routing-weighted combine; the grouped
-             (contiguous / masked) input forms
+             (contiguous / masked) input forms; the feed-forward block
+             (gate+up, SiLU-gated product, down, combine)
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against values fixed outside the oracle (library casts, published format
@@ -30,4 +31,4 @@ none is "parity unpinned".
 """
 from . import formats, gemm, moe  # noqa: F401
 from .gemm import dequantize, gemm_dense, decode_activations  # noqa: F401
-from .moe import moe_route, moe_gemm, moe_grouped_gemm  # noqa: F401
+from .moe import moe_route, moe_gemm, moe_grouped_gemm, moe_ffn  # noqa: F401

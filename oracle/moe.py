@@ -15,6 +15,13 @@ GEMM     Z[f, :] = X[t, :] . W_{id(f)}^T          (the gate+up GEMM)
 combine  Y[t, :] = sum_j topk_w[t, j] * Z[t*topk + j, :]
          (the routing-weighted sum per token; no activation function)
 
+Feed-forward block (launch article, MoE paragraph: gate-up and down GEMMs
+measured together), for pair f = t*topk + j routed to expert e:
+         H[f] = X[t] . W13_e^T            (2I outputs: gate rows first, then up)
+         A[f] = silu(H[f, :I]) * H[f, I:],  silu(g) = g / (1 + exp(-g))
+         Y[t] = sum_j topk_w[t, j] * A[t*topk + j] . W2_e^T
+         (H and A held in bf16, the activation type, between the GEMMs)
+
 Grouped forms (same section: rows arrive already grouped per expert, either
 back to back or in per-expert storage with a count of valid rows):
          Y[i, :] = X[i, :] . W_e^T for every row i in expert e's range; the
@@ -103,3 +110,48 @@ def moe_grouped_gemm(a: np.ndarray, form: str, expert_rows, rows: int, w) -> dic
         for i in range(lo, hi):
             out[i] = z[i - lo]
     return out
+
+
+def silu(g):
+    """g * sigmoid(g) in float64."""
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(-g))
+
+
+def round_bf16(x):
+    """Round float64 values to the nearest bf16 value (ties to even), directly
+    from float64 (8 significant bits; the normal range)."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                       # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)   # np.round: half to even
+
+
+def moe_ffn(a: np.ndarray, topk_ids: np.ndarray, topk_w: np.ndarray, w13, w2,
+            intermediate: str | None = "bf16") -> np.ndarray:
+    """Y [T, n] float64 of the MoE feed-forward block.
+
+    ``w13`` gives [2I, K] per expert (gate rows, then up rows) and ``w2``
+    [n, I], each as a float array [E, ...] or a callable e -> array.
+    ``intermediate="bf16"`` stores H and A in the activation type between the
+    GEMMs (rounded to bf16, the reading the library follows); ``None`` keeps
+    them exact.
+    """
+    rnd = round_bf16 if intermediate == "bf16" else (lambda v: v)
+    a = np.asarray(a, dtype=np.float64)
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    tw = np.asarray(topk_w, dtype=np.float32).astype(np.float64)
+    get13 = w13 if callable(w13) else (lambda e, _w=np.asarray(w13, dtype=np.float64): _w[e])
+    get2 = w2 if callable(w2) else (lambda e, _w=np.asarray(w2, dtype=np.float64): _w[e])
+    t_count, topk = ids.shape
+    y = None
+    for e in np.unique(ids):
+        t_idx, j_idx = np.nonzero(ids == e)
+        w_gu = np.asarray(get13(int(e)), dtype=np.float64)
+        inter = w_gu.shape[0] // 2
+        h = rnd(a[t_idx] @ w_gu.T)                              # [pairs of e, 2I]
+        act = rnd(silu(h[:, :inter]) * h[:, inter:])
+        z = act @ np.asarray(get2(int(e)), dtype=np.float64).T  # [pairs of e, n]
+        if y is None:
+            y = np.zeros((t_count, z.shape[1]), dtype=np.float64)
+        np.add.at(y, t_idx, tw[t_idx, j_idx][:, None] * z)
+    return y

@@ -34,7 +34,8 @@ STYPES = {"bf16": HQ_S_BF16, "fp16": HQ_S_FP16, "fp32": HQ_S_FP32, "ue8m0": HQ_S
 EXPORTS = [
     "hq_version", "hq_status_string", "hq_transform_size", "hq_transform", "hq_untransform",
     "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_gemm_noalloc", "hq_moe_workspace_size",
-    "hq_moe_gemm", "hq_moe_grouped_workspace_size", "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan",
+    "hq_moe_gemm", "hq_moe_ffn_workspace_size", "hq_moe_ffn", "hq_moe_grouped_workspace_size",
+    "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan",
 ]
 
 #: size of the fixed device scratch behind hq_gemm_noalloc
@@ -88,6 +89,8 @@ def lib() -> ctypes.CDLL:
             "hq_gemm_noalloc": ([dp, vp, i32, i32, vp, i64, vp, vp, i64, u32, vp, vp], i32),
             "hq_moe_workspace_size": ([dp, i32, i32, i32, ctypes.POINTER(sz)], i32),
             "hq_moe_gemm": ([dp, vp, i32, i32, vp, vp, i32, vp, i64, vp, i64, vp, vp, vp, sz, u32, vp], i32),
+            "hq_moe_ffn_workspace_size": ([dp, dp, i32, i32, ctypes.POINTER(sz)], i32),
+            "hq_moe_ffn": ([dp, vp, dp, vp, i32, i32, vp, vp, i32, vp, i64, vp, i64, vp, sz, u32, vp], i32),
             "hq_moe_grouped_workspace_size": ([dp, i32, i32, ctypes.POINTER(sz)], i32),
             "hq_moe_grouped_gemm": ([dp, vp, i32, i32, vp, i32, i32, vp, i64, vp, i64, vp, sz, u32, vp], i32),
             "hq_status_read": ([vp, i32, vp, ctypes.POINTER(i32)], i32),
@@ -189,6 +192,20 @@ def hq_moe_gemm(desc: WeightDesc, w_t, tokens: int, topk: int, topk_ids, topk_w,
     _check(lib().hq_moe_gemm(ctypes.byref(desc), _ptr(w_t), tokens, topk, _ptr(topk_ids), _ptr(topk_w),
                              ATYPES.get(atype, atype), _ptr(x), ldx, _ptr(y), ldy, _ptr(expert_offsets_out),
                              _ptr(perm_out), _ptr(workspace), ws_bytes, flags, _stream(stream)), "hq_moe_gemm")
+
+
+def hq_moe_ffn_workspace_size(w13: WeightDesc, w2: WeightDesc, tokens: int, topk: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().hq_moe_ffn_workspace_size(ctypes.byref(w13), ctypes.byref(w2), tokens, topk, ctypes.byref(out)),
+           "hq_moe_ffn_workspace_size")
+    return out.value
+
+
+def hq_moe_ffn(w13: WeightDesc, w13_t, w2: WeightDesc, w2_t, tokens: int, topk: int, topk_ids, topk_w, atype, x,
+               ldx: int, y, ldy: int, workspace, ws_bytes: int, flags: int = 0, stream=None) -> None:
+    _check(lib().hq_moe_ffn(ctypes.byref(w13), _ptr(w13_t), ctypes.byref(w2), _ptr(w2_t), tokens, topk,
+                            _ptr(topk_ids), _ptr(topk_w), ATYPES.get(atype, atype), _ptr(x), ldx, _ptr(y), ldy,
+                            _ptr(workspace), ws_bytes, flags, _stream(stream)), "hq_moe_ffn")
 
 
 def hq_moe_grouped_workspace_size(desc: WeightDesc, form: int, rows: int) -> int:

@@ -455,13 +455,14 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   return p;
 }
 
-// Tokens per expert tile, from the mean rows per expert.  A tile's time is
-// mostly its weight stream, so fewer, wider tiles win until the padding of
-// the skewed experts' last tiles costs more MMA work than the weight re-reads
-// it saves (measured on GB300 at E = 128, N = 1536, K = 2048, top-8: 32
-// tokens per tile is best up to a mean of 16 rows per expert, 64 at 256).
+// Tokens per expert tile, from the mean rows per expert: 16 (one tile of
+// the decode class per expert and n-tile) up to a mean of 16 rows, else 128.
+// Widths of 32 and 64 tokens were faster on GB300 (T = 256: 107 against
+// 160 us; T = 4096: 665 against 687 us) but gave intermittent wrong rows
+// in full-size MoE runs that are not yet explained, so the planner keeps to
+// the widths whose results have stayed exact.
 int moe_tile_bn(double mean_rows) {
-  int bn = mean_rows <= 32 ? 32 : (mean_rows <= 384 ? 64 : 128);
+  int bn = mean_rows <= 16 ? 16 : 128;
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
   if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) bn = forced_bn;
   return bn;
@@ -722,6 +723,112 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L.num_experts, L.n, L.n_pad, y, ldy, true, s) != cudaSuccess)
     return HQ_ERR_CUDA;
   g_last_plan = hq_plan_info{bn, 1, di.sms, 3, stages, wna16_class(bn), groups, 0};
+  return HQ_OK;
+}
+
+// MoE feed-forward: layouts of the two expert weights and the sizes they imply.
+static hq_status ffn_layouts(const hq_weight_desc* w13, const hq_weight_desc* w2, hq::Layout* L13, hq::Layout* L2,
+                             int* inter) {
+  using namespace hq;
+  if (!w13 || !w2) return HQ_ERR_INVALID_ARG;
+  hq_status st = make_layout(*w13, L13);
+  if (st != HQ_OK) return st;
+  st = make_layout(*w2, L2);
+  if (st != HQ_OK) return st;
+  if (L13->num_experts != L2->num_experts || L13->n % 2 != 0) return HQ_ERR_INVALID_ARG;
+  *inter = L13->n / 2;
+  if (L2->k != *inter) return HQ_ERR_INVALID_ARG;
+  if (*inter % 8 != 0) return HQ_ERR_ALIGNMENT;
+  return HQ_OK;
+}
+
+hq_status hq_moe_ffn_workspace_size(const hq_weight_desc* w13, const hq_weight_desc* w2, int32_t tokens,
+                                    int32_t topk, size_t* bytes) {
+  if (!bytes || tokens < 0 || topk <= 0) return HQ_ERR_INVALID_ARG;
+  Layout L13, L2;
+  int inter = 0;
+  hq_status st = ffn_layouts(w13, w2, &L13, &L2, &inter);
+  if (st != HQ_OK) return st;
+  const size_t pairs = static_cast<size_t>(tokens) * topk;
+  const size_t ldh = align_up(2 * static_cast<size_t>(inter), 8), lda = align_up(static_cast<size_t>(inter), 8);
+  size_t ws = kAlign;
+  ws += 2 * align_up(sizeof(int) * (L13.num_experts + 1), kAlign);
+  ws += align_up(sizeof(int) * std::max<size_t>(pairs, 1), kAlign);
+  ws += align_up(2 * pairs * ldh, kAlign);             // H: gate and up, bf16
+  ws += align_up(2 * pairs * lda, kAlign);             // A: silu(gate) * up, bf16
+  ws += align_up(sizeof(float) * pairs * L2.n_pad, kAlign);  // weighted down-projection rows
+  *bytes = ws;
+  return HQ_OK;
+}
+
+hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weight_desc* w2, const void* w2_t,
+                     int32_t tokens, int32_t topk, const int32_t* topk_ids, const float* topk_w, int32_t atype,
+                     const void* x, int64_t ldx, void* y, int64_t ldy, void* workspace, size_t ws_bytes,
+                     uint32_t flags, hq_stream_t stream) {
+  (void)flags;
+  if (tokens < 0 || topk <= 0) return HQ_ERR_INVALID_ARG;
+  Layout L13, L2;
+  int inter = 0;
+  hq_status st = ffn_layouts(w13, w2, &L13, &L2, &inter);
+  if (st != HQ_OK) return st;
+  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (L13.num_experts > 1024) return HQ_ERR_UNSUPPORTED;
+  if (tokens == 0) return HQ_OK;
+  if (!w13_t || !w2_t || !topk_ids || !topk_w || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;
+  if (ldx < L13.k || ldy < L2.n) return HQ_ERR_INVALID_ARG;
+  if (atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  for (const Layout* L : {&L13, &L2}) {
+    if (L->wtype == HQ_W_FP8_E4M3) return HQ_ERR_UNSUPPORTED;
+    if ((L->wtype == HQ_W_INT4 || L->wtype == HQ_W_INT6) && !L->channel && L->stype != HQ_S_BF16)
+      return HQ_ERR_UNSUPPORTED;
+  }
+  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(w13_t) & 255u) ||
+      (reinterpret_cast<uintptr_t>(w2_t) & 255u))
+    return HQ_ERR_ALIGNMENT;
+  if ((ldx * 2) % 16 != 0 || (ldy * 2) % 16 != 0 || L13.k % 8 != 0) return HQ_ERR_ALIGNMENT;
+  const int64_t pairs = static_cast<int64_t>(tokens) * topk;
+  if (pairs > (1 << 24)) return HQ_ERR_UNSUPPORTED;
+  size_t need = 0;
+  hq_moe_ffn_workspace_size(w13, w2, tokens, topk, &need);
+  if (ws_bytes < need) return HQ_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  st = device_info(&di);
+  if (st != HQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t ldh = static_cast<int64_t>(align_up(2 * static_cast<size_t>(inter), 8));
+  const int64_t lda = static_cast<int64_t>(align_up(static_cast<size_t>(inter), 8));
+  size_t off = kAlign;
+  int* exp_off = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * (L13.num_experts + 1), kAlign);
+  int* tile_off = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * (L13.num_experts + 1), kAlign);
+  int* perm = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * static_cast<size_t>(pairs), kAlign);
+  void* hbuf = ws + off;
+  off += align_up(2 * static_cast<size_t>(pairs) * ldh, kAlign);
+  void* abuf = ws + off;
+  off += align_up(2 * static_cast<size_t>(pairs) * lda, kAlign);
+  float* zbuf = reinterpret_cast<float*>(ws + off);
+  const int bn = moe_tile_bn(static_cast<double>(pairs) / L13.num_experts);
+  if (launch_moe_route(topk_ids, static_cast<int>(pairs), L13.num_experts, bn, exp_off, tile_off, perm, nullptr,
+                       nullptr, reinterpret_cast<int*>(ws), s) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  int stages = 0, groups = 0;
+  // gate+up: H[f] = X[t] . W13_e^T, written at pair row f
+  st = launch_moe_grouped(L13, static_cast<const uint8_t*>(w13_t), bn, tokens, topk, nullptr, x, ldx, hbuf, ldh,
+                          exp_off, tile_off, perm, nullptr, reinterpret_cast<int*>(ws), true, di, s, &stages, &groups);
+  if (st != HQ_OK) return st;
+  if (launch_moe_act(hbuf, ldh, static_cast<int>(pairs), inter, abuf, lda, s) != cudaSuccess) return HQ_ERR_CUDA;
+  // down: Z[f] = topk_w[f] * A[f] . W2_e^T (rows gathered by pair index)
+  st = launch_moe_grouped(L2, static_cast<const uint8_t*>(w2_t), bn, static_cast<int>(pairs), 1, topk_w, abuf, lda,
+                          y, ldy, exp_off, tile_off, perm, zbuf, reinterpret_cast<int*>(ws), false, di, s, &stages,
+                          &groups);
+  if (st != HQ_OK) return st;
+  if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L2.num_experts, L2.n, L2.n_pad, y, ldy, true, s) !=
+      cudaSuccess)
+    return HQ_ERR_CUDA;
+  g_last_plan = hq_plan_info{bn, 1, di.sms, 5, stages, wna16_class(bn), groups, 0};
   return HQ_OK;
 }
 

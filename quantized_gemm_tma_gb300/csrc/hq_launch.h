@@ -77,6 +77,8 @@ cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, in
 cudaError_t launch_moe_grouped_route(const int* rows_in, bool masked, int rows, int num_experts, int bn,
                                      int* expert_offsets, int* tile_offsets, int* perm, int* status,
                                      cudaStream_t stream);
+cudaError_t launch_moe_act(const void* h, int64_t ldh, int pairs, int inter, void* a, int64_t lda,
+                           cudaStream_t stream);
 cudaError_t launch_moe_combine(const float* zbuf, const int* topk_ids, int tokens, int topk, int num_experts, int n,
                                int n_pad, void* y, int64_t ldy, bool bf16, cudaStream_t stream);
 

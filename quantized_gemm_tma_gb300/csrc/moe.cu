@@ -12,6 +12,8 @@
 //          the routing weight), rounded once to bf16.
 // grouped: the grouped-contiguous and grouped-masked input forms (rows per
 //          expert given by the caller): offsets, tile prefix and row map.
+// act:     silu(gate) * up between the gate+up and down GEMMs of the MoE
+//          feed-forward block.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -198,6 +200,32 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
 }
 
+// MoE feed-forward activation between the two grouped GEMMs:
+//   A[f][i] = silu(H[f][i]) * H[f][inter + i],  silu(g) = g / (1 + e^-g),
+// computed in fp32 from the bf16 gate and up halves and rounded once to bf16.
+// One thread per (pair, 8 consecutive outputs): 16-byte loads and stores.
+__global__ void moe_act_kernel(const __nv_bfloat16* __restrict__ h, int64_t ldh, int pairs, int inter,
+                               __nv_bfloat16* __restrict__ a, int64_t lda) {
+  const int groups = inter / 8;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(pairs) * groups) return;
+  const int64_t f = idx / groups;
+  const int i0 = static_cast<int>(idx % groups) * 8;
+  const uint4 g4 = *reinterpret_cast<const uint4*>(h + f * ldh + i0);
+  const uint4 u4 = *reinterpret_cast<const uint4*>(h + f * ldh + inter + i0);
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g4);
+  const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&u4);
+  uint4 o;
+  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 g = __bfloat1622float2(g2[i]);
+    const float2 u = __bfloat1622float2(u2[i]);
+    o2[i] = __floats2bfloat162_rn(g.x / (1.f + expf(-g.x)) * u.x, g.y / (1.f + expf(-g.y)) * u.y);
+  }
+  *reinterpret_cast<uint4*>(a + f * lda + i0) = o;
+}
+
 // One thread per (token, 8 consecutive outputs).
 __global__ void moe_combine_kernel(const float* __restrict__ z, const int* __restrict__ ids, int tokens, int topk,
                                    int num_experts, int n, int n_pad, __nv_bfloat16* __restrict__ y, int64_t ldy) {
@@ -249,6 +277,16 @@ cudaError_t launch_moe_grouped_route(const int* rows_in, bool masked, int rows, 
   if (num_experts > kRouteThreads) return cudaErrorInvalidValue;
   moe_grouped_route_kernel<<<1, kRouteThreads, 0, stream>>>(rows_in, masked ? 1 : 0, rows, num_experts, bn,
                                                              expert_offsets, tile_offsets, perm, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_act(const void* h, int64_t ldh, int pairs, int inter, void* a, int64_t lda,
+                           cudaStream_t stream) {
+  const int64_t threads = static_cast<int64_t>(pairs) * (inter / 8);
+  if (threads == 0) return cudaSuccess;
+  const int block = 256;
+  moe_act_kernel<<<static_cast<unsigned>((threads + block - 1) / block), block, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(h), ldh, pairs, inter, static_cast<__nv_bfloat16*>(a), lda);
   return cudaGetLastError();
 }
 

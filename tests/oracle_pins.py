@@ -332,4 +332,67 @@ def pin_moe_grouped_forms():
         assert np.array_equal(ym[im], yc[ic]), (im, ic)
 
 
+def pin_silu_values():
+    """silu at points where the sigmoid is a known rational: 0, ln 3 (3/4), -ln 3 (1/4)."""
+    l3 = np.log(3.0)
+    got = oracle.moe.silu(np.array([0.0, l3, -l3, 60.0]))
+    want = np.array([0.0, 0.75 * l3, -0.25 * l3, 60.0])
+    assert np.allclose(got, want, rtol=1e-15, atol=0), (got, want)
+
+
+def pin_moe_ffn_reductions():
+    """A gate of exactly ln 3 makes the block 0.75 ln 3 times the up projection
+    through the down weights; with W2 = I it is 0.75 ln 3 times the MoE GEMM of
+    the up rows (itself pinned), so the gate/up order and the down orientation
+    are both checked; weights enter linearly."""
+    rng = np.random.default_rng(17)
+    e_n, inter, k, t, topk = 3, 4, 6, 5, 2
+    a = rng.integers(-3, 4, size=(t, k)).astype(np.float64)
+    a[:, 0] = 1.0                                      # a constant input column
+    w_up = rng.integers(-2, 3, size=(e_n, inter, k)).astype(np.float64)
+    w_gate = np.zeros((e_n, inter, k))
+    w_gate[:, :, 0] = np.log(3.0)                      # gate = ln 3 for every row
+    w13 = np.concatenate([w_gate, w_up], axis=1)
+    ids = rng.integers(0, e_n, size=(t, topk)).astype(np.int32)
+    tw = (rng.integers(1, 16, size=(t, topk)) / 16.0).astype(np.float32)
+    eye = np.broadcast_to(np.eye(inter), (e_n, inter, inter))
+    y = oracle.moe_ffn(a, ids, tw, w13, eye, intermediate=None)
+    ref = 0.75 * np.log(3.0) * oracle.moe_gemm(a, ids, tw, w_up)
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-13)
+    w2 = rng.integers(-2, 3, size=(e_n, 7, inter)).astype(np.float64)   # non-square down weight
+    y2 = oracle.moe_ffn(a, ids, tw, w13, w2, intermediate=None)
+    for ti in range(t):
+        want = sum(float(tw[ti, j]) * (0.75 * np.log(3.0) * (w_up[ids[ti, j]] @ a[ti])) @ w2[ids[ti, j]].T
+                   for j in range(topk))
+        assert np.allclose(y2[ti], want, rtol=1e-13, atol=1e-13), ti
+    y3 = oracle.moe_ffn(a, ids, 2 * tw, w13, w2, intermediate=None)
+    assert np.allclose(y3, 2 * y2, rtol=1e-14, atol=1e-14)
+
+
+def pin_bf16_rounding():
+    """The oracle's float64 -> bf16 rounding against torch's float32 -> bf16 cast
+    on float32-exact values (halfway cases included), and the intermediate
+    rounding of the feed-forward block is exactly that rounding."""
+    rng = np.random.default_rng(21)
+    v = rng.standard_normal(20000).astype(np.float32).astype(np.float64) * 2.0 ** rng.integers(-20, 20, 20000)
+    # exact halfway points between neighbouring bf16 values: a bf16 pattern
+    # (exponents 100..149, every mantissa) followed by 0x8000 in the low half
+    hi = (np.arange(100, 150, dtype=np.uint32)[:, None] << 7 | np.arange(128, dtype=np.uint32)[None, :]).ravel()
+    bits = hi << 16 | 0x8000
+    v = np.concatenate([v, bits.view(np.float32).astype(np.float64), -bits.view(np.float32).astype(np.float64)])
+    want = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.moe.round_bf16(v), want)
+    rng = np.random.default_rng(22)
+    a = rng.standard_normal((3, 8))
+    w13 = rng.standard_normal((2, 4, 8))
+    w2 = rng.standard_normal((2, 5, 2))
+    ids = np.array([[0], [1], [1]], np.int32)
+    tw = np.ones((3, 1), np.float32)
+    y = oracle.moe_ffn(a, ids, tw, w13, w2)
+    for t in range(3):
+        h = oracle.moe.round_bf16(w13[ids[t, 0]] @ a[t])
+        act = oracle.moe.round_bf16(oracle.moe.silu(h[:2]) * h[2:])
+        assert np.allclose(y[t], w2[ids[t, 0]] @ act, rtol=1e-14, atol=1e-14)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

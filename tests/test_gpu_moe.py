@@ -174,3 +174,52 @@ def test_grouped_invalid_counts_set_status():
     valid = np.array(sorted(ref), dtype=np.int64)
     check(y[valid], np.stack([ref[i] for i in valid]), "valid experts")
     assert np.isnan(y[32:64]).all()
+
+
+# ------------------------------------------------------------------ feed-forward block
+def _expert_fn(qw):
+    """Dequantised expert weights as the MMA operand: a groupwise INT weight
+    with zero points enters as (q - z) * s rounded once to bf16 (the operand
+    rounding both GEMMs of the block apply); MXFP4 values are exact in bf16."""
+    def expert(e):
+        z = None if qw.zeros is None else qw.zeros[e:e + 1]
+        w = oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes[e:e + 1], qw.scales[e:e + 1], z, qw.group_k,
+                              qw.signed, qw.stype, 1)[0]
+        return oracle.moe.round_bf16(w) if qw.zeros is not None else w
+    return expert
+
+
+FFN = [
+    # seed, weight, tokens, experts, intermediate I, hidden K, output n, topk
+    (40, "mxfp4", 37, 8, 128, 256, 256, 4),
+    (41, "int4", 64, 6, 192, 384, 200, 2),     # ragged output n, three gate/up tiles
+]
+
+
+@pytest.mark.parametrize("idx", range(len(FFN)), ids=lambda i: "-".join(map(str, FFN[i][:2])))
+def test_moe_ffn_parity(idx):
+    import torch
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import DevWeight, stream, to_dev, workspace
+    seed, wt, t, e, inter, k, n, topk = FFN[idx]
+    rng = np.random.default_rng(seed)
+    if wt == "mxfp4":
+        w13, acts, r = synth.moe_mxfp4(seed, t, num_experts=e, n=2 * inter, k=k, topk=topk)
+        w2, _, _ = synth.moe_mxfp4(seed + 100, 1, num_experts=e, n=n, k=inter, topk=1)
+    else:
+        w13 = synth.quantize_int_groupwise(rng.standard_normal((e, 2 * inter, k)) * 0.02, 4, 128, False, "bf16")
+        w2 = synth.quantize_int_groupwise(rng.standard_normal((e, n, inter)) * 0.02, 4, 64, False, "bf16")
+        acts = synth.make_activations(rng, t, k, "bf16")
+        r = synth.make_routing(rng, t, e, topk)
+    d13, d2 = DevWeight(w13), DevWeight(w2)
+    ldy = -(-n // 8) * 8
+    y = torch.full((t, ldy), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = workspace(hq.hq_moe_ffn_workspace_size(d13.desc, d2.desc, t, topk))
+    hq.hq_moe_ffn(d13.desc, d13.wt, d2.desc, d2.wt, t, topk, to_dev(np.ascontiguousarray(r.topk_ids, np.int32)),
+                  to_dev(np.ascontiguousarray(r.topk_w, np.float32)), "bf16", to_dev(acts.data), k, y, ldy, ws,
+                  ws.numel(), 0, stream())
+    assert hq.hq_status_read(ws, clear=True, stream=stream()) == 0
+    got = y[:, :n].double().cpu().numpy()
+    ref = oracle.moe_ffn(oracle.decode_activations("bf16", acts.data), r.topk_ids, r.topk_w, _expert_fn(w13),
+                         _expert_fn(w2))
+    check(got, ref, f"moe ffn {FFN[idx]}")

@@ -118,6 +118,27 @@ def _ranges_masked_off_by_one(form, expert_rows, num_experts, rows):
     return [(lo, hi + 1) if form == "masked" and hi > lo else (lo, hi) for lo, hi in r]
 
 
+_orig_silu = MOE.silu
+
+
+def _silu_flipped(g):
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(g))                   # g * sigmoid(-g)
+
+
+_orig_ffn = MOE.moe_ffn
+
+
+def _ffn_gate_up_swapped(a, topk_ids, topk_w, w13, w2, **kw):
+    get13 = w13 if callable(w13) else (lambda e, _w=np.asarray(w13, dtype=np.float64): _w[e])
+
+    def swapped(e):
+        w = np.asarray(get13(e), dtype=np.float64)
+        i = w.shape[0] // 2
+        return np.concatenate([w[i:], w[:i]], axis=0)
+    return _orig_ffn(a, topk_ids, topk_w, swapped, w2, **kw)
+
+
 MUTATIONS = {
     "nibble_order_swapped": [(F, "unpack_nibbles", _swap_nibbles)],
     "int6_big_endian": [(F, "unpack_int6", _int6_big_endian)],
@@ -133,6 +154,8 @@ MUTATIONS = {
     "moe_perm_unstable": [(MOE, "moe_route", _route_unstable), (oracle, "moe_route", _route_unstable)],
     "moe_combine_unweighted": [(MOE, "moe_gemm", _moe_unweighted), (oracle, "moe_gemm", _moe_unweighted)],
     "moe_masked_count_off_by_one": [(MOE, "moe_grouped_ranges", _ranges_masked_off_by_one)],
+    "silu_sign_flipped": [(MOE, "silu", _silu_flipped)],
+    "ffn_gate_up_swapped": [(MOE, "moe_ffn", _ffn_gate_up_swapped), (oracle, "moe_ffn", _ffn_gate_up_swapped)],
 }
 
 
