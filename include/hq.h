@@ -113,7 +113,9 @@ typedef enum {
  * Constraints: INT4/INT6 group_k in {0, 32, 64, 128} or a multiple of 128,
  * dividing K; INT6 needs K % 4 == 0; MXFP4 group_k = 32 (K % 32 == 0) and
  * stype UE8M0; FP8 group_k = group_n = 128 and stype FP32; INT stype BF16 or
- * FP16.  The codes/scales/zeros pointers are read by hq_transform only; the
+ * FP16.  N and K at most 2^28 (HQ_ERR_UNSUPPORTED above, so that tile counts
+ * and in-tile offsets fit 32-bit integers).
+ * The codes/scales/zeros pointers are read by hq_transform only; the
  * GEMM calls use the shape fields and ignore the pointers.
  */
 typedef struct {
@@ -195,7 +197,8 @@ hq_status hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);
  *
  * wdesc     shape of the weight (pointers ignored); num_experts must be 1
  * w_t       hq_transform output for wdesc
- * m         rows of X and Y (0 is a no-op)
+ * m         rows of X and Y (0 is a no-op); at most 2^30, with
+ *           (m/16 + 1) * ceil(n/128) below 2^31 (HQ_ERR_UNSUPPORTED beyond)
  * atype     hq_atype; INT with group scales needs stype == atype; MXFP4 needs
  *           BF16; FP8 weights need FP8 activations
  * x, ldx    X [m][k] row-major, row stride ldx elements (ldx >= k; the row
@@ -273,6 +276,8 @@ hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int3
  * tokens, topk T and top-k; topk_ids int32 [T][topk], topk_w float32 [T][topk]
  * x, ldx       activations [T][k]; y, ldy output [T][n] (bf16 for BF16 acts)
  * expert_offsets_out  optional int32 [E+1]; perm_out optional int32 [T*topk]
+ * Limits (HQ_ERR_UNSUPPORTED beyond): E <= 1024, T*topk <= 2^24 and
+ * (T*topk/16 + E + 1) * ceil(n/128) below 2^31.
  * An expert id outside [0, E) makes its pair contribute nothing and sets
  * HQ_ERR_INVALID_VALUE in the workspace status word.
  */
@@ -304,7 +309,8 @@ hq_status hq_moe_ffn_workspace_size(const hq_weight_desc* w13, const hq_weight_d
  * w13, w13_t   gate+up experts [E][2I][k] and their transform (I % 8 == 0)
  * w2, w2_t     down experts [E][n][I] and their transform (same E)
  * other arguments as hq_moe_gemm (bf16 activations; x [T][k], y [T][n]).
- * Invalid expert ids: as hq_moe_gemm.  Asynchronous.
+ * Invalid expert ids and limits: as hq_moe_gemm (the tile bound with the
+ * larger of 2I and n).  Asynchronous.
  */
 hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weight_desc* w2, const void* w2_t,
                      int32_t tokens, int32_t topk, const int32_t* topk_ids, const float* topk_w, int32_t atype,
@@ -339,6 +345,8 @@ hq_status hq_moe_grouped_workspace_size(const hq_weight_desc* desc, int32_t form
  * expected_rows  rows per expert the caller expects (picks the tile width;
  *              the counts stay on the device); <= 0: derived from `rows`
  * x, ldx       activations (bf16); y, ldy output (bf16), 16-byte aligned rows
+ * Limits (HQ_ERR_UNSUPPORTED beyond): E <= 1024, at most 2^24 rows of X (E*rows
+ *              when masked), and (those rows/16 + E + 1) * ceil(n/128) below 2^31.
  * Rows outside every expert's range are neither read nor written.  Invalid
  * offsets or counts make that expert contribute nothing and set
  * HQ_ERR_INVALID_VALUE in the workspace status word.  Asynchronous.

@@ -21,6 +21,7 @@ namespace hq {
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kMaxDim = 1 << 28;  // largest N and K (tile counts and offsets stay in 32 bits)
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -138,6 +139,13 @@ hq_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tiles are counted in 32-bit integers on the device.  `rows` rows in at most
+// `groups` separately tiled runs (experts) need at most rows / 16 + groups + 1
+// tiles of the narrowest width (16 tokens) per column of output tiles.
+bool tiles_fit(int64_t rows, int64_t groups, int n_tiles) {
+  return (rows / 16 + groups + 1) * static_cast<int64_t>(n_tiles) <= INT32_MAX;
+}
+
 // Tuning and trace switches from the environment, read once per process.
 struct EnvKnobs {
   int force_bn = 0, force_splitk = 0, force_issuers = 0, trace = 0;
@@ -172,6 +180,7 @@ int env_int(const char* name, int dflt) {
 // ------------------------------------------------------------------ layout
 hq_status make_layout(const hq_weight_desc& d, Layout* L) {
   if (d.n <= 0 || d.k <= 0 || d.num_experts <= 0) return HQ_ERR_INVALID_ARG;
+  if (d.n > kMaxDim || d.k > kMaxDim) return HQ_ERR_UNSUPPORTED;
   if (d.wtype < HQ_W_INT4 || d.wtype > HQ_W_FP8_E4M3) return HQ_ERR_INVALID_ARG;
   if (d.stype < HQ_S_BF16 || d.stype > HQ_S_UE8M0) return HQ_ERR_INVALID_ARG;
   std::memset(L, 0, sizeof(*L));
@@ -525,6 +534,7 @@ hq_status hq_gemm_workspace_size(const hq_weight_desc* desc, int32_t m, int32_t 
   Layout L;
   hq_status st = make_layout(*desc, &L);
   if (st != HQ_OK) return st;
+  if (m > (1 << 30) || !tiles_fit(m, 0, L.n_tiles)) return HQ_ERR_UNSUPPORTED;
   size_t ws = kAlign;  // status word
   if (m > 0) {
     // split-K scratch of the largest plan any sm_103 device would choose
@@ -554,6 +564,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   if (L.num_experts != 1) return HQ_ERR_INVALID_ARG;
   if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
   if (m == 0) return HQ_OK;
+  if (m > (1 << 30) || !tiles_fit(m, 0, L.n_tiles)) return HQ_ERR_UNSUPPORTED;
   if (!w_t || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;
   if (ldx < L.k || ldy < L.n) return HQ_ERR_INVALID_ARG;
   const bool fp8 = L.wtype == HQ_W_FP8_E4M3;
@@ -693,7 +704,7 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
     return HQ_ERR_ALIGNMENT;
   if ((ldx * 2) % 16 != 0 || (ldy * 2) % 16 != 0 || L.k % 8 != 0) return HQ_ERR_ALIGNMENT;
   const int64_t pairs = static_cast<int64_t>(tokens) * topk;
-  if (pairs > (1 << 24)) return HQ_ERR_UNSUPPORTED;
+  if (pairs > (1 << 24) || !tiles_fit(pairs, L.num_experts, L.n_tiles)) return HQ_ERR_UNSUPPORTED;
   size_t need = 0;
   hq_moe_workspace_size(wdesc, tokens, topk, atype, &need);
   if (ws_bytes < need) return HQ_ERR_WORKSPACE_TOO_SMALL;
@@ -787,7 +798,8 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
     return HQ_ERR_ALIGNMENT;
   if ((ldx * 2) % 16 != 0 || (ldy * 2) % 16 != 0 || L13.k % 8 != 0) return HQ_ERR_ALIGNMENT;
   const int64_t pairs = static_cast<int64_t>(tokens) * topk;
-  if (pairs > (1 << 24)) return HQ_ERR_UNSUPPORTED;
+  if (pairs > (1 << 24) || !tiles_fit(pairs, L13.num_experts, std::max(L13.n_tiles, L2.n_tiles)))
+    return HQ_ERR_UNSUPPORTED;
   size_t need = 0;
   hq_moe_ffn_workspace_size(w13, w2, tokens, topk, &need);
   if (ws_bytes < need) return HQ_ERR_WORKSPACE_TOO_SMALL;
@@ -869,7 +881,7 @@ hq_status hq_moe_grouped_gemm(const hq_weight_desc* wdesc, const void* w_t, int3
   if ((ldx * 2) % 16 != 0 || (ldy * 2) % 16 != 0 || L.k % 8 != 0) return HQ_ERR_ALIGNMENT;
   const bool masked = form == HQ_MOE_GROUPED_MASKED;
   const int64_t x_rows = masked ? static_cast<int64_t>(rows) * L.num_experts : rows;
-  if (x_rows > (1 << 24)) return HQ_ERR_UNSUPPORTED;
+  if (x_rows > (1 << 24) || !tiles_fit(x_rows, L.num_experts, L.n_tiles)) return HQ_ERR_UNSUPPORTED;
   size_t need = 0;
   hq_moe_grouped_workspace_size(wdesc, form, rows, &need);
   if (ws_bytes < need) return HQ_ERR_WORKSPACE_TOO_SMALL;

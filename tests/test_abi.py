@@ -142,3 +142,33 @@ def test_workspace_sizes_bounded(hq):
     # large M needs no split-K scratch; small M needs at most 64 splits of fp32 partials
     assert big < 64 << 20
     assert small <= 256 + 64 * 16 * 8192 * 4 + (1 << 20)
+
+
+def test_size_limits_rejected_on_host(hq):
+    """Shapes whose tile counts or offsets would leave 32-bit range are
+    refused before any launch (and before any device query)."""
+    fake = 0x10000
+    for kw in (dict(n=(1 << 28) + 128), dict(k=(1 << 28) + 128)):
+        with pytest.raises(hq.HQError) as ei:
+            hq.hq_transform_size(_desc(hq, **kw))
+        assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
+    hq.hq_transform_size(_desc(hq, n=1 << 20, k=1 << 20))  # large but within the limits
+    # dense: M above 2^30, or (M/16 + 1) * n_tiles at 2^31
+    d = _desc(hq, n=1 << 20)  # 8192 n-tiles
+    for m in ((1 << 30) + 1, (1 << 22) * 16):
+        with pytest.raises(hq.HQError) as ei:
+            hq.hq_gemm_workspace_size(d, m, "bf16")
+        assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
+        with pytest.raises(hq.HQError) as ei:
+            hq.hq_gemm(d, fake, m, "bf16", fake, 512, None, fake, 1 << 20, fake, 1 << 20, 0, None)
+        assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
+    # MoE: 2^24 pairs over 8192 n-tiles overflow the device tile counter
+    dm = hq.make_desc("mxfp4", "ue8m0", 1 << 20, 2048, num_experts=8, group_k=32)
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_moe_gemm(dm, fake, 1 << 21, 8, fake, fake, "bf16", fake, 2048, fake, 1 << 20, None, None, fake,
+                       1 << 62)
+    assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_moe_grouped_gemm(dm, fake, hq.HQ_MOE_GROUPED_MASKED, 1 << 21, fake, 0, "bf16", fake, 2048, fake,
+                               1 << 20, fake, 1 << 62)
+    assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
