@@ -139,6 +139,23 @@ def _ffn_gate_up_swapped(a, topk_ids, topk_w, w13, w2, **kw):
     return _orig_ffn(a, topk_ids, topk_w, swapped, w2, **kw)
 
 
+def _bf16_truncate(x):
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.trunc(m * 256.0) / 256.0, e)   # toward zero instead of to nearest
+
+
+def _bf16_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.sign(m) * np.floor(np.abs(m) * 256.0 + 0.5) / 256.0, e)   # halfway cases away from zero
+
+
+def _ffn_unrounded(a, topk_ids, topk_w, w13, w2, **kw):
+    kw["intermediate"] = None                          # H and A kept exact between the GEMMs
+    return _orig_ffn(a, topk_ids, topk_w, w13, w2, **kw)
+
+
 MUTATIONS = {
     "nibble_order_swapped": [(F, "unpack_nibbles", _swap_nibbles)],
     "int6_big_endian": [(F, "unpack_int6", _int6_big_endian)],
@@ -156,6 +173,9 @@ MUTATIONS = {
     "moe_masked_count_off_by_one": [(MOE, "moe_grouped_ranges", _ranges_masked_off_by_one)],
     "silu_sign_flipped": [(MOE, "silu", _silu_flipped)],
     "ffn_gate_up_swapped": [(MOE, "moe_ffn", _ffn_gate_up_swapped), (oracle, "moe_ffn", _ffn_gate_up_swapped)],
+    "bf16_round_truncates": [(MOE, "round_bf16", _bf16_truncate)],
+    "bf16_round_ties_away": [(MOE, "round_bf16", _bf16_ties_away)],
+    "ffn_intermediates_unrounded": [(MOE, "moe_ffn", _ffn_unrounded), (oracle, "moe_ffn", _ffn_unrounded)],
 }
 
 
