@@ -148,7 +148,7 @@ bool tiles_fit(int64_t rows, int64_t groups, int n_tiles) {
 
 // Tuning and trace switches from the environment, read once per process.
 struct EnvKnobs {
-  int force_bn = 0, force_splitk = 0, force_issuers = 0, trace = 0;
+  int force_bn = 0, force_splitk = 0, trace = 0;
 };
 const EnvKnobs& env() {
   static const EnvKnobs k = [] {
@@ -159,7 +159,6 @@ const EnvKnobs& env() {
     };
     e.force_bn = get("HQ_FORCE_BN");
     e.force_splitk = get("HQ_FORCE_SPLITK");
-    e.force_issuers = get("HQ_FORCE_ISSUERS");
     e.trace = get("HQ_TRACE");
     return e;
   }();
@@ -170,7 +169,6 @@ int env_int(const char* name, int dflt) {
   int v = 0;
   if (!std::strcmp(name, "HQ_FORCE_BN")) v = env().force_bn;
   else if (!std::strcmp(name, "HQ_FORCE_SPLITK")) v = env().force_splitk;
-  else if (!std::strcmp(name, "HQ_FORCE_ISSUERS")) v = env().force_issuers;
   else if (!std::strcmp(name, "HQ_TRACE")) v = env().trace;
   return v ? v : dflt;
 }
