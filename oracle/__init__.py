@@ -18,7 +18,8 @@ it; the product path never calls it.
 Modules:
     formats  decoders of the storage formats (int4, int6, e2m1, UE8M0, e4m3,
              bf16, fp16), each from its bit-field definition
-    gemm     dequantisation and the dense GEMM
+    gemm     dequantisation (int4, int6, mxfp4, fp8 blocks, nvfp4, mxint4)
+             and the dense GEMM
     moe      routing (count, prefix sum, stable permutation) and the MoE
              grouped GEMM with the routing-weighted combine; the grouped
              (contiguous / masked) input forms; the feed-forward block

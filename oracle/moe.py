@@ -75,10 +75,12 @@ def moe_reference(qw, acts, routing) -> np.ndarray:
     """Convenience wrapper over ``synth`` containers."""
     from .gemm import dequantize, decode_activations
 
+    ts = getattr(qw, "tensor_scale", None)
+
     def expert(e):
         z = None if qw.zeros is None else qw.zeros[e:e + 1]
         return dequantize(qw.wtype, qw.n, qw.k, qw.codes[e:e + 1], qw.scales[e:e + 1], z,
-                          qw.group_k, qw.signed, qw.stype, 1)[0]
+                          qw.group_k, qw.signed, qw.stype, 1, None if ts is None else ts[e:e + 1])[0]
     return moe_gemm(decode_activations(acts.atype, acts.data, acts.scales),
                     routing.topk_ids, routing.topk_w, expert)
 

@@ -24,6 +24,9 @@ MoE).  All arrays are C-contiguous numpy arrays with a leading expert axis E
 * mxfp4  codes  uint8 [E, N, ceil(K/2)], nibbles as int4, each nibble an OCP
                 e2m1 value (bit 3 sign, bits 2..1 exponent, bit 0 mantissa).
 * fp8    codes  uint8 [E, N, K], OCP e4m3 ("fn" variant) bytes.
+* nvfp4  codes  as mxfp4; scales e4m3 bytes uint8 [E, N, K/16]; plus a
+                float32 tensor scale per expert, tensor_scale [E].
+* mxint4 codes  as symmetric int4; scales UE8M0 bytes uint8 [E, N, K/32].
 * scales        int formats: bf16/fp16 bit patterns uint16 [E, N, G] with
                 G = K/group_k groups (G = 1 for channelwise, group_k = 0);
                 mxfp4: UE8M0 exponent bytes uint8 [E, N, K/32];
@@ -47,7 +50,7 @@ __all__ = [
     "QuantWeight", "Activations", "MoeRouting",
     "to_bf16_bits", "to_fp16_bits", "to_e4m3_bytes",
     "pack_nibbles", "pack_int6",
-    "quantize_int_groupwise", "quantize_fp8_block", "quantize_mxfp4",
+    "quantize_int_groupwise", "quantize_fp8_block", "quantize_mxfp4", "quantize_nvfp4", "quantize_mxint4",
     "quantize_fp8_acts", "make_activations", "make_routing",
     "dense_w4a16_sym", "dense_w4a16_asym", "dense_int6_channel",
     "dense_fp8_block", "moe_mxfp4", "random_codes_weight",
@@ -60,17 +63,18 @@ __all__ = [
 @dataclass
 class QuantWeight:
     """One quantized weight in the standard storage format (see module doc)."""
-    wtype: str                 # "int4" | "int6" | "mxfp4" | "fp8"
+    wtype: str                 # "int4" | "int6" | "mxfp4" | "fp8" | "nvfp4" | "mxint4"
     n: int
     k: int
     num_experts: int
     group_k: int               # 0 = channelwise
     group_n: int               # 1, or 128 for fp8 block scales
-    stype: str                 # "bf16" | "fp16" | "ue8m0" | "fp32"
+    stype: str                 # "bf16" | "fp16" | "ue8m0" | "fp32" | "e4m3"
     signed: bool               # int formats: symmetric two's complement codes
     codes: np.ndarray
     scales: np.ndarray
     zeros: Optional[np.ndarray] = None
+    tensor_scale: Optional[np.ndarray] = None   # nvfp4: float32 [E]
 
     @property
     def has_zeros(self) -> bool:
@@ -273,6 +277,52 @@ def quantize_mxfp4(w: np.ndarray) -> QuantWeight:
                        scales=big.astype(np.uint8).reshape(e, n, k // 32))
 
 
+def quantize_nvfp4(w: np.ndarray) -> QuantWeight:
+    """w [E, N, K] -> e2m1 codes, one e4m3 scale per 16 values along K and one
+    float32 tensor scale per expert.
+
+    g = float32(absmax of the expert / (6 * 448)), so that every block scale
+    fits e4m3; block scale s = e4m3(absmax_16 / 6 / g) (round to nearest even,
+    saturating); elements are rounded to e2m1 after division by the stored
+    s * g, saturating at 6.  A block whose scale rounds to zero stores 1.0; an
+    all-zero expert g = 1.
+    """
+    w = np.asarray(w, dtype=np.float64)
+    e, n, k = w.shape
+    assert k % 16 == 0
+    amax_e = np.abs(w.reshape(e, -1)).max(axis=1)
+    g = np.where(amax_e > 0, amax_e / (6.0 * 448.0), 1.0).astype(np.float32)
+    gd = g.astype(np.float64)[:, None, None]
+    wg = w.reshape(e, n, k // 16, 16)
+    sb = to_e4m3_bytes(np.abs(wg).max(axis=-1) / 6.0 / gd)
+    sb = np.where(_e4m3_bytes_to_f64(sb) > 0, sb, np.uint8(0x38)).astype(np.uint8)   # 0x38 = 1.0
+    div = _e4m3_bytes_to_f64(sb)[..., None] * gd[..., None]
+    u = _e2m1_encode(wg / div).reshape(e, n, k)
+    return QuantWeight(wtype="nvfp4", n=n, k=k, num_experts=e, group_k=16, group_n=1, stype="e4m3",
+                       signed=True, codes=pack_nibbles(u), scales=sb.reshape(e, n, k // 16), tensor_scale=g)
+
+
+def quantize_mxint4(w: np.ndarray) -> QuantWeight:
+    """w [E, N, K] -> 4-bit two's complement codes with one UE8M0 scale per 32
+    values along K.
+
+    Shared exponent per block = floor(log2(absmax)) - 2, so absmax / 2^(E-127)
+    lies in [4, 8); biased by 127 and clamped to [0, 254]; q = clamp(rne(w /
+    2^(E-127)), -8, 7).  A zero block takes E = 127.
+    """
+    w = np.asarray(w, dtype=np.float64)
+    e, n, k = w.shape
+    assert k % 32 == 0
+    wg = w.reshape(e, n, k // 32, 32)
+    amax = np.abs(wg).max(axis=-1)
+    _, ex = np.frexp(amax)
+    big = np.where(amax > 0, np.clip(ex - 1 - 2 + 127, 0, 254), 127).astype(np.int64)
+    q = np.clip(_rne(np.ldexp(wg, (127 - big)[..., None].astype(np.int32))), -8, 7).astype(np.int64)
+    return QuantWeight(wtype="mxint4", n=n, k=k, num_experts=e, group_k=32, group_n=1, stype="ue8m0",
+                       signed=True, codes=pack_nibbles((q & 0xF).reshape(e, n, k)),
+                       scales=big.astype(np.uint8).reshape(e, n, k // 32))
+
+
 def quantize_fp8_acts(x: np.ndarray) -> Activations:
     """x [M, K] -> e4m3 bytes with float32 per-token per-128-K-group scales."""
     x = np.asarray(x, dtype=np.float64)
@@ -399,6 +449,17 @@ def random_codes_weight(seed: int, wtype: str, n: int, k: int, num_experts: int 
         u = rng.integers(0, 16, size=(e, n, k))
         sc = rng.integers(118, 124, size=(e, n, k // 32)).astype(np.uint8)
         return QuantWeight("mxfp4", n, k, e, 32, 1, "ue8m0", True, pack_nibbles(u), sc)
+    if wtype == "mxint4":
+        u = rng.integers(0, 16, size=(e, n, k))
+        sc = rng.integers(118, 124, size=(e, n, k // 32)).astype(np.uint8)
+        return QuantWeight("mxint4", n, k, e, 32, 1, "ue8m0", True, pack_nibbles(u), sc)
+    if wtype == "nvfp4":
+        u = rng.integers(0, 16, size=(e, n, k))
+        # positive e4m3 scales with exponent fields 4..9 (2^-3 .. 2^2), every mantissa
+        sc = ((rng.integers(4, 10, size=(e, n, k // 16)) << 3) | rng.integers(0, 8, size=(e, n, k // 16)))
+        ts = np.exp2(rng.uniform(-8, -4, size=e)).astype(np.float32)
+        return QuantWeight("nvfp4", n, k, e, 16, 1, "e4m3", True, pack_nibbles(u), sc.astype(np.uint8),
+                           tensor_scale=ts)
     if wtype == "fp8":
         b = rng.integers(0, 256, size=(e, n, k)).astype(np.uint8)
         b[(b & 0x7F) == 0x7F] = 0x00        # no NaN codes

@@ -133,7 +133,7 @@ def _case_inputs(c):
     codes = np.array(c["codes"], np.uint8)[None]
     if c["wtype"] == "fp8":
         scales = np.array(c["scales"], np.float32)[None]
-    elif c["wtype"] == "mxfp4":
+    elif c["wtype"] in ("mxfp4", "nvfp4", "mxint4"):
         scales = np.array(c["scales"], np.uint8)[None]
     else:
         scales = np.array(c["scales_bits"], np.uint16)[None]
@@ -144,8 +144,9 @@ def _case_inputs(c):
 def pin_hand_gemm_cases():
     for c in _hand_cases():
         xd, xs, codes, scales, zeros = _case_inputs(c)
+        ts = np.array(c["tensor_scale"], np.float32) if "tensor_scale" in c else None
         w = oracle.dequantize(c["wtype"], c["n"], c["k"], codes, scales, zeros, c["group_k"],
-                              c["signed"], c["stype"], 1)
+                              c["signed"], c["stype"], 1, ts)
         a = oracle.decode_activations(c["atype"], xd, xs)
         nz = len(c["x_values"][0])
         assert np.array_equal(a[:, :nz], np.array(c["x_values"], np.float64)), c["name"]
@@ -191,7 +192,7 @@ def pin_integer_invariant():
 
 def _scalar_code(wtype, row_bytes, kk):
     """Independent per-element unpacking (bit arithmetic on one Python int)."""
-    if wtype in ("int4", "mxfp4"):
+    if wtype in ("int4", "mxfp4", "nvfp4", "mxint4"):
         return (int(row_bytes[kk // 2]) >> (4 * (kk % 2))) & 0xF
     stream = int.from_bytes(bytes(int(b) for b in row_bytes), "little")
     return (stream >> (6 * kk)) & 0x3F
@@ -205,14 +206,17 @@ def _frac_bf16(u):
 def pin_rational_bruteforce():
     """Tiny random problems: oracle vs exact rational arithmetic in Python loops."""
     e2m1_tab = {int(c): Fraction(v) for c, v in _load_table("e2m1_ocp_mx_v1.txt")}
+    e4 = lambda b: Fraction(float(torch.tensor([int(b)], dtype=torch.uint8)
+                                  .view(torch.float8_e4m3fn).double().item()))
     for seed, wtype, zeros, group in ((1, "int4", False, 32), (2, "int4", True, 32), (3, "int6", True, 64),
-                                      (4, "int6", False, 0), (5, "mxfp4", False, 32)):
+                                      (4, "int6", False, 0), (5, "mxfp4", False, 32), (6, "nvfp4", False, 16),
+                                      (7, "mxint4", False, 32)):
         m, n, k = 2, 3, 64
         qw = synth.random_codes_weight(seed, wtype, n, k, group_k=group, has_zeros=zeros)
         x = synth.make_activations(np.random.default_rng(seed), m, k, "bf16")
         y = oracle.gemm_dense(oracle.decode_activations("bf16", x.data),
                               oracle.dequantize(qw.wtype, n, k, qw.codes, qw.scales, qw.zeros, qw.group_k,
-                                                qw.signed, qw.stype, 1))
+                                                qw.signed, qw.stype, 1, qw.tensor_scale))
         bits = 6 if wtype == "int6" else 4
         for i in range(m):
             for j in range(n):
@@ -221,6 +225,10 @@ def pin_rational_bruteforce():
                     c = _scalar_code(wtype, qw.codes[0, j], kk)
                     if wtype == "mxfp4":
                         wv = e2m1_tab[c] * Fraction(2) ** (int(qw.scales[0, j, kk // 32]) - 127)
+                    elif wtype == "nvfp4":
+                        wv = e2m1_tab[c] * e4(qw.scales[0, j, kk // 16]) * Fraction(float(qw.tensor_scale[0]))
+                    elif wtype == "mxint4":
+                        wv = (c - 16 if c >= 8 else c) * Fraction(2) ** (int(qw.scales[0, j, kk // 32]) - 127)
                     else:
                         gi = 0 if group == 0 else kk // group
                         s = _frac_bf16(qw.scales[0, j, gi])
@@ -273,6 +281,22 @@ def pin_quant_roundtrip():
     again = synth.quantize_mxfp4(w)
     assert np.array_equal(again.scales, e)
     assert np.array_equal(oracle.dequantize("mxfp4", 1, 32, again.codes, again.scales, None, 32, True, "ue8m0", 1), w)
+    # nvfp4: every block holds a magnitude 6 and the largest block scale is
+    # 448, so the tensor scale and every block scale are recovered
+    codes = np.array([[list(range(16)) * 2]], np.int64)
+    sb = np.array([[[0x7E, 0x38]]], np.uint8)          # 448, 1.0
+    g = np.array([2.0 ** -10], np.float32)
+    w = oracle.dequantize("nvfp4", 1, 32, synth.pack_nibbles(codes), sb, None, 16, True, "e4m3", 1, g)
+    again = synth.quantize_nvfp4(w)
+    assert np.array_equal(again.tensor_scale, g) and np.array_equal(again.scales, sb)
+    assert np.array_equal(oracle.dequantize("nvfp4", 1, 32, again.codes, again.scales, None, 16, True, "e4m3", 1,
+                                            again.tensor_scale), w)
+    # mxint4: the block's largest magnitude is 7 (in [4, 8)), so E is recovered
+    q = np.array([[[7, -3, 0, 1, -7, 2, 5, -1] * 4]], np.int64)
+    e = np.array([[[121]]], np.uint8)
+    w = oracle.dequantize("mxint4", 1, 32, synth.pack_nibbles(q & 0xF), e, None, 32, True, "ue8m0", 1)
+    again = synth.quantize_mxint4(w)
+    assert np.array_equal(again.scales, e) and np.array_equal(again.codes, synth.pack_nibbles(q & 0xF))
 
 
 def pin_moe_route_properties():

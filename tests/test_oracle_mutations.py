@@ -65,16 +65,38 @@ _orig_dequant = G.dequantize
 
 
 def _zero_after_scale(wtype, n, k, codes, scales, zeros=None, group_k=128, signed=True, stype="bf16",
-                      num_experts=1):
+                      num_experts=1, tensor_scale=None):
     # w = q*s - z instead of (q - z)*s
     if zeros is None or wtype not in ("int4", "int6"):
-        return _orig_dequant(wtype, n, k, codes, scales, zeros, group_k, signed, stype, num_experts)
+        return _orig_dequant(wtype, n, k, codes, scales, zeros, group_k, signed, stype, num_experts, tensor_scale)
     w_nz = _orig_dequant(wtype, n, k, codes, scales, None, group_k, False, stype, num_experts)
     bits = 4 if wtype == "int4" else 6
     unpack = F.unpack_nibbles if bits == 4 else F.unpack_int6
     g = 1 if group_k == 0 else k // group_k
     z = unpack(np.asarray(zeros).reshape(num_experts, n, -1), g)[:, :, G._group_index(k, group_k)]
     return w_nz - z
+
+
+def _nvfp4_variant(group, use_g):
+    def dq(wtype, n, k, codes, scales, zeros=None, group_k=128, signed=True, stype="bf16", num_experts=1,
+           tensor_scale=None):
+        if wtype != "nvfp4":
+            return _orig_dequant(wtype, n, k, codes, scales, zeros, group_k, signed, stype, num_experts, tensor_scale)
+        e = num_experts
+        u = F.unpack_nibbles(np.asarray(codes).reshape(e, n, -1), k)
+        sc = F.e4m3_to_f64(np.asarray(scales).reshape(e, n, k // 16))[:, :, np.arange(k) // group]
+        g = np.asarray(tensor_scale, np.float32).astype(np.float64).reshape(e, 1, 1) if use_g else 1.0
+        return F.e2m1_to_f64(u) * sc * g
+    return dq
+
+
+def _mxint4_unsigned(wtype, n, k, codes, scales, zeros=None, group_k=128, signed=True, stype="bf16",
+                     num_experts=1, tensor_scale=None):
+    if wtype != "mxint4":
+        return _orig_dequant(wtype, n, k, codes, scales, zeros, group_k, signed, stype, num_experts, tensor_scale)
+    u = F.unpack_nibbles(np.asarray(codes).reshape(num_experts, n, -1), k)     # codes left unsigned
+    sc = F.ue8m0_to_f64(np.asarray(scales).reshape(num_experts, n, k // 32))[:, :, np.arange(k) // 32]
+    return u * sc
 
 
 def _gemm_transposed_weight(a, w):
@@ -173,6 +195,11 @@ MUTATIONS = {
     "moe_masked_count_off_by_one": [(MOE, "moe_grouped_ranges", _ranges_masked_off_by_one)],
     "silu_sign_flipped": [(MOE, "silu", _silu_flipped)],
     "ffn_gate_up_swapped": [(MOE, "moe_ffn", _ffn_gate_up_swapped), (oracle, "moe_ffn", _ffn_gate_up_swapped)],
+    "nvfp4_scale_per_32": [(G, "dequantize", _nvfp4_variant(32, True)),
+                           (oracle, "dequantize", _nvfp4_variant(32, True))],
+    "nvfp4_tensor_scale_dropped": [(G, "dequantize", _nvfp4_variant(16, False)),
+                                   (oracle, "dequantize", _nvfp4_variant(16, False))],
+    "mxint4_codes_unsigned": [(G, "dequantize", _mxint4_unsigned), (oracle, "dequantize", _mxint4_unsigned)],
     "bf16_round_truncates": [(MOE, "round_bf16", _bf16_truncate)],
     "bf16_round_ties_away": [(MOE, "round_bf16", _bf16_ties_away)],
     "ffn_intermediates_unrounded": [(MOE, "moe_ffn", _ffn_unrounded), (oracle, "moe_ffn", _ffn_unrounded)],
