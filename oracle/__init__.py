@@ -24,12 +24,14 @@ Modules:
              grouped GEMM with the routing-weighted combine; the grouped
              (contiguous / masked) input forms; the feed-forward block
              (gate+up, SiLU-gated product, down, combine)
+    w4a8     MXFP8 quantisation of the activations (OCP MX conversion,
+             e4m3 elements) and the W4A8-MXFP4 product
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against values fixed outside the oracle (library casts, published format
 tables, hand-worked cases, exact integer and rational arithmetic, invariants);
 none is "parity unpinned".
 """
-from . import formats, gemm, moe  # noqa: F401
+from . import formats, gemm, moe, w4a8  # noqa: F401
 from .gemm import dequantize, gemm_dense, decode_activations  # noqa: F401
 from .moe import moe_route, moe_gemm, moe_grouped_gemm, moe_ffn  # noqa: F401

@@ -419,4 +419,98 @@ def pin_bf16_rounding():
         assert np.allclose(y[t], w2[ids[t, 0]] @ act, rtol=1e-14, atol=1e-14)
 
 
+# ---------------------------------------------------------------------------
+# W4A8-MXFP4: MXFP8 activation quantisation and the block-scaled product
+# ---------------------------------------------------------------------------
+def _torch_e4m3_sat(v):
+    """torch's round-to-nearest-even cast, after clamping to +-448 (torch does
+    not saturate)."""
+    v = np.clip(np.asarray(v, np.float64), -448.0, 448.0).astype(np.float32)
+    return torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_encoder():
+    """The oracle's e4m3 encoder against torch's cast: every finite value, every
+    midpoint between neighbours (ties to even), random values; saturation,
+    signed zero and the subnormal boundary by hand."""
+    enc = oracle.w4a8.e4m3_encode
+    vals = np.unique(np.abs(torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()))
+    vals = vals[np.isfinite(vals)]                            # 0 .. 448, 127 magnitudes
+    mids = (vals[1:] + vals[:-1]) / 2
+    rng = np.random.default_rng(31)
+    rnd = rng.uniform(-448, 448, 5000) * 2.0 ** rng.integers(-14, 1, 5000)
+    for v in (vals, -vals[1:], mids, -mids, rnd):
+        assert np.array_equal(enc(v), _torch_e4m3_sat(v))
+    # 448 is S.1111.110; anything larger saturates to it (0x7E / 0xFE)
+    assert enc(np.array([448.0, 448.5, 464.0, 480.0, 1e9, -500.0])).tolist() == [0x7E] * 5 + [0xFE]
+    # -0 keeps its sign; 2^-10 is the tie between 0 and 2^-9 (even: 0); just above rounds up
+    assert enc(np.array([-0.0, 2.0 ** -10, 2.0 ** -10 * 1.0001, 2.0 ** -9])).tolist() == [0x80, 0x00, 0x01, 0x01]
+
+
+def pin_mx_shared_exponent():
+    """floor(log2 amax) - 8 + 127 on hand-picked block maxima, clamped to [0, 254]."""
+    amax = np.array([448.0, 480.0, 511.9, 512.0, 1.0, 0.75, 3.0, 0.0, 2.0 ** -140, 2.0 ** 130, 2.0 ** 200])
+    want = [127, 127, 127, 128, 119, 118, 120, 0, 0, 249, 254]
+    assert oracle.w4a8.mx_shared_exponent(amax, 8).tolist() == want
+
+
+def pin_mxfp8_hand_block():
+    """One block of 32 worked by hand.  amax = 3 gives E = 1 - 8 + 127 = 120
+    (scale 2^-7), so each element is x * 128 rounded on the e4m3 grid:
+      1.0        -> 128 = 1.0 * 2^7       -> exp 14, mant 0 -> 0x70
+      -3.0       -> -384 = -1.5 * 2^8     -> 0x80 | 15 << 3 | 4 = 0xFC
+      13/128     -> 13 = 1.625 * 2^3      -> 10 << 3 | 5 = 0x55
+      12.5/128   -> 12.5, tie between 12 and 13 on the unit grid -> 12 (even)
+                    = 1.5 * 2^3           -> 0x54
+      2^-16      -> 2^-9, the smallest subnormal -> 0x01
+      2^-17      -> 2^-10, tie between 0 and 2^-9 -> 0 -> 0x00
+      the other 26 elements 0            -> 0x00"""
+    x = np.zeros((1, 32))
+    x[0, :6] = [1.0, -3.0, 13 / 128, 12.5 / 128, 2.0 ** -16, 2.0 ** -17]
+    q, e = oracle.w4a8.mxfp8_quantize(x)
+    assert e.tolist() == [[120]]
+    assert q[0, :6].tolist() == [0x70, 0xFC, 0x55, 0x54, 0x01, 0x00] and not q[0, 6:].any()
+    assert np.array_equal(oracle.w4a8.mxfp8_decode(q, e)[0, :4], [1.0, -3.0, 13 / 128, 12 / 128])
+
+
+def _floor_log2(fr):
+    """floor(log2 fr) of a positive Fraction, by exact comparison."""
+    e = 0
+    while Fraction(2) ** e > fr:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= fr:
+        e += 1
+    return e
+
+
+def pin_w4a8_rational_bruteforce():
+    """Tiny W4A8-MXFP4 products against exact rationals: the block exponent
+    from exact comparisons, the element rounding from torch's e4m3 cast, the
+    weights from the OCP e2m1 table."""
+    e2m1_tab = {int(c): Fraction(v) for c, v in _load_table("e2m1_ocp_mx_v1.txt")}
+    e4 = lambda b: Fraction(float(torch.tensor([int(b)], dtype=torch.uint8)
+                                  .view(torch.float8_e4m3fn).double().item()))
+    for seed in (41, 42):
+        m, n, k = 2, 3, 96
+        qw = synth.random_codes_weight(seed, "mxfp4", n, k)
+        rng = np.random.default_rng(seed)
+        xv = rng.standard_normal((m, k)) * 2.0 ** rng.integers(-6, 6, (m, 1))
+        xv[0, 32:64] = 0.0                                   # an all-zero block
+        x = oracle.decode_activations("bf16", synth.to_bf16_bits(xv))
+        w = oracle.dequantize("mxfp4", n, k, qw.codes, qw.scales, None, 32, True, "ue8m0", 1)[0]
+        y = oracle.w4a8.w4a8_mxfp4_gemm(x, w)
+        for i in range(m):
+            xs = []
+            for b in range(k // 32):
+                blk = [Fraction(float(v)) for v in x[i, 32 * b:32 * b + 32]]
+                amax = max(abs(v) for v in blk)
+                ex = 0 if amax == 0 else min(254, max(0, _floor_log2(amax) - 8 + 127))
+                sc = Fraction(2) ** (ex - 127)
+                xs += [e4(_torch_e4m3_sat(np.array([float(v / sc)]))[0]) * sc for v in blk]
+            for j in range(n):
+                acc = sum(xs[kk] * e2m1_tab[_scalar_code("mxfp4", qw.codes[0, j], kk)]
+                          * Fraction(2) ** (int(qw.scales[0, j, kk // 32]) - 127) for kk in range(k))
+                assert abs(float(acc) - y[i, j]) <= 1e-12 * abs(float(acc)) + 1e-300, (seed, i, j)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -13,6 +13,7 @@ import oracle_pins as P
 from oracle import formats as F
 from oracle import gemm as G
 from oracle import moe as MOE
+from oracle import w4a8 as W
 
 
 def _swap_nibbles(packed, count):
@@ -178,6 +179,30 @@ def _ffn_unrounded(a, topk_ids, topk_w, w13, w2, **kw):
     return _orig_ffn(a, topk_ids, topk_w, w13, w2, **kw)
 
 
+_orig_shared_exp = W.mx_shared_exponent
+
+
+def _shared_exp_emax_7(amax, emax):
+    return _orig_shared_exp(amax, emax - 1)             # e4m3's largest exponent taken as 7
+
+
+def _e4m3_variant(rounding, saturate):
+    def enc(v):
+        v = np.asarray(v, dtype=np.float64)
+        a = np.minimum(np.abs(v), 448.0) if saturate else np.abs(v)
+        _, ex = np.frexp(a)
+        e = np.maximum(np.where(a > 0, ex - 1, -6), -6)
+        q = np.ldexp(1.0, (e - 3).astype(np.int32))
+        r = rounding(a / q) * q
+        _, rex = np.frexp(r)
+        re = rex - 1
+        normal = r >= 2.0 ** -6
+        code = np.where(normal, ((re + 7) << 3) | np.rint((np.ldexp(r, (-re).astype(np.int32)) - 1) * 8).astype(np.int64),
+                        np.rint(r / 2.0 ** -9).astype(np.int64))
+        return ((np.signbit(v).astype(np.int64) << 7) | (code & 0x7F)).astype(np.uint8)
+    return enc
+
+
 MUTATIONS = {
     "nibble_order_swapped": [(F, "unpack_nibbles", _swap_nibbles)],
     "int6_big_endian": [(F, "unpack_int6", _int6_big_endian)],
@@ -200,6 +225,9 @@ MUTATIONS = {
     "nvfp4_tensor_scale_dropped": [(G, "dequantize", _nvfp4_variant(16, False)),
                                    (oracle, "dequantize", _nvfp4_variant(16, False))],
     "mxint4_codes_unsigned": [(G, "dequantize", _mxint4_unsigned), (oracle, "dequantize", _mxint4_unsigned)],
+    "mx_shared_exponent_emax_7": [(W, "mx_shared_exponent", _shared_exp_emax_7)],
+    "e4m3_encode_truncates": [(W, "e4m3_encode", _e4m3_variant(np.trunc, True))],
+    "e4m3_encode_no_saturation": [(W, "e4m3_encode", _e4m3_variant(np.round, False))],
     "bf16_round_truncates": [(MOE, "round_bf16", _bf16_truncate)],
     "bf16_round_ties_away": [(MOE, "round_bf16", _bf16_ties_away)],
     "ffn_intermediates_unrounded": [(MOE, "moe_ffn", _ffn_unrounded), (oracle, "moe_ffn", _ffn_unrounded)],
