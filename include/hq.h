@@ -380,6 +380,19 @@ typedef struct {
 } hq_plan_info;
 hq_status hq_last_plan(hq_plan_info* info);
 
+/*
+ * hq_plan_query — the launch plan hq_gemm would choose for this weight, M,
+ * activation type and flags on a device with `sms` SMs (1..192) and
+ * `smem_optin` bytes of opt-in shared memory per block, computed on the host
+ * alone: no device is queried and nothing is launched (for tests and capacity
+ * planning).  Validation as hq_gemm's for the shape and types; m = 0 gives an
+ * all-zero plan.  The plan of an actual call depends only on these inputs
+ * (the device's SM count and opt-in shared memory), so it equals what
+ * hq_last_plan reports after hq_gemm on such a device.
+ */
+hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, int32_t sms, int64_t smem_optin,
+                        uint32_t flags, hq_plan_info* info);
+
 #ifdef __cplusplus
 }
 #endif

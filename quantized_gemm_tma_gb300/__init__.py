@@ -35,7 +35,7 @@ EXPORTS = [
     "hq_version", "hq_status_string", "hq_transform_size", "hq_transform", "hq_untransform",
     "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_gemm_noalloc", "hq_moe_workspace_size",
     "hq_moe_gemm", "hq_moe_ffn_workspace_size", "hq_moe_ffn", "hq_moe_grouped_workspace_size",
-    "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan",
+    "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan", "hq_plan_query",
 ]
 
 #: size of the fixed device scratch behind hq_gemm_noalloc
@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "hq_moe_grouped_gemm": ([dp, vp, i32, i32, vp, i32, i32, vp, i64, vp, i64, vp, sz, u32, vp], i32),
             "hq_status_read": ([vp, i32, vp, ctypes.POINTER(i32)], i32),
             "hq_last_plan": ([ctypes.POINTER(PlanInfo)], i32),
+            "hq_plan_query": ([dp, i32, i32, i32, i64, u32, ctypes.POINTER(PlanInfo)], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -229,8 +230,21 @@ def hq_status_read(workspace, clear: bool = False, stream=None) -> int:
     return out.value
 
 
+def _plan_dict(info: PlanInfo) -> dict:
+    return {"bn": info.bn, "splits": info.splits, "grid": info.grid, "launches": info.launches,
+            "stages": info.stages, "tile_class": info.tile_class, "groups": info.groups}
+
+
 def hq_last_plan() -> dict:
     info = PlanInfo()
     _check(lib().hq_last_plan(ctypes.byref(info)), "hq_last_plan")
-    return {"bn": info.bn, "splits": info.splits, "grid": info.grid, "launches": info.launches,
-            "stages": info.stages, "tile_class": info.tile_class, "groups": info.groups}
+    return _plan_dict(info)
+
+
+def hq_plan_query(desc: WeightDesc, m: int, atype, sms: int, smem_optin: int, flags: int = 0) -> dict:
+    """The plan hq_gemm would choose on a device with `sms` SMs and `smem_optin`
+    bytes of opt-in shared memory (host only: no device needed)."""
+    info = PlanInfo()
+    _check(lib().hq_plan_query(ctypes.byref(desc), m, ATYPES.get(atype, atype), sms, smem_optin, flags,
+                               ctypes.byref(info)), "hq_plan_query")
+    return _plan_dict(info)

@@ -664,6 +664,35 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   return launch_wna16(l, p, maps, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
+hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, int32_t sms, int64_t smem_optin,
+                        uint32_t flags, hq_plan_info* info) {
+  if (!wdesc || !info || m < 0 || sms <= 0 || sms > kPlanSmsBound || smem_optin <= 0) return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*wdesc, &L);
+  if (st != HQ_OK) return st;
+  if (L.num_experts != 1) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (m > (1 << 30) || !tiles_fit(m, 0, L.n_tiles)) return HQ_ERR_UNSUPPORTED;
+  const bool fp8 = L.wtype == HQ_W_FP8_E4M3;
+  if (fp8 != (atype == HQ_A_FP8_E4M3)) return HQ_ERR_UNSUPPORTED;
+  if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && (L.stype == HQ_S_BF16) != (atype == HQ_A_BF16))
+    return HQ_ERR_UNSUPPORTED;
+  if (L.wtype == HQ_W_MXFP4 && atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  *info = hq_plan_info{};
+  if (m == 0) return HQ_OK;
+  const size_t optin = static_cast<size_t>(smem_optin);
+  if (fp8) {
+    const Fp8Plan pl = plan_fp8(L, m, sms, optin, flags);
+    *info = hq_plan_info{pl.bn, pl.splits, pl.grid, 1, pl.stages, 0, 0, 0};
+    return HQ_OK;
+  }
+  const DensePlan pl = plan_wna16(L, m, sms, optin, flags);
+  if (pl.stages < 2) return HQ_ERR_UNSUPPORTED;
+  *info = hq_plan_info{pl.bn, pl.cluster == 2 ? 2 : (pl.stream_k ? 0 : 1), pl.grid, 1, pl.stages, pl.cls, pl.groups,
+                       0};
+  return HQ_OK;
+}
+
 // ------------------------------------------------------------------ MoE
 hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int32_t topk, int32_t atype,
                                 size_t* bytes) {

@@ -1,0 +1,90 @@
+"""The host-side launch planner (no GPU): tile width, work split and grid for
+the benchmark shapes on a 152-SM device with 227 KB of opt-in shared memory,
+through hq_plan_query."""
+import pytest
+
+SMS, OPTIN = 152, 232448
+
+WHOLE, STREAM_K, CLUSTER = 1, 0, 2
+
+
+@pytest.fixture(scope="module")
+def hq():
+    import quantized_gemm_tma_gb300 as m
+    from quantized_gemm_tma_gb300 import _build
+    _build.build()
+    return m
+
+
+def _int4(hq, n=8192, k=8192):
+    return hq.make_desc("int4", "bf16", n, k, group_k=128, signed_codes=False, has_zeros=True)
+
+
+@pytest.mark.parametrize("m,bn,cls,split,grid", [
+    (1, 16, 0, CLUSTER, 128),       # 64 tiles fill 57..76 of the SMs twice over: 2-CTA K split
+    (16, 16, 0, CLUSTER, 128),
+    (48, 48, 1, CLUSTER, 128),
+    (128, 128, 2, CLUSTER, 128),
+    (1024, 256, 3, WHOLE, SMS),     # 256 wide tiles: whole tiles beat stream-K
+    (4096, 256, 3, WHOLE, SMS),
+])
+def test_dense_int4_bench_shapes(hq, m, bn, cls, split, grid):
+    p = hq.hq_plan_query(_int4(hq), m, "bf16", SMS, OPTIN)
+    assert (p["bn"], p["tile_class"], p["splits"], p["grid"]) == (bn, cls, split, grid), p
+    assert p["stages"] >= 2 and p["launches"] == 1
+
+
+def test_dense_few_tiles_take_stream_k(hq):
+    # N = 4096: 32 tiles are too few for the cluster split; the K-blocks are
+    # dealt out over every SM, at least 8 per CTA
+    p = hq.hq_plan_query(_int4(hq, n=4096), 16, "bf16", SMS, OPTIN)
+    assert (p["splits"], p["grid"]) == (STREAM_K, SMS), p
+    p = hq.hq_plan_query(_int4(hq, n=256, k=1024), 16, "bf16", SMS, OPTIN)   # 2 tiles x 8 K-blocks
+    assert (p["splits"], p["grid"]) == (STREAM_K, 2), p
+
+
+def test_batch_invariant_never_splits_k(hq):
+    for m in (1, 16, 128, 1024):
+        p = hq.hq_plan_query(_int4(hq), m, "bf16", SMS, OPTIN, hq.HQ_FLAG_BATCH_INVARIANT)
+        assert p["splits"] == WHOLE, (m, p)
+    p = hq.hq_plan_query(hq.make_desc("fp8", "fp32", 4096, 7168, group_k=128, group_n=128), 64, "fp8", SMS, OPTIN,
+                         hq.HQ_FLAG_BATCH_INVARIANT)
+    assert p["splits"] == 1, p
+
+
+def test_single_k_block_is_never_split(hq):
+    p = hq.hq_plan_query(_int4(hq, n=1024, k=128), 16, "bf16", SMS, OPTIN)
+    assert (p["splits"], p["grid"]) == (WHOLE, 8), p
+
+
+def test_fp8_block_plans(hq):
+    d = hq.make_desc("fp8", "fp32", 4096, 7168, group_k=128, group_n=128)
+    p = hq.hq_plan_query(d, 64, "fp8", SMS, OPTIN)      # 32 tiles of 128 x 128: split K four ways
+    assert (p["bn"], p["splits"], p["grid"]) == (128, 4, 128), p
+    p = hq.hq_plan_query(d, 4096, "fp8", SMS, OPTIN)    # 512 tiles of 128 x 256: no split
+    assert (p["bn"], p["splits"], p["grid"]) == (256, 1, SMS), p
+
+
+def test_plan_tracks_sm_count_and_shared_memory(hq):
+    # fewer SMs: 64 tiles no longer fit the cluster rule (2 x 64 > 100)
+    p = hq.hq_plan_query(_int4(hq), 16, "bf16", 100, OPTIN)
+    assert p["splits"] != CLUSTER and p["grid"] <= 100, p
+    # less shared memory: fewer pipeline stages, still at least two
+    big = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, OPTIN)
+    small = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, 160 * 1024)
+    assert 2 <= small["stages"] < big["stages"], (small, big)
+
+
+def test_plan_query_validation(hq):
+    d = _int4(hq)
+    for args, want in [((d, -1, "bf16", SMS, OPTIN), hq.HQ_ERR_INVALID_ARG),
+                       ((d, 16, "bf16", 0, OPTIN), hq.HQ_ERR_INVALID_ARG),
+                       ((d, 16, "bf16", SMS, 0), hq.HQ_ERR_INVALID_ARG),
+                       ((d, 16, "fp16", SMS, OPTIN), hq.HQ_ERR_UNSUPPORTED),   # bf16 scales need bf16
+                       ((d, 16, "fp8", SMS, OPTIN), hq.HQ_ERR_UNSUPPORTED),
+                       ((hq.make_desc("mxfp4", "ue8m0", 256, 256, num_experts=4, group_k=32), 16, "bf16", SMS,
+                         OPTIN), hq.HQ_ERR_INVALID_ARG)]:
+        with pytest.raises(hq.HQError) as ei:
+            hq.hq_plan_query(*args)
+        assert ei.value.status == want, (args[1:], ei.value.status)
+    assert hq.hq_plan_query(d, 0, "bf16", SMS, OPTIN)["launches"] == 0
