@@ -148,7 +148,7 @@ bool tiles_fit(int64_t rows, int64_t groups, int n_tiles) {
 
 // Tuning and trace switches from the environment, read once per process.
 struct EnvKnobs {
-  int force_bn = 0, force_splitk = 0, trace = 0;
+  int force_bn = 0, force_splitk = 0, force_wstages = 0, force_xstages = 0, trace = 0;
 };
 const EnvKnobs& env() {
   static const EnvKnobs k = [] {
@@ -159,6 +159,8 @@ const EnvKnobs& env() {
     };
     e.force_bn = get("HQ_FORCE_BN");
     e.force_splitk = get("HQ_FORCE_SPLITK");
+    e.force_wstages = get("HQ_FORCE_WSTAGES");
+    e.force_xstages = get("HQ_FORCE_XSTAGES");
     e.trace = get("HQ_TRACE");
     return e;
   }();
@@ -169,6 +171,8 @@ int env_int(const char* name, int dflt) {
   int v = 0;
   if (!std::strcmp(name, "HQ_FORCE_BN")) v = env().force_bn;
   else if (!std::strcmp(name, "HQ_FORCE_SPLITK")) v = env().force_splitk;
+  else if (!std::strcmp(name, "HQ_FORCE_WSTAGES")) v = env().force_wstages;
+  else if (!std::strcmp(name, "HQ_FORCE_XSTAGES")) v = env().force_xstages;
   else if (!std::strcmp(name, "HQ_TRACE")) v = env().trace;
   return v ? v : dflt;
 }
@@ -410,9 +414,12 @@ void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_
                  int* x_stages, int* groups) {
   const size_t cap = std::min<size_t>(smem_optin, 232448);
   static const int kXWant[4] = {6, 3, 3, 2};
-  int sx = kXWant[cls], sw = 0;
+  // sweep overrides (clamped to [2, 12] and to what fits)
+  const int fx = env_int("HQ_FORCE_XSTAGES", 0), fw = env_int("HQ_FORCE_WSTAGES", 0);
+  int sx = fx >= 2 ? std::min(fx, 12) : kXWant[cls], sw = 0;
+  const int sw_max = fw >= 2 ? std::min(fw, 12) : 8;
   for (; sx >= 2; --sx) {
-    for (sw = 8; sw >= 2; --sw)
+    for (sw = sw_max; sw >= 2; --sw)
       if (wna16_smem_bytes(cls, sw, sx, L.tile_bytes, bn, num_experts) <= cap) break;
     if (sw >= 2) break;
   }

@@ -88,3 +88,20 @@ def test_plan_query_validation(hq):
             hq.hq_plan_query(*args)
         assert ei.value.status == want, (args[1:], ei.value.status)
     assert hq.hq_plan_query(d, 0, "bf16", SMS, OPTIN)["launches"] == 0
+
+
+def test_stage_override_switch(hq):
+    """HQ_FORCE_WSTAGES (read once per process) caps the weight ring for sweeps."""
+    import os
+    import subprocess
+    import sys
+    code = ("import quantized_gemm_tma_gb300 as hq; "
+            "d = hq.make_desc('int4', 'bf16', 8192, 8192, group_k=128, signed_codes=False, has_zeros=True); "
+            "print(hq.hq_plan_query(d, 4096, 'bf16', 152, 232448)['stages'])")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, HQ_FORCE_WSTAGES="3", PYTHONPATH=root)
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert int(out.stdout.strip()) == 3
+    default = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, OPTIN)["stages"]
+    assert default > 3
