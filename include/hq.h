@@ -357,6 +357,17 @@ hq_status hq_moe_grouped_gemm(const hq_weight_desc* wdesc, const void* w_t, int3
                               hq_stream_t stream);
 
 /*
+ * hq_selftest_wait_timeout — exercise the device-side failure path shared by
+ * every kernel of the library, without a fault: one CTA waits on a barrier
+ * that nothing completes, with the library's bounded wait (about 2 s); when
+ * the wait runs out it records HQ_ERR_DEVICE_TIMEOUT in the status word of
+ * `workspace` (16-byte aligned, at least 256 bytes, initialised) and exits
+ * normally.  The context stays usable; hq_status_read reports and clears the
+ * word.  For tests of failure detection.  Asynchronous.
+ */
+hq_status hq_selftest_wait_timeout(void* workspace, hq_stream_t stream);
+
+/*
  * hq_status_read — synchronise `stream` and read the device status word of a
  * workspace (HQ_OK when no device-side error was recorded).  With clear != 0
  * the word is reset to HQ_OK afterwards.

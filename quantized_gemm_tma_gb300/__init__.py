@@ -35,7 +35,7 @@ EXPORTS = [
     "hq_version", "hq_status_string", "hq_transform_size", "hq_transform", "hq_untransform",
     "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_gemm_noalloc", "hq_moe_workspace_size",
     "hq_moe_gemm", "hq_moe_ffn_workspace_size", "hq_moe_ffn", "hq_moe_grouped_workspace_size",
-    "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan", "hq_plan_query",
+    "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan", "hq_plan_query", "hq_selftest_wait_timeout",
 ]
 
 #: size of the fixed device scratch behind hq_gemm_noalloc
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
             "hq_status_read": ([vp, i32, vp, ctypes.POINTER(i32)], i32),
             "hq_last_plan": ([ctypes.POINTER(PlanInfo)], i32),
             "hq_plan_query": ([dp, i32, i32, i32, i64, u32, ctypes.POINTER(PlanInfo)], i32),
+            "hq_selftest_wait_timeout": ([vp, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -233,6 +234,10 @@ def hq_status_read(workspace, clear: bool = False, stream=None) -> int:
 def _plan_dict(info: PlanInfo) -> dict:
     return {"bn": info.bn, "splits": info.splits, "grid": info.grid, "launches": info.launches,
             "stages": info.stages, "tile_class": info.tile_class, "groups": info.groups}
+
+
+def hq_selftest_wait_timeout(workspace, stream=None) -> None:
+    _check(lib().hq_selftest_wait_timeout(_ptr(workspace), _stream(stream)), "hq_selftest_wait_timeout")
 
 
 def hq_last_plan() -> dict:

@@ -700,6 +700,17 @@ hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, i
   return HQ_OK;
 }
 
+hq_status hq_selftest_wait_timeout(void* workspace, hq_stream_t stream) {
+  if (!workspace) return HQ_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return HQ_ERR_ALIGNMENT;
+  DevInfo di;
+  hq_status st = device_info(&di);
+  if (st != HQ_OK) return st;
+  return launch_wait_timeout(static_cast<int*>(workspace), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? HQ_OK
+             : HQ_ERR_CUDA;
+}
+
 // ------------------------------------------------------------------ MoE
 hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int32_t topk, int32_t atype,
                                 size_t* bytes) {

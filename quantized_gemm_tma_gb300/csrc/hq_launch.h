@@ -70,6 +70,9 @@ cudaError_t launch_fp8(const Fp8Params& p, const CUtensorMap& tmap, int bn_max, 
                        cudaStream_t stream);
 uint32_t fp8_smem_bytes(int stages, int bn);
 
+// selftest.cu: one CTA whose bounded wait runs out and records HQ_ERR_DEVICE_TIMEOUT in *status
+cudaError_t launch_wait_timeout(int* status, cudaStream_t stream);
+
 // moe.cu
 cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, int bn, int* expert_offsets,
                              int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* status,

@@ -172,3 +172,10 @@ def test_size_limits_rejected_on_host(hq):
         hq.hq_moe_grouped_gemm(dm, fake, hq.HQ_MOE_GROUPED_MASKED, 1 << 21, fake, 0, "bf16", fake, 2048, fake,
                                1 << 20, fake, 1 << 62)
     assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
+
+
+def test_selftest_timeout_host_validation(hq):
+    for ws, want in [(None, hq.HQ_ERR_INVALID_ARG), (0x10008, hq.HQ_ERR_ALIGNMENT)]:
+        with pytest.raises(hq.HQError) as ei:
+            hq.hq_selftest_wait_timeout(ws)
+        assert ei.value.status == want
