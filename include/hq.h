@@ -404,6 +404,15 @@ hq_status hq_last_plan(hq_plan_info* info);
 hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, int32_t sms, int64_t smem_optin,
                         uint32_t flags, hq_plan_info* info);
 
+/*
+ * hq_moe_plan_query — as hq_plan_query, for hq_moe_gemm with `tokens` tokens
+ * routed to `topk` experts each: the expert tile width (tokens per tile, from
+ * the mean routed rows per expert), its class, the ring stages and the grid
+ * (one CTA per SM); launches = 3 (route, grouped GEMM, combine).  Host only.
+ */
+hq_status hq_moe_plan_query(const hq_weight_desc* wdesc, int32_t tokens, int32_t topk, int32_t sms,
+                            int64_t smem_optin, hq_plan_info* info);
+
 #ifdef __cplusplus
 }
 #endif

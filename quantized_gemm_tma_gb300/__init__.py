@@ -36,6 +36,7 @@ EXPORTS = [
     "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_gemm_noalloc", "hq_moe_workspace_size",
     "hq_moe_gemm", "hq_moe_ffn_workspace_size", "hq_moe_ffn", "hq_moe_grouped_workspace_size",
     "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan", "hq_plan_query", "hq_selftest_wait_timeout",
+    "hq_moe_plan_query",
 ]
 
 #: size of the fixed device scratch behind hq_gemm_noalloc
@@ -97,6 +98,7 @@ def lib() -> ctypes.CDLL:
             "hq_last_plan": ([ctypes.POINTER(PlanInfo)], i32),
             "hq_plan_query": ([dp, i32, i32, i32, i64, u32, ctypes.POINTER(PlanInfo)], i32),
             "hq_selftest_wait_timeout": ([vp, vp], i32),
+            "hq_moe_plan_query": ([dp, i32, i32, i32, i64, ctypes.POINTER(PlanInfo)], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -252,4 +254,12 @@ def hq_plan_query(desc: WeightDesc, m: int, atype, sms: int, smem_optin: int, fl
     info = PlanInfo()
     _check(lib().hq_plan_query(ctypes.byref(desc), m, ATYPES.get(atype, atype), sms, smem_optin, flags,
                                ctypes.byref(info)), "hq_plan_query")
+    return _plan_dict(info)
+
+
+def hq_moe_plan_query(desc: WeightDesc, tokens: int, topk: int, sms: int, smem_optin: int) -> dict:
+    """The plan hq_moe_gemm would choose on such a device (host only)."""
+    info = PlanInfo()
+    _check(lib().hq_moe_plan_query(ctypes.byref(desc), tokens, topk, sms, smem_optin, ctypes.byref(info)),
+           "hq_moe_plan_query")
     return _plan_dict(info)

@@ -711,6 +711,27 @@ hq_status hq_selftest_wait_timeout(void* workspace, hq_stream_t stream) {
              : HQ_ERR_CUDA;
 }
 
+hq_status hq_moe_plan_query(const hq_weight_desc* wdesc, int32_t tokens, int32_t topk, int32_t sms,
+                            int64_t smem_optin, hq_plan_info* info) {
+  if (!wdesc || !info || tokens < 0 || topk <= 0 || sms <= 0 || sms > kPlanSmsBound || smem_optin <= 0)
+    return HQ_ERR_INVALID_ARG;
+  Layout L;
+  hq_status st = make_layout(*wdesc, &L);
+  if (st != HQ_OK) return st;
+  if (L.num_experts > 1024 || L.wtype == HQ_W_FP8_E4M3) return HQ_ERR_UNSUPPORTED;
+  const int64_t pairs = static_cast<int64_t>(tokens) * topk;
+  if (pairs > (1 << 24) || !tiles_fit(pairs, L.num_experts, L.n_tiles)) return HQ_ERR_UNSUPPORTED;
+  *info = hq_plan_info{};
+  if (tokens == 0) return HQ_OK;
+  const int bn = moe_tile_bn(static_cast<double>(pairs) / L.num_experts);
+  const int cls = wna16_class(bn);
+  int stages = 0, x_stages = 0, groups = 0;
+  plan_stages(cls, L, bn, L.num_experts, static_cast<size_t>(smem_optin), &stages, &x_stages, &groups);
+  if (stages < 2) return HQ_ERR_UNSUPPORTED;
+  *info = hq_plan_info{bn, 1, sms, 3, stages, cls, groups, 0};
+  return HQ_OK;
+}
+
 // ------------------------------------------------------------------ MoE
 hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int32_t topk, int32_t atype,
                                 size_t* bytes) {

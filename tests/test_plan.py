@@ -105,3 +105,24 @@ def test_stage_override_switch(hq):
     assert int(out.stdout.strip()) == 3
     default = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, OPTIN)["stages"]
     assert default > 3
+
+
+@pytest.mark.parametrize("tokens,bn,cls", [(1, 16, 0), (16, 16, 0), (256, 16, 0), (257, 128, 2), (4096, 128, 2)])
+def test_moe_tile_width_from_mean_rows(hq, tokens, bn, cls):
+    """E = 128, top-8: 16-token expert tiles up to a mean of 16 routed rows per expert, then 128."""
+    d = hq.make_desc("mxfp4", "ue8m0", 1536, 2048, num_experts=128, group_k=32)
+    p = hq.hq_moe_plan_query(d, tokens, 8, SMS, OPTIN)
+    assert (p["bn"], p["tile_class"], p["grid"], p["launches"]) == (bn, cls, SMS, 3), p
+    assert p["stages"] >= 2
+
+
+def test_moe_plan_query_validation(hq):
+    d = hq.make_desc("mxfp4", "ue8m0", 1536, 2048, num_experts=128, group_k=32)
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_moe_plan_query(d, 16, 0, SMS, OPTIN)
+    assert ei.value.status == hq.HQ_ERR_INVALID_ARG
+    f8 = hq.make_desc("fp8", "fp32", 256, 256, num_experts=4, group_k=128, group_n=128)
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_moe_plan_query(f8, 16, 2, SMS, OPTIN)
+    assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
+    assert hq.hq_moe_plan_query(d, 0, 8, SMS, OPTIN)["launches"] == 0
