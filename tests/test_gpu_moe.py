@@ -67,20 +67,6 @@ def test_int4_experts():
     check(y, _ref(qw, acts, r), "int4 experts")
 
 
-def test_moe_plan_query_matches_the_launch():
-    import torch
-    import quantized_gemm_tma_gb300 as hq
-    from gpu_helpers import DevWeight, run_moe
-    props = torch.cuda.get_device_properties(0)
-    optin = getattr(props, "shared_memory_per_block_optin", 232448)
-    for seed, t, e, n, k, topk in ((30, 24, 8, 256, 256, 2), (31, 300, 4, 256, 256, 4)):
-        qw, acts, r = synth.moe_mxfp4(seed, t, num_experts=e, n=n, k=k, topk=topk)
-        dw = DevWeight(qw)
-        y, st = run_moe(dw, acts, r)
-        assert st == 0
-        assert hq.hq_last_plan() == hq.hq_moe_plan_query(dw.desc, t, topk, props.multi_processor_count, optin)
-
-
 def test_invalid_expert_id_sets_status():
     import quantized_gemm_tma_gb300 as hq
     qw, acts, r = synth.moe_mxfp4(7, 8, num_experts=4, n=128, k=128, topk=2)
