@@ -68,3 +68,20 @@ def test_layer_forward_matches_oracle(hq):
     lin.load(dev(qw.codes), dev(qw.scales)).transform()
     check(lin(dev(acts.data), dev(acts.scales)).double().cpu().numpy(), oracle.gemm.reference(qw, acts),
           "layer fp8")
+
+
+@pytest.mark.parametrize("wtype,stype,group_k,zeros,n,k", [
+    ("int4", "bf16", 128, False, 200, 512), ("int4", "fp16", 32, True, 130, 96), ("int4", "bf16", 0, True, 77, 260),
+    ("int6", "fp16", 0, False, 256, 512), ("int6", "bf16", 64, True, 130, 384), ("mxfp4", "ue8m0", 32, False, 150, 96),
+    ("fp8", "fp32", 128, False, 130, 200),
+])
+def test_layer_sizes_match_the_standard_format(hq, wtype, stype, group_k, zeros, n, k):
+    """The sizes QuantLinear checks are those of the standard-format arrays the generators write."""
+    from quantized_gemm_tma_gb300.layer import QuantLinear
+    qw = synth.random_codes_weight(5, wtype, n, k, group_k=group_k, has_zeros=zeros,
+                                   stype=stype if stype in ("bf16", "fp16") else None)
+    lin = QuantLinear(n, k, wtype, stype, group_k=group_k, group_n=128 if wtype == "fp8" else 1,
+                      signed_codes=qw.signed, has_zeros=zeros)
+    want = lin.standard_bytes()
+    assert want["codes"] == qw.codes.nbytes and want["scales"] == qw.scales.nbytes
+    assert want["zeros"] == (qw.zeros.nbytes if zeros else 0)
