@@ -30,6 +30,7 @@ workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import tempfile
 import json
 import os
 import statistics
@@ -111,10 +112,11 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, out_dir: str | None = None):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.out_dir = out_dir or tempfile.mkdtemp(prefix="hq_clocks_")
+        self.path = os.path.join(self.out_dir, f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
@@ -360,7 +362,7 @@ def run_gpu(args, rank: int, world: int):
             done += k
         return out
 
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev.index, args.clocks_dir) as clk:
         barrier()
         wall0 = time.perf_counter()
         torch.cuda._sleep(HEAD_START_CYCLES)
@@ -528,6 +530,9 @@ def main():
                     help="end-to-end pass with the copies on their own streams, overlapping the GEMMs")
     ap.add_argument("--m-sweep", type=str, default=",".join(map(str, M_SWEEP)),
                     help="comma-separated M values of the dense sweep")
+    ap.add_argument("--clocks-dir", type=str, default=None,
+                    help="directory for the nvidia-smi clock samples of the timed region (default: a new "
+                         "temporary directory)")
     args = ap.parse_args()
     args.m_sweep = [int(v) for v in args.m_sweep.split(",") if v]
     args.warmup = max(args.warmup, 3)

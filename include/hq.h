@@ -135,8 +135,17 @@ typedef struct {
 } hq_weight_desc;
 
 /* flags for hq_gemm / hq_moe_gemm */
-#define HQ_FLAG_BATCH_INVARIANT 0x1u /* no split-K: the reduction order does not depend on M
-                                        ([WIKI] "Precision and deployment considerations") */
+/*
+ * HQ_FLAG_BATCH_INVARIANT: a row of Y is bit-identical whatever M is and
+ * whatever the other rows of X hold ([WIKI] "Precision and deployment
+ * considerations": no Stream-K, and the same MMA configuration at every batch
+ * size).  hq_gemm then runs one kernel configuration for every M: WnA16 with
+ * 64-token tiles, group scales folded into the 16-bit operand, the K-blocks
+ * accumulated by two issuers (even and odd K-blocks, summed in that order),
+ * no split-K, stream-K or cluster split; FP8 with 128-row weight tiles and no
+ * split-K.  Decode-sized M is slower this way than with the default plans.
+ */
+#define HQ_FLAG_BATCH_INVARIANT 0x1u
 
 /* Library version (major*10000 + minor*100 + patch). */
 int32_t hq_version(void);
@@ -217,6 +226,9 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
                   const void* x, int64_t ldx, const float* x_scales, void* y, int64_t ldy,
                   void* workspace, size_t ws_bytes, uint32_t flags, hq_stream_t stream);
 
+/* hq_gemm_noalloc only: clear the scratch's status word and counters first. */
+#define HQ_FLAG_NOALLOC_RESET 0x100u
+
 /* Bytes of the fixed device scratch behind hq_gemm_noalloc (8 MiB). */
 #define HQ_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
@@ -233,15 +245,21 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
  * zero at module load; no call allocates host or device memory.
  *
  * Arguments are hq_gemm's, less workspace/ws_bytes, plus:
+ * flags          hq_gemm's flags, plus HQ_FLAG_NOALLOC_RESET: before the
+ *                GEMM, clear the scratch's status word and split-K counters
+ *                with cudaMemsetAsync on `stream` (allocates nothing).
  * device_status  optional 4-byte device word; if non-null, the scratch's
  *                status word is copied there on `stream` after the GEMM.
  *                That word is sticky: once a bounded device-side wait has run
- *                out it stays set for the life of the process (the split-K
- *                counters may then be stale), and every later copy shows it.
+ *                out it stays set (and the split-K counters may be stale)
+ *                until a call passes HQ_FLAG_NOALLOC_RESET, which is the way
+ *                back to correct results after such an error.
  *
  * Set-up: the first call with a given device current looks up the scratch's
- * address (cudaGetSymbolAddress) and caches it; make that first call before
- * any stream capture.
+ * address (cudaGetSymbolAddress) and caches it, keyed by the device and its
+ * CUDA context (a context destroyed and created again, e.g. after
+ * cudaDeviceReset, gets a fresh lookup); make that first call before any
+ * stream capture.
  * Limit: a problem whose hq_gemm_workspace_size() exceeds
  * HQ_NOALLOC_SCRATCH_BYTES is rejected with HQ_ERR_WORKSPACE_TOO_SMALL before
  * anything is launched; use hq_gemm with a workspace for it.
@@ -412,6 +430,17 @@ hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, i
  */
 hq_status hq_moe_plan_query(const hq_weight_desc* wdesc, int32_t tokens, int32_t topk, int32_t sms,
                             int64_t smem_optin, hq_plan_info* info);
+
+/*
+ * hq_tuning_reload — read the tuning switches again from the environment
+ * (HQ_FORCE_BN, HQ_FORCE_SPLITK, HQ_FORCE_WSTAGES, HQ_FORCE_XSTAGES,
+ * HQ_TRACE).  They are otherwise read once, at the first call that plans a
+ * launch.  For sweeps and tests that compare plans in one process; call it
+ * only while no other call of this library runs.  The pages have no
+ * counterpart (their tuning configuration is an object passed to the layer,
+ * aiwiki article, section "Configuration model").
+ */
+void hq_tuning_reload(void);
 
 #ifdef __cplusplus
 }

@@ -24,6 +24,7 @@ HQ_W_INT4, HQ_W_INT6, HQ_W_MXFP4, HQ_W_FP8_E4M3 = 0, 1, 2, 3
 HQ_A_BF16, HQ_A_FP16, HQ_A_FP8_E4M3 = 0, 1, 2
 HQ_S_BF16, HQ_S_FP16, HQ_S_FP32, HQ_S_UE8M0 = 0, 1, 2, 3
 HQ_FLAG_BATCH_INVARIANT = 0x1
+HQ_FLAG_NOALLOC_RESET = 0x100
 HQ_MOE_GROUPED_CONTIGUOUS, HQ_MOE_GROUPED_MASKED = 0, 1
 
 WTYPES = {"int4": HQ_W_INT4, "int6": HQ_W_INT6, "mxfp4": HQ_W_MXFP4, "fp8": HQ_W_FP8_E4M3}
@@ -36,7 +37,7 @@ EXPORTS = [
     "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_gemm_noalloc", "hq_moe_workspace_size",
     "hq_moe_gemm", "hq_moe_ffn_workspace_size", "hq_moe_ffn", "hq_moe_grouped_workspace_size",
     "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan", "hq_plan_query", "hq_selftest_wait_timeout",
-    "hq_moe_plan_query",
+    "hq_moe_plan_query", "hq_tuning_reload",
 ]
 
 #: size of the fixed device scratch behind hq_gemm_noalloc
@@ -99,6 +100,7 @@ def lib() -> ctypes.CDLL:
             "hq_plan_query": ([dp, i32, i32, i32, i64, u32, ctypes.POINTER(PlanInfo)], i32),
             "hq_selftest_wait_timeout": ([vp, vp], i32),
             "hq_moe_plan_query": ([dp, i32, i32, i32, i64, ctypes.POINTER(PlanInfo)], i32),
+            "hq_tuning_reload": ([], None),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -263,3 +265,8 @@ def hq_moe_plan_query(desc: WeightDesc, tokens: int, topk: int, sms: int, smem_o
     _check(lib().hq_moe_plan_query(ctypes.byref(desc), tokens, topk, sms, smem_optin, ctypes.byref(info)),
            "hq_moe_plan_query")
     return _plan_dict(info)
+
+
+def hq_tuning_reload() -> None:
+    """Re-read the HQ_FORCE_* / HQ_TRACE switches from the environment."""
+    lib().hq_tuning_reload()

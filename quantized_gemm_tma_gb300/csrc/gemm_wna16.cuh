@@ -35,9 +35,9 @@
 //                have converted the codes.
 //   warp 21      activation producer: per stage one tensor copy per 64-column
 //                slab (128-byte swizzle) into the activation ring, released
-//                by the MMA; MoE rows are gathered by routing index (per-lane
-//                16-byte copies, or four rows per tile::gather4 copy for
-//                16-token tiles).
+//                by the MMA; MoE rows are gathered by routing index, four
+//                rows per tile::gather4 tensor copy, the copies of a stage
+//                issued by all 32 lanes.
 //   warps 22..   MMA issuers: issuer p takes K-block p of every stage and
 //                accumulates into its own TMEM accumulator, so two threads
 //                issue tcgen05.mma.kind::f16 concurrently for narrow tiles
@@ -373,9 +373,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // With streams, issuer p takes K-block p of every stage, i.e. the K-blocks
   // of streams p and 2 + p alternately.
   constexpr int KR = kKRing / ISS;  // promotion: accumulator ring per issuer
-  // MoE with wide tiles gathers activation rows with per-lane cp.async (one
-  // tile::gather4 copy moves only 512 bytes, too few for bn >= 64)
-  constexpr bool kLaneGather = MOE && CLS >= 1;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from smem_raw by an offset so that the
   // compiler keeps shared-memory addressing for every access through it
@@ -420,6 +417,14 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = dev::lane_id();
+  // Streams of one stage parity skip the other parity's stages, so a weight
+  // ring slot must always carry stages of one parity (even depth); an odd
+  // depth would let a parity wait pass one phase early.  The planner never
+  // asks for one; refuse it before any barrier, TMEM or copy exists.
+  if (kStream && (SW & 1)) {
+    if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0, static_cast<int>(HQ_ERR_INVALID_ARG));
+    return;
+  }
   if (threadIdx.x == 0) HQ_TRACE_CTA(0);
 
   if (threadIdx.x == 0) {
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       dev::mbar_init(&w_empty[s], kStream ? 8 : kDqWarps);  // streams: the two of the stage's parity
     }
     for (int s = 0; s < SX; ++s) {
-      dev::mbar_init(&x_full[s], kLaneGather ? 32u : 1u);
+      dev::mbar_init(&x_full[s], 1);
       dev::mbar_init(&x_empty[s], ISS);
     }
     for (int a = 0; a < NAB; ++a) {
@@ -548,11 +553,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     Ring rg;
     int issued = 0;
     bool ok = true;
-    // per-lane gathers: the stage whose copies were issued last.  Each lane
-    // counts in on a stage only after its copies have completed and it has
-    // fenced them into the async proxy the tensor cores read through; that
-    // happens once the next stage is issued, so two stages are in flight.
-    [[maybe_unused]] int pend = -1;
     Unit u;
     while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
       if constexpr (MOE) {
@@ -567,47 +567,22 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           break;
         }
         uint8_t* xs = x_st + rg.s * x_stage;
-        if constexpr (kLaneGather) {
-          // rows r = lane + 32 j, sixteen 16-byte chunks per row and K-block
-          // (two 128-byte swizzled slabs); columns past K are zero-filled
-          for (int r = static_cast<int>(lane); r < u.rows; r += 32) {
-            const __nv_bfloat16* src_row = p.x_rows + static_cast<int64_t>(s_tok[r]) * p.ldx;
-            for (int z = 0; z < 2 * cnt; ++z) {
-              const int col0 = (2 * kb + z) * 64;
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const int col = col0 + c * 8;
-                const bool valid = col < p.k;
-                uint8_t* dst = xs + z * slab + r * 128 + ((c ^ (r & 7)) << 4);
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dev::smem_u32(dst)),
-                             "l"(valid ? src_row + col : src_row), "r"(valid ? 16u : 0u)
-                             : "memory");
-              }
-            }
+        if (lane == 0) dev::mbar_arrive_expect_tx(&x_full[rg.s], 2u * cnt * slab);
+        if constexpr (MOE) {
+          // gathered rows, four per tensor copy (one-row boxes), the stage's
+          // copies dealt out over the lanes; rows past the unit (token index
+          // T) and columns past K are out of range and zero-filled
+          __syncwarp();
+          const int per_slab = bn >> 2;
+          for (int i = static_cast<int>(lane); i < 2 * cnt * per_slab; i += 32) {
+            const int z = i / per_slab, r = 4 * (i - z * per_slab);
+            dev::tma_gather4(xs + z * slab + r * 128, &tmap_x, &x_full[rg.s], (2 * kb + z) * 64, s_tok[r],
+                             s_tok[r + 1], s_tok[r + 2], s_tok[r + 3]);
           }
-          asm volatile("cp.async.commit_group;" ::: "memory");
-          if (pend >= 0) {
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-            dev::fence_proxy_async_smem();
-            dev::mbar_arrive(&x_full[pend]);
-          }
-          pend = rg.s;
         } else if (lane == 0) {
-          dev::mbar_arrive_expect_tx(&x_full[rg.s], 2u * cnt * slab);
-          for (int z = 0; z < 2 * cnt; ++z) {
-            const int x = (2 * kb + z) * 64;
-            if constexpr (MOE) {
-              // gathered rows, four per tensor copy (one-row boxes); rows past
-              // the unit and columns past K are out of range and zero-filled
-              for (int r = 0; r < bn; r += 4)
-                dev::tma_gather4(xs + z * slab + r * 128, &tmap_x, &x_full[rg.s], x, s_tok[r], s_tok[r + 1],
-                                 s_tok[r + 2], s_tok[r + 3]);
-            } else {
-              // one 64-column slab of bn rows; columns past K and rows past M
-              // are zero-filled by the tensor copy
-              dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], x, u.row0);
-            }
-          }
+          // one 64-column slab of bn rows; columns past K and rows past M
+          // are zero-filled by the tensor copy
+          for (int z = 0; z < 2 * cnt; ++z) dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], (2 * kb + z) * 64, u.row0);
         }
         rg.next(SX);
         ++issued;
@@ -615,13 +590,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       if constexpr (MOE) __syncwarp();  // s_tok is rewritten for the next unit
     }
     if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
-    if constexpr (kLaneGather) {
-      asm volatile("cp.async.wait_all;" ::: "memory");
-      if (pend >= 0) {
-        dev::fence_proxy_async_smem();
-        dev::mbar_arrive(&x_full[pend]);
-      }
-    }
     if (lane == 0) {
       for (int s = 0; s < SX && s < issued; ++s) {
         const int last = ((issued - 1 - s) / SX) * SX + s;
@@ -688,7 +656,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
                 break;
               }
               HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
-              if constexpr (kLaneGather) dev::fence_proxy_async_smem();  // cp.async rows -> tensor-core reads
               dev::tc_fence_after();
               const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(t * 64 + h * 32);
 #pragma unroll
@@ -712,7 +679,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               break;
             }
             HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
-            if constexpr (kLaneGather) dev::fence_proxy_async_smem();  // cp.async rows -> tensor-core reads
             dev::tc_fence_after();
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + 2u * pidx * slab;
             const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(slot) * 64u;

@@ -146,25 +146,29 @@ bool tiles_fit(int64_t rows, int64_t groups, int n_tiles) {
   return (rows / 16 + groups + 1) * static_cast<int64_t>(n_tiles) <= INT32_MAX;
 }
 
-// Tuning and trace switches from the environment, read once per process.
+// Tuning and trace switches from the environment, read on first use and
+// again by hq_tuning_reload().
 struct EnvKnobs {
   int force_bn = 0, force_splitk = 0, force_wstages = 0, force_xstages = 0, trace = 0;
 };
+EnvKnobs read_env() {
+  EnvKnobs e;
+  auto get = [](const char* name) {
+    const char* v = std::getenv(name);
+    return v ? std::atoi(v) : 0;
+  };
+  e.force_bn = get("HQ_FORCE_BN");
+  e.force_splitk = get("HQ_FORCE_SPLITK");
+  e.force_wstages = get("HQ_FORCE_WSTAGES");
+  e.force_xstages = get("HQ_FORCE_XSTAGES");
+  e.trace = get("HQ_TRACE");
+  return e;
+}
+EnvKnobs g_knobs;
+std::once_flag g_knobs_once;
 const EnvKnobs& env() {
-  static const EnvKnobs k = [] {
-    EnvKnobs e;
-    auto get = [](const char* name) {
-      const char* v = std::getenv(name);
-      return v ? std::atoi(v) : 0;
-    };
-    e.force_bn = get("HQ_FORCE_BN");
-    e.force_splitk = get("HQ_FORCE_SPLITK");
-    e.force_wstages = get("HQ_FORCE_WSTAGES");
-    e.force_xstages = get("HQ_FORCE_XSTAGES");
-    e.trace = get("HQ_TRACE");
-    return e;
-  }();
-  return k;
+  std::call_once(g_knobs_once, [] { g_knobs = read_env(); });
+  return g_knobs;
 }
 
 int env_int(const char* name, int dflt) {
@@ -337,6 +341,11 @@ hq_status hq_status_read(void* workspace, int32_t clear, hq_stream_t stream, int
   return HQ_OK;
 }
 
+void hq_tuning_reload(void) {
+  env();  // the first read has happened, so this one is not overwritten by it
+  g_knobs = read_env();
+}
+
 hq_status hq_last_plan(hq_plan_info* info) {
   if (!info) return HQ_ERR_INVALID_ARG;
   *info = g_last_plan;
@@ -351,9 +360,13 @@ namespace {
 
 constexpr int kMaxSplits = 64;
 constexpr int kPlanSmsBound = 192;  // >= the SM count of any sm_103 part (workspace sizing)
-// split-K runs only on problems of at most this many output tiles
-constexpr int kMaxSplitTiles = 512;
-constexpr size_t kCounterBytes = sizeof(int) * kMaxSplitTiles * 8;
+// split-K runs only on problems of at most kMaxSplitTiles output tiles
+constexpr size_t kCounterBytes = kWsCounterBytes;
+static_assert(kAlign == kWsStatusBytes, "the status region is one alignment unit");
+
+// Tokens per tile of every batch-invariant WnA16 plan (FP8: weight rows).
+constexpr int kInvariantBn = 64;
+constexpr int kInvariantFp8Bn = 128;
 
 struct DensePlan {
   int cls, bn, m_tiles, tiles, stages, x_stages, groups, grid, stream_k, cluster;
@@ -371,9 +384,10 @@ struct Fp8Plan {
 Fp8Plan plan_fp8(const Layout& L, int m, int sms, size_t smem_optin, uint32_t flags) {
   Fp8Plan p{};
   p.m_tiles = cdiv(m, 128);
-  p.bn = (L.n_tiles >= 2 && p.m_tiles * cdiv(L.n_tiles, 2) >= sms / 2) ? 256 : 128;
+  const bool inv = (flags & HQ_FLAG_BATCH_INVARIANT) != 0;
+  p.bn = inv ? kInvariantFp8Bn : (L.n_tiles >= 2 && p.m_tiles * cdiv(L.n_tiles, 2) >= sms / 2) ? 256 : 128;
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
-  if (forced_bn == 128 || forced_bn == 256) p.bn = forced_bn;
+  if (!inv && (forced_bn == 128 || forced_bn == 256)) p.bn = forced_bn;
   p.n_groups = cdiv(L.n_tiles, p.bn / 128);
   const int tiles = p.m_tiles * p.n_groups;
   int splits = 1;
@@ -418,8 +432,14 @@ void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_
   const int fx = env_int("HQ_FORCE_XSTAGES", 0), fw = env_int("HQ_FORCE_WSTAGES", 0);
   int sx = fx >= 2 ? std::min(fx, 12) : kXWant[cls], sw = 0;
   const int sw_max = fw >= 2 ? std::min(fw, 12) : 8;
+  // Two K-blocks per stage: the dequantiser streams of one stage parity wait
+  // only on the stages of that parity, so every slot of the weight ring must
+  // always hold stages of one parity, i.e. an even ring depth.  With an odd
+  // depth a slot alternates parities and a stream's parity wait on it could
+  // pass one phase early, while the other parity's copy is still landing.
+  const int sw_step = wna16_kps(cls) == 2 ? 2 : 1;
   for (; sx >= 2; --sx) {
-    for (sw = sw_max; sw >= 2; --sw)
+    for (sw = sw_max - (sw_max % sw_step); sw >= 2; sw -= sw_step)
       if (wna16_smem_bytes(cls, sw, sx, L.tile_bytes, bn, num_experts) <= cap) break;
     if (sw >= 2) break;
   }
@@ -435,9 +455,14 @@ int wna16_class(int bn) { return bn <= 16 ? 0 : (bn <= 64 ? 1 : (bn <= 128 ? 2 :
 // of weight K-blocks.
 DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_t flags) {
   DensePlan p{};
-  p.bn = m <= 64 ? std::max(16, cdiv(m, 16) * 16) : (m <= 128 ? 128 : (m <= 192 ? 192 : 256));
+  // Batch invariance: one configuration for every M (64-token tiles of the
+  // two-K-block class, whose two issuers accumulate even and odd K-blocks
+  // and are summed in that order; group scales folded into the operand; no
+  // K split), so a row's result does not depend on the other rows.
+  const bool inv = (flags & HQ_FLAG_BATCH_INVARIANT) != 0;
+  p.bn = inv ? kInvariantBn : m <= 64 ? std::max(16, cdiv(m, 16) * 16) : (m <= 128 ? 128 : (m <= 192 ? 192 : 256));
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
-  if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) p.bn = forced_bn;
+  if (!inv && forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) p.bn = forced_bn;
   p.cls = wna16_class(p.bn);
   p.m_tiles = cdiv(m, p.bn);
   p.tiles = p.m_tiles * L.n_tiles;
@@ -469,14 +494,13 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   return p;
 }
 
-// Tokens per expert tile, from the mean rows per expert: 16 (one tile of
-// the decode class per expert and n-tile) up to a mean of 16 rows, else 128.
-// Widths of 32 and 64 tokens were faster on GB300 (T = 256: 107 against
-// 160 us; T = 4096: 665 against 687 us) but gave intermittent wrong rows
-// in full-size MoE runs that are not yet explained, so the planner keeps to
-// the widths whose results have stayed exact.
+// Tokens per expert tile, from the mean rows per expert: 16 (the decode
+// class) up to a mean of 2 rows, 32 up to 32, 64 up to 384, else 128.  On
+// GB300 (E = 128, N = 1536, K = 2048, top-8) the wider tiles of the
+// two-K-block class beat 16-token tiles at T = 256 (107 against 160 us) and
+// 128-token tiles at T = 4096 (665 against 687 us).
 int moe_tile_bn(double mean_rows) {
-  int bn = mean_rows <= 16 ? 16 : 128;
+  int bn = mean_rows <= 2 ? 16 : mean_rows <= 32 ? 32 : mean_rows <= 384 ? 64 : 128;
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
   if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) bn = forced_bn;
   return bn;
@@ -507,7 +531,6 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, int x_r
   p.status = status;
   p.num_experts = L.num_experts; p.topk = topk;
   p.tile_offsets = tile_off; p.expert_offsets = exp_off; p.perm = perm; p.topk_w = topk_w; p.zbuf = zbuf;
-  p.x_rows = static_cast<const __nv_bfloat16*>(x); p.ldx = ldx;
   plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups);
   if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
   Wna16Launch l{};

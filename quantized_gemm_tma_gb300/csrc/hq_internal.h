@@ -48,6 +48,13 @@ constexpr uint32_t kHeaderBytes = 256;
 constexpr uint32_t kMagic = 0x31545148u;  // "HQT1"
 constexpr uint32_t kLayoutVersion = 1;
 
+// Head of every GEMM workspace: the status word region, then a fixed region
+// of split-K / stream-K counters (8 per tile, at most kMaxSplitTiles tiles),
+// then the fp32 partials.
+constexpr size_t kWsStatusBytes = 256;
+constexpr int kMaxSplitTiles = 512;
+constexpr size_t kWsCounterBytes = sizeof(int) * kMaxSplitTiles * 8;
+
 // Device-side header of a transformed weight.
 struct TileHeader {
   uint32_t magic;
@@ -122,8 +129,6 @@ struct GemmParams {
   const int* expert_offsets;// [E+1] row prefix
   const int* perm;          // [T*topk]
   const float* topk_w;      // [T*topk]
-  const __nv_bfloat16* x_rows;  // MoE: activations [T][ldx] (per-lane row gather)
-  int64_t ldx;
   float* zbuf;              // [T*topk][n_pad] weighted per-pair outputs
   int moe_direct;           // grouped forms: row f of Y (16-bit, ldy) instead of a weighted zbuf row
 };

@@ -13,7 +13,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (hq_gemm, hq_gemm_workspace_size, hq_transform, hq_transform_size, make_desc)
+from . import (hq_gemm, hq_gemm_workspace_size, hq_status_read, hq_transform, hq_transform_size,
+               hq_workspace_init, make_desc)
 
 _ELEM = {"bf16": 2, "fp16": 2, "fp8": 1}
 
@@ -23,7 +24,15 @@ def _cdiv(a: int, b: int) -> int:
 
 
 class QuantLinear:
-    """Y = a(X) . dequant(W)^T for one dense quantized weight W [n, k]."""
+    """Y = a(X) . dequant(W)^T for one dense quantized weight W [n, k].
+
+    The layer keeps one workspace (status word and split-K counters) for all
+    its calls, so calls of one layer must be ordered on one stream (or by
+    events); calls that overlap on the GPU race on it.  ``status()`` reads
+    the workspace's device status word and, when a device-side error was
+    recorded there, clears the whole workspace so that later calls start
+    from zeroed counters.
+    """
 
     def __init__(self, n: int, k: int, wtype: str, stype: str, group_k: int = 128, group_n: int = 1,
                  signed_codes: bool = True, has_zeros: bool = False, device="cuda"):
@@ -126,3 +135,15 @@ class QuantLinear:
         hq_gemm(desc, self.wt, m, atype, x, ldx, x_scales if atype == "fp8" else None, y, ldy, self._ws,
                 self._ws.numel(), flags, torch.cuda.current_stream(x.device))
         return y[:, :self.n]
+
+    def status(self, clear: bool = True) -> int:
+        """Synchronise the current stream and return the device status of the
+        last calls (0 = HQ_OK).  With ``clear``, a non-zero status resets the
+        workspace (status word and split-K counters) on the current stream."""
+        if self._ws is None:
+            return 0
+        s = torch.cuda.current_stream(self._ws.device)
+        st = hq_status_read(self._ws, clear=False, stream=s)
+        if st != 0 and clear:
+            hq_workspace_init(self._ws, self._ws.numel(), s)
+        return st

@@ -109,3 +109,30 @@ def run_moe(dw: DevWeight, acts, routing, ws: torch.Tensor | None = None, want_r
     if want_route:
         return out, st, offs.cpu().numpy(), perm[: t * topk].cpu().numpy()
     return out, st
+
+
+class tuning:
+    """Set HQ_FORCE_* switches for the duration of a ``with`` block (in this
+    process: the library re-reads them through hq_tuning_reload)."""
+
+    def __init__(self, **switches):
+        self.switches = {k: str(v) for k, v in switches.items()}
+        self.saved = {}
+
+    def __enter__(self):
+        import os
+        for k, v in self.switches.items():
+            self.saved[k] = os.environ.get(k)
+            os.environ[k] = v
+        hq.hq_tuning_reload()
+        return self
+
+    def __exit__(self, *exc):
+        import os
+        for k, v in self.saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+        hq.hq_tuning_reload()
+        return False

@@ -179,3 +179,15 @@ def test_selftest_timeout_host_validation(hq):
         with pytest.raises(hq.HQError) as ei:
             hq.hq_selftest_wait_timeout(ws)
         assert ei.value.status == want
+
+
+def test_noalloc_rejects_problems_beyond_the_scratch(hq):
+    """hq_gemm_noalloc refuses, on the host and before any device query or
+    launch, a problem whose workspace would exceed its fixed scratch."""
+    d = hq.make_desc("int4", "bf16", 16384, 16384, group_k=128, has_zeros=True, signed_codes=False)
+    assert hq.hq_gemm_workspace_size(d, 64, "bf16") > hq.HQ_NOALLOC_SCRATCH_BYTES
+    fake = 0x10000  # never dereferenced: the size check comes first
+    for flags in (0, hq.HQ_FLAG_NOALLOC_RESET):
+        with pytest.raises(hq.HQError) as ei:
+            hq.hq_gemm_noalloc(d, fake, 64, "bf16", fake, 16384, None, fake, 16384, flags, None, None)
+        assert ei.value.status == hq.HQ_ERR_WORKSPACE_TOO_SMALL

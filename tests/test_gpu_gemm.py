@@ -161,6 +161,7 @@ def test_workspace_reused_across_shapes():
 # ------------------------------------------------------------------ full size, sampled rows
 FULL = [
     ("c1_w4a16_sym_16x1024x1024", synth.dense_w4a16_sym, 16, 1024, 1024),
+    ("c1_w4a16_sym_1x1024x1024", synth.dense_w4a16_sym, 1, 1024, 1024),
     ("c2_w4a16_asym_m1", synth.dense_w4a16_asym, 1, 8192, 8192),
     ("c2_w4a16_asym_m16", synth.dense_w4a16_asym, 16, 8192, 8192),
     ("c2_w4a16_asym_m128", synth.dense_w4a16_asym, 128, 8192, 8192),
@@ -182,3 +183,93 @@ def test_full_size_sampled(idx):
     rng = np.random.default_rng(idx)
     rows = np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, size=min(m, 24))]))
     check(y[rows], _ref(qw, acts, rows), name)
+
+
+# ------------------------------------------------------------------ full size: class 1, batch invariance
+@pytest.fixture(scope="module")
+def c2_full():
+    """The asymmetric INT4 g128 weight at N = K = 8192 (the decode benchmark
+    shape) with 1024 activation rows, its transform, and its dequantised
+    values (float64) for the oracle."""
+    from gpu_helpers import DevWeight
+    qw, acts = synth.dense_w4a16_asym(0, 1024, 8192, 8192)
+    w = oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes, qw.scales, qw.zeros, qw.group_k, qw.signed, qw.stype,
+                          qw.num_experts)
+    return qw, acts, DevWeight(qw), w
+
+
+def _head(acts, m):
+    return synth.Activations(acts.atype, m, acts.k, acts.data[:m], None if acts.scales is None else acts.scales[:m])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("m", [32, 48, 64])
+def test_class1_full_size_every_split(c2_full, m):
+    """Tiles of 32..64 tokens (two K-blocks per stage, weight ring wrapped
+    many times) at N = K = 8192 under each work split: the 2-CTA cluster split
+    the planner picks, stream-K and whole tiles.  Three calls each, every one
+    bit-identical; sampled rows against the oracle."""
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import run_gemm, tuning
+    qw, acts, dw, w = c2_full
+    a = _head(acts, m)
+    rows = np.unique(np.concatenate([[0, m - 1], np.random.default_rng(m).integers(0, m, size=12)]))
+    ref = oracle.gemm_dense(oracle.decode_activations(a.atype, a.data)[rows], w)
+    for switches, split in (({}, 2), ({"HQ_FORCE_SPLITK": 1}, 0), ({"HQ_FORCE_SPLITK": 2}, 1)):
+        with tuning(**switches):
+            outs = [run_gemm(dw, a) for _ in range(3)]
+            plan = hq.hq_last_plan()
+        assert (plan["bn"], plan["tile_class"], plan["splits"]) == (m, 1, split), plan
+        assert plan["stages"] % 2 == 0, plan
+        check(outs[0][rows], ref, f"m={m} split={split}")
+        for i, y in enumerate(outs[1:], 1):
+            assert np.array_equal(y, outs[0]), f"m={m} split={split}: call {i} differs from call 0"
+
+
+INVARIANT_M = [1, 16, 17, 64, 128, 256, 1024]
+
+
+@pytest.mark.slow
+def test_batch_invariant_rows_bit_identical(c2_full):
+    """HQ_FLAG_BATCH_INVARIANT: rows 0..15 of X are the same at every M, the
+    other rows differ in number; rows 0..15 of Y are bit-identical at
+    M = 1, 16, 17, 64, 128, 256, 1024 (N = K = 8192, asymmetric INT4 g128),
+    and agree with the oracle."""
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import run_gemm
+    qw, acts, dw, w = c2_full
+    head = {}
+    for m in INVARIANT_M:
+        y = run_gemm(dw, _head(acts, m), flags=hq.HQ_FLAG_BATCH_INVARIANT)
+        p = hq.hq_last_plan()
+        assert (p["bn"], p["tile_class"], p["splits"]) == (64, 1, 1), (m, p)
+        head[m] = y[:16]
+    ref = oracle.gemm_dense(oracle.decode_activations(acts.atype, acts.data[:16]), w)
+    check(head[1024], ref, "batch-invariant rows 0..15")
+    for m in INVARIANT_M:
+        r = min(m, 16)
+        assert np.array_equal(head[m][:r], head[1024][:r]), f"M={m}: rows differ from M=1024"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("kind", ["int6_channel_fp16", "int4_sym_g32", "fp8_block"])
+def test_batch_invariant_other_formats(kind):
+    """The same row identity for INT6 channelwise (fp16), symmetric INT4 with
+    32-wide groups, and FP8 with block scales."""
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import DevWeight, run_gemm
+    if kind == "int6_channel_fp16":
+        qw, acts = synth.dense_int6_channel(60, 1024, 2048, 2048)
+        ms = INVARIANT_M
+    elif kind == "int4_sym_g32":
+        qw, acts = synth.dense_w4a16_sym(61, 1024, 1536, 2048, group_k=32)
+        ms = INVARIANT_M
+    else:
+        qw, acts = synth.dense_fp8_block(62, 1024, 2048, 3072)
+        ms = [1, 64, 130, 512, 1024]
+    dw = DevWeight(qw)
+    head = {m: run_gemm(dw, _head(acts, m), flags=hq.HQ_FLAG_BATCH_INVARIANT)[:16] for m in ms}
+    check(head[ms[-1]], _ref(qw, _head(acts, 16)), f"{kind} batch-invariant rows")
+    for m in ms:
+        r = min(m, 16)
+        assert np.array_equal(head[m][:r], head[ms[-1]][:r]), f"{kind} M={m}: rows differ"

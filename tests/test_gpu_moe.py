@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 import synth
-from tolerance import check
+from tolerance import check, check_ffn
 
 pytestmark = pytest.mark.gpu
 
@@ -178,15 +178,38 @@ def test_grouped_invalid_counts_set_status():
 
 # ------------------------------------------------------------------ feed-forward block
 def _expert_fn(qw):
-    """Dequantised expert weights as the MMA operand: a groupwise INT weight
-    with zero points enters as (q - z) * s rounded once to bf16 (the operand
-    rounding both GEMMs of the block apply); MXFP4 values are exact in bf16."""
+    """Expert weights [N, K] in float64, dequantised exactly (no operand rounding)."""
     def expert(e):
         z = None if qw.zeros is None else qw.zeros[e:e + 1]
-        w = oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes[e:e + 1], qw.scales[e:e + 1], z, qw.group_k,
-                              qw.signed, qw.stype, 1)[0]
-        return oracle.moe.round_bf16(w) if qw.zeros is not None else w
+        return oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes[e:e + 1], qw.scales[e:e + 1], z, qw.group_k,
+                                 qw.signed, qw.stype, 1)[0]
     return expert
+
+
+def _cached(fn):
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            cache[e] = fn(e)
+        return cache[e]
+    return get
+
+
+def _run_ffn(d13, d2, acts, r, n):
+    import torch
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import stream, to_dev, workspace
+    t, k = acts.m, acts.k
+    topk = r.topk_ids.shape[1]
+    ldy = -(-n // 8) * 8
+    y = torch.full((t, ldy), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = workspace(hq.hq_moe_ffn_workspace_size(d13.desc, d2.desc, t, topk))
+    hq.hq_moe_ffn(d13.desc, d13.wt, d2.desc, d2.wt, t, topk, to_dev(np.ascontiguousarray(r.topk_ids, np.int32)),
+                  to_dev(np.ascontiguousarray(r.topk_w, np.float32)), "bf16", to_dev(acts.data), k, y, ldy, ws,
+                  ws.numel(), 0, stream())
+    st = hq.hq_status_read(ws, clear=True, stream=stream())
+    return y[:, :n].double().cpu().numpy(), st
 
 
 FFN = [
@@ -198,9 +221,9 @@ FFN = [
 
 @pytest.mark.parametrize("idx", range(len(FFN)), ids=lambda i: "-".join(map(str, FFN[i][:2])))
 def test_moe_ffn_parity(idx):
-    import torch
-    import quantized_gemm_tma_gb300 as hq
-    from gpu_helpers import DevWeight, stream, to_dev, workspace
+    """The feed-forward block against the exact oracle (exact expert weights,
+    exact intermediates) at the block tolerance of two chained GEMMs."""
+    from gpu_helpers import DevWeight
     seed, wt, t, e, inter, k, n, topk = FFN[idx]
     rng = np.random.default_rng(seed)
     if wt == "mxfp4":
@@ -211,15 +234,78 @@ def test_moe_ffn_parity(idx):
         w2 = synth.quantize_int_groupwise(rng.standard_normal((e, n, inter)) * 0.02, 4, 64, False, "bf16")
         acts = synth.make_activations(rng, t, k, "bf16")
         r = synth.make_routing(rng, t, e, topk)
-    d13, d2 = DevWeight(w13), DevWeight(w2)
-    ldy = -(-n // 8) * 8
-    y = torch.full((t, ldy), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = workspace(hq.hq_moe_ffn_workspace_size(d13.desc, d2.desc, t, topk))
-    hq.hq_moe_ffn(d13.desc, d13.wt, d2.desc, d2.wt, t, topk, to_dev(np.ascontiguousarray(r.topk_ids, np.int32)),
-                  to_dev(np.ascontiguousarray(r.topk_w, np.float32)), "bf16", to_dev(acts.data), k, y, ldy, ws,
-                  ws.numel(), 0, stream())
-    assert hq.hq_status_read(ws, clear=True, stream=stream()) == 0
-    got = y[:, :n].double().cpu().numpy()
+    got, st = _run_ffn(DevWeight(w13), DevWeight(w2), acts, r, n)
+    assert st == 0
     ref = oracle.moe_ffn(oracle.decode_activations("bf16", acts.data), r.topk_ids, r.topk_w, _expert_fn(w13),
-                         _expert_fn(w2))
-    check(got, ref, f"moe ffn {FFN[idx]}")
+                         _expert_fn(w2), intermediate=None)
+    check_ffn(got, ref, f"moe ffn {FFN[idx]}")
+
+
+# ------------------------------------------------------------------ full size: every tile width, the FFN
+@pytest.fixture(scope="module")
+def moe_full():
+    """E = 128, N = 1536, K = 2048 MXFP4 gate+up experts, T = 4096 tokens of
+    activations and skewed top-8 routing (the T = 256 case takes the first
+    256 tokens), the transformed weight, and a caching expert dequantiser."""
+    from gpu_helpers import DevWeight
+    qw, acts, r = synth.moe_mxfp4(0, 4096)
+    return qw, acts, r, DevWeight(qw), _cached(_expert_fn(qw))
+
+
+def _first(acts, r, t):
+    return (synth.Activations(acts.atype, t, acts.k, acts.data[:t]),
+            synth.MoeRouting(r.topk_ids[:t], r.topk_w[:t], r.extra))
+
+
+_WIDTH_REFS = {}
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("bn", [16, 32, 48, 64, 128])
+def test_every_tile_width_full_size_repeated(moe_full, bn):
+    """Full-size MoE at every expert tile width the planner can choose (the
+    two-K-block stream dequantisers for 16..64 tokens, per-lane row gathers
+    for 32..128), T = 256 (every token checked) and T = 4096 (64 sampled
+    tokens).  Four calls each: every call bit-identical to the first (a
+    race shows up as a difference), the first against the oracle."""
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import run_moe, tuning
+    qw, acts, r, dw, expert = moe_full
+    for t in (256, 4096):
+        a, rt = _first(acts, r, t)
+        rows = np.arange(t) if t <= 256 else np.unique(np.concatenate(
+            [[0, t - 1], np.random.default_rng(t).integers(0, t, size=62)]))
+        if t not in _WIDTH_REFS:
+            _WIDTH_REFS[t] = oracle.moe_gemm(oracle.decode_activations("bf16", a.data)[rows], rt.topk_ids[rows],
+                                             rt.topk_w[rows], expert)
+        outs = []
+        with tuning(HQ_FORCE_BN=bn):
+            for _ in range(4):
+                y, st = run_moe(dw, a, rt)
+                assert st == 0, st
+                p = hq.hq_last_plan()
+                assert p["bn"] == bn, p
+                outs.append(y)
+        if p["tile_class"] <= 1:
+            assert p["stages"] % 2 == 0, p
+        check(outs[0][rows], _WIDTH_REFS[t], f"T={t} bn={bn}")
+        for i, y in enumerate(outs[1:], 1):
+            assert np.array_equal(y, outs[0]), f"T={t} bn={bn}: call {i} differs from call 0"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("tokens", [256, 4096])
+def test_moe_ffn_full_size_sampled(moe_full, tokens):
+    """The feed-forward block at the benchmark shape: the gate+up experts
+    above (I = 768), MXFP4 down experts [128][2048][768], 16 sampled tokens
+    against the exact oracle."""
+    from gpu_helpers import DevWeight
+    qw, acts, r, dw, expert = moe_full
+    w2, _, _ = synth.moe_mxfp4(1, 1, num_experts=128, n=2048, k=768)
+    a, rt = _first(acts, r, tokens)
+    got, st = _run_ffn(dw, DevWeight(w2), a, rt, 2048)
+    assert st == 0
+    rows = np.unique(np.concatenate([[0, tokens - 1], np.random.default_rng(tokens + 1).integers(0, tokens, 14)]))
+    ref = oracle.moe_ffn(oracle.decode_activations("bf16", a.data)[rows], rt.topk_ids[rows], rt.topk_w[rows], expert,
+                         _expert_fn(w2), intermediate=None)
+    check_ffn(got[rows], ref, f"moe ffn full size T={tokens}")

@@ -43,13 +43,20 @@ def test_dense_few_tiles_take_stream_k(hq):
     assert (p["splits"], p["grid"]) == (STREAM_K, 2), p
 
 
-def test_batch_invariant_never_splits_k(hq):
-    for m in (1, 16, 128, 1024):
+def test_batch_invariant_plans_one_configuration(hq):
+    """With the flag every M gets the same kernel configuration: 64-token
+    tiles of class 1, whole tiles (no stream-K, no cluster split); FP8 gets
+    128-row weight tiles and no split-K."""
+    plans = []
+    for m in (1, 16, 17, 64, 128, 256, 1024, 4096):
         p = hq.hq_plan_query(_int4(hq), m, "bf16", SMS, OPTIN, hq.HQ_FLAG_BATCH_INVARIANT)
-        assert p["splits"] == WHOLE, (m, p)
-    p = hq.hq_plan_query(hq.make_desc("fp8", "fp32", 4096, 7168, group_k=128, group_n=128), 64, "fp8", SMS, OPTIN,
-                         hq.HQ_FLAG_BATCH_INVARIANT)
-    assert p["splits"] == 1, p
+        assert (p["bn"], p["tile_class"], p["splits"]) == (64, 1, WHOLE), (m, p)
+        plans.append((p["stages"], p["groups"]))
+    assert len(set(plans)) == 1, plans
+    f8 = hq.make_desc("fp8", "fp32", 4096, 7168, group_k=128, group_n=128)
+    for m in (64, 512, 4096):
+        p = hq.hq_plan_query(f8, m, "fp8", SMS, OPTIN, hq.HQ_FLAG_BATCH_INVARIANT)
+        assert (p["bn"], p["splits"]) == (128, 1), (m, p)
 
 
 def test_single_k_block_is_never_split(hq):
@@ -107,13 +114,33 @@ def test_stage_override_switch(hq):
     assert default > 3
 
 
-@pytest.mark.parametrize("tokens,bn,cls", [(1, 16, 0), (16, 16, 0), (256, 16, 0), (257, 128, 2), (4096, 128, 2)])
+@pytest.mark.parametrize("tokens,bn,cls", [(1, 16, 0), (16, 16, 0), (32, 16, 0), (33, 32, 1), (256, 32, 1),
+                                           (512, 32, 1), (513, 64, 1), (4096, 64, 1), (6144, 64, 1),
+                                           (6145, 128, 2)])
 def test_moe_tile_width_from_mean_rows(hq, tokens, bn, cls):
-    """E = 128, top-8: 16-token expert tiles up to a mean of 16 routed rows per expert, then 128."""
+    """E = 128, top-8: expert tiles of 16 tokens up to a mean of 2 routed rows
+    per expert, 32 up to 32, 64 up to 384, else 128."""
     d = hq.make_desc("mxfp4", "ue8m0", 1536, 2048, num_experts=128, group_k=32)
     p = hq.hq_moe_plan_query(d, tokens, 8, SMS, OPTIN)
     assert (p["bn"], p["tile_class"], p["grid"], p["launches"]) == (bn, cls, SMS, 3), p
     assert p["stages"] >= 2
+    if p["tile_class"] <= 1:
+        assert p["stages"] % 2 == 0, p   # two K-blocks per stage: even weight ring
+
+
+@pytest.mark.parametrize("bn", [16, 32, 48, 64])
+def test_two_k_block_classes_plan_an_even_weight_ring(hq, bn):
+    """Stages of two K-blocks are split between dequantiser streams by stage
+    parity, so every weight-ring slot must keep one parity: the ring depth is
+    even for every tile width of classes 0 and 1, dense and MoE, with and
+    without zero points, for every format."""
+    descs = [_int4(hq), hq.make_desc("int4", "bf16", 8192, 8192, group_k=32, signed_codes=False, has_zeros=True),
+             hq.make_desc("int6", "fp16", 8192, 8192, group_k=0), hq.make_desc("mxfp4", "ue8m0", 1536, 2048,
+                                                                               group_k=32)]
+    for d in descs:
+        for optin in (OPTIN, 200 * 1024, 160 * 1024):
+            p = hq.hq_plan_query(d, bn, "fp16" if d.wtype == hq.HQ_W_INT6 else "bf16", SMS, optin)
+            assert p["bn"] == bn and p["tile_class"] <= 1 and p["stages"] % 2 == 0, (bn, optin, p)
 
 
 def test_moe_plan_query_validation(hq):
