@@ -274,7 +274,8 @@ hq_status hq_gemm_noalloc(const hq_weight_desc* wdesc, const void* w_t, int32_t 
 
 /*
  * hq_moe_workspace_size — workspace for hq_moe_gemm (status word, routing
- * counts and offsets, permutation, per-pair fp32 outputs).
+ * counts and offsets, permutation, per-pair fp32 outputs, and the routed
+ * activation rows in expert order: T*topk rows of K bf16).
  */
 hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int32_t topk,
                                 int32_t atype, size_t* bytes);
@@ -307,8 +308,9 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
 
 /*
  * hq_moe_ffn_workspace_size — workspace for hq_moe_ffn (status word, routing
- * offsets and permutation, the bf16 gate/up rows and activations of every
- * routed pair, and its fp32 weighted down-projection rows).
+ * offsets and permutation, the routed activation rows in expert order, the
+ * bf16 gate/up rows and activations of every routed pair, and its fp32
+ * weighted down-projection rows).
  */
 hq_status hq_moe_ffn_workspace_size(const hq_weight_desc* w13, const hq_weight_desc* w2, int32_t tokens,
                                     int32_t topk, size_t* bytes);
@@ -346,8 +348,8 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
 
 /*
  * hq_moe_grouped_workspace_size — workspace for hq_moe_grouped_gemm (status
- * word, compacted offsets and tile prefix, row map of up to E*rows (masked)
- * or rows (contiguous) entries).
+ * word, compacted offsets, tile prefix and each expert's first X row, row map
+ * of up to E*rows (masked) or rows (contiguous) entries).
  */
 hq_status hq_moe_grouped_workspace_size(const hq_weight_desc* desc, int32_t form, int32_t rows, size_t* bytes);
 
@@ -426,7 +428,8 @@ hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, i
  * hq_moe_plan_query — as hq_plan_query, for hq_moe_gemm with `tokens` tokens
  * routed to `topk` experts each: the expert tile width (tokens per tile, from
  * the mean routed rows per expert), its class, the ring stages and the grid
- * (one CTA per SM); launches = 3 (route, grouped GEMM, combine).  Host only.
+ * (one CTA per SM); launches = 4 (route, permute, grouped GEMM, combine).
+ * Host only.
  */
 hq_status hq_moe_plan_query(const hq_weight_desc* wdesc, int32_t tokens, int32_t topk, int32_t sms,
                             int64_t smem_optin, hq_plan_info* info);

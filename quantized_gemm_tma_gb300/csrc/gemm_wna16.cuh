@@ -278,6 +278,7 @@ __device__ __forceinline__ uint64_t weight_policy(const GemmParams& p) {
 // ---------------------------------------------------------------- work units
 struct Unit {
   int e, nt, mt, tile, row0, rows, kb0, kb1;
+  int xrow0;  // row of X (the tensor map's outer coordinate) of the unit's first token
 };
 
 // The CTA's list of units.  Every role walks the same list.
@@ -294,7 +295,9 @@ struct Sched {
     w = blockIdx.x;
   }
 
-  __device__ __forceinline__ bool next(const GemmParams& p, const int* s_tile_off, const int* s_row_off, Unit& u) {
+  // MoE: s_tabs holds the m-tile prefix [E+1], the row prefix [E+1] and the
+  // X row base of each expert [E], back to back in shared memory.
+  __device__ __forceinline__ bool next(const GemmParams& p, const int* s_tabs, Unit& u) {
     if constexpr (!MOE) {
       if (p.cluster == 2) {
         // one tile per 2-CTA cluster: rank 0 the lower half of K, rank 1 the rest
@@ -322,9 +325,13 @@ struct Sched {
       u.mt = u.tile / p.n_tiles;
       u.e = 0;
       u.row0 = u.mt * p.bn;
+      u.xrow0 = u.row0;
       u.rows = min(p.bn, p.m - u.row0);
       return true;
     } else {
+      const int* s_tile_off = s_tabs;
+      const int* s_row_off = s_tabs + p.num_experts + 1;
+      const int* s_xbase = s_row_off + p.num_experts + 1;
       const int total = s_tile_off[p.num_experts] * p.n_tiles;
       if (w >= total) return false;
       const int tile = w / p.n_tiles;
@@ -340,6 +347,7 @@ struct Sched {
       u.tile = w;
       u.row0 = s_row_off[lo] + u.mt * p.bn;
       u.rows = min(p.bn, s_row_off[lo + 1] - u.row0);
+      u.xrow0 = s_xbase[lo] + u.mt * p.bn;
       u.kb0 = 0;
       u.kb1 = p.k_tiles;
       w += gridDim.x;
@@ -407,13 +415,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   float* s_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16 +
                                             ((16u - (dev::smem_u32(tmem_slot) & 15u)) & 15u));
   float* s_red = s_scale + (CLS == 0 ? 2 * kSRing * kTileN : 0);  // cluster split: [128][16] fp32 (16-byte aligned)
-  int* s_tok = reinterpret_cast<int*>(s_red + (CLS == 0 ? kTileN * 16 : 0));  // MoE: token per row
-  int* s_tile_off = s_tok + (MOE ? BNMAX : 0);
-  int* s_row_off = s_tile_off + (MOE ? p.num_experts + 1 : 0);
+  // MoE: m-tile prefix [E+1], row prefix [E+1], X row base per expert [E]
+  int* s_tabs = reinterpret_cast<int*>(s_red + (CLS == 0 ? kTileN * 16 : 0));
+  int* s_tabs_end = s_tabs + (MOE ? 3 * p.num_experts + 2 : 0);
   // dense Y stores: per epilogue warp two staging boxes of 16 tokens x 32 rows
   // (16-bit), 128-byte aligned
   uint16_t* y_stage = reinterpret_cast<uint16_t*>(
-      reinterpret_cast<uint8_t*>(s_row_off) + ((128u - (dev::smem_u32(s_row_off) & 127u)) & 127u));
+      reinterpret_cast<uint8_t*>(s_tabs_end) + ((128u - (dev::smem_u32(s_tabs_end) & 127u)) & 127u));
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = dev::lane_id();
@@ -480,7 +488,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         sc.init(p);
         const uint64_t pol = weight_policy<MOE>(p);
         Unit u;
-        while (n_pre < SW && sc.next(p, s_tile_off, s_row_off, u)) {
+        while (n_pre < SW && sc.next(p, s_tabs, u)) {
           const uint8_t* wt = p.tiles + static_cast<uint64_t>(u.nt) * p.k_tiles * tile_bytes;
           for (int kb = u.kb0; kb < u.kb1 && n_pre < SW; kb += KPS, ++n_pre) {
             const uint32_t wbytes = static_cast<uint32_t>(min(KPS, u.kb1 - kb)) * tile_bytes;
@@ -497,9 +505,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   dev::grid_dep_launch();
   if (threadIdx.x == 0) HQ_TRACE_CTA(1);
   if constexpr (MOE) {
-    for (int i = threadIdx.x; i <= p.num_experts; i += blockDim.x) {
-      s_tile_off[i] = p.tile_offsets[i];
-      s_row_off[i] = p.expert_offsets[i];
+    const int E = p.num_experts;
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+      s_tabs[i] = p.tile_offsets[i];
+      s_tabs[E + 1 + i] = p.expert_offsets[i];
+      if (i < E) s_tabs[2 * E + 2 + i] = p.x_base[i];
     }
     __syncthreads();
   }
@@ -514,7 +524,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     const uint64_t pol = weight_policy<MOE>(p);
     [[maybe_unused]] int tr = 0;
     Unit u;
-    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+    while (ok && sc.next(p, s_tabs, u)) {
       const uint8_t* wt = p.tiles + static_cast<uint64_t>(u.e) * p.expert_stride +
                           static_cast<uint64_t>(u.nt) * p.k_tiles * tile_bytes;
       for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
@@ -554,12 +564,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     int issued = 0;
     bool ok = true;
     Unit u;
-    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
-      if constexpr (MOE) {
-        for (int r = static_cast<int>(lane); r < BNMAX; r += 32)
-          s_tok[r] = (r < u.rows) ? p.perm[u.row0 + r] / p.topk : p.m;  // p.m = T: out of range
-        __syncwarp();
-      }
+    while (ok && sc.next(p, s_tabs, u)) {
       for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
         const int cnt = min(KPS, u.kb1 - kb);
         if (!warp_wait(&x_empty[rg.s], rg.ph ^ 1u, abort_flag)) {
@@ -567,27 +572,19 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           break;
         }
         uint8_t* xs = x_st + rg.s * x_stage;
-        if (lane == 0) dev::mbar_arrive_expect_tx(&x_full[rg.s], 2u * cnt * slab);
-        if constexpr (MOE) {
-          // gathered rows, four per tensor copy (one-row boxes), the stage's
-          // copies dealt out over the lanes; rows past the unit (token index
-          // T) and columns past K are out of range and zero-filled
-          __syncwarp();
-          const int per_slab = bn >> 2;
-          for (int i = static_cast<int>(lane); i < 2 * cnt * per_slab; i += 32) {
-            const int z = i / per_slab, r = 4 * (i - z * per_slab);
-            dev::tma_gather4(xs + z * slab + r * 128, &tmap_x, &x_full[rg.s], (2 * kb + z) * 64, s_tok[r],
-                             s_tok[r + 1], s_tok[r + 2], s_tok[r + 3]);
-          }
-        } else if (lane == 0) {
-          // one 64-column slab of bn rows; columns past K and rows past M
-          // are zero-filled by the tensor copy
-          for (int z = 0; z < 2 * cnt; ++z) dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], (2 * kb + z) * 64, u.row0);
+        if (lane == 0) {
+          // one 64-column slab of bn rows per copy, from X row xrow0 on (MoE:
+          // the expert's rows stand together in X); columns past K and rows
+          // past the end of X are zero-filled by the tensor copy, and rows
+          // past the unit belong to other experts: their output columns are
+          // never stored
+          dev::mbar_arrive_expect_tx(&x_full[rg.s], 2u * cnt * slab);
+          for (int z = 0; z < 2 * cnt; ++z)
+            dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], (2 * kb + z) * 64, u.xrow0);
         }
         rg.next(SX);
         ++issued;
       }
-      if constexpr (MOE) __syncwarp();  // s_tok is rewritten for the next unit
     }
     if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
     if (lane == 0) {
@@ -616,7 +613,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       [[maybe_unused]] uint32_t cs0 = 0, cs1 = 0;  // streams: K-blocks taken from streams pidx, 2 + pidx
       [[maybe_unused]] uint32_t S = 0;           // streams: stage counter
       Unit u;
-      while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+      while (ok && sc.next(p, s_tabs, u)) {
         // whole-unit accumulator (double-buffered across units) unless promoting
         const int buf = DACC == 1 ? 0 : (ui & 1);
         if (!promote) {
@@ -764,7 +761,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       if (lane == 0) dev::mbar_arrive(&a_full[hs]);
     };
     Unit u;
-    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+    while (ok && sc.next(p, s_tabs, u)) {
       const int n = u.nt * kTileN + r;
       zrow = static_cast<uint32_t>(p.zero_sym);
       if (p.channel && p.has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
@@ -853,7 +850,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     [[maybe_unused]] int tr = 0, ts = 0;
     const bool trace_me = (dw % WG) == 0 && lane == 0;
     Unit u;
-    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+    while (ok && sc.next(p, s_tabs, u)) {
       const int n = u.nt * kTileN + r;
       uint32_t zrow = static_cast<uint32_t>(p.zero_sym);
       if (p.channel && p.has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
@@ -978,7 +975,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     // INT4 bf16 operands without a folded scale carry an extra 2^-7
     constexpr float kOpFix = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
     Unit u;
-    while (ok && sc.next(p, s_tile_off, s_row_off, u)) {
+    while (ok && sc.next(p, s_tabs, u)) {
       const int n = u.nt * kTileN + r;
       const bool n_ok = n < p.n;
       const float rs = (p.channel && n_ok) ? p.row_scale[static_cast<size_t>(u.e) * p.n_pad + n] * kOpFix : 1.f;
@@ -999,7 +996,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
 #pragma unroll
         for (int k = 0; k < kMoeRegs; ++k) {
           const int col = 32 * k + static_cast<int>(lane);
-          w_reg[k] = (col < u.rows && !p.moe_direct) ? p.topk_w[f_reg[k]] : 0.f;
+          w_reg[k] = (col < u.rows && p.moe_out == kMoeOutZ) ? p.topk_w[f_reg[k]] : 0.f;
         }
       }
       // columns [16 ch, 16 ch + 16) of this row: partial, MoE row or Y
@@ -1079,8 +1076,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             const int f = __shfl_sync(0xffffffffu, fr, ((ch & 1) << 4) + i);
             const float wf = __shfl_sync(0xffffffffu, wr, ((ch & 1) << 4) + i);
             if (col < u.rows && n_ok) {
-              if (p.moe_direct) {  // grouped forms: Y row f directly, 16-bit
-                const size_t off = static_cast<size_t>(f) * p.ldy + n;
+              if (p.moe_out != kMoeOutZ) {  // a 16-bit Y row: f (grouped forms) or the routed position
+                const size_t row = p.moe_out == kMoeOutRowMap ? static_cast<size_t>(f)
+                                                               : static_cast<size_t>(u.row0 + col);
+                const size_t off = row * p.ldy + n;
                 if constexpr (BF16) reinterpret_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(v[i] * rs);
                 else reinterpret_cast<__half*>(p.y)[off] = __float2half_rn(v[i] * rs);
               } else {
@@ -1353,7 +1352,7 @@ inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int 
       (2u * w_stages + 2u * x_stages + 2u * (C::kKps == 2 ? kABars : kASlots) + 2u * C::kDacc + 1u + 2u * kKRing +
        2u * kSRing + 1u) * 8u + 16u;
   const uint32_t scales = CLS == 0 ? 4u * 2u * kSRing * kTileN + 4u * kTileN * 16u : 0u;
-  const uint32_t moe = 4u * (C::kBnMax + 2u * (num_experts + 1));
+  const uint32_t moe = num_experts ? 4u * (3u * num_experts + 2u) : 0u;
   const uint32_t ystage = num_experts == 0 ? kEpiWarps * 2u * 16u * 32u * 2u + 128u : 0u;  // dense Y boxes
   return w + x + bars + scales + moe + ystage + 1024u /* alignment slack */;
 }

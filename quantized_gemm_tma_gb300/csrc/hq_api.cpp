@@ -494,25 +494,29 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   return p;
 }
 
-// Tokens per expert tile, from the mean rows per expert: 16 (the decode
-// class) up to a mean of 2 rows, 32 up to 32, 64 up to 384, else 128.  On
-// GB300 (E = 128, N = 1536, K = 2048, top-8) the wider tiles of the
-// two-K-block class beat 16-token tiles at T = 256 (107 against 160 us) and
-// 128-token tiles at T = 4096 (665 against 687 us).
+// Tokens per expert tile, from the mean routed rows per expert: 16 (the
+// decode class) up to a mean of 1 row, 32 up to 8, 64 up to 64, else 128.
+// Measured on GB300 (E = 128, N = 1536, K = 2048, top-8, µs per call for
+// tiles of 16 / 32 / 64 / 128 / 256 tokens): T = 16 48.1 / 47.4 / 48.8 /
+// 61.2 / 99.7, T = 256 121.8 / 89.5 / 86.2 / 106.2 / 190.6, T = 4096
+// 1166 / 647 / 428 / 375 / 521.
 int moe_tile_bn(double mean_rows) {
-  int bn = mean_rows <= 2 ? 16 : mean_rows <= 32 ? 32 : mean_rows <= 384 ? 64 : 128;
+  int bn = mean_rows <= 1 ? 16 : mean_rows <= 8 ? 32 : mean_rows <= 64 ? 64 : 128;
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
   if (forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) bn = forced_bn;
   return bn;
 }
 
-// The grouped WnA16 GEMM over routed rows whose offsets, m-tile prefix and row
-// map are already in the workspace.  Row p of expert e's group reads X row
-// perm[p] / topk and writes either the weighted fp32 row zbuf[perm[p]]
-// (indexed form, combined afterwards) or Y row perm[p] directly (grouped forms).
-hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, int x_rows, int topk, const float* topk_w,
-                             const void* x, int64_t ldx, void* y, int64_t ldy, const int* exp_off,
-                             const int* tile_off, const int* perm, float* zbuf, int* status, bool direct,
+// The grouped WnA16 GEMM over routed rows whose offsets, m-tile prefix, row
+// map and X row bases are already in the workspace.  The routed rows of expert
+// e stand together in X from row x_base[e] on (the permuted activations of the
+// indexed form, the caller's rows of the grouped forms); each unit loads whole
+// tiles of them.  Routed position p of expert e's group writes, by `out`: the
+// weighted fp32 row zbuf[perm[p]] (indexed form, combined afterwards), the
+// 16-bit Y row perm[p] (grouped forms), or the 16-bit Y row p (routed order).
+hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const void* x, int64_t ldx, int x_rows,
+                             const int* x_base, int out, const float* topk_w, void* y, int64_t ldy,
+                             const int* exp_off, const int* tile_off, const int* perm, float* zbuf, int* status,
                              const DevInfo& di, cudaStream_t s, int* stages, int* groups) {
   const int cls = wna16_class(bn);
   GemmParams p{};
@@ -527,10 +531,11 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, int x_r
   p.bn = bn; p.m_tiles = 0; p.num_tiles = 0; p.stream_k = 0; p.iters = 0; p.cluster = 1;
   p.promote = (cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
   p.idesc = idesc_f16(true, 128, bn);
-  p.y = y; p.ldy = ldy; p.moe_direct = direct ? 1 : 0;
+  p.y = y; p.ldy = ldy; p.moe_out = out;
   p.status = status;
-  p.num_experts = L.num_experts; p.topk = topk;
+  p.num_experts = L.num_experts; p.topk = 1;
   p.tile_offsets = tile_off; p.expert_offsets = exp_off; p.perm = perm; p.topk_w = topk_w; p.zbuf = zbuf;
+  p.x_base = x_base;
   plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups);
   if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
   Wna16Launch l{};
@@ -540,9 +545,9 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, int x_r
   l.moe = true;
   l.grid = di.sms;
   l.smem = wna16_smem_bytes(cls, p.stages, p.x_stages, L.tile_bytes, bn, L.num_experts);
-  // X [rows][K] gathered by row index: one-row boxes of 64 columns (four rows per copy)
+  // X [x_rows][K]: one box = 64 columns (128 bytes, swizzled) of bn rows
   Wna16Maps maps;
-  hq_status st = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, x_rows, ldx, 64, 1);
+  hq_status st = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, x_rows, ldx, 64, bn);
   if (st != HQ_OK) return st;
   maps.y = maps.x;  // MoE output rows use plain stores
   if (launch_wna16(l, p, maps, s) != cudaSuccess) return HQ_ERR_CUDA;
@@ -550,6 +555,10 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, int x_r
   *groups = p.groups;
   return HQ_OK;
 }
+
+// Row pitch (elements) of the permuted activations: K rounded up to 8 bf16
+// (16 bytes, the tensor-map stride rule).
+inline int64_t permuted_ld(int k) { return (static_cast<int64_t>(k) + 7) / 8 * 8; }
 
 }  // namespace
 }  // namespace hq
@@ -751,7 +760,7 @@ hq_status hq_moe_plan_query(const hq_weight_desc* wdesc, int32_t tokens, int32_t
   int stages = 0, x_stages = 0, groups = 0;
   plan_stages(cls, L, bn, L.num_experts, static_cast<size_t>(smem_optin), &stages, &x_stages, &groups);
   if (stages < 2) return HQ_ERR_UNSUPPORTED;
-  *info = hq_plan_info{bn, 1, sms, 3, stages, cls, groups, 0};
+  *info = hq_plan_info{bn, 1, sms, 4, stages, cls, groups, 0};
   return HQ_OK;
 }
 
@@ -768,6 +777,7 @@ hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int3
   ws += 2 * align_up(sizeof(int) * (L.num_experts + 1), kAlign);
   ws += align_up(sizeof(int) * std::max<size_t>(pairs, 1), kAlign);
   ws += align_up(sizeof(float) * pairs * L.n_pad, kAlign);
+  ws += align_up(2 * pairs * static_cast<size_t>(permuted_ld(L.k)), kAlign);  // permuted activations, bf16
   *bytes = ws;
   return HQ_OK;
 }
@@ -811,18 +821,24 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   int* perm = reinterpret_cast<int*>(ws + off);
   off += align_up(sizeof(int) * std::max<int64_t>(pairs, 1), kAlign);
   float* zbuf = reinterpret_cast<float*>(ws + off);
+  off += align_up(sizeof(float) * static_cast<size_t>(pairs) * L.n_pad, kAlign);
+  void* xg = ws + off;  // the routed activation rows in expert order
+  const int64_t ldg = permuted_ld(L.k);
 
   const int bn = moe_tile_bn(static_cast<double>(pairs) / L.num_experts);
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L.num_experts, bn, exp_off, tile_off, perm,
                        expert_offsets_out, perm_out, reinterpret_cast<int*>(ws), s) != cudaSuccess)
     return HQ_ERR_CUDA;
+  if (launch_moe_permute(x, ldx, tokens, perm, exp_off + L.num_experts, static_cast<int>(pairs), topk, L.k, xg, ldg,
+                         di.sms, s) != cudaSuccess)
+    return HQ_ERR_CUDA;
   int stages = 0, groups = 0;
-  st = launch_moe_grouped(L, wt, bn, tokens, topk, topk_w, x, ldx, y, ldy, exp_off, tile_off, perm, zbuf,
-                          reinterpret_cast<int*>(ws), false, di, s, &stages, &groups);
+  st = launch_moe_grouped(L, wt, bn, xg, ldg, static_cast<int>(pairs), exp_off, kMoeOutZ, topk_w, y, ldy, exp_off,
+                          tile_off, perm, zbuf, reinterpret_cast<int*>(ws), di, s, &stages, &groups);
   if (st != HQ_OK) return st;
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L.num_experts, L.n, L.n_pad, y, ldy, true, s) != cudaSuccess)
     return HQ_ERR_CUDA;
-  g_last_plan = hq_plan_info{bn, 1, di.sms, 3, stages, wna16_class(bn), groups, 0};
+  g_last_plan = hq_plan_info{bn, 1, di.sms, 4, stages, wna16_class(bn), groups, 0};
   return HQ_OK;
 }
 
@@ -857,6 +873,7 @@ hq_status hq_moe_ffn_workspace_size(const hq_weight_desc* w13, const hq_weight_d
   ws += align_up(2 * pairs * ldh, kAlign);             // H: gate and up, bf16
   ws += align_up(2 * pairs * lda, kAlign);             // A: silu(gate) * up, bf16
   ws += align_up(sizeof(float) * pairs * L2.n_pad, kAlign);  // weighted down-projection rows
+  ws += align_up(2 * pairs * static_cast<size_t>(permuted_ld(L13.k)), kAlign);  // permuted activations, bf16
   *bytes = ws;
   return HQ_OK;
 }
@@ -911,25 +928,32 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
   void* abuf = ws + off;
   off += align_up(2 * static_cast<size_t>(pairs) * lda, kAlign);
   float* zbuf = reinterpret_cast<float*>(ws + off);
+  off += align_up(sizeof(float) * static_cast<size_t>(pairs) * L2.n_pad, kAlign);
+  void* xg = ws + off;  // the routed activation rows in expert order
+  const int64_t ldg = permuted_ld(L13.k);
   const int bn = moe_tile_bn(static_cast<double>(pairs) / L13.num_experts);
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L13.num_experts, bn, exp_off, tile_off, perm, nullptr,
                        nullptr, reinterpret_cast<int*>(ws), s) != cudaSuccess)
     return HQ_ERR_CUDA;
+  if (launch_moe_permute(x, ldx, tokens, perm, exp_off + L13.num_experts, static_cast<int>(pairs), topk, L13.k, xg,
+                         ldg, di.sms, s) != cudaSuccess)
+    return HQ_ERR_CUDA;
   int stages = 0, groups = 0;
-  // gate+up: H[f] = X[t] . W13_e^T, written at pair row f
-  st = launch_moe_grouped(L13, static_cast<const uint8_t*>(w13_t), bn, tokens, topk, nullptr, x, ldx, hbuf, ldh,
-                          exp_off, tile_off, perm, nullptr, reinterpret_cast<int*>(ws), true, di, s, &stages, &groups);
+  // gate+up: H[p] = Xg[p] . W13_e^T, in routed order
+  st = launch_moe_grouped(L13, static_cast<const uint8_t*>(w13_t), bn, xg, ldg, static_cast<int>(pairs), exp_off,
+                          kMoeOutRouted, nullptr, hbuf, ldh, exp_off, tile_off, perm, nullptr,
+                          reinterpret_cast<int*>(ws), di, s, &stages, &groups);
   if (st != HQ_OK) return st;
   if (launch_moe_act(hbuf, ldh, static_cast<int>(pairs), inter, abuf, lda, s) != cudaSuccess) return HQ_ERR_CUDA;
-  // down: Z[f] = topk_w[f] * A[f] . W2_e^T (rows gathered by pair index)
-  st = launch_moe_grouped(L2, static_cast<const uint8_t*>(w2_t), bn, static_cast<int>(pairs), 1, topk_w, abuf, lda,
-                          y, ldy, exp_off, tile_off, perm, zbuf, reinterpret_cast<int*>(ws), false, di, s, &stages,
-                          &groups);
+  // down: Z[perm[p]] = topk_w[perm[p]] * A[p] . W2_e^T (A in routed order)
+  st = launch_moe_grouped(L2, static_cast<const uint8_t*>(w2_t), bn, abuf, lda, static_cast<int>(pairs), exp_off,
+                          kMoeOutZ, topk_w, y, ldy, exp_off, tile_off, perm, zbuf, reinterpret_cast<int*>(ws), di, s,
+                          &stages, &groups);
   if (st != HQ_OK) return st;
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L2.num_experts, L2.n, L2.n_pad, y, ldy, true, s) !=
       cudaSuccess)
     return HQ_ERR_CUDA;
-  g_last_plan = hq_plan_info{bn, 1, di.sms, 5, stages, wna16_class(bn), groups, 0};
+  g_last_plan = hq_plan_info{bn, 1, di.sms, 6, stages, wna16_class(bn), groups, 0};
   return HQ_OK;
 }
 
@@ -941,7 +965,7 @@ hq_status hq_moe_grouped_workspace_size(const hq_weight_desc* desc, int32_t form
   if (st != HQ_OK) return st;
   const int64_t x_rows = form == HQ_MOE_GROUPED_MASKED ? static_cast<int64_t>(rows) * L.num_experts : rows;
   size_t ws = kAlign;
-  ws += 2 * align_up(sizeof(int) * (L.num_experts + 1), kAlign);
+  ws += 3 * align_up(sizeof(int) * (L.num_experts + 1), kAlign);
   ws += align_up(sizeof(int) * std::max<int64_t>(x_rows, 1), kAlign);
   *bytes = ws;
   return HQ_OK;
@@ -985,6 +1009,8 @@ hq_status hq_moe_grouped_gemm(const hq_weight_desc* wdesc, const void* w_t, int3
   off += align_up(sizeof(int) * (L.num_experts + 1), kAlign);
   int* tile_off = reinterpret_cast<int*>(ws + off);
   off += align_up(sizeof(int) * (L.num_experts + 1), kAlign);
+  int* x_base = reinterpret_cast<int*>(ws + off);
+  off += align_up(sizeof(int) * (L.num_experts + 1), kAlign);
   int* perm = reinterpret_cast<int*>(ws + off);
   // tile width from the caller's expected rows per expert (the counts stay on
   // the device), else from the mean that fills the given rows
@@ -992,12 +1018,12 @@ hq_status hq_moe_grouped_gemm(const hq_weight_desc* wdesc, const void* w_t, int3
                            : masked          ? static_cast<double>(rows)
                                              : static_cast<double>(rows) / L.num_experts;
   const int bn = moe_tile_bn(mean_rows);
-  if (launch_moe_grouped_route(expert_rows, masked, rows, L.num_experts, bn, exp_off, tile_off, perm,
+  if (launch_moe_grouped_route(expert_rows, masked, rows, L.num_experts, bn, exp_off, tile_off, perm, x_base,
                                reinterpret_cast<int*>(ws), s) != cudaSuccess)
     return HQ_ERR_CUDA;
   int stages = 0, groups = 0;
-  st = launch_moe_grouped(L, wt, bn, static_cast<int>(x_rows), 1, nullptr, x, ldx, y, ldy, exp_off, tile_off, perm,
-                          nullptr, reinterpret_cast<int*>(ws), true, di, s, &stages, &groups);
+  st = launch_moe_grouped(L, wt, bn, x, ldx, static_cast<int>(x_rows), x_base, kMoeOutRowMap, nullptr, y, ldy,
+                          exp_off, tile_off, perm, nullptr, reinterpret_cast<int*>(ws), di, s, &stages, &groups);
   if (st != HQ_OK) return st;
   g_last_plan = hq_plan_info{bn, 1, di.sms, 2, stages, wna16_class(bn), groups, 0};
   return HQ_OK;

@@ -127,11 +127,17 @@ struct GemmParams {
   int num_experts, topk;
   const int* tile_offsets;  // [E+1] m-tile prefix over experts
   const int* expert_offsets;// [E+1] row prefix
-  const int* perm;          // [T*topk]
+  const int* perm;          // [rows]: routed position -> pair index f (indexed) or X/Y row (grouped forms)
   const float* topk_w;      // [T*topk]
+  const int* x_base;        // [E]: X row of each expert's first routed row (its rows stand together in X)
   float* zbuf;              // [T*topk][n_pad] weighted per-pair outputs
-  int moe_direct;           // grouped forms: row f of Y (16-bit, ldy) instead of a weighted zbuf row
+  int moe_out;              // kMoeOutZ, kMoeOutRowMap or kMoeOutRouted
 };
+
+// MoE output modes: the weighted fp32 row zbuf[perm[p]] (combined afterwards),
+// the 16-bit Y row perm[p] (grouped forms), or the 16-bit Y row p itself
+// (rows in routed order, the feed-forward block's gate+up output).
+constexpr int kMoeOutZ = 0, kMoeOutRowMap = 1, kMoeOutRouted = 2;
 
 struct Fp8Params {
   const uint8_t* tiles;

@@ -78,8 +78,12 @@ cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, in
                              int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* status,
                              cudaStream_t stream);
 cudaError_t launch_moe_grouped_route(const int* rows_in, bool masked, int rows, int num_experts, int bn,
-                                     int* expert_offsets, int* tile_offsets, int* perm, int* status,
+                                     int* expert_offsets, int* tile_offsets, int* perm, int* x_base, int* status,
                                      cudaStream_t stream);
+// Xg[p][:k] = X[perm[p] / topk][:k] for p < *routed (a device count of at
+// most `pairs`); bf16, k, ldx and ldg multiples of 8
+cudaError_t launch_moe_permute(const void* x, int64_t ldx, int tokens, const int* perm, const int* routed,
+                               int pairs, int topk, int k, void* xg, int64_t ldg, int sms, cudaStream_t stream);
 cudaError_t launch_moe_act(const void* h, int64_t ldh, int pairs, int inter, void* a, int64_t lda,
                            cudaStream_t stream);
 cudaError_t launch_moe_combine(const float* zbuf, const int* topk_ids, int tokens, int topk, int num_experts, int n,

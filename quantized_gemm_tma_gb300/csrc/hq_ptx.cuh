@@ -187,18 +187,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, ui
       : "memory");
 }
 
-// Gather four rows (y0..y3) of one 64-element-wide column slab starting at x
-// into four consecutive 128-byte rows of shared memory; the map's box is one
-// row high.  Out-of-range rows and columns are zero-filled.
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-      "%4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
-      "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
-      : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -10,12 +10,18 @@
 //          the prefix of m-tiles per expert for the grouped GEMM scheduler.
 // combine: Y[t, :] = sum_j Z[t*topk + j, :] in slot order (Z already carries
 //          the routing weight), rounded once to bf16.
+// permute: the routed activation rows in expert order (the grouped-contiguous
+//          organisation of an indexed input): Xg[p, :] = X[perm[p] / topk, :],
+//          so that the grouped GEMM loads whole tiles of an expert's rows.
 // grouped: the grouped-contiguous and grouped-masked input forms (rows per
-//          expert given by the caller): offsets, tile prefix and row map.
+//          expert given by the caller): offsets, tile prefix, row map and the
+//          X row where each expert's rows start.
 // act:     silu(gate) * up between the gate+up and down GEMMs of the MoE
 //          feed-forward block.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "hq_internal.h"
 #include "hq_launch.h"
@@ -154,7 +160,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 __global__ void __launch_bounds__(kRouteThreads, 1)
     moe_grouped_route_kernel(const int* __restrict__ rows_in, int masked, int rows, int num_experts, int bn,
                              int* __restrict__ exp_off, int* __restrict__ tile_off, int* __restrict__ perm,
-                             int* __restrict__ status) {
+                             int* __restrict__ x_base, int* __restrict__ status) {
   __shared__ int warp_tot[33];
   __shared__ int s_off[kRouteThreads];
   __shared__ int s_base[kRouteThreads];
@@ -186,6 +192,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   if (tid < E) {
     exp_off[tid] = row_base;
     tile_off[tid] = tile_base;
+    x_base[tid] = base;
     s_off[tid] = row_base;
     s_base[tid] = base;
   }
@@ -197,6 +204,24 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   for (int e = warp; e < E; e += kRouteWarps) {
     const int o = s_off[e], b = s_base[e], c = (e + 1 < E ? s_off[e + 1] : rows_total) - o;
     for (int r = lane; r < c; r += 32) perm[o + r] = b + r;
+  }
+}
+
+// Xg[p, :] = X[perm[p] / topk, :] for the routed positions p < *routed (the
+// route's row total: pairs with an invalid expert id are not routed), K bf16
+// values per row (K a multiple of 8): one thread per 16-byte chunk, rows of X
+// read through L2 (each token's row serves its topk pairs), Xg written once.
+__global__ void moe_permute_kernel(const uint4* __restrict__ x, int64_t ldx16, int tokens,
+                                   const int* __restrict__ perm, const int* __restrict__ routed, int topk,
+                                   int chunks, uint4* __restrict__ xg, int64_t ldg16) {
+  const int64_t total = static_cast<int64_t>(*routed) * chunks;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t p = i / chunks;
+    const int c = static_cast<int>(i - p * chunks);
+    const int t = perm[p] / topk;
+    if (t < 0 || t >= tokens) continue;
+    xg[p * ldg16 + c] = __ldg(x + t * ldx16 + c);
   }
 }
 
@@ -272,11 +297,25 @@ cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, in
 }
 
 cudaError_t launch_moe_grouped_route(const int* rows_in, bool masked, int rows, int num_experts, int bn,
-                                     int* expert_offsets, int* tile_offsets, int* perm, int* status,
+                                     int* expert_offsets, int* tile_offsets, int* perm, int* x_base, int* status,
                                      cudaStream_t stream) {
   if (num_experts > kRouteThreads) return cudaErrorInvalidValue;
   moe_grouped_route_kernel<<<1, kRouteThreads, 0, stream>>>(rows_in, masked ? 1 : 0, rows, num_experts, bn,
-                                                             expert_offsets, tile_offsets, perm, status);
+                                                             expert_offsets, tile_offsets, perm, x_base, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_permute(const void* x, int64_t ldx, int tokens, const int* perm, const int* routed,
+                               int pairs, int topk, int k, void* xg, int64_t ldg, int sms, cudaStream_t stream) {
+  if (pairs == 0) return cudaSuccess;
+  if (k % 8 || ldx % 8 || ldg % 8) return cudaErrorInvalidValue;
+  const int chunks = k / 8;
+  const int64_t total = static_cast<int64_t>(pairs) * chunks;  // at most this many routed chunks
+  const int block = 256;
+  const int64_t want = (total + block - 1) / block;
+  const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sms) * 8));
+  moe_permute_kernel<<<grid, block, 0, stream>>>(static_cast<const uint4*>(x), ldx / 8, tokens, perm, routed, topk,
+                                                 chunks, static_cast<uint4*>(xg), ldg / 8);
   return cudaGetLastError();
 }
 

@@ -114,15 +114,14 @@ def test_stage_override_switch(hq):
     assert default > 3
 
 
-@pytest.mark.parametrize("tokens,bn,cls", [(1, 16, 0), (16, 16, 0), (32, 16, 0), (33, 32, 1), (256, 32, 1),
-                                           (512, 32, 1), (513, 64, 1), (4096, 64, 1), (6144, 64, 1),
-                                           (6145, 128, 2)])
+@pytest.mark.parametrize("tokens,bn,cls", [(1, 16, 0), (16, 16, 0), (17, 32, 1), (128, 32, 1), (129, 64, 1),
+                                           (256, 64, 1), (1024, 64, 1), (1025, 128, 2), (4096, 128, 2)])
 def test_moe_tile_width_from_mean_rows(hq, tokens, bn, cls):
-    """E = 128, top-8: expert tiles of 16 tokens up to a mean of 2 routed rows
-    per expert, 32 up to 32, 64 up to 384, else 128."""
+    """E = 128, top-8: expert tiles of 16 tokens up to a mean of 1 routed row
+    per expert, 32 up to 8, 64 up to 64, else 128."""
     d = hq.make_desc("mxfp4", "ue8m0", 1536, 2048, num_experts=128, group_k=32)
     p = hq.hq_moe_plan_query(d, tokens, 8, SMS, OPTIN)
-    assert (p["bn"], p["tile_class"], p["grid"], p["launches"]) == (bn, cls, SMS, 3), p
+    assert (p["bn"], p["tile_class"], p["grid"], p["launches"]) == (bn, cls, SMS, 4), p
     assert p["stages"] >= 2
     if p["tile_class"] <= 1:
         assert p["stages"] % 2 == 0, p   # two K-blocks per stage: even weight ring
