@@ -53,6 +53,20 @@ X_COPIES = 4       # rotated activation copies per M
 MOE_COPIES = 2     # rotated MoE expert sets (213 MB each)
 MOE_H = MOE_K      # feed-forward block: down projection [E][hidden = K][intermediate = N / 2]
 HEAD_START_CYCLES = 200_000_000
+# The other dense configurations, timed the same way as the sweep (extra keys
+# of the JSON line): INT6 channelwise with fp16 activations at M = 128, and
+# FP8 e4m3 with 128 x 128 block scales at M in {64, 512, 4096}.
+EXTRA = {
+    "c3_int6_channel_fp16": {"n": 8192, "k": 8192, "ms": [128], "copies": 4,
+                             "workload": "dense INT6 channelwise symmetric (fp16 row scales), fp16 activations, "
+                                         "N=K=8192, M=128"},
+    "c4_fp8_block": {"n": 4096, "k": 7168, "ms": [64, 512, 4096], "copies": 6,
+                     "workload": "dense W8A8 FP8: e4m3 weights with fp32 128x128 block scales, e4m3 activations "
+                                 "with per-token per-128-K fp32 scales, N=4096, K=7168, M sweep {64,512,4096}"},
+}
+# FP8 dense peak: the measured bf16 peak times 2, the nominal fp8:bf16 ratio of
+# the tensor cores (4.5 : 2.25 PFLOP/s dense)
+FP8_PER_BF16 = 2.0
 BLOCK = 25         # back-to-back calls of one shape between two events
 # DRAM bytes (read + write) per launch of the WnA16 INT4 kernel, from the ncu
 # traffic capture listed in profiles/wna16_int4_asym_g128_n8192_k8192.md,
@@ -69,6 +83,16 @@ def dense_bytes(m: int) -> int:
 
 def dense_flops(m: int) -> int:
     return 2 * m * N * K
+
+
+def extra_bytes(name: str, m: int) -> int:
+    """Algorithmic bytes of one call of an extra configuration (output excluded)."""
+    cfg = EXTRA[name]
+    n, k = cfg["n"], cfg["k"]
+    if name.startswith("c3"):   # 6-bit codes, fp16 row scales, fp16 activations
+        return n * k * 3 // 4 + n * 2 + m * k * 2
+    kb = -(-k // 128)           # e4m3 weights, fp32 block scales, e4m3 activations, fp32 per-token scales
+    return n * k + (-(-n // 128)) * kb * 4 + m * k + m * kb * 4
 
 
 def ncu_traffic(m: int):
@@ -241,7 +265,52 @@ def run_gpu(args, rank: int, world: int):
         xh[m] = torch.from_numpy(xb.view(np.int16)).pin_memory()
         yh[m] = torch.empty((m, N), dtype=torch.bfloat16).pin_memory()
     launches = {"n": 0}
-    rot = {"w": 0, "x": 0, "moe": 0}
+    rot = {"w": 0, "x": 0, "moe": 0, "extra": 0}
+
+    # ---- the other dense configurations (weights rotated over copies > L2)
+    extra = {}
+    if not args.no_extra:
+        for name, cfg in EXTRA.items():
+            n_, k_ = cfg["n"], cfg["k"]
+            if name.startswith("c3"):
+                eq, _ = synth.dense_int6_channel(0, 1, n_, k_)
+                atype = "fp16"
+                edesc = hq.make_desc("int6", "fp16", n_, k_, 1, 0, 1, True, False, to_dev(eq.codes),
+                                     to_dev(eq.scales), None)
+            else:
+                eq, _ = synth.dense_fp8_block(0, 1, n_, k_)
+                atype = "fp8"
+                edesc = hq.make_desc("fp8", "fp32", n_, k_, 1, 128, 128, True, False, to_dev(eq.codes),
+                                     to_dev(eq.scales), None)
+            nb = hq.hq_transform_size(edesc)
+            ewts = []
+            for _ in range(cfg["copies"]):
+                w = torch.empty(nb, dtype=torch.uint8, device=dev)
+                hq.hq_transform(edesc, w, nb, sh)
+                ewts.append(w)
+            per = {}
+            for m in cfg["ms"]:
+                erng = np.random.default_rng(100 + m)
+                a = synth.make_activations(erng, m, k_, atype)
+                xd = to_dev(a.data)
+                xsd = to_dev(np.ascontiguousarray(a.scales, np.float32)) if a.scales is not None else None
+                yd = torch.empty((m, n_), dtype=torch.float16 if atype == "fp16" else torch.bfloat16, device=dev)
+                wsd = torch.zeros(max(hq.hq_gemm_workspace_size(edesc, m, atype), 256), dtype=torch.uint8,
+                                  device=dev)
+                per[m] = {"x": xd, "xs": xsd, "y": yd, "ws": wsd}
+            extra[name] = {"desc": edesc, "wts": ewts, "atype": atype, "per": per, "cfg": cfg}
+            del eq
+
+    def extra_call(key):
+        name, m = key
+        e = extra[name]
+        d = e["per"][m]
+        wt = e["wts"][rot["extra"] % len(e["wts"])]
+        rot["extra"] += 1
+        k_ = e["cfg"]["k"]
+        hq.hq_gemm(e["desc"], wt, m, e["atype"], d["x"], k_, d["xs"], d["y"], e["cfg"]["n"], d["ws"],
+                   d["ws"].numel(), 0, sh)
+        launches["n"] += hq.hq_last_plan()["launches"]
 
     def gemm(m):
         wt = wts[rot["w"] % W_COPIES]
@@ -334,6 +403,9 @@ def run_gpu(args, rank: int, world: int):
             for t in MOE_T:
                 timed(moe_call, t)
                 timed(ffn_call, t)
+        for name, e in extra.items():
+            for m in e["cfg"]["ms"]:
+                timed(extra_call, (name, m))
     torch.cuda.synchronize()
     st = hq.hq_status_read(wss[args.m_sweep[0]], 0, sh)
     if st != 0:
@@ -346,6 +418,7 @@ def run_gpu(args, rank: int, world: int):
     per_m = {m: [] for m in args.m_sweep}
     per_t = {t: [] for t in MOE_T}
     per_f = {t: [] for t in MOE_T}
+    per_x = {(name, m): [] for name, e in extra.items() for m in e["cfg"]["ms"]}
 
     def blocks(fn, arg, n):
         out = []
@@ -374,10 +447,12 @@ def run_gpu(args, rank: int, world: int):
                 events += [("m", t, *b) for b in blocks(moe_call, t, args.steps)]
             for t in MOE_T:
                 events += [("f", t, *b) for b in blocks(ffn_call, t, args.steps)]
+        for key in per_x:
+            events += [("x", key, *b) for b in blocks(extra_call, key, args.steps)]
         barrier()
         wall = time.perf_counter() - wall0
     for kind, key, k, e0, e1 in events:
-        {"d": per_m, "m": per_t, "f": per_f}[kind][key].append(e0.elapsed_time(e1) * 1e-3 / k)
+        {"d": per_m, "m": per_t, "f": per_f, "x": per_x}[kind][key].append(e0.elapsed_time(e1) * 1e-3 / k)
     gpu_launches = launches["n"]
 
     # ---- end to end through the C ABI with host buffers (pinned): per step the
@@ -438,8 +513,17 @@ def run_gpu(args, rank: int, world: int):
         res["moe"] = {t: statistics.mean(v) for t, v in per_t.items()}
         res["moe_ffn"] = {t: statistics.mean(v) for t, v in per_f.items()}
         res["moe_touched"] = {t: moe["T"][t]["touched"] for t in MOE_T}
+    res["extra"] = {}
+    for (name, m), v in per_x.items():
+        extra_call((name, m))
+        res["extra"].setdefault(name, {})[m] = {"s": statistics.mean(v), "s_min": min(v),
+                                                "plan": hq.hq_last_plan()}
+    for name, e in extra.items():
+        st = hq.hq_status_read(e["per"][e["cfg"]["ms"][0]]["ws"], 0, sh)
+        if st != 0:
+            raise RuntimeError(f"device status ({name}): {hq.status_string(st)}")
     torch.cuda.synchronize()
-    if args.c1_graph:
+    if not args.no_c1_graph:
         res["c1_graph"] = c1_graph_loop(hq, synth, torch, dev)
     return res
 
@@ -524,8 +608,10 @@ def main():
     ap.add_argument("--no-moe", action="store_true", help="skip the MoE sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
-    ap.add_argument("--c1-graph", action="store_true",
-                    help="also time the M=16, N=K=1024 case as a CUDA graph over many weight copies")
+    ap.add_argument("--no-c1-graph", action="store_true",
+                    help="skip the M=16, N=K=1024 case timed as a CUDA graph over many weight copies")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the INT6 channelwise and FP8 block-scaled configurations")
     ap.add_argument("--e2e-overlap", action="store_true",
                     help="end-to-end pass with the copies on their own streams, overlapping the GEMMs")
     ap.add_argument("--m-sweep", type=str, default=",".join(map(str, M_SWEEP)),
@@ -624,7 +710,28 @@ def main():
         "clocks": res["clocks"],
     }
     if "c1_graph" in res:
-        line["c1_graph"] = res["c1_graph"]
+        c1 = res["c1_graph"]
+        c1["roofline_frac"] = round(c1["GB/s"] / pk["hbm_gbs"], 3)
+        c1["bound"] = "hbm"
+        line["c1_graph"] = c1
+    for name, per in res.get("extra", {}).items():
+        cfg = EXTRA[name]
+        fp8 = name.startswith("c4")
+        tc_peak = pk["bf16_tflops"] * (FP8_PER_BF16 if fp8 else 1.0)
+        esw = []
+        for m in cfg["ms"]:
+            t = per[m]["s"]
+            by, fl = extra_bytes(name, m), 2 * m * cfg["n"] * cfg["k"]
+            t_hbm, t_tc = by / (pk["hbm_gbs"] * 1e9), fl / (tc_peak * 1e12)
+            esw.append({"m": m, "us": round(t * 1e6, 2), "us_min": round(per[m]["s_min"] * 1e6, 2),
+                        "tflops": round(fl / t / 1e12, 2), "gbs": round(by / t / 1e9, 1),
+                        "roofline_frac": round(max(t_hbm, t_tc) / t, 3), "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                        "algorithmic_bytes": by, "plan": per[m]["plan"]})
+        line[name] = {"workload": cfg["workload"], "sweep": esw,
+                      "tensor_peak_tflops": round(tc_peak, 1),
+                      "tensor_peak_source": (f"measured bf16 x {FP8_PER_BF16} (nominal fp8:bf16 ratio)" if fp8
+                                             else "measured bf16"),
+                      "l2": f"calls rotate over {cfg['copies']} weight copies (more than L2)"}
     if "moe" in res:
         msw = []
         for t in MOE_T:

@@ -67,7 +67,9 @@ typedef enum {
   HQ_W_INT4 = 0,      /* 4-bit integer codes, symmetric (two's complement) or with zero points */
   HQ_W_INT6 = 1,      /* 6-bit integer codes, symmetric or with zero points */
   HQ_W_MXFP4 = 2,     /* OCP MX e2m1 elements with one UE8M0 scale per 32 along K */
-  HQ_W_FP8_E4M3 = 3   /* OCP e4m3 elements with float32 128x128 block scales */
+  HQ_W_FP8_E4M3 = 3,  /* OCP e4m3 elements with float32 128x128 block scales */
+  HQ_W_NVFP4 = 4,     /* e2m1 elements, one e4m3 scale per 16 along K, one float32 scale per expert */
+  HQ_W_MXINT4 = 5     /* 4-bit two's complement codes with one UE8M0 scale per 32 along K */
 } hq_wtype;
 
 /* Activation types ([README] Support Matrix rows FP16, BF16, FP8 e4m3). */
@@ -82,7 +84,8 @@ typedef enum {
   HQ_S_BF16 = 0,
   HQ_S_FP16 = 1,
   HQ_S_FP32 = 2,
-  HQ_S_UE8M0 = 3
+  HQ_S_UE8M0 = 3,
+  HQ_S_E4M3 = 4       /* OCP e4m3 "fn" bytes (NVFP4 block scales) */
 } hq_stype;
 
 /*
@@ -102,20 +105,27 @@ typedef enum {
  *                                            code k in bits [6k, 6k+6)
  *   MXFP4  codes  uint8 [E][N][K/2]          nibbles as INT4; e2m1 = S.EE.M
  *   FP8    codes  uint8 [E][N][K]            e4m3 "fn" bytes
- *   scales INT4/INT6: bf16 or fp16 [E][N][G]; MXFP4: UE8M0 bytes [E][N][K/32];
+ *   NVFP4  codes  as MXFP4
+ *   MXINT4 codes  as INT4 (two's complement)
+ *   scales INT4/INT6: bf16 or fp16 [E][N][G]; MXFP4 and MXINT4: UE8M0 bytes
+ *          [E][N][K/32]; NVFP4: e4m3 bytes [E][N][K/16];
  *          FP8: float32 [E][ceil(N/128)][ceil(K/128)]
+ *   tensor_scales  NVFP4 only: float32 [E], one secondary scale per expert
  *   zeros  INT4/INT6 with has_zeros only: unsigned codes packed exactly like
  *          that format's codes, [E][N][packed(G)] (INT4: ceil(G/2) bytes,
  *          INT6: 3*ceil(G/4) bytes)
  * Dequantisation: symmetric int  w = q * s;  zero point  w = (q - z) * s;
- * MXFP4  w = e2m1(q) * 2^(E - 127);  FP8  w = e4m3(q) * s_w[n/128][k/128].
+ * MXFP4  w = e2m1(q) * 2^(E - 127);  FP8  w = e4m3(q) * s_w[n/128][k/128];
+ * NVFP4  w = e2m1(q) * e4m3(s[n][k/16]) * g[e];  MXINT4  w = q * 2^(E - 127).
  *
  * Constraints: INT4/INT6 group_k in {0, 32, 64, 128} or a multiple of 128,
  * dividing K; INT6 needs K % 4 == 0; MXFP4 group_k = 32 (K % 32 == 0) and
  * stype UE8M0; FP8 group_k = group_n = 128 and stype FP32; INT stype BF16 or
- * FP16.  N and K at most 2^28 (HQ_ERR_UNSUPPORTED above, so that tile counts
+ * FP16; NVFP4 group_k = 16 (K % 16 == 0) and stype E4M3; MXINT4 group_k =
+ * 32 (K % 32 == 0) and stype UE8M0 (signed_codes ignored: always two's
+ * complement).  N and K at most 2^28 (HQ_ERR_UNSUPPORTED above, so that tile counts
  * and in-tile offsets fit 32-bit integers).
- * The codes/scales/zeros pointers are read by hq_transform only; the
+ * The codes/scales/zeros/tensor_scales pointers are read by hq_transform only; the
  * GEMM calls use the shape fields and ignore the pointers.
  */
 typedef struct {
@@ -132,6 +142,7 @@ typedef struct {
   const void* codes;    /* device pointer, standard format */
   const void* scales;   /* device pointer, standard format */
   const void* zeros;    /* device pointer or NULL */
+  const void* tensor_scales; /* NVFP4: device pointer, float32 [E]; else ignored */
 } hq_weight_desc;
 
 /* flags for hq_gemm / hq_moe_gemm */
@@ -180,7 +191,8 @@ hq_status hq_transform(const hq_weight_desc* desc, void* dst, size_t dst_bytes, 
 /*
  * hq_untransform — the exact inverse of hq_transform: writes the standard
  * format back into caller buffers codes/scales/zeros (sizes as in the
- * descriptor layout; zeros ignored without has_zeros).  Bit-exact for every
+ * descriptor layout; zeros ignored without has_zeros; for NVFP4 the float32
+ * tensor scales [E] are written to `zeros`).  Bit-exact for every
  * input hq_transform accepts.  Asynchronous.
  */
 hq_status hq_untransform(const hq_weight_desc* desc, const void* src, void* codes, void* scales,
@@ -208,8 +220,8 @@ hq_status hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);
  * w_t       hq_transform output for wdesc
  * m         rows of X and Y (0 is a no-op); at most 2^30, with
  *           (m/16 + 1) * ceil(n/128) below 2^31 (HQ_ERR_UNSUPPORTED beyond)
- * atype     hq_atype; INT with group scales needs stype == atype; MXFP4 needs
- *           BF16; FP8 weights need FP8 activations
+ * atype     hq_atype; INT with group scales needs stype == atype; MXFP4,
+ *           NVFP4 and MXINT4 need BF16; FP8 weights need FP8 activations
  * x, ldx    X [m][k] row-major, row stride ldx elements (ldx >= k; the row
  *           pitch a multiple of 16 bytes; x 16-byte aligned)
  * x_scales  FP8 activations only: float32 [m][ceil(k/128)] row-major

@@ -20,16 +20,17 @@ LIB_PATH = os.path.join(PKG, "libhq.so")
 # enums of hq.h
 HQ_OK, HQ_ERR_INVALID_ARG, HQ_ERR_UNSUPPORTED, HQ_ERR_ALIGNMENT = 0, 1, 2, 3
 HQ_ERR_WORKSPACE_TOO_SMALL, HQ_ERR_CUDA, HQ_ERR_DEVICE_TIMEOUT, HQ_ERR_ARCH, HQ_ERR_INVALID_VALUE = 4, 5, 6, 7, 8
-HQ_W_INT4, HQ_W_INT6, HQ_W_MXFP4, HQ_W_FP8_E4M3 = 0, 1, 2, 3
+HQ_W_INT4, HQ_W_INT6, HQ_W_MXFP4, HQ_W_FP8_E4M3, HQ_W_NVFP4, HQ_W_MXINT4 = 0, 1, 2, 3, 4, 5
 HQ_A_BF16, HQ_A_FP16, HQ_A_FP8_E4M3 = 0, 1, 2
-HQ_S_BF16, HQ_S_FP16, HQ_S_FP32, HQ_S_UE8M0 = 0, 1, 2, 3
+HQ_S_BF16, HQ_S_FP16, HQ_S_FP32, HQ_S_UE8M0, HQ_S_E4M3 = 0, 1, 2, 3, 4
 HQ_FLAG_BATCH_INVARIANT = 0x1
 HQ_FLAG_NOALLOC_RESET = 0x100
 HQ_MOE_GROUPED_CONTIGUOUS, HQ_MOE_GROUPED_MASKED = 0, 1
 
-WTYPES = {"int4": HQ_W_INT4, "int6": HQ_W_INT6, "mxfp4": HQ_W_MXFP4, "fp8": HQ_W_FP8_E4M3}
+WTYPES = {"int4": HQ_W_INT4, "int6": HQ_W_INT6, "mxfp4": HQ_W_MXFP4, "fp8": HQ_W_FP8_E4M3, "nvfp4": HQ_W_NVFP4,
+          "mxint4": HQ_W_MXINT4}
 ATYPES = {"bf16": HQ_A_BF16, "fp16": HQ_A_FP16, "fp8": HQ_A_FP8_E4M3}
-STYPES = {"bf16": HQ_S_BF16, "fp16": HQ_S_FP16, "fp32": HQ_S_FP32, "ue8m0": HQ_S_UE8M0}
+STYPES = {"bf16": HQ_S_BF16, "fp16": HQ_S_FP16, "fp32": HQ_S_FP32, "ue8m0": HQ_S_UE8M0, "e4m3": HQ_S_E4M3}
 
 #: every symbol include/hq.h declares
 EXPORTS = [
@@ -57,6 +58,7 @@ class WeightDesc(ctypes.Structure):
         ("num_experts", ctypes.c_int32), ("group_k", ctypes.c_int32), ("group_n", ctypes.c_int32),
         ("signed_codes", ctypes.c_int32), ("has_zeros", ctypes.c_int32), ("reserved", ctypes.c_int32),
         ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zeros", ctypes.c_void_p),
+        ("tensor_scales", ctypes.c_void_p),
     ]
 
 
@@ -140,11 +142,11 @@ def hq_version() -> int:
 
 
 def make_desc(wtype, stype, n, k, num_experts=1, group_k=128, group_n=1, signed_codes=True, has_zeros=False,
-              codes=None, scales=None, zeros=None) -> WeightDesc:
+              codes=None, scales=None, zeros=None, tensor_scales=None) -> WeightDesc:
     """Build an hq_weight_desc (enum names or values accepted)."""
     return WeightDesc(WTYPES.get(wtype, wtype), STYPES.get(stype, stype), n, k, num_experts, group_k, group_n,
                       1 if signed_codes else 0, 1 if has_zeros else 0, 0,
-                      _ptr(codes), _ptr(scales), _ptr(zeros))
+                      _ptr(codes), _ptr(scales), _ptr(zeros), _ptr(tensor_scales))
 
 
 def hq_transform_size(desc: WeightDesc) -> int:

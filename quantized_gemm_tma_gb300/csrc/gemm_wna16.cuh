@@ -1,5 +1,6 @@
 // gemm_wna16.cuh — the weight-only-quantized GEMM kernel for sm_103a:
-// low-bit weights (INT4 / INT6 / MXFP4) against BF16 or FP16 activations, in
+// low-bit weights (INT4 / INT6 / MXFP4 / NVFP4 / MXINT4) against BF16 or FP16
+// activations (the MX and NVFP4 formats against BF16 only), in
 // a dense form and an MoE grouped form ("WnA16": low-bit weights with 16-bit
 // activations — Humming launch article, WnA16 paragraph; MoE GEMM — README
 // "Key Features").
@@ -51,6 +52,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "hq_internal.h"
@@ -245,6 +247,53 @@ __device__ __forceinline__ void dq_mxfp4(const uint4 q, uint32_t E, uint32_t (&o
       if (big) v = h2mul<true>(v, s2);
       o[4 * j + i] = v;
     }
+  }
+}
+
+// One e4m3 byte -> the same value as a bf16 pair (exact: 4 significant bits,
+// exponents -9..8).
+__device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t b) {
+  const __half h(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3));
+  const uint32_t x = __float_as_uint(__half2float(h)) >> 16;
+  return x | (x << 16);
+}
+
+// NVFP4 chunk: 32 e2m1 codes, those of words 0-1 under the e4m3 scale in the
+// low byte of s2, those of words 2-3 under the high byte.  The code placed as
+// a bf16 (as for MXFP4) is e2m1 * 2^-126; one multiply by 2^126 makes it the
+// e2m1 value, a second by the block scale gives e2m1 * s, at most 6
+// significant bits, exact.  The tensor scale is applied to the fp32 sums.
+__device__ __forceinline__ void dq_nvfp4(const uint4 q, uint32_t s2, uint32_t (&o)[16]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  constexpr uint32_t k2p126 = (253u << 7) * 0x00010001u;
+  const uint32_t s_lo = e4m3_to_bf16x2(s2 & 0xFFu), s_hi = e4m3_to_bf16x2((s2 >> 8) & 0xFFu);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t x = w[j];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int sm = 6 - 4 * i, ss = 12 - 4 * i;
+      const uint32_t mag = (sm >= 0 ? (x << sm) : (x >> (-sm))) & 0x01C001C0u;
+      const uint32_t sgn = (x << ss) & 0x80008000u;
+      o[4 * j + i] = h2mul<true>(h2mul<true>(mag | sgn, k2p126), j < 2 ? s_lo : s_hi);
+    }
+  }
+}
+
+// MXINT4 chunk: offset-binary codes u = q + 8 under one UE8M0 exponent E.
+// The INT4 conversion gives (u - 8) * 2^-7 exactly; a multiply by 2^(E-120)
+// gives q * 2^(E-127), exact whenever it is representable.  For E > 247 the
+// power is applied in two exact steps (2^127, then 2^(E-247)).
+__device__ __forceinline__ void dq_mxint4(const uint4 q, uint32_t E, uint32_t (&o)[16]) {
+  dq_int4<true, false>(q, 8u, 0u, o);
+  const bool big = E > 247u;
+  const uint32_t s1 = big ? (254u << 7) * 0x00010001u : ((E + 7u) << 7) * 0x00010001u;
+  const uint32_t s2 = ((E - 120u) << 7) * 0x00010001u;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint32_t v = h2mul<true>(o[i], s1);
+    if (big) v = h2mul<true>(v, s2);
+    o[i] = v;
   }
 }
 
@@ -733,8 +782,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         const int c = c0 + i;
         const uint4 q = *reinterpret_cast<const uint4*>(wsm + (c * kTileN + r) * 16);
         uint32_t z = zrow, sc16 = 0;
-        if constexpr (FMT == static_cast<int>(WFmt::MXFP4)) {
+        if constexpr (FMT == static_cast<int>(WFmt::MXFP4) || FMT == static_cast<int>(WFmt::MXINT4)) {
           sc16 = wsm[p.scale_off + r * 4 + c];
+        } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
+          sc16 = reinterpret_cast<const uint16_t*>(wsm + p.scale_off + r * 8)[c];
         } else if (!p.channel) {
           const int g = (p.g_kb > 1) ? (32 * c) / p.group_k : 0;
           sc16 = reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r * p.g_kb + g];
@@ -748,6 +799,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           const uint32_t c2 = (magic_half<BF16>() + z) * 0x00010001u;
           if (p.channel || promote) dq_int6<BF16, false>(q, qh, c2, 0, o[i]);
           else dq_int6<BF16, true>(q, qh, c2, sc16 * 0x00010001u, o[i]);
+        } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
+          dq_nvfp4(q, sc16, o[i]);
+        } else if constexpr (FMT == static_cast<int>(WFmt::MXINT4)) {
+          dq_mxint4(q, sc16, o[i]);
         } else {
           dq_mxfp4(q, sc16, o[i]);
         }
@@ -873,8 +928,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             qc[i] = *reinterpret_cast<const uint4*>(wsm + (c * kTileN + r) * 16);
             if constexpr (FMT == static_cast<int>(WFmt::INT6))
               qh[i] = *reinterpret_cast<const uint2*>(wsm + p.hi_off + (c * kTileN + r) * 8);
-            if constexpr (FMT == static_cast<int>(WFmt::MXFP4)) {
+            if constexpr (FMT == static_cast<int>(WFmt::MXFP4) || FMT == static_cast<int>(WFmt::MXINT4)) {
               ss[i] = wsm[p.scale_off + r * 4 + c];
+              zz[i] = 0;
+            } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
+              ss[i] = reinterpret_cast<const uint16_t*>(wsm + p.scale_off + r * 8)[c];
               zz[i] = 0;
             } else {
               zz[i] = zrow;
@@ -912,6 +970,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               const uint32_t c2 = (magic_half<BF16>() + zz[i]) * 0x00010001u;
               if (p.channel || promote) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o[i]);
               else dq_int6<BF16, true>(qc[i], qh[i], c2, ss[i] * 0x00010001u, o[i]);
+            } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
+              dq_nvfp4(qc[i], ss[i], o[i]);
+            } else if constexpr (FMT == static_cast<int>(WFmt::MXINT4)) {
+              dq_mxint4(qc[i], ss[i], o[i]);
             } else {
               dq_mxfp4(qc[i], ss[i], o[i]);
             }
@@ -978,7 +1040,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     while (ok && sc.next(p, s_tabs, u)) {
       const int n = u.nt * kTileN + r;
       const bool n_ok = n < p.n;
-      const float rs = (p.channel && n_ok) ? p.row_scale[static_cast<size_t>(u.e) * p.n_pad + n] * kOpFix : 1.f;
+      float rs = (p.channel && n_ok) ? p.row_scale[static_cast<size_t>(u.e) * p.n_pad + n] * kOpFix : 1.f;
+      if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) rs = p.tensor_scale[u.e];  // the per-expert tensor scale
       const bool partial = !MOE && p.stream_k && (u.kb0 > 0 || u.kb1 < p.k_tiles);
       float* pslot = partial ? p.partials + static_cast<size_t>(2 * blockIdx.x + (ui == 0 ? 0 : 1)) * bn * kTileN
                              : nullptr;

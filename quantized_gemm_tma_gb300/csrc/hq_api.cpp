@@ -187,11 +187,12 @@ int env_int(const char* name, int dflt) {
 hq_status make_layout(const hq_weight_desc& d, Layout* L) {
   if (d.n <= 0 || d.k <= 0 || d.num_experts <= 0) return HQ_ERR_INVALID_ARG;
   if (d.n > kMaxDim || d.k > kMaxDim) return HQ_ERR_UNSUPPORTED;
-  if (d.wtype < HQ_W_INT4 || d.wtype > HQ_W_FP8_E4M3) return HQ_ERR_INVALID_ARG;
-  if (d.stype < HQ_S_BF16 || d.stype > HQ_S_UE8M0) return HQ_ERR_INVALID_ARG;
+  if (d.wtype < HQ_W_INT4 || d.wtype > HQ_W_MXINT4) return HQ_ERR_INVALID_ARG;
+  if (d.stype < HQ_S_BF16 || d.stype > HQ_S_E4M3) return HQ_ERR_INVALID_ARG;
   std::memset(L, 0, sizeof(*L));
   L->wtype = d.wtype; L->stype = d.stype; L->n = d.n; L->k = d.k; L->num_experts = d.num_experts;
-  L->group_k = d.group_k; L->signed_codes = d.signed_codes ? 1 : 0; L->has_zeros = d.has_zeros ? 1 : 0;
+  L->group_k = d.group_k; L->signed_codes = (d.signed_codes || d.wtype == HQ_W_MXINT4) ? 1 : 0;
+  L->has_zeros = d.has_zeros ? 1 : 0;
   L->n_tiles = cdiv(d.n, kTileN); L->k_tiles = cdiv(d.k, kTileK);
   L->n_pad = L->n_tiles * kTileN; L->k_pad = L->k_tiles * kTileK;
   const bool is_int = d.wtype == HQ_W_INT4 || d.wtype == HQ_W_INT6;
@@ -208,8 +209,11 @@ hq_status make_layout(const hq_weight_desc& d, Layout* L) {
     L->channel = g == 0;
     L->groups = g == 0 ? 1 : d.k / g;
     L->g_kb = g == 0 ? 0 : (g < 128 ? 128 / g : 1);
-  } else if (d.wtype == HQ_W_MXFP4) {
+  } else if (d.wtype == HQ_W_MXFP4 || d.wtype == HQ_W_MXINT4) {
     if (d.stype != HQ_S_UE8M0 || d.group_k != 32 || d.k % 32 != 0 || d.has_zeros) return HQ_ERR_INVALID_ARG;
+    if (d.group_n != 1 && d.group_n != 0) return HQ_ERR_INVALID_ARG;
+  } else if (d.wtype == HQ_W_NVFP4) {
+    if (d.stype != HQ_S_E4M3 || d.group_k != 16 || d.k % 16 != 0 || d.has_zeros) return HQ_ERR_INVALID_ARG;
     if (d.group_n != 1 && d.group_n != 0) return HQ_ERR_INVALID_ARG;
   } else {
     if (d.stype != HQ_S_FP32 || d.group_k != 128 || d.group_n != 128 || d.has_zeros) return HQ_ERR_INVALID_ARG;
@@ -218,7 +222,9 @@ hq_status make_layout(const hq_weight_desc& d, Layout* L) {
   switch (d.wtype) {
     case HQ_W_INT4: codes = 8192; break;
     case HQ_W_INT6: codes = 8192; hi = 4096; break;
-    case HQ_W_MXFP4: codes = 8192; sc = 512; break;
+    case HQ_W_MXFP4:
+    case HQ_W_MXINT4: codes = 8192; sc = 512; break;
+    case HQ_W_NVFP4: codes = 8192; sc = 1024; break;
     default: codes = 16384; break;
   }
   if (is_int && !L->channel) {
@@ -247,6 +253,10 @@ hq_status make_layout(const hq_weight_desc& d, Layout* L) {
     L->blk_off = off;
     off = align_up(off + 4ull * d.num_experts * L->n_tiles * L->k_tiles, kAlign);
   }
+  if (d.wtype == HQ_W_NVFP4) {
+    L->ts_off = off;
+    off = align_up(off + 4ull * d.num_experts, kAlign);
+  }
   L->total = off;
   return HQ_OK;
 }
@@ -258,7 +268,7 @@ using namespace hq;
 // ====================================================================== C ABI
 extern "C" {
 
-int32_t hq_version(void) { return 100; }
+int32_t hq_version(void) { return 200; }
 
 const char* hq_status_string(int32_t s) {
   switch (s) {
@@ -290,6 +300,8 @@ hq_status hq_transform(const hq_weight_desc* desc, void* dst, size_t dst_bytes, 
   hq_status st = make_layout(*desc, &L);
   if (st != HQ_OK) return st;
   if (!desc->codes || !desc->scales || (L.has_zeros && !desc->zeros)) return HQ_ERR_INVALID_ARG;
+  if (desc->wtype == HQ_W_NVFP4 && !desc->tensor_scales) return HQ_ERR_INVALID_ARG;
+  if (desc->wtype == HQ_W_NVFP4 && (reinterpret_cast<uintptr_t>(desc->tensor_scales) & 3u)) return HQ_ERR_ALIGNMENT;
   if (dst_bytes < L.total) return HQ_ERR_WORKSPACE_TOO_SMALL;
   if ((reinterpret_cast<uintptr_t>(dst) & 255u) != 0) return HQ_ERR_ALIGNMENT;
   if (desc->wtype == HQ_W_FP8_E4M3 && (reinterpret_cast<uintptr_t>(desc->scales) & 3u)) return HQ_ERR_ALIGNMENT;
@@ -313,7 +325,7 @@ hq_status hq_untransform(const hq_weight_desc* desc, const void* src, void* code
   Layout L;
   hq_status st = make_layout(*desc, &L);
   if (st != HQ_OK) return st;
-  if (L.has_zeros && !zeros) return HQ_ERR_INVALID_ARG;
+  if ((L.has_zeros || L.wtype == HQ_W_NVFP4) && !zeros) return HQ_ERR_INVALID_ARG;
   DevInfo di;
   st = device_info(&di);
   if (st != HQ_OK) return st;
@@ -450,6 +462,17 @@ void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_
 
 int wna16_class(int bn) { return bn <= 16 ? 0 : (bn <= 64 ? 1 : (bn <= 128 ? 2 : 3)); }
 
+// WFmt of a weight type handled by the WnA16 kernel
+int wna16_fmt(int wtype) {
+  switch (wtype) {
+    case HQ_W_INT4: return static_cast<int>(WFmt::INT4);
+    case HQ_W_INT6: return static_cast<int>(WFmt::INT6);
+    case HQ_W_NVFP4: return static_cast<int>(WFmt::NVFP4);
+    case HQ_W_MXINT4: return static_cast<int>(WFmt::MXINT4);
+    default: return static_cast<int>(WFmt::MXFP4);
+  }
+}
+
 // Heuristic for one GB300: tokens per tile from M; problems with fewer than
 // four tiles per SM are split stream-K so every SM streams the same number
 // of weight K-blocks.
@@ -527,6 +550,7 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   p.zero_sym = (L.has_zeros || !L.signed_codes) ? 0 : (L.wtype == HQ_W_INT4 ? 8 : 32);
   p.row_scale = L.channel ? reinterpret_cast<const float*>(wt + L.row_off) : nullptr;
   p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
+  p.tensor_scale = L.wtype == HQ_W_NVFP4 ? reinterpret_cast<const float*>(wt + L.ts_off) : nullptr;
   p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = x_rows;
   p.bn = bn; p.m_tiles = 0; p.num_tiles = 0; p.stream_k = 0; p.iters = 0; p.cluster = 1;
   p.promote = (cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
@@ -539,7 +563,7 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups);
   if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
   Wna16Launch l{};
-  l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
+  l.fmt = wna16_fmt(L.wtype);
   l.bf16 = true;
   l.cls = cls;
   l.moe = true;
@@ -610,7 +634,8 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel) {
     if ((L.stype == HQ_S_BF16) != (atype == HQ_A_BF16)) return HQ_ERR_UNSUPPORTED;
   }
-  if (L.wtype == HQ_W_MXFP4 && atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  if ((L.wtype == HQ_W_MXFP4 || L.wtype == HQ_W_NVFP4 || L.wtype == HQ_W_MXINT4) && atype != HQ_A_BF16)
+    return HQ_ERR_UNSUPPORTED;
   const uint32_t xelem = fp8 ? 1 : 2;
   if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(w_t) & 255u))
     return HQ_ERR_ALIGNMENT;
@@ -664,6 +689,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   p.zero_sym = (L.has_zeros || !L.signed_codes) ? 0 : (L.wtype == HQ_W_INT4 ? 8 : 32);
   p.row_scale = L.channel ? reinterpret_cast<const float*>(wt + L.row_off) : nullptr;
   p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
+  p.tensor_scale = L.wtype == HQ_W_NVFP4 ? reinterpret_cast<const float*>(wt + L.ts_off) : nullptr;
   p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = m;
   p.bn = pl.bn; p.m_tiles = pl.m_tiles; p.num_tiles = pl.tiles;
   p.stages = pl.stages; p.x_stages = pl.x_stages; p.groups = pl.groups;
@@ -689,7 +715,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
     if (st != HQ_OK) return st;
   }
   Wna16Launch l{};
-  l.fmt = L.wtype == HQ_W_INT4 ? 0 : (L.wtype == HQ_W_INT6 ? 1 : 2);
+  l.fmt = wna16_fmt(L.wtype);
   l.bf16 = atype == HQ_A_BF16;
   l.cls = pl.cls;
   l.moe = false;
@@ -716,7 +742,8 @@ hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, i
   if (fp8 != (atype == HQ_A_FP8_E4M3)) return HQ_ERR_UNSUPPORTED;
   if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && (L.stype == HQ_S_BF16) != (atype == HQ_A_BF16))
     return HQ_ERR_UNSUPPORTED;
-  if (L.wtype == HQ_W_MXFP4 && atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  if ((L.wtype == HQ_W_MXFP4 || L.wtype == HQ_W_NVFP4 || L.wtype == HQ_W_MXINT4) && atype != HQ_A_BF16)
+    return HQ_ERR_UNSUPPORTED;
   *info = hq_plan_info{};
   if (m == 0) return HQ_OK;
   const size_t optin = static_cast<size_t>(smem_optin);

@@ -8,6 +8,7 @@
 //             so that one CTA streams contiguous memory along K ]
 //   [ row region (channelwise INT): fp32 scale [E][n_pad], u8 zero [E][n_pad] ]
 //   [ block region (FP8): fp32 block scales [E][n_tiles][k_tiles] ]
+//   [ tensor region (NVFP4): fp32 tensor scale [E] ]
 //
 // A tile covers 128 weight rows (n) x 128 reduction columns (k).  Rows and K
 // are padded to multiples of 128 with codes that decode to zero.
@@ -29,6 +30,9 @@
 //   scales (groupwise INT): 16-bit [row][g], g_kb = groups per tile
 //   zeros (groupwise INT with zero points): u8 [row][g]
 //   MXFP4 scales: UE8M0 u8 [row][4] (one per 32-column chunk)
+//   NVFP4: codes as MXFP4; scales e4m3 u8 [row][8] (one per 16 columns:
+//     words 0-1 of chunk c use scale 2c, words 2-3 scale 2c+1)
+//   MXINT4: codes as symmetric INT4 (offset-binary u = q+8); scales as MXFP4
 //   FP8: the 128 x 128-byte A-operand image in the 128-byte swizzled K-major
 //     layout: row r at r*128, 16-byte chunk j stored at chunk j ^ (r % 8).
 #pragma once
@@ -72,7 +76,7 @@ struct Layout {
   int g_kb;     // INT groupwise: scale groups stored per tile (1, 2 or 4)
   int groups;   // scale groups per row in the standard format (INT)
   uint32_t codes_bytes, hi_off, scale_off, scale_bytes, zero_off, zero_bytes, tile_bytes;
-  uint64_t tiles_off, expert_stride, row_off, row_zero_off, blk_off, total;
+  uint64_t tiles_off, expert_stride, row_off, row_zero_off, blk_off, ts_off, total;
 };
 
 // Fill L from a descriptor; returns HQ_OK or the validation error.
@@ -96,7 +100,7 @@ HQ_HD constexpr uint32_t idesc_e4m3(int m, int n) {
 }
 
 // ------------------------------------------------------------------ GEMM
-enum class WFmt : int { INT4 = 0, INT6 = 1, MXFP4 = 2 };
+enum class WFmt : int { INT4 = 0, INT6 = 1, MXFP4 = 2, NVFP4 = 3, MXINT4 = 4 };
 
 struct GemmParams {
   const uint8_t* tiles;     // tile (e=0, nt=0, kt=0)
@@ -105,6 +109,7 @@ struct GemmParams {
   int g_kb, group_k, has_zeros, channel, zero_sym;  // zero_sym: implicit zero for symmetric codes
   const float* row_scale;   // channel: [E][n_pad]
   const uint8_t* row_zero;  // channel with zeros: [E][n_pad]
+  const float* tensor_scale;// NVFP4: [E], applied to the fp32 sums
   int n, n_pad, k, k_tiles, n_tiles;
   int m;                    // dense: rows of X / Y
   int bn;                   // MMA N (tokens per tile), multiple of 16

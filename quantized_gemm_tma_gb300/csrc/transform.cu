@@ -18,13 +18,16 @@ struct TArgs {
   const uint8_t* codes;
   const uint8_t* scales;
   const uint8_t* zeros;
+  const float* tensor_scales;  // NVFP4: [E]
   uint8_t* dst;  // transformed buffer (header first)
 };
 
 __device__ __forceinline__ int std_code_bytes_per_row(const Layout& L) {
   switch (L.wtype) {
     case HQ_W_INT4:
-    case HQ_W_MXFP4: return (L.k + 1) / 2;
+    case HQ_W_MXFP4:
+    case HQ_W_NVFP4:
+    case HQ_W_MXINT4: return (L.k + 1) / 2;
     case HQ_W_INT6: return 3 * L.k / 4;
     default: return L.k;
   }
@@ -61,7 +64,8 @@ __device__ __forceinline__ uint32_t read_zero(const Layout& L, const uint8_t* zr
 
 // offset-binary code stored in the tile for a standard code
 __device__ __forceinline__ uint32_t to_tile_code(const Layout& L, uint32_t c) {
-  if (L.wtype == HQ_W_MXFP4 || L.wtype == HQ_W_FP8_E4M3) return c;  // float codes are stored as they are
+  if (L.wtype == HQ_W_MXFP4 || L.wtype == HQ_W_NVFP4 || L.wtype == HQ_W_FP8_E4M3) return c;  // float codes as they are
+  if (L.wtype == HQ_W_MXINT4) return c ^ 0x8u;  // always two's complement: q + 8
   if (L.has_zeros || !L.signed_codes) return c;
   return L.wtype == HQ_W_INT4 ? (c ^ 0x8u) : (c ^ 0x20u);  // q + 2^(b-1)
 }
@@ -69,7 +73,7 @@ __device__ __forceinline__ uint32_t to_tile_code(const Layout& L, uint32_t c) {
 __device__ __forceinline__ uint32_t from_tile_code(const Layout& L, uint32_t u) { return to_tile_code(L, u); }
 
 __device__ __forceinline__ uint32_t pad_code(const Layout& L) {
-  if (L.wtype == HQ_W_INT4 && !L.has_zeros && L.signed_codes) return 8u;
+  if ((L.wtype == HQ_W_INT4 && !L.has_zeros && L.signed_codes) || L.wtype == HQ_W_MXINT4) return 8u;
   if (L.wtype == HQ_W_INT6 && !L.has_zeros && L.signed_codes) return 32u;
   return 0u;
 }
@@ -169,7 +173,28 @@ __global__ void __launch_bounds__(128) repack_kernel(const TArgs a) {
       *reinterpret_cast<uint2*>(tile + L.hi_off + (c * kTileN + r) * 8) = make_uint2(hi[0], hi[1]);
   }
 
-  if (L.wtype == HQ_W_MXFP4) {
+  if (L.wtype == HQ_W_NVFP4) {
+    // e4m3 block scales [row][8]; a NaN scale or tensor scale is invalid
+    uint32_t sc[2] = {0, 0};
+    for (int j = 0; j < 8; ++j) {
+      const int kk = kt * kTileK + 16 * j;
+      uint32_t b = 0;
+      if (row_ok && kk < L.k) {
+        b = a.scales[rowsN * (L.k / 16) + kk / 16];
+        if ((b & 0x7Fu) == 0x7Fu) ++invalid;
+      }
+      sc[j / 4] |= b << (8 * (j % 4));
+    }
+    *reinterpret_cast<uint2*>(tile + L.scale_off + r * 8) = make_uint2(sc[0], sc[1]);
+    if (kt == 0 && nt == 0 && r == 0) {
+      const float g = a.tensor_scales[e];
+      if (g != g) ++invalid;
+      reinterpret_cast<float*>(a.dst + L.ts_off)[e] = g;
+    }
+    if (invalid) atomicAdd(&hdr->invalid_count, invalid);
+    return;
+  }
+  if (L.wtype == HQ_W_MXFP4 || L.wtype == HQ_W_MXINT4) {
     uint32_t sc = 0;
     for (int c = 0; c < 4; ++c) {
       const int kk = kt * kTileK + 32 * c;
@@ -278,7 +303,16 @@ __global__ void __launch_bounds__(128) unpack_meta_kernel(const TArgs a, uint8_t
     }
     return;
   }
-  if (L.wtype == HQ_W_MXFP4) {
+  if (L.wtype == HQ_W_NVFP4) {
+    for (int g = 0; g < L.k / 16; ++g) {
+      const int kt = g / 8, j = g % 8;
+      scales_out[row * (L.k / 16) + g] = tile_at(kt)[L.scale_off + r * 8 + j];
+    }
+    // the tensor scales go to the zeros argument (NVFP4 has no zero points)
+    if (n == 0) reinterpret_cast<float*>(zeros_out)[e] = reinterpret_cast<const float*>(a.dst + L.ts_off)[e];
+    return;
+  }
+  if (L.wtype == HQ_W_MXFP4 || L.wtype == HQ_W_MXINT4) {
     for (int g = 0; g < L.k / 32; ++g) {
       const int kt = g / 4, c = g % 4;
       scales_out[row * (L.k / 32) + g] = tile_at(kt)[L.scale_off + r * 4 + c];
@@ -329,7 +363,8 @@ __global__ void __launch_bounds__(128) unpack_meta_kernel(const TArgs a, uint8_t
 
 cudaError_t launch_repack(const Layout& L, const hq_weight_desc& d, void* dst, cudaStream_t stream) {
   TArgs a{L, static_cast<const uint8_t*>(d.codes), static_cast<const uint8_t*>(d.scales),
-          static_cast<const uint8_t*>(d.zeros), static_cast<uint8_t*>(dst)};
+          static_cast<const uint8_t*>(d.zeros), static_cast<const float*>(d.tensor_scales),
+          static_cast<uint8_t*>(dst)};
   cudaError_t err = cudaMemsetAsync(dst, 0, L.total, stream);
   if (err != cudaSuccess) return err;
   dim3 grid(L.k_tiles, L.n_tiles, L.num_experts);
@@ -339,7 +374,7 @@ cudaError_t launch_repack(const Layout& L, const hq_weight_desc& d, void* dst, c
 
 cudaError_t launch_unpack(const Layout& L, const void* src, void* codes, void* scales, void* zeros,
                           cudaStream_t stream) {
-  TArgs a{L, nullptr, nullptr, nullptr, const_cast<uint8_t*>(static_cast<const uint8_t*>(src))};
+  TArgs a{L, nullptr, nullptr, nullptr, nullptr, const_cast<uint8_t*>(static_cast<const uint8_t*>(src))};
   dim3 grid(L.k_tiles, L.n_tiles, L.num_experts);
   unpack_codes_kernel<<<grid, 128, 0, stream>>>(a, static_cast<uint8_t*>(codes));
   cudaError_t err = cudaGetLastError();

@@ -9,12 +9,16 @@ namespace hq {
 cudaError_t launch_wna16_int4(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
 cudaError_t launch_wna16_int6(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
 cudaError_t launch_wna16_mxfp4(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
+cudaError_t launch_wna16_nvfp4(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
+cudaError_t launch_wna16_mxint4(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
 
 cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const Wna16Maps& maps, cudaStream_t stream) {
   switch (l.fmt) {
     case 0: return launch_wna16_int4(l, p, maps, stream);
     case 1: return launch_wna16_int6(l, p, maps, stream);
     case 2: return launch_wna16_mxfp4(l, p, maps, stream);
+    case 3: return launch_wna16_nvfp4(l, p, maps, stream);
+    case 4: return launch_wna16_mxint4(l, p, maps, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -421,6 +421,22 @@ def moe_mxfp4(seed: int, tokens: int, num_experts: int = 128, n: int = 1536, k: 
     return qw, x, r
 
 
+def moe_experts(seed: int, wtype: str, num_experts: int = 128, n: int = 1536, k: int = 2048) -> QuantWeight:
+    """MoE expert weights W~N(0,0.02) [E, N, K] quantised to NVFP4, MXINT4 or
+    MXFP4 (drawn and quantised eight experts at a time to bound memory)."""
+    quant = {"nvfp4": quantize_nvfp4, "mxint4": quantize_mxint4, "mxfp4": quantize_mxfp4}[wtype]
+    rng = np.random.default_rng(seed)
+    parts = []
+    for e0 in range(0, num_experts, 8):
+        ne = min(8, num_experts - e0)
+        parts.append(quant(rng.standard_normal((ne, n, k), dtype=np.float32) * np.float32(0.02)))
+    q0 = parts[0]
+    ts = None if q0.tensor_scale is None else np.concatenate([q.tensor_scale for q in parts])
+    return QuantWeight(wtype, n, k, num_experts, q0.group_k, q0.group_n, q0.stype, q0.signed,
+                       np.concatenate([q.codes for q in parts]), np.concatenate([q.scales for q in parts]),
+                       None, ts)
+
+
 def random_codes_weight(seed: int, wtype: str, n: int, k: int, num_experts: int = 1,
                         group_k: int = 128, signed: bool = True, has_zeros: bool = False,
                         stype: Optional[str] = None) -> QuantWeight:

@@ -39,8 +39,11 @@ class DevWeight:
         self.codes = to_dev(qw.codes)
         self.scales = to_dev(qw.scales)
         self.zeros = to_dev(qw.zeros) if qw.zeros is not None else None
+        ts = getattr(qw, "tensor_scale", None)
+        self.tensor_scales = to_dev(np.asarray(ts, np.float32)) if ts is not None else None
         self.desc = hq.make_desc(qw.wtype, qw.stype, qw.n, qw.k, qw.num_experts, qw.group_k, qw.group_n,
-                                 qw.signed, qw.has_zeros, self.codes, self.scales, self.zeros)
+                                 qw.signed, qw.has_zeros, self.codes, self.scales, self.zeros,
+                                 self.tensor_scales)
         self.size = hq.hq_transform_size(self.desc)
         self.wt = torch.empty(self.size + 256, dtype=torch.uint8, device="cuda")
         off = (-self.wt.data_ptr()) % 256
@@ -52,6 +55,8 @@ class DevWeight:
         codes = torch.zeros_like(self.codes)
         scales = torch.zeros_like(self.scales)
         zeros = torch.zeros_like(self.zeros) if self.zeros is not None else None
+        if self.tensor_scales is not None:          # NVFP4: tensor scales come back through `zeros`
+            zeros = torch.zeros_like(self.tensor_scales)
         hq.hq_untransform(self.desc, self.wt, codes, scales, zeros, stream())
         torch.cuda.synchronize()
         return codes, scales, zeros

@@ -49,6 +49,10 @@ def _desc(hq, **kw):
     (dict(wtype="int6", k=130, group_k=0), 1), (dict(stype="fp32"), 1), (dict(wtype="mxfp4", stype="bf16"), 1),
     (dict(wtype="mxfp4", stype="ue8m0", group_k=64), 1), (dict(wtype="fp8", stype="fp32", group_k=128, group_n=1), 1),
     (dict(wtype=7), 1), (dict(num_experts=0), 1),
+    (dict(wtype="nvfp4", stype="ue8m0", group_k=16), 1), (dict(wtype="nvfp4", stype="e4m3", group_k=32), 1),
+    (dict(wtype="nvfp4", stype="e4m3", group_k=16, k=520), 1),
+    (dict(wtype="nvfp4", stype="e4m3", group_k=16, has_zeros=True), 1),
+    (dict(wtype="mxint4", stype="e4m3", group_k=32), 1), (dict(wtype="mxint4", stype="ue8m0", group_k=16), 1),
 ])
 def test_transform_size_validation(hq, kw, status):
     with pytest.raises(hq.HQError) as ei:
@@ -61,6 +65,12 @@ def test_transform_size_layouts(hq):
     assert hq.hq_transform_size(_desc(hq, n=128, k=128)) == 256 + 8192 + 256
     s = hq.hq_transform_size(_desc(hq, n=8192, k=8192, has_zeros=True, signed_codes=False))
     assert s == 256 + 64 * 64 * (8192 + 256 + 128)
+    # nvfp4: codes + e4m3 scales [128][8] per tile, then the float32 tensor scales (one 256-byte block)
+    assert hq.hq_transform_size(hq.make_desc("nvfp4", "e4m3", 128, 128, group_k=16)) == 256 + 8192 + 1024 + 256
+    assert hq.hq_transform_size(hq.make_desc("nvfp4", "e4m3", 256, 256, num_experts=3, group_k=16)) == \
+        256 + 3 * 4 * (8192 + 1024) + 256
+    # mxint4: codes + UE8M0 scales [128][4] per tile, like mxfp4
+    assert hq.hq_transform_size(hq.make_desc("mxint4", "ue8m0", 128, 128, group_k=32)) == 256 + 8192 + 512
     # fp8: 16 KiB images + block scales
     d = hq.make_desc("fp8", "fp32", 4096, 7168, group_k=128, group_n=128)
     assert hq.hq_transform_size(d) >= 256 + 32 * 56 * 16384 + 4 * 32 * 56

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 def _ref(qw, acts, rows=None):
     w = oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes, qw.scales, qw.zeros, qw.group_k, qw.signed, qw.stype,
-                          qw.num_experts)
+                          qw.num_experts, qw.tensor_scale)
     a = oracle.decode_activations(acts.atype, acts.data, acts.scales)
     if rows is not None:
         a = a[rows]
@@ -88,6 +88,37 @@ def test_mxfp4_extreme_exponents():
     y = _gpu(qw, acts)
     r = _ref(qw, acts)
     check(y, r, "mxfp4 extreme exponents")
+
+
+N3 = [
+    # wtype, m, n, k: every tile-width class, ragged M, N and K (K = 4 tiles + one group)
+    ("nvfp4", 16, 384, 1024),
+    ("nvfp4", 37, 200, 528),
+    ("nvfp4", 100, 256, 512),
+    ("nvfp4", 300, 256, 256),
+    ("mxint4", 16, 384, 1024),
+    ("mxint4", 45, 200, 544),
+    ("mxint4", 200, 256, 512),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(N3)), ids=lambda i: "-".join(map(str, N3[i])))
+def test_nvfp4_mxint4_dense(idx):
+    wtype, m, n, k = N3[idx]
+    rng = np.random.default_rng(60 + idx)
+    w = rng.standard_normal((1, n, k)) * 0.02
+    qw = synth.quantize_nvfp4(w) if wtype == "nvfp4" else synth.quantize_mxint4(w)
+    acts = synth.make_activations(rng, m, k, "bf16")
+    check(_gpu(qw, acts), _ref(qw, acts), f"{wtype} {m}x{n}x{k}")
+
+
+def test_mxint4_extreme_exponents():
+    """UE8M0 exponents at the low end (q * 2^-122) and above 247 (the two-step
+    power), against small activations so the sums stay finite."""
+    qw = synth.random_codes_weight(9, "mxint4", 128, 256)
+    qw.scales[:] = np.where(np.arange(8)[None, None, :] % 2 == 0, 5, 248).astype(np.uint8)[:, :, :8]
+    acts = synth.make_activations(np.random.default_rng(9), 16, 256, "bf16", std=2.0 ** -20)
+    check(_gpu(qw, acts), _ref(qw, acts), "mxint4 extreme exponents")
 
 
 def test_strided_x_and_y():

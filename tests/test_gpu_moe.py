@@ -16,8 +16,9 @@ def _ref(qw, acts, routing, tokens=None):
 
     def expert(e):
         z = None if qw.zeros is None else qw.zeros[e:e + 1]
+        ts = None if qw.tensor_scale is None else qw.tensor_scale[e:e + 1]
         return oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes[e:e + 1], qw.scales[e:e + 1], z, qw.group_k,
-                                 qw.signed, qw.stype, 1)[0]
+                                 qw.signed, qw.stype, 1, ts)[0]
     return oracle.moe_gemm(a, ids, tw, expert)
 
 
@@ -65,6 +66,18 @@ def test_int4_experts():
     y, st = _run(qw, acts, r)
     assert st == 0
     check(y, _ref(qw, acts, r), "int4 experts")
+
+
+@pytest.mark.parametrize("wtype", ["nvfp4", "mxint4"])
+def test_nvfp4_mxint4_experts(wtype):
+    rng = np.random.default_rng(16)
+    w = rng.standard_normal((6, 256, 512)) * 0.02 * np.exp2(rng.integers(-2, 3, size=(6, 1, 1)))
+    qw = synth.quantize_nvfp4(w) if wtype == "nvfp4" else synth.quantize_mxint4(w)
+    acts = synth.make_activations(rng, 40, 512, "bf16")
+    r = synth.make_routing(rng, 40, 6, 2)
+    y, st = _run(qw, acts, r)
+    assert st == 0
+    check(y, _ref(qw, acts, r), f"{wtype} experts")
 
 
 def test_invalid_expert_id_sets_status():
@@ -309,3 +322,18 @@ def test_moe_ffn_full_size_sampled(moe_full, tokens):
     ref = oracle.moe_ffn(oracle.decode_activations("bf16", a.data)[rows], rt.topk_ids[rows], rt.topk_w[rows], expert,
                          _expert_fn(w2), intermediate=None)
     check_ffn(got[rows], ref, f"moe ffn full size T={tokens}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wtype", ["nvfp4", "mxint4"])
+def test_nvfp4_mxint4_experts_full_size(moe_full, wtype):
+    """The gate+up shape (E = 128, N = 1536, K = 2048) with NVFP4 or MXINT4
+    experts, T = 4096 tokens of the routing above, 32 sampled tokens against
+    the oracle."""
+    from gpu_helpers import DevWeight, run_moe
+    _, acts, r, _, _ = moe_full
+    qw = synth.moe_experts(3, wtype)
+    y, st = run_moe(DevWeight(qw), acts, r)
+    assert st == 0
+    rows = np.unique(np.concatenate([[0, 4095], np.random.default_rng(5).integers(0, 4096, size=30)]))
+    check(y[rows], _ref(qw, acts, r, rows), f"{wtype} experts full size")

@@ -23,6 +23,10 @@ CASES = [
     ("mxfp4", 150, 96, 32, True, False, "ue8m0"),
     ("fp8", 256, 384, 128, True, False, "fp32"),
     ("fp8", 130, 200, 128, True, False, "fp32"),
+    ("nvfp4", 256, 512, 16, True, False, "e4m3"),
+    ("nvfp4", 150, 96, 16, True, False, "e4m3"),      # ragged N, K < one tile
+    ("mxint4", 256, 512, 32, True, False, "ue8m0"),
+    ("mxint4", 150, 96, 32, True, False, "ue8m0"),
 ]
 
 
@@ -38,6 +42,8 @@ def test_roundtrip_bit_exact(idx):
     assert np.array_equal(scales.cpu().numpy().view(qw.scales.dtype), qw.scales)
     if zeros:
         assert np.array_equal(z.cpu().numpy(), qw.zeros)
+    if qw.tensor_scale is not None:                  # NVFP4 tensor scales come back through `zeros`
+        assert np.array_equal(z.cpu().numpy(), qw.tensor_scale)
 
 
 def test_roundtrip_moe_experts():
@@ -47,6 +53,26 @@ def test_roundtrip_moe_experts():
     codes, scales, _ = dw.untransform()
     assert np.array_equal(codes.cpu().numpy(), qw.codes)
     assert np.array_equal(scales.cpu().numpy(), qw.scales)
+
+
+def test_roundtrip_nvfp4_experts():
+    from gpu_helpers import DevWeight
+    qw = synth.random_codes_weight(5, "nvfp4", 200, 160, num_experts=3)
+    dw = DevWeight(qw)
+    codes, scales, ts = dw.untransform()
+    assert np.array_equal(codes.cpu().numpy(), qw.codes)
+    assert np.array_equal(scales.cpu().numpy(), qw.scales)
+    assert np.array_equal(ts.cpu().numpy(), qw.tensor_scale)
+
+
+def test_transform_rejects_nan_nvfp4_scale():
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import DevWeight
+    qw = synth.random_codes_weight(6, "nvfp4", 128, 128)
+    qw.scales[0, 9, 3] = 0xFF                        # e4m3 NaN
+    with pytest.raises(hq.HQError) as ei:
+        DevWeight(qw)
+    assert ei.value.status == hq.HQ_ERR_INVALID_VALUE
 
 
 def test_transform_rejects_nan_scale():
