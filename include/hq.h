@@ -336,7 +336,10 @@ hq_status hq_moe_ffn_workspace_size(const hq_weight_desc* w13, const hq_weight_d
  *   H[f] = a(X[t]) . dequant(W13_e)^T         (2I outputs: gate, then up)
  *   A[f] = silu(H[f][0, I)) * H[f][I, 2I)      silu(g) = g / (1 + exp(-g))
  *   Y[t] = sum_j topk_w[t][j] * (A[t*topk + j] . dequant(W2_{e})^T)
- * H and A are rounded to bf16 (the activation type) between the GEMMs.
+ * A is held in bf16 (the activation type) between the GEMMs.  When I is a
+ * multiple of 128 the gate+up GEMM computes A in its epilogue from the fp32
+ * gate and up sums (H is never stored); otherwise H is stored in bf16 and an
+ * elementwise kernel computes A from it.
  *
  * w13, w13_t   gate+up experts [E][2I][k] and their transform (I % 8 == 0)
  * w2, w2_t     down experts [E][n][I] and their transform (same E)

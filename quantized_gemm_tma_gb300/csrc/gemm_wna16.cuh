@@ -335,6 +335,8 @@ template <bool MOE>
 struct Sched {
   long long it, it_end;  // stream-K: K-block iteration range of this CTA
   int w;                 // whole-tile / MoE: next work index
+  int half = 0;          // MoE gated: the up tile of the last gate tile is next
+  Unit gate;             // MoE gated: that gate tile's unit
 
   __device__ __forceinline__ void init(const GemmParams& p) {
     if (!MOE && p.stream_k) {
@@ -381,10 +383,20 @@ struct Sched {
       const int* s_tile_off = s_tabs;
       const int* s_row_off = s_tabs + p.num_experts + 1;
       const int* s_xbase = s_row_off + p.num_experts + 1;
-      const int total = s_tile_off[p.num_experts] * p.n_tiles;
+      // gated: work items are (expert, m-tile, gate n-tile), each run as the
+      // gate tile and then the up tile I / 128 n-tiles further on
+      const bool gated = p.moe_out == kMoeOutGated;
+      const int nt_items = gated ? p.n_tiles / 2 : p.n_tiles;
+      if (gated && half) {
+        u = gate;
+        u.nt += nt_items;
+        half = 0;
+        return true;
+      }
+      const int total = s_tile_off[p.num_experts] * nt_items;
       if (w >= total) return false;
-      const int tile = w / p.n_tiles;
-      u.nt = w % p.n_tiles;
+      const int tile = w / nt_items;
+      u.nt = w % nt_items;
       // expert e: last index with tile_off[e] <= tile
       int lo = 0, hi = p.num_experts;  // invariant tile_off[lo] <= tile < tile_off[hi]
       while (hi - lo > 1) {
@@ -400,6 +412,10 @@ struct Sched {
       u.kb0 = 0;
       u.kb1 = p.k_tiles;
       w += gridDim.x;
+      if (gated) {
+        gate = u;
+        half = 1;
+      }
       return true;
     }
   }
@@ -1036,12 +1052,39 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     const bool trace_me = quarter == 0 && lane == 0;
     // INT4 bf16 operands without a folded scale carry an extra 2^-7
     constexpr float kOpFix = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
+    // MoE gated: the gate tile's sums of the promotion path, kept for its up tile
+    [[maybe_unused]] float gtot[CLS == 0 ? BNMAX : 1];
+    const bool gated = MOE && p.moe_out == kMoeOutGated;
+    // MoE gated, other paths: this CTA's gate sums [BNMAX columns][128 rows] in
+    // global memory (L2-resident); a thread reads back only what it wrote
+    float* const gbuf = gated ? p.gate_buf + static_cast<size_t>(blockIdx.x) * BNMAX * kTileN + r : nullptr;
+    const int half_n = p.n_tiles / 2 * kTileN;  // gated: I, the first up row
     Unit u;
     while (ok && sc.next(p, s_tabs, u)) {
       const int n = u.nt * kTileN + r;
       const bool n_ok = n < p.n;
+      // gated units come in pairs: the gate tile (even unit), then its up tile
+      const bool gate_half = gated && (ui & 1) == 0;
       float rs = (p.channel && n_ok) ? p.row_scale[static_cast<size_t>(u.e) * p.n_pad + n] * kOpFix : 1.f;
       if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) rs = p.tensor_scale[u.e];  // the per-expert tensor scale
+      // gated, up tile: the row scale of the matching gate row
+      float rs_gate = rs;
+      if (gated && !gate_half && p.channel)
+        rs_gate = p.row_scale[static_cast<size_t>(u.e) * p.n_pad + n - half_n] * kOpFix;
+      // silu(gate) * up of 16 columns of this row, stored at routed row p,
+      // output column n - I (the gate row)
+      [[maybe_unused]] auto emit_gated16 = [&](int ch, const float (&g)[16], const float (&v)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int col = ch * 16 + i;
+          if (col < u.rows && n_ok) {
+            const float gs = g[i] * rs_gate;
+            const float a = gs / (1.f + expf(-gs)) * (v[i] * rs);
+            const size_t off = static_cast<size_t>(u.row0 + col) * p.ldy + (n - half_n);
+            reinterpret_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(a);
+          }
+        }
+      };
       const bool partial = !MOE && p.stream_k && (u.kb0 > 0 || u.kb1 < p.k_tiles);
       float* pslot = partial ? p.partials + static_cast<size_t>(2 * blockIdx.x + (ui == 0 ? 0 : 1)) * bn * kTileN
                              : nullptr;
@@ -1203,13 +1246,25 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             if (q) ++ck1; else ++ck0;
           }
           if (!ok) break;
+          if (gate_half) {
 #pragma unroll
-          for (int ch = 0; ch < BNMAX / 16; ++ch) {
-            if (ch * 16 < bn) {
-              float v[16];
+            for (int i = 0; i < BNMAX; ++i) gtot[i] = tot[i];
+          } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = tot[ch * 16 + i];
-              emit16(ch, v);
+            for (int ch = 0; ch < BNMAX / 16; ++ch) {
+              if (ch * 16 < bn) {
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = tot[ch * 16 + i];
+                if (gated) {
+                  float g[16];
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) g[i] = gtot[ch * 16 + i];
+                  emit_gated16(ch, g, v);
+                } else {
+                  emit16(ch, v);
+                }
+              }
             }
           }
         }
@@ -1245,7 +1300,31 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         };
         bool xchg = false;
         if constexpr (CLS >= 1 && !MOE) xchg = p.cluster == 2;
-        if (!xchg) {
+        if (gate_half) {
+          // the gate tile's sums wait in the CTA's gate buffer for its up tile
+          for (int ch = 0; ch < (bn >> 4); ++ch) {
+            float v[16];
+            acc16(ch, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) __stcg(gbuf + (ch * 16 + i) * kTileN, v[i]);
+          }
+        } else if (gated) {
+          // the gate sums of chunk ch + 1 are loaded while chunk ch is combined
+          float g[16], gn[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) g[i] = __ldcg(gbuf + i * kTileN);
+          for (int ch = 0; ch < (bn >> 4); ++ch) {
+            if ((ch + 1) * 16 < bn) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) gn[i] = __ldcg(gbuf + ((ch + 1) * 16 + i) * kTileN);
+            }
+            float v[16];
+            acc16(ch, v);
+            emit_gated16(ch, g, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) g[i] = gn[i];
+          }
+        } else if (!xchg) {
           for (int ch = 0; ch < (bn >> 4); ++ch) {
             float v[16];
             acc16(ch, v);

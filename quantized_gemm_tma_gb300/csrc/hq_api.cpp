@@ -530,6 +530,11 @@ int moe_tile_bn(double mean_rows) {
   return bn;
 }
 
+// The gated feed-forward output's gate buffer: one [128 tokens][128 rows]
+// fp32 block per CTA (tiles of at most 128 tokens), for any sm_103 SM count.
+constexpr int kGateBufBn = 128;
+constexpr size_t kGateBufBytes = sizeof(float) * kPlanSmsBound * kGateBufBn * kTileN;
+
 // The grouped WnA16 GEMM over routed rows whose offsets, m-tile prefix, row
 // map and X row bases are already in the workspace.  The routed rows of expert
 // e stand together in X from row x_base[e] on (the permuted activations of the
@@ -540,7 +545,8 @@ int moe_tile_bn(double mean_rows) {
 hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const void* x, int64_t ldx, int x_rows,
                              const int* x_base, int out, const float* topk_w, void* y, int64_t ldy,
                              const int* exp_off, const int* tile_off, const int* perm, float* zbuf, int* status,
-                             const DevInfo& di, cudaStream_t s, int* stages, int* groups) {
+                             const DevInfo& di, cudaStream_t s, int* stages, int* groups,
+                             float* gate_buf = nullptr) {
   const int cls = wna16_class(bn);
   GemmParams p{};
   p.tiles = wt + L.tiles_off;
@@ -560,6 +566,8 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   p.num_experts = L.num_experts; p.topk = 1;
   p.tile_offsets = tile_off; p.expert_offsets = exp_off; p.perm = perm; p.topk_w = topk_w; p.zbuf = zbuf;
   p.x_base = x_base;
+  p.gate_buf = gate_buf;
+  if (out == kMoeOutGated && (!gate_buf || di.sms > kPlanSmsBound || bn > kGateBufBn)) return HQ_ERR_UNSUPPORTED;
   plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups);
   if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
   Wna16Launch l{};
@@ -901,6 +909,7 @@ hq_status hq_moe_ffn_workspace_size(const hq_weight_desc* w13, const hq_weight_d
   ws += align_up(2 * pairs * lda, kAlign);             // A: silu(gate) * up, bf16
   ws += align_up(sizeof(float) * pairs * L2.n_pad, kAlign);  // weighted down-projection rows
   ws += align_up(2 * pairs * static_cast<size_t>(permuted_ld(L13.k)), kAlign);  // permuted activations, bf16
+  ws += kGateBufBytes;  // per-CTA gate sums of the fused silu(gate) * up
   *bytes = ws;
   return HQ_OK;
 }
@@ -958,6 +967,8 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
   off += align_up(sizeof(float) * static_cast<size_t>(pairs) * L2.n_pad, kAlign);
   void* xg = ws + off;  // the routed activation rows in expert order
   const int64_t ldg = permuted_ld(L13.k);
+  off += align_up(2 * static_cast<size_t>(pairs) * static_cast<size_t>(ldg), kAlign);
+  float* gate_buf = reinterpret_cast<float*>(ws + off);
   const int bn = moe_tile_bn(static_cast<double>(pairs) / L13.num_experts);
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L13.num_experts, bn, exp_off, tile_off, perm, nullptr,
                        nullptr, reinterpret_cast<int*>(ws), s) != cudaSuccess)
@@ -966,12 +977,24 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
                          ldg, di.sms, s) != cudaSuccess)
     return HQ_ERR_CUDA;
   int stages = 0, groups = 0;
-  // gate+up: H[p] = Xg[p] . W13_e^T, in routed order
-  st = launch_moe_grouped(L13, static_cast<const uint8_t*>(w13_t), bn, xg, ldg, static_cast<int>(pairs), exp_off,
-                          kMoeOutRouted, nullptr, hbuf, ldh, exp_off, tile_off, perm, nullptr,
-                          reinterpret_cast<int*>(ws), di, s, &stages, &groups);
-  if (st != HQ_OK) return st;
-  if (launch_moe_act(hbuf, ldh, static_cast<int>(pairs), inter, abuf, lda, s) != cudaSuccess) return HQ_ERR_CUDA;
+  // gate+up with silu(gate) * up in its epilogue when the up rows start on a
+  // tile boundary (I a multiple of 128) and the tiles have two accumulator
+  // buffers (at most 128 tokens): A[p] straight from the two accumulators.
+  // Otherwise H[p] = Xg[p] . W13_e^T in routed order, then an elementwise
+  // kernel.
+  const bool fused = inter % kTileN == 0 && bn <= kGateBufBn && di.sms <= kPlanSmsBound;
+  if (fused) {
+    st = launch_moe_grouped(L13, static_cast<const uint8_t*>(w13_t), bn, xg, ldg, static_cast<int>(pairs), exp_off,
+                            kMoeOutGated, nullptr, abuf, lda, exp_off, tile_off, perm, nullptr,
+                            reinterpret_cast<int*>(ws), di, s, &stages, &groups, gate_buf);
+    if (st != HQ_OK) return st;
+  } else {
+    st = launch_moe_grouped(L13, static_cast<const uint8_t*>(w13_t), bn, xg, ldg, static_cast<int>(pairs), exp_off,
+                            kMoeOutRouted, nullptr, hbuf, ldh, exp_off, tile_off, perm, nullptr,
+                            reinterpret_cast<int*>(ws), di, s, &stages, &groups);
+    if (st != HQ_OK) return st;
+    if (launch_moe_act(hbuf, ldh, static_cast<int>(pairs), inter, abuf, lda, s) != cudaSuccess) return HQ_ERR_CUDA;
+  }
   // down: Z[perm[p]] = topk_w[perm[p]] * A[p] . W2_e^T (A in routed order)
   st = launch_moe_grouped(L2, static_cast<const uint8_t*>(w2_t), bn, abuf, lda, static_cast<int>(pairs), exp_off,
                           kMoeOutZ, topk_w, y, ldy, exp_off, tile_off, perm, zbuf, reinterpret_cast<int*>(ws), di, s,
@@ -980,7 +1003,7 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L2.num_experts, L2.n, L2.n_pad, y, ldy, true, s) !=
       cudaSuccess)
     return HQ_ERR_CUDA;
-  g_last_plan = hq_plan_info{bn, 1, di.sms, 6, stages, wna16_class(bn), groups, 0};
+  g_last_plan = hq_plan_info{bn, 1, di.sms, fused ? 5 : 6, stages, wna16_class(bn), groups, 0};
   return HQ_OK;
 }
 

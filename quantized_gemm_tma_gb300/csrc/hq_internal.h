@@ -136,13 +136,18 @@ struct GemmParams {
   const float* topk_w;      // [T*topk]
   const int* x_base;        // [E]: X row of each expert's first routed row (its rows stand together in X)
   float* zbuf;              // [T*topk][n_pad] weighted per-pair outputs
+  float* gate_buf;          // gated: [grid][bn max of the class][128] fp32 gate sums, one block per CTA
   int moe_out;              // kMoeOutZ, kMoeOutRowMap or kMoeOutRouted
 };
 
 // MoE output modes: the weighted fp32 row zbuf[perm[p]] (combined afterwards),
-// the 16-bit Y row perm[p] (grouped forms), or the 16-bit Y row p itself
-// (rows in routed order, the feed-forward block's gate+up output).
-constexpr int kMoeOutZ = 0, kMoeOutRowMap = 1, kMoeOutRouted = 2;
+// the 16-bit Y row perm[p] (grouped forms), the 16-bit Y row p itself (rows in
+// routed order, the feed-forward block's gate+up output), or, gated, the
+// 16-bit row p of silu(gate) * up: the weight holds 2I rows (gate rows, then
+// up rows, I a multiple of 128) and each CTA takes a gate tile and the
+// matching up tile as two consecutive units, writing I outputs per row; the
+// gate tile's fp32 sums wait for the up tile in the CTA's block of gate_buf.
+constexpr int kMoeOutZ = 0, kMoeOutRowMap = 1, kMoeOutRouted = 2, kMoeOutGated = 3;
 
 struct Fp8Params {
   const uint8_t* tiles;

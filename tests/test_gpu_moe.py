@@ -194,8 +194,9 @@ def _expert_fn(qw):
     """Expert weights [N, K] in float64, dequantised exactly (no operand rounding)."""
     def expert(e):
         z = None if qw.zeros is None else qw.zeros[e:e + 1]
+        ts = None if qw.tensor_scale is None else qw.tensor_scale[e:e + 1]
         return oracle.dequantize(qw.wtype, qw.n, qw.k, qw.codes[e:e + 1], qw.scales[e:e + 1], z, qw.group_k,
-                                 qw.signed, qw.stype, 1)[0]
+                                 qw.signed, qw.stype, 1, ts)[0]
     return expert
 
 
@@ -226,29 +227,44 @@ def _run_ffn(d13, d2, acts, r, n):
 
 
 FFN = [
-    # seed, weight, tokens, experts, intermediate I, hidden K, output n, topk
-    (40, "mxfp4", 37, 8, 128, 256, 256, 4),
-    (41, "int4", 64, 6, 192, 384, 200, 2),     # ragged output n, three gate/up tiles
+    # seed, weight, tokens, experts, intermediate I, hidden K, output n, topk, fused
+    (40, "mxfp4", 37, 8, 128, 256, 256, 4, True),    # 32-token tiles
+    (41, "int4", 64, 6, 192, 384, 200, 2, False),    # I not a multiple of 128: H stored, elementwise kernel
+    (42, "int4", 4, 8, 256, 512, 256, 2, True),      # 16-token tiles, group scales promoted in fp32
+    (43, "mxfp4", 300, 4, 256, 256, 128, 4, True),   # 128-token tiles
+    (44, "int6ch", 40, 4, 128, 256, 256, 2, True),   # row scales of the gate and the up rows
+    (45, "nvfp4", 64, 4, 128, 256, 256, 2, True),    # per-expert tensor scales
 ]
+
+
+def _ffn_weight(kind, rng, e, n, k, seed):
+    if kind == "mxfp4":
+        return synth.moe_mxfp4(seed, 1, num_experts=e, n=n, k=k, topk=1)[0]
+    w = rng.standard_normal((e, n, k)) * 0.02
+    if kind == "int4":
+        return synth.quantize_int_groupwise(w, 4, 128 if k % 128 == 0 else 64, False, "bf16")
+    if kind == "int6ch":
+        return synth.quantize_int_groupwise(w, 6, 0, True, "bf16")
+    return synth.quantize_nvfp4(w)
 
 
 @pytest.mark.parametrize("idx", range(len(FFN)), ids=lambda i: "-".join(map(str, FFN[i][:2])))
 def test_moe_ffn_parity(idx):
     """The feed-forward block against the exact oracle (exact expert weights,
-    exact intermediates) at the block tolerance of two chained GEMMs."""
+    exact intermediates) at the block tolerance of two chained GEMMs; with I a
+    multiple of 128 silu(gate) * up comes from the gate+up epilogue (five
+    launches), else from an elementwise kernel between the GEMMs (six)."""
+    import quantized_gemm_tma_gb300 as hq
     from gpu_helpers import DevWeight
-    seed, wt, t, e, inter, k, n, topk = FFN[idx]
+    seed, wt, t, e, inter, k, n, topk, fused = FFN[idx]
     rng = np.random.default_rng(seed)
-    if wt == "mxfp4":
-        w13, acts, r = synth.moe_mxfp4(seed, t, num_experts=e, n=2 * inter, k=k, topk=topk)
-        w2, _, _ = synth.moe_mxfp4(seed + 100, 1, num_experts=e, n=n, k=inter, topk=1)
-    else:
-        w13 = synth.quantize_int_groupwise(rng.standard_normal((e, 2 * inter, k)) * 0.02, 4, 128, False, "bf16")
-        w2 = synth.quantize_int_groupwise(rng.standard_normal((e, n, inter)) * 0.02, 4, 64, False, "bf16")
-        acts = synth.make_activations(rng, t, k, "bf16")
-        r = synth.make_routing(rng, t, e, topk)
+    w13 = _ffn_weight(wt, rng, e, 2 * inter, k, seed)
+    w2 = _ffn_weight(wt, rng, e, n, inter, seed + 100)
+    acts = synth.make_activations(rng, t, k, "bf16")
+    r = synth.make_routing(rng, t, e, topk)
     got, st = _run_ffn(DevWeight(w13), DevWeight(w2), acts, r, n)
     assert st == 0
+    assert hq.hq_last_plan()["launches"] == (5 if fused else 6), hq.hq_last_plan()
     ref = oracle.moe_ffn(oracle.decode_activations("bf16", acts.data), r.topk_ids, r.topk_w, _expert_fn(w13),
                          _expert_fn(w2), intermediate=None)
     check_ffn(got, ref, f"moe ffn {FFN[idx]}")
