@@ -403,6 +403,24 @@ hq_status hq_moe_grouped_gemm(const hq_weight_desc* wdesc, const void* w_t, int3
 hq_status hq_selftest_wait_timeout(void* workspace, hq_stream_t stream);
 
 /*
+ * hq_mxfp8_quantize — activations to MXFP8, the activation side of the
+ * W4A8-MXFP4 product ([LAUNCH] paragraph "Efficient W4A8-MXFP4 inference on
+ * existing GPUs": MXFP4 weights with 8-bit floating-point activations).  OCP
+ * MX v1.0 conversion with e4m3 elements, per row and per 32 along K:
+ *   E = clamp(floor(log2(max |x|)) - 8 + 127, 0, 254)   (all-zero block: 0)
+ *   q = e4m3(x / 2^(E - 127)), round to nearest even, saturating at +-448,
+ *       the sign of zero kept
+ *
+ * m, k       rows and columns (k % 32 == 0; m = 0 is a no-op)
+ * x, ldx     bf16 [m][k], row stride ldx elements (x 16-byte aligned, ldx % 8 == 0)
+ * q, ldq     e4m3 bytes [m][k] out, row stride ldq bytes (q 8-byte aligned, ldq % 8 == 0)
+ * e, lde     UE8M0 bytes [m][k/32] out, row stride lde bytes
+ * Non-finite inputs give unspecified codes.  Asynchronous.
+ */
+hq_status hq_mxfp8_quantize(int32_t m, int32_t k, const void* x, int64_t ldx, void* q, int64_t ldq, void* e,
+                            int64_t lde, hq_stream_t stream);
+
+/*
  * hq_status_read — synchronise `stream` and read the device status word of a
  * workspace (HQ_OK when no device-side error was recorded).  With clear != 0
  * the word is reset to HQ_OK afterwards.

@@ -38,7 +38,7 @@ EXPORTS = [
     "hq_gemm_workspace_size", "hq_workspace_init", "hq_gemm", "hq_gemm_noalloc", "hq_moe_workspace_size",
     "hq_moe_gemm", "hq_moe_ffn_workspace_size", "hq_moe_ffn", "hq_moe_grouped_workspace_size",
     "hq_moe_grouped_gemm", "hq_status_read", "hq_last_plan", "hq_plan_query", "hq_selftest_wait_timeout",
-    "hq_moe_plan_query", "hq_tuning_reload",
+    "hq_moe_plan_query", "hq_tuning_reload", "hq_mxfp8_quantize",
 ]
 
 #: size of the fixed device scratch behind hq_gemm_noalloc
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
             "hq_selftest_wait_timeout": ([vp, vp], i32),
             "hq_moe_plan_query": ([dp, i32, i32, i32, i64, ctypes.POINTER(PlanInfo)], i32),
             "hq_tuning_reload": ([], None),
+            "hq_mxfp8_quantize": ([i32, i32, vp, i64, vp, i64, vp, i64, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -244,6 +245,11 @@ def _plan_dict(info: PlanInfo) -> dict:
 
 def hq_selftest_wait_timeout(workspace, stream=None) -> None:
     _check(lib().hq_selftest_wait_timeout(_ptr(workspace), _stream(stream)), "hq_selftest_wait_timeout")
+
+
+def hq_mxfp8_quantize(m: int, k: int, x, ldx: int, q, ldq: int, e, lde: int, stream=None) -> None:
+    _check(lib().hq_mxfp8_quantize(m, k, _ptr(x), ldx, _ptr(q), ldq, _ptr(e), lde, _stream(stream)),
+           "hq_mxfp8_quantize")
 
 
 def hq_last_plan() -> dict:

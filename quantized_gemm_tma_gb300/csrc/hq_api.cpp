@@ -799,6 +799,21 @@ hq_status hq_moe_plan_query(const hq_weight_desc* wdesc, int32_t tokens, int32_t
   return HQ_OK;
 }
 
+hq_status hq_mxfp8_quantize(int32_t m, int32_t k, const void* x, int64_t ldx, void* q, int64_t ldq, void* e,
+                            int64_t lde, hq_stream_t stream) {
+  if (m < 0 || k <= 0 || k % 32 != 0 || k > kMaxDim) return HQ_ERR_INVALID_ARG;
+  if (m == 0) return HQ_OK;
+  if (m > (1 << 30)) return HQ_ERR_UNSUPPORTED;
+  if (!x || !q || !e || ldx < k || ldq < k || lde < k / 32) return HQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || ldx % 8 != 0 || (reinterpret_cast<uintptr_t>(q) & 7u) || ldq % 8 != 0) return HQ_ERR_ALIGNMENT;
+  DevInfo di;
+  hq_status st = device_info(&di);
+  if (st != HQ_OK) return st;
+  return launch_mxfp8_quantize(x, ldx, m, k, q, ldq, e, lde, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? HQ_OK
+             : HQ_ERR_CUDA;
+}
+
 // ------------------------------------------------------------------ MoE
 hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int32_t topk, int32_t atype,
                                 size_t* bytes) {

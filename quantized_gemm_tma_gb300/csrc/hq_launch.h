@@ -73,6 +73,10 @@ uint32_t fp8_smem_bytes(int stages, int bn);
 // selftest.cu: one CTA whose bounded wait runs out and records HQ_ERR_DEVICE_TIMEOUT in *status
 cudaError_t launch_wait_timeout(int* status, cudaStream_t stream);
 
+// quant.cu: x bf16 [m][ldx] -> e4m3 codes [m][ldq] and UE8M0 exponents [m][lde] (k % 32 == 0)
+cudaError_t launch_mxfp8_quantize(const void* x, int64_t ldx, int m, int k, void* q, int64_t ldq, void* e,
+                                  int64_t lde, cudaStream_t stream);
+
 // moe.cu
 cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, int bn, int* expert_offsets,
                              int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* status,

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def _header_functions():
     src = open(os.path.join(ROOT, "include", "hq.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(hq_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(hq_[a-z0-9_]+)\s*\(", src)))
 
 
 @pytest.fixture(scope="module")
@@ -201,3 +201,16 @@ def test_noalloc_rejects_problems_beyond_the_scratch(hq):
         with pytest.raises(hq.HQError) as ei:
             hq.hq_gemm_noalloc(d, fake, 64, "bf16", fake, 16384, None, fake, 16384, flags, None, None)
         assert ei.value.status == hq.HQ_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_mxfp8_quantize_host_validation(hq):
+    fake = 0x10000
+    for args, want in [((4, 48, fake, 48, fake, 48, fake, 2), hq.HQ_ERR_INVALID_ARG),        # k % 32
+                       ((4, 64, fake, 60, fake, 64, fake, 2), hq.HQ_ERR_INVALID_ARG),        # ldx < k
+                       ((4, 64, fake + 8, 64, fake, 64, fake, 2), hq.HQ_ERR_ALIGNMENT),      # x not 16-byte aligned
+                       ((4, 64, fake, 68, fake, 64, fake, 2), hq.HQ_ERR_ALIGNMENT),          # ldx % 8
+                       ((4, 64, fake, 64, fake + 4, 64, fake, 2), hq.HQ_ERR_ALIGNMENT)]:     # q not 8-byte aligned
+        with pytest.raises(hq.HQError) as ei:
+            hq.hq_mxfp8_quantize(*args)
+        assert ei.value.status == want, (args, ei.value.status)
+    hq.hq_mxfp8_quantize(0, 64, 0, 64, 0, 64, 0, 2)     # no rows: no-op without a device
