@@ -76,7 +76,9 @@ typedef enum {
 typedef enum {
   HQ_A_BF16 = 0,
   HQ_A_FP16 = 1,
-  HQ_A_FP8_E4M3 = 2   /* with float32 per-token, per-128-K-group scales */
+  HQ_A_FP8_E4M3 = 2,  /* with float32 per-token, per-128-K-group scales */
+  HQ_A_MXFP8_E4M3 = 3 /* MXFP8: e4m3 codes with one UE8M0 exponent per 32 along K (from hq_mxfp8_quantize);
+                         against MXFP4 weights this is the W4A8-MXFP4 product */
 } hq_atype;
 
 /* Scale types ([README] Key Features: BF16, FP16, UE8M0; float32 for FP8 block scales). */
@@ -220,11 +222,18 @@ hq_status hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);
  * w_t       hq_transform output for wdesc
  * m         rows of X and Y (0 is a no-op); at most 2^30, with
  *           (m/16 + 1) * ceil(n/128) below 2^31 (HQ_ERR_UNSUPPORTED beyond)
- * atype     hq_atype; INT with group scales needs stype == atype; MXFP4,
- *           NVFP4 and MXINT4 need BF16; FP8 weights need FP8 activations
+ * atype     hq_atype; INT with group scales needs stype == atype; MXFP4
+ *           takes BF16 or MXFP8 (W4A8-MXFP4, [LAUNCH] paragraph "Efficient
+ *           W4A8-MXFP4 inference on existing GPUs"; k % 128 == 0); NVFP4 and
+ *           MXINT4 need BF16; FP8 weights need FP8 activations
  * x, ldx    X [m][k] row-major, row stride ldx elements (ldx >= k; the row
  *           pitch a multiple of 16 bytes; x 16-byte aligned)
- * x_scales  FP8 activations only: float32 [m][ceil(k/128)] row-major
+ * x_scales  FP8 activations: float32 [m][ceil(k/128)] row-major (16-byte
+ *           aligned).  MXFP8 activations: the UE8M0 bytes [m][k/32]
+ *           row-major, as hq_mxfp8_quantize writes them with lde = k/32
+ *           (4-byte aligned).  Otherwise ignored.
+ *           W4A8-MXFP4 computes Y = sum_k e4m3(x)·2^(Ex-127)·e2m1(w)·2^(Ew-127)
+ *           with the block-scaled MMA (one exponent of each operand per 32 K)
  * y, ldy    Y [m][n] row-major, bf16 for BF16/FP8 activations, fp16 for FP16;
  *           y 16-byte aligned, ldy even; with ldy a multiple of 8 the rows are
  *           written by tensor stores, otherwise by plain stores
@@ -235,7 +244,7 @@ hq_status hq_workspace_init(void* workspace, size_t bytes, hq_stream_t stream);
  * return before any launch; device timeouts go to the workspace status word.
  */
 hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32_t atype,
-                  const void* x, int64_t ldx, const float* x_scales, void* y, int64_t ldy,
+                  const void* x, int64_t ldx, const void* x_scales, void* y, int64_t ldy,
                   void* workspace, size_t ws_bytes, uint32_t flags, hq_stream_t stream);
 
 /* hq_gemm_noalloc only: clear the scratch's status word and counters first. */
@@ -281,7 +290,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
  * stream or order them with events.
  */
 hq_status hq_gemm_noalloc(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32_t atype,
-                          const void* x, int64_t ldx, const float* x_scales, void* y, int64_t ldy,
+                          const void* x, int64_t ldx, const void* x_scales, void* y, int64_t ldy,
                           uint32_t flags, int32_t* device_status, hq_stream_t stream);
 
 /*

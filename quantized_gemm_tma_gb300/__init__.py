@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(PKG, "libhq.so")
 HQ_OK, HQ_ERR_INVALID_ARG, HQ_ERR_UNSUPPORTED, HQ_ERR_ALIGNMENT = 0, 1, 2, 3
 HQ_ERR_WORKSPACE_TOO_SMALL, HQ_ERR_CUDA, HQ_ERR_DEVICE_TIMEOUT, HQ_ERR_ARCH, HQ_ERR_INVALID_VALUE = 4, 5, 6, 7, 8
 HQ_W_INT4, HQ_W_INT6, HQ_W_MXFP4, HQ_W_FP8_E4M3, HQ_W_NVFP4, HQ_W_MXINT4 = 0, 1, 2, 3, 4, 5
-HQ_A_BF16, HQ_A_FP16, HQ_A_FP8_E4M3 = 0, 1, 2
+HQ_A_BF16, HQ_A_FP16, HQ_A_FP8_E4M3, HQ_A_MXFP8_E4M3 = 0, 1, 2, 3
 HQ_S_BF16, HQ_S_FP16, HQ_S_FP32, HQ_S_UE8M0, HQ_S_E4M3 = 0, 1, 2, 3, 4
 HQ_FLAG_BATCH_INVARIANT = 0x1
 HQ_FLAG_NOALLOC_RESET = 0x100
@@ -29,7 +29,7 @@ HQ_MOE_GROUPED_CONTIGUOUS, HQ_MOE_GROUPED_MASKED = 0, 1
 
 WTYPES = {"int4": HQ_W_INT4, "int6": HQ_W_INT6, "mxfp4": HQ_W_MXFP4, "fp8": HQ_W_FP8_E4M3, "nvfp4": HQ_W_NVFP4,
           "mxint4": HQ_W_MXINT4}
-ATYPES = {"bf16": HQ_A_BF16, "fp16": HQ_A_FP16, "fp8": HQ_A_FP8_E4M3}
+ATYPES = {"bf16": HQ_A_BF16, "fp16": HQ_A_FP16, "fp8": HQ_A_FP8_E4M3, "mxfp8": HQ_A_MXFP8_E4M3}
 STYPES = {"bf16": HQ_S_BF16, "fp16": HQ_S_FP16, "fp32": HQ_S_FP32, "ue8m0": HQ_S_UE8M0, "e4m3": HQ_S_E4M3}
 
 #: every symbol include/hq.h declares

@@ -297,6 +297,41 @@ __device__ __forceinline__ void dq_mxint4(const uint4 q, uint32_t E, uint32_t (&
   }
 }
 
+// MXFP4 chunk for the 8-bit A operand (W4A8): 32 e2m1 codes -> 32 e4m3
+// bytes in K order, four per 32-bit word (one TMEM column holds four
+// consecutive K).  Every e2m1 value is exact in e4m3; the UE8M0 exponent is
+// applied by the block-scaled MMA.  Word j of a chunk holds k = 8j + e, element
+// e in nibble e / 2 + 4 (e % 2); the low three bits of a code index a byte
+// table of e4m3 magnitudes, bit 3 is the sign (e4m3 bit 7).
+__device__ __forceinline__ void dq_mxfp4_e4m3(const uint4 q, uint32_t (&o)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  constexpr uint32_t kLo = 0x3C383000u, kHi = 0x4C484440u;  // e4m3 of 0, .5, 1, 1.5 | 2, 3, 4, 6
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t a = w[j] & 0x0F0F0F0Fu, b = (w[j] >> 4) & 0x0F0F0F0Fu;  // nibbles 0,2,4,6 | 1,3,5,7
+    const uint32_t v[2] = {__byte_perm(a, b, 0x6420u), __byte_perm(a, b, 0x7531u)};  // k = 8j + 0..3 | 4..7
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t x = v[h] & 0x07070707u;
+      x = (x | (x >> 4)) & 0x00FF00FFu;
+      x = (x | (x >> 8)) & 0x0000FFFFu;  // the four table indices as byte selectors
+      o[2 * j + h] = __byte_perm(kLo, kHi, x) | ((v[h] & 0x08080808u) << 4);
+    }
+  }
+}
+
+// W4A8 scale factors of one K-block, in the TMEM layout the block-scaled MMA
+// reads: for lane l of every lane quarter, column j of a 4-column group holds
+// the UE8M0 exponent of row (or token) 32j + l, the same byte in all four byte
+// positions.  wordA/wordB: the exponents of the four 32-K sub-blocks of the
+// K-block in bytes 0..3; sub selects one.
+__device__ __forceinline__ void st_mx_scales(uint32_t taddr, const uint32_t (&words)[4], int sub) {
+  uint32_t v[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = ((words[j] >> (8 * sub)) & 0xFFu) * 0x01010101u;
+  dev::tmem_st4(taddr, v[0], v[1], v[2], v[3]);
+}
+
 // All lanes wait; the outcome is made warp-uniform so that the .sync.aligned
 // tcgen05 instructions that follow are always executed by the full warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -443,6 +478,12 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // of its rows per warp, so the four warps sharing a scheduler are at
   // different points of their pipelines instead of in lock step.
   constexpr bool kStream = KPS == 2;
+  // W4A8: e4m3 activations (one 128-byte swizzled slab per K-block instead of
+  // two of bf16), e4m3 weights in TMEM (32 columns per K-block: A at columns
+  // [0, 32) of each 64-column A slot, UE8M0 scale factors in [32, 64)), and
+  // block-scaled K32 MMAs.
+  constexpr bool A8 = FMT == static_cast<int>(WFmt::MXFP4_A8);
+  constexpr uint32_t kSlabsKb = A8 ? 1u : 2u;  // activation slabs per K-block
   // With streams, issuer p takes K-block p of every stage, i.e. the K-blocks
   // of streams p and 2 + p alternately.
   constexpr int KR = kKRing / ISS;  // promotion: accumulator ring per issuer
@@ -457,7 +498,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   const uint32_t tile_bytes = p.tile_bytes;
   const uint32_t w_stage = (KPS * tile_bytes + 1023u) & ~1023u;
   const uint32_t slab = static_cast<uint32_t>(bn) * 128u;  // bn rows x 64 K (128 bytes, swizzled)
-  const uint32_t x_stage = 2u * KPS * slab;
+  const uint32_t x_stage = kSlabsKb * KPS * slab;
   uint8_t* x_st = smem;                    // slabs first: 1024-byte aligned at any bn
   uint8_t* w_st = smem + SX * x_stage;
   uint64_t* w_full = reinterpret_cast<uint64_t*>(w_st + SW * w_stage);
@@ -643,9 +684,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           // past the end of X are zero-filled by the tensor copy, and rows
           // past the unit belong to other experts: their output columns are
           // never stored
-          dev::mbar_arrive_expect_tx(&x_full[rg.s], 2u * cnt * slab);
-          for (int z = 0; z < 2 * cnt; ++z)
-            dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], (2 * kb + z) * 64, u.xrow0);
+          const int zs = static_cast<int>(kSlabsKb) * cnt;
+          dev::mbar_arrive_expect_tx(&x_full[rg.s], static_cast<uint32_t>(zs) * slab);
+          for (int z = 0; z < zs; ++z)
+            dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], A8 ? (kb + z) * 128 : (2 * kb + z) * 64,
+                             u.xrow0);
         }
         rg.next(SX);
         ++issued;
@@ -708,7 +751,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               ok = false;
               break;
             }
-            const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + 2u * q * slab;
+            const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * q * slab;
             const uint32_t d_tmem = promote ? tmem + kAccCol0 + static_cast<uint32_t>(ks * BNMAX)
                                             : tmem + kAccCol0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = promote || first;
@@ -719,11 +762,24 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               }
               HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
               dev::tc_fence_after();
-              const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(t * 64 + h * 32);
+              if constexpr (A8) {
+                // half h = 32-K sub-blocks 2h, 2h + 1: A at t*64 + h*16 + 8i,
+                // their scale factors at t*64 + 32 + h*16 + 8i (A) and + 4 (B)
+                const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(t * 64 + h * 16);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bdesc = dev::sw128_desc(xs + h * slab + kk * 32);
-                dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && h == 0 && kk == 0) ? 0u : 1u);
+                for (int i = 0; i < 2; ++i) {
+                  const uint64_t bdesc = dev::sw128_desc(xs + (2 * h + i) * 32);
+                  const uint32_t sfa = a_tmem + 32u + static_cast<uint32_t>(i * 8);
+                  dev::mma_mx_ts(d_tmem, a_tmem + i * 8, bdesc, idesc, sfa, sfa + 4u,
+                                 (fresh && h == 0 && i == 0) ? 0u : 1u);
+                }
+              } else {
+                const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(t * 64 + h * 32);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t bdesc = dev::sw128_desc(xs + h * slab + kk * 32);
+                  dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && h == 0 && kk == 0) ? 0u : 1u);
+                }
               }
               dev::tc_commit(&a_empty[2 * t + h]);
             }
@@ -742,15 +798,25 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             }
             HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
             dev::tc_fence_after();
-            const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + 2u * pidx * slab;
+            const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * pidx * slab;
             const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(slot) * 64u;
             const uint32_t d_tmem = promote ? tmem + kAccCol0 + static_cast<uint32_t>(ks * BNMAX)
                                             : tmem + kAccCol0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = promote || first;
+            if constexpr (A8) {
+              // 32-K sub-block c: A at slot*64 + 8c, scale factors at slot*64 + 32 + 8c (A), + 4 (B)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bdesc = dev::sw128_desc(xs + (kk >> 2) * slab + (kk & 3) * 32);
-              dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && kk == 0) ? 0u : 1u);
+              for (int c = 0; c < 4; ++c) {
+                const uint64_t bdesc = dev::sw128_desc(xs + c * 32);
+                const uint32_t sfa = a_tmem + 32u + static_cast<uint32_t>(c * 8);
+                dev::mma_mx_ts(d_tmem, a_tmem + c * 8, bdesc, idesc, sfa, sfa + 4u, (fresh && c == 0) ? 0u : 1u);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t bdesc = dev::sw128_desc(xs + (kk >> 2) * slab + (kk & 3) * 32);
+                dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && kk == 0) ? 0u : 1u);
+              }
             }
             dev::tc_commit(&a_empty[slot]);
             if (promote) dev::tc_commit(&k_full[ks]);
@@ -865,6 +931,64 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             // The first half is published after the second is converted (the
             // arithmetic covers its TMEM stores); the second right away.
             const uint32_t aph = (ca & 1u) ^ 1u;
+            if constexpr (A8) {
+              // scale exponents of this K-block: weight rows 32j + lane (from
+              // the tile) and tokens 32j + lane (from the activations' UE8M0
+              // array; tokens past the unit get 2^0)
+              uint32_t ww[4], xw[4];
+              const int kbg = kb + pos;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int tok = 32 * j + static_cast<int>(lane);
+                ww[j] = *reinterpret_cast<const uint32_t*>(wsm + p.scale_off + (32 * j + lane) * 4);
+                xw[j] = tok < u.rows ? *reinterpret_cast<const uint32_t*>(
+                                           p.x_mx + static_cast<int64_t>(u.row0 + tok) * p.ld_mx + kbg * 4)
+                                     : 0x7F7F7F7Fu;
+              }
+              uint32_t o8[2][8];
+              auto conv8 = [&](int c0) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                  dq_mxfp4_e4m3(*reinterpret_cast<const uint4*>(wsm + ((c0 + i) * kTileN + r) * 16), o8[i]);
+              };
+              auto st_half = [&](int h) {
+                uint32_t o16[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  o16[i] = o8[0][i];
+                  o16[8 + i] = o8[1][i];
+                }
+                dev::tmem_st16(a_lane + h * 16, o16);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                  st_mx_scales(a_lane + 32 + h * 16 + i * 8, ww, 2 * h + i);
+                  st_mx_scales(a_lane + 32 + h * 16 + i * 8 + 4, xw, 2 * h + i);
+                }
+              };
+              conv8(0);
+              if (!warp_wait(&a_empty[2 * t], aph, abort_flag)) {
+                ok = false;
+                break;
+              }
+              dev::tc_fence_after();
+              st_half(0);
+              conv8(2);
+              __syncwarp();
+              if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
+              publish(2 * t);
+              if (!warp_wait(&a_empty[2 * t + 1], aph, abort_flag)) {
+                ok = false;
+                break;
+              }
+              dev::tc_fence_after();
+              st_half(1);
+              publish(2 * t + 1);
+              ++ca;
+              if (pos < cnt) ++cpos;
+              ++ts;
+              rg.next(SW);
+              continue;
+            }
             uint32_t o[2][16];
             convert2(wsm, 0, o);
             if (trace_me) HQ_TRACE(5 + t, tr, (12ull << 24) | ts);
@@ -936,8 +1060,19 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         uint4 qc[G];
         uint2 qh[G];
         uint32_t zz[G], ss[G];
+        [[maybe_unused]] uint32_t ww[4], xw[4];  // W4A8: weight / token scale exponents of the K-block
         if (real) {
           const uint8_t* wsm = w_st + rg.s * w_stage + gi * tile_bytes;
+          if constexpr (A8) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int tok = 32 * j + static_cast<int>(lane);
+              ww[j] = *reinterpret_cast<const uint32_t*>(wsm + p.scale_off + (32 * j + lane) * 4);
+              xw[j] = tok < u.rows ? *reinterpret_cast<const uint32_t*>(
+                                         p.x_mx + static_cast<int64_t>(u.row0 + tok) * p.ld_mx + (kb + gi) * 4)
+                                   : 0x7F7F7F7Fu;
+            }
+          }
 #pragma unroll
           for (int i = 0; i < G; ++i) {
             const int c = sub * G + i;
@@ -976,7 +1111,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         // convert first: the arithmetic covers the previous K-block's TMEM
         // stores still in flight and the MMA that frees this K-block's slot
         uint32_t o[G][16];
-        if (real) {
+        [[maybe_unused]] uint32_t o8[8];
+        if (real && A8) {
+          dq_mxfp4_e4m3(qc[0], o8);
+        } else if (real) {
 #pragma unroll
           for (int i = 0; i < G; ++i) {
             if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
@@ -1018,8 +1156,15 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           }
           if (trace_me) HQ_TRACE(5 + gi, tr, (6ull << 24) | ts);
           dev::tc_fence_after();
+          if constexpr (A8) {
+            // 32-K sub-block `sub` (one per warp, G = 1): e4m3 codes and both scale groups
+            dev::tmem_st8(a_lane + slot * 64 + sub * 8, o8);
+            st_mx_scales(a_lane + slot * 64 + 32 + sub * 8, ww, sub);
+            st_mx_scales(a_lane + slot * 64 + 32 + sub * 8 + 4, xw, sub);
+          } else {
 #pragma unroll
-          for (int i = 0; i < G; ++i) dev::tmem_st16(a_lane + slot * 64 + (sub * G + i) * 16, o[i]);
+            for (int i = 0; i < G; ++i) dev::tmem_st16(a_lane + slot * 64 + (sub * G + i) * 16, o[i]);
+          }
           pend = slot;
           if (trace_me) HQ_TRACE(5 + gi, tr, (7ull << 24) | ts);
           ++ca;

@@ -476,7 +476,7 @@ int wna16_fmt(int wtype) {
 // Heuristic for one GB300: tokens per tile from M; problems with fewer than
 // four tiles per SM are split stream-K so every SM streams the same number
 // of weight K-blocks.
-DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_t flags) {
+DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_t flags, bool a8 = false) {
   DensePlan p{};
   // Batch invariance: one configuration for every M (64-token tiles of the
   // two-K-block class, whose two issuers accumulate even and odd K-blocks
@@ -486,6 +486,9 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   p.bn = inv ? kInvariantBn : m <= 64 ? std::max(16, cdiv(m, 16) * 16) : (m <= 128 ? 128 : (m <= 192 ? 192 : 256));
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
   if (!inv && forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) p.bn = forced_bn;
+  // W4A8: tiles of at most 128 tokens (the scale factors of one MMA's tokens
+  // fill one group of TMEM columns)
+  if (a8) p.bn = std::min(p.bn, 128);
   p.cls = wna16_class(p.bn);
   p.m_tiles = cdiv(m, p.bn);
   p.tiles = p.m_tiles * L.n_tiles;
@@ -599,7 +602,7 @@ extern "C" {
 
 hq_status hq_gemm_workspace_size(const hq_weight_desc* desc, int32_t m, int32_t atype, size_t* bytes) {
   if (!desc || !bytes || m < 0) return HQ_ERR_INVALID_ARG;
-  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_MXFP8_E4M3) return HQ_ERR_INVALID_ARG;
   Layout L;
   hq_status st = make_layout(*desc, &L);
   if (st != HQ_OK) return st;
@@ -613,7 +616,7 @@ hq_status hq_gemm_workspace_size(const hq_weight_desc* desc, int32_t m, int32_t 
         const Fp8Plan p = plan_fp8(L, m, sms, 232448, 0);
         best = std::max(best, splitk_bytes(p.splits, m, L.n_pad));
       } else {
-        const DensePlan p = plan_wna16(L, m, sms, 232448, 0);
+        const DensePlan p = plan_wna16(L, m, sms, 232448, 0, atype == HQ_A_MXFP8_E4M3);
         if (p.stream_k) best = std::max(best, streamk_bytes(p.grid, p.bn));
       }
     }
@@ -624,31 +627,36 @@ hq_status hq_gemm_workspace_size(const hq_weight_desc* desc, int32_t m, int32_t 
 }
 
 hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32_t atype, const void* x,
-                  int64_t ldx, const float* x_scales, void* y, int64_t ldy, void* workspace, size_t ws_bytes,
+                  int64_t ldx, const void* x_scales, void* y, int64_t ldy, void* workspace, size_t ws_bytes,
                   uint32_t flags, hq_stream_t stream) {
   if (!wdesc || m < 0) return HQ_ERR_INVALID_ARG;
   Layout L;
   hq_status st = make_layout(*wdesc, &L);
   if (st != HQ_OK) return st;
   if (L.num_experts != 1) return HQ_ERR_INVALID_ARG;
-  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_MXFP8_E4M3) return HQ_ERR_INVALID_ARG;
   if (m == 0) return HQ_OK;
   if (m > (1 << 30) || !tiles_fit(m, 0, L.n_tiles)) return HQ_ERR_UNSUPPORTED;
   if (!w_t || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;
   if (ldx < L.k || ldy < L.n) return HQ_ERR_INVALID_ARG;
   const bool fp8 = L.wtype == HQ_W_FP8_E4M3;
+  const bool a8 = atype == HQ_A_MXFP8_E4M3;  // W4A8-MXFP4
   if (fp8 != (atype == HQ_A_FP8_E4M3)) return HQ_ERR_UNSUPPORTED;
-  if (fp8 && !x_scales) return HQ_ERR_INVALID_ARG;
+  if (a8 && L.wtype != HQ_W_MXFP4) return HQ_ERR_UNSUPPORTED;
+  if (a8 && L.k % kTileK != 0) return HQ_ERR_INVALID_ARG;
+  if ((fp8 || a8) && !x_scales) return HQ_ERR_INVALID_ARG;
   if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel) {
     if ((L.stype == HQ_S_BF16) != (atype == HQ_A_BF16)) return HQ_ERR_UNSUPPORTED;
   }
-  if ((L.wtype == HQ_W_MXFP4 || L.wtype == HQ_W_NVFP4 || L.wtype == HQ_W_MXINT4) && atype != HQ_A_BF16)
-    return HQ_ERR_UNSUPPORTED;
-  const uint32_t xelem = fp8 ? 1 : 2;
+  if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && a8) return HQ_ERR_UNSUPPORTED;
+  if ((L.wtype == HQ_W_NVFP4 || L.wtype == HQ_W_MXINT4) && atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  if (L.wtype == HQ_W_MXFP4 && atype != HQ_A_BF16 && !a8) return HQ_ERR_UNSUPPORTED;
+  const uint32_t xelem = (fp8 || a8) ? 1 : 2;
   if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(w_t) & 255u))
     return HQ_ERR_ALIGNMENT;
   if ((ldx * xelem) % 16 != 0 || (ldy * 2) % 4 != 0) return HQ_ERR_ALIGNMENT;
   if (fp8 && !aligned16(x_scales)) return HQ_ERR_ALIGNMENT;
+  if (a8 && (reinterpret_cast<uintptr_t>(x_scales) & 3u)) return HQ_ERR_ALIGNMENT;
   if (ws_bytes < kAlign) return HQ_ERR_WORKSPACE_TOO_SMALL;
   DevInfo di;
   st = device_info(&di);
@@ -667,7 +675,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
     p.expert_stride = L.expert_stride;
     p.tile_bytes = L.tile_bytes;
     p.blk_scale = reinterpret_cast<const float*>(wt + L.blk_off);
-    p.x_scale = x_scales;
+    p.x_scale = static_cast<const float*>(x_scales);
     p.n = L.n; p.n_pad = L.n_pad; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = m;
     p.bn = pl.bn; p.m_tiles = pl.m_tiles; p.stages = pl.stages;
     p.splits = pl.splits; p.kb_per_split = pl.kb_per_split;
@@ -686,7 +694,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
     return launch_fp8(p, tm, pl.bn, pl.grid, pl.smem, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
   }
 
-  const DensePlan pl = plan_wna16(L, m, di.sms, di.smem_optin, flags);
+  const DensePlan pl = plan_wna16(L, m, di.sms, di.smem_optin, flags, a8);
   if (pl.stages < 2) return HQ_ERR_UNSUPPORTED;
   if (ws_bytes < kAlign + (pl.stream_k ? streamk_bytes(pl.grid, pl.bn) : 0)) return HQ_ERR_WORKSPACE_TOO_SMALL;
   GemmParams p{};
@@ -703,28 +711,32 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   p.stages = pl.stages; p.x_stages = pl.x_stages; p.groups = pl.groups;
   p.stream_k = pl.stream_k; p.iters = pl.iters; p.cluster = pl.cluster;
   p.promote = (pl.cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
-  p.idesc = idesc_f16(atype == HQ_A_BF16, 128, pl.bn);
+  p.idesc = a8 ? idesc_mx_e4m3(128, pl.bn) : idesc_f16(atype == HQ_A_BF16, 128, pl.bn);
+  p.x_mx = a8 ? static_cast<const uint8_t*>(x_scales) : nullptr;
+  p.ld_mx = L.k / 32;
   p.y = y; p.ldy = ldy;
   p.status = reinterpret_cast<int*>(ws);
   p.counters = reinterpret_cast<int*>(ws + kAlign);
   p.partials = reinterpret_cast<float*>(ws + kAlign + kCounterBytes);
   p.num_experts = 1;
-  // X [M][K]: one box = 64 columns (128 bytes, swizzled) of bn rows
-  const CUtensorMapDataType t16 = atype == HQ_A_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  // X [M][K]: one box = 128 bytes (64 bf16/fp16 or 128 e4m3 columns, swizzled) of bn rows
+  const CUtensorMapDataType t16 = atype == HQ_A_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   Wna16Maps maps;
-  st = encode_2d(&maps.x, t16, 2, x, L.k, m, ldx, 64, pl.bn);
+  st = a8 ? encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, x, L.k, m, ldx, 128, pl.bn)
+          : encode_2d(&maps.x, t16, 2, x, L.k, m, ldx, 64, pl.bn);
   if (st != HQ_OK) return st;
   // Y [M][N]: tensor stores of 16 tokens x 32 output rows when its row pitch
   // is a multiple of 16 bytes (the tensor-map stride rule); plain stores else
   p.y_tma = (ldy * 2) % 16 == 0 ? 1 : 0;
   maps.y = maps.x;
   if (p.y_tma) {
-    st = encode_2d(&maps.y, t16, 2, y, L.n, m, ldy, 32, 16, 0, false);
+    st = encode_2d(&maps.y, a8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : t16, 2, y, L.n, m, ldy, 32, 16, 0, false);
     if (st != HQ_OK) return st;
   }
   Wna16Launch l{};
   l.fmt = wna16_fmt(L.wtype);
-  l.bf16 = atype == HQ_A_BF16;
+  l.bf16 = atype != HQ_A_FP16;
+  if (a8) l.fmt = static_cast<int>(WFmt::MXFP4_A8);
   l.cls = pl.cls;
   l.moe = false;
   l.grid = pl.grid;
@@ -744,14 +756,16 @@ hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, i
   hq_status st = make_layout(*wdesc, &L);
   if (st != HQ_OK) return st;
   if (L.num_experts != 1) return HQ_ERR_INVALID_ARG;
-  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_MXFP8_E4M3) return HQ_ERR_INVALID_ARG;
   if (m > (1 << 30) || !tiles_fit(m, 0, L.n_tiles)) return HQ_ERR_UNSUPPORTED;
   const bool fp8 = L.wtype == HQ_W_FP8_E4M3;
   if (fp8 != (atype == HQ_A_FP8_E4M3)) return HQ_ERR_UNSUPPORTED;
+  const bool a8 = atype == HQ_A_MXFP8_E4M3;
+  if (a8 && (L.wtype != HQ_W_MXFP4 || L.k % kTileK != 0)) return HQ_ERR_UNSUPPORTED;
   if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && (L.stype == HQ_S_BF16) != (atype == HQ_A_BF16))
     return HQ_ERR_UNSUPPORTED;
-  if ((L.wtype == HQ_W_MXFP4 || L.wtype == HQ_W_NVFP4 || L.wtype == HQ_W_MXINT4) && atype != HQ_A_BF16)
-    return HQ_ERR_UNSUPPORTED;
+  if ((L.wtype == HQ_W_NVFP4 || L.wtype == HQ_W_MXINT4) && atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  if (L.wtype == HQ_W_MXFP4 && atype != HQ_A_BF16 && !a8) return HQ_ERR_UNSUPPORTED;
   *info = hq_plan_info{};
   if (m == 0) return HQ_OK;
   const size_t optin = static_cast<size_t>(smem_optin);
@@ -760,7 +774,7 @@ hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, i
     *info = hq_plan_info{pl.bn, pl.splits, pl.grid, 1, pl.stages, 0, 0, 0};
     return HQ_OK;
   }
-  const DensePlan pl = plan_wna16(L, m, sms, optin, flags);
+  const DensePlan pl = plan_wna16(L, m, sms, optin, flags, a8);
   if (pl.stages < 2) return HQ_ERR_UNSUPPORTED;
   *info = hq_plan_info{pl.bn, pl.cluster == 2 ? 2 : (pl.stream_k ? 0 : 1), pl.grid, 1, pl.stages, pl.cls, pl.groups,
                        0};
@@ -818,7 +832,7 @@ hq_status hq_mxfp8_quantize(int32_t m, int32_t k, const void* x, int64_t ldx, vo
 hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int32_t topk, int32_t atype,
                                 size_t* bytes) {
   if (!desc || !bytes || tokens < 0 || topk <= 0) return HQ_ERR_INVALID_ARG;
-  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_MXFP8_E4M3) return HQ_ERR_INVALID_ARG;
   Layout L;
   hq_status st = make_layout(*desc, &L);
   if (st != HQ_OK) return st;
@@ -841,7 +855,7 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   Layout L;
   hq_status st = make_layout(*wdesc, &L);
   if (st != HQ_OK) return st;
-  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_MXFP8_E4M3) return HQ_ERR_INVALID_ARG;
   if (L.num_experts > 1024) return HQ_ERR_UNSUPPORTED;
   if (tokens == 0) return HQ_OK;
   if (!w_t || !topk_ids || !topk_w || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;
@@ -939,7 +953,7 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
   int inter = 0;
   hq_status st = ffn_layouts(w13, w2, &L13, &L2, &inter);
   if (st != HQ_OK) return st;
-  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_MXFP8_E4M3) return HQ_ERR_INVALID_ARG;
   if (L13.num_experts > 1024) return HQ_ERR_UNSUPPORTED;
   if (tokens == 0) return HQ_OK;
   if (!w13_t || !w2_t || !topk_ids || !topk_w || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;
@@ -1046,7 +1060,7 @@ hq_status hq_moe_grouped_gemm(const hq_weight_desc* wdesc, const void* w_t, int3
   Layout L;
   hq_status st = make_layout(*wdesc, &L);
   if (st != HQ_OK) return st;
-  if (atype < HQ_A_BF16 || atype > HQ_A_FP8_E4M3) return HQ_ERR_INVALID_ARG;
+  if (atype < HQ_A_BF16 || atype > HQ_A_MXFP8_E4M3) return HQ_ERR_INVALID_ARG;
   if (L.num_experts > 1024) return HQ_ERR_UNSUPPORTED;
   if (rows == 0) return HQ_OK;
   if (!w_t || !expert_rows || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;

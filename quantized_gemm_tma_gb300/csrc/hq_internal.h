@@ -94,13 +94,22 @@ HQ_HD constexpr uint32_t idesc_f16(bool bf16, int m, int n) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
+// Block-scaled MMA (kind::mxf8f6f4.block_scale.scale_vec::1X), e4m3 x e4m3
+// with UE8M0 scale factors: A/B format 0 (E4M3) at bits 7-9 / 10-12, both
+// K-major, N >> 3 at bit 17, scale format E8M0 (bit 23), M >> 4 at bit 24,
+// scale-factor ids 0 (bits 4-5 for B, 29-30 for A), K = 32.
+HQ_HD constexpr uint32_t idesc_mx_e4m3(int m, int n) {
+  return (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24);
+}
 HQ_HD constexpr uint32_t idesc_e4m3(int m, int n) {
   return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // ------------------------------------------------------------------ GEMM
-enum class WFmt : int { INT4 = 0, INT6 = 1, MXFP4 = 2, NVFP4 = 3, MXINT4 = 4 };
+// MXFP4_A8: MXFP4 weights against MXFP8 activations (e4m3 codes with one
+// UE8M0 exponent per 32 along K), block-scaled MMA.
+enum class WFmt : int { INT4 = 0, INT6 = 1, MXFP4 = 2, NVFP4 = 3, MXINT4 = 4, MXFP4_A8 = 5 };
 
 struct GemmParams {
   const uint8_t* tiles;     // tile (e=0, nt=0, kt=0)
@@ -137,6 +146,8 @@ struct GemmParams {
   const int* x_base;        // [E]: X row of each expert's first routed row (its rows stand together in X)
   float* zbuf;              // [T*topk][n_pad] weighted per-pair outputs
   float* gate_buf;          // gated: [grid][bn max of the class][128] fp32 gate sums, one block per CTA
+  const uint8_t* x_mx;      // MXFP4_A8: activation UE8M0 exponents [m][k/32] (rows 4-byte aligned)
+  int64_t ld_mx;            // MXFP4_A8: row stride of x_mx in bytes
   int moe_out;              // kMoeOutZ, kMoeOutRowMap or kMoeOutRouted
 };
 

@@ -85,7 +85,7 @@ hq_status scratch_address(void** out) {
 }  // namespace
 
 extern "C" hq_status hq_gemm_noalloc(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32_t atype,
-                                     const void* x, int64_t ldx, const float* x_scales, void* y, int64_t ldy,
+                                     const void* x, int64_t ldx, const void* x_scales, void* y, int64_t ldy,
                                      uint32_t flags, int32_t* device_status, hq_stream_t stream) {
   if (!wdesc || m < 0) return HQ_ERR_INVALID_ARG;
   const bool reset = (flags & HQ_FLAG_NOALLOC_RESET) != 0;

@@ -11,6 +11,7 @@ cudaError_t launch_wna16_int6(const Wna16Launch&, const GemmParams&, const Wna16
 cudaError_t launch_wna16_mxfp4(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
 cudaError_t launch_wna16_nvfp4(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
 cudaError_t launch_wna16_mxint4(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
+cudaError_t launch_wna16_w4a8(const Wna16Launch&, const GemmParams&, const Wna16Maps&, cudaStream_t);
 
 cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const Wna16Maps& maps, cudaStream_t stream) {
   switch (l.fmt) {
@@ -19,6 +20,7 @@ cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const Wna16M
     case 2: return launch_wna16_mxfp4(l, p, maps, stream);
     case 3: return launch_wna16_nvfp4(l, p, maps, stream);
     case 4: return launch_wna16_mxint4(l, p, maps, stream);
+    case 5: return launch_wna16_w4a8(l, p, maps, stream);
     default: return cudaErrorInvalidValue;
   }
 }

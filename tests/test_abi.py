@@ -214,3 +214,20 @@ def test_mxfp8_quantize_host_validation(hq):
             hq.hq_mxfp8_quantize(*args)
         assert ei.value.status == want, (args, ei.value.status)
     hq.hq_mxfp8_quantize(0, 64, 0, 64, 0, 64, 0, 2)     # no rows: no-op without a device
+
+
+def test_w4a8_host_validation(hq):
+    """MXFP8 activations (W4A8-MXFP4) are taken only against MXFP4 weights,
+    with K a multiple of 128 and 4-byte aligned exponent rows; checked on the
+    host before any device query."""
+    fake = 0x10000
+    mx = hq.make_desc("mxfp4", "ue8m0", 256, 512, group_k=32)
+    i4 = hq.make_desc("int4", "bf16", 256, 512, group_k=128)
+    cases = [(i4, 512, fake, hq.HQ_ERR_UNSUPPORTED),                   # INT4 weights
+             (hq.make_desc("mxfp4", "ue8m0", 256, 544, group_k=32), 544, fake, hq.HQ_ERR_INVALID_ARG),  # K % 128
+             (mx, 512, None, hq.HQ_ERR_INVALID_ARG),                   # no exponents
+             (mx, 512, fake + 2, hq.HQ_ERR_ALIGNMENT)]                 # exponents not 4-byte aligned
+    for d, k, xs, want in cases:
+        with pytest.raises(hq.HQError) as ei:
+            hq.hq_gemm(d, fake, 16, "mxfp8", fake, k, xs, fake, 256, fake, 1 << 20, 0, None)
+        assert ei.value.status == want, (k, xs, ei.value.status)

@@ -152,3 +152,18 @@ def test_moe_plan_query_validation(hq):
         hq.hq_moe_plan_query(f8, 16, 2, SMS, OPTIN)
     assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
     assert hq.hq_moe_plan_query(d, 0, 8, SMS, OPTIN)["launches"] == 0
+
+
+def test_w4a8_plans(hq):
+    """W4A8-MXFP4 plans tiles of at most 128 tokens (the scale factors of one
+    MMA's tokens fill one TMEM column group), with the usual work splits."""
+    d = hq.make_desc("mxfp4", "ue8m0", 8192, 8192, group_k=32)
+    for m, bn, cls, split in ((1, 16, 0, CLUSTER), (16, 16, 0, CLUSTER), (48, 48, 1, CLUSTER),
+                              (128, 128, 2, CLUSTER), (1024, 128, 2, WHOLE), (4096, 128, 2, WHOLE)):
+        p = hq.hq_plan_query(d, m, "mxfp8", SMS, OPTIN)
+        assert (p["bn"], p["tile_class"], p["splits"]) == (bn, cls, split), (m, p)
+        if cls <= 1:
+            assert p["stages"] % 2 == 0, p
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_plan_query(hq.make_desc("int4", "bf16", 8192, 8192, group_k=128), 16, "mxfp8", SMS, OPTIN)
+    assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
