@@ -63,6 +63,10 @@ EXTRA = {
     "c4_fp8_block": {"n": 4096, "k": 7168, "ms": [64, 512, 4096], "copies": 6,
                      "workload": "dense W8A8 FP8: e4m3 weights with fp32 128x128 block scales, e4m3 activations "
                                  "with per-token per-128-K fp32 scales, N=4096, K=7168, M sweep {64,512,4096}"},
+    "w4a8_mxfp4": {"n": 8192, "k": 8192, "ms": [1, 16, 128, 1024, 4096], "copies": 8,
+                   "workload": "dense W4A8-MXFP4: MXFP4 weights (e2m1, UE8M0 per 32) against MXFP8 activations "
+                               "(e4m3, UE8M0 per 32, quantised from bf16 by hq_mxfp8_quantize before the timed "
+                               "calls), block-scaled MMA, N=K=8192, M sweep {1,16,128,1024,4096}"},
 }
 # FP8 dense peak: the measured bf16 peak times 2, the nominal fp8:bf16 ratio of
 # the tensor cores (4.5 : 2.25 PFLOP/s dense)
@@ -91,6 +95,8 @@ def extra_bytes(name: str, m: int) -> int:
     n, k = cfg["n"], cfg["k"]
     if name.startswith("c3"):   # 6-bit codes, fp16 row scales, fp16 activations
         return n * k * 3 // 4 + n * 2 + m * k * 2
+    if name.startswith("w4a8"):  # e2m1 codes + UE8M0 per 32; e4m3 activations + UE8M0 per 32
+        return n * k // 2 + n * k // 32 + m * k + m * k // 32
     kb = -(-k // 128)           # e4m3 weights, fp32 block scales, e4m3 activations, fp32 per-token scales
     return n * k + (-(-n // 128)) * kb * 4 + m * k + m * kb * 4
 
@@ -277,6 +283,11 @@ def run_gpu(args, rank: int, world: int):
                 atype = "fp16"
                 edesc = hq.make_desc("int6", "fp16", n_, k_, 1, 0, 1, True, False, to_dev(eq.codes),
                                      to_dev(eq.scales), None)
+            elif name.startswith("w4a8"):
+                eq = synth.quantize_mxfp4(np.random.default_rng(0).standard_normal((1, n_, k_)) * 0.02)
+                atype = "mxfp8"
+                edesc = hq.make_desc("mxfp4", "ue8m0", n_, k_, 1, 32, 1, True, False, to_dev(eq.codes),
+                                     to_dev(eq.scales), None)
             else:
                 eq, _ = synth.dense_fp8_block(0, 1, n_, k_)
                 atype = "fp8"
@@ -291,13 +302,30 @@ def run_gpu(args, rank: int, world: int):
             per = {}
             for m in cfg["ms"]:
                 erng = np.random.default_rng(100 + m)
-                a = synth.make_activations(erng, m, k_, atype)
-                xd = to_dev(a.data)
-                xsd = to_dev(np.ascontiguousarray(a.scales, np.float32)) if a.scales is not None else None
+                if atype == "mxfp8":
+                    # bf16 activations quantised on the device (MXFP8 codes and exponents)
+                    xb = to_dev(synth.to_bf16_bits(erng.standard_normal((m, k_))))
+                    xd = torch.empty((m, k_), dtype=torch.uint8, device=dev)
+                    xsd = torch.empty((m, k_ // 32), dtype=torch.uint8, device=dev)
+                    hq.hq_mxfp8_quantize(m, k_, xb, k_, xd, k_, xsd, k_ // 32, sh)
+                    torch.cuda.synchronize()
+                    # the quantiser's own time per call (CUDA events, 20 calls)
+                    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    q0.record(stream)
+                    for _ in range(20):
+                        hq.hq_mxfp8_quantize(m, k_, xb, k_, xd, k_, xsd, k_ // 32, sh)
+                    q1.record(stream)
+                    torch.cuda.synchronize()
+                    per_quant = q0.elapsed_time(q1) * 1e-3 / 20
+                else:
+                    a = synth.make_activations(erng, m, k_, atype)
+                    xd = to_dev(a.data)
+                    xsd = to_dev(np.ascontiguousarray(a.scales, np.float32)) if a.scales is not None else None
+                    per_quant = None
                 yd = torch.empty((m, n_), dtype=torch.float16 if atype == "fp16" else torch.bfloat16, device=dev)
                 wsd = torch.zeros(max(hq.hq_gemm_workspace_size(edesc, m, atype), 256), dtype=torch.uint8,
                                   device=dev)
-                per[m] = {"x": xd, "xs": xsd, "y": yd, "ws": wsd}
+                per[m] = {"x": xd, "xs": xsd, "y": yd, "ws": wsd, "quant_s": per_quant}
             extra[name] = {"desc": edesc, "wts": ewts, "atype": atype, "per": per, "cfg": cfg}
             del eq
 
@@ -517,7 +545,8 @@ def run_gpu(args, rank: int, world: int):
     for (name, m), v in per_x.items():
         extra_call((name, m))
         res["extra"].setdefault(name, {})[m] = {"s": statistics.mean(v), "s_min": min(v),
-                                                "plan": hq.hq_last_plan()}
+                                                "plan": hq.hq_last_plan(),
+                                                "quant_s": extra[name]["per"][m]["quant_s"]}
     for name, e in extra.items():
         st = hq.hq_status_read(e["per"][e["cfg"]["ms"][0]]["ws"], 0, sh)
         if st != 0:
@@ -716,7 +745,7 @@ def main():
         line["c1_graph"] = c1
     for name, per in res.get("extra", {}).items():
         cfg = EXTRA[name]
-        fp8 = name.startswith("c4")
+        fp8 = name.startswith("c4") or name.startswith("w4a8")
         tc_peak = pk["bf16_tflops"] * (FP8_PER_BF16 if fp8 else 1.0)
         esw = []
         for m in cfg["ms"]:
@@ -727,6 +756,8 @@ def main():
                         "tflops": round(fl / t / 1e12, 2), "gbs": round(by / t / 1e9, 1),
                         "roofline_frac": round(max(t_hbm, t_tc) / t, 3), "bound": "hbm" if t_hbm >= t_tc else "tensor",
                         "algorithmic_bytes": by, "plan": per[m]["plan"]})
+            if per[m].get("quant_s") is not None:
+                esw[-1]["mxfp8_quantize_us"] = round(per[m]["quant_s"] * 1e6, 2)
         line[name] = {"workload": cfg["workload"], "sweep": esw,
                       "tensor_peak_tflops": round(tc_peak, 1),
                       "tensor_peak_source": (f"measured bf16 x {FP8_PER_BF16} (nominal fp8:bf16 ratio)" if fp8

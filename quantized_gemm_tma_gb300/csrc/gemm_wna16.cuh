@@ -171,28 +171,38 @@ __device__ __forceinline__ uint32_t f16x2_of(float f) {
 //         rounds the product once, as (u - z) * s would be.
 //   fp16: OR with 1024.0 (0x6400) puts u (16u) in the mantissa; one FMA with
 //         1 (1/16) minus 1024 + z (64 + z) gives u - z exactly.
+// The constants of one (zero point, scale) group, computed once and applied to
+// every chunk of the group.
+struct Int4Consts {
+  uint32_t c_lo, c_hi, a_lo, a_hi, sc;
+};
 template <bool BF16, bool SCALE>
-__device__ __forceinline__ void dq_int4(const uint4 q, uint32_t z, uint32_t s16, uint32_t (&o)[16]) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  uint32_t c_lo, c_hi, a_lo, a_hi, sc = 0;
+__device__ __forceinline__ Int4Consts int4_consts(uint32_t z, uint32_t s16) {
+  Int4Consts k{};
   if constexpr (BF16) {
-    c_lo = 0x7E807E80u;  // 2^126
-    c_hi = 0x7C807C80u;  // 2^122
+    k.c_lo = 0x7E807E80u;  // 2^126
+    k.c_hi = 0x7C807C80u;  // 2^122
     // -z * 2^-7 and s * 2^7 are exact in bf16: take the top half of the fp32 bits
     const float zf = __uint_as_float(0x4B000000u | z) - 8388608.f;
     const uint32_t zb = __float_as_uint(zf * -0.0078125f) >> 16;
-    a_lo = a_hi = zb | (zb << 16);
+    k.a_lo = k.a_hi = zb | (zb << 16);
     if constexpr (SCALE) {
       const uint32_t sb = __float_as_uint(__uint_as_float(s16 << 16) * 128.f) >> 16;
-      sc = sb | (sb << 16);
+      k.sc = sb | (sb << 16);
     }
   } else {
-    c_lo = 0x3C003C00u;  // 1
-    c_hi = 0x2C002C00u;  // 1/16
-    a_lo = f16x2_of(-(1024.f + static_cast<float>(z)));
-    a_hi = f16x2_of(-(64.f + static_cast<float>(z)));
-    if constexpr (SCALE) sc = s16 * 0x00010001u;
+    k.c_lo = 0x3C003C00u;  // 1
+    k.c_hi = 0x2C002C00u;  // 1/16
+    k.a_lo = f16x2_of(-(1024.f + static_cast<float>(z)));
+    k.a_hi = f16x2_of(-(64.f + static_cast<float>(z)));
+    if constexpr (SCALE) k.sc = s16 * 0x00010001u;
   }
+  return k;
+}
+
+template <bool BF16, bool SCALE>
+__device__ __forceinline__ void dq_int4_apply(const uint4 q, const Int4Consts& k, uint32_t (&o)[16]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
   constexpr uint32_t M = BF16 ? 0u : 0x64006400u;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -201,13 +211,16 @@ __device__ __forceinline__ void dq_int4(const uint4 q, uint32_t z, uint32_t s16,
                            (w8 & 0x00F000F0u) | M};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t t = h2fma<BF16>(p[i], (i & 1) ? c_hi : c_lo, (i & 1) ? a_hi : a_lo);
-      o[4 * j + i] = SCALE ? h2mul<BF16>(t, sc) : t;
+      const uint32_t t = h2fma<BF16>(p[i], (i & 1) ? k.c_hi : k.c_lo, (i & 1) ? k.a_hi : k.a_lo);
+      o[4 * j + i] = SCALE ? h2mul<BF16>(t, k.sc) : t;
     }
   }
 }
 
-// INT6 chunk: low nibbles as INT4, top two bits from the rotated hi words.
+template <bool BF16, bool SCALE>
+__device__ __forceinline__ void dq_int4(const uint4 q, uint32_t z, uint32_t s16, uint32_t (&o)[16]) {
+  dq_int4_apply<BF16, SCALE>(q, int4_consts<BF16, SCALE>(z, s16), o);
+}
 template <bool BF16, bool SCALE>
 __device__ __forceinline__ void dq_int6(const uint4 q, const uint2 h, uint32_t c2, uint32_t s2, uint32_t (&o)[16]) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -319,6 +332,29 @@ __device__ __forceinline__ void dq_mxfp4_e4m3(const uint4 q, uint32_t (&o)[8]) {
     }
   }
 }
+
+// The same conversion without a table: an e2m1 code placed at e4m3 bits
+// [4:2] (sign at bit 7) is the e4m3 number of value x * 2^-6, exactly — e2m1's
+// exponent bias is 6 below e4m3's, and e2m1's subnormal 0.5 lands on e4m3's
+// subnormal grid.  The 2^6 goes into the sub-block's UE8M0 weight exponent
+// (mx_w_exp_fold).
+__device__ __forceinline__ void dq_mxfp4_e4m3_s6(const uint4 q, uint32_t (&o)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    // nibbles 0,2,4,6 (elements 0,4,1,5) | 1,3,5,7 (elements 2,6,3,7), one per byte
+    const uint32_t a = ((w[j] << 2) & 0x1C1C1C1Cu) | ((w[j] << 4) & 0x80808080u);
+    const uint32_t b = ((w[j] >> 2) & 0x1C1C1C1Cu) | (w[j] & 0x80808080u);
+    o[2 * j] = __byte_perm(a, b, 0x6420u);
+    o[2 * j + 1] = __byte_perm(a, b, 0x7531u);
+  }
+}
+
+// Four UE8M0 weight exponents (one per byte) with the 2^6 of dq_mxfp4_e4m3_s6
+// folded in: +6 on every byte up to 248.  A byte above 248 keeps its value and
+// its sub-block is converted with the exact table instead (mx_big marks it).
+__device__ __forceinline__ uint32_t mx_big(uint32_t w) { return __vcmpgtu4(w, 0xF8F8F8F8u); }
+__device__ __forceinline__ uint32_t mx_w_exp_fold(uint32_t w) { return __vadd4(w, 0x06060606u & ~mx_big(w)); }
 
 // W4A8 scale factors of one K-block, in the TMEM layout the block-scaled MMA
 // reads: for lane l of every lane quarter, column j of a 4-column group holds
@@ -501,7 +537,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   const uint32_t x_stage = kSlabsKb * KPS * slab;
   uint8_t* x_st = smem;                    // slabs first: 1024-byte aligned at any bn
   uint8_t* w_st = smem + SX * x_stage;
-  uint64_t* w_full = reinterpret_cast<uint64_t*>(w_st + SW * w_stage);
+  // W4A8: the activation exponent words of each weight stage, [stage][K-block
+  // of the stage][token], copied in by the weight producer
+  uint32_t* e_st = reinterpret_cast<uint32_t*>(w_st + SW * w_stage);
+  constexpr uint32_t kEStage = A8 ? KPS * 128u : 0u;  // words per stage
+  uint64_t* w_full = reinterpret_cast<uint64_t*>(e_st + SW * kEStage);
   uint64_t* w_empty = w_full + SW;
   uint64_t* x_full = w_empty + SW;
   uint64_t* x_empty = x_full + SX;
@@ -543,7 +583,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SW; ++s) {
-      dev::mbar_init(&w_full[s], 1);
+      // W4A8: the tensor copy's arrival, then one per producer lane when its
+      // exponent copies have landed
+      dev::mbar_init(&w_full[s], A8 ? 33 : 1);
       dev::mbar_init(&w_empty[s], kStream ? 8 : kDqWarps);  // streams: the two of the stage's parity
     }
     for (int s = 0; s < SX; ++s) {
@@ -646,6 +688,26 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
                                 &w_full[rg.s], pol);
           }
         }
+        if constexpr (A8) {
+          // one exponent word (four 32-K sub-blocks) per token and K-block of
+          // the stage; tokens past the unit get zero exponents (their
+          // activation rows are zero-filled and their columns never stored)
+          const int cnt = min(KPS, u.kb1 - kb);
+          uint32_t* es = e_st + rg.s * kEStage;
+#pragma unroll
+          for (int i = 0; i < KPS; ++i) {
+            if (i < cnt) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int tok = 32 * j + static_cast<int>(lane);
+                const bool in = tok < u.rows;
+                const uint8_t* src = p.x_mx + (in ? static_cast<int64_t>(u.row0 + tok) * p.ld_mx + (kb + i) * 4 : 0);
+                dev::cp_async4(es + i * 128 + tok, src, in ? 4u : 0u);
+              }
+            }
+          }
+          dev::cp_async_arrive(&w_full[rg.s]);
+        }
         if (lane == 0) HQ_TRACE(0, tr, (1ull << 24) | issued);
         rg.next(SW);
         ++issued;
@@ -653,6 +715,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     }
     if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
     // drain: every copy this warp issued has landed before the CTA can exit
+    if constexpr (A8) dev::cp_async_wait_all();
     if (lane == 0) {
       for (int s = 0; s < SW && s < issued; ++s) {
         const int last = ((issued - 1 - s) / SW) * SW + s;
@@ -857,8 +920,32 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     [[maybe_unused]] int tr = 0, ts = 0;
     const bool trace_me = quarter == 0 && lane == 0;
     uint32_t zrow = 0;
+    // INT4 with one scale group per tile (group 128): the group's constants are
+    // computed once per K-block (gk_valid), not per chunk
+    [[maybe_unused]] Int4Consts gk{};
+    [[maybe_unused]] bool gk_valid = false;
     // chunks c0, c0 + 1 (64 K) of this row -> 2 x 16 pairs
     auto convert2 = [&](const uint8_t* wsm, int c0, uint32_t (&o)[2][16]) {
+      if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
+        if (!p.channel && p.g_kb == 1) {
+          if (!gk_valid) {
+            const uint32_t s16 = promote ? 0u : reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r];
+            const uint32_t z = p.has_zeros ? wsm[p.zero_off + r] : zrow;
+            gk = promote ? int4_consts<BF16, false>(z, 0u) : int4_consts<BF16, true>(z, s16);
+            gk_valid = true;
+          }
+          const uint4 q0 = *reinterpret_cast<const uint4*>(wsm + (c0 * kTileN + r) * 16);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(wsm + ((c0 + 1) * kTileN + r) * 16);
+          if (promote) {
+            dq_int4_apply<BF16, false>(q0, gk, o[0]);
+            dq_int4_apply<BF16, false>(q1, gk, o[1]);
+          } else {
+            dq_int4_apply<BF16, true>(q0, gk, o[0]);
+            dq_int4_apply<BF16, true>(q1, gk, o[1]);
+          }
+          return;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int c = c0 + i;
@@ -933,23 +1020,27 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             const uint32_t aph = (ca & 1u) ^ 1u;
             if constexpr (A8) {
               // scale exponents of this K-block: weight rows 32j + lane (from
-              // the tile) and tokens 32j + lane (from the activations' UE8M0
-              // array; tokens past the unit get 2^0)
+              // the tile, with the conversion's 2^6 folded in) and tokens
+              // 32j + lane (staged beside the tile by the weight producer)
               uint32_t ww[4], xw[4];
-              const int kbg = kb + pos;
+              const uint32_t* es = e_st + rg.s * kEStage + pos * 128;
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                const int tok = 32 * j + static_cast<int>(lane);
-                ww[j] = *reinterpret_cast<const uint32_t*>(wsm + p.scale_off + (32 * j + lane) * 4);
-                xw[j] = tok < u.rows ? *reinterpret_cast<const uint32_t*>(
-                                           p.x_mx + static_cast<int64_t>(u.row0 + tok) * p.ld_mx + kbg * 4)
-                                     : 0x7F7F7F7Fu;
+                ww[j] = mx_w_exp_fold(*reinterpret_cast<const uint32_t*>(wsm + p.scale_off + (32 * j + lane) * 4));
+                xw[j] = es[32 * j + lane];
               }
+              // this lane's row: sub-blocks whose exponent cannot take the fold
+              // are converted exactly (rare: a block scale above 2^121)
+              const uint32_t big = mx_big(*reinterpret_cast<const uint32_t*>(wsm + p.scale_off + r * 4));
+              const bool any_big = __any_sync(0xffffffffu, big != 0u);
               uint32_t o8[2][8];
               auto conv8 = [&](int c0) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
-                  dq_mxfp4_e4m3(*reinterpret_cast<const uint4*>(wsm + ((c0 + i) * kTileN + r) * 16), o8[i]);
+                for (int i = 0; i < 2; ++i) {
+                  const uint4 q = *reinterpret_cast<const uint4*>(wsm + ((c0 + i) * kTileN + r) * 16);
+                  dq_mxfp4_e4m3_s6(q, o8[i]);
+                  if (any_big && ((big >> (8 * (c0 + i))) & 1u)) dq_mxfp4_e4m3(q, o8[i]);
+                }
               };
               auto st_half = [&](int h) {
                 uint32_t o16[16];
@@ -990,6 +1081,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               continue;
             }
             uint32_t o[2][16];
+            gk_valid = false;
             convert2(wsm, 0, o);
             if (trace_me) HQ_TRACE(5 + t, tr, (12ull << 24) | ts);
             if (!warp_wait(&a_empty[2 * t], aph, abort_flag)) {
@@ -1064,13 +1156,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         if (real) {
           const uint8_t* wsm = w_st + rg.s * w_stage + gi * tile_bytes;
           if constexpr (A8) {
+            // weight exponents with the conversion's 2^6 folded in; token
+            // exponents staged beside the tile by the weight producer
+            const uint32_t* es = e_st + rg.s * kEStage + gi * 128;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const int tok = 32 * j + static_cast<int>(lane);
-              ww[j] = *reinterpret_cast<const uint32_t*>(wsm + p.scale_off + (32 * j + lane) * 4);
-              xw[j] = tok < u.rows ? *reinterpret_cast<const uint32_t*>(
-                                         p.x_mx + static_cast<int64_t>(u.row0 + tok) * p.ld_mx + (kb + gi) * 4)
-                                   : 0x7F7F7F7Fu;
+              ww[j] = mx_w_exp_fold(*reinterpret_cast<const uint32_t*>(wsm + p.scale_off + (32 * j + lane) * 4));
+              xw[j] = es[32 * j + lane];
             }
           }
 #pragma unroll
@@ -1079,7 +1171,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             qc[i] = *reinterpret_cast<const uint4*>(wsm + (c * kTileN + r) * 16);
             if constexpr (FMT == static_cast<int>(WFmt::INT6))
               qh[i] = *reinterpret_cast<const uint2*>(wsm + p.hi_off + (c * kTileN + r) * 8);
-            if constexpr (FMT == static_cast<int>(WFmt::MXFP4) || FMT == static_cast<int>(WFmt::MXINT4)) {
+            if constexpr (FMT == static_cast<int>(WFmt::MXFP4) || FMT == static_cast<int>(WFmt::MXINT4) || A8) {
               ss[i] = wsm[p.scale_off + r * 4 + c];
               zz[i] = 0;
             } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
@@ -1113,7 +1205,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         uint32_t o[G][16];
         [[maybe_unused]] uint32_t o8[8];
         if (real && A8) {
-          dq_mxfp4_e4m3(qc[0], o8);
+          // exact table for a sub-block whose exponent cannot take the fold
+          dq_mxfp4_e4m3_s6(qc[0], o8);
+          if (__any_sync(0xffffffffu, ss[0] > 248u) && ss[0] > 248u) dq_mxfp4_e4m3(qc[0], o8);
         } else if (real) {
 #pragma unroll
           for (int i = 0; i < G; ++i) {
@@ -1631,10 +1725,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
 
 // Dynamic shared memory bytes for a launch of class CLS.
 template <int CLS>
-inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts) {
+inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts, bool a8) {
   using C = Cls<CLS>;
-  const uint32_t w = static_cast<uint32_t>(w_stages) * ((C::kKps * tile_bytes + 1023u) & ~1023u);
-  const uint32_t x = static_cast<uint32_t>(x_stages) * 2u * C::kKps * static_cast<uint32_t>(bn) * 128u;
+  const uint32_t w = static_cast<uint32_t>(w_stages) * ((C::kKps * tile_bytes + 1023u) & ~1023u) +
+                     (a8 ? static_cast<uint32_t>(w_stages) * C::kKps * 512u : 0u);  // W4A8 exponent words
+  const uint32_t x = static_cast<uint32_t>(x_stages) * (a8 ? 1u : 2u) * C::kKps * static_cast<uint32_t>(bn) * 128u;
   const uint32_t bars =
       (2u * w_stages + 2u * x_stages + 2u * (C::kKps == 2 ? kABars : kASlots) + 2u * C::kDacc + 1u + 2u * kKRing +
        2u * kSRing + 1u) * 8u + 16u;

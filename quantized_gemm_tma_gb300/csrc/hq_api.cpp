@@ -437,7 +437,7 @@ size_t splitk_bytes(int splits, int m, int n_pad) {
 // Shared-memory rings for a tile-width class: a few activation stages (the
 // MMA holds them), then as many weight stages as fit, up to 8.
 void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_optin, int* w_stages,
-                 int* x_stages, int* groups) {
+                 int* x_stages, int* groups, bool a8 = false) {
   const size_t cap = std::min<size_t>(smem_optin, 232448);
   static const int kXWant[4] = {6, 3, 3, 2};
   // sweep overrides (clamped to [2, 12] and to what fits)
@@ -452,7 +452,7 @@ void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_
   const int sw_step = wna16_kps(cls) == 2 ? 2 : 1;
   for (; sx >= 2; --sx) {
     for (sw = sw_max - (sw_max % sw_step); sw >= 2; sw -= sw_step)
-      if (wna16_smem_bytes(cls, sw, sx, L.tile_bytes, bn, num_experts) <= cap) break;
+      if (wna16_smem_bytes(cls, sw, sx, L.tile_bytes, bn, num_experts, a8) <= cap) break;
     if (sw >= 2) break;
   }
   *w_stages = sw >= 2 && sx >= 2 ? sw : 0;
@@ -502,17 +502,17 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   const int forced_sk = env_int("HQ_FORCE_SPLITK", 0);  // 1: stream-K on, 2: off
   if (forced_sk == 1 && !(flags & HQ_FLAG_BATCH_INVARIANT) && p.tiles <= kMaxSplitTiles) p.stream_k = 1;
   if (forced_sk == 2) p.stream_k = 0;
-  plan_stages(p.cls, L, p.bn, 0, smem_optin, &p.stages, &p.x_stages, &p.groups);
+  plan_stages(p.cls, L, p.bn, 0, smem_optin, &p.stages, &p.x_stages, &p.groups, a8);
   // A tile per 2-CTA cluster, K split in halves and combined through
   // distributed shared memory, when that fills most SMs: no cross-CTA global
   // reduction at all.
   p.cluster = 1;
   if (!(flags & HQ_FLAG_BATCH_INVARIANT) && L.k_tiles >= 2 && 2 * p.tiles <= sms && 8 * p.tiles >= 3 * sms &&
-      env_int("HQ_FORCE_SPLITK", 0) == 0 && wna16_cluster_fits(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn)) {
+      env_int("HQ_FORCE_SPLITK", 0) == 0 && wna16_cluster_fits(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn, a8)) {
     p.cluster = 2;
     p.stream_k = 0;
   }
-  p.smem = wna16_smem_bytes(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn, 0);
+  p.smem = wna16_smem_bytes(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn, 0, a8);
   // stream-K: at least 8 K-blocks per CTA, so that partial tiles stay few
   p.grid = p.cluster == 2 ? 2 * p.tiles
            : p.stream_k ? static_cast<int>(std::min<long long>(sms, std::max<long long>(1, (p.iters + 7) / 8)))

@@ -59,11 +59,12 @@ struct Wna16Maps {
   CUtensorMap x, y;
 };
 cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const Wna16Maps& maps, cudaStream_t stream);
-uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts);
+uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts,
+                          bool a8 = false);
 int wna16_kps(int cls);  // K-blocks per shared-memory stage
 // whether a 2-CTA cluster split of this class can pass rank 1's sums through
 // rank 0's ring area
-bool wna16_cluster_fits(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn);
+bool wna16_cluster_fits(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, bool a8 = false);
 
 // gemm_fp8.cu
 cudaError_t launch_fp8(const Fp8Params& p, const CUtensorMap& tmap, int bn_max, int grid, uint32_t smem,

@@ -25,19 +25,20 @@ cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const Wna16M
   }
 }
 
-uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts) {
+uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts,
+                          bool a8) {
   switch (cls) {
-    case 0: return wna16::smem_bytes<0>(w_stages, x_stages, tile_bytes, bn, num_experts);
-    case 1: return wna16::smem_bytes<1>(w_stages, x_stages, tile_bytes, bn, num_experts);
-    case 2: return wna16::smem_bytes<2>(w_stages, x_stages, tile_bytes, bn, num_experts);
-    default: return wna16::smem_bytes<3>(w_stages, x_stages, tile_bytes, bn, num_experts);
+    case 0: return wna16::smem_bytes<0>(w_stages, x_stages, tile_bytes, bn, num_experts, a8);
+    case 1: return wna16::smem_bytes<1>(w_stages, x_stages, tile_bytes, bn, num_experts, a8);
+    case 2: return wna16::smem_bytes<2>(w_stages, x_stages, tile_bytes, bn, num_experts, a8);
+    default: return wna16::smem_bytes<3>(w_stages, x_stages, tile_bytes, bn, num_experts, a8);
   }
 }
 
-bool wna16_cluster_fits(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn) {
+bool wna16_cluster_fits(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, bool a8) {
   if (cls == 0) return true;  // bn <= 16: rank 1's sums go to a dedicated buffer
   const uint32_t kps = static_cast<uint32_t>(wna16_kps(cls));
-  const uint64_t rings = static_cast<uint64_t>(x_stages) * 2u * kps * static_cast<uint32_t>(bn) * 128u +
+  const uint64_t rings = static_cast<uint64_t>(x_stages) * (a8 ? 1u : 2u) * kps * static_cast<uint32_t>(bn) * 128u +
                          static_cast<uint64_t>(w_stages) * ((kps * tile_bytes + 1023u) & ~1023u);
   const uint32_t need = cls == 1 ? wna16::xchg_bytes<1>() : cls == 2 ? wna16::xchg_bytes<2>() : wna16::xchg_bytes<3>();
   return need <= rings;

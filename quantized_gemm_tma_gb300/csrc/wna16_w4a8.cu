@@ -32,3 +32,23 @@ cudaError_t launch_wna16_w4a8(const Wna16Launch& l, const GemmParams& p, const W
 }
 
 }  // namespace hq
+
+#if defined(HQ_ENABLE_TRACE) || defined(HQ_ENABLE_TRACE_CTA)
+// Debug builds only: copy (and optionally clear) the W4A8 kernel's event trace.
+extern "C" int hq_trace_read_w4a8(void* dst, size_t bytes, int clear) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+  if (bytes < sizeof(hq::dev::g_trace) + sizeof(hq::dev::g_trace_cta)) return 6;
+  if (cudaMemcpyFromSymbol(dst, hq::dev::g_trace, sizeof(hq::dev::g_trace)) != cudaSuccess) return 2;
+  if (cudaMemcpyFromSymbol(static_cast<char*>(dst) + sizeof(hq::dev::g_trace), hq::dev::g_trace_cta,
+                           sizeof(hq::dev::g_trace_cta)) != cudaSuccess)
+    return 5;
+  if (clear) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, hq::dev::g_trace) != cudaSuccess) return 3;
+    if (cudaMemset(p, 0, sizeof(hq::dev::g_trace)) != cudaSuccess) return 4;
+    if (cudaGetSymbolAddress(&p, hq::dev::g_trace_cta) != cudaSuccess) return 3;
+    if (cudaMemset(p, 0, sizeof(hq::dev::g_trace_cta)) != cudaSuccess) return 4;
+  }
+  return 0;
+}
+#endif

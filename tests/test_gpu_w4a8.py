@@ -83,6 +83,30 @@ def test_w4a8_extreme_exponents():
         check(y[i:i + 1], r[i:i + 1], f"w4a8 extreme exponents row {i}")
 
 
+@pytest.mark.parametrize("m", [16, 24, 100])
+def test_w4a8_large_weight_exponents(m):
+    """Weight block scales from 2^122 to 2^127 (UE8M0 249..254), mixed within
+    rows with ordinary ones, against activations near 2^-100: those sub-blocks
+    take the exact conversion table instead of the shifted conversion whose
+    2^6 goes into the weight exponent.  m = 16 and 24 run the two-K-block
+    streams, m = 100 one K-block per stage."""
+    from gpu_helpers import DevWeight
+    n, k = 256, 1024
+    qw = synth.random_codes_weight(84 + m, "mxfp4", n, k)
+    rng = np.random.default_rng(84 + m)
+    sc = rng.integers(115, 135, size=qw.scales.shape)
+    big = rng.random(qw.scales.shape) < 0.3
+    sc[big] = rng.integers(249, 255, size=int(big.sum()))
+    qw.scales[:] = sc.astype(np.uint8)
+    x = rng.standard_normal((m, k)) * np.exp2(rng.integers(-110, -100, size=(m, k // 32))).repeat(32, axis=1)
+    xb = synth.to_bf16_bits(x)
+    y = _w4a8(DevWeight(qw), xb, k)
+    r = _ref(qw, xb)
+    assert np.isfinite(r).all()
+    for i in range(m):
+        check(y[i:i + 1], r[i:i + 1], f"w4a8 large weight exponents row {i}")
+
+
 @pytest.mark.parametrize("splitk", ["cluster", "stream_k", "whole"])
 def test_w4a8_work_splits(splitk):
     """N = 8192 gives 64 weight tiles: the 2-CTA cluster split (the planner's
