@@ -747,11 +747,17 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           // past the end of X are zero-filled by the tensor copy, and rows
           // past the unit belong to other experts: their output columns are
           // never stored
-          const int zs = static_cast<int>(kSlabsKb) * cnt;
-          dev::mbar_arrive_expect_tx(&x_full[rg.s], static_cast<uint32_t>(zs) * slab);
-          for (int z = 0; z < zs; ++z)
-            dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], A8 ? (kb + z) * 128 : (2 * kb + z) * 64,
-                             u.xrow0);
+          if (p.x3d) {
+            // every slab of the stage in one box (slabs past K read as zeros)
+            dev::mbar_arrive_expect_tx(&x_full[rg.s], x_stage);
+            dev::tma_load_3d(xs, &tmap_x, &x_full[rg.s], 0, u.xrow0, static_cast<int>(kSlabsKb) * kb);
+          } else {
+            const int zs = static_cast<int>(kSlabsKb) * cnt;
+            dev::mbar_arrive_expect_tx(&x_full[rg.s], static_cast<uint32_t>(zs) * slab);
+            for (int z = 0; z < zs; ++z)
+              dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], A8 ? (kb + z) * 128 : (2 * kb + z) * 64,
+                               u.xrow0);
+          }
         }
         rg.next(SX);
         ++issued;

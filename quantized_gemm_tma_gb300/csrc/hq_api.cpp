@@ -85,8 +85,11 @@ hq_status encode_uncached(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t 
                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
-    cuuint64_t dims[3] = {inner, outer, slabs & 0xffffffffull};
-    cuuint64_t strides[2] = {row_stride_elems * elem, inner * elem};
+    // slabs = (slabs per box << 32) | slab count: the matrix seen as
+    // [slab][row][box_inner], slab z starting box_inner elements after slab
+    // z - 1, so that one box holds several consecutive slabs of the same rows
+    cuuint64_t dims[3] = {box_inner, outer, slabs & 0xffffffffull};
+    cuuint64_t strides[2] = {row_stride_elems * elem, static_cast<cuuint64_t>(box_inner) * elem};
     cuuint32_t box[3] = {box_inner, box_outer, static_cast<cuuint32_t>(slabs >> 32)};
     cuuint32_t estr[3] = {1, 1, 1};
     r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -138,6 +141,23 @@ hq_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, 
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Activation map of the WnA16 kernel: X [rows][k] in 128-byte slabs (box_inner
+// elements) of bn rows.  When k fills whole slabs, one 3-D box carries the
+// `per_stage` slabs of a stage (one tensor copy per stage; *x3d = 1); else one
+// 2-D box per slab, which zero-fills the columns past k.
+hq_status encode_x(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, const void* x, int64_t k,
+                   int64_t rows, int64_t ldx, uint32_t box_inner, int bn, int per_stage, int* x3d) {
+  *x3d = 0;
+  if (k % box_inner == 0) {
+    const uint64_t slabs = (static_cast<uint64_t>(per_stage) << 32) | static_cast<uint64_t>(k / box_inner);
+    if (encode_2d(map, dtype, elem, x, k, rows, ldx, box_inner, bn, slabs) == HQ_OK) {
+      *x3d = 1;
+      return HQ_OK;
+    }
+  }
+  return encode_2d(map, dtype, elem, x, k, rows, ldx, box_inner, bn);
+}
 
 // Tiles are counted in 32-bit integers on the device.  `rows` rows in at most
 // `groups` separately tiled runs (experts) need at most rows / 16 + groups + 1
@@ -580,9 +600,10 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   l.moe = true;
   l.grid = di.sms;
   l.smem = wna16_smem_bytes(cls, p.stages, p.x_stages, L.tile_bytes, bn, L.num_experts);
-  // X [x_rows][K]: one box = 64 columns (128 bytes, swizzled) of bn rows
+  // X [x_rows][K]: slabs of 64 columns (128 bytes, swizzled) of bn rows
   Wna16Maps maps;
-  hq_status st = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, x_rows, ldx, 64, bn);
+  hq_status st = encode_x(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, x_rows, ldx, 64, bn,
+                          2 * wna16_kps(cls), &p.x3d);
   if (st != HQ_OK) return st;
   maps.y = maps.x;  // MoE output rows use plain stores
   if (launch_wna16(l, p, maps, s) != cudaSuccess) return HQ_ERR_CUDA;
@@ -722,8 +743,9 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   // X [M][K]: one box = 128 bytes (64 bf16/fp16 or 128 e4m3 columns, swizzled) of bn rows
   const CUtensorMapDataType t16 = atype == HQ_A_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   Wna16Maps maps;
-  st = a8 ? encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, x, L.k, m, ldx, 128, pl.bn)
-          : encode_2d(&maps.x, t16, 2, x, L.k, m, ldx, 64, pl.bn);
+  st = a8 ? encode_x(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, x, L.k, m, ldx, 128, pl.bn, wna16_kps(pl.cls),
+                     &p.x3d)
+          : encode_x(&maps.x, t16, 2, x, L.k, m, ldx, 64, pl.bn, 2 * wna16_kps(pl.cls), &p.x3d);
   if (st != HQ_OK) return st;
   // Y [M][N]: tensor stores of 16 tokens x 32 output rows when its row pitch
   // is a multiple of 16 bytes (the tensor-map stride rule); plain stores else
@@ -744,8 +766,8 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   g_last_plan = hq_plan_info{pl.bn, pl.cluster == 2 ? 2 : (pl.stream_k ? 0 : 1), pl.grid, 1, pl.stages, pl.cls,
                              pl.groups, 0};
   if (env_int("HQ_TRACE", 0))
-    std::fprintf(stderr, "hq_gemm: m=%d n=%d k=%d bn=%d cls=%d stream_k=%d grid=%d stages=%d groups=%d smem=%u\n", m,
-                 L.n, L.k, pl.bn, pl.cls, pl.stream_k, pl.grid, pl.stages, pl.groups, pl.smem);
+    std::fprintf(stderr, "hq_gemm: m=%d n=%d k=%d bn=%d cls=%d stream_k=%d grid=%d stages=%d groups=%d smem=%u x3d=%d\n",
+                 m, L.n, L.k, pl.bn, pl.cls, pl.stream_k, pl.grid, pl.stages, pl.groups, pl.smem, p.x3d);
   return launch_wna16(l, p, maps, s) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 

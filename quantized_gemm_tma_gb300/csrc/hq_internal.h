@@ -128,6 +128,7 @@ struct GemmParams {
   int stream_k;             // dense: deal K-blocks out in equal ranges (1) or whole tiles (0)
   int promote;              // one accumulator per K-block, group scale applied in fp32 by the epilogue
   int cluster;              // dense: 2 = a 2-CTA cluster per tile, each CTA half of K, combined in shared memory
+  int x3d;                  // activation map is 3-D: one box = every slab of a stage
   long long iters;          // stream-K: tiles * k_tiles
   uint32_t idesc;
   // output
