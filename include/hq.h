@@ -296,7 +296,9 @@ hq_status hq_gemm_noalloc(const hq_weight_desc* wdesc, const void* w_t, int32_t 
 /*
  * hq_moe_workspace_size — workspace for hq_moe_gemm (status word, routing
  * counts and offsets, permutation, per-pair fp32 outputs, and the routed
- * activation rows in expert order: T*topk rows of K bf16).
+ * activation rows in expert order: T*topk rows of K bf16, or for
+ * HQ_A_MXFP8_E4M3 T*topk rows of K e4m3 bytes and K/32 exponents in the same
+ * space).  The size does not depend on atype.
  */
 hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int32_t topk,
                                 int32_t atype, size_t* bytes);
@@ -315,6 +317,12 @@ hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int3
  * wdesc, w_t   expert weights [E][N][K] and their transform
  * tokens, topk T and top-k; topk_ids int32 [T][topk], topk_w float32 [T][topk]
  * x, ldx       activations [T][k]; y, ldy output [T][n] (bf16 for BF16 acts)
+ * atype        HQ_A_BF16, or HQ_A_MXFP8_E4M3 for W4A8-MXFP4 (MXFP4 experts,
+ *              k % 128 == 0): x still holds bf16 rows; each routed row is
+ *              quantised to MXFP8 as it is gathered (e4m3 elements under one
+ *              UE8M0 exponent per 32 along K, the conversion of
+ *              hq_mxfp8_quantize) and multiplied on the block-scaled MMA,
+ *              so a(X[t]) = mxfp8(X[t]); y is bf16
  * expert_offsets_out  optional int32 [E+1]; perm_out optional int32 [T*topk]
  * Limits (HQ_ERR_UNSUPPORTED beyond): E <= 1024, T*topk <= 2^24 and
  * (T*topk/16 + E + 1) * ceil(n/128) below 2^31.

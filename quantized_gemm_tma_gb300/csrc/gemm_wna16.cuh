@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               for (int j = 0; j < 4; ++j) {
                 const int tok = 32 * j + static_cast<int>(lane);
                 const bool in = tok < u.rows;
-                const uint8_t* src = p.x_mx + (in ? static_cast<int64_t>(u.row0 + tok) * p.ld_mx + (kb + i) * 4 : 0);
+                const uint8_t* src = p.x_mx + (in ? static_cast<int64_t>(u.xrow0 + tok) * p.ld_mx + (kb + i) * 4 : 0);
                 dev::cp_async4(es + i * 128 + tok, src, in ? 4u : 0u);
               }
             }

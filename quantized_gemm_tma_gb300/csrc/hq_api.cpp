@@ -569,7 +569,12 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
                              const int* x_base, int out, const float* topk_w, void* y, int64_t ldy,
                              const int* exp_off, const int* tile_off, const int* perm, float* zbuf, int* status,
                              const DevInfo& di, cudaStream_t s, int* stages, int* groups,
-                             float* gate_buf = nullptr) {
+                             float* gate_buf = nullptr, const uint8_t* x_mx = nullptr, int64_t ld_mx = 0) {
+  // W4A8: x holds MXFP8 codes [x_rows][ldx bytes] and x_mx their UE8M0
+  // exponents [x_rows][ld_mx]
+  const bool a8 = x_mx != nullptr;
+  if (a8 && (bn > 128 || L.wtype != HQ_W_MXFP4 || L.k % kTileK != 0 || ld_mx % 4 != 0 || out == kMoeOutGated))
+    return HQ_ERR_UNSUPPORTED;
   const int cls = wna16_class(bn);
   GemmParams p{};
   p.tiles = wt + L.tiles_off;
@@ -583,7 +588,9 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = x_rows;
   p.bn = bn; p.m_tiles = 0; p.num_tiles = 0; p.stream_k = 0; p.iters = 0; p.cluster = 1;
   p.promote = (cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
-  p.idesc = idesc_f16(true, 128, bn);
+  p.idesc = a8 ? idesc_mx_e4m3(128, bn) : idesc_f16(true, 128, bn);
+  p.x_mx = x_mx;
+  p.ld_mx = static_cast<int>(ld_mx);
   p.y = y; p.ldy = ldy; p.moe_out = out;
   p.status = status;
   p.num_experts = L.num_experts; p.topk = 1;
@@ -591,19 +598,21 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   p.x_base = x_base;
   p.gate_buf = gate_buf;
   if (out == kMoeOutGated && (!gate_buf || di.sms > kPlanSmsBound || bn > kGateBufBn)) return HQ_ERR_UNSUPPORTED;
-  plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups);
+  plan_stages(cls, L, bn, L.num_experts, di.smem_optin, &p.stages, &p.x_stages, &p.groups, a8);
   if (p.stages < 2) return HQ_ERR_UNSUPPORTED;
   Wna16Launch l{};
-  l.fmt = wna16_fmt(L.wtype);
+  l.fmt = a8 ? static_cast<int>(WFmt::MXFP4_A8) : wna16_fmt(L.wtype);
   l.bf16 = true;
   l.cls = cls;
   l.moe = true;
   l.grid = di.sms;
-  l.smem = wna16_smem_bytes(cls, p.stages, p.x_stages, L.tile_bytes, bn, L.num_experts);
-  // X [x_rows][K]: slabs of 64 columns (128 bytes, swizzled) of bn rows
+  l.smem = wna16_smem_bytes(cls, p.stages, p.x_stages, L.tile_bytes, bn, L.num_experts, a8);
+  // X [x_rows][K]: slabs of 128 bytes (64 bf16 or 128 e4m3 columns, swizzled) of bn rows
   Wna16Maps maps;
-  hq_status st = encode_x(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, x_rows, ldx, 64, bn,
-                          2 * wna16_kps(cls), &p.x3d);
+  hq_status st = a8 ? encode_x(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, x, L.k, x_rows, ldx, 128, bn,
+                               wna16_kps(cls), &p.x3d)
+                    : encode_x(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.k, x_rows, ldx, 64, bn,
+                               2 * wna16_kps(cls), &p.x3d);
   if (st != HQ_OK) return st;
   maps.y = maps.x;  // MoE output rows use plain stores
   if (launch_wna16(l, p, maps, s) != cudaSuccess) return HQ_ERR_CUDA;
@@ -882,7 +891,10 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   if (tokens == 0) return HQ_OK;
   if (!w_t || !topk_ids || !topk_w || !x || !y || !workspace) return HQ_ERR_INVALID_ARG;
   if (ldx < L.k || ldy < L.n) return HQ_ERR_INVALID_ARG;
-  if (atype != HQ_A_BF16) return HQ_ERR_UNSUPPORTED;
+  // W4A8-MXFP4: bf16 activations quantised to MXFP8 as they are gathered
+  const bool a8 = atype == HQ_A_MXFP8_E4M3;
+  if (atype != HQ_A_BF16 && !a8) return HQ_ERR_UNSUPPORTED;
+  if (a8 && (L.wtype != HQ_W_MXFP4 || L.k % kTileK != 0)) return HQ_ERR_UNSUPPORTED;
   if (L.wtype == HQ_W_FP8_E4M3) return HQ_ERR_UNSUPPORTED;
   if ((L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.stype != HQ_S_BF16) return HQ_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(w_t) & 255u))
@@ -910,17 +922,27 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   off += align_up(sizeof(float) * static_cast<size_t>(pairs) * L.n_pad, kAlign);
   void* xg = ws + off;  // the routed activation rows in expert order
   const int64_t ldg = permuted_ld(L.k);
+  // W4A8: e4m3 rows [pairs][k] then their exponents [pairs][k/32] in the same
+  // region (k + k/32 bytes a row, within the 2k of a bf16 row)
+  uint8_t* xq = static_cast<uint8_t*>(xg);
+  uint8_t* xe = xq + static_cast<size_t>(pairs) * L.k;
 
   const int bn = moe_tile_bn(static_cast<double>(pairs) / L.num_experts);
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L.num_experts, bn, exp_off, tile_off, perm,
                        expert_offsets_out, perm_out, reinterpret_cast<int*>(ws), s) != cudaSuccess)
     return HQ_ERR_CUDA;
-  if (launch_moe_permute(x, ldx, tokens, perm, exp_off + L.num_experts, static_cast<int>(pairs), topk, L.k, xg, ldg,
-                         di.sms, s) != cudaSuccess)
-    return HQ_ERR_CUDA;
+  const cudaError_t pe =
+      a8 ? launch_moe_permute_mxfp8(x, ldx, tokens, perm, exp_off + L.num_experts, static_cast<int>(pairs), topk, L.k,
+                                    xq, L.k, xe, L.k / 32, s)
+         : launch_moe_permute(x, ldx, tokens, perm, exp_off + L.num_experts, static_cast<int>(pairs), topk, L.k, xg,
+                              ldg, di.sms, s);
+  if (pe != cudaSuccess) return HQ_ERR_CUDA;
   int stages = 0, groups = 0;
-  st = launch_moe_grouped(L, wt, bn, xg, ldg, static_cast<int>(pairs), exp_off, kMoeOutZ, topk_w, y, ldy, exp_off,
-                          tile_off, perm, zbuf, reinterpret_cast<int*>(ws), di, s, &stages, &groups);
+  st = a8 ? launch_moe_grouped(L, wt, bn, xq, L.k, static_cast<int>(pairs), exp_off, kMoeOutZ, topk_w, y, ldy, exp_off,
+                               tile_off, perm, zbuf, reinterpret_cast<int*>(ws), di, s, &stages, &groups, nullptr, xe,
+                               L.k / 32)
+          : launch_moe_grouped(L, wt, bn, xg, ldg, static_cast<int>(pairs), exp_off, kMoeOutZ, topk_w, y, ldy, exp_off,
+                               tile_off, perm, zbuf, reinterpret_cast<int*>(ws), di, s, &stages, &groups);
   if (st != HQ_OK) return st;
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L.num_experts, L.n, L.n_pad, y, ldy, true, s) != cudaSuccess)
     return HQ_ERR_CUDA;

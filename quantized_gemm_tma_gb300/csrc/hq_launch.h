@@ -89,6 +89,11 @@ cudaError_t launch_moe_grouped_route(const int* rows_in, bool masked, int rows, 
 // most `pairs`); bf16, k, ldx and ldg multiples of 8
 cudaError_t launch_moe_permute(const void* x, int64_t ldx, int tokens, const int* perm, const int* routed,
                                int pairs, int topk, int k, void* xg, int64_t ldg, int sms, cudaStream_t stream);
+// W4A8: the same gather quantised to MXFP8, Q[p][:k] e4m3 and Ex[p][:k/32]
+// UE8M0 (k % 32 == 0; ldx, ldq multiples of 8)
+cudaError_t launch_moe_permute_mxfp8(const void* x, int64_t ldx, int tokens, const int* perm, const int* routed,
+                                     int pairs, int topk, int k, void* q, int64_t ldq, void* ex, int64_t lde,
+                                     cudaStream_t stream);
 cudaError_t launch_moe_act(const void* h, int64_t ldh, int pairs, int inter, void* a, int64_t lda,
                            cudaStream_t stream);
 cudaError_t launch_moe_combine(const float* zbuf, const int* topk_ids, int tokens, int topk, int num_experts, int n,

@@ -12,7 +12,8 @@
 //          the routing weight), rounded once to bf16.
 // permute: the routed activation rows in expert order (the grouped-contiguous
 //          organisation of an indexed input): Xg[p, :] = X[perm[p] / topk, :],
-//          so that the grouped GEMM loads whole tiles of an expert's rows.
+//          so that the grouped GEMM loads whole tiles of an expert's rows;
+//          for W4A8 the gathered rows are quantised to MXFP8 on the way.
 // grouped: the grouped-contiguous and grouped-masked input forms (rows per
 //          expert given by the caller): offsets, tile prefix, row map and the
 //          X row where each expert's rows start.
@@ -25,6 +26,7 @@
 
 #include "hq_internal.h"
 #include "hq_launch.h"
+#include "mxfp8.cuh"
 
 namespace hq {
 namespace {
@@ -225,6 +227,34 @@ __global__ void moe_permute_kernel(const uint4* __restrict__ x, int64_t ldx16, i
   }
 }
 
+// The same gather quantising each row to MXFP8 (W4A8): Q[p][:k] e4m3 and
+// Ex[p][:k/32] UE8M0 of X[perm[p] / topk], the conversion of the standalone
+// quantiser.  One thread per 8 elements of every slot up to `pairs` (the four
+// lanes of a 32-element block are consecutive: k % 32 == 0); slots past the
+// device count *routed are left alone, and every lane takes part in the
+// block's shuffles.
+__global__ void __launch_bounds__(256) moe_permute_mxfp8_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
+                                                                int tokens, const int* __restrict__ perm,
+                                                                const int* __restrict__ routed, int pairs, int topk,
+                                                                int k, uint8_t* __restrict__ q, int64_t ldq,
+                                                                uint8_t* __restrict__ ex, int64_t lde) {
+  const int per_row = k / 8;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t rows = min(*routed, pairs);
+  const bool live = idx < rows * per_row;
+  const int64_t p = live ? idx / per_row : 0;
+  const int j = live ? static_cast<int>(idx - p * per_row) : 0;
+  const int t = live ? perm[p] / topk : -1;
+  uint4 raw = make_uint4(0, 0, 0, 0);
+  if (t >= 0 && t < tokens) raw = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * ldx + 8 * j));
+  int E = 0;
+  const uint2 packed = dev::mxfp8_quantize8(raw, &E);
+  if (live) {
+    *reinterpret_cast<uint2*>(q + p * ldq + 8 * j) = packed;
+    if ((j & 3) == 0) ex[p * lde + j / 4] = static_cast<uint8_t>(E);
+  }
+}
+
 // MoE feed-forward activation between the two grouped GEMMs:
 //   A[f][i] = silu(H[f][i]) * H[f][inter + i],  silu(g) = g / (1 + e^-g),
 // computed in fp32 from the bf16 gate and up halves and rounded once to bf16.
@@ -316,6 +346,19 @@ cudaError_t launch_moe_permute(const void* x, int64_t ldx, int tokens, const int
   const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sms) * 8));
   moe_permute_kernel<<<grid, block, 0, stream>>>(static_cast<const uint4*>(x), ldx / 8, tokens, perm, routed, topk,
                                                  chunks, static_cast<uint4*>(xg), ldg / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_permute_mxfp8(const void* x, int64_t ldx, int tokens, const int* perm, const int* routed,
+                                     int pairs, int topk, int k, void* q, int64_t ldq, void* ex, int64_t lde,
+                                     cudaStream_t stream) {
+  if (pairs == 0) return cudaSuccess;
+  if (k % 32 || ldx % 8 || ldq % 8) return cudaErrorInvalidValue;
+  const int64_t threads = static_cast<int64_t>(pairs) * (k / 8);
+  const int block = 256;
+  moe_permute_mxfp8_kernel<<<static_cast<unsigned>((threads + block - 1) / block), block, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(x), ldx, tokens, perm, routed, pairs, topk, k, static_cast<uint8_t*>(q), ldq,
+      static_cast<uint8_t*>(ex), lde);
   return cudaGetLastError();
 }
 

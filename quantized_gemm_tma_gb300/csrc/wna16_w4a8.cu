@@ -1,7 +1,7 @@
 // wna16_w4a8.cu — instantiations and launcher of the WnA16 kernel for
 // W4A8-MXFP4: MXFP4 weights against MXFP8 activations, block-scaled MMA
-// (dense, tiles of at most 128 tokens; own translation unit so the formats
-// compile in parallel).
+// (dense and MoE grouped, tiles of at most 128 tokens; own translation unit
+// so the formats compile in parallel).
 #include "gemm_wna16.cuh"
 #include "hq_launch.h"
 
@@ -10,9 +10,9 @@ namespace {
 
 constexpr int kFmt = static_cast<int>(WFmt::MXFP4_A8);
 
-template <int CLS>
+template <int CLS, bool MOE>
 cudaError_t run(const Wna16Launch& l, const GemmParams& p, const Wna16Maps& maps, cudaStream_t stream) {
-  auto k = wna16::wna16_kernel<kFmt, true, CLS, false>;
+  auto k = wna16::wna16_kernel<kFmt, true, CLS, MOE>;
   cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k));
   if (e != cudaSuccess) return e;
   return launch_pdl(reinterpret_cast<const void*>(k), l.grid, wna16::threads<CLS>(), l.smem, stream, p.cluster, p,
@@ -22,11 +22,11 @@ cudaError_t run(const Wna16Launch& l, const GemmParams& p, const Wna16Maps& maps
 }  // namespace
 
 cudaError_t launch_wna16_w4a8(const Wna16Launch& l, const GemmParams& p, const Wna16Maps& maps, cudaStream_t stream) {
-  if (l.moe || !l.bf16) return cudaErrorInvalidValue;
+  if (!l.bf16) return cudaErrorInvalidValue;
   switch (l.cls) {
-    case 0: return run<0>(l, p, maps, stream);
-    case 1: return run<1>(l, p, maps, stream);
-    case 2: return run<2>(l, p, maps, stream);
+    case 0: return l.moe ? run<0, true>(l, p, maps, stream) : run<0, false>(l, p, maps, stream);
+    case 1: return l.moe ? run<1, true>(l, p, maps, stream) : run<1, false>(l, p, maps, stream);
+    case 2: return l.moe ? run<2, true>(l, p, maps, stream) : run<2, false>(l, p, maps, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -94,7 +94,10 @@ def run_gemm(dw: DevWeight, acts, ldx: int | None = None, ldy: int | None = None
     return y[:m, :n].double().cpu().numpy()
 
 
-def run_moe(dw: DevWeight, acts, routing, ws: torch.Tensor | None = None, want_route: bool = False):
+def run_moe(dw: DevWeight, acts, routing, ws: torch.Tensor | None = None, want_route: bool = False,
+            atype: str = "bf16"):
+    """hq_moe_gemm on device copies; atype "mxfp8" quantises the bf16 rows to
+    MXFP8 as they are gathered (W4A8)."""
     t, k = acts.m, acts.k
     topk = routing.topk_ids.shape[1]
     n = dw.qw.n
@@ -105,10 +108,10 @@ def run_moe(dw: DevWeight, acts, routing, ws: torch.Tensor | None = None, want_r
     e = dw.qw.num_experts
     offs = torch.full((e + 1,), -1, dtype=torch.int32, device="cuda") if want_route else None
     perm = torch.full((max(t * topk, 1),), -1, dtype=torch.int32, device="cuda") if want_route else None
-    need = hq.hq_moe_workspace_size(dw.desc, t, topk, "bf16")
+    need = hq.hq_moe_workspace_size(dw.desc, t, topk, atype)
     if ws is None:
         ws = workspace(need)
-    hq.hq_moe_gemm(dw.desc, dw.wt, t, topk, ids, tw, "bf16", x, k, y, n, offs, perm, ws, ws.numel(), 0, stream())
+    hq.hq_moe_gemm(dw.desc, dw.wt, t, topk, ids, tw, atype, x, k, y, n, offs, perm, ws, ws.numel(), 0, stream())
     st = hq.hq_status_read(ws, clear=True, stream=stream())
     out = y[:t, :n].double().cpu().numpy()
     if want_route:

@@ -117,6 +117,17 @@ def test_moe_host_validation(hq):
     assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
     need = hq.hq_moe_workspace_size(d, 4096, 8, "bf16")
     assert need >= 4096 * 8 * 1536 * 4
+    # W4A8 (activations quantised to MXFP8 on the gather): MXFP4 experts only,
+    # K a multiple of 128; the quantised rows fit the bf16 rows' space
+    assert hq.hq_moe_workspace_size(d, 4096, 8, "mxfp8") == need
+    di4 = hq.make_desc("int4", "bf16", 1536, 2048, num_experts=128, group_k=128)
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_moe_gemm(di4, fake, 16, 8, fake, fake, "mxfp8", fake, 2048, fake, 1536, None, None, fake, 1 << 30)
+    assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
+    dk = hq.make_desc("mxfp4", "ue8m0", 1536, 2080, num_experts=128, group_k=32)
+    with pytest.raises(hq.HQError) as ei:
+        hq.hq_moe_gemm(dk, fake, 16, 8, fake, fake, "mxfp8", fake, 2080, fake, 1536, None, None, fake, 1 << 30)
+    assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
 
 
 def test_moe_grouped_host_validation(hq):
