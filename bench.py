@@ -401,6 +401,16 @@ def run_gpu(args, rank: int, world: int):
                        None, None, d["ws"], d["ws"].numel(), 0, sh)
         launches["n"] += hq.hq_last_plan()["launches"]
 
+    def moe_a8_call(t):
+        # W4A8-MXFP4: the same experts and routing, bf16 rows quantised to
+        # MXFP8 in the gather, block-scaled grouped GEMM
+        d = moe["T"][t]
+        mwt = moe["wt"][rot["moe"] % MOE_COPIES]
+        rot["moe"] += 1
+        hq.hq_moe_gemm(moe["desc"], mwt, t, MOE_TOPK, d["ids"], d["w"], "mxfp8", d["x"], MOE_K, d["y"], MOE_N,
+                       None, None, d["ws"], d["ws"].numel(), 0, sh)
+        launches["n"] += hq.hq_last_plan()["launches"]
+
     def ffn_call(t):
         d = moe["T"][t]
         i = rot["moe"] % MOE_COPIES
@@ -430,6 +440,7 @@ def run_gpu(args, rank: int, world: int):
         if moe:
             for t in MOE_T:
                 timed(moe_call, t)
+                timed(moe_a8_call, t)
                 timed(ffn_call, t)
         for name, e in extra.items():
             for m in e["cfg"]["ms"]:
@@ -446,6 +457,7 @@ def run_gpu(args, rank: int, world: int):
     per_m = {m: [] for m in args.m_sweep}
     per_t = {t: [] for t in MOE_T}
     per_f = {t: [] for t in MOE_T}
+    per_a8 = {t: [] for t in MOE_T}
     per_x = {(name, m): [] for name, e in extra.items() for m in e["cfg"]["ms"]}
 
     def blocks(fn, arg, n):
@@ -474,13 +486,16 @@ def run_gpu(args, rank: int, world: int):
             for t in MOE_T:
                 events += [("m", t, *b) for b in blocks(moe_call, t, args.steps)]
             for t in MOE_T:
+                events += [("a", t, *b) for b in blocks(moe_a8_call, t, args.steps)]
+            for t in MOE_T:
                 events += [("f", t, *b) for b in blocks(ffn_call, t, args.steps)]
         for key in per_x:
             events += [("x", key, *b) for b in blocks(extra_call, key, args.steps)]
         barrier()
         wall = time.perf_counter() - wall0
     for kind, key, k, e0, e1 in events:
-        {"d": per_m, "m": per_t, "f": per_f, "x": per_x}[kind][key].append(e0.elapsed_time(e1) * 1e-3 / k)
+        {"d": per_m, "m": per_t, "f": per_f, "a": per_a8, "x": per_x}[kind][key].append(
+            e0.elapsed_time(e1) * 1e-3 / k)
     gpu_launches = launches["n"]
 
     # ---- end to end through the C ABI with host buffers (pinned): per step the
@@ -540,6 +555,7 @@ def run_gpu(args, rank: int, world: int):
     if moe:
         res["moe"] = {t: statistics.mean(v) for t, v in per_t.items()}
         res["moe_ffn"] = {t: statistics.mean(v) for t, v in per_f.items()}
+        res["moe_w4a8"] = {t: statistics.mean(v) for t, v in per_a8.items()}
         res["moe_touched"] = {t: moe["T"][t]["touched"] for t in MOE_T}
     res["extra"] = {}
     for (name, m), v in per_x.items():
@@ -645,12 +661,15 @@ def main():
                     help="end-to-end pass with the copies on their own streams, overlapping the GEMMs")
     ap.add_argument("--m-sweep", type=str, default=",".join(map(str, M_SWEEP)),
                     help="comma-separated M values of the dense sweep")
+    ap.add_argument("--moe-t", type=str, default=",".join(map(str, MOE_T)),
+                    help="comma-separated token counts of the MoE sweep")
     ap.add_argument("--clocks-dir", type=str, default=None,
                     help="directory for the nvidia-smi clock samples of the timed region (default: a new "
                          "temporary directory)")
     args = ap.parse_args()
     args.m_sweep = [int(v) for v in args.m_sweep.split(",") if v]
     args.warmup = max(args.warmup, 3)
+    MOE_T[:] = [int(v) for v in args.moe_t.split(",") if v]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -782,9 +801,21 @@ def main():
             roof_t = max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
             fsw.append({"tokens": t, "us": round(tt * 1e6, 2), "tflops": round(fl / tt / 1e12, 2),
                         "gbs": round(by / tt / 1e9, 1), "roofline_frac": round(roof_t / tt, 3)})
+        asw = []
+        for t in MOE_T:
+            tt = res["moe_w4a8"][t]
+            fl = 2 * t * MOE_TOPK * MOE_N * MOE_K
+            by = res["moe_touched"][t] * (MOE_N * MOE_K // 2 + MOE_N * MOE_K // 32) + t * MOE_K * 2
+            roof_t = max(by / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * FP8_PER_BF16 * 1e12))
+            asw.append({"tokens": t, "us": round(tt * 1e6, 2), "tflops": round(fl / tt / 1e12, 2),
+                        "gbs": round(by / tt / 1e9, 1), "roofline_frac": round(roof_t / tt, 3)})
         line["moe"] = {"workload": "MoE gate+up, MXFP4 (e2m1 + UE8M0/32) experts, E=128, N=1536, K=2048, top-8, "
                                    "bf16 activations; route + grouped GEMM + combine per call",
                        "sweep": msw,
+                       "w4a8_workload": "the same MoE with W4A8-MXFP4: routed bf16 rows quantised to MXFP8 in the "
+                                        "gather, block-scaled grouped GEMM (roofline against the fp8 peak, measured "
+                                        f"bf16 x {FP8_PER_BF16})",
+                       "w4a8_sweep": asw,
                        "ffn_workload": "MoE feed-forward block: the gate+up experts above, SiLU(gate)*up, down "
                                        "experts E=128, N=2048, K=768 (MXFP4), routing-weighted combine per call",
                        "ffn_sweep": fsw}

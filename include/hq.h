@@ -487,6 +487,7 @@ hq_status hq_moe_plan_query(const hq_weight_desc* wdesc, int32_t tokens, int32_t
 /*
  * hq_tuning_reload — read the tuning switches again from the environment
  * (HQ_FORCE_BN, HQ_FORCE_SPLITK, HQ_FORCE_WSTAGES, HQ_FORCE_XSTAGES,
+ * HQ_FORCE_X2D: one 2-D activation copy per slab instead of one per stage,
  * HQ_TRACE).  They are otherwise read once, at the first call that plans a
  * launch.  For sweeps and tests that compare plans in one process; call it
  * only while no other call of this library runs.  The pages have no

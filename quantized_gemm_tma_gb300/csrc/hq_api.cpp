@@ -142,6 +142,8 @@ hq_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int env_int(const char* name, int dflt);
+
 // Activation map of the WnA16 kernel: X [rows][k] in 128-byte slabs (box_inner
 // elements) of bn rows.  When k fills whole slabs, one 3-D box carries the
 // `per_stage` slabs of a stage (one tensor copy per stage; *x3d = 1); else one
@@ -149,7 +151,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 hq_status encode_x(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem, const void* x, int64_t k,
                    int64_t rows, int64_t ldx, uint32_t box_inner, int bn, int per_stage, int* x3d) {
   *x3d = 0;
-  if (k % box_inner == 0) {
+  if (k % box_inner == 0 && env_int("HQ_FORCE_X2D", 0) == 0) {
     const uint64_t slabs = (static_cast<uint64_t>(per_stage) << 32) | static_cast<uint64_t>(k / box_inner);
     if (encode_2d(map, dtype, elem, x, k, rows, ldx, box_inner, bn, slabs) == HQ_OK) {
       *x3d = 1;
@@ -169,7 +171,7 @@ bool tiles_fit(int64_t rows, int64_t groups, int n_tiles) {
 // Tuning and trace switches from the environment, read on first use and
 // again by hq_tuning_reload().
 struct EnvKnobs {
-  int force_bn = 0, force_splitk = 0, force_wstages = 0, force_xstages = 0, trace = 0;
+  int force_bn = 0, force_splitk = 0, force_wstages = 0, force_xstages = 0, force_x2d = 0, trace = 0;
 };
 EnvKnobs read_env() {
   EnvKnobs e;
@@ -181,6 +183,7 @@ EnvKnobs read_env() {
   e.force_splitk = get("HQ_FORCE_SPLITK");
   e.force_wstages = get("HQ_FORCE_WSTAGES");
   e.force_xstages = get("HQ_FORCE_XSTAGES");
+  e.force_x2d = get("HQ_FORCE_X2D");
   e.trace = get("HQ_TRACE");
   return e;
 }
@@ -197,6 +200,7 @@ int env_int(const char* name, int dflt) {
   else if (!std::strcmp(name, "HQ_FORCE_SPLITK")) v = env().force_splitk;
   else if (!std::strcmp(name, "HQ_FORCE_WSTAGES")) v = env().force_wstages;
   else if (!std::strcmp(name, "HQ_FORCE_XSTAGES")) v = env().force_xstages;
+  else if (!std::strcmp(name, "HQ_FORCE_X2D")) v = env().force_x2d;
   else if (!std::strcmp(name, "HQ_TRACE")) v = env().trace;
   return v ? v : dflt;
 }
