@@ -916,6 +916,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     const int r = quarter * 32 + static_cast<int>(lane);  // weight row within the tile (TMEM lane)
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol0 + static_cast<uint32_t>(t * 64);
     const bool promote = CLS == 0 && p.promote;
+    // the weight-tile layout fields this role reads per K-block, in registers
+    const uint32_t q_scale_off = p.scale_off, q_zero_off = p.zero_off, q_hi_off = p.hi_off;
+    const int q_g_kb = p.g_kb, q_group_k = p.group_k, q_has_zeros = p.has_zeros, q_channel = p.channel;
     Sched<MOE> sc;
     sc.init(p);
     Ring rg;
@@ -933,10 +936,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     // chunks c0, c0 + 1 (64 K) of this row -> 2 x 16 pairs
     auto convert2 = [&](const uint8_t* wsm, int c0, uint32_t (&o)[2][16]) {
       if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
-        if (!p.channel && p.g_kb == 1) {
+        if (!q_channel && q_g_kb == 1) {
           if (!gk_valid) {
-            const uint32_t s16 = promote ? 0u : reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r];
-            const uint32_t z = p.has_zeros ? wsm[p.zero_off + r] : zrow;
+            const uint32_t s16 = promote ? 0u : reinterpret_cast<const uint16_t*>(wsm + q_scale_off)[r];
+            const uint32_t z = q_has_zeros ? wsm[q_zero_off + r] : zrow;
             gk = promote ? int4_consts<BF16, false>(z, 0u) : int4_consts<BF16, true>(z, s16);
             gk_valid = true;
           }
@@ -958,21 +961,21 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         const uint4 q = *reinterpret_cast<const uint4*>(wsm + (c * kTileN + r) * 16);
         uint32_t z = zrow, sc16 = 0;
         if constexpr (FMT == static_cast<int>(WFmt::MXFP4) || FMT == static_cast<int>(WFmt::MXINT4)) {
-          sc16 = wsm[p.scale_off + r * 4 + c];
+          sc16 = wsm[q_scale_off + r * 4 + c];
         } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
-          sc16 = reinterpret_cast<const uint16_t*>(wsm + p.scale_off + r * 8)[c];
-        } else if (!p.channel) {
-          const int g = (p.g_kb > 1) ? (32 * c) / p.group_k : 0;
-          sc16 = reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r * p.g_kb + g];
-          if (p.has_zeros) z = wsm[p.zero_off + r * p.g_kb + g];
+          sc16 = reinterpret_cast<const uint16_t*>(wsm + q_scale_off + r * 8)[c];
+        } else if (!q_channel) {
+          const int g = (q_g_kb > 1) ? (32 * c) / q_group_k : 0;
+          sc16 = reinterpret_cast<const uint16_t*>(wsm + q_scale_off)[r * q_g_kb + g];
+          if (q_has_zeros) z = wsm[q_zero_off + r * q_g_kb + g];
         }
         if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
-          if (p.channel || promote) dq_int4<BF16, false>(q, z, sc16, o[i]);
+          if (q_channel || promote) dq_int4<BF16, false>(q, z, sc16, o[i]);
           else dq_int4<BF16, true>(q, z, sc16, o[i]);
         } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
-          const uint2 qh = *reinterpret_cast<const uint2*>(wsm + p.hi_off + (c * kTileN + r) * 8);
+          const uint2 qh = *reinterpret_cast<const uint2*>(wsm + q_hi_off + (c * kTileN + r) * 8);
           const uint32_t c2 = (magic_half<BF16>() + z) * 0x00010001u;
-          if (p.channel || promote) dq_int6<BF16, false>(q, qh, c2, 0, o[i]);
+          if (q_channel || promote) dq_int6<BF16, false>(q, qh, c2, 0, o[i]);
           else dq_int6<BF16, true>(q, qh, c2, sc16 * 0x00010001u, o[i]);
         } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
           dq_nvfp4(q, sc16, o[i]);
@@ -994,7 +997,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     while (ok && sc.next(p, s_tabs, u)) {
       const int n = u.nt * kTileN + r;
       zrow = static_cast<uint32_t>(p.zero_sym);
-      if (p.channel && p.has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
+      if (q_channel && q_has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
       for (int kb = u.kb0; kb < u.kb1; kb += KPS, ++S) {
         const int cnt = min(KPS, u.kb1 - kb);
         if ((S & 1u) == sg) {
@@ -1013,7 +1016,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             // kSRing positions back has been read.
             if (promote) {
               constexpr float kOpFixD = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
-              const uint32_t s16 = reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r * p.g_kb];
+              const uint32_t s16 = reinterpret_cast<const uint16_t*>(wsm + q_scale_off)[r * q_g_kb];
               const float sf = BF16 ? __uint_as_float(s16 << 16)
                                     : __half2float(__ushort_as_half(static_cast<unsigned short>(s16)));
               const int si = pos * kSRing + static_cast<int>(cpos % kSRing);
@@ -1032,12 +1035,12 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               const uint32_t* es = e_st + rg.s * kEStage + pos * 128;
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                ww[j] = mx_w_exp_fold(*reinterpret_cast<const uint32_t*>(wsm + p.scale_off + (32 * j + lane) * 4));
+                ww[j] = mx_w_exp_fold(*reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4));
                 xw[j] = es[32 * j + lane];
               }
               // this lane's row: sub-blocks whose exponent cannot take the fold
               // are converted exactly (rare: a block scale above 2^121)
-              const uint32_t big = mx_big(*reinterpret_cast<const uint32_t*>(wsm + p.scale_off + r * 4));
+              const uint32_t big = mx_big(*reinterpret_cast<const uint32_t*>(wsm + q_scale_off + r * 4));
               const bool any_big = __any_sync(0xffffffffu, big != 0u);
               uint32_t o8[2][8];
               auto conv8 = [&](int c0) {
@@ -1134,6 +1137,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     const int r = quarter * 32 + static_cast<int>(lane);  // weight row within the tile (TMEM lane)
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol0;
     const bool promote = CLS == 0 && p.promote;
+    // the weight-tile layout fields this role reads per K-block, in registers
+    const uint32_t q_scale_off = p.scale_off, q_zero_off = p.zero_off, q_hi_off = p.hi_off;
+    const int q_g_kb = p.g_kb, q_group_k = p.group_k, q_has_zeros = p.has_zeros, q_channel = p.channel;
     Sched<MOE> sc;
     sc.init(p);
     Ring rg;
@@ -1146,7 +1152,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     while (ok && sc.next(p, s_tabs, u)) {
       const int n = u.nt * kTileN + r;
       uint32_t zrow = static_cast<uint32_t>(p.zero_sym);
-      if (p.channel && p.has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
+      if (q_channel && q_has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
       for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
         const int cnt = min(KPS, u.kb1 - kb);
         if (!warp_wait(&w_full[rg.s], rg.ph, abort_flag)) {
@@ -1167,7 +1173,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             const uint32_t* es = e_st + rg.s * kEStage + gi * 128;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              ww[j] = mx_w_exp_fold(*reinterpret_cast<const uint32_t*>(wsm + p.scale_off + (32 * j + lane) * 4));
+              ww[j] = mx_w_exp_fold(*reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4));
               xw[j] = es[32 * j + lane];
             }
           }
@@ -1176,20 +1182,20 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             const int c = sub * G + i;
             qc[i] = *reinterpret_cast<const uint4*>(wsm + (c * kTileN + r) * 16);
             if constexpr (FMT == static_cast<int>(WFmt::INT6))
-              qh[i] = *reinterpret_cast<const uint2*>(wsm + p.hi_off + (c * kTileN + r) * 8);
+              qh[i] = *reinterpret_cast<const uint2*>(wsm + q_hi_off + (c * kTileN + r) * 8);
             if constexpr (FMT == static_cast<int>(WFmt::MXFP4) || FMT == static_cast<int>(WFmt::MXINT4) || A8) {
-              ss[i] = wsm[p.scale_off + r * 4 + c];
+              ss[i] = wsm[q_scale_off + r * 4 + c];
               zz[i] = 0;
             } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
-              ss[i] = reinterpret_cast<const uint16_t*>(wsm + p.scale_off + r * 8)[c];
+              ss[i] = reinterpret_cast<const uint16_t*>(wsm + q_scale_off + r * 8)[c];
               zz[i] = 0;
             } else {
               zz[i] = zrow;
               ss[i] = 0;
-              if (!p.channel) {
-                const int g = (p.g_kb > 1) ? (32 * c) / p.group_k : 0;
-                ss[i] = reinterpret_cast<const uint16_t*>(wsm + p.scale_off)[r * p.g_kb + g];
-                if (p.has_zeros) zz[i] = wsm[p.zero_off + r * p.g_kb + g];
+              if (!q_channel) {
+                const int g = (q_g_kb > 1) ? (32 * c) / q_group_k : 0;
+                ss[i] = reinterpret_cast<const uint16_t*>(wsm + q_scale_off)[r * q_g_kb + g];
+                if (q_has_zeros) zz[i] = wsm[q_zero_off + r * q_g_kb + g];
               }
             }
           }
@@ -1218,11 +1224,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
 #pragma unroll
           for (int i = 0; i < G; ++i) {
             if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
-              if (p.channel || promote) dq_int4<BF16, false>(qc[i], zz[i], ss[i], o[i]);
+              if (q_channel || promote) dq_int4<BF16, false>(qc[i], zz[i], ss[i], o[i]);
               else dq_int4<BF16, true>(qc[i], zz[i], ss[i], o[i]);
             } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
               const uint32_t c2 = (magic_half<BF16>() + zz[i]) * 0x00010001u;
-              if (p.channel || promote) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o[i]);
+              if (q_channel || promote) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o[i]);
               else dq_int6<BF16, true>(qc[i], qh[i], c2, ss[i] * 0x00010001u, o[i]);
             } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
               dq_nvfp4(qc[i], ss[i], o[i]);
