@@ -26,6 +26,7 @@
 
 #include "hq_internal.h"
 #include "hq_launch.h"
+#include "hq_ptx.cuh"
 #include "mxfp8.cuh"
 
 namespace hq {
@@ -68,6 +69,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     moe_route_kernel(const int* __restrict__ ids, int pairs, int num_experts, int bn, int* __restrict__ exp_off,
                      int* __restrict__ tile_off, int* __restrict__ perm, int* __restrict__ off_out,
                      int* __restrict__ perm_out, int* __restrict__ status) {
+  // launched with programmatic dependent launch: the previous grid and its
+  // memory are complete before anything here touches global memory
+  dev::grid_dep_wait();
+  dev::grid_dep_launch();
   extern __shared__ int sm[];
   int* wcnt = sm;                                  // [warps][E]: per-warp counts, then write cursors
   int* warp_tot = sm + kRouteWarps * num_experts;  // [33]
@@ -163,6 +168,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     moe_grouped_route_kernel(const int* __restrict__ rows_in, int masked, int rows, int num_experts, int bn,
                              int* __restrict__ exp_off, int* __restrict__ tile_off, int* __restrict__ perm,
                              int* __restrict__ x_base, int* __restrict__ status) {
+  // launched with programmatic dependent launch: the previous grid and its
+  // memory are complete before anything here touches global memory
+  dev::grid_dep_wait();
+  dev::grid_dep_launch();
   __shared__ int warp_tot[33];
   __shared__ int s_off[kRouteThreads];
   __shared__ int s_base[kRouteThreads];
@@ -261,6 +270,8 @@ __global__ void __launch_bounds__(256) moe_permute_mxfp8_kernel(const __nv_bfloa
 // One thread per (pair, 8 consecutive outputs): 16-byte loads and stores.
 __global__ void moe_act_kernel(const __nv_bfloat16* __restrict__ h, int64_t ldh, int pairs, int inter,
                                __nv_bfloat16* __restrict__ a, int64_t lda) {
+  dev::grid_dep_wait();
+  dev::grid_dep_launch();
   const int groups = inter / 8;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(pairs) * groups) return;
@@ -284,6 +295,8 @@ __global__ void moe_act_kernel(const __nv_bfloat16* __restrict__ h, int64_t ldh,
 // One thread per (token, 8 consecutive outputs).
 __global__ void moe_combine_kernel(const float* __restrict__ z, const int* __restrict__ ids, int tokens, int topk,
                                    int num_experts, int n, int n_pad, __nv_bfloat16* __restrict__ y, int64_t ldy) {
+  dev::grid_dep_wait();
+  dev::grid_dep_launch();
   const int groups = (n + 7) / 8;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(tokens) * groups) return;
@@ -321,18 +334,18 @@ cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, in
   const size_t smem = sizeof(int) * (static_cast<size_t>(kRouteWarps) * num_experts + 33);
   cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(moe_route_kernel));
   if (e != cudaSuccess) return e;
-  moe_route_kernel<<<1, kRouteThreads, smem, stream>>>(topk_ids, pairs, num_experts, bn, expert_offsets,
-                                                        tile_offsets, perm, offsets_out, perm_out, status);
-  return cudaGetLastError();
+  return launch_pdl(reinterpret_cast<const void*>(moe_route_kernel), 1, kRouteThreads, static_cast<uint32_t>(smem),
+                    stream, 1, topk_ids, pairs, num_experts, bn, expert_offsets, tile_offsets, perm, offsets_out,
+                    perm_out, status);
 }
 
 cudaError_t launch_moe_grouped_route(const int* rows_in, bool masked, int rows, int num_experts, int bn,
                                      int* expert_offsets, int* tile_offsets, int* perm, int* x_base, int* status,
                                      cudaStream_t stream) {
   if (num_experts > kRouteThreads) return cudaErrorInvalidValue;
-  moe_grouped_route_kernel<<<1, kRouteThreads, 0, stream>>>(rows_in, masked ? 1 : 0, rows, num_experts, bn,
-                                                             expert_offsets, tile_offsets, perm, x_base, status);
-  return cudaGetLastError();
+  const int masked_i = masked ? 1 : 0;
+  return launch_pdl(reinterpret_cast<const void*>(moe_grouped_route_kernel), 1, kRouteThreads, 0u, stream, 1,
+                    rows_in, masked_i, rows, num_experts, bn, expert_offsets, tile_offsets, perm, x_base, status);
 }
 
 cudaError_t launch_moe_permute(const void* x, int64_t ldx, int tokens, const int* perm, const int* routed,
@@ -367,9 +380,10 @@ cudaError_t launch_moe_act(const void* h, int64_t ldh, int pairs, int inter, voi
   const int64_t threads = static_cast<int64_t>(pairs) * (inter / 8);
   if (threads == 0) return cudaSuccess;
   const int block = 256;
-  moe_act_kernel<<<static_cast<unsigned>((threads + block - 1) / block), block, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(h), ldh, pairs, inter, static_cast<__nv_bfloat16*>(a), lda);
-  return cudaGetLastError();
+  const __nv_bfloat16* hp = static_cast<const __nv_bfloat16*>(h);
+  __nv_bfloat16* ap = static_cast<__nv_bfloat16*>(a);
+  return launch_pdl(reinterpret_cast<const void*>(moe_act_kernel), static_cast<int>((threads + block - 1) / block),
+                    block, 0u, stream, 1, hp, ldh, pairs, inter, ap, lda);
 }
 
 cudaError_t launch_moe_combine(const float* zbuf, const int* topk_ids, int tokens, int topk, int num_experts, int n,
@@ -377,9 +391,9 @@ cudaError_t launch_moe_combine(const float* zbuf, const int* topk_ids, int token
   (void)bf16;
   const int64_t threads = static_cast<int64_t>(tokens) * ((n + 7) / 8);
   const int block = 256;
-  moe_combine_kernel<<<static_cast<unsigned>((threads + block - 1) / block), block, 0, stream>>>(
-      zbuf, topk_ids, tokens, topk, num_experts, n, n_pad, static_cast<__nv_bfloat16*>(y), ldy);
-  return cudaGetLastError();
+  __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(y);
+  return launch_pdl(reinterpret_cast<const void*>(moe_combine_kernel), static_cast<int>((threads + block - 1) / block),
+                    block, 0u, stream, 1, zbuf, topk_ids, tokens, topk, num_experts, n, n_pad, yp, ldy);
 }
 
 }  // namespace hq
