@@ -745,6 +745,7 @@ hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int3
   ws += 2 * align_up(sizeof(int) * (L.num_experts + 1), kAlign);
   ws += align_up(sizeof(int) * std::max<size_t>(pairs, 1), kAlign);
   ws += align_up(sizeof(float) * pairs * L.n_pad, kAlign);
+  ws += align_up(sizeof(int) * kRouteMaxBlocks * L.num_experts, kAlign);  // routing: per-block expert counts
   *bytes = ws;
   return HQ_OK;
 }
@@ -788,10 +789,12 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   int* perm = reinterpret_cast<int*>(ws + off);
   off += align_up(sizeof(int) * std::max<int64_t>(pairs, 1), kAlign);
   float* zbuf = reinterpret_cast<float*>(ws + off);
+  off += align_up(sizeof(float) * static_cast<size_t>(pairs) * L.n_pad, kAlign);
+  int* counts = reinterpret_cast<int*>(ws + off);
 
   const int bn = moe_tile_bn(static_cast<double>(pairs) / L.num_experts);
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L.num_experts, bn, exp_off, tile_off, perm,
-                       expert_offsets_out, perm_out, reinterpret_cast<int*>(ws), s) != cudaSuccess)
+                       expert_offsets_out, perm_out, counts, reinterpret_cast<int*>(ws), s) != cudaSuccess)
     return HQ_ERR_CUDA;
   int stages = 0, groups = 0;
   st = launch_moe_grouped(L, wt, bn, tokens, topk, topk_w, x, ldx, y, ldy, exp_off, tile_off, perm, zbuf,
@@ -834,6 +837,7 @@ hq_status hq_moe_ffn_workspace_size(const hq_weight_desc* w13, const hq_weight_d
   ws += align_up(2 * pairs * ldh, kAlign);             // H: gate and up, bf16
   ws += align_up(2 * pairs * lda, kAlign);             // A: silu(gate) * up, bf16
   ws += align_up(sizeof(float) * pairs * L2.n_pad, kAlign);  // weighted down-projection rows
+  ws += align_up(sizeof(int) * kRouteMaxBlocks * L13.num_experts, kAlign);  // routing: per-block expert counts
   *bytes = ws;
   return HQ_OK;
 }
@@ -888,9 +892,11 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
   void* abuf = ws + off;
   off += align_up(2 * static_cast<size_t>(pairs) * lda, kAlign);
   float* zbuf = reinterpret_cast<float*>(ws + off);
+  off += align_up(sizeof(float) * static_cast<size_t>(pairs) * L2.n_pad, kAlign);
+  int* counts = reinterpret_cast<int*>(ws + off);
   const int bn = moe_tile_bn(static_cast<double>(pairs) / L13.num_experts);
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L13.num_experts, bn, exp_off, tile_off, perm, nullptr,
-                       nullptr, reinterpret_cast<int*>(ws), s) != cudaSuccess)
+                       nullptr, counts, reinterpret_cast<int*>(ws), s) != cudaSuccess)
     return HQ_ERR_CUDA;
   int stages = 0, groups = 0;
   // gate+up: H[f] = X[t] . W13_e^T, written at pair row f
