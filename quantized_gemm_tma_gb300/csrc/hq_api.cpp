@@ -877,6 +877,7 @@ hq_status hq_moe_workspace_size(const hq_weight_desc* desc, int32_t tokens, int3
   ws += align_up(sizeof(int) * std::max<size_t>(pairs, 1), kAlign);
   ws += align_up(sizeof(float) * pairs * L.n_pad, kAlign);
   ws += align_up(2 * pairs * static_cast<size_t>(permuted_ld(L.k)), kAlign);  // permuted activations, bf16
+  ws += align_up(sizeof(int) * kRouteMaxBlocks * L.num_experts, kAlign);  // routing: per-block expert counts
   *bytes = ws;
   return HQ_OK;
 }
@@ -930,10 +931,12 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   // region (k + k/32 bytes a row, within the 2k of a bf16 row)
   uint8_t* xq = static_cast<uint8_t*>(xg);
   uint8_t* xe = xq + static_cast<size_t>(pairs) * L.k;
+  off += align_up(2 * static_cast<size_t>(pairs) * static_cast<size_t>(ldg), kAlign);
+  int* counts = reinterpret_cast<int*>(ws + off);
 
   const int bn = moe_tile_bn(static_cast<double>(pairs) / L.num_experts);
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L.num_experts, bn, exp_off, tile_off, perm,
-                       expert_offsets_out, perm_out, reinterpret_cast<int*>(ws), s) != cudaSuccess)
+                       expert_offsets_out, perm_out, counts, reinterpret_cast<int*>(ws), s) != cudaSuccess)
     return HQ_ERR_CUDA;
   const cudaError_t pe =
       a8 ? launch_moe_permute_mxfp8(x, ldx, tokens, perm, exp_off + L.num_experts, static_cast<int>(pairs), topk, L.k,
@@ -987,6 +990,7 @@ hq_status hq_moe_ffn_workspace_size(const hq_weight_desc* w13, const hq_weight_d
   ws += align_up(sizeof(float) * pairs * L2.n_pad, kAlign);  // weighted down-projection rows
   ws += align_up(2 * pairs * static_cast<size_t>(permuted_ld(L13.k)), kAlign);  // permuted activations, bf16
   ws += kGateBufBytes;  // per-CTA gate sums of the fused silu(gate) * up
+  ws += align_up(sizeof(int) * kRouteMaxBlocks * L13.num_experts, kAlign);  // routing: per-block expert counts
   *bytes = ws;
   return HQ_OK;
 }
@@ -1046,9 +1050,11 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
   const int64_t ldg = permuted_ld(L13.k);
   off += align_up(2 * static_cast<size_t>(pairs) * static_cast<size_t>(ldg), kAlign);
   float* gate_buf = reinterpret_cast<float*>(ws + off);
+  off += kGateBufBytes;
+  int* counts = reinterpret_cast<int*>(ws + off);
   const int bn = moe_tile_bn(static_cast<double>(pairs) / L13.num_experts);
   if (launch_moe_route(topk_ids, static_cast<int>(pairs), L13.num_experts, bn, exp_off, tile_off, perm, nullptr,
-                       nullptr, reinterpret_cast<int*>(ws), s) != cudaSuccess)
+                       nullptr, counts, reinterpret_cast<int*>(ws), s) != cudaSuccess)
     return HQ_ERR_CUDA;
   if (launch_moe_permute(x, ldx, tokens, perm, exp_off + L13.num_experts, static_cast<int>(pairs), topk, L13.k, xg,
                          ldg, di.sms, s) != cudaSuccess)

@@ -79,8 +79,15 @@ cudaError_t launch_mxfp8_quantize(const void* x, int64_t ldx, int m, int k, void
                                   int64_t lde, cudaStream_t stream);
 
 // moe.cu
+// Routing of more than kRouteSinglePairs pairs runs on up to kRouteMaxBlocks
+// blocks of about kRoutePairsPerBlock pairs each, through an int32 table of
+// per-block expert counts [blocks][E] in the workspace (`counts`).
+constexpr int kRouteSinglePairs = 8192;
+constexpr int kRouteMaxBlocks = 128;
+constexpr int kRoutePairsPerBlock = 2048;
+int moe_route_blocks(int pairs);
 cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, int bn, int* expert_offsets,
-                             int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* status,
+                             int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* counts, int* status,
                              cudaStream_t stream);
 cudaError_t launch_moe_grouped_route(const int* rows_in, bool masked, int rows, int num_experts, int bn,
                                      int* expert_offsets, int* tile_offsets, int* perm, int* x_base, int* status,

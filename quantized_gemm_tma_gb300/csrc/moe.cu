@@ -35,6 +35,7 @@ namespace {
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteChunk = 8;  // expert ids per lane loaded together
+constexpr int kCountThreads = 256;
 
 // Block-wide exclusive scan of one value per thread (threads >= count hold 0).
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
@@ -65,10 +66,38 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& t
   return r;
 }
 
+// Many pairs: block b counts the experts of its contiguous segment of
+// blk_seg pairs into counts[b][E]; the route kernel below, one block per
+// segment, turns the table into each block's write base.
+__global__ void __launch_bounds__(kCountThreads)
+    moe_route_count_kernel(const int* __restrict__ ids, int pairs, int num_experts, int blk_seg,
+                           int* __restrict__ counts, int* __restrict__ status) {
+  extern __shared__ int cnt_s[];  // [E]
+  const int E = num_experts;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = 0;
+  __syncthreads();
+  const int g0 = blockIdx.x * blk_seg, g1 = min(pairs, g0 + blk_seg);
+  bool bad = false;
+  for (int f = g0 + static_cast<int>(threadIdx.x); f < g1; f += blockDim.x) {
+    const int e = ids[f];
+    if (e >= 0 && e < E) atomicAdd(&cnt_s[e], 1);
+    else bad = true;
+  }
+  if (bad) atomicCAS(status, 0, static_cast<int>(HQ_ERR_INVALID_VALUE));
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[static_cast<size_t>(blockIdx.x) * E + e] = cnt_s[e];
+}
+
+// Block b routes the pairs [b blk_seg, (b + 1) blk_seg): per-warp histograms
+// of its segment, then a stable scatter.  With one block (counts == nullptr)
+// the expert totals are the block's own; with several, counts[gridDim.x][E]
+// gives the totals and the pairs of earlier blocks, so every pair lands
+// where the stable counting sort over all pairs puts it.
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    moe_route_kernel(const int* __restrict__ ids, int pairs, int num_experts, int bn, int* __restrict__ exp_off,
-                     int* __restrict__ tile_off, int* __restrict__ perm, int* __restrict__ off_out,
-                     int* __restrict__ perm_out, int* __restrict__ status) {
+    moe_route_kernel(const int* __restrict__ ids, int pairs, int num_experts, int bn, int blk_seg,
+                     const int* __restrict__ counts, int* __restrict__ exp_off, int* __restrict__ tile_off,
+                     int* __restrict__ perm, int* __restrict__ off_out, int* __restrict__ perm_out,
+                     int* __restrict__ status) {
   // launched with programmatic dependent launch: the previous grid and its
   // memory are complete before anything here touches global memory
   dev::grid_dep_wait();
@@ -78,8 +107,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   int* warp_tot = sm + kRouteWarps * num_experts;  // [33]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = num_experts;
-  const int seg = (pairs + kRouteWarps - 1) / kRouteWarps;
-  const int f0 = warp * seg, f1 = min(pairs, f0 + seg);
+  const int g0 = blockIdx.x * blk_seg, g1 = min(pairs, g0 + blk_seg);
+  const int seg = (g1 - g0 + kRouteWarps - 1) / kRouteWarps;
+  const int f0 = g0 + warp * seg, f1 = min(g1, f0 + seg);
 
   for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) wcnt[i] = 0;
   __syncthreads();
@@ -100,29 +130,42 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       else bad = true;
     }
   }
-  if (bad) atomicCAS(status, 0, static_cast<int>(HQ_ERR_INVALID_VALUE));
+  if (bad && counts == nullptr) atomicCAS(status, 0, static_cast<int>(HQ_ERR_INVALID_VALUE));
   __syncthreads();
 
-  // per-expert totals and exclusive prefix over experts (rows and m-tiles)
-  int cnt = 0;
-  if (tid < E)
-    for (int w = 0; w < kRouteWarps; ++w) cnt += wcnt[w * E + tid];
+  // per-expert totals (and the pairs of earlier blocks), exclusive prefix
+  // over experts (rows and m-tiles)
+  int cnt = 0, before = 0;
+  if (tid < E) {
+    if (counts == nullptr) {
+      for (int w = 0; w < kRouteWarps; ++w) cnt += wcnt[w * E + tid];
+    } else {
+      for (int b = 0; b < static_cast<int>(gridDim.x); ++b) {
+        const int c = counts[static_cast<size_t>(b) * E + tid];
+        cnt += c;
+        if (b < static_cast<int>(blockIdx.x)) before += c;
+      }
+    }
+  }
   int rows_total = 0, tiles_total = 0;
   const int row_base = block_exclusive_scan(tid < E ? cnt : 0, warp_tot, rows_total);
   const int tile_base = block_exclusive_scan(tid < E ? (cnt + bn - 1) / bn : 0, warp_tot, tiles_total);
   if (tid < E) {
-    exp_off[tid] = row_base;
-    tile_off[tid] = tile_base;
-    if (off_out) off_out[tid] = row_base;
-    // write cursor of each warp for this expert: row_base + counts of earlier warps
-    int run = row_base;
+    if (blockIdx.x == 0) {
+      exp_off[tid] = row_base;
+      tile_off[tid] = tile_base;
+      if (off_out) off_out[tid] = row_base;
+    }
+    // write cursor of each warp for this expert: the pairs routed to it by
+    // earlier blocks and by this block's earlier warps come first
+    int run = row_base + before;
     for (int w = 0; w < kRouteWarps; ++w) {
       const int c = wcnt[w * E + tid];
       wcnt[w * E + tid] = run;
       run += c;
     }
   }
-  if (tid == 0) {
+  if (tid == 0 && blockIdx.x == 0) {
     exp_off[E] = rows_total;
     tile_off[E] = tiles_total;
     if (off_out) off_out[E] = rows_total;
@@ -328,15 +371,30 @@ __global__ void moe_combine_kernel(const float* __restrict__ z, const int* __res
 
 }  // namespace
 
+int moe_route_blocks(int pairs) {
+  if (pairs <= kRouteSinglePairs) return 1;
+  return std::min(kRouteMaxBlocks, (pairs + kRoutePairsPerBlock - 1) / kRoutePairsPerBlock);
+}
+
 cudaError_t launch_moe_route(const int* topk_ids, int pairs, int num_experts, int bn, int* expert_offsets,
-                             int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* status,
-                             cudaStream_t stream) {
+                             int* tile_offsets, int* perm, int* offsets_out, int* perm_out, int* counts,
+                             int* status, cudaStream_t stream) {
   const size_t smem = sizeof(int) * (static_cast<size_t>(kRouteWarps) * num_experts + 33);
   cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(moe_route_kernel));
   if (e != cudaSuccess) return e;
-  return launch_pdl(reinterpret_cast<const void*>(moe_route_kernel), 1, kRouteThreads, static_cast<uint32_t>(smem),
-                    stream, 1, topk_ids, pairs, num_experts, bn, expert_offsets, tile_offsets, perm, offsets_out,
-                    perm_out, status);
+  const int blocks = moe_route_blocks(pairs);
+  const int blk_seg = (pairs + blocks - 1) / blocks;
+  if (blocks > 1) {
+    moe_route_count_kernel<<<blocks, kCountThreads, sizeof(int) * num_experts, stream>>>(topk_ids, pairs,
+                                                                                       num_experts, blk_seg,
+                                                                                       counts, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int* block_counts = blocks > 1 ? counts : nullptr;
+  return launch_pdl(reinterpret_cast<const void*>(moe_route_kernel), blocks, kRouteThreads,
+                    static_cast<uint32_t>(smem), stream, 1, topk_ids, pairs, num_experts, bn, blk_seg, block_counts,
+                    expert_offsets, tile_offsets, perm, offsets_out, perm_out, status);
 }
 
 cudaError_t launch_moe_grouped_route(const int* rows_in, bool masked, int rows, int num_experts, int bn,

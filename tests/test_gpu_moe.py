@@ -33,6 +33,7 @@ SMALL = [
     (1, 1, 8, 128, 256, 2),
     (2, 200, 16, 384, 384, 8),
     (3, 64, 4, 200, 160, 3),      # ragged N and K
+    (4, 2100, 8, 128, 128, 4),    # 8400 pairs: routing on several blocks
 ]
 
 
