@@ -337,7 +337,7 @@ __device__ __forceinline__ void dq_mxfp4_e4m3(const uint4 q, uint32_t (&o)[8]) {
 // [4:2] (sign at bit 7) is the e4m3 number of value x * 2^-6, exactly — e2m1's
 // exponent bias is 6 below e4m3's, and e2m1's subnormal 0.5 lands on e4m3's
 // subnormal grid.  The 2^6 goes into the sub-block's UE8M0 weight exponent
-// (mx_w_exp_fold).
+// (st_mx_scales with fold).
 __device__ __forceinline__ void dq_mxfp4_e4m3_s6(const uint4 q, uint32_t (&o)[8]) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -350,21 +350,25 @@ __device__ __forceinline__ void dq_mxfp4_e4m3_s6(const uint4 q, uint32_t (&o)[8]
   }
 }
 
-// Four UE8M0 weight exponents (one per byte) with the 2^6 of dq_mxfp4_e4m3_s6
-// folded in: +6 on every byte up to 248.  A byte above 248 keeps its value and
-// its sub-block is converted with the exact table instead (mx_big marks it).
-__device__ __forceinline__ uint32_t mx_big(uint32_t w) { return __vcmpgtu4(w, 0xF8F8F8F8u); }
-__device__ __forceinline__ uint32_t mx_w_exp_fold(uint32_t w) { return __vadd4(w, 0x06060606u & ~mx_big(w)); }
+// A UE8M0 weight exponent takes the 2^6 of dq_mxfp4_e4m3_s6 when it is at
+// most 248; a larger one keeps its value and its sub-block is converted with
+// the exact table instead.
+__device__ __forceinline__ uint32_t mx_fold(uint32_t e) { return e <= 248u ? e + 6u : e; }
 
 // W4A8 scale factors of one K-block, in the TMEM layout the block-scaled MMA
 // reads: for lane l of every lane quarter, column j of a 4-column group holds
 // the UE8M0 exponent of row (or token) 32j + l, the same byte in all four byte
-// positions.  wordA/wordB: the exponents of the four 32-K sub-blocks of the
-// K-block in bytes 0..3; sub selects one.
+// positions.  words: the exponents of the four 32-K sub-blocks of the
+// K-block in bytes 0..3; sub selects one; FOLD applies mx_fold (weights).
+template <bool FOLD>
 __device__ __forceinline__ void st_mx_scales(uint32_t taddr, const uint32_t (&words)[4], int sub) {
   uint32_t v[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) v[j] = ((words[j] >> (8 * sub)) & 0xFFu) * 0x01010101u;
+  for (int j = 0; j < 4; ++j) {
+    uint32_t e = (words[j] >> (8 * sub)) & 0xFFu;
+    if constexpr (FOLD) e = mx_fold(e);
+    v[j] = e * 0x01010101u;
+  }
   dev::tmem_st4(taddr, v[0], v[1], v[2], v[3]);
 }
 
@@ -1029,26 +1033,29 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             const uint32_t aph = (ca & 1u) ^ 1u;
             if constexpr (A8) {
               // scale exponents of this K-block: weight rows 32j + lane (from
-              // the tile, with the conversion's 2^6 folded in) and tokens
-              // 32j + lane (staged beside the tile by the weight producer)
+              // the tile; the conversion's 2^6 is folded in when they are
+              // stored) and tokens 32j + lane (staged beside the tile by the
+              // weight producer)
               uint32_t ww[4], xw[4];
               const uint32_t* es = e_st + rg.s * kEStage + pos * 128;
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                ww[j] = mx_w_exp_fold(*reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4));
+                ww[j] = *reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4);
                 xw[j] = es[32 * j + lane];
               }
               // this lane's row: sub-blocks whose exponent cannot take the fold
-              // are converted exactly (rare: a block scale above 2^121)
-              const uint32_t big = mx_big(*reinterpret_cast<const uint32_t*>(wsm + q_scale_off + r * 4));
-              const bool any_big = __any_sync(0xffffffffu, big != 0u);
+              // are converted exactly (rare: a block scale above 2^121); the
+              // warp checks for bytes of 248 and up (top five bits set) first
+              const uint32_t own = *reinterpret_cast<const uint32_t*>(wsm + q_scale_off + r * 4);
+              const bool any_big =
+                  __any_sync(0xffffffffu, (own & (own << 1) & (own << 2) & (own << 3) & (own << 4) & 0x80808080u) != 0u);
               uint32_t o8[2][8];
               auto conv8 = [&](int c0) {
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                   const uint4 q = *reinterpret_cast<const uint4*>(wsm + ((c0 + i) * kTileN + r) * 16);
                   dq_mxfp4_e4m3_s6(q, o8[i]);
-                  if (any_big && ((big >> (8 * (c0 + i))) & 1u)) dq_mxfp4_e4m3(q, o8[i]);
+                  if (any_big && ((own >> (8 * (c0 + i))) & 0xFFu) > 248u) dq_mxfp4_e4m3(q, o8[i]);
                 }
               };
               auto st_half = [&](int h) {
@@ -1061,8 +1068,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
                 dev::tmem_st16(a_lane + h * 16, o16);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                  st_mx_scales(a_lane + 32 + h * 16 + i * 8, ww, 2 * h + i);
-                  st_mx_scales(a_lane + 32 + h * 16 + i * 8 + 4, xw, 2 * h + i);
+                  st_mx_scales<true>(a_lane + 32 + h * 16 + i * 8, ww, 2 * h + i);
+                  st_mx_scales<false>(a_lane + 32 + h * 16 + i * 8 + 4, xw, 2 * h + i);
                 }
               };
               conv8(0);
@@ -1168,12 +1175,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         if (real) {
           const uint8_t* wsm = w_st + rg.s * w_stage + gi * tile_bytes;
           if constexpr (A8) {
-            // weight exponents with the conversion's 2^6 folded in; token
-            // exponents staged beside the tile by the weight producer
+            // weight exponents (the conversion's 2^6 is folded in when they
+            // are stored); token exponents staged beside the tile by the
+            // weight producer
             const uint32_t* es = e_st + rg.s * kEStage + gi * 128;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              ww[j] = mx_w_exp_fold(*reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4));
+              ww[j] = *reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4);
               xw[j] = es[32 * j + lane];
             }
           }
@@ -1265,8 +1273,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           if constexpr (A8) {
             // 32-K sub-block `sub` (one per warp, G = 1): e4m3 codes and both scale groups
             dev::tmem_st8(a_lane + slot * 64 + sub * 8, o8);
-            st_mx_scales(a_lane + slot * 64 + 32 + sub * 8, ww, sub);
-            st_mx_scales(a_lane + slot * 64 + 32 + sub * 8 + 4, xw, sub);
+            st_mx_scales<true>(a_lane + slot * 64 + 32 + sub * 8, ww, sub);
+            st_mx_scales<false>(a_lane + slot * 64 + 32 + sub * 8 + 4, xw, sub);
           } else {
 #pragma unroll
             for (int i = 0; i < G; ++i) dev::tmem_st16(a_lane + slot * 64 + (sub * G + i) * 16, o[i]);
