@@ -337,7 +337,7 @@ __device__ __forceinline__ void dq_mxfp4_e4m3(const uint4 q, uint32_t (&o)[8]) {
 // [4:2] (sign at bit 7) is the e4m3 number of value x * 2^-6, exactly — e2m1's
 // exponent bias is 6 below e4m3's, and e2m1's subnormal 0.5 lands on e4m3's
 // subnormal grid.  The 2^6 goes into the sub-block's UE8M0 weight exponent
-// (st_mx_scales with fold).
+// (mx_fold, mx_fold_words).
 __device__ __forceinline__ void dq_mxfp4_e4m3_s6(const uint4 q, uint32_t (&o)[8]) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -355,21 +355,36 @@ __device__ __forceinline__ void dq_mxfp4_e4m3_s6(const uint4 q, uint32_t (&o)[8]
 // the exact table instead.
 __device__ __forceinline__ uint32_t mx_fold(uint32_t e) { return e <= 248u ? e + 6u : e; }
 
-// W4A8 scale factors of one K-block, in the TMEM layout the block-scaled MMA
-// reads: for lane l of every lane quarter, column j of a 4-column group holds
-// the UE8M0 exponent of row (or token) 32j + l, the same byte in all four byte
-// positions.  words: the exponents of the four 32-K sub-blocks of the
-// K-block in bytes 0..3; sub selects one; FOLD applies mx_fold (weights).
-template <bool FOLD>
-__device__ __forceinline__ void st_mx_scales(uint32_t taddr, const uint32_t (&words)[4], int sub) {
-  uint32_t v[4];
+// W4A8 scale factors in the TMEM layout the block-scaled MMA reads
+// (scale_vec::1X): for lane l of every lane quarter, column j of a group holds
+// the word of row (or token) 32j + l whose byte s is the UE8M0 exponent of
+// 32-K sub-block s; the MMA of sub-block s selects byte s by its scale-factor
+// ids.  A group of 4 columns covers 128 rows.
+//
+// mx_fold_words: the weight words with mx_fold applied to every byte; the
+// common case (no byte of the warp's words reaches 248) is one add per word.
+__device__ __forceinline__ void mx_fold_words(uint32_t (&w)[4]) {
+  uint32_t hi = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t e = (words[j] >> (8 * sub)) & 0xFFu;
-    if constexpr (FOLD) e = mx_fold(e);
-    v[j] = e * 0x01010101u;
+  for (int j = 0; j < 4; ++j) hi |= w[j] & (w[j] << 1) & (w[j] << 2) & (w[j] << 3) & (w[j] << 4);
+  if (!__any_sync(0xffffffffu, (hi & 0x80808080u) != 0u)) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] += 0x06060606u;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t o = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) o |= mx_fold((w[j] >> (8 * b)) & 0xFFu) << (8 * b);
+      w[j] = o;
+    }
   }
-  dev::tmem_st4(taddr, v[0], v[1], v[2], v[3]);
+}
+
+// The MX instruction descriptor of sub-block s: scale-factor ids for B
+// (bits 4-5) and A (bits 29-30).
+__device__ __forceinline__ uint32_t mx_idesc_sub(uint32_t idesc, int s) {
+  return idesc | (static_cast<uint32_t>(s) << 4) | (static_cast<uint32_t>(s) << 29);
 }
 
 // All lanes wait; the outcome is made warp-uniform so that the .sync.aligned
@@ -544,7 +559,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // W4A8: the activation exponent words of each weight stage, [stage][K-block
   // of the stage][token], copied in by the weight producer
   uint32_t* e_st = reinterpret_cast<uint32_t*>(w_st + SW * w_stage);
-  constexpr uint32_t kEStage = A8 ? KPS * 128u : 0u;  // words per stage
+  constexpr uint32_t kETok = BNMAX > 128 ? BNMAX : 128;  // token words per K-block
+  constexpr uint32_t kEStage = A8 ? KPS * kETok : 0u;    // words per stage
   uint64_t* w_full = reinterpret_cast<uint64_t*>(e_st + SW * kEStage);
   uint64_t* w_empty = w_full + SW;
   uint64_t* x_full = w_empty + SW;
@@ -702,11 +718,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           for (int i = 0; i < KPS; ++i) {
             if (i < cnt) {
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
+              for (int j = 0; j < static_cast<int>(kETok / 32); ++j) {
                 const int tok = 32 * j + static_cast<int>(lane);
                 const bool in = tok < u.rows;
                 const uint8_t* src = p.x_mx + (in ? static_cast<int64_t>(u.xrow0 + tok) * p.ld_mx + (kb + i) * 4 : 0);
-                dev::cp_async4(es + i * 128 + tok, src, in ? 4u : 0u);
+                dev::cp_async4(es + i * kETok + tok, src, in ? 4u : 0u);
               }
             }
           }
@@ -837,14 +853,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               dev::tc_fence_after();
               if constexpr (A8) {
                 // half h = 32-K sub-blocks 2h, 2h + 1: A at t*64 + h*16 + 8i,
-                // their scale factors at t*64 + 32 + h*16 + 8i (A) and + 4 (B)
+                // the half's scale factors at t*64 + 32 + h*16 (A) and + 4 (B)
                 const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(t * 64 + h * 16);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                   const uint64_t bdesc = dev::sw128_desc(xs + (2 * h + i) * 32);
-                  const uint32_t sfa = a_tmem + 32u + static_cast<uint32_t>(i * 8);
-                  dev::mma_mx_ts(d_tmem, a_tmem + i * 8, bdesc, idesc, sfa, sfa + 4u,
-                                 (fresh && h == 0 && i == 0) ? 0u : 1u);
+                  dev::mma_mx_ts(d_tmem, a_tmem + i * 8, bdesc, mx_idesc_sub(idesc, 2 * h + i), a_tmem + 32u,
+                                 a_tmem + 36u, (fresh && h == 0 && i == 0) ? 0u : 1u);
                 }
               } else {
                 const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(t * 64 + h * 32);
@@ -877,12 +892,12 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
                                             : tmem + kAccCol0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = promote || first;
             if constexpr (A8) {
-              // 32-K sub-block c: A at slot*64 + 8c, scale factors at slot*64 + 32 + 8c (A), + 4 (B)
+              // 32-K sub-block c: A at slot*64 + 8c, scale factors at slot*64 + 32 (A) and + 36 (B)
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 const uint64_t bdesc = dev::sw128_desc(xs + c * 32);
-                const uint32_t sfa = a_tmem + 32u + static_cast<uint32_t>(c * 8);
-                dev::mma_mx_ts(d_tmem, a_tmem + c * 8, bdesc, idesc, sfa, sfa + 4u, (fresh && c == 0) ? 0u : 1u);
+                dev::mma_mx_ts(d_tmem, a_tmem + c * 8, bdesc, mx_idesc_sub(idesc, c), a_tmem + 32u, a_tmem + 36u,
+                               (fresh && c == 0) ? 0u : 1u);
               }
             } else {
 #pragma unroll
@@ -1037,12 +1052,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               // stored) and tokens 32j + lane (staged beside the tile by the
               // weight producer)
               uint32_t ww[4], xw[4];
-              const uint32_t* es = e_st + rg.s * kEStage + pos * 128;
+              const uint32_t* es = e_st + rg.s * kEStage + pos * kETok;
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 ww[j] = *reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4);
                 xw[j] = es[32 * j + lane];
               }
+              mx_fold_words(ww);
               // this lane's row: sub-blocks whose exponent cannot take the fold
               // are converted exactly (rare: a block scale above 2^121); the
               // warp checks for bytes of 248 and up (top five bits set) first
@@ -1066,11 +1082,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
                   o16[8 + i] = o8[1][i];
                 }
                 dev::tmem_st16(a_lane + h * 16, o16);
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                  st_mx_scales<true>(a_lane + 32 + h * 16 + i * 8, ww, 2 * h + i);
-                  st_mx_scales<false>(a_lane + 32 + h * 16 + i * 8 + 4, xw, 2 * h + i);
-                }
+                // each half slot carries its own copy of the scale factors
+                // (A: 4 columns, B: 4 columns for up to 128 tokens)
+                dev::tmem_st4(a_lane + 32 + h * 16, ww[0], ww[1], ww[2], ww[3]);
+                dev::tmem_st4(a_lane + 32 + h * 16 + 4, xw[0], xw[1], xw[2], xw[3]);
               };
               conv8(0);
               if (!warp_wait(&a_empty[2 * t], aph, abort_flag)) {
@@ -1171,18 +1186,23 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         uint4 qc[G];
         uint2 qh[G];
         uint32_t zz[G], ss[G];
-        [[maybe_unused]] uint32_t ww[4], xw[4];  // W4A8: weight / token scale exponents of the K-block
+        [[maybe_unused]] uint32_t ww[4], xw[4];  // W4A8: weight / token scale exponent words of the K-block
         if (real) {
           const uint8_t* wsm = w_st + rg.s * w_stage + gi * tile_bytes;
           if constexpr (A8) {
-            // weight exponents (the conversion's 2^6 is folded in when they
-            // are stored); token exponents staged beside the tile by the
-            // weight producer
-            const uint32_t* es = e_st + rg.s * kEStage + gi * 128;
+            // the scale factors of the K-block are stored by three of the four
+            // warps of each lane quarter: sub 0 the weight words (with the
+            // conversion's 2^6 folded in), sub 1 and 2 the token words of
+            // tokens 0..127 and 128..255 (staged beside the tile by the
+            // weight producer)
+            const uint32_t* es = e_st + rg.s * kEStage + gi * kETok;
+            if (sub == 0) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              ww[j] = *reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4);
-              xw[j] = es[32 * j + lane];
+              for (int j = 0; j < 4; ++j) ww[j] = *reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4);
+              mx_fold_words(ww);
+            } else if (sub == 1 || (sub == 2 && kETok > 128)) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) xw[j] = es[32 * (j + 4 * (sub - 1)) + lane];
             }
           }
 #pragma unroll
@@ -1271,10 +1291,12 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           if (trace_me) HQ_TRACE(5 + gi, tr, (6ull << 24) | ts);
           dev::tc_fence_after();
           if constexpr (A8) {
-            // 32-K sub-block `sub` (one per warp, G = 1): e4m3 codes and both scale groups
+            // 32-K sub-block `sub` (one per warp, G = 1): e4m3 codes; scale
+            // factors A at slot*64 + 32 (4 columns), B at slot*64 + 36 (4 or 8)
             dev::tmem_st8(a_lane + slot * 64 + sub * 8, o8);
-            st_mx_scales<true>(a_lane + slot * 64 + 32 + sub * 8, ww, sub);
-            st_mx_scales<false>(a_lane + slot * 64 + 32 + sub * 8 + 4, xw, sub);
+            if (sub == 0) dev::tmem_st4(a_lane + slot * 64 + 32, ww[0], ww[1], ww[2], ww[3]);
+            else if (sub == 1) dev::tmem_st4(a_lane + slot * 64 + 36, xw[0], xw[1], xw[2], xw[3]);
+            else if (sub == 2 && kETok > 128) dev::tmem_st4(a_lane + slot * 64 + 40, xw[0], xw[1], xw[2], xw[3]);
           } else {
 #pragma unroll
             for (int i = 0; i < G; ++i) dev::tmem_st16(a_lane + slot * 64 + (sub * G + i) * 16, o[i]);
@@ -1748,7 +1770,8 @@ template <int CLS>
 inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts, bool a8) {
   using C = Cls<CLS>;
   const uint32_t w = static_cast<uint32_t>(w_stages) * ((C::kKps * tile_bytes + 1023u) & ~1023u) +
-                     (a8 ? static_cast<uint32_t>(w_stages) * C::kKps * 512u : 0u);  // W4A8 exponent words
+                     (a8 ? static_cast<uint32_t>(w_stages) * C::kKps * 4u * (C::kBnMax > 128 ? C::kBnMax : 128)
+                         : 0u);  // W4A8 token exponent words
   const uint32_t x = static_cast<uint32_t>(x_stages) * (a8 ? 1u : 2u) * C::kKps * static_cast<uint32_t>(bn) * 128u;
   const uint32_t bars =
       (2u * w_stages + 2u * x_stages + 2u * (C::kKps == 2 ? kABars : kASlots) + 2u * C::kDacc + 1u + 2u * kKRing +

@@ -510,9 +510,6 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
   p.bn = inv ? kInvariantBn : m <= 64 ? std::max(16, cdiv(m, 16) * 16) : (m <= 128 ? 128 : (m <= 192 ? 192 : 256));
   const int forced_bn = env_int("HQ_FORCE_BN", 0);
   if (!inv && forced_bn >= 16 && forced_bn % 16 == 0 && forced_bn <= 256) p.bn = forced_bn;
-  // W4A8: tiles of at most 128 tokens (the scale factors of one MMA's tokens
-  // fill one group of TMEM columns)
-  if (a8) p.bn = std::min(p.bn, 128);
   p.cls = wna16_class(p.bn);
   p.m_tiles = cdiv(m, p.bn);
   p.tiles = p.m_tiles * L.n_tiles;
@@ -577,7 +574,7 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   // W4A8: x holds MXFP8 codes [x_rows][ldx bytes] and x_mx their UE8M0
   // exponents [x_rows][ld_mx]
   const bool a8 = x_mx != nullptr;
-  if (a8 && (bn > 128 || L.wtype != HQ_W_MXFP4 || L.k % kTileK != 0 || ld_mx % 4 != 0 || out == kMoeOutGated))
+  if (a8 && (L.wtype != HQ_W_MXFP4 || L.k % kTileK != 0 || ld_mx % 4 != 0 || out == kMoeOutGated))
     return HQ_ERR_UNSUPPORTED;
   const int cls = wna16_class(bn);
   GemmParams p{};

@@ -1,7 +1,7 @@
 // wna16_w4a8.cu — instantiations and launcher of the WnA16 kernel for
 // W4A8-MXFP4: MXFP4 weights against MXFP8 activations, block-scaled MMA
-// (dense and MoE grouped, tiles of at most 128 tokens; own translation unit
-// so the formats compile in parallel).
+// (dense and MoE grouped, every tile class; own translation unit so the
+// formats compile in parallel).
 #include "gemm_wna16.cuh"
 #include "hq_launch.h"
 
@@ -27,6 +27,7 @@ cudaError_t launch_wna16_w4a8(const Wna16Launch& l, const GemmParams& p, const W
     case 0: return l.moe ? run<0, true>(l, p, maps, stream) : run<0, false>(l, p, maps, stream);
     case 1: return l.moe ? run<1, true>(l, p, maps, stream) : run<1, false>(l, p, maps, stream);
     case 2: return l.moe ? run<2, true>(l, p, maps, stream) : run<2, false>(l, p, maps, stream);
+    case 3: return l.moe ? run<3, true>(l, p, maps, stream) : run<3, false>(l, p, maps, stream);
     default: return cudaErrorInvalidValue;
   }
 }

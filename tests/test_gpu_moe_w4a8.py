@@ -53,10 +53,10 @@ def test_small_parity_and_routing(idx):
     check(y, _ref(qw, acts, r), f"w4a8 moe {SMALL[idx]}")
 
 
-@pytest.mark.parametrize("bn", [16, 32, 64, 128])
+@pytest.mark.parametrize("bn", [16, 32, 64, 128, 256])
 def test_every_tile_width(bn):
-    """Tiles of 16 / 32 / 64 / 128 routed rows (forced), a hot expert with
-    many m-tiles and empty experts."""
+    """Tiles of 16 / 32 / 64 / 128 / 256 routed rows (forced), a hot expert
+    with many m-tiles and empty experts."""
     from gpu_helpers import tuning
     qw, acts, r = synth.moe_mxfp4(9, 300, num_experts=8, n=256, k=512, topk=2)
     r.topk_ids[:, 0] = 3

@@ -107,6 +107,19 @@ def test_w4a8_large_weight_exponents(m):
         check(y[i:i + 1], r[i:i + 1], f"w4a8 large weight exponents row {i}")
 
 
+@pytest.mark.parametrize("bn", [16, 32, 48, 64, 128, 192, 256])
+def test_w4a8_every_tile_width(bn):
+    """Tiles of every width the planner can choose (forced), ragged M and N:
+    the scale factors of up to 256 tokens beside the A operand."""
+    from gpu_helpers import DevWeight, tuning
+    m, n, k = 300, 384, 1024
+    qw = _weight(85, n, k)
+    x = synth.make_activations(np.random.default_rng(85), m, k, "bf16").data
+    with tuning(HQ_FORCE_BN=bn):
+        y = _w4a8(DevWeight(qw), x, k)
+    check(y, _ref(qw, x), f"w4a8 bn={bn}")
+
+
 @pytest.mark.parametrize("splitk", ["cluster", "stream_k", "whole"])
 def test_w4a8_work_splits(splitk):
     """N = 8192 gives 64 weight tiles: the 2-CTA cluster split (the planner's

@@ -155,11 +155,12 @@ def test_moe_plan_query_validation(hq):
 
 
 def test_w4a8_plans(hq):
-    """W4A8-MXFP4 plans tiles of at most 128 tokens (the scale factors of one
-    MMA's tokens fill one TMEM column group), with the usual work splits."""
+    """W4A8-MXFP4 plans the same tile widths and work splits as W4A16 (256
+    tokens at large M: the scale factors of a tile's tokens take 8 TMEM
+    columns beside the A operand)."""
     d = hq.make_desc("mxfp4", "ue8m0", 8192, 8192, group_k=32)
     for m, bn, cls, split in ((1, 16, 0, CLUSTER), (16, 16, 0, CLUSTER), (48, 48, 1, CLUSTER),
-                              (128, 128, 2, CLUSTER), (1024, 128, 2, WHOLE), (4096, 128, 2, WHOLE)):
+                              (128, 128, 2, CLUSTER), (1024, 256, 3, WHOLE), (4096, 256, 3, WHOLE)):
         p = hq.hq_plan_query(d, m, "mxfp8", SMS, OPTIN)
         assert (p["bn"], p["tile_class"], p["splits"]) == (bn, cls, split), (m, p)
         if cls <= 1:
