@@ -64,9 +64,10 @@ namespace wna16 {
 // Tile-width classes: maximum tokens per tile, K-blocks per stage (= MMA
 // issuers), accumulator buffers.  With one K-block per stage the 16
 // dequantiser warps share a ring of four A slots of 64 TMEM columns; with two
-// they form four streams of four warps, each owning one slot used as two half
-// slots of 32 columns.  TMEM: A slots in columns [0, 256), accumulators
-// (kDacc x kIss x kBnMax columns, or the promotion ring) in [256, 512).
+// they form four streams of four warps, each owning a ring of half slots of
+// 32 TMEM columns (one K-block = two half slots).  TMEM: A slots in columns
+// [0, acc_col0), accumulators (kDacc x kIss x kBnMax columns, or the promotion
+// ring) from acc_col0 on.
 template <int CLS>
 struct Cls;
 template <>
@@ -81,16 +82,27 @@ struct Cls<3> { static constexpr int kBnMax = 256, kKps = 1, kIss = 1, kDacc = 1
 constexpr int kEpiWarps = 4;
 constexpr int kDqWarps = 16;
 constexpr int kASlots = 4;
-constexpr int kABars = 8;  // A-slot barriers: kASlots slots, or 4 streams x 2 half slots
 constexpr int kDqWarp0 = kEpiWarps;                        // first dequant warp
 constexpr int kProdWarp = kDqWarp0 + kDqWarps;             // weight producer warp
 constexpr int kXProdWarp = kProdWarp + 1;                  // activation producer warp
 constexpr int kIssWarp0 = kXProdWarp + 1;                  // first MMA issuer warp
 constexpr int kKRing = 8;  // promotion: per-K-block accumulators over all issuers (class 0)
-constexpr int kSRing = 8;  // promotion: per-K-block row scales per group, in shared memory
 constexpr uint32_t kACol0 = 0;
-constexpr uint32_t kAccCol0 = 256;
 constexpr uint32_t kTmemCols = 512;
+
+// Streams: half slots per stream, a ring that K-block c of a stream fills at
+// positions 2c and 2c + 1.  A ring of three for the 16-token class (its
+// accumulators fit in the last 128 columns), which lets a stream's first half
+// reuse the slot of K-block c - 2 instead of waiting for the MMA of K-block
+// c - 1, measured no faster at M = 16 (18.2 against 17.8 us), so every class
+// keeps two.
+template <int CLS>
+constexpr int half_ring() { return 2; }
+template <int CLS>
+constexpr uint32_t acc_col0() { return static_cast<uint32_t>(4 * 64); }
+// A-slot barriers of each kind: four slots, or four streams' half slots
+template <int CLS>
+constexpr int a_bars() { return Cls<CLS>::kKps == 2 ? 4 * half_ring<CLS>() : kASlots; }
 
 template <int CLS>
 constexpr int threads() { return 32 * (kIssWarp0 + Cls<CLS>::kIss); }
@@ -566,21 +578,21 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   uint64_t* x_full = w_empty + SW;
   uint64_t* x_empty = x_full + SX;
   uint64_t* a_full = x_empty + SX;
-  constexpr int NAB = kStream ? kABars : kASlots;  // A-slot barriers of each kind
+  constexpr int NAB = a_bars<CLS>();  // A-slot barriers of each kind
+  constexpr int HR = half_ring<CLS>();  // streams: half slots per stream
+  constexpr uint32_t ACC0 = acc_col0<CLS>();
   uint64_t* a_empty = a_full + NAB;
   uint64_t* acc_full = a_empty + NAB;
   uint64_t* acc_empty = acc_full + DACC;
   uint64_t* tear = acc_empty + DACC;
   uint64_t* k_full = tear + 1;          // promotion: [ISS][KR]
   uint64_t* k_empty = k_full + kKRing;  // promotion: [ISS][KR]
-  uint64_t* s_full = k_empty + kKRing;  // promotion: [G][kSRing]
-  uint64_t* red_full = s_full + 2 * kSRing;  // cluster split: the peer's half arrived
+  uint64_t* red_full = k_empty + kKRing;  // cluster split: the peer's half arrived
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // promotion: [G][kSRing][128], 16-byte aligned
-  float* s_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16 +
-                                            ((16u - (dev::smem_u32(tmem_slot) & 15u)) & 15u));
-  float* s_red = s_scale + (CLS == 0 ? 2 * kSRing * kTileN : 0);  // cluster split: [128][16] fp32 (16-byte aligned)
+  // cluster split, class 0: rank 1's sums [128][16] fp32, 16-byte aligned
+  float* s_red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16 +
+                                          ((16u - (dev::smem_u32(tmem_slot) & 15u)) & 15u));
   // MoE: m-tile prefix [E+1], row prefix [E+1], X row base per expert [E]
   int* s_tabs = reinterpret_cast<int*>(s_red + (CLS == 0 ? kTileN * 16 : 0));
   int* s_tabs_end = s_tabs + (MOE ? 3 * p.num_experts + 2 : 0);
@@ -625,7 +637,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       dev::mbar_init(&k_full[k], 1);
       dev::mbar_init(&k_empty[k], kEpiWarps);
     }
-    for (int k = 0; k < 2 * kSRing; ++k) dev::mbar_init(&s_full[k], 4);
     dev::mbar_init(red_full, kEpiWarps);
     *abort_flag = 0;
     dev::fence_barrier_init();
@@ -834,42 +845,45 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           const int q = pidx;
           if (kStream && q < cnt) {
             const int t = 2 * static_cast<int>(S & 1u) + q;
-            const uint32_t aph = ((S & 1u) ? cs1 : cs0) & 1u;
+            const uint32_t cst = (S & 1u) ? cs1 : cs0;  // K-blocks taken from stream t so far
             const int ks = pidx * KR + static_cast<int>(ck % KR);
             if (promote && !dev::mbar_wait(&k_empty[ks], ((ck / KR) & 1u) ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * q * slab;
-            const uint32_t d_tmem = promote ? tmem + kAccCol0 + static_cast<uint32_t>(ks * BNMAX)
-                                            : tmem + kAccCol0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
+            const uint32_t d_tmem = promote ? tmem + ACC0 + static_cast<uint32_t>(ks * BNMAX)
+                                            : tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = promote || first;
             for (int h = 0; h < 2 && ok; ++h) {
-              if (!dev::mbar_wait(&a_full[2 * t + h], aph, abort_flag)) {
+              // half h of the stream's K-block cst is its half slot 2 cst + h of the ring
+              const uint32_t hn = 2u * cst + static_cast<uint32_t>(h);
+              const int hs = t * HR + static_cast<int>(hn % HR);
+              if (!dev::mbar_wait(&a_full[hs], (hn / HR) & 1u, abort_flag)) {
                 ok = false;
                 break;
               }
               HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
               dev::tc_fence_after();
               if constexpr (A8) {
-                // half h = 32-K sub-blocks 2h, 2h + 1: A at t*64 + h*16 + 8i,
-                // the half's scale factors at t*64 + 32 + h*16 (A) and + 4 (B)
-                const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(t * 64 + h * 16);
+                // half h = 32-K sub-blocks 2h, 2h + 1: A at the half slot's
+                // columns 8i, its scale factors at + 16 (A) and + 20 (B)
+                const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                   const uint64_t bdesc = dev::sw128_desc(xs + (2 * h + i) * 32);
-                  dev::mma_mx_ts(d_tmem, a_tmem + i * 8, bdesc, mx_idesc_sub(idesc, 2 * h + i), a_tmem + 32u,
-                                 a_tmem + 36u, (fresh && h == 0 && i == 0) ? 0u : 1u);
+                  dev::mma_mx_ts(d_tmem, a_tmem + i * 8, bdesc, mx_idesc_sub(idesc, 2 * h + i), a_tmem + 16u,
+                                 a_tmem + 20u, (fresh && h == 0 && i == 0) ? 0u : 1u);
                 }
               } else {
-                const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(t * 64 + h * 32);
+                const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                   const uint64_t bdesc = dev::sw128_desc(xs + h * slab + kk * 32);
                   dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && h == 0 && kk == 0) ? 0u : 1u);
                 }
               }
-              dev::tc_commit(&a_empty[2 * t + h]);
+              dev::tc_commit(&a_empty[hs]);
             }
             if (!ok) break;
             if (promote) dev::tc_commit(&k_full[ks]);
@@ -888,8 +902,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             dev::tc_fence_after();
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * pidx * slab;
             const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(slot) * 64u;
-            const uint32_t d_tmem = promote ? tmem + kAccCol0 + static_cast<uint32_t>(ks * BNMAX)
-                                            : tmem + kAccCol0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
+            const uint32_t d_tmem = promote ? tmem + ACC0 + static_cast<uint32_t>(ks * BNMAX)
+                                            : tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = promote || first;
             if constexpr (A8) {
               // 32-K sub-block c: A at slot*64 + 8c, scale factors at slot*64 + 32 (A) and + 36 (B)
@@ -933,7 +947,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     const int pos = t & 1;                  // K-block of those stages it converts
     const int quarter = warp & 3;
     const int r = quarter * 32 + static_cast<int>(lane);  // weight row within the tile (TMEM lane)
-    const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol0 + static_cast<uint32_t>(t * 64);
+    // this lane's row in the stream's ring of half slots (32 columns each)
+    const uint32_t a_lane =
+        tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol0 + static_cast<uint32_t>(t * HR * 32);
     const bool promote = CLS == 0 && p.promote;
     // the weight-tile layout fields this role reads per K-block, in registers
     const uint32_t q_scale_off = p.scale_off, q_zero_off = p.zero_off, q_hi_off = p.hi_off;
@@ -1027,25 +1043,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           if (trace_me) HQ_TRACE(5 + t, tr, (5ull << 24) | ts);
           if (pos < cnt) {
             const uint8_t* wsm = w_st + rg.s * w_stage + pos * tile_bytes;
-            // promotion: the row's group scale goes to the epilogue through a
-            // ring.  Before this write the stream has seen the MMAs of its
-            // K-block before last complete; each of them waited until the
-            // epilogue released the accumulator KR uses back, and the epilogue
-            // reads a scale before releasing its accumulator, so every scale
-            // kSRing positions back has been read.
-            if (promote) {
-              constexpr float kOpFixD = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
-              const uint32_t s16 = reinterpret_cast<const uint16_t*>(wsm + q_scale_off)[r * q_g_kb];
-              const float sf = BF16 ? __uint_as_float(s16 << 16)
-                                    : __half2float(__ushort_as_half(static_cast<unsigned short>(s16)));
-              const int si = pos * kSRing + static_cast<int>(cpos % kSRing);
-              s_scale[si * kTileN + r] = sf * kOpFixD;
-              __syncwarp();
-              if (lane == 0) dev::mbar_arrive(&s_full[si]);
-            }
             // The first half is published after the second is converted (the
             // arithmetic covers its TMEM stores); the second right away.
-            const uint32_t aph = (ca & 1u) ^ 1u;
+            // the K-block's two half slots in the stream's ring, and the
+            // phase parity of the MMA release each waits for
+            const uint32_t hn0 = 2u * ca, hn1 = hn0 + 1u;
+            const int j0 = static_cast<int>(hn0 % HR), j1 = static_cast<int>(hn1 % HR);
+            const uint32_t eph0 = ((hn0 / HR) & 1u) ^ 1u, eph1 = ((hn1 / HR) & 1u) ^ 1u;
             if constexpr (A8) {
               // scale exponents of this K-block: weight rows 32j + lane (from
               // the tile; the conversion's 2^6 is folded in when they are
@@ -1074,37 +1078,38 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
                   if (any_big && ((own >> (8 * (c0 + i))) & 0xFFu) > 248u) dq_mxfp4_e4m3(q, o8[i]);
                 }
               };
-              auto st_half = [&](int h) {
+              // half slot j: e4m3 codes of two sub-blocks in columns
+              // [0, 16), its own copy of the scale factors at 16 (A, 4
+              // columns) and 20 (B, 4 columns for up to 128 tokens)
+              auto st_half = [&](int j) {
                 uint32_t o16[16];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   o16[i] = o8[0][i];
                   o16[8 + i] = o8[1][i];
                 }
-                dev::tmem_st16(a_lane + h * 16, o16);
-                // each half slot carries its own copy of the scale factors
-                // (A: 4 columns, B: 4 columns for up to 128 tokens)
-                dev::tmem_st4(a_lane + 32 + h * 16, ww[0], ww[1], ww[2], ww[3]);
-                dev::tmem_st4(a_lane + 32 + h * 16 + 4, xw[0], xw[1], xw[2], xw[3]);
+                dev::tmem_st16(a_lane + j * 32, o16);
+                dev::tmem_st4(a_lane + j * 32 + 16, ww[0], ww[1], ww[2], ww[3]);
+                dev::tmem_st4(a_lane + j * 32 + 20, xw[0], xw[1], xw[2], xw[3]);
               };
               conv8(0);
-              if (!warp_wait(&a_empty[2 * t], aph, abort_flag)) {
+              if (!warp_wait(&a_empty[t * HR + j0], eph0, abort_flag)) {
                 ok = false;
                 break;
               }
               dev::tc_fence_after();
-              st_half(0);
+              st_half(j0);
               conv8(2);
               __syncwarp();
               if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
-              publish(2 * t);
-              if (!warp_wait(&a_empty[2 * t + 1], aph, abort_flag)) {
+              publish(t * HR + j0);
+              if (!warp_wait(&a_empty[t * HR + j1], eph1, abort_flag)) {
                 ok = false;
                 break;
               }
               dev::tc_fence_after();
-              st_half(1);
-              publish(2 * t + 1);
+              st_half(j1);
+              publish(t * HR + j1);
               ++ca;
               if (pos < cnt) ++cpos;
               ++ts;
@@ -1115,28 +1120,28 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             gk_valid = false;
             convert2(wsm, 0, o);
             if (trace_me) HQ_TRACE(5 + t, tr, (12ull << 24) | ts);
-            if (!warp_wait(&a_empty[2 * t], aph, abort_flag)) {
+            if (!warp_wait(&a_empty[t * HR + j0], eph0, abort_flag)) {
               ok = false;
               break;
             }
             if (trace_me) HQ_TRACE(5 + t, tr, (6ull << 24) | ts);
             dev::tc_fence_after();
-            dev::tmem_st16(a_lane + 0, o[0]);
-            dev::tmem_st16(a_lane + 16, o[1]);
+            dev::tmem_st16(a_lane + j0 * 32, o[0]);
+            dev::tmem_st16(a_lane + j0 * 32 + 16, o[1]);
             convert2(wsm, 2, o);
             // every lane's codes are consumed: the stage may be refilled
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
-            publish(2 * t);
+            publish(t * HR + j0);
             if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
-            if (!warp_wait(&a_empty[2 * t + 1], aph, abort_flag)) {
+            if (!warp_wait(&a_empty[t * HR + j1], eph1, abort_flag)) {
               ok = false;
               break;
             }
             dev::tc_fence_after();
-            dev::tmem_st16(a_lane + 32, o[0]);
-            dev::tmem_st16(a_lane + 48, o[1]);
-            publish(2 * t + 1);
+            dev::tmem_st16(a_lane + j1 * 32, o[0]);
+            dev::tmem_st16(a_lane + j1 * 32 + 16, o[1]);
+            publish(t * HR + j1);
             if (trace_me) HQ_TRACE(5 + t, tr, (7ull << 24) | ts);
             ++ca;
           } else {
@@ -1227,18 +1232,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               }
             }
           }
-        }
-        // promotion: the row's group scale goes to the epilogue through a ring
-        // (one phase per kSRing K-blocks; the epilogue trails by at most
-        // kASlots/G + kKRing K-blocks, fewer than kSRing)
-        if (promote && real && sub == 0) {
-          constexpr float kOpFixD = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
-          const uint32_t s16 = ss[0];
-          const float sf = BF16 ? __uint_as_float(s16 << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(s16)));
-          const int si = gi * kSRing + static_cast<int>(ca % kSRing);
-          s_scale[si * kTileN + r] = sf * kOpFixD;
-          __syncwarp();
-          if (lane == 0) dev::mbar_arrive(&s_full[si]);
         }
         // convert first: the arithmetic covers the previous K-block's TMEM
         // stores still in flight and the MMA that frees this K-block's slot
@@ -1493,7 +1486,17 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         if (p.promote) {
           promoted = true;
           // sum the unit's per-K-block accumulators in K order, each times its
-          // group scale (read-only, loaded one K-block ahead)
+          // row's group scale, read from the transformed weight in global
+          // memory (read-only during the call; the tile's copy into shared
+          // memory has just brought it into L2), two K-blocks ahead
+          constexpr float kOpFixD = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
+          const uint8_t* srow = p.tiles + static_cast<uint64_t>(u.e) * p.expert_stride +
+                                static_cast<uint64_t>(u.nt) * p.k_tiles * tile_bytes + p.scale_off + 2u * r;
+          auto scale_of = [&](int kb) -> uint32_t {
+            return kb < u.kb1 ? __ldg(reinterpret_cast<const uint16_t*>(srow + static_cast<uint64_t>(kb) * tile_bytes))
+                              : 0u;
+          };
+          uint32_t sq0 = scale_of(u.kb0), sq1 = scale_of(u.kb0 + 1);
           float tot[BNMAX];
 #pragma unroll
           for (int i = 0; i < BNMAX; ++i) tot[i] = 0.f;
@@ -1501,16 +1504,18 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             const int q = (kb - u.kb0) & (KPS - 1);
             const uint32_t cq = q ? ck1 : ck0;
             const int ks = q * KR + static_cast<int>(cq % KR);
-            const int si = q * kSRing + static_cast<int>(cq % kSRing);
-            if (!warp_wait(&s_full[si], (cq / kSRing) & 1u, abort_flag) ||
-                !warp_wait(&k_full[ks], (cq / KR) & 1u, abort_flag)) {
+            const uint32_t s16 = sq0;
+            sq0 = sq1;
+            sq1 = scale_of(kb + 2);
+            if (!warp_wait(&k_full[ks], (cq / KR) & 1u, abort_flag)) {
               ok = false;
               break;
             }
             if (trace_me) HQ_TRACE(9, tr, (14ull << 24) | kb);
-            const float s_cur = s_scale[si * kTileN + r];
+            const float s_cur = (BF16 ? __uint_as_float(s16 << 16)
+                                      : __half2float(__ushort_as_half(static_cast<unsigned short>(s16)))) * kOpFixD;
             dev::tc_fence_after();
-            const uint32_t acc = tmem + lane_base + kAccCol0 + static_cast<uint32_t>(ks * BNMAX);
+            const uint32_t acc = tmem + lane_base + ACC0 + static_cast<uint32_t>(ks * BNMAX);
 #pragma unroll
             for (int ch = 0; ch < BNMAX / 16; ++ch) {
               if (ch * 16 < bn) {
@@ -1563,7 +1568,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         // accumulators are summed in issuer order
         const uint32_t parts = (1u << min(ISS, u.kb1 - u.kb0)) - 1u;
         const int is0 = __ffs(parts) - 1;
-        const uint32_t acc0 = tmem + lane_base + kAccCol0 + static_cast<uint32_t>(buf * ISS * BNMAX);
+        const uint32_t acc0 = tmem + lane_base + ACC0 + static_cast<uint32_t>(buf * ISS * BNMAX);
         // the issuers' partial accumulators of 16 columns, summed in issuer order
         auto acc16 = [&](int ch, float (&v)[16]) {
           uint32_t a[16];
@@ -1774,9 +1779,9 @@ inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int 
                          : 0u);  // W4A8 token exponent words
   const uint32_t x = static_cast<uint32_t>(x_stages) * (a8 ? 1u : 2u) * C::kKps * static_cast<uint32_t>(bn) * 128u;
   const uint32_t bars =
-      (2u * w_stages + 2u * x_stages + 2u * (C::kKps == 2 ? kABars : kASlots) + 2u * C::kDacc + 1u + 2u * kKRing +
-       2u * kSRing + 1u) * 8u + 16u;
-  const uint32_t scales = CLS == 0 ? 4u * 2u * kSRing * kTileN + 4u * kTileN * 16u : 0u;
+      (2u * w_stages + 2u * x_stages + 2u * a_bars<CLS>() + 2u * C::kDacc + 1u + 2u * kKRing +
+       1u) * 8u + 16u;
+  const uint32_t scales = CLS == 0 ? 4u * kTileN * 16u : 0u;  // cluster split exchange of class 0
   const uint32_t moe = num_experts ? 4u * (3u * num_experts + 2u) : 0u;
   const uint32_t ystage = num_experts == 0 ? kEpiWarps * 2u * 16u * 32u * 2u + 128u : 0u;  // dense Y boxes
   return w + x + bars + scales + moe + ystage + 1024u /* alignment slack */;
