@@ -958,7 +958,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     sc.init(p);
     Ring rg;
     uint32_t ca = 0;    // this stream's K-blocks so far (one use of each half slot per K-block)
-    uint32_t cpos = 0;  // K-blocks at position pos so far, both parities (scale ring index)
     uint32_t S = 0;     // stage counter
     bool ok = true;
     [[maybe_unused]] int tr = 0, ts = 0;
@@ -1111,7 +1110,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               st_half(j1);
               publish(t * HR + j1);
               ++ca;
-              if (pos < cnt) ++cpos;
               ++ts;
               rg.next(SW);
               continue;
@@ -1149,7 +1147,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
           }
         }
-        if (pos < cnt) ++cpos;
         ++ts;
         rg.next(SW);
       }
