@@ -418,12 +418,13 @@ struct Ring {
   }
 };
 
-// L2 policy of the weight copies: a dense problem with one row of tiles reads
-// every weight byte once (evict first, keep the cache for activations); with
-// several, each weight tile is read again by the next row of tiles.
+// L2 policy of the weight copies: a problem with one row of tiles (MoE: one
+// per expert, on average) reads every weight byte once (evict first, keep the
+// cache for activations); with several, each weight tile is read again by
+// the next row of tiles.
 template <bool MOE>
 __device__ __forceinline__ uint64_t weight_policy(const GemmParams& p) {
-  return (!MOE && p.m_tiles > 1) ? dev::policy_evict_normal() : dev::policy_evict_first();
+  return p.m_tiles > 1 ? dev::policy_evict_normal() : dev::policy_evict_first();
 }
 
 // ---------------------------------------------------------------- work units

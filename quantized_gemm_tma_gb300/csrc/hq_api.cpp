@@ -587,7 +587,10 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   p.row_zero = (L.channel && L.has_zeros) ? wt + L.row_zero_off : nullptr;
   p.tensor_scale = L.wtype == HQ_W_NVFP4 ? reinterpret_cast<const float*>(wt + L.ts_off) : nullptr;
   p.n = L.n; p.n_pad = L.n_pad; p.k = L.k; p.k_tiles = L.k_tiles; p.n_tiles = L.n_tiles; p.m = x_rows;
-  p.bn = bn; p.m_tiles = 0; p.num_tiles = 0; p.stream_k = 0; p.iters = 0; p.cluster = 1;
+  // m_tiles: whether an expert's weights are, on average, read by more than one
+  // tile row (their copies are then kept in L2 for the next row)
+  p.bn = bn; p.num_tiles = 0; p.stream_k = 0; p.iters = 0; p.cluster = 1;
+  p.m_tiles = static_cast<int64_t>(x_rows) > static_cast<int64_t>(L.num_experts) * bn ? 2 : 1;
   p.promote = (cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
   p.idesc = a8 ? idesc_mx_e4m3(128, bn) : idesc_f16(true, 128, bn);
   p.x_mx = x_mx;

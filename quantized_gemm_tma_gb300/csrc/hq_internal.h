@@ -122,7 +122,8 @@ struct GemmParams {
   int n, n_pad, k, k_tiles, n_tiles;
   int m;                    // dense: rows of X / Y
   int bn;                   // MMA N (tokens per tile), multiple of 16
-  int m_tiles, num_tiles;   // dense: token tiles, output tiles (m_tiles * n_tiles)
+  int m_tiles, num_tiles;   // dense: token tiles, output tiles (m_tiles * n_tiles); MoE: m_tiles = 2
+                            // when the routed rows average more than a tile per expert, else 1
   int stages, x_stages;     // weight-ring and activation-ring stages
   int groups;               // dequantiser groups (for reporting)
   int stream_k;             // dense: deal K-blocks out in equal ranges (1) or whole tiles (0)
