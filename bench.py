@@ -72,11 +72,12 @@ EXTRA = {
 # the tensor cores (4.5 : 2.25 PFLOP/s dense)
 FP8_PER_BF16 = 2.0
 BLOCK = 25         # back-to-back calls of one shape between two events
-# DRAM bytes (read + write) per launch of the WnA16 INT4 kernel, from the ncu
-# traffic capture listed in profiles/wna16_int4_asym_g128_n8192_k8192.md,
-# keyed by M; valid only while the kernel sources hash to `sha` (else null).
-NCU_TRAFFIC = {"sha": "29395d556d0a38cd", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
-               "bytes": {16: 35_468_544, 128: 37_302_784, 1024: 53_039_360, 4096: 165_367_296}}
+# DRAM bytes (read + write) per launch of the WnA16 INT4 kernel, from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum, third warm-up pass of
+# the dense sweep; the command is kept with the profile summaries), keyed by
+# M; valid only while the kernel sources hash to `sha` (else null).
+NCU_TRAFFIC = {"sha": "c302f5dac023c679", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
+               "bytes": {16: 35_468_544, 128: 37_303_296, 1024: 52_814_080, 4096: 164_220_416}}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
