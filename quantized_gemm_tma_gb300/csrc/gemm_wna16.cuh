@@ -66,8 +66,7 @@ namespace wna16 {
 // dequantiser warps share a ring of four A slots of 64 TMEM columns; with two
 // they form four streams of four warps, each owning a ring of half slots of
 // 32 TMEM columns (one K-block = two half slots).  TMEM: A slots in columns
-// [0, acc_col0), accumulators (kDacc x kIss x kBnMax columns, or the promotion
-// ring) from acc_col0 on.
+// [0, acc_col0), accumulators (kDacc x kIss x kBnMax columns) from acc_col0 on.
 template <int CLS>
 struct Cls;
 template <>
@@ -86,7 +85,6 @@ constexpr int kDqWarp0 = kEpiWarps;                        // first dequant warp
 constexpr int kProdWarp = kDqWarp0 + kDqWarps;             // weight producer warp
 constexpr int kXProdWarp = kProdWarp + 1;                  // activation producer warp
 constexpr int kIssWarp0 = kXProdWarp + 1;                  // first MMA issuer warp
-constexpr int kKRing = 8;  // promotion: per-K-block accumulators over all issuers (class 0)
 constexpr uint32_t kACol0 = 0;
 constexpr uint32_t kTmemCols = 512;
 
@@ -554,7 +552,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   constexpr uint32_t kSlabsKb = A8 ? 1u : 2u;  // activation slabs per K-block
   // With streams, issuer p takes K-block p of every stage, i.e. the K-blocks
   // of streams p and 2 + p alternately.
-  constexpr int KR = kKRing / ISS;  // promotion: accumulator ring per issuer
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from smem_raw by an offset so that the
   // compiler keeps shared-memory addressing for every access through it
@@ -586,9 +583,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   uint64_t* acc_full = a_empty + NAB;
   uint64_t* acc_empty = acc_full + DACC;
   uint64_t* tear = acc_empty + DACC;
-  uint64_t* k_full = tear + 1;          // promotion: [ISS][KR]
-  uint64_t* k_empty = k_full + kKRing;  // promotion: [ISS][KR]
-  uint64_t* red_full = k_empty + kKRing;  // cluster split: the peer's half arrived
+  uint64_t* red_full = tear + 1;  // cluster split: the peer's half arrived
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // cluster split, class 0: rank 1's sums [128][16] fp32, 16-byte aligned
@@ -634,10 +629,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       dev::mbar_init(&acc_empty[b], kEpiWarps);
     }
     dev::mbar_init(tear, ISS);
-    for (int k = 0; k < kKRing; ++k) {
-      dev::mbar_init(&k_full[k], 1);
-      dev::mbar_init(&k_empty[k], kEpiWarps);
-    }
     dev::mbar_init(red_full, kEpiWarps);
     *abort_flag = 0;
     dev::fence_barrier_init();
@@ -813,9 +804,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       Sched<MOE> sc;
       sc.init(p);
       Ring rx;
-      uint32_t cu = 0, ck = 0;
+      uint32_t cu = 0;
       const uint32_t idesc = p.idesc;
-      const bool promote = CLS == 0 && p.promote;
       bool ok = true;
       int ui = 0;
       [[maybe_unused]] int tr = 0, ts = 0;
@@ -823,9 +813,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       [[maybe_unused]] uint32_t S = 0;           // streams: stage counter
       Unit u;
       while (ok && sc.next(p, s_tabs, u)) {
-        // whole-unit accumulator (double-buffered across units) unless promoting
+        // whole-unit accumulator (double-buffered across units where TMEM allows)
         const int buf = DACC == 1 ? 0 : (ui & 1);
-        if (!promote) {
+        {
           const uint32_t accph = static_cast<uint32_t>(DACC == 1 ? ui : (ui >> 1)) & 1u;
           if (!dev::mbar_wait(&acc_empty[buf], accph ^ 1u, abort_flag)) {
             ok = false;
@@ -847,15 +837,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           if (kStream && q < cnt) {
             const int t = 2 * static_cast<int>(S & 1u) + q;
             const uint32_t cst = (S & 1u) ? cs1 : cs0;  // K-blocks taken from stream t so far
-            const int ks = pidx * KR + static_cast<int>(ck % KR);
-            if (promote && !dev::mbar_wait(&k_empty[ks], ((ck / KR) & 1u) ^ 1u, abort_flag)) {
-              ok = false;
-              break;
-            }
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * q * slab;
-            const uint32_t d_tmem = promote ? tmem + ACC0 + static_cast<uint32_t>(ks * BNMAX)
-                                            : tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
-            const bool fresh = promote || first;
+            const uint32_t d_tmem = tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
+            const bool fresh = first;
             for (int h = 0; h < 2 && ok; ++h) {
               // half h of the stream's K-block cst is its half slot 2 cst + h of the ring
               const uint32_t hn = 2u * cst + static_cast<uint32_t>(h);
@@ -887,15 +871,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               dev::tc_commit(&a_empty[hs]);
             }
             if (!ok) break;
-            if (promote) dev::tc_commit(&k_full[ks]);
-            ++ck;
             if (S & 1u) ++cs1; else ++cs0;
             first = false;
           } else if (!kStream && pidx < cnt) {
             const int slot = pidx * DA + static_cast<int>(cu % DA);
-            const int ks = pidx * KR + static_cast<int>(ck % KR);
-            if (!dev::mbar_wait(&a_full[slot], (cu / DA) & 1u, abort_flag) ||
-                (promote && !dev::mbar_wait(&k_empty[ks], ((ck / KR) & 1u) ^ 1u, abort_flag))) {
+            if (!dev::mbar_wait(&a_full[slot], (cu / DA) & 1u, abort_flag)) {
               ok = false;
               break;
             }
@@ -903,9 +883,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             dev::tc_fence_after();
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * pidx * slab;
             const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(slot) * 64u;
-            const uint32_t d_tmem = promote ? tmem + ACC0 + static_cast<uint32_t>(ks * BNMAX)
-                                            : tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
-            const bool fresh = promote || first;
+            const uint32_t d_tmem = tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
+            const bool fresh = first;
             if constexpr (A8) {
               // 32-K sub-block c: A at slot*64 + 8c, scale factors at slot*64 + 32 (A) and + 36 (B)
 #pragma unroll
@@ -922,9 +901,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               }
             }
             dev::tc_commit(&a_empty[slot]);
-            if (promote) dev::tc_commit(&k_full[ks]);
             ++cu;
-            ++ck;
             first = false;
           }
           dev::tc_commit(&x_empty[rx.s]);
@@ -934,7 +911,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           rx.next(SX);
         }
         if (!ok) break;
-        if (!promote) dev::tc_commit(&acc_full[buf]);
+        dev::tc_commit(&acc_full[buf]);
         ++ui;
       }
       if (!ok) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
@@ -951,7 +928,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     // this lane's row in the stream's ring of half slots (32 columns each)
     const uint32_t a_lane =
         tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol0 + static_cast<uint32_t>(t * HR * 32);
-    const bool promote = CLS == 0 && p.promote;
     // the weight-tile layout fields this role reads per K-block, in registers
     const uint32_t q_scale_off = p.scale_off, q_zero_off = p.zero_off, q_hi_off = p.hi_off;
     const int q_g_kb = p.g_kb, q_group_k = p.group_k, q_has_zeros = p.has_zeros, q_channel = p.channel;
@@ -973,20 +949,15 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
         if (!q_channel && q_g_kb == 1) {
           if (!gk_valid) {
-            const uint32_t s16 = promote ? 0u : reinterpret_cast<const uint16_t*>(wsm + q_scale_off)[r];
+            const uint32_t s16 = reinterpret_cast<const uint16_t*>(wsm + q_scale_off)[r];
             const uint32_t z = q_has_zeros ? wsm[q_zero_off + r] : zrow;
-            gk = promote ? int4_consts<BF16, false>(z, 0u) : int4_consts<BF16, true>(z, s16);
+            gk = int4_consts<BF16, true>(z, s16);
             gk_valid = true;
           }
           const uint4 q0 = *reinterpret_cast<const uint4*>(wsm + (c0 * kTileN + r) * 16);
           const uint4 q1 = *reinterpret_cast<const uint4*>(wsm + ((c0 + 1) * kTileN + r) * 16);
-          if (promote) {
-            dq_int4_apply<BF16, false>(q0, gk, o[0]);
-            dq_int4_apply<BF16, false>(q1, gk, o[1]);
-          } else {
-            dq_int4_apply<BF16, true>(q0, gk, o[0]);
-            dq_int4_apply<BF16, true>(q1, gk, o[1]);
-          }
+          dq_int4_apply<BF16, true>(q0, gk, o[0]);
+          dq_int4_apply<BF16, true>(q1, gk, o[1]);
           return;
         }
       }
@@ -1005,12 +976,12 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           if (q_has_zeros) z = wsm[q_zero_off + r * q_g_kb + g];
         }
         if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
-          if (q_channel || promote) dq_int4<BF16, false>(q, z, sc16, o[i]);
+          if (q_channel) dq_int4<BF16, false>(q, z, sc16, o[i]);
           else dq_int4<BF16, true>(q, z, sc16, o[i]);
         } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
           const uint2 qh = *reinterpret_cast<const uint2*>(wsm + q_hi_off + (c * kTileN + r) * 8);
           const uint32_t c2 = (magic_half<BF16>() + z) * 0x00010001u;
-          if (q_channel || promote) dq_int6<BF16, false>(q, qh, c2, 0, o[i]);
+          if (q_channel) dq_int6<BF16, false>(q, qh, c2, 0, o[i]);
           else dq_int6<BF16, true>(q, qh, c2, sc16 * 0x00010001u, o[i]);
         } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
           dq_nvfp4(q, sc16, o[i]);
@@ -1161,7 +1132,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     const int sub = (dw % WG) >> 2;         // which G chunks of the 4 this warp converts
     const int r = quarter * 32 + static_cast<int>(lane);  // weight row within the tile (TMEM lane)
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol0;
-    const bool promote = CLS == 0 && p.promote;
     // the weight-tile layout fields this role reads per K-block, in registers
     const uint32_t q_scale_off = p.scale_off, q_zero_off = p.zero_off, q_hi_off = p.hi_off;
     const int q_g_kb = p.g_kb, q_group_k = p.group_k, q_has_zeros = p.has_zeros, q_channel = p.channel;
@@ -1243,11 +1213,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
 #pragma unroll
           for (int i = 0; i < G; ++i) {
             if constexpr (FMT == static_cast<int>(WFmt::INT4)) {
-              if (q_channel || promote) dq_int4<BF16, false>(qc[i], zz[i], ss[i], o[i]);
+              if (q_channel) dq_int4<BF16, false>(qc[i], zz[i], ss[i], o[i]);
               else dq_int4<BF16, true>(qc[i], zz[i], ss[i], o[i]);
             } else if constexpr (FMT == static_cast<int>(WFmt::INT6)) {
               const uint32_t c2 = (magic_half<BF16>() + zz[i]) * 0x00010001u;
-              if (q_channel || promote) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o[i]);
+              if (q_channel) dq_int6<BF16, false>(qc[i], qh[i], c2, 0, o[i]);
               else dq_int6<BF16, true>(qc[i], qh[i], c2, ss[i] * 0x00010001u, o[i]);
             } else if constexpr (FMT == static_cast<int>(WFmt::NVFP4)) {
               dq_nvfp4(qc[i], ss[i], o[i]);
@@ -1316,19 +1286,14 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     sc.init(p);
     bool ok = true;
     int ui = 0;
-    // promotion: K-blocks taken from each issuer's accumulator ring (issuer q
-    // takes position q of every stage, so this also indexes its scale ring)
-    [[maybe_unused]] uint32_t ck0 = 0, ck1 = 0;
     [[maybe_unused]] uint32_t ystg = 0;  // dense: tensor stores of Y issued by this warp
     [[maybe_unused]] int tr = 0;
     const bool trace_me = quarter == 0 && lane == 0;
     // INT4 bf16 operands without a folded scale carry an extra 2^-7
     constexpr float kOpFix = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
-    // MoE gated: the gate tile's sums of the promotion path, kept for its up tile
-    [[maybe_unused]] float gtot[CLS == 0 ? BNMAX : 1];
     const bool gated = MOE && p.moe_out == kMoeOutGated;
-    // MoE gated, other paths: this CTA's gate sums [BNMAX columns][128 rows] in
-    // global memory (L2-resident); a thread reads back only what it wrote
+    // MoE gated: this CTA's gate sums [BNMAX columns][128 rows] in global
+    // memory (L2-resident); a thread reads back only what it wrote
     float* const gbuf = gated ? p.gate_buf + static_cast<size_t>(blockIdx.x) * BNMAX * kTileN + r : nullptr;
     const int half_n = p.n_tiles / 2 * kTileN;  // gated: I, the first up row
     Unit u;
@@ -1479,81 +1444,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           }
         }
       };
-      bool promoted = false;
-      if constexpr (CLS == 0) {
-        if (p.promote) {
-          promoted = true;
-          // sum the unit's per-K-block accumulators in K order, each times its
-          // row's group scale, read from the transformed weight in global
-          // memory (read-only during the call; the tile's copy into shared
-          // memory has just brought it into L2), two K-blocks ahead
-          constexpr float kOpFixD = (FMT == static_cast<int>(WFmt::INT4) && BF16) ? 128.f : 1.f;
-          const uint8_t* srow = p.tiles + static_cast<uint64_t>(u.e) * p.expert_stride +
-                                static_cast<uint64_t>(u.nt) * p.k_tiles * tile_bytes + p.scale_off + 2u * r;
-          auto scale_of = [&](int kb) -> uint32_t {
-            return kb < u.kb1 ? __ldg(reinterpret_cast<const uint16_t*>(srow + static_cast<uint64_t>(kb) * tile_bytes))
-                              : 0u;
-          };
-          uint32_t sq0 = scale_of(u.kb0), sq1 = scale_of(u.kb0 + 1);
-          float tot[BNMAX];
-#pragma unroll
-          for (int i = 0; i < BNMAX; ++i) tot[i] = 0.f;
-          for (int kb = u.kb0; kb < u.kb1; ++kb) {
-            const int q = (kb - u.kb0) & (KPS - 1);
-            const uint32_t cq = q ? ck1 : ck0;
-            const int ks = q * KR + static_cast<int>(cq % KR);
-            const uint32_t s16 = sq0;
-            sq0 = sq1;
-            sq1 = scale_of(kb + 2);
-            if (!warp_wait(&k_full[ks], (cq / KR) & 1u, abort_flag)) {
-              ok = false;
-              break;
-            }
-            if (trace_me) HQ_TRACE(9, tr, (14ull << 24) | kb);
-            const float s_cur = (BF16 ? __uint_as_float(s16 << 16)
-                                      : __half2float(__ushort_as_half(static_cast<unsigned short>(s16)))) * kOpFixD;
-            dev::tc_fence_after();
-            const uint32_t acc = tmem + lane_base + ACC0 + static_cast<uint32_t>(ks * BNMAX);
-#pragma unroll
-            for (int ch = 0; ch < BNMAX / 16; ++ch) {
-              if (ch * 16 < bn) {
-                uint32_t a[16];
-                dev::tmem_ld16(acc + ch * 16, a);
-                dev::tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) tot[ch * 16 + i] = fmaf(s_cur, __uint_as_float(a[i]), tot[ch * 16 + i]);
-              }
-            }
-            dev::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) dev::mbar_arrive(&k_empty[ks]);
-            if (q) ++ck1; else ++ck0;
-          }
-          if (!ok) break;
-          if (gate_half) {
-#pragma unroll
-            for (int i = 0; i < BNMAX; ++i) gtot[i] = tot[i];
-          } else {
-#pragma unroll
-            for (int ch = 0; ch < BNMAX / 16; ++ch) {
-              if (ch * 16 < bn) {
-                float v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = tot[ch * 16 + i];
-                if (gated) {
-                  float g[16];
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) g[i] = gtot[ch * 16 + i];
-                  emit_gated16(ch, g, v);
-                } else {
-                  emit16(ch, v);
-                }
-              }
-            }
-          }
-        }
-      }
-      if (!promoted) {
+      {
         const int buf = DACC == 1 ? 0 : (ui & 1);
         const uint32_t accph = static_cast<uint32_t>(DACC == 1 ? ui : (ui >> 1)) & 1u;
         if (!warp_wait(&acc_full[buf], accph, abort_flag)) {
@@ -1777,7 +1668,7 @@ inline uint32_t smem_bytes(int w_stages, int x_stages, uint32_t tile_bytes, int 
                          : 0u);  // W4A8 token exponent words
   const uint32_t x = static_cast<uint32_t>(x_stages) * (a8 ? 1u : 2u) * C::kKps * static_cast<uint32_t>(bn) * 128u;
   const uint32_t bars =
-      (2u * w_stages + 2u * x_stages + 2u * a_bars<CLS>() + 2u * C::kDacc + 1u + 2u * kKRing +
+      (2u * w_stages + 2u * x_stages + 2u * a_bars<CLS>() + 2u * C::kDacc + 1u +
        1u) * 8u + 16u;
   const uint32_t scales = CLS == 0 ? 4u * kTileN * 16u : 0u;  // cluster split exchange of class 0
   const uint32_t moe = num_experts ? 4u * (3u * num_experts + 2u) : 0u;

@@ -591,7 +591,6 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   // tile row (their copies are then kept in L2 for the next row)
   p.bn = bn; p.num_tiles = 0; p.stream_k = 0; p.iters = 0; p.cluster = 1;
   p.m_tiles = static_cast<int64_t>(x_rows) > static_cast<int64_t>(L.num_experts) * bn ? 2 : 1;
-  p.promote = (cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
   p.idesc = a8 ? idesc_mx_e4m3(128, bn) : idesc_f16(true, 128, bn);
   p.x_mx = x_mx;
   p.ld_mx = static_cast<int>(ld_mx);
@@ -744,7 +743,6 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   p.bn = pl.bn; p.m_tiles = pl.m_tiles; p.num_tiles = pl.tiles;
   p.stages = pl.stages; p.x_stages = pl.x_stages; p.groups = pl.groups;
   p.stream_k = pl.stream_k; p.iters = pl.iters; p.cluster = pl.cluster;
-  p.promote = (pl.cls == 0 && (L.wtype == HQ_W_INT4 || L.wtype == HQ_W_INT6) && !L.channel && L.g_kb == 1) ? 1 : 0;
   p.idesc = a8 ? idesc_mx_e4m3(128, pl.bn) : idesc_f16(atype == HQ_A_BF16, 128, pl.bn);
   p.x_mx = a8 ? static_cast<const uint8_t*>(x_scales) : nullptr;
   p.ld_mx = L.k / 32;

@@ -127,7 +127,6 @@ struct GemmParams {
   int stages, x_stages;     // weight-ring and activation-ring stages
   int groups;               // dequantiser groups (for reporting)
   int stream_k;             // dense: deal K-blocks out in equal ranges (1) or whole tiles (0)
-  int promote;              // one accumulator per K-block, group scale applied in fp32 by the epilogue
   int cluster;              // dense: 2 = a 2-CTA cluster per tile, each CTA half of K, combined in shared memory
   int x3d;                  // activation map is 3-D: one box = every slab of a stage
   long long iters;          // stream-K: tiles * k_tiles

@@ -231,7 +231,7 @@ FFN = [
     # seed, weight, tokens, experts, intermediate I, hidden K, output n, topk, fused
     (40, "mxfp4", 37, 8, 128, 256, 256, 4, True),    # 32-token tiles
     (41, "int4", 64, 6, 192, 384, 200, 2, False),    # I not a multiple of 128: H stored, elementwise kernel
-    (42, "int4", 4, 8, 256, 512, 256, 2, True),      # 16-token tiles, group scales promoted in fp32
+    (42, "int4", 4, 8, 256, 512, 256, 2, True),      # 16-token tiles, asymmetric INT4 g128
     (43, "mxfp4", 300, 4, 256, 256, 128, 4, True),   # 128-token tiles
     (44, "int6ch", 40, 4, 128, 256, 256, 2, True),   # row scales of the gate and the up rows
     (45, "nvfp4", 64, 4, 128, 256, 256, 2, True),    # per-expert tensor scales
