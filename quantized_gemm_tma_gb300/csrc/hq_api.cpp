@@ -463,7 +463,7 @@ size_t splitk_bytes(int splits, int m, int n_pad) {
 void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_optin, int* w_stages,
                  int* x_stages, int* groups, bool a8 = false) {
   const size_t cap = std::min<size_t>(smem_optin, 232448);
-  static const int kXWant[4] = {6, 3, 3, 2};
+  static const int kXWant[5] = {6, 3, 3, 2, 2};
   // sweep overrides (clamped to [2, 12] and to what fits)
   const int fx = env_int("HQ_FORCE_XSTAGES", 0), fw = env_int("HQ_FORCE_WSTAGES", 0);
   int sx = fx >= 2 ? std::min(fx, 12) : kXWant[cls], sw = 0;
@@ -532,6 +532,17 @@ DensePlan plan_wna16(const Layout& L, int m, int sms, size_t smem_optin, uint32_
       env_int("HQ_FORCE_SPLITK", 0) == 0 && wna16_cluster_fits(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn, a8)) {
     p.cluster = 2;
     p.stream_k = 0;
+  }
+  // 128-token tiles with one tile per CTA: the stream class (class 4)
+  if (p.cls == 2 && (p.cluster == 2 || (!p.stream_k && p.tiles <= sms))) {
+    int st4 = 0, sx4 = 0, g4 = 0;
+    plan_stages(4, L, p.bn, 0, smem_optin, &st4, &sx4, &g4, a8);
+    if (st4 >= 2 && (p.cluster != 2 || wna16_cluster_fits(4, st4, sx4, L.tile_bytes, p.bn, a8))) {
+      p.cls = 4;
+      p.stages = st4;
+      p.x_stages = sx4;
+      p.groups = g4;
+    }
   }
   p.smem = wna16_smem_bytes(p.cls, p.stages, p.x_stages, L.tile_bytes, p.bn, 0, a8);
   // stream-K: at least 8 K-blocks per CTA, so that partial tiles stay few

@@ -44,7 +44,7 @@ cudaError_t launch_unpack(const Layout& L, const void* src, void* codes, void* s
                           cudaStream_t stream);
 
 // wna16_*.cu: fmt = WFmt; cls = tile-width class (0: bn <= 16, 1: <= 64,
-// 2: <= 128, 3: <= 256)
+// 2: <= 128, 3: <= 256, 4: dense <= 128 with one tile per CTA)
 struct Wna16Launch {
   int fmt;
   bool bf16;

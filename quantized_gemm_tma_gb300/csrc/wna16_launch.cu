@@ -31,6 +31,7 @@ uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_byt
     case 0: return wna16::smem_bytes<0>(w_stages, x_stages, tile_bytes, bn, num_experts, a8);
     case 1: return wna16::smem_bytes<1>(w_stages, x_stages, tile_bytes, bn, num_experts, a8);
     case 2: return wna16::smem_bytes<2>(w_stages, x_stages, tile_bytes, bn, num_experts, a8);
+    case 4: return wna16::smem_bytes<4>(w_stages, x_stages, tile_bytes, bn, num_experts, a8);
     default: return wna16::smem_bytes<3>(w_stages, x_stages, tile_bytes, bn, num_experts, a8);
   }
 }
@@ -40,7 +41,10 @@ bool wna16_cluster_fits(int cls, int w_stages, int x_stages, uint32_t tile_bytes
   const uint32_t kps = static_cast<uint32_t>(wna16_kps(cls));
   const uint64_t rings = static_cast<uint64_t>(x_stages) * (a8 ? 1u : 2u) * kps * static_cast<uint32_t>(bn) * 128u +
                          static_cast<uint64_t>(w_stages) * ((kps * tile_bytes + 1023u) & ~1023u);
-  const uint32_t need = cls == 1 ? wna16::xchg_bytes<1>() : cls == 2 ? wna16::xchg_bytes<2>() : wna16::xchg_bytes<3>();
+  const uint32_t need = cls == 1   ? wna16::xchg_bytes<1>()
+                        : cls == 2 ? wna16::xchg_bytes<2>()
+                        : cls == 4 ? wna16::xchg_bytes<4>()
+                                   : wna16::xchg_bytes<3>();
   return need <= rings;
 }
 
@@ -49,6 +53,7 @@ int wna16_kps(int cls) {
     case 0: return wna16::Cls<0>::kKps;
     case 1: return wna16::Cls<1>::kKps;
     case 2: return wna16::Cls<2>::kKps;
+    case 4: return wna16::Cls<4>::kKps;
     default: return wna16::Cls<3>::kKps;
   }
 }

@@ -23,6 +23,9 @@ cudaError_t run_cls(const Wna16Launch& l, const GemmParams& p, const Wna16Maps& 
     case 1: return run<BF16, 1, MOE>(l, p, maps, stream);
     case 2: return run<BF16, 2, MOE>(l, p, maps, stream);
     case 3: return run<BF16, 3, MOE>(l, p, maps, stream);
+    case 4:  // dense only
+      if constexpr (!MOE) return run<BF16, 4, false>(l, p, maps, stream);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }

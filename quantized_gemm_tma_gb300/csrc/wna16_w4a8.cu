@@ -28,6 +28,7 @@ cudaError_t launch_wna16_w4a8(const Wna16Launch& l, const GemmParams& p, const W
     case 1: return l.moe ? run<1, true>(l, p, maps, stream) : run<1, false>(l, p, maps, stream);
     case 2: return l.moe ? run<2, true>(l, p, maps, stream) : run<2, false>(l, p, maps, stream);
     case 3: return l.moe ? run<3, true>(l, p, maps, stream) : run<3, false>(l, p, maps, stream);
+    case 4: return l.moe ? cudaErrorInvalidValue : run<4, false>(l, p, maps, stream);  // dense only
     default: return cudaErrorInvalidValue;
   }
 }

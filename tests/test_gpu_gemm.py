@@ -159,8 +159,8 @@ CLUSTER = [
     # rank 1 the extra block)
     ("w4a16_cls0_m16", synth.dense_w4a16_asym, 16, 8192, 640),
     ("w4a16_cls1_m40", synth.dense_w4a16_asym, 40, 8192, 512),
-    ("w4a16_cls2_m100_ragged", synth.dense_w4a16_asym, 100, 8000, 384),
-    ("int6_cls2_fp16", synth.dense_int6_channel, 128, 7680, 256),
+    ("w4a16_cls4_m100_ragged", synth.dense_w4a16_asym, 100, 8000, 384),
+    ("int6_cls4_fp16", synth.dense_int6_channel, 128, 7680, 256),
     ("w4a16_cls3_m200", synth.dense_w4a16_sym, 200, 8192, 256),
 ]
 
@@ -173,6 +173,19 @@ def test_cluster_split(idx):
     y = _gpu(qw, acts)
     assert hq.hq_last_plan()["splits"] == 2, hq.hq_last_plan()
     check(y, _ref(qw, acts), name)
+
+
+@pytest.mark.parametrize("n,cls", [(12800, 4), (20480, 2)], ids=["one_tile_per_cta", "many_tiles_per_cta"])
+def test_128_token_classes(n, cls):
+    """Tiles of 65..128 tokens, whole tiles: the stream class with one
+    accumulator (4) when every CTA runs one tile (100 tiles), the one-K-block
+    class with two accumulators (2) when CTAs run several (160 tiles on 152
+    SMs; the 2-CTA cluster split of class 4 is in test_cluster_split)."""
+    import quantized_gemm_tma_gb300 as hq
+    qw, acts = synth.dense_w4a16_asym(46, 100, n, 512)
+    y = _gpu(qw, acts)
+    assert hq.hq_last_plan()["tile_class"] == cls, hq.hq_last_plan()
+    check(y, _ref(qw, acts), f"128-token class {cls}")
 
 
 def test_workspace_reused_across_shapes():

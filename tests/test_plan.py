@@ -24,7 +24,7 @@ def _int4(hq, n=8192, k=8192):
     (1, 16, 0, CLUSTER, 128),       # 64 tiles fill 57..76 of the SMs twice over: 2-CTA K split
     (16, 16, 0, CLUSTER, 128),
     (48, 48, 1, CLUSTER, 128),
-    (128, 128, 2, CLUSTER, 128),
+    (128, 128, 4, CLUSTER, 128),
     (1024, 256, 3, WHOLE, SMS),     # 256 wide tiles: whole tiles beat stream-K
     (4096, 256, 3, WHOLE, SMS),
 ])
@@ -160,7 +160,7 @@ def test_w4a8_plans(hq):
     columns beside the A operand)."""
     d = hq.make_desc("mxfp4", "ue8m0", 8192, 8192, group_k=32)
     for m, bn, cls, split in ((1, 16, 0, CLUSTER), (16, 16, 0, CLUSTER), (48, 48, 1, CLUSTER),
-                              (128, 128, 2, CLUSTER), (1024, 256, 3, WHOLE), (4096, 256, 3, WHOLE)):
+                              (128, 128, 4, CLUSTER), (1024, 256, 3, WHOLE), (4096, 256, 3, WHOLE)):
         p = hq.hq_plan_query(d, m, "mxfp8", SMS, OPTIN)
         assert (p["bn"], p["tile_class"], p["splits"]) == (bn, cls, split), (m, p)
         if cls <= 1:
