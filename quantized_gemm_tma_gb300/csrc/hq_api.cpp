@@ -459,11 +459,14 @@ size_t splitk_bytes(int splits, int m, int n_pad) {
 }
 
 // Shared-memory rings for a tile-width class: a few activation stages (the
-// MMA holds them), then as many weight stages as fit, up to 8.
+// MMA holds them), then as many weight stages as fit, up to 8.  Tiles of 256
+// tokens take three activation stages (192 KB for bf16) and leave the
+// weights two: one 128 x 256 x 128 MMA block (about 0.65 us on one SM) does
+// not cover the L2 latency of the next 64 KB stage behind a single one.
 void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_optin, int* w_stages,
                  int* x_stages, int* groups, bool a8 = false) {
   const size_t cap = std::min<size_t>(smem_optin, 232448);
-  static const int kXWant[5] = {6, 3, 3, 2, 2};
+  static const int kXWant[5] = {6, 3, 3, 3, 2};
   // sweep overrides (clamped to [2, 12] and to what fits)
   const int fx = env_int("HQ_FORCE_XSTAGES", 0), fw = env_int("HQ_FORCE_WSTAGES", 0);
   int sx = fx >= 2 ? std::min(fx, 12) : kXWant[cls], sw = 0;

@@ -76,10 +76,15 @@ def test_plan_tracks_sm_count_and_shared_memory(hq):
     # fewer SMs: 64 tiles no longer fit the cluster rule (2 x 64 > 100)
     p = hq.hq_plan_query(_int4(hq), 16, "bf16", 100, OPTIN)
     assert p["splits"] != CLUSTER and p["grid"] <= 100, p
-    # less shared memory: fewer pipeline stages, still at least two
-    big = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, OPTIN)
-    small = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, 160 * 1024)
+    # less shared memory: fewer weight stages, still at least two
+    big = hq.hq_plan_query(_int4(hq), 16, "bf16", SMS, OPTIN)
+    small = hq.hq_plan_query(_int4(hq), 16, "bf16", SMS, 160 * 1024)
     assert 2 <= small["stages"] < big["stages"], (small, big)
+    # 256-token tiles: three 64 KB activation stages leave room for two weight
+    # stages; with less shared memory two activation stages and more weights
+    wide = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, OPTIN)
+    narrow = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, 200 * 1024)
+    assert wide["tile_class"] == narrow["tile_class"] == 3 and wide["stages"] == 2 < narrow["stages"], (wide, narrow)
 
 
 def test_plan_query_validation(hq):
@@ -98,7 +103,8 @@ def test_plan_query_validation(hq):
 
 
 def test_stage_override_switch(hq):
-    """HQ_FORCE_WSTAGES (read once per process) caps the weight ring for sweeps."""
+    """HQ_FORCE_XSTAGES / HQ_FORCE_WSTAGES (read once per process) set the
+    activation ring and cap the weight ring for sweeps."""
     import os
     import subprocess
     import sys
@@ -106,12 +112,18 @@ def test_stage_override_switch(hq):
             "d = hq.make_desc('int4', 'bf16', 8192, 8192, group_k=128, signed_codes=False, has_zeros=True); "
             "print(hq.hq_plan_query(d, 4096, 'bf16', 152, 232448)['stages'])")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, HQ_FORCE_WSTAGES="3", PYTHONPATH=root)
-    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
-    assert out.returncode == 0, out.stderr
-    assert int(out.stdout.strip()) == 3
-    default = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, OPTIN)["stages"]
-    assert default > 3
+
+    def stages(**force):
+        env = dict(os.environ, PYTHONPATH=root, **force)
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+        assert out.returncode == 0, out.stderr
+        return int(out.stdout.strip())
+
+    # two 64 KB activation stages leave room for the whole weight ring, which
+    # the second switch caps
+    assert stages(HQ_FORCE_XSTAGES="2") == 8
+    assert stages(HQ_FORCE_XSTAGES="2", HQ_FORCE_WSTAGES="3") == 3
+    assert hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, OPTIN)["stages"] == 2
 
 
 @pytest.mark.parametrize("tokens,bn,cls", [(1, 16, 0), (16, 16, 0), (17, 32, 1), (128, 32, 1), (129, 64, 1),
