@@ -23,9 +23,11 @@
 //                accumulators, sum the issuers' partial accumulators, scale,
 //                and store Y through shared-memory boxes and tensor stores
 //                (or a partial, a cluster exchange, or MoE per-pair rows).
-//   warps 4-19   dequantisers.  Two K-blocks per stage (bn <= 64): four
-//                streams, stream t converting K-block t & 1 of every stage of
-//                parity t >> 1 (a whole K-block of its 32 rows per warp).  One
+//   warps 4-19   dequantisers.  Two K-blocks per stage (bn <= 64, and dense
+//                tiles of 128 tokens): four streams, stream t converting
+//                K-block t & 1 of every stage of parity t >> 1 (a whole K-block
+//                of its 32 rows per warp); W4A8 tiles of 256 tokens: four
+//                streams, stream t taking every fourth stage.  Otherwise one
 //                K-block per stage: all 16 warps on each K-block, one 32-column
 //                chunk each.  A thread owns one weight row (its TMEM lane),
 //                turns the packed codes into bf16x2/f16x2 pairs and writes
@@ -105,9 +107,10 @@ template <int CLS>
 constexpr int half_ring() { return 2; }
 template <int CLS>
 constexpr uint32_t acc_col0() { return static_cast<uint32_t>(4 * 64); }
-// A-slot barriers of each kind: four slots, or four streams' half slots
+// A-slot barriers of each kind: four streams' half slots (eight), of which
+// the classes without streams use the first four (kASlots)
 template <int CLS>
-constexpr int a_bars() { return Cls<CLS>::kKps == 2 ? 4 * half_ring<CLS>() : kASlots; }
+constexpr int a_bars() { return 4 * half_ring<CLS>(); }
 
 template <int CLS>
 constexpr int threads() { return 32 * (kIssWarp0 + Cls<CLS>::kIss); }
@@ -546,16 +549,20 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   constexpr int G = KPS;                 // dequantiser groups
   constexpr int WG = kDqWarps / G;        // warps per group
   constexpr int DA = kASlots / G;         // A slots per group
-  // Two K-blocks per stage: the dequantisers work as four streams.  Stream t
-  // takes K-block (t & 1) of every stage of parity (t >> 1), a whole K-block
-  // of its rows per warp, so the four warps sharing a scheduler are at
-  // different points of their pipelines instead of in lock step.
-  constexpr bool kStream = KPS == 2;
   // W4A8: e4m3 activations (one 128-byte swizzled slab per K-block instead of
   // two of bf16), e4m3 weights in TMEM (32 columns per K-block: A at columns
   // [0, 32) of each 64-column A slot, UE8M0 scale factors in [32, 64)), and
   // block-scaled K32 MMAs.
   constexpr bool A8 = FMT == static_cast<int>(WFmt::MXFP4_A8);
+  // Streams: the dequantisers work as four streams of four warps, a whole
+  // K-block of its rows per warp, so the four warps sharing a scheduler are at
+  // different points of their pipelines instead of in lock step, and the
+  // per-K-block waits and hand-offs are paid by four warps instead of sixteen.
+  // With two K-blocks per stage stream t takes K-block (t & 1) of every stage
+  // of parity (t >> 1); W4A8 tiles of 256 tokens (one K-block per stage, an
+  // MMA block twice as fast as bf16's) have stream t take every fourth stage.
+  constexpr bool kStream = KPS == 2 || (CLS == 3 && A8);
+  constexpr int NSTG = kStream ? 4 / KPS : 1;  // stream period in stages
   constexpr uint32_t kSlabsKb = A8 ? 1u : 2u;  // activation slabs per K-block
   // With streams, issuer p takes K-block p of every stage, i.e. the K-blocks
   // of streams p and 2 + p alternately.
@@ -606,11 +613,12 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = dev::lane_id();
-  // Streams of one stage parity skip the other parity's stages, so a weight
-  // ring slot must always carry stages of one parity (even depth); an odd
-  // depth would let a parity wait pass one phase early.  The planner never
-  // asks for one; refuse it before any barrier, TMEM or copy exists.
-  if (kStream && (SW & 1)) {
+  // A stream skips the stages of the other streams, so a weight ring slot
+  // must always carry stages of one residue modulo the stream period (a depth
+  // that is a multiple of it); otherwise a stream's parity wait could pass
+  // one phase early.  The planner never asks for one; refuse it before any
+  // barrier, TMEM or copy exists.
+  if (kStream && (SW % NSTG)) {
     if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0, static_cast<int>(HQ_ERR_INVALID_ARG));
     return;
   }
@@ -621,7 +629,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       // W4A8: the tensor copy's arrival, then one per producer lane when its
       // exponent copies have landed
       dev::mbar_init(&w_full[s], A8 ? 33 : 1);
-      dev::mbar_init(&w_empty[s], kStream ? 8 : kDqWarps);  // streams: the two of the stage's parity
+      dev::mbar_init(&w_empty[s], kStream ? 4 * KPS : kDqWarps);  // streams: the warps of those that take it
     }
     for (int s = 0; s < SX; ++s) {
       dev::mbar_init(&x_full[s], 1);
@@ -762,6 +770,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     Ring rg;
     int issued = 0;
     bool ok = true;
+    [[maybe_unused]] int tr = 0;
     Unit u;
     while (ok && sc.next(p, s_tabs, u)) {
       for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
@@ -788,6 +797,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               dev::tma_load_2d(xs + z * slab, &tmap_x, &x_full[rg.s], A8 ? (kb + z) * 128 : (2 * kb + z) * 64,
                                u.xrow0);
           }
+          HQ_TRACE(3, tr, (16ull << 24) | issued);
         }
         rg.next(SX);
         ++issued;
@@ -816,7 +826,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       bool ok = true;
       int ui = 0;
       [[maybe_unused]] int tr = 0, ts = 0;
-      [[maybe_unused]] uint32_t cs0 = 0, cs1 = 0;  // streams: K-blocks taken from streams pidx, 2 + pidx
+      // streams: K-blocks taken from each stream this issuer reads (two K-blocks
+      // per stage: streams pidx and 2 + pidx; one: all four)
+      [[maybe_unused]] uint32_t cs0 = 0, cs1 = 0, cs2 = 0, cs3 = 0;
       [[maybe_unused]] uint32_t S = 0;           // streams: stage counter
       Unit u;
       while (ok && sc.next(p, s_tabs, u)) {
@@ -839,11 +851,14 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           }
           HQ_TRACE(1 + pidx, tr, (2ull << 24) | ts);
           // stream mode: K-block pidx of this stage comes from stream
-          // 2 (S & 1) + pidx, in two halves (64 K each) published separately
+          // 2 (S & 1) + pidx (one K-block per stage: stream S & 3), in two
+          // halves (64 K each) published separately
           const int q = pidx;
           if (kStream && q < cnt) {
-            const int t = 2 * static_cast<int>(S & 1u) + q;
-            const uint32_t cst = (S & 1u) ? cs1 : cs0;  // K-blocks taken from stream t so far
+            const int t = KPS == 2 ? 2 * static_cast<int>(S & 1u) + q : static_cast<int>(S & 3u);
+            const int ci = KPS == 2 ? static_cast<int>(S & 1u) : t;
+            // K-blocks taken from stream t so far
+            const uint32_t cst = ci == 0 ? cs0 : ci == 1 ? cs1 : ci == 2 ? cs2 : cs3;
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * q * slab;
             const uint32_t d_tmem = tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = first;
@@ -878,7 +893,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               dev::tc_commit(&a_empty[hs]);
             }
             if (!ok) break;
-            if (S & 1u) ++cs1; else ++cs0;
+            if (ci == 0) ++cs0;
+            else if (ci == 1) ++cs1;
+            else if (ci == 2) ++cs2;
+            else ++cs3;
             first = false;
           } else if (!kStream && pidx < cnt) {
             const int slot = pidx * DA + static_cast<int>(cu % DA);
@@ -928,8 +946,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     // ============================================================ dequantisers (streams)
     const int dw = warp - kDqWarp0;
     const int t = dw >> 2;                  // stream
-    const uint32_t sg = static_cast<uint32_t>(t >> 1);  // parity of the stages it takes
-    const int pos = t & 1;                  // K-block of those stages it converts
+    // the stages it takes (S % NSTG == sg) and the K-block of them it converts
+    const uint32_t sg = KPS == 2 ? static_cast<uint32_t>(t >> 1) : static_cast<uint32_t>(t);
+    const int pos = KPS == 2 ? (t & 1) : 0;
     const int quarter = warp & 3;
     const int r = quarter * 32 + static_cast<int>(lane);  // weight row within the tile (TMEM lane)
     // this lane's row in the stream's ring of half slots (32 columns each)
@@ -1013,7 +1032,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       if (q_channel && q_has_zeros) zrow = p.row_zero[static_cast<size_t>(u.e) * p.n_pad + n];
       for (int kb = u.kb0; kb < u.kb1; kb += KPS, ++S) {
         const int cnt = min(KPS, u.kb1 - kb);
-        if ((S & 1u) == sg) {
+        if ((S % NSTG) == sg) {
           if (!warp_wait(&w_full[rg.s], rg.ph, abort_flag)) {
             ok = false;
             break;
@@ -1033,13 +1052,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               // the tile; the conversion's 2^6 is folded in when they are
               // stored) and tokens 32j + lane (staged beside the tile by the
               // weight producer)
-              uint32_t ww[4], xw[4];
+              constexpr int kXW = static_cast<int>(kETok / 32);  // token words: 4, or 8 for 256 tokens
+              uint32_t ww[4], xw[kXW];
               const uint32_t* es = e_st + rg.s * kEStage + pos * kETok;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                ww[j] = *reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4);
-                xw[j] = es[32 * j + lane];
-              }
+              for (int j = 0; j < 4; ++j) ww[j] = *reinterpret_cast<const uint32_t*>(wsm + q_scale_off + (32 * j + lane) * 4);
+#pragma unroll
+              for (int j = 0; j < kXW; ++j) xw[j] = es[32 * j + lane];
               mx_fold_words(ww);
               // this lane's row: sub-blocks whose exponent cannot take the fold
               // are converted exactly (rare: a block scale above 2^121); the
@@ -1058,7 +1077,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               };
               // half slot j: e4m3 codes of two sub-blocks in columns
               // [0, 16), its own copy of the scale factors at 16 (A, 4
-              // columns) and 20 (B, 4 columns for up to 128 tokens)
+              // columns) and 20 (B, 4 columns per 128 tokens)
               auto st_half = [&](int j) {
                 uint32_t o16[16];
 #pragma unroll
@@ -1069,18 +1088,22 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
                 dev::tmem_st16(a_lane + j * 32, o16);
                 dev::tmem_st4(a_lane + j * 32 + 16, ww[0], ww[1], ww[2], ww[3]);
                 dev::tmem_st4(a_lane + j * 32 + 20, xw[0], xw[1], xw[2], xw[3]);
+                if constexpr (kXW == 8) dev::tmem_st4(a_lane + j * 32 + 24, xw[4], xw[5], xw[6], xw[7]);
               };
               conv8(0);
+              if (trace_me) HQ_TRACE(5 + t, tr, (12ull << 24) | ts);
               if (!warp_wait(&a_empty[t * HR + j0], eph0, abort_flag)) {
                 ok = false;
                 break;
               }
+              if (trace_me) HQ_TRACE(5 + t, tr, (6ull << 24) | ts);
               dev::tc_fence_after();
               st_half(j0);
               conv8(2);
               __syncwarp();
               if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
               publish(t * HR + j0);
+              if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
               if (!warp_wait(&a_empty[t * HR + j1], eph1, abort_flag)) {
                 ok = false;
                 break;
@@ -1088,6 +1111,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               dev::tc_fence_after();
               st_half(j1);
               publish(t * HR + j1);
+              if (trace_me) HQ_TRACE(5 + t, tr, (7ull << 24) | ts);
               ++ca;
               ++ts;
               rg.next(SW);

@@ -471,14 +471,16 @@ void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_
   const int fx = env_int("HQ_FORCE_XSTAGES", 0), fw = env_int("HQ_FORCE_WSTAGES", 0);
   int sx = fx >= 2 ? std::min(fx, 12) : kXWant[cls], sw = 0;
   const int sw_max = fw >= 2 ? std::min(fw, 12) : 8;
-  // Two K-blocks per stage: the dequantiser streams of one stage parity wait
-  // only on the stages of that parity, so every slot of the weight ring must
-  // always hold stages of one parity, i.e. an even ring depth.  With an odd
-  // depth a slot alternates parities and a stream's parity wait on it could
-  // pass one phase early, while the other parity's copy is still landing.
-  const int sw_step = wna16_kps(cls) == 2 ? 2 : 1;
+  // A dequantiser stream waits only on the stages it takes (every second with
+  // two K-blocks per stage, every fourth for W4A8 256-token tiles), so every
+  // slot of the weight ring must always hold stages of one residue, i.e. a
+  // ring depth that is a multiple of that period.  Otherwise a slot cycles
+  // through residues and a stream's parity wait on it could pass one phase
+  // early, while another stream's copy is still landing.
+  const int sw_step = wna16_stream_period(cls, a8);
+  const int sw_top = std::max(sw_step, sw_max - sw_max % sw_step);
   for (; sx >= 2; --sx) {
-    for (sw = sw_max - (sw_max % sw_step); sw >= 2; sw -= sw_step)
+    for (sw = sw_top; sw >= 2; sw -= sw_step)
       if (wna16_smem_bytes(cls, sw, sx, L.tile_bytes, bn, num_experts, a8) <= cap) break;
     if (sw >= 2) break;
   }

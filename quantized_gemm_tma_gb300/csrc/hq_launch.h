@@ -62,6 +62,9 @@ cudaError_t launch_wna16(const Wna16Launch& l, const GemmParams& p, const Wna16M
 uint32_t wna16_smem_bytes(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, int num_experts,
                           bool a8 = false);
 int wna16_kps(int cls);  // K-blocks per shared-memory stage
+// stages between two a dequantiser stream takes (1: no streams); the weight
+// ring's depth is a multiple of it
+int wna16_stream_period(int cls, bool a8);
 // whether a 2-CTA cluster split of this class can pass rank 1's sums through
 // rank 0's ring area
 bool wna16_cluster_fits(int cls, int w_stages, int x_stages, uint32_t tile_bytes, int bn, bool a8 = false);

@@ -175,8 +175,10 @@ def test_w4a8_plans(hq):
                               (128, 128, 4, CLUSTER), (1024, 256, 3, WHOLE), (4096, 256, 3, WHOLE)):
         p = hq.hq_plan_query(d, m, "mxfp8", SMS, OPTIN)
         assert (p["bn"], p["tile_class"], p["splits"]) == (bn, cls, split), (m, p)
-        if cls <= 1:
+        if cls in (0, 1, 4):
             assert p["stages"] % 2 == 0, p
+        if cls == 3:   # four dequantiser streams, each on every fourth stage
+            assert p["stages"] % 4 == 0, p
     with pytest.raises(hq.HQError) as ei:
         hq.hq_plan_query(hq.make_desc("int4", "bf16", 8192, 8192, group_k=128), 16, "mxfp8", SMS, OPTIN)
     assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
