@@ -26,7 +26,8 @@
 //   warps 4-19   dequantisers.  Two K-blocks per stage (bn <= 64, and dense
 //                tiles of 128 tokens): four streams, stream t converting
 //                K-block t & 1 of every stage of parity t >> 1 (a whole K-block
-//                of its 32 rows per warp); W4A8 tiles of 256 tokens: four
+//                of its 32 rows per warp); tiles of 128 tokens with one
+//                K-block per stage and W4A8 tiles of 256 tokens: four
 //                streams, stream t taking every fourth stage.  Otherwise one
 //                K-block per stage: all 16 warps on each K-block, one 32-column
 //                chunk each.  A thread owns one weight row (its TMEM lane),
@@ -559,9 +560,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // different points of their pipelines instead of in lock step, and the
   // per-K-block waits and hand-offs are paid by four warps instead of sixteen.
   // With two K-blocks per stage stream t takes K-block (t & 1) of every stage
-  // of parity (t >> 1); W4A8 tiles of 256 tokens (one K-block per stage, an
-  // MMA block twice as fast as bf16's) have stream t take every fourth stage.
-  constexpr bool kStream = KPS == 2 || (CLS == 3 && A8);
+  // of parity (t >> 1); tiles of 128 tokens with one K-block per stage (MoE,
+  // and dense problems with several tiles per CTA) and W4A8 tiles of 256
+  // tokens (an MMA block twice as fast as bf16's) have stream t take every
+  // fourth stage.
+  constexpr bool kStream = KPS == 2 || CLS == 2 || (CLS == 3 && A8);
   constexpr int NSTG = kStream ? 4 / KPS : 1;  // stream period in stages
   constexpr uint32_t kSlabsKb = A8 ? 1u : 2u;  // activation slabs per K-block
   // With streams, issuer p takes K-block p of every stage, i.e. the K-blocks

@@ -472,7 +472,8 @@ void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_
   int sx = fx >= 2 ? std::min(fx, 12) : kXWant[cls], sw = 0;
   const int sw_max = fw >= 2 ? std::min(fw, 12) : 8;
   // A dequantiser stream waits only on the stages it takes (every second with
-  // two K-blocks per stage, every fourth for W4A8 256-token tiles), so every
+  // two K-blocks per stage, every fourth for 128-token tiles with one K-block
+  // per stage and W4A8 256-token tiles), so every
   // slot of the weight ring must always hold stages of one residue, i.e. a
   // ring depth that is a multiple of that period.  Otherwise a slot cycles
   // through residues and a stream's parity wait on it could pass one phase

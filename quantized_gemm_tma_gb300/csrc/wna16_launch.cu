@@ -50,7 +50,7 @@ bool wna16_cluster_fits(int cls, int w_stages, int x_stages, uint32_t tile_bytes
 
 int wna16_stream_period(int cls, bool a8) {
   if (cls == 0 || cls == 1 || cls == 4) return 2;  // two K-blocks per stage
-  return cls == 3 && a8 ? 4 : 1;                    // W4A8 256-token tiles: one
+  return cls == 2 || (cls == 3 && a8) ? 4 : 1;      // one K-block per stage
 }
 
 int wna16_kps(int cls) {

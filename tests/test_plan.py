@@ -137,6 +137,8 @@ def test_moe_tile_width_from_mean_rows(hq, tokens, bn, cls):
     assert p["stages"] >= 2
     if p["tile_class"] <= 1:
         assert p["stages"] % 2 == 0, p   # two K-blocks per stage: even weight ring
+    if p["tile_class"] == 2:
+        assert p["stages"] % 4 == 0, p   # four dequantiser streams, each on every fourth stage
 
 
 @pytest.mark.parametrize("bn", [16, 32, 48, 64])
