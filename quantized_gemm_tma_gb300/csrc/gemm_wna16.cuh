@@ -566,6 +566,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // fourth stage.
   constexpr bool kStream = KPS == 2 || CLS == 2 || (CLS == 3 && A8);
   constexpr int NSTG = kStream ? 4 / KPS : 1;  // stream period in stages
+  // Streams with one K-block per stage run ahead of the MMA, so a stream
+  // publishes its K-block once, both half slots together, on the barrier pair
+  // of its first half slot, and the issuer waits and commits once per K-block
+  // (the W4A8 scale factors then live in the first half slot only)
+  constexpr bool kKbPub = kStream && KPS == 1;
   constexpr uint32_t kSlabsKb = A8 ? 1u : 2u;  // activation slabs per K-block
   // With streams, issuer p takes K-block p of every stage, i.e. the K-blocks
   // of streams p and 2 + p alternately.
@@ -595,6 +600,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   uint64_t* a_full = x_empty + SX;
   constexpr int NAB = a_bars<CLS>();  // A-slot barriers of each kind
   constexpr int HR = half_ring<CLS>();  // streams: half slots per stream
+  static_assert(!kKbPub || HR == 2, "a whole-K-block publish assumes a stream's K-block fills its ring");
   constexpr uint32_t ACC0 = acc_col0<CLS>();
   uint64_t* a_empty = a_full + NAB;
   uint64_t* acc_full = a_empty + NAB;
@@ -854,8 +860,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           }
           HQ_TRACE(1 + pidx, tr, (2ull << 24) | ts);
           // stream mode: K-block pidx of this stage comes from stream
-          // 2 (S & 1) + pidx (one K-block per stage: stream S & 3), in two
-          // halves (64 K each) published separately
+          // 2 (S & 1) + pidx, in two halves (64 K each) published separately
+          // (one K-block per stage: stream S & 3, published whole)
           const int q = pidx;
           if (kStream && q < cnt) {
             const int t = KPS == 2 ? 2 * static_cast<int>(S & 1u) + q : static_cast<int>(S & 3u);
@@ -865,35 +871,62 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * q * slab;
             const uint32_t d_tmem = tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = first;
-            for (int h = 0; h < 2 && ok; ++h) {
-              // half h of the stream's K-block cst is its half slot 2 cst + h of the ring
-              const uint32_t hn = 2u * cst + static_cast<uint32_t>(h);
-              const int hs = t * HR + static_cast<int>(hn % HR);
-              if (!dev::mbar_wait(&a_full[hs], (hn / HR) & 1u, abort_flag)) {
+            if constexpr (kKbPub) {
+              // the stream's K-block cst: one wait, its two half slots' MMAs,
+              // one release (descriptor of 32-byte step k: base + 2k)
+              const int hs = t * HR;
+              if (!dev::mbar_wait(&a_full[hs], cst & 1u, abort_flag)) {
                 ok = false;
                 break;
               }
               HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
               dev::tc_fence_after();
+              const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
+              const uint64_t bd0 = dev::sw128_desc(xs);
               if constexpr (A8) {
-                // half h = 32-K sub-blocks 2h, 2h + 1: A at the half slot's
-                // columns 8i, its scale factors at + 16 (A) and + 20 (B)
-                const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                  const uint64_t bdesc = dev::sw128_desc(xs + (2 * h + i) * 32);
-                  dev::mma_mx_ts(d_tmem, a_tmem + i * 8, bdesc, mx_idesc_sub(idesc, 2 * h + i), a_tmem + 16u,
-                                 a_tmem + 20u, (fresh && h == 0 && i == 0) ? 0u : 1u);
-                }
+                for (int c = 0; c < 4; ++c)
+                  dev::mma_mx_ts(d_tmem, a_tmem + (c >> 1) * 32 + (c & 1) * 8, bd0 + 2u * c, mx_idesc_sub(idesc, c),
+                                 a_tmem + 16u, a_tmem + 20u, (fresh && c == 0) ? 0u : 1u);
               } else {
-                const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t bdesc = dev::sw128_desc(xs + h * slab + kk * 32);
-                  dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && h == 0 && kk == 0) ? 0u : 1u);
-                }
+                for (int c = 0; c < 8; ++c)
+                  dev::mma_f16_ts(d_tmem, a_tmem + (c >> 2) * 32 + (c & 3) * 8,
+                                  bd0 + static_cast<uint64_t>(((c >> 2) * slab + (c & 3) * 32) >> 4), idesc,
+                                  (fresh && c == 0) ? 0u : 1u);
               }
               dev::tc_commit(&a_empty[hs]);
+            } else {
+              for (int h = 0; h < 2 && ok; ++h) {
+                // half h of the stream's K-block cst is its half slot 2 cst + h of the ring
+                const uint32_t hn = 2u * cst + static_cast<uint32_t>(h);
+                const int hs = t * HR + static_cast<int>(hn % HR);
+                if (!dev::mbar_wait(&a_full[hs], (hn / HR) & 1u, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
+                dev::tc_fence_after();
+                if constexpr (A8) {
+                  // half h = 32-K sub-blocks 2h, 2h + 1: A at the half slot's
+                  // columns 8i, its scale factors at + 16 (A) and + 20 (B)
+                  const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
+#pragma unroll
+                  for (int i = 0; i < 2; ++i) {
+                    const uint64_t bdesc = dev::sw128_desc(xs + (2 * h + i) * 32);
+                    dev::mma_mx_ts(d_tmem, a_tmem + i * 8, bdesc, mx_idesc_sub(idesc, 2 * h + i), a_tmem + 16u,
+                                   a_tmem + 20u, (fresh && h == 0 && i == 0) ? 0u : 1u);
+                  }
+                } else {
+                  const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t bdesc = dev::sw128_desc(xs + h * slab + kk * 32);
+                    dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && h == 0 && kk == 0) ? 0u : 1u);
+                  }
+                }
+                dev::tc_commit(&a_empty[hs]);
+              }
             }
             if (!ok) break;
             if (ci == 0) ++cs0;
@@ -1081,7 +1114,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               // half slot j: e4m3 codes of two sub-blocks in columns
               // [0, 16), its own copy of the scale factors at 16 (A, 4
               // columns) and 20 (B, 4 columns per 128 tokens)
-              auto st_half = [&](int j) {
+              auto st_half = [&](int j, bool sf) {
                 uint32_t o16[16];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -1089,9 +1122,11 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
                   o16[8 + i] = o8[1][i];
                 }
                 dev::tmem_st16(a_lane + j * 32, o16);
-                dev::tmem_st4(a_lane + j * 32 + 16, ww[0], ww[1], ww[2], ww[3]);
-                dev::tmem_st4(a_lane + j * 32 + 20, xw[0], xw[1], xw[2], xw[3]);
-                if constexpr (kXW == 8) dev::tmem_st4(a_lane + j * 32 + 24, xw[4], xw[5], xw[6], xw[7]);
+                if (sf) {
+                  dev::tmem_st4(a_lane + j * 32 + 16, ww[0], ww[1], ww[2], ww[3]);
+                  dev::tmem_st4(a_lane + j * 32 + 20, xw[0], xw[1], xw[2], xw[3]);
+                  if constexpr (kXW == 8) dev::tmem_st4(a_lane + j * 32 + 24, xw[4], xw[5], xw[6], xw[7]);
+                }
               };
               conv8(0);
               if (trace_me) HQ_TRACE(5 + t, tr, (12ull << 24) | ts);
@@ -1101,19 +1136,25 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               }
               if (trace_me) HQ_TRACE(5 + t, tr, (6ull << 24) | ts);
               dev::tc_fence_after();
-              st_half(j0);
+              st_half(j0, true);
               conv8(2);
               __syncwarp();
               if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
-              publish(t * HR + j0);
-              if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
-              if (!warp_wait(&a_empty[t * HR + j1], eph1, abort_flag)) {
-                ok = false;
-                break;
+              if constexpr (kKbPub) {
+                st_half(j1, false);  // the MMAs of both halves read the first half's scale factors
+                publish(t * HR + j0);
+                if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
+              } else {
+                publish(t * HR + j0);
+                if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
+                if (!warp_wait(&a_empty[t * HR + j1], eph1, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                dev::tc_fence_after();
+                st_half(j1, true);
+                publish(t * HR + j1);
               }
-              dev::tc_fence_after();
-              st_half(j1);
-              publish(t * HR + j1);
               if (trace_me) HQ_TRACE(5 + t, tr, (7ull << 24) | ts);
               ++ca;
               ++ts;
@@ -1136,16 +1177,23 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             // every lane's codes are consumed: the stage may be refilled
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
-            publish(t * HR + j0);
-            if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
-            if (!warp_wait(&a_empty[t * HR + j1], eph1, abort_flag)) {
-              ok = false;
-              break;
+            if constexpr (kKbPub) {
+              dev::tmem_st16(a_lane + j1 * 32, o[0]);
+              dev::tmem_st16(a_lane + j1 * 32 + 16, o[1]);
+              publish(t * HR + j0);
+              if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
+            } else {
+              publish(t * HR + j0);
+              if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
+              if (!warp_wait(&a_empty[t * HR + j1], eph1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              dev::tc_fence_after();
+              dev::tmem_st16(a_lane + j1 * 32, o[0]);
+              dev::tmem_st16(a_lane + j1 * 32 + 16, o[1]);
+              publish(t * HR + j1);
             }
-            dev::tc_fence_after();
-            dev::tmem_st16(a_lane + j1 * 32, o[0]);
-            dev::tmem_st16(a_lane + j1 * 32 + 16, o[1]);
-            publish(t * HR + j1);
             if (trace_me) HQ_TRACE(5 + t, tr, (7ull << 24) | ts);
             ++ca;
           } else {
