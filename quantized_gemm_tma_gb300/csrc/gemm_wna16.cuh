@@ -835,9 +835,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       bool ok = true;
       int ui = 0;
       [[maybe_unused]] int tr = 0, ts = 0;
-      // streams: K-blocks taken from each stream this issuer reads (two K-blocks
-      // per stage: streams pidx and 2 + pidx; one: all four)
-      [[maybe_unused]] uint32_t cs0 = 0, cs1 = 0, cs2 = 0, cs3 = 0;
       [[maybe_unused]] uint32_t S = 0;           // streams: stage counter
       Unit u;
       while (ok && sc.next(p, s_tabs, u)) {
@@ -865,9 +862,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           const int q = pidx;
           if (kStream && q < cnt) {
             const int t = KPS == 2 ? 2 * static_cast<int>(S & 1u) + q : static_cast<int>(S & 3u);
-            const int ci = KPS == 2 ? static_cast<int>(S & 1u) : t;
-            // K-blocks taken from stream t so far
-            const uint32_t cst = ci == 0 ? cs0 : ci == 1 ? cs1 : ci == 2 ? cs2 : cs3;
+            // K-blocks taken from stream t so far: one per stream period
+            const uint32_t cst = S / static_cast<uint32_t>(NSTG);
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * q * slab;
             const uint32_t d_tmem = tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = first;
@@ -929,10 +925,6 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               }
             }
             if (!ok) break;
-            if (ci == 0) ++cs0;
-            else if (ci == 1) ++cs1;
-            else if (ci == 2) ++cs2;
-            else ++cs3;
             first = false;
           } else if (!kStream && pidx < cnt) {
             const int slot = pidx * DA + static_cast<int>(cu % DA);
