@@ -569,8 +569,20 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // Streams with one K-block per stage run ahead of the MMA, so a stream
   // publishes its K-block once, both half slots together, on the barrier pair
   // of its first half slot, and the issuer waits and commits once per K-block
-  // (the W4A8 scale factors then live in the first half slot only)
+  // (the W4A8 scale factors then live in the first half slot only).
   constexpr bool kKbPub = kStream && KPS == 1;
+  // The single issuing thread pays for every wait and commit on its own
+  // (about 100-300 cycles each against 500 cycles of MMA per W4A8 K-block),
+  // so for W4A8 tiles of 256 tokens the stream also waits for the stage's
+  // activations before it publishes, and the activation producer refills a
+  // slot once the K-block that read it has released its stream's A slot: the
+  // issuer waits once and commits once per K-block.  Both parity waits are
+  // unambiguous with an activation ring of exactly four stages, one stream
+  // period: the producer's on the release (the stream's next K-block needs
+  // activations not yet loaded) and the stream's on the activations (below).
+  // (The 128-token MoE tiles keep the issuer's activation waits: four 32 KB
+  // activation stages would leave their weights half the ring.)
+  constexpr bool kXMerge = kKbPub && CLS == 3;
   constexpr uint32_t kSlabsKb = A8 ? 1u : 2u;  // activation slabs per K-block
   // With streams, issuer p takes K-block p of every stage, i.e. the K-blocks
   // of streams p and 2 + p alternately.
@@ -625,9 +637,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // A stream skips the stages of the other streams, so a weight ring slot
   // must always carry stages of one residue modulo the stream period (a depth
   // that is a multiple of it); otherwise a stream's parity wait could pass
-  // one phase early.  The planner never asks for one; refuse it before any
-  // barrier, TMEM or copy exists.
-  if (kStream && (SW % NSTG)) {
+  // one phase early.  W4A8 256-token tiles also need an activation ring of
+  // exactly four stages (above).  The planner never asks for anything else;
+  // refuse it before any barrier, TMEM or copy exists.
+  if ((kStream && (SW % NSTG)) || (kXMerge && SX != 4)) {
     if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0, static_cast<int>(HQ_ERR_INVALID_ARG));
     return;
   }
@@ -784,7 +797,18 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
     while (ok && sc.next(p, s_tabs, u)) {
       for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
         const int cnt = min(KPS, u.kb1 - kb);
-        if (!warp_wait(&x_empty[rg.s], rg.ph ^ 1u, abort_flag)) {
+        if constexpr (kXMerge) {
+          // the slot's previous stage, issued - SX, was read by the MMAs of
+          // K-block (issued - SX) / 4 of stream (issued - SX) % 4; their
+          // completion releases that stream's A slot
+          if (issued >= SX) {
+            const int prev = issued - SX;
+            if (!warp_wait(&a_empty[(prev & 3) * HR], static_cast<uint32_t>(prev >> 2) & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+          }
+        } else if (!warp_wait(&x_empty[rg.s], rg.ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -836,6 +860,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
       int ui = 0;
       [[maybe_unused]] int tr = 0, ts = 0;
       [[maybe_unused]] uint32_t S = 0;           // streams: stage counter
+      [[maybe_unused]] uint32_t cs0 = 0, cs1 = 0;  // two K-blocks per stage: K-blocks taken from streams pidx, 2 + pidx
       Unit u;
       while (ok && sc.next(p, s_tabs, u)) {
         // whole-unit accumulator (double-buffered across units where TMEM allows)
@@ -851,7 +876,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         bool first = true;
         for (int kb = u.kb0; kb < u.kb1; kb += KPS) {
           const int cnt = min(KPS, u.kb1 - kb);
-          if (!dev::mbar_wait(&x_full[rx.s], rx.ph, abort_flag)) {
+          // W4A8 256-token tiles: the stream's publish covers the activations
+          if (!kXMerge && !dev::mbar_wait(&x_full[rx.s], rx.ph, abort_flag)) {
             ok = false;
             break;
           }
@@ -862,8 +888,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           const int q = pidx;
           if (kStream && q < cnt) {
             const int t = KPS == 2 ? 2 * static_cast<int>(S & 1u) + q : static_cast<int>(S & 3u);
-            // K-blocks taken from stream t so far: one per stream period
-            const uint32_t cst = S / static_cast<uint32_t>(NSTG);
+            // K-blocks taken from stream t so far: one per stream period with
+            // one K-block per stage; with two, a unit's last stage may carry
+            // one K-block only, so the issuer counts them per stage parity
+            const uint32_t cst = KPS == 1 ? S / static_cast<uint32_t>(NSTG) : ((S & 1u) ? cs1 : cs0);
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * q * slab;
             const uint32_t d_tmem = tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = first;
@@ -925,6 +953,10 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               }
             }
             if (!ok) break;
+            if (KPS == 2) {
+              if (S & 1u) ++cs1;
+              else ++cs0;
+            }
             first = false;
           } else if (!kStream && pidx < cnt) {
             const int slot = pidx * DA + static_cast<int>(cu % DA);
@@ -957,7 +989,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             ++cu;
             first = false;
           }
-          dev::tc_commit(&x_empty[rx.s]);
+          if constexpr (!kXMerge) dev::tc_commit(&x_empty[rx.s]);  // else: the A-slot release frees it
           HQ_TRACE(1 + pidx, tr, (4ull << 24) | ts);
           ++ts;
           ++S;
@@ -1046,6 +1078,15 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         }
       }
     };
+    // W4A8 256-token tiles: the stage's activations have landed (the issuer
+    // waits on this stream's publish only).  With a ring of exactly four
+    // activation stages the parity wait is unambiguous: the stream has seen
+    // the MMA of its previous K-block (stage S - 4, the slot's previous
+    // stage) complete, and stage S + 4 cannot load before this publish.
+    auto x_landed = [&]() -> bool {
+      if constexpr (!kXMerge) return true;
+      return warp_wait(&x_full[S & 3u], (S >> 2) & 1u, abort_flag);
+    };
     // issued stores -> visible to the MMA, then count in on the half slot
     auto publish = [&](int hs) {
       dev::tmem_st_wait();
@@ -1122,7 +1163,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               };
               conv8(0);
               if (trace_me) HQ_TRACE(5 + t, tr, (12ull << 24) | ts);
-              if (!warp_wait(&a_empty[t * HR + j0], eph0, abort_flag)) {
+              if (!warp_wait(&a_empty[t * HR + j0], eph0, abort_flag) || !x_landed()) {
                 ok = false;
                 break;
               }
@@ -1157,7 +1198,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             gk_valid = false;
             convert2(wsm, 0, o);
             if (trace_me) HQ_TRACE(5 + t, tr, (12ull << 24) | ts);
-            if (!warp_wait(&a_empty[t * HR + j0], eph0, abort_flag)) {
+            if (!warp_wait(&a_empty[t * HR + j0], eph0, abort_flag) || !x_landed()) {
               ok = false;
               break;
             }
@@ -1197,6 +1238,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
         rg.next(SW);
       }
     }
+    dev::tmem_st_wait();  // a wait that gave up may leave stores of this warp in flight
     if (!ok && lane == 0) dev::raise_error(p.status, abort_flag, HQ_ERR_DEVICE_TIMEOUT);
   } else if (warp >= kDqWarp0) {
     // ============================================================ dequantisers

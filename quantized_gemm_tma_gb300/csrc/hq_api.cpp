@@ -479,8 +479,15 @@ void plan_stages(int cls, const Layout& L, int bn, int num_experts, size_t smem_
   // through residues and a stream's parity wait on it could pass one phase
   // early, while another stream's copy is still landing.
   const int sw_step = wna16_stream_period(cls, a8);
+  // W4A8 256-token tiles refill an activation slot on the A-slot release of
+  // the stream that read it, and their streams wait for the stage's
+  // activations themselves: parity waits that need a ring of exactly four
+  // stages
+  const bool x4 = cls == 3 && a8;
+  if (x4) sx = 4;
+  const int sx_min = x4 ? 4 : 2;
   const int sw_top = std::max(sw_step, sw_max - sw_max % sw_step);
-  for (; sx >= 2; --sx) {
+  for (; sx >= sx_min; --sx) {
     for (sw = sw_top; sw >= 2; sw -= sw_step)
       if (wna16_smem_bytes(cls, sw, sx, L.tile_bytes, bn, num_experts, a8) <= cap) break;
     if (sw >= 2) break;
