@@ -66,7 +66,7 @@ class PlanInfo(ctypes.Structure):
     """hq_plan_info."""
     _fields_ = [("bn", ctypes.c_int32), ("splits", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("launches", ctypes.c_int32), ("stages", ctypes.c_int32), ("tile_class", ctypes.c_int32),
-                ("groups", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("groups", ctypes.c_int32), ("x_stages", ctypes.c_int32)]
 
 
 _lib = None
@@ -240,7 +240,7 @@ def hq_status_read(workspace, clear: bool = False, stream=None) -> int:
 
 def _plan_dict(info: PlanInfo) -> dict:
     return {"bn": info.bn, "splits": info.splits, "grid": info.grid, "launches": info.launches,
-            "stages": info.stages, "tile_class": info.tile_class, "groups": info.groups}
+            "stages": info.stages, "tile_class": info.tile_class, "groups": info.groups, "x_stages": info.x_stages}
 
 
 def hq_selftest_wait_timeout(workspace, stream=None) -> None:

@@ -799,7 +799,7 @@ hq_status hq_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t m, int32
   l.grid = pl.grid;
   l.smem = pl.smem;
   g_last_plan = hq_plan_info{pl.bn, pl.cluster == 2 ? 2 : (pl.stream_k ? 0 : 1), pl.grid, 1, pl.stages, pl.cls,
-                             pl.groups, 0};
+                             pl.groups, pl.x_stages};
   if (env_int("HQ_TRACE", 0))
     std::fprintf(stderr, "hq_gemm: m=%d n=%d k=%d bn=%d cls=%d stream_k=%d grid=%d stages=%d groups=%d smem=%u x3d=%d\n",
                  m, L.n, L.k, pl.bn, pl.cls, pl.stream_k, pl.grid, pl.stages, pl.groups, pl.smem, p.x3d);
@@ -834,7 +834,7 @@ hq_status hq_plan_query(const hq_weight_desc* wdesc, int32_t m, int32_t atype, i
   const DensePlan pl = plan_wna16(L, m, sms, optin, flags, a8);
   if (pl.stages < 2) return HQ_ERR_UNSUPPORTED;
   *info = hq_plan_info{pl.bn, pl.cluster == 2 ? 2 : (pl.stream_k ? 0 : 1), pl.grid, 1, pl.stages, pl.cls, pl.groups,
-                       0};
+                       pl.x_stages};
   return HQ_OK;
 }
 
@@ -866,7 +866,7 @@ hq_status hq_moe_plan_query(const hq_weight_desc* wdesc, int32_t tokens, int32_t
   int stages = 0, x_stages = 0, groups = 0;
   plan_stages(cls, L, bn, L.num_experts, static_cast<size_t>(smem_optin), &stages, &x_stages, &groups);
   if (stages < 2) return HQ_ERR_UNSUPPORTED;
-  *info = hq_plan_info{bn, 1, sms, 4, stages, cls, groups, 0};
+  *info = hq_plan_info{bn, 1, sms, 4, stages, cls, groups, x_stages};
   return HQ_OK;
 }
 

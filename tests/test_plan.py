@@ -85,6 +85,7 @@ def test_plan_tracks_sm_count_and_shared_memory(hq):
     wide = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, OPTIN)
     narrow = hq.hq_plan_query(_int4(hq), 4096, "bf16", SMS, 200 * 1024)
     assert wide["tile_class"] == narrow["tile_class"] == 3 and wide["stages"] == 2 < narrow["stages"], (wide, narrow)
+    assert (wide["x_stages"], narrow["x_stages"]) == (3, 2), (wide, narrow)
 
 
 def test_plan_query_validation(hq):
@@ -181,6 +182,10 @@ def test_w4a8_plans(hq):
             assert p["stages"] % 2 == 0, p
         if cls == 3:   # four dequantiser streams, each on every fourth stage
             assert p["stages"] % 4 == 0, p
+            # the streams wait for their stage's activations and the producer
+            # refills on their A-slot release: exactly one stream period of
+            # activation stages keeps both parity waits unambiguous
+            assert p["x_stages"] == 4, p
     with pytest.raises(hq.HQError) as ei:
         hq.hq_plan_query(hq.make_desc("int4", "bf16", 8192, 8192, group_k=128), 16, "mxfp8", SMS, OPTIN)
     assert ei.value.status == hq.HQ_ERR_UNSUPPORTED
