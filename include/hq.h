@@ -457,7 +457,7 @@ typedef struct {
   int32_t stages;      /* shared-memory pipeline stages */
   int32_t tile_class;  /* WnA16 tile-width class (0: bn <= 16, 1: <= 64, 2: <= 128, 3: <= 256) */
   int32_t groups;      /* WnA16 dequantiser groups of four warps */
-  int32_t x_stages;    /* WnA16 activation ring stages (dense calls and both plan queries; otherwise 0) */
+  int32_t x_stages;    /* WnA16 activation ring stages (FP8: 0) */
 } hq_plan_info;
 hq_status hq_last_plan(hq_plan_info* info);
 

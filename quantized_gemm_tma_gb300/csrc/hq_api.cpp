@@ -26,6 +26,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 thread_local hq_plan_info g_last_plan{};
+thread_local int g_moe_x_stages = 0;  // activation stages of this thread's last grouped MoE launch
 
 // ------------------------------------------------------------------ devices
 struct DevInfo {
@@ -645,6 +646,7 @@ hq_status launch_moe_grouped(const Layout& L, const uint8_t* wt, int bn, const v
   if (launch_wna16(l, p, maps, s) != cudaSuccess) return HQ_ERR_CUDA;
   *stages = p.stages;
   *groups = p.groups;
+  g_moe_x_stages = p.x_stages;
   return HQ_OK;
 }
 
@@ -975,7 +977,7 @@ hq_status hq_moe_gemm(const hq_weight_desc* wdesc, const void* w_t, int32_t toke
   if (st != HQ_OK) return st;
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L.num_experts, L.n, L.n_pad, y, ldy, true, s) != cudaSuccess)
     return HQ_ERR_CUDA;
-  g_last_plan = hq_plan_info{bn, 1, di.sms, 4, stages, wna16_class(bn), groups, 0};
+  g_last_plan = hq_plan_info{bn, 1, di.sms, 4, stages, wna16_class(bn), groups, g_moe_x_stages};
   return HQ_OK;
 }
 
@@ -1108,7 +1110,7 @@ hq_status hq_moe_ffn(const hq_weight_desc* w13, const void* w13_t, const hq_weig
   if (launch_moe_combine(zbuf, topk_ids, tokens, topk, L2.num_experts, L2.n, L2.n_pad, y, ldy, true, s) !=
       cudaSuccess)
     return HQ_ERR_CUDA;
-  g_last_plan = hq_plan_info{bn, 1, di.sms, fused ? 5 : 6, stages, wna16_class(bn), groups, 0};
+  g_last_plan = hq_plan_info{bn, 1, di.sms, fused ? 5 : 6, stages, wna16_class(bn), groups, g_moe_x_stages};
   return HQ_OK;
 }
 
@@ -1180,7 +1182,7 @@ hq_status hq_moe_grouped_gemm(const hq_weight_desc* wdesc, const void* w_t, int3
   st = launch_moe_grouped(L, wt, bn, x, ldx, static_cast<int>(x_rows), x_base, kMoeOutRowMap, nullptr, y, ldy,
                           exp_off, tile_off, perm, nullptr, reinterpret_cast<int*>(ws), di, s, &stages, &groups);
   if (st != HQ_OK) return st;
-  g_last_plan = hq_plan_info{bn, 1, di.sms, 2, stages, wna16_class(bn), groups, 0};
+  g_last_plan = hq_plan_info{bn, 1, di.sms, 2, stages, wna16_class(bn), groups, g_moe_x_stages};
   return HQ_OK;
 }
 

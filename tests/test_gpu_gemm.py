@@ -188,6 +188,20 @@ def test_128_token_classes(n, cls):
     check(y, _ref(qw, acts), f"128-token class {cls}")
 
 
+def test_128_token_streams_under_stream_k():
+    """Tiles of 128 tokens with one K-block per stage (four dequantiser
+    streams, each on every fourth stage) under stream-K, whose CTAs take K
+    ranges of any length and several units each."""
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import tuning
+    qw, acts = synth.dense_w4a16_asym(47, 100, 20480, 1536)
+    with tuning(HQ_FORCE_SPLITK=1):
+        y = _gpu(qw, acts)
+        p = hq.hq_last_plan()
+    assert (p["tile_class"], p["splits"]) == (2, 0), p
+    check(y, _ref(qw, acts), "128-token streams, stream-K")
+
+
 def test_workspace_reused_across_shapes():
     """One workspace serves split-K problems of different shapes in turn: the
     fp32 partials of one shape never land on the counters of the next."""

@@ -137,6 +137,25 @@ def test_w4a8_work_splits(splitk):
     check(y, _ref(qw, x), f"w4a8 {splitk}")
 
 
+@pytest.mark.parametrize("splitk", ["cluster", "stream_k", "whole"])
+def test_w4a8_256_token_tiles_every_split(splitk):
+    """Tiles of 256 tokens (four dequantiser streams, each on every fourth
+    stage, with four activation stages) under each work split: stream-K hands
+    CTAs K ranges of any length, the cluster split half of K each."""
+    import quantized_gemm_tma_gb300 as hq
+    from gpu_helpers import DevWeight, tuning
+    m, n, k = 256, 8192, 1024
+    qw = _weight(84, n, k)
+    x = synth.make_activations(np.random.default_rng(84), m, k, "bf16").data
+    switches = {"cluster": {}, "stream_k": {"HQ_FORCE_SPLITK": 1}, "whole": {"HQ_FORCE_SPLITK": 2}}[splitk]
+    with tuning(**switches):
+        y = _w4a8(DevWeight(qw), x, k)
+        p = hq.hq_last_plan()
+    assert (p["bn"], p["tile_class"], p["x_stages"]) == (256, 3, 4), p
+    assert p["splits"] == {"cluster": 2, "stream_k": 0, "whole": 1}[splitk], p
+    check(y, _ref(qw, x), f"w4a8 256-token {splitk}")
+
+
 def test_w4a8_batch_invariant():
     """With HQ_FLAG_BATCH_INVARIANT rows 0..15 are bit-identical at every M."""
     import quantized_gemm_tma_gb300 as hq
