@@ -172,10 +172,11 @@ def test_moe_plan_query_validation(hq):
 def test_w4a8_plans(hq):
     """W4A8-MXFP4 plans the same tile widths and work splits as W4A16 (256
     tokens at large M: the scale factors of a tile's tokens take 8 TMEM
-    columns beside the A operand)."""
+    columns beside the A operand); its 128-token tiles keep the class with
+    one K-block per stage even with one tile per CTA."""
     d = hq.make_desc("mxfp4", "ue8m0", 8192, 8192, group_k=32)
     for m, bn, cls, split in ((1, 16, 0, CLUSTER), (16, 16, 0, CLUSTER), (48, 48, 1, CLUSTER),
-                              (128, 128, 4, CLUSTER), (1024, 256, 3, WHOLE), (4096, 256, 3, WHOLE)):
+                              (128, 128, 2, CLUSTER), (1024, 256, 3, WHOLE), (4096, 256, 3, WHOLE)):
         p = hq.hq_plan_query(d, m, "mxfp8", SMS, OPTIN)
         assert (p["bn"], p["tile_class"], p["splits"]) == (bn, cls, split), (m, p)
         if cls in (0, 1, 4):
