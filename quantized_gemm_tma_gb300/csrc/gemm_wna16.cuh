@@ -28,8 +28,9 @@
 //                K-block t & 1 of every stage of parity t >> 1 (a whole K-block
 //                of its 32 rows per warp); tiles of 128 tokens with one
 //                K-block per stage and W4A8 tiles of 256 tokens: four
-//                streams, stream t taking every fourth stage.  Otherwise one
-//                K-block per stage: all 16 warps on each K-block, one 32-column
+//                streams, stream t taking every fourth stage.  A stream
+//                publishes each K-block whole.  Otherwise (bf16/fp16 tiles of
+//                256 tokens) all 16 warps on each K-block, one 32-column
 //                chunk each.  A thread owns one weight row (its TMEM lane),
 //                turns the packed codes into bf16x2/f16x2 pairs and writes
 //                them into an A slot in TMEM with tcgen05.st.
@@ -98,12 +99,12 @@ constexpr int kIssWarp0 = kXProdWarp + 1;                  // first MMA issuer w
 constexpr uint32_t kACol0 = 0;
 constexpr uint32_t kTmemCols = 512;
 
-// Streams: half slots per stream, a ring that K-block c of a stream fills at
-// positions 2c and 2c + 1.  A ring of three for the 16-token class (its
-// accumulators fit in the last 128 columns), which lets a stream's first half
-// reuse the slot of K-block c - 2 instead of waiting for the MMA of K-block
-// c - 1, measured no faster at M = 16 (18.2 against 17.8 us), so every class
-// keeps two.
+// Streams: half slots per stream; each K-block of a stream fills both and is
+// published whole.  (A ring of three for the 16-token class, whose
+// accumulators fit in the last 128 columns, let a stream's first half reuse
+// the slot of K-block c - 2 instead of waiting for the MMA of K-block c - 1
+// when halves were published separately; it measured no faster at M = 16:
+// 18.2 against 17.8 us.)
 template <int CLS>
 constexpr int half_ring() { return 2; }
 template <int CLS>
@@ -566,11 +567,13 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // fourth stage.
   constexpr bool kStream = KPS == 2 || CLS == 2 || (CLS == 3 && A8);
   constexpr int NSTG = kStream ? 4 / KPS : 1;  // stream period in stages
-  // Streams with one K-block per stage run ahead of the MMA, so a stream
-  // publishes its K-block once, both half slots together, on the barrier pair
-  // of its first half slot, and the issuer waits and commits once per K-block
-  // (the W4A8 scale factors then live in the first half slot only).
-  constexpr bool kKbPub = kStream && KPS == 1;
+  // A stream publishes its K-block once, both half slots together, on the
+  // barrier pair of its first half slot, and the issuer waits and commits
+  // once per K-block (the W4A8 scale factors then live in the first half
+  // slot only): every wait and commit costs the single issuing thread about
+  // 100-300 cycles, more than publishing the first half early gains
+  // (N = K = 8192: M = 16 16.3 -> 15.4 us, M = 64 19.8 -> 18.6 us; W4A8
+  // M = 4096 263 -> 233 us).
   // The single issuing thread pays for every wait and commit on its own
   // (about 100-300 cycles each against 500 cycles of MMA per W4A8 K-block),
   // so for W4A8 tiles of 256 tokens the stream also waits for the stage's
@@ -582,7 +585,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   // activations not yet loaded) and the stream's on the activations (below).
   // (The 128-token MoE tiles keep the issuer's activation waits: four 32 KB
   // activation stages would leave their weights half the ring.)
-  constexpr bool kXMerge = kKbPub && CLS == 3;
+  constexpr bool kXMerge = kStream && CLS == 3;
   constexpr uint32_t kSlabsKb = A8 ? 1u : 2u;  // activation slabs per K-block
   // With streams, issuer p takes K-block p of every stage, i.e. the K-blocks
   // of streams p and 2 + p alternately.
@@ -612,7 +615,7 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
   uint64_t* a_full = x_empty + SX;
   constexpr int NAB = a_bars<CLS>();  // A-slot barriers of each kind
   constexpr int HR = half_ring<CLS>();  // streams: half slots per stream
-  static_assert(!kKbPub || HR == 2, "a whole-K-block publish assumes a stream's K-block fills its ring");
+  static_assert(HR == 2, "a stream publishes whole K-blocks: its ring holds one K-block");
   constexpr uint32_t ACC0 = acc_col0<CLS>();
   uint64_t* a_empty = a_full + NAB;
   uint64_t* acc_full = a_empty + NAB;
@@ -883,8 +886,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           }
           HQ_TRACE(1 + pidx, tr, (2ull << 24) | ts);
           // stream mode: K-block pidx of this stage comes from stream
-          // 2 (S & 1) + pidx, in two halves (64 K each) published separately
-          // (one K-block per stage: stream S & 3, published whole)
+          // 2 (S & 1) + pidx (one K-block per stage: stream S & 3), published
+          // whole
           const int q = pidx;
           if (kStream && q < cnt) {
             const int t = KPS == 2 ? 2 * static_cast<int>(S & 1u) + q : static_cast<int>(S & 3u);
@@ -895,63 +898,30 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             const uint32_t xs = dev::smem_u32(x_st + rx.s * x_stage) + kSlabsKb * q * slab;
             const uint32_t d_tmem = tmem + ACC0 + static_cast<uint32_t>((buf * ISS + pidx) * BNMAX);
             const bool fresh = first;
-            if constexpr (kKbPub) {
-              // the stream's K-block cst: one wait, its two half slots' MMAs,
-              // one release (descriptor of 32-byte step k: base + 2k)
-              const int hs = t * HR;
-              if (!dev::mbar_wait(&a_full[hs], cst & 1u, abort_flag)) {
-                ok = false;
-                break;
-              }
-              HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
-              dev::tc_fence_after();
-              const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
-              const uint64_t bd0 = dev::sw128_desc(xs);
-              if constexpr (A8) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                  dev::mma_mx_ts(d_tmem, a_tmem + (c >> 1) * 32 + (c & 1) * 8, bd0 + 2u * c, mx_idesc_sub(idesc, c),
-                                 a_tmem + 16u, a_tmem + 20u, (fresh && c == 0) ? 0u : 1u);
-              } else {
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                  dev::mma_f16_ts(d_tmem, a_tmem + (c >> 2) * 32 + (c & 3) * 8,
-                                  bd0 + static_cast<uint64_t>(((c >> 2) * slab + (c & 3) * 32) >> 4), idesc,
-                                  (fresh && c == 0) ? 0u : 1u);
-              }
-              dev::tc_commit(&a_empty[hs]);
-            } else {
-              for (int h = 0; h < 2 && ok; ++h) {
-                // half h of the stream's K-block cst is its half slot 2 cst + h of the ring
-                const uint32_t hn = 2u * cst + static_cast<uint32_t>(h);
-                const int hs = t * HR + static_cast<int>(hn % HR);
-                if (!dev::mbar_wait(&a_full[hs], (hn / HR) & 1u, abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
-                dev::tc_fence_after();
-                if constexpr (A8) {
-                  // half h = 32-K sub-blocks 2h, 2h + 1: A at the half slot's
-                  // columns 8i, its scale factors at + 16 (A) and + 20 (B)
-                  const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
-#pragma unroll
-                  for (int i = 0; i < 2; ++i) {
-                    const uint64_t bdesc = dev::sw128_desc(xs + (2 * h + i) * 32);
-                    dev::mma_mx_ts(d_tmem, a_tmem + i * 8, bdesc, mx_idesc_sub(idesc, 2 * h + i), a_tmem + 16u,
-                                   a_tmem + 20u, (fresh && h == 0 && i == 0) ? 0u : 1u);
-                  }
-                } else {
-                  const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
-#pragma unroll
-                  for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bdesc = dev::sw128_desc(xs + h * slab + kk * 32);
-                    dev::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, (fresh && h == 0 && kk == 0) ? 0u : 1u);
-                  }
-                }
-                dev::tc_commit(&a_empty[hs]);
-              }
+            // the stream's K-block cst: one wait, its two half slots' MMAs,
+            // one release (descriptor of 32-byte step k: base + 2k)
+            const int hs = t * HR;
+            if (!dev::mbar_wait(&a_full[hs], cst & 1u, abort_flag)) {
+              ok = false;
+              break;
             }
+            HQ_TRACE(1 + pidx, tr, (3ull << 24) | ts);
+            dev::tc_fence_after();
+            const uint32_t a_tmem = tmem + kACol0 + static_cast<uint32_t>(hs * 32);
+            const uint64_t bd0 = dev::sw128_desc(xs);
+            if constexpr (A8) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                dev::mma_mx_ts(d_tmem, a_tmem + (c >> 1) * 32 + (c & 1) * 8, bd0 + 2u * c, mx_idesc_sub(idesc, c),
+                               a_tmem + 16u, a_tmem + 20u, (fresh && c == 0) ? 0u : 1u);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                dev::mma_f16_ts(d_tmem, a_tmem + (c >> 2) * 32 + (c & 3) * 8,
+                                bd0 + static_cast<uint64_t>(((c >> 2) * slab + (c & 3) * 32) >> 4), idesc,
+                                (fresh && c == 0) ? 0u : 1u);
+            }
+            dev::tc_commit(&a_empty[hs]);
             if (!ok) break;
             if (KPS == 2) {
               if (S & 1u) ++cs1;
@@ -1109,13 +1079,12 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
           if (trace_me) HQ_TRACE(5 + t, tr, (5ull << 24) | ts);
           if (pos < cnt) {
             const uint8_t* wsm = w_st + rg.s * w_stage + pos * tile_bytes;
-            // The first half is published after the second is converted (the
-            // arithmetic covers its TMEM stores); the second right away.
-            // the K-block's two half slots in the stream's ring, and the
-            // phase parity of the MMA release each waits for
-            const uint32_t hn0 = 2u * ca, hn1 = hn0 + 1u;
-            const int j0 = static_cast<int>(hn0 % HR), j1 = static_cast<int>(hn1 % HR);
-            const uint32_t eph0 = ((hn0 / HR) & 1u) ^ 1u, eph1 = ((hn1 / HR) & 1u) ^ 1u;
+            // The K-block fills the stream's two half slots (the first half
+            // is stored while the second is converted) once the MMAs of the
+            // stream's previous K-block have released them, and is published
+            // whole on the first slot's barrier pair.
+            constexpr int j0 = 0, j1 = 1;
+            const uint32_t eph0 = (ca & 1u) ^ 1u;  // release parity of the previous K-block
             if constexpr (A8) {
               // scale exponents of this K-block: weight rows 32j + lane (from
               // the tile; the conversion's 2^6 is folded in when they are
@@ -1173,21 +1142,8 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
               conv8(2);
               __syncwarp();
               if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
-              if constexpr (kKbPub) {
-                st_half(j1, false);  // the MMAs of both halves read the first half's scale factors
-                publish(t * HR + j0);
-                if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
-              } else {
-                publish(t * HR + j0);
-                if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
-                if (!warp_wait(&a_empty[t * HR + j1], eph1, abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                dev::tc_fence_after();
-                st_half(j1, true);
-                publish(t * HR + j1);
-              }
+              st_half(j1, false);  // the MMAs of both halves read the first half's scale factors
+              publish(t * HR + j0);
               if (trace_me) HQ_TRACE(5 + t, tr, (7ull << 24) | ts);
               ++ca;
               ++ts;
@@ -1210,23 +1166,9 @@ __global__ void __launch_bounds__(threads<CLS>(), 1)
             // every lane's codes are consumed: the stage may be refilled
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(&w_empty[rg.s]);
-            if constexpr (kKbPub) {
-              dev::tmem_st16(a_lane + j1 * 32, o[0]);
-              dev::tmem_st16(a_lane + j1 * 32 + 16, o[1]);
-              publish(t * HR + j0);
-              if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
-            } else {
-              publish(t * HR + j0);
-              if (trace_me) HQ_TRACE(5 + t, tr, (13ull << 24) | ts);
-              if (!warp_wait(&a_empty[t * HR + j1], eph1, abort_flag)) {
-                ok = false;
-                break;
-              }
-              dev::tc_fence_after();
-              dev::tmem_st16(a_lane + j1 * 32, o[0]);
-              dev::tmem_st16(a_lane + j1 * 32 + 16, o[1]);
-              publish(t * HR + j1);
-            }
+            dev::tmem_st16(a_lane + j1 * 32, o[0]);
+            dev::tmem_st16(a_lane + j1 * 32 + 16, o[1]);
+            publish(t * HR + j0);
             if (trace_me) HQ_TRACE(5 + t, tr, (7ull << 24) | ts);
             ++ca;
           } else {
