@@ -76,8 +76,8 @@ BLOCK = 25         # back-to-back calls of one shape between two events
 # capture (dram__bytes_read.sum + dram__bytes_write.sum, third warm-up pass of
 # the dense sweep; the command is kept with the profile summaries), keyed by
 # M; valid only while the kernel sources hash to `sha` (else null).
-NCU_TRAFFIC = {"sha": "fc874fbe7ee0da28", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
-               "bytes": {16: 35_467_776, 128: 37_306_368, 1024: 52_733_952, 4096: 167_084_800}}
+NCU_TRAFFIC = {"sha": "7f5bdcb60b8360de", "files": ["gemm_wna16.cuh", "hq_ptx.cuh", "wna16_int4.cu"],
+               "bytes": {16: 35_467_776, 128: 37_304_576, 1024: 53_092_608, 4096: 170_119_424}}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
