@@ -501,18 +501,19 @@ def run_gpu(args, rank: int, world: int):
 
     # ---- end to end through the C ABI with host buffers (pinned): per step the
     # host clock runs from the first H2D enqueue to the last D2H completion.
-    # With --e2e-overlap the copies run on their own streams (inputs on one,
-    # results on another), ordered against the GEMMs by events, so the copies
-    # of one shape overlap the GEMMs of the others, largest M first.
+    # By default the copies run on their own streams (inputs on one, results on
+    # another), ordered against the GEMMs by events, so the copies of one shape
+    # overlap the GEMMs of the others, largest M first; --e2e-serial keeps every
+    # copy and GEMM in order on the GEMM stream.
     e2e_times = []
     if not args.no_e2e:
-        if args.e2e_overlap:
+        if not args.e2e_serial:
             s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
             order = sorted(args.m_sweep, reverse=True)
         for step in range(args.warmup + args.steps):
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            if args.e2e_overlap:
+            if not args.e2e_serial:
                 landed = {}
                 with torch.cuda.stream(s_in):
                     for m in order:
@@ -658,8 +659,10 @@ def main():
                     help="skip the M=16, N=K=1024 case timed as a CUDA graph over many weight copies")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the INT6 channelwise and FP8 block-scaled configurations")
-    ap.add_argument("--e2e-overlap", action="store_true",
-                    help="end-to-end pass with the copies on their own streams, overlapping the GEMMs")
+    ap.add_argument("--e2e-serial", action="store_true",
+                    help="end-to-end pass with every copy and GEMM in order on one stream (default: the copies "
+                         "on their own streams, overlapping the GEMMs of the other shapes, as a pipelined "
+                         "caller issues them)")
     ap.add_argument("--m-sweep", type=str, default=",".join(map(str, M_SWEEP)),
                     help="comma-separated M values of the dense sweep")
     ap.add_argument("--moe-t", type=str, default=",".join(map(str, MOE_T)),
@@ -754,7 +757,7 @@ def main():
             "value": round(world * flops_step / e2e_s / 1e12, 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": sum(m * K * 2 for m in sw), "d2h_bytes_per_step": sum(m * N * 2 for m in sw),
             "ms_per_step": round(e2e_s * 1e3, 4),
-            "copies": "own streams, overlapping the GEMMs" if args.e2e_overlap else "on the GEMM stream, in order"},
+            "copies": "on the GEMM stream, in order" if args.e2e_serial else "own streams, overlapping the GEMMs"},
         "gpu_launches": res["gpu_launches"],
         "clocks": res["clocks"],
     }
